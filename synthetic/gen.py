@@ -1,0 +1,194 @@
+"""Seeded synthetic inputs for the DFlash drafting workloads.
+
+Everything here is input preparation: random draws, rounding to the storage
+type, request lengths, page tables, synthetic target tokens.  None of the
+drafting arithmetic (projections, norms, attention, selection, verification)
+lives in this module; the oracle and the CUDA path each implement that on
+their own and receive these arrays as inputs.
+
+Determinism: every array is drawn from numpy's Philox counter-based
+generator keyed by (seed, array name, chunk index), so results do not depend
+on the thread count used to produce them and any chunk can be regenerated
+alone.
+
+Storage: bf16 matrices are returned as ``uint16`` arrays of bf16 bit
+patterns (round-to-nearest-even from the fp32 draw); fp32 configs return
+``float32`` arrays.  Norm gains and biases are always ``float32``.
+"""
+from __future__ import annotations
+
+import os
+import zlib
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+CHUNK = 1 << 22
+
+
+def _threads() -> int:
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def _gen(seed: int, name: str, chunk: int) -> np.random.Generator:
+    ss = np.random.SeedSequence([int(seed), zlib.crc32(name.encode()), int(chunk)])
+    return np.random.Generator(np.random.Philox(ss))
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round fp32 values to the nearest bf16 (ties to even); returns uint16 bits."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    r = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((u + r) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def normal(shape, std: float, seed: int, name: str, dtype: str = "f32") -> np.ndarray:
+    """N(0, std^2) draws of ``shape``; dtype "bf16" returns rounded bf16 bits."""
+    shape = tuple(int(s) for s in shape)
+    n = int(np.prod(shape)) if shape else 1
+    out = np.empty(n, dtype=np.uint16 if dtype == "bf16" else np.float32)
+    nchunks = (n + CHUNK - 1) // CHUNK
+
+    def work(ci: int) -> None:
+        lo = ci * CHUNK
+        hi = min(n, lo + CHUNK)
+        v = _gen(seed, name, ci).standard_normal(hi - lo, dtype=np.float32)
+        if std != 1.0:
+            v *= np.float32(std)
+        if dtype == "bf16":
+            out[lo:hi] = f32_to_bf16_bits(v)
+        else:
+            out[lo:hi] = v
+
+    if nchunks <= 1:
+        for ci in range(nchunks):
+            work(ci)
+    else:
+        with ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(work, range(nchunks)))
+    return out.reshape(shape)
+
+
+def gain(n: int, seed: int, name: str) -> np.ndarray:
+    """RMSNorm gain 1 + 0.1*N(0,1): a kernel that ignores the gain fails parity."""
+    return (1.0 + 0.1 * normal((n,), 1.0, seed, name)).astype(np.float32)
+
+
+CONV_SITES = ("pre_attn", "post_attn", "pre_ffn", "post_ffn")
+
+
+def make_weights(cfg, seed: int) -> dict:
+    """Random-init drafter weights, N(0, 1/fan_in), stored in ``cfg.dtype``.
+
+    Layout (row-major, ``y = W x`` with W[out, in]):
+      w_fc [H, n_sel*H_t], g_fc [H]; embed [V, H]; lm_head [V, H]; g_final [H]
+      layers[l]: g_attn [H], w_q [nq*d, H], w_k [nkv*d, H], w_v [nkv*d, H],
+                 g_q [d], g_k [d], w_o [H, nq*d], g_ffn [H],
+                 w_gate [F, H], w_up [F, H], w_down [H, F],
+                 conv[site] = (w [2*H/16, H], b [2*H/16])   (use_conv only)
+      sel: e256 [V, 256], a [r, 256], b [r, 256], w_g [H], b_g ()   (use_selector only)
+    """
+    dt = cfg.dtype
+    H, d, F, V = cfg.hidden, cfg.head_dim, cfg.ffn, cfg.vocab
+    nq, nkv = cfg.n_q_heads, cfg.n_kv_heads
+    W = {
+        "w_fc": normal((H, cfg.feat_in), cfg.feat_in ** -0.5, seed, "w_fc", dt),
+        "g_fc": gain(H, seed, "g_fc"),
+        "embed": normal((V, H), 1.0, seed, "embed", dt),
+        "lm_head": normal((V, H), H ** -0.5, seed, "lm_head", dt),
+        "g_final": gain(H, seed, "g_final"),
+        "layers": [],
+    }
+    for l in range(cfg.n_layers):
+        p = f"L{l}."
+        lw = {
+            "g_attn": gain(H, seed, p + "g_attn"),
+            "w_q": normal((nq * d, H), H ** -0.5, seed, p + "w_q", dt),
+            "w_k": normal((nkv * d, H), H ** -0.5, seed, p + "w_k", dt),
+            "w_v": normal((nkv * d, H), H ** -0.5, seed, p + "w_v", dt),
+            "g_q": gain(d, seed, p + "g_q"),
+            "g_k": gain(d, seed, p + "g_k"),
+            "w_o": normal((H, nq * d), (nq * d) ** -0.5, seed, p + "w_o", dt),
+            "g_ffn": gain(H, seed, p + "g_ffn"),
+            "w_gate": normal((F, H), H ** -0.5, seed, p + "w_gate", dt),
+            "w_up": normal((F, H), H ** -0.5, seed, p + "w_up", dt),
+            "w_down": normal((H, F), F ** -0.5, seed, p + "w_down", dt),
+        }
+        if cfg.use_conv:
+            G2 = 2 * cfg.conv_groups
+            lw["conv"] = {
+                s: (normal((G2, H), H ** -0.5, seed, p + "conv." + s + ".w", dt),
+                    (0.1 * normal((G2,), 1.0, seed, p + "conv." + s + ".b")).astype(np.float32))
+                for s in CONV_SITES
+            }
+        W["layers"].append(lw)
+    if cfg.use_selector:
+        E, r = cfg.sel_dim, cfg.sel_rank
+        std = (E * r ** 0.5) ** -0.5   # keeps u(p).w(c) near unit scale
+        W["sel"] = {
+            "e256": normal((V, E), 1.0, seed, "sel.e256", dt),
+            "a": normal((r, E), std, seed, "sel.a", dt),
+            "b": normal((r, E), std, seed, "sel.b", dt),
+            "w_g": normal((H,), H ** -0.5, seed, "sel.w_g"),
+            "b_g": np.float32(0.1),
+        }
+    return W
+
+
+def context_lengths(wl) -> np.ndarray:
+    if wl.explicit_ctx is not None:
+        return np.asarray(wl.explicit_ctx, dtype=np.int32)
+    g = _gen(wl.seed, "ctx_len", 0)
+    return g.integers(wl.ctx_lo, wl.ctx_hi + 1, size=wl.batch).astype(np.int32)
+
+
+def anchors(wl, step: int = 0) -> np.ndarray:
+    g = _gen(wl.seed, "anchor", step)
+    return g.integers(0, wl.cfg.vocab - 1, size=wl.batch).astype(np.int32)
+
+
+def target_hidden(cfg, n_tokens: int, seed: int, name: str) -> np.ndarray:
+    """Concatenated target hidden states [n_tokens, n_sel*H_t], N(0,1)."""
+    return normal((n_tokens, cfg.feat_in), 1.0, seed, "X." + name, cfg.dtype)
+
+
+def page_table(ctx_capacity: np.ndarray, page_size: int, seed: int):
+    """Random page assignment: returns (table [B, max_pages] int32, num_pages).
+
+    Request b owns ceil(cap_b / page_size) pages drawn from a seeded random
+    permutation of the pool, so page indirection is exercised.  Unused table
+    entries are -1 and are never read by a correct kernel.
+    """
+    cap = np.asarray(ctx_capacity, dtype=np.int64)
+    npg = (cap + page_size - 1) // page_size
+    total = int(npg.sum())
+    maxp = max(1, int(npg.max()) if len(npg) else 1)
+    perm = _gen(seed, "pages", 0).permutation(total).astype(np.int32)
+    tab = np.full((len(cap), maxp), -1, dtype=np.int32)
+    o = 0
+    for b, k in enumerate(npg):
+        tab[b, :k] = perm[o:o + k]
+        o += k
+    return tab, total
+
+
+def target_ids(draft: np.ndarray, p_accept, vocab: int, seed: int, step: int = 0) -> np.ndarray:
+    """Synthetic target tokens [B, 16] for greedy verification.
+
+    Position i (0-based, < 15) equals draft[:, i] with probability p_accept[i],
+    otherwise it is uniform over the vocabulary minus draft[:, i].  The last
+    position (the bonus after a fully accepted block) is uniform.
+    """
+    draft = np.asarray(draft, dtype=np.int64)
+    B, S1 = draft.shape
+    g = _gen(seed, "target_ids", step)
+    u = g.random((B, S1))
+    alt = g.integers(0, vocab - 1, size=(B, S1))
+    alt = alt + (alt >= draft)
+    t = np.where(u < np.asarray(p_accept)[None, :S1], draft, alt)
+    last = g.integers(0, vocab, size=(B, 1))
+    return np.concatenate([t, last], axis=1).astype(np.int32)
