@@ -1,0 +1,585 @@
+// C ABI of libdflash: argument validation, workspace layout, and the launch
+// sequence of each call of the drafting hot path (see include/dflash.h).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+struct dflash_ctx {
+  dflash_config cfg;
+  dflash_weights w;
+  std::vector<dflash_layer_weights> layers;
+  int device = 0;
+  int num_sms = 148;
+  unsigned long long timeout_ns = 2000000000ull;
+  int gemm_ctas = 0;
+  int attn_split = 0;
+  dflash::Profiler prof;
+};
+
+namespace dflash {
+
+static thread_local std::string g_err;
+
+int set_error(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_check(cudaError_t e, const char *what) {
+  if (e == cudaSuccess) return DFLASH_OK;
+  return set_error(DFLASH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elt_bytes, uint64_t cols,
+                 uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return set_error(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (reinterpret_cast<uintptr_t>(base) & 15 || row_stride_bytes % 16)
+    return set_error(DFLASH_ERR_ALIGN, "TMA operand base / row stride must be 16-byte aligned");
+  (void)elt_bytes;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llux%llu tensor", static_cast<int>(r),
+                     static_cast<unsigned long long>(rows), static_cast<unsigned long long>(cols));
+  return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------ profiler
+cudaEvent_t Profiler::take() {
+  if (used < pool.size()) return pool[used++];
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  pool.push_back(e);
+  ++used;
+  return e;
+}
+void Profiler::reset() {
+  recs.clear();
+  used = 0;
+}
+Profiler::~Profiler() {
+  for (auto e : pool) cudaEventDestroy(e);
+}
+
+ProfScope::ProfScope(const Launch &l, const char *name, double bytes, double flops) : lc(l) {
+  if (!lc.prof || !lc.prof->on) return;
+  Profiler::Rec r;
+  r.name = name;
+  r.a = lc.prof->take();
+  r.b = lc.prof->take();
+  r.bytes = bytes;
+  r.flops = flops;
+  cudaEventRecord(r.a, lc.stream);
+  lc.prof->recs.push_back(r);
+  idx = static_cast<int>(lc.prof->recs.size()) - 1;
+}
+ProfScope::~ProfScope() {
+  if (idx >= 0) cudaEventRecord(lc.prof->recs[idx].b, lc.stream);
+}
+
+// ------------------------------------------------------------------ workspace layout
+namespace {
+
+constexpr int GEMM_COUNTERS = 1 << 16;
+constexpr int GEMM_MAX_BN = 256;
+constexpr int ATTN_SLOTS = 4096;
+constexpr int TOPK_MAX_CHUNKS = 64;
+
+struct Layout {
+  size_t status, gemm_ctr, gemm_part, attn_ctr, attn_o, attn_ml, topk_ctr, topk_part;
+  size_t x, u, u2, qkv, q, bk, bv, o, ysub, coef, hmid, hmask, hfinal, logits, scores;
+  size_t fc, f, kvproj, ctx_saved;
+  size_t total;
+  size_t gemm_part_floats;
+};
+
+Layout layout(const dflash_ctx *c, int B, int Tn) {
+  const dflash_config &g = c->cfg;
+  const size_t te = g.dtype == DFLASH_F32 ? 4 : 2;
+  const size_t H = g.hidden, d = g.head_dim, nq = g.n_q_heads, nkv = g.n_kv_heads, F = g.ffn, V = g.vocab;
+  const size_t R = static_cast<size_t>(B) * 16, gq = nq / nkv;
+  Layout L = {};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) & ~static_cast<size_t>(255);
+    return o;
+  };
+  L.status = take(256);
+  L.gemm_ctr = take(sizeof(int) * GEMM_COUNTERS);
+  L.gemm_part_floats = static_cast<size_t>(c->num_sms) * 2 * 128 * GEMM_MAX_BN;
+  L.gemm_part = take(4 * L.gemm_part_floats);
+  L.attn_ctr = take(sizeof(int) * static_cast<size_t>(B) * nkv);
+  L.attn_o = take(4ull * ATTN_SLOTS * 16 * gq * 128);
+  L.attn_ml = take(4ull * ATTN_SLOTS * 16 * gq * 2);
+  L.topk_ctr = take(sizeof(int) * static_cast<size_t>(B) * 15);
+  L.topk_part = take(8ull * B * 15 * TOPK_MAX_CHUNKS * 16);
+  L.x = take(4 * R * H);
+  L.u = take(te * R * H);
+  L.u2 = take(te * R * H);
+  L.qkv = take(4 * R * (nq + 2 * nkv) * d);
+  L.q = take(te * R * nq * d);
+  L.bk = take(te * R * nkv * d);
+  L.bv = take(te * R * nkv * d);
+  L.o = take(te * R * nq * d);
+  L.ysub = take(te * R * H);
+  L.coef = take(4 * R * (H / 8));
+  L.hmid = take(te * R * F);
+  L.hmask = take(te * B * 15 * H);
+  L.hfinal = take(te * R * H);
+  L.logits = take(4ull * B * 15 * V);
+  L.scores = take(4ull * B * 15 * 256);
+  L.fc = take(4ull * Tn * H);
+  L.f = take(te * Tn * H);
+  L.kvproj = take(4ull * g.n_layers * Tn * 2 * nkv * d);
+  L.ctx_saved = take(sizeof(int) * static_cast<size_t>(B));
+  L.total = off;
+  return L;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+  return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+Launch make_launch(dflash_ctx *c, void *ws, cudaStream_t s) {
+  Launch lc;
+  lc.stream = s;
+  lc.num_sms = c->num_sms;
+  lc.status = ws ? at<int>(ws, 0) : nullptr;
+  lc.timeout_ns = c->timeout_ns;
+  lc.gemm_ctas = c->gemm_ctas;
+  lc.prof = &c->prof;
+  return lc;
+}
+
+// One projection of the drafter on the path's GEMM (tcgen05 for bf16, CUDA
+// cores for fp32).
+int proj(dflash_ctx *c, const Launch &lc, void *ws, const Layout &L, const void *W, int ldw, const void *X, int ldx,
+         int M, int N, int K, int epi, void *out, int ldo, const float *bias, const char *name) {
+  if (c->cfg.dtype == DFLASH_F32)
+    return gemm_f32(lc, static_cast<const float *>(W), ldw, static_cast<const float *>(X), ldx, M, N, K,
+                    epi == EPI_STORE_T ? EPI_F32 : epi, out, ldo, bias, name);
+  GemmScratch sc;
+  sc.partials = at<float>(ws, L.gemm_part);
+  sc.partial_floats = L.gemm_part_floats;
+  sc.counters = at<int>(ws, L.gemm_ctr);
+  sc.n_counters = GEMM_COUNTERS;
+  return gemm_bf16(lc, W, ldw, X, ldx, M, N, K, epi, out, ldo, bias, sc, name);
+}
+
+int check_ws(const dflash_ctx *c, void *ws, size_t bytes, int B, int Tn) {
+  if (!ws) return set_error(DFLASH_ERR_ARG, "workspace is null");
+  if (!aligned16(ws)) return set_error(DFLASH_ERR_ALIGN, "workspace must be 16-byte aligned");
+  const size_t need = layout(c, B, Tn).total;
+  if (bytes < need)
+    return set_error(DFLASH_ERR_SHAPE, "workspace of %zu bytes is smaller than the %zu needed for batch %d", bytes, need,
+                     B);
+  return DFLASH_OK;
+}
+
+int check_kv(const dflash_ctx *c, const dflash_kv *kv) {
+  if (!kv || !kv->k_cache || !kv->v_cache || !kv->page_table) return set_error(DFLASH_ERR_ARG, "null KV cache");
+  if (kv->num_pages <= 0 || kv->max_pages <= 0) return set_error(DFLASH_ERR_SHAPE, "empty KV page pool");
+  if (!aligned16(kv->k_cache) || !aligned16(kv->v_cache)) return set_error(DFLASH_ERR_ALIGN, "KV cache not aligned");
+  (void)c;
+  return DFLASH_OK;
+}
+
+size_t layer_elems(const dflash_ctx *c, const dflash_kv *kv) {
+  return static_cast<size_t>(kv->num_pages) * c->cfg.n_kv_heads * c->cfg.page_size * c->cfg.head_dim;
+}
+
+}  // namespace
+}  // namespace dflash
+
+using namespace dflash;
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char *dflash_last_error(void) { return g_err.c_str(); }
+
+int dflash_create(const dflash_config *cfg, const dflash_weights *w, dflash_ctx **out) {
+  if (!cfg || !w || !out) return set_error(DFLASH_ERR_ARG, "dflash_create: null argument");
+  *out = nullptr;
+  const dflash_config &g = *cfg;
+  if (g.dtype != DFLASH_BF16 && g.dtype != DFLASH_F32) return set_error(DFLASH_ERR_ARG, "dtype must be bf16 or fp32");
+  if (g.block_size != 16 || g.top_k != 16 || g.page_size != 64)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "block_size and top_k must be 16, page_size 64");
+  if (g.hidden <= 0 || g.hidden % 16 || g.n_layers < 1 || g.n_layers > 16 || g.n_q_heads <= 0 || g.n_kv_heads <= 0 ||
+      g.n_q_heads % g.n_kv_heads || g.ffn <= 0 || g.ffn % 8 || g.vocab < 16 || g.target_hidden <= 0 ||
+      g.n_target_layers <= 0 || (g.n_target_layers * g.target_hidden) % 8)
+    return set_error(DFLASH_ERR_SHAPE, "inconsistent drafter shape");
+  if (g.dtype == DFLASH_BF16 && (g.head_dim != 128 || g.n_q_heads / g.n_kv_heads > 8))
+    return set_error(DFLASH_ERR_UNSUPPORTED, "bf16 path: head_dim must be 128 and q heads per kv head <= 8");
+  if (g.dtype == DFLASH_F32 && g.head_dim != 64 && g.head_dim != 128)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (g.mask_id < 0 || g.mask_id >= g.vocab) return set_error(DFLASH_ERR_ARG, "mask_id outside the vocabulary");
+  if (g.use_selector && (g.sel_rank < 1 || g.sel_rank > 64 || g.sel_dim < 1 || g.sel_dim > 1024))
+    return set_error(DFLASH_ERR_UNSUPPORTED, "selector rank must be 1..64 and width 1..1024");
+  if (!(g.eps >= 0.f) || !(g.rope_base > 1.f)) return set_error(DFLASH_ERR_ARG, "eps / rope_base out of range");
+  const void *req[] = {w->w_fc, w->embed, w->lm_head, w->g_final};
+  for (const void *p : req)
+    if (!p || !aligned16(p)) return set_error(DFLASH_ERR_ALIGN, "model weight missing or not 16-byte aligned");
+  if (g.fc_norm && !w->g_fc) return set_error(DFLASH_ERR_ARG, "fc_norm needs g_fc");
+  if (!w->layers) return set_error(DFLASH_ERR_ARG, "null layer array");
+  for (int l = 0; l < g.n_layers; ++l) {
+    const dflash_layer_weights &lw = w->layers[l];
+    const void *lp[] = {lw.g_attn, lw.w_qkv, lw.w_o, lw.g_ffn, lw.w_gu, lw.w_down};
+    for (const void *p : lp)
+      if (!p || !aligned16(p)) return set_error(DFLASH_ERR_ALIGN, "layer %d weight missing or misaligned", l);
+    if (g.qk_norm && (!lw.g_q || !lw.g_k)) return set_error(DFLASH_ERR_ARG, "layer %d: qk_norm needs g_q, g_k", l);
+    if (g.use_conv)
+      for (int s = 0; s < 4; ++s)
+        if (!lw.w_conv[s] || !lw.b_conv[s] || !aligned16(lw.w_conv[s]))
+          return set_error(DFLASH_ERR_ARG, "layer %d: conv site %d weights missing", l, s);
+  }
+  if (g.use_selector && (!w->sel_e256 || !w->sel_a || !w->sel_b || !w->sel_w_g))
+    return set_error(DFLASH_ERR_ARG, "selector weights missing");
+  dflash_ctx *c = new dflash_ctx();
+  c->cfg = g;
+  c->w = *w;
+  c->layers.assign(w->layers, w->layers + g.n_layers);
+  c->w.layers = c->layers.data();
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    delete c;
+    return set_error(DFLASH_ERR_CUDA, "no CUDA device");
+  }
+  *out = c;
+  return DFLASH_OK;
+}
+
+void dflash_destroy(dflash_ctx *ctx) { delete ctx; }
+
+size_t dflash_workspace_bytes(const dflash_ctx *ctx, int max_batch, int max_new_tokens) {
+  if (!ctx || max_batch < 0 || max_new_tokens < 0) return 0;
+  return layout(ctx, max_batch < 1 ? 1 : max_batch, max_new_tokens).total;
+}
+
+int dflash_set_wait_timeout(dflash_ctx *ctx, unsigned long long ns) {
+  if (!ctx || ns == 0) return set_error(DFLASH_ERR_ARG, "bad timeout");
+  ctx->timeout_ns = ns;
+  return DFLASH_OK;
+}
+
+int dflash_set_gemm_ctas(dflash_ctx *ctx, int ctas) {
+  if (!ctx || ctas < 0) return set_error(DFLASH_ERR_ARG, "bad CTA count");
+  ctx->gemm_ctas = ctas > ctx->num_sms ? ctx->num_sms : ctas;
+  return DFLASH_OK;
+}
+
+int dflash_set_attn_split(dflash_ctx *ctx, int tokens) {
+  if (!ctx || tokens < 0 || tokens % 64) return set_error(DFLASH_ERR_ARG, "split must be a multiple of 64");
+  ctx->attn_split = tokens;
+  return DFLASH_OK;
+}
+
+int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv, const void *target_hidden, const int32_t *cu_new,
+                          int total_new, const int32_t *ctx_len_in, int32_t *ctx_len_out, int batch, void *workspace,
+                          size_t workspace_bytes, dflash_stream_t stream) {
+  if (!ctx) return set_error(DFLASH_ERR_ARG, "null context");
+  if (batch < 0 || total_new < 0) return set_error(DFLASH_ERR_ARG, "negative batch / token count");
+  if (batch == 0 || total_new == 0) return DFLASH_OK;
+  if (!target_hidden || !cu_new || !ctx_len_in || !ctx_len_out)
+    return set_error(DFLASH_ERR_ARG, "dflash_inject_context: null argument");
+  if (!aligned16(target_hidden)) return set_error(DFLASH_ERR_ALIGN, "target_hidden must be 16-byte aligned");
+  if (int e = check_kv(ctx, kv)) return e;
+  if (int e = check_ws(ctx, workspace, workspace_bytes, batch, total_new)) return e;
+  const dflash_config &g = ctx->cfg;
+  const bool f32 = g.dtype == DFLASH_F32;
+  const Layout L = layout(ctx, batch, total_new);
+  Launch lc = make_launch(ctx, workspace, reinterpret_cast<cudaStream_t>(stream));
+  const int H = g.hidden, d = g.head_dim, nq = g.n_q_heads, nkv = g.n_kv_heads, K = g.n_target_layers * g.target_hidden;
+  const size_t te = f32 ? 4 : 2;
+  // context feature: fc projection, then RMSNorm
+  if (int e = proj(ctx, lc, workspace, L, ctx->w.w_fc, K, target_hidden, K, total_new, H, K, EPI_F32,
+                   at<float>(workspace, L.fc), H, nullptr, "fc"))
+    return e;
+  if (int e = feature_norm(lc, f32, at<float>(workspace, L.fc), total_new, H, ctx->w.g_fc, g.eps, g.fc_norm != 0,
+                           at<void>(workspace, L.f), ctx_len_in, at<int32_t>(workspace, L.ctx_saved), batch))
+    return e;
+  // every layer's own K/V projection of the feature (rows nq*d.. of w_qkv)
+  std::vector<const float *> gk(g.n_layers);
+  for (int l = 0; l < g.n_layers; ++l) {
+    const dflash_layer_weights &lw = ctx->layers[l];
+    const void *wkv = static_cast<const char *>(lw.w_qkv) + te * static_cast<size_t>(nq) * d * H;
+    float *dst = at<float>(workspace, L.kvproj) + static_cast<size_t>(l) * total_new * 2 * nkv * d;
+    if (int e = proj(ctx, lc, workspace, L, wkv, H, at<void>(workspace, L.f), H, total_new, 2 * nkv * d, H, EPI_F32,
+                     dst, 2 * nkv * d, nullptr, "kv_inject"))
+      return e;
+    gk[l] = lw.g_k;
+  }
+  return inject_scatter(lc, f32, at<float>(workspace, L.kvproj), total_new, g.n_layers, nkv, d, gk.data(),
+                        g.qk_norm != 0, g.eps, g.rope_base, cu_new, batch, at<int32_t>(workspace, L.ctx_saved),
+                        ctx_len_out, *kv, layer_elems(ctx, kv));
+}
+
+int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_len, const int32_t *anchor_ids,
+                       int batch, int32_t *topk_ids, float *topk_logits, void *final_hidden, float *logits,
+                       void *workspace, size_t workspace_bytes, dflash_stream_t stream) {
+  if (!ctx) return set_error(DFLASH_ERR_ARG, "null context");
+  if (batch < 0) return set_error(DFLASH_ERR_ARG, "negative batch");
+  if (batch == 0) return DFLASH_OK;
+  if (!ctx_len || !anchor_ids || !topk_ids || !topk_logits)
+    return set_error(DFLASH_ERR_ARG, "dflash_draft_block: null argument");
+  if (final_hidden && !aligned16(final_hidden)) return set_error(DFLASH_ERR_ALIGN, "final_hidden not aligned");
+  if (int e = check_kv(ctx, kv)) return e;
+  if (int e = check_ws(ctx, workspace, workspace_bytes, batch, 0)) return e;
+  const dflash_config &g = ctx->cfg;
+  const bool f32 = g.dtype == DFLASH_F32;
+  const Layout L = layout(ctx, batch, 0);
+  Launch lc = make_launch(ctx, workspace, reinterpret_cast<cudaStream_t>(stream));
+  void *ws = workspace;
+  const int B = batch, R = B * 16, H = g.hidden, d = g.head_dim, nq = g.n_q_heads, nkv = g.n_kv_heads;
+  const int F = g.ffn, V = g.vocab, nh = nq + 2 * nkv, G8 = H / 8;
+  float *x = at<float>(ws, L.x);
+  void *u = at<void>(ws, L.u), *u2 = at<void>(ws, L.u2), *ysub = at<void>(ws, L.ysub);
+  float *coef = at<float>(ws, L.coef);
+  void *hfinal = final_hidden ? final_hidden : at<void>(ws, L.hfinal);
+  float *lg = logits ? logits : at<float>(ws, L.logits);
+
+  // split-KV plan: enough CTAs to cover the SMs twice, at most ATTN_SLOTS
+  // partial slots, splits of at most 4096 tokens when that fits
+  const int max_ctx = kv->max_pages * g.page_size;
+  int split = ctx->attn_split;
+  if (split <= 0) {
+    const int bh = B * nkv;
+    int want = (2 * ctx->num_sms + bh - 1) / bh;
+    split = (max_ctx + want - 1) / want;
+    split = split < 128 ? 128 : split;
+    split = split > 4096 ? 4096 : split;
+    split = (split + 63) / 64 * 64;
+  }
+  int max_splits = (max_ctx + split - 1) / split;
+  if (max_splits < 1) max_splits = 1;
+  if (static_cast<long long>(max_splits) * B * nkv > ATTN_SLOTS) {
+    max_splits = ATTN_SLOTS / (B * nkv);
+    if (max_splits < 1) max_splits = 1;
+    split = ((max_ctx + max_splits - 1) / max_splits + 63) / 64 * 64;
+    max_splits = (max_ctx + split - 1) / split;
+  }
+
+  if (int e = embed_rmsnorm(lc, f32, ctx->w.embed, anchor_ids, g.mask_id, V, ctx->layers[0].g_attn, g.eps, B, H, x, u))
+    return e;
+  const size_t lelems = layer_elems(ctx, kv);
+  const size_t te = f32 ? 4 : 2;
+  for (int l = 0; l < g.n_layers; ++l) {
+    const dflash_layer_weights &lw = ctx->layers[l];
+    const void *ua = u;
+    // ---- attention sublayer
+    if (g.use_conv) {
+      if (int e = proj(ctx, lc, ws, L, lw.w_conv[0], H, u, H, R, G8, H, EPI_TANH_BIAS, coef, G8, lw.b_conv[0], "conv_coef"))
+        return e;
+      if (int e = conv_apply(lc, f32, u, coef, B, H, u2, nullptr)) return e;
+      ua = u2;
+    }
+    if (int e = proj(ctx, lc, ws, L, lw.w_qkv, H, ua, H, R, nh * d, H, EPI_F32, at<float>(ws, L.qkv), nh * d, nullptr,
+                     "qkv"))
+      return e;
+    if (int e = qk_norm_rope(lc, f32, at<float>(ws, L.qkv), B, nq, nkv, d, lw.g_q, lw.g_k, g.qk_norm != 0, g.eps,
+                             g.rope_base, ctx_len, at<void>(ws, L.q), at<void>(ws, L.bk), at<void>(ws, L.bv)))
+      return e;
+    AttnArgs aa = {};
+    aa.q = at<void>(ws, L.q);
+    aa.k_cache = static_cast<const char *>(kv->k_cache) + te * lelems * l;
+    aa.v_cache = static_cast<const char *>(kv->v_cache) + te * lelems * l;
+    aa.bk = at<void>(ws, L.bk);
+    aa.bv = at<void>(ws, L.bv);
+    aa.page_table = kv->page_table;
+    aa.max_pages = kv->max_pages;
+    aa.num_pages = kv->num_pages;
+    aa.page_size = g.page_size;
+    aa.ctx_len = ctx_len;
+    aa.out = at<void>(ws, L.o);
+    aa.part_o = at<float>(ws, L.attn_o);
+    aa.part_ml = at<float>(ws, L.attn_ml);
+    aa.counters = at<int>(ws, L.attn_ctr);
+    aa.B = B;
+    aa.nq = nq;
+    aa.nkv = nkv;
+    aa.d = d;
+    aa.split_tokens = split;
+    aa.max_splits = max_splits;
+    if (int e = f32 ? attention_f32(lc, aa) : attention_bf16(lc, aa)) return e;
+    if (g.use_conv) {
+      if (int e = proj(ctx, lc, ws, L, lw.w_o, nq * d, aa.out, nq * d, R, H, nq * d, EPI_STORE_T, ysub, H, nullptr, "o_proj"))
+        return e;
+      if (int e = proj(ctx, lc, ws, L, lw.w_conv[1], H, ysub, H, R, G8, H, EPI_TANH_BIAS, coef, G8, lw.b_conv[1], "conv_coef"))
+        return e;
+      if (int e = conv_apply(lc, f32, ysub, coef, B, H, nullptr, x)) return e;
+    } else {
+      if (int e = proj(ctx, lc, ws, L, lw.w_o, nq * d, aa.out, nq * d, R, H, nq * d, EPI_ADD_F32, x, H, nullptr, "o_proj"))
+        return e;
+    }
+    // ---- FFN sublayer
+    if (int e = rmsnorm_rows(lc, f32, x, R, H, lw.g_ffn, g.eps, u, nullptr)) return e;
+    ua = u;
+    if (g.use_conv) {
+      if (int e = proj(ctx, lc, ws, L, lw.w_conv[2], H, u, H, R, G8, H, EPI_TANH_BIAS, coef, G8, lw.b_conv[2], "conv_coef"))
+        return e;
+      if (int e = conv_apply(lc, f32, u, coef, B, H, u2, nullptr)) return e;
+      ua = u2;
+    }
+    if (int e = proj(ctx, lc, ws, L, lw.w_gu, H, ua, H, R, 2 * F, H, EPI_SWIGLU, at<void>(ws, L.hmid), F, nullptr,
+                     "gate_up"))
+      return e;
+    if (g.use_conv) {
+      if (int e = proj(ctx, lc, ws, L, lw.w_down, F, at<void>(ws, L.hmid), F, R, H, F, EPI_STORE_T, ysub, H, nullptr,
+                       "down"))
+        return e;
+      if (int e = proj(ctx, lc, ws, L, lw.w_conv[3], H, ysub, H, R, G8, H, EPI_TANH_BIAS, coef, G8, lw.b_conv[3], "conv_coef"))
+        return e;
+      if (int e = conv_apply(lc, f32, ysub, coef, B, H, nullptr, x)) return e;
+    } else {
+      if (int e = proj(ctx, lc, ws, L, lw.w_down, F, at<void>(ws, L.hmid), F, R, H, F, EPI_ADD_F32, x, H, nullptr,
+                       "down"))
+        return e;
+    }
+    if (l + 1 < g.n_layers)
+      if (int e = rmsnorm_rows(lc, f32, x, R, H, ctx->layers[l + 1].g_attn, g.eps, u, nullptr)) return e;
+  }
+  if (int e = rmsnorm_rows(lc, f32, x, R, H, ctx->w.g_final, g.eps, hfinal, at<void>(ws, L.hmask))) return e;
+  if (int e = proj(ctx, lc, ws, L, ctx->w.lm_head, H, at<void>(ws, L.hmask), H, B * 15, V, H, EPI_F32, lg, V, nullptr,
+                   "lm_head"))
+    return e;
+  return topk16(lc, lg, B * 15, V, topk_ids, topk_logits, at<uint64_t>(ws, L.topk_part), at<int>(ws, L.topk_ctr),
+                TOPK_MAX_CHUNKS);
+}
+
+int dflash_select_path(dflash_ctx *ctx, const int32_t *anchor_ids, const int32_t *topk_ids, const float *topk_logits,
+                       const void *final_hidden, int batch, int32_t *draft_ids, float *pair_scores_out,
+                       void *workspace, size_t workspace_bytes, dflash_stream_t stream) {
+  if (!ctx) return set_error(DFLASH_ERR_ARG, "null context");
+  if (batch < 0) return set_error(DFLASH_ERR_ARG, "negative batch");
+  if (batch == 0) return DFLASH_OK;
+  if (!topk_ids || !draft_ids) return set_error(DFLASH_ERR_ARG, "dflash_select_path: null argument");
+  const dflash_config &g = ctx->cfg;
+  Launch lc = make_launch(ctx, workspace, reinterpret_cast<cudaStream_t>(stream));
+  if (!g.use_selector) return greedy_path(lc, nullptr, topk_ids, batch, false, draft_ids);
+  if (!anchor_ids || !topk_logits || !final_hidden)
+    return set_error(DFLASH_ERR_ARG, "dflash_select_path: the selector needs anchors, logits and final_hidden");
+  float *sc = pair_scores_out;
+  if (!sc) {
+    if (int e = check_ws(ctx, workspace, workspace_bytes, batch, 0)) return e;
+    sc = at<float>(workspace, layout(ctx, batch, 0).scores);
+  }
+  if (int e = pair_scores(lc, g.dtype == DFLASH_F32, anchor_ids, topk_ids, topk_logits, final_hidden, batch, g.hidden,
+                          ctx->w.sel_e256, ctx->w.sel_a, ctx->w.sel_b, g.sel_rank, g.sel_dim, ctx->w.sel_w_g,
+                          ctx->w.sel_b_g, sc))
+    return e;
+  return greedy_path(lc, sc, topk_ids, batch, true, draft_ids);
+}
+
+int dflash_verify_greedy(const int32_t *draft_ids, const int32_t *target_ids, int batch, int32_t *accept_len,
+                         int32_t *bonus, int32_t *committed, dflash_stream_t stream) {
+  if (batch < 0) return set_error(DFLASH_ERR_ARG, "negative batch");
+  if (batch == 0) return DFLASH_OK;
+  if (!draft_ids || !target_ids || !accept_len || !bonus || !committed)
+    return set_error(DFLASH_ERR_ARG, "dflash_verify_greedy: null argument");
+  Launch lc;
+  lc.stream = reinterpret_cast<cudaStream_t>(stream);
+  return verify(lc, draft_ids, target_ids, batch, accept_len, bonus, committed);
+}
+
+int dflash_read_status(const void *workspace, int *device_status, dflash_stream_t stream) {
+  if (!workspace || !device_status) return set_error(DFLASH_ERR_ARG, "null argument");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (int e = cuda_check(cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s), "status read"))
+    return e;
+  if (int e = cuda_check(cudaStreamSynchronize(s), "status sync")) return e;
+  *device_status = v;
+  if (v != 0) {
+    cudaMemsetAsync(const_cast<void *>(workspace), 0, sizeof(int), s);
+    cudaStreamSynchronize(s);
+    return set_error(v, "a kernel reported status %d", v);
+  }
+  return DFLASH_OK;
+}
+
+int dflash_profile_begin(dflash_ctx *ctx) {
+  if (!ctx) return set_error(DFLASH_ERR_ARG, "null context");
+  ctx->prof.reset();
+  ctx->prof.on = true;
+  return DFLASH_OK;
+}
+
+int dflash_profile_end(dflash_ctx *ctx, dflash_kernel_stat *out, int max_out, int *n_out) {
+  if (!ctx || !n_out) return set_error(DFLASH_ERR_ARG, "null argument");
+  ctx->prof.on = false;
+  std::map<std::string, dflash_kernel_stat> agg;
+  std::vector<std::string> order;
+  for (auto &r : ctx->prof.recs) {
+    if (int e = cuda_check(cudaEventSynchronize(r.b), "profile sync")) return e;
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, r.a, r.b);
+    auto it = agg.find(r.name);
+    if (it == agg.end()) {
+      dflash_kernel_stat s = {};
+      snprintf(s.name, sizeof(s.name), "%s", r.name);
+      it = agg.emplace(r.name, s).first;
+      order.push_back(r.name);
+    }
+    it->second.launches += 1;
+    it->second.ms += ms;
+    it->second.bytes += r.bytes > 0 ? r.bytes : 0;
+    it->second.flops += r.flops > 0 ? r.flops : 0;
+  }
+  int n = 0;
+  for (auto &nm : order) {
+    if (out && n < max_out) out[n] = agg[nm];
+    ++n;
+  }
+  *n_out = n;
+  ctx->prof.reset();
+  return DFLASH_OK;
+}
+
+int dflash_debug_wait_flag(const int32_t *flag, unsigned long long timeout_ns, void *workspace,
+                           dflash_stream_t stream) {
+  if (!flag || !workspace || timeout_ns == 0) return set_error(DFLASH_ERR_ARG, "null argument");
+  Launch lc;
+  lc.stream = reinterpret_cast<cudaStream_t>(stream);
+  lc.status = at<int>(workspace, 0);
+  lc.timeout_ns = timeout_ns;
+  return wait_flag(lc, flag);
+}
+
+}  // extern "C"

@@ -1,0 +1,393 @@
+// Row-wise kernels of the drafting step: embedding gather + RMSNorm, RMSNorm,
+// context-feature norm, per-head q/k RMSNorm + RoPE, KV-injection scatter into
+// the paged cache, and the DFlash-2 dynamic short convolution.
+//
+// Readings used where the pages give no layer internals (Qwen3-shaped
+// drafter): RMSNorm y = g * x / sqrt(mean(x^2) + eps); RoPE pairs (i, i+d/2)
+// with theta_i = base^(-2i/d), rotation (x, y) -> (x cos - y sin, y cos + x sin);
+// the rotation angle is formed and range-reduced in fp64 so long positions
+// keep full fp32 accuracy.
+#include "common.cuh"
+#include "internal.h"
+
+#include <math.h>
+
+namespace dflash {
+namespace {
+
+template <typename T>
+__host__ __device__ inline T *tp(void *p) {
+  return static_cast<T *>(p);
+}
+
+// Block-wide sum for blockDim.x a multiple of 32 (<= 1024).
+__device__ __forceinline__ float block_sum(float v, float *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int i = 0; i < nw; ++i) t += red[i];
+  return t;
+}
+
+// cos / sin of pos * base^(-2i/d)
+__device__ __forceinline__ void rope_cs(int pos, int i, int d, float rope_base, float &c, float &s) {
+  const double theta = exp2(-2.0 * i / d * log2(static_cast<double>(rope_base)));
+  double a = static_cast<double>(pos) * theta;
+  const double twopi = 6.283185307179586476925286766559;
+  a -= twopi * rint(a / twopi);
+  sincosf(static_cast<float>(a), &s, &c);
+}
+
+// ------------------------------------------------------------------ embed
+// x[b*16+j] = E[id] (fp32 residual stream); u = RMSNorm(x) (activation dtype)
+template <typename T>
+__global__ void __launch_bounds__(256) embed_rmsnorm_kernel(const T *embed, const int32_t *anchor, int mask_id,
+                                                            int vocab, const float *gain, float eps, int H,
+                                                            float *x, T *u, int *status) {
+  grid_dep_wait();
+  __shared__ float red[32];
+  const int row = blockIdx.x, b = row >> 4, j = row & 15;
+  int id = j == 0 ? anchor[b] : mask_id;
+  if (id < 0 || id >= vocab) {
+    if (threadIdx.x == 0) report(status, DFLASH_ERR_DEVICE);
+    id = 0;
+  }
+  const T *e = embed + static_cast<size_t>(id) * H;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < H; c += blockDim.x) {
+    const float v = Elt<T>::ld(e + c);
+    x[static_cast<size_t>(row) * H + c] = v;
+    ss += v * v;
+  }
+  const float r = rsqrtf(block_sum(ss, red) / H + eps);
+  for (int c = threadIdx.x; c < H; c += blockDim.x)
+    Elt<T>::st(u + static_cast<size_t>(row) * H + c, x[static_cast<size_t>(row) * H + c] * r * gain[c]);
+}
+
+// ------------------------------------------------------------------ rmsnorm
+// out[row] = RMSNorm(x[row]); if out_mask is given, rows with j >= 1 are also
+// written compactly to out_mask[b*15 + j-1] (LM-head input of the mask rows).
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float *x, int H, const float *gain, float eps, T *out,
+                                                      T *out_mask) {
+  grid_dep_wait();
+  __shared__ float red[32];
+  const int row = blockIdx.x;
+  const float *xr = x + static_cast<size_t>(row) * H;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < H; c += blockDim.x) ss += xr[c] * xr[c];
+  const float r = rsqrtf(block_sum(ss, red) / H + eps);
+  const int b = row >> 4, j = row & 15;
+  T *o = out ? out + static_cast<size_t>(row) * H : nullptr;
+  T *om = (out_mask && j > 0) ? out_mask + static_cast<size_t>(b * 15 + j - 1) * H : nullptr;
+  for (int c = threadIdx.x; c < H; c += blockDim.x) {
+    const float v = xr[c] * r * gain[c];
+    if (o) Elt<T>::st(o + c, v);
+    if (om) Elt<T>::st(om + c, v);
+  }
+}
+
+// ------------------------------------------------------------------ feature
+// f = RMSNorm(fc output) (or the plain projection); block 0 also saves the
+// incoming context lengths so the scatter can read them even when the caller
+// updates ctx_len in place.
+template <typename T>
+__global__ void __launch_bounds__(256) feature_norm_kernel(const float *in, int H, const float *gain, float eps,
+                                                           int apply, T *out, const int32_t *ctx_in,
+                                                           int32_t *ctx_saved, int B) {
+  grid_dep_wait();
+  __shared__ float red[32];
+  const int row = blockIdx.x;
+  if (row == 0)
+    for (int b = threadIdx.x; b < B; b += blockDim.x) ctx_saved[b] = ctx_in[b];
+  const float *xr = in + static_cast<size_t>(row) * H;
+  float r = 1.f;
+  if (apply) {
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < H; c += blockDim.x) ss += xr[c] * xr[c];
+    r = rsqrtf(block_sum(ss, red) / H + eps);
+  }
+  for (int c = threadIdx.x; c < H; c += blockDim.x)
+    Elt<T>::st(out + static_cast<size_t>(row) * H + c, apply ? xr[c] * r * gain[c] : xr[c]);
+}
+
+// ------------------------------------------------------------------ q/k norm + rope
+// qkv: fp32 [B*16][(nq+2nkv)*d].  One warp per (token, head).  q heads ->
+// q_out [B*16][nq*d]; k heads -> bk [B][nkv][16][d] (normed, rotated);
+// v heads -> bv [B][nkv][16][d].
+template <typename T, int DPL>
+__global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, int nkv, const float *g_q,
+                                                      const float *g_k, int qk_norm, float eps, float rope_base,
+                                                      const int32_t *ctx_len, T *q_out, T *bk, T *bv) {
+  grid_dep_wait();
+  constexpr int D = DPL * 32;
+  const int tok = blockIdx.x, b = tok >> 4, j = tok & 15;
+  const int head = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int nh = nq + 2 * nkv;
+  if (head >= nh) return;
+  const float *src = qkv + static_cast<size_t>(tok) * nh * D + static_cast<size_t>(head) * D;
+  float v[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) v[i] = src[lane + 32 * i];
+  if (head >= nq + nkv) {   // value head: copy
+    T *dst = bv + ((static_cast<size_t>(b) * nkv + (head - nq - nkv)) * 16 + j) * D;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + lane + 32 * i, v[i]);
+    return;
+  }
+  const bool is_q = head < nq;
+  if (qk_norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) ss += v[i] * v[i];
+    const float r = rsqrtf(warp_sum(ss) / D + eps);
+    const float *g = is_q ? g_q : g_k;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) v[i] *= r * g[lane + 32 * i];
+  }
+  const int pos = ctx_len[b] + j;
+  float o[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL / 2; ++i) {   // pairs (lane + 32i, lane + 32i + D/2)
+    float c, s;
+    rope_cs(pos, lane + 32 * i, D, rope_base, c, s);
+    const float x1 = v[i], x2 = v[i + DPL / 2];
+    o[i] = x1 * c - x2 * s;
+    o[i + DPL / 2] = x2 * c + x1 * s;
+  }
+  T *dst = is_q ? q_out + static_cast<size_t>(tok) * nq * D + static_cast<size_t>(head) * D
+                : bk + ((static_cast<size_t>(b) * nkv + (head - nq)) * 16 + j) * D;
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + lane + 32 * i, o[i]);
+}
+
+// ------------------------------------------------------------------ injection scatter
+// kvproj: fp32 [L][T][2*nkv*d] (k heads then v heads of each layer's W_k, W_v
+// applied to the context feature).  Token t belongs to the request b with
+// cu_new[b] <= t < cu_new[b+1], position ctx_saved[b] + t - cu_new[b].
+struct ScatterArgs {
+  const float *kvproj;
+  int T, L, nkv;
+  const float *g_k[16];
+  int qk_norm;
+  float eps, rope_base;
+  const int32_t *cu_new;
+  int B;
+  const int32_t *ctx_saved;
+  int32_t *ctx_out;
+  void *k_cache, *v_cache;
+  const int32_t *page_table;
+  int num_pages, max_pages, page;
+  size_t layer_elems;
+  int *status;
+};
+
+template <typename T, int DPL>
+__global__ void __launch_bounds__(256) inject_scatter_kernel(const ScatterArgs a) {
+  grid_dep_wait();
+  constexpr int D = DPL * 32;
+  const int t = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int unit = blockIdx.y * 8 + (threadIdx.x >> 5);   // (layer, k/v, head)
+  if (t == 0 && blockIdx.y == 0)
+    for (int b = threadIdx.x; b < a.B; b += blockDim.x)
+      a.ctx_out[b] = a.ctx_saved[b] + (a.cu_new[b + 1] - a.cu_new[b]);
+  if (unit >= a.L * 2 * a.nkv) return;
+  const int l = unit / (2 * a.nkv), kv = (unit / a.nkv) & 1, h = unit % a.nkv;
+  // request of token t: last b with cu_new[b] <= t
+  int lo = 0, hi = a.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.cu_new[mid] <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int b = lo;
+  const int pos = a.ctx_saved[b] + t - a.cu_new[b];
+  const int pidx = pos / a.page;
+  const int pg = (pos >= 0 && pidx < a.max_pages) ? a.page_table[static_cast<size_t>(b) * a.max_pages + pidx] : -1;
+  if (pg < 0 || pg >= a.num_pages) {
+    if (lane == 0) report(a.status, DFLASH_ERR_DEVICE);
+    return;
+  }
+  const float *src = a.kvproj + (static_cast<size_t>(l) * a.T + t) * (2 * a.nkv * D) + (kv * a.nkv + h) * D;
+  float v[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) v[i] = src[lane + 32 * i];
+  if (kv == 0) {
+    if (a.qk_norm) {
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) ss += v[i] * v[i];
+      const float r = rsqrtf(warp_sum(ss) / D + a.eps);
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) v[i] *= r * a.g_k[l][lane + 32 * i];
+    }
+    float o[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL / 2; ++i) {
+      float c, s;
+      rope_cs(pos, lane + 32 * i, D, a.rope_base, c, s);
+      o[i] = v[i] * c - v[i + DPL / 2] * s;
+      o[i + DPL / 2] = v[i + DPL / 2] * c + v[i] * s;
+    }
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) v[i] = o[i];
+  }
+  T *cache = static_cast<T *>(kv == 0 ? a.k_cache : a.v_cache) + l * a.layer_elems;
+  T *dst = cache + ((static_cast<size_t>(pg) * a.nkv + h) * a.page + pos % a.page) * D;
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + lane + 32 * i, v[i]);
+}
+
+// ------------------------------------------------------------------ short conv
+// DFlash-2 ("DFlash 2", Arquitectura del Sistema item 2): two taps along the
+// block, coefficients per 16-channel group, nothing before position 0.
+//   coef: fp32 [B*16][H/8] = tanh(W_c y + b_c): [0, H/16) current tap a,
+//         [H/16, H/8) previous tap b.
+//   out_j = y_j + a_j * y_j + b_j * y_{j-1}
+// pre sites: out_t = conv(y) (activation dtype); post sites: x_add += conv(y).
+template <typename T>
+__global__ void __launch_bounds__(256) conv_kernel(const T *y, const float *coef, int H, T *out_t, float *x_add) {
+  grid_dep_wait();
+  const int b = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= H) return;
+  const int G = H / 16, grp = c >> 4;
+  float prev = 0.f;
+  for (int j = 0; j < 16; ++j) {
+    const size_t row = static_cast<size_t>(b) * 16 + j;
+    const float cur = Elt<T>::ld(y + row * H + c);
+    const float a = coef[row * (2 * G) + grp], bb = coef[row * (2 * G) + G + grp];
+    const float v = cur + a * cur + bb * prev;
+    if (out_t)
+      Elt<T>::st(out_t + row * H + c, v);
+    else
+      x_add[row * H + c] += v;
+    prev = cur;
+  }
+}
+
+template <typename F>
+int run(const Launch &lc, const char *name, F f) {
+  ProfScope ps(lc, name, -1.0, -1.0);
+  f();
+  return cuda_check(cudaGetLastError(), name);
+}
+
+}  // namespace
+
+int embed_rmsnorm(const Launch &lc, bool f32, const void *embed, const int32_t *anchor, int mask_id, int vocab,
+                  const float *gain, float eps, int B, int H, float *x, void *u) {
+  return run(lc, "embed_norm", [&] {
+    if (f32)
+      embed_rmsnorm_kernel<float><<<B * 16, 256, 0, lc.stream>>>(static_cast<const float *>(embed), anchor, mask_id,
+                                                                 vocab, gain, eps, H, x, tp<float>(u), lc.status);
+    else
+      embed_rmsnorm_kernel<__nv_bfloat16><<<B * 16, 256, 0, lc.stream>>>(
+          static_cast<const __nv_bfloat16 *>(embed), anchor, mask_id, vocab, gain, eps, H, x,
+          tp<__nv_bfloat16>(u), lc.status);
+  });
+}
+
+int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, const float *gain, float eps,
+                 void *out, void *out_mask_rows) {
+  return run(lc, "rmsnorm", [&] {
+    if (f32)
+      rmsnorm_kernel<float><<<rows, 256, 0, lc.stream>>>(x, H, gain, eps, tp<float>(out), tp<float>(out_mask_rows));
+    else
+      rmsnorm_kernel<__nv_bfloat16><<<rows, 256, 0, lc.stream>>>(x, H, gain, eps, tp<__nv_bfloat16>(out),
+                                                                 tp<__nv_bfloat16>(out_mask_rows));
+  });
+}
+
+int feature_norm(const Launch &lc, bool f32, const float *in, int rows, int H, const float *gain, float eps,
+                 bool apply_norm, void *out, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B) {
+  if (rows <= 0) return DFLASH_OK;
+  return run(lc, "feature_norm", [&] {
+    if (f32)
+      feature_norm_kernel<float><<<rows, 256, 0, lc.stream>>>(in, H, gain, eps, apply_norm, tp<float>(out),
+                                                              ctx_len_in, ctx_len_saved, B);
+    else
+      feature_norm_kernel<__nv_bfloat16><<<rows, 256, 0, lc.stream>>>(in, H, gain, eps, apply_norm,
+                                                                      tp<__nv_bfloat16>(out), ctx_len_in,
+                                                                      ctx_len_saved, B);
+  });
+}
+
+int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int nq, int nkv, int d, const float *g_q,
+                 const float *g_k, bool qk_norm, float eps, float rope_base, const int32_t *ctx_len, void *q_out,
+                 void *bk, void *bv) {
+  dim3 grid(B * 16, (nq + 2 * nkv + 7) / 8);
+  return run(lc, "qk_norm_rope", [&] {
+#define QK(T, DPL)                                                                                              \
+  qk_rope_kernel<T, DPL><<<grid, 256, 0, lc.stream>>>(qkv, nq, nkv, g_q, g_k, qk_norm, eps, rope_base, ctx_len, \
+                                                      tp<T>(q_out), tp<T>(bk), tp<T>(bv))
+    if (f32 && d == 64)
+      QK(float, 2);
+    else if (f32)
+      QK(float, 4);
+    else if (d == 64)
+      QK(__nv_bfloat16, 2);
+    else
+      QK(__nv_bfloat16, 4);
+#undef QK
+  });
+}
+
+int inject_scatter(const Launch &lc, bool f32, const float *kvproj, int T, int L, int nkv, int d,
+                   const float *const *g_k, bool qk_norm, float eps, float rope_base, const int32_t *cu_new, int B,
+                   const int32_t *ctx_len_saved, int32_t *ctx_len_out, const dflash_kv &kv, size_t layer_elems) {
+  if (T <= 0) return DFLASH_OK;
+  if (L > 16) return set_error(DFLASH_ERR_UNSUPPORTED, "at most 16 drafter layers");
+  ScatterArgs a = {};
+  a.kvproj = kvproj;
+  a.T = T;
+  a.L = L;
+  a.nkv = nkv;
+  for (int l = 0; l < L; ++l) a.g_k[l] = g_k[l];
+  a.qk_norm = qk_norm;
+  a.eps = eps;
+  a.rope_base = rope_base;
+  a.cu_new = cu_new;
+  a.B = B;
+  a.ctx_saved = ctx_len_saved;
+  a.ctx_out = ctx_len_out;
+  a.k_cache = kv.k_cache;
+  a.v_cache = kv.v_cache;
+  a.page_table = kv.page_table;
+  a.num_pages = kv.num_pages;
+  a.max_pages = kv.max_pages;
+  a.page = 64;
+  a.layer_elems = layer_elems;
+  a.status = lc.status;
+  dim3 grid(T, (L * 2 * nkv + 7) / 8);
+  return run(lc, "inject_scatter", [&] {
+    if (f32 && d == 64)
+      inject_scatter_kernel<float, 2><<<grid, 256, 0, lc.stream>>>(a);
+    else if (f32)
+      inject_scatter_kernel<float, 4><<<grid, 256, 0, lc.stream>>>(a);
+    else if (d == 64)
+      inject_scatter_kernel<__nv_bfloat16, 2><<<grid, 256, 0, lc.stream>>>(a);
+    else
+      inject_scatter_kernel<__nv_bfloat16, 4><<<grid, 256, 0, lc.stream>>>(a);
+  });
+}
+
+int conv_apply(const Launch &lc, bool f32, const void *y, const float *coef, int B, int H, void *out_t,
+               float *x_add) {
+  dim3 grid((H + 255) / 256, B);
+  return run(lc, "short_conv", [&] {
+    if (f32)
+      conv_kernel<float><<<grid, 256, 0, lc.stream>>>(static_cast<const float *>(y), coef, H, tp<float>(out_t), x_add);
+    else
+      conv_kernel<__nv_bfloat16><<<grid, 256, 0, lc.stream>>>(static_cast<const __nv_bfloat16 *>(y), coef, H,
+                                                              tp<__nv_bfloat16>(out_t), x_add);
+  });
+}
+
+}  // namespace dflash

@@ -1,0 +1,410 @@
+// Persistent stream-K GEMM on the 5th-generation tensor cores (tcgen05).
+//
+//   out[m][n] = epi( sum_k X[m][k] * W[n][k] )      W: [N][K] weights, X: [M][K]
+//
+// Every drafter projection (context feature, per-layer K/V injection, QKV, O,
+// gate/up, down, conv coefficients, LM head) is this contraction.  During a
+// drafting step M is tiny (16 tokens per request) while W is up to 1.2 GB, so
+// the kernel is built around streaming W at HBM speed:
+//   * swap-AB: the weight tile is the 128-row UMMA "M" operand, the token
+//     tile (BN = 16..256 rows) the "N" operand; the accumulator sits in TMEM
+//     as [weight row = lane][token = column];
+//   * stream-K: the (tile, 64-wide k-block) iteration space is cut into one
+//     contiguous range per CTA, one persistent CTA per SM, so a GEMM with 32
+//     row tiles still keeps all SMs streaming.  A tile split across CTAs is
+//     finished by whichever CTA completes it last (per-tile counter), which
+//     sums the fp32 partials in CTA order - deterministic, no spin-waits;
+//   * warp roles: warp 0 issues TMA loads into a STAGES-deep ring of
+//     128-byte-swizzled tiles, warp 1 owns TMEM and issues tcgen05.mma from
+//     one thread, warps 2-5 drain TMEM (double-buffered) into the epilogue.
+// Every mbarrier wait is bounded (status word + unwind on timeout).
+#include "common.cuh"
+#include "internal.h"
+
+#include <algorithm>
+
+namespace dflash {
+namespace {
+
+constexpr int BM = 128;   // weight rows per tile (UMMA M)
+constexpr int BK = 64;    // bf16 elements per stage row = 128 bytes = one swizzle row
+constexpr int UK = 16;    // K per tcgen05.mma (kind::f16)
+constexpr int NTHREADS = 192;
+
+template <int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+};
+
+struct Params {
+  int M, N, K;
+  int tok_tiles, kbpt;
+  long long total;     // tiles * kbpt
+  int G;               // CTAs
+  int epi;
+  void *out;
+  int ldo;
+  const float *bias;
+  float *partials;     // [G][2][BM*BN]
+  int *counters;       // [tiles]
+  int *status;
+  unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ long long range_begin(long long total, int G, int c) {
+  return static_cast<long long>(c) * total / G;
+}
+// CTA whose range contains iteration i (ranges [c*T/G, (c+1)*T/G)).
+__device__ __forceinline__ int cta_of(long long i, long long total, int G) {
+  return static_cast<int>(((i + 1) * G + total - 1) / total) - 1;
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// Apply the epilogue to 16 consecutive token columns of weight row n.
+__device__ __forceinline__ void finalize(const Params &p, const float (&v)[16], int n, int tok0) {
+  const bool nok = n < p.N;
+  switch (p.epi) {
+    case EPI_BF16: {
+      __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (nok && tok0 + i < p.M) o[static_cast<size_t>(tok0 + i) * p.ldo + n] = f2bf(v[i]);
+    } break;
+    case EPI_F32: {
+      float *o = static_cast<float *>(p.out);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (nok && tok0 + i < p.M) o[static_cast<size_t>(tok0 + i) * p.ldo + n] = v[i];
+    } break;
+    case EPI_ADD_F32: {
+      float *o = static_cast<float *>(p.out);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (nok && tok0 + i < p.M) o[static_cast<size_t>(tok0 + i) * p.ldo + n] += v[i];
+    } break;
+    case EPI_SWIGLU: {
+      __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float up = __shfl_xor_sync(0xffffffffu, v[i], 1);
+        if (nok && !(n & 1) && tok0 + i < p.M) o[static_cast<size_t>(tok0 + i) * p.ldo + (n >> 1)] = f2bf(silu(v[i]) * up);
+      }
+    } break;
+    case EPI_TANH_BIAS: {
+      float *o = static_cast<float *>(p.out);
+      const float b = nok ? p.bias[n] : 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (nok && tok0 + i < p.M) o[static_cast<size_t>(tok0 + i) * p.ldo + n] = tanhf(v[i] + b);
+    } break;
+    default:
+      break;
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const Params p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t *base = smem_raw + pad;
+  uint8_t *sA = base;
+  uint8_t *sB = base + C::STAGES * C::A_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::STAGES * C::B_BYTES);
+  uint64_t *empty = full + C::STAGES;
+  uint64_t *tfull = empty + C::STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *bcast = reinterpret_cast<int *>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    mbar_init(&tempty[0], 4);
+    mbar_init(&tempty[1], 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Operands and outputs may be produced / consumed by the neighbouring
+  // kernels of the step: wait for them here (no-op without PDL).
+  grid_dep_wait();
+
+  const long long begin = range_begin(p.total, p.G, blockIdx.x);
+  const long long end = range_begin(p.total, p.G, blockIdx.x + 1);
+  const int first_tile = static_cast<int>(begin / p.kbpt);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      uint32_t stage = 0, phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (long long it = begin; it < end && ok;) {
+        const int tile = static_cast<int>(it / p.kbpt);
+        const int kb0 = static_cast<int>(it % p.kbpt);
+        const int kb1 = static_cast<int>((kb0 + (end - it) < p.kbpt ? kb0 + (end - it) : p.kbpt));
+        const int row0 = (tile / p.tok_tiles) * BM;
+        const int tok0 = (tile % p.tok_tiles) * BN;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          tma_load_2d_hint(sA + stage * C::A_BYTES, &tmW, &full[stage], kb * BK, row0, pol_w);
+          tma_load_2d(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * BK, tok0);
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        it += kb1 - kb0;
+      }
+      grid_dep_launch();
+      if (!ok) {
+        report(p.status, DFLASH_ERR_TIMEOUT);
+        *abort_flag = 1;
+        // let every issued copy land before the CTA's shared memory goes away
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (issued <= s) break;
+          const long long last = s + C::STAGES * ((issued - 1 - s) / C::STAGES);
+          mbar_wait(&full[s], static_cast<uint32_t>((last / C::STAGES) & 1), nullptr, p.timeout_ns);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      uint32_t stage = 0, phase = 0;
+      int seg = 0;
+      bool ok = true;
+      for (long long it = begin; it < end && ok; ++seg) {
+        const int kb0 = static_cast<int>(it % p.kbpt);
+        const int kb1 = static_cast<int>((kb0 + (end - it) < p.kbpt ? kb0 + (end - it) : p.kbpt));
+        const int buf = seg & 1;
+        if (!mbar_wait(&tempty[buf], static_cast<uint32_t>(((seg >> 1) & 1) ^ 1), abort_flag, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / UK; ++k)
+            umma_bf16(d, sdesc_k_sw128(a0 + k * UK * 2), sdesc_k_sw128(b0 + k * UK * 2), idesc,
+                      (kb > kb0 || k > 0) ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[buf]);
+        it += kb1 - kb0;
+      }
+      if (!ok) {
+        report(p.status, DFLASH_ERR_TIMEOUT);
+        *abort_flag = 1;
+        umma_commit(drain);   // all issued MMAs retire before TMEM is freed
+        mbar_wait(drain, 0, nullptr, p.timeout_ns);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;              // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;         // weight row within the tile
+    const int et = threadIdx.x - 64;     // 0..127
+    int seg = 0;
+    for (long long it = begin; it < end; ++seg) {
+      const int tile = static_cast<int>(it / p.kbpt);
+      const int kb0 = static_cast<int>(it % p.kbpt);
+      const int kb1 = static_cast<int>((kb0 + (end - it) < p.kbpt ? kb0 + (end - it) : p.kbpt));
+      const int buf = seg & 1;
+      const bool got = mbar_wait(&tfull[buf], static_cast<uint32_t>((seg >> 1) & 1), abort_flag, p.timeout_ns);
+      // one uniform decision for all 128 epilogue threads (they meet at named barriers below)
+      if (bar_or(1, 128, !got || *abort_flag)) {
+        if (et == 0) report(p.status, DFLASH_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int n = (tile / p.tok_tiles) * BM + r;
+      const int tok0 = (tile % p.tok_tiles) * BN;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      float v[16];
+      if (kb0 == 0 && kb1 == p.kbpt) {
+        for (int c = 0; c < BN / 16; ++c) {
+          tmem_ld16(taddr + c * 16, v);
+          finalize(p, v, n, tok0 + c * 16);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+      } else {
+        const int slot = (tile == first_tile) ? 0 : 1;
+        float *P = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * (BM * BN);
+        for (int c = 0; c < BN / 16; ++c) {
+          tmem_ld16(taddr + c * 16, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) __stcg(&P[(c * 16 + i) * BM + r], v[i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+        __threadfence();
+        epi_bar();
+        if (et == 0) {
+          const int nk = kb1 - kb0;
+          const int old = atomicAdd(&p.counters[tile], nk);
+          const int last = (old + nk == p.kbpt) ? 1 : 0;
+          if (last) p.counters[tile] = 0;   // self-cleaning for the next launch
+          *bcast = last;
+          __threadfence();
+        }
+        epi_bar();
+        if (*bcast) {
+          const long long t_beg = static_cast<long long>(tile) * p.kbpt;
+          const int c_lo = cta_of(t_beg, p.total, p.G);
+          const int c_hi = cta_of(t_beg + p.kbpt - 1, p.total, p.G);
+          for (int c = 0; c < BN / 16; ++c) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            for (int cc = c_lo; cc <= c_hi; ++cc) {
+              const int ft = static_cast<int>(range_begin(p.total, p.G, cc) / p.kbpt);
+              const float *Q = p.partials + (static_cast<size_t>(cc) * 2 + (ft == tile ? 0 : 1)) * (BM * BN);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] += __ldcg(&Q[(c * 16 + i) * BM + r]);
+            }
+            finalize(p, v, n, tok0 + c * 16);
+          }
+        }
+        epi_bar();
+      }
+      it += kb1 - kb0;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int BN>
+int launch(const Launch &lc, const CUtensorMap &tW, const CUtensorMap &tX, const Params &p) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                Cfg<BN>::SMEM),
+                           "gemm smem attribute"))
+      return e;
+    attr_done = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.G);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tW, tX, p), "gemm launch");
+}
+
+}  // namespace
+
+int gemm_bf16(const Launch &lc, const void *W, int ldw, const void *X, int ldx, int M, int N, int K, int epi,
+              void *out, int ldo, const float *bias, const GemmScratch &sc, const char *name) {
+  if (M <= 0 || N <= 0 || K <= 0) return DFLASH_OK;
+  if (!W || !X || !out) return set_error(DFLASH_ERR_ARG, "gemm %s: null operand", name);
+  if ((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(X)) & 15 || (ldw * 2) % 16 || (ldx * 2) % 16)
+    return set_error(DFLASH_ERR_ALIGN, "gemm %s: operands / row strides must be 16-byte aligned", name);
+  if (epi == EPI_STORE_T) epi = EPI_BF16;
+  const int BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  Params p = {};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.tok_tiles = (M + BN - 1) / BN;
+  const int row_tiles = (N + BM - 1) / BM;
+  p.kbpt = (K + BK - 1) / BK;
+  const long long tiles = static_cast<long long>(row_tiles) * p.tok_tiles;
+  p.total = tiles * p.kbpt;
+  const int cap = lc.gemm_ctas > 0 ? lc.gemm_ctas : lc.num_sms;
+  p.G = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, (p.total + 3) / 4)));
+  p.epi = epi;
+  p.out = out;
+  p.ldo = ldo;
+  p.bias = bias;
+  p.partials = sc.partials;
+  p.counters = sc.counters;
+  p.status = lc.status;
+  p.timeout_ns = lc.timeout_ns;
+  if (tiles > sc.n_counters || static_cast<size_t>(p.G) * 2 * BM * BN > sc.partial_floats)
+    return set_error(DFLASH_ERR_SHAPE, "gemm %s: workspace too small for %lld tiles", name, tiles);
+  CUtensorMap tW, tX;
+  if (int e = make_tmap_2d(&tW, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, static_cast<uint64_t>(ldw) * 2, BK, BM))
+    return e;
+  if (int e = make_tmap_2d(&tX, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M, static_cast<uint64_t>(ldx) * 2, BK, BN))
+    return e;
+  const double out_bytes = (epi == EPI_F32 || epi == EPI_TANH_BIAS) ? 4.0 * M * N
+                           : epi == EPI_ADD_F32                      ? 8.0 * M * N
+                           : epi == EPI_SWIGLU                       ? 1.0 * M * N
+                                                                     : 2.0 * M * N;
+  ProfScope ps(lc, name, 2.0 * N * K + 2.0 * M * K + out_bytes, 2.0 * M * N * K);
+  switch (BN) {
+    case 16: return launch<16>(lc, tW, tX, p);
+    case 32: return launch<32>(lc, tW, tX, p);
+    case 64: return launch<64>(lc, tW, tX, p);
+    case 128: return launch<128>(lc, tW, tX, p);
+    default: return launch<256>(lc, tW, tX, p);
+  }
+}
+
+}  // namespace dflash

@@ -1,0 +1,129 @@
+// Host-side interfaces shared by the translation units of libdflash.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/dflash.h"
+
+namespace dflash {
+
+// GEMM epilogues: out[m][n] = epi(sum_k X[m][k] * W[n][k])
+enum Epi : int {
+  EPI_BF16 = 0,       // out (bf16)  = acc
+  EPI_F32 = 1,        // out (fp32)  = acc
+  EPI_ADD_F32 = 2,    // out (fp32) += acc          (residual stream)
+  EPI_SWIGLU = 3,     // rows 2i / 2i+1 = gate_i / up_i: out[m][i] = silu(gate) * up (out dtype)
+  EPI_TANH_BIAS = 4,  // out (fp32)  = tanh(acc + bias[n])   (conv coefficients)
+  EPI_STORE_T = 5     // out (activation dtype) = acc  (bf16 or fp32 by the ctx dtype)
+};
+
+// Per-launch timing of kernel families (dflash_profile_begin / _end).
+struct Profiler {
+  struct Rec {
+    const char *name;
+    cudaEvent_t a, b;
+    double bytes, flops;
+  };
+  bool on = false;
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> pool;
+  size_t used = 0;
+  cudaEvent_t take();
+  void reset();
+  ~Profiler();
+};
+
+struct Launch {
+  cudaStream_t stream = nullptr;
+  int num_sms = 148;
+  int *status = nullptr;                 // device status word
+  unsigned long long timeout_ns = 2000000000ull;
+  int gemm_ctas = 0;                     // 0 = SM count
+  Profiler *prof = nullptr;
+};
+
+// RAII: records CUDA events around the launches in its scope when profiling.
+struct ProfScope {
+  const Launch &lc;
+  int idx = -1;
+  ProfScope(const Launch &l, const char *name, double bytes, double flops);
+  ~ProfScope();
+};
+
+struct GemmScratch {
+  float *partials = nullptr;   // [ctas][2][128 * 256] fp32
+  size_t partial_floats = 0;
+  int *counters = nullptr;     // one per output tile, zero between launches
+  int n_counters = 0;
+};
+
+int set_error(int code, const char *fmt, ...);
+int cuda_check(cudaError_t e, const char *what);
+
+// TMA descriptor of a row-major 2-D tensor [rows][cols] with 128-byte
+// swizzle; box = box_cols x box_rows.
+int make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elt_bytes, uint64_t cols,
+                 uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows);
+
+// bf16 operands on tcgen05 tensor cores.  W: [N][ldw], X: [M][ldx].
+int gemm_bf16(const Launch &lc, const void *W, int ldw, const void *X, int ldx, int M, int N, int K, int epi,
+              void *out, int ldo, const float *bias, const GemmScratch &sc, const char *name);
+// fp32 operands on CUDA cores (tiny fp32 configurations).
+int gemm_f32(const Launch &lc, const float *W, int ldw, const float *X, int ldx, int M, int N, int K, int epi,
+             void *out, int ldo, const float *bias, const char *name);
+
+// ---------------------------------------------------------------- attention
+struct AttnArgs {
+  const void *q;            // [B*16][nq*d] (dtype)
+  const void *k_cache;      // this layer: [num_pages][nkv][page][d]
+  const void *v_cache;
+  const void *bk, *bv;      // block K/V [B][nkv][16][d]
+  const int32_t *page_table;
+  int max_pages, num_pages, page_size;
+  const int32_t *ctx_len;   // [B]
+  void *out;                // [B*16][nq*d] (dtype)
+  float *part_o;            // split partials
+  float *part_ml;
+  int *counters;            // [B*nkv]
+  int B, nq, nkv, d;
+  int split_tokens;         // multiple of page_size
+  int max_splits;
+};
+int attention_bf16(const Launch &lc, const AttnArgs &a);
+int attention_f32(const Launch &lc, const AttnArgs &a);
+
+// ---------------------------------------------------------------- elementwise
+int embed_rmsnorm(const Launch &lc, bool f32, const void *embed, const int32_t *anchor, int mask_id, int vocab,
+                  const float *gain, float eps, int B, int H, float *x, void *u);
+int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, const float *gain, float eps,
+                 void *out, void *out_mask_rows);
+int feature_norm(const Launch &lc, bool f32, const float *in, int rows, int H, const float *gain, float eps,
+                 bool apply_norm, void *out, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B);
+int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int nq, int nkv, int d,
+                 const float *g_q, const float *g_k, bool qk_norm, float eps, float rope_base,
+                 const int32_t *ctx_len, void *q_out, void *bk, void *bv);
+int inject_scatter(const Launch &lc, bool f32, const float *kvproj, int T, int L, int nkv, int d,
+                   const float *const *g_k, bool qk_norm, float eps, float rope_base, const int32_t *cu_new,
+                   int B, const int32_t *ctx_len_saved, int32_t *ctx_len_out, const dflash_kv &kv,
+                   size_t layer_elems);
+int conv_apply(const Launch &lc, bool f32, const void *y, const float *coef, int B, int H, void *out_t,
+               float *x_add);
+
+// ---------------------------------------------------------------- top-k / select / verify
+int topk16(const Launch &lc, const float *logits, int rows, int V, int32_t *ids, float *vals,
+           uint64_t *part_keys, int *counters, int max_chunks);
+int pair_scores(const Launch &lc, bool f32, const int32_t *anchor, const int32_t *topk_ids,
+                const float *topk_logits, const void *final_hidden, int B, int H, const void *e256,
+                const void *sel_a, const void *sel_b, int r, int E, const float *w_g, float b_g, float *scores);
+int greedy_path(const Launch &lc, const float *scores, const int32_t *topk_ids, int B, bool use_scores,
+                int32_t *draft);
+int verify(const Launch &lc, const int32_t *draft, const int32_t *target, int B, int32_t *accept, int32_t *bonus,
+           int32_t *committed);
+int wait_flag(const Launch &lc, const int32_t *flag);
+
+}  // namespace dflash

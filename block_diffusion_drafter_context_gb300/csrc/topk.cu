@@ -1,0 +1,138 @@
+// Top-16 candidates per mask position ("DFlash 2", Arquitectura del Sistema
+// item 1: the drafter proposes a list of 16 candidates per position).
+//
+// Order: value descending, token id ascending on ties.  Each (value, id) is
+// packed into one 64-bit key whose unsigned order is exactly that order, so
+// every key is unique and the selection is deterministic.
+//
+// One row = the fp32 logits of one mask position over the vocabulary.  A row
+// is cut into chunks, one CTA each, to fill the GPU when there are few rows.
+// Every warp streams its share with 128-bit loads and keeps a sorted top-16
+// in lanes 0..15; an element enters only if it beats the warp's current 16th
+// key (ballot), which after the first few hundred elements almost never
+// happens, so the scan runs at load speed.  Warps merge in shared memory;
+// chunks merge in the CTA that finishes a row last (per-row counter).
+#include "common.cuh"
+#include "internal.h"
+
+namespace dflash {
+namespace {
+
+constexpr int K = 16;
+constexpr int WARPS = 8;
+
+__device__ __forceinline__ uint64_t make_key(float v, int id) {
+  uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);   // -0 and +0 compare equal
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(id));
+}
+__device__ __forceinline__ float key_value(uint64_t k) {
+  uint32_t u = static_cast<uint32_t>(k >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(u);
+}
+__device__ __forceinline__ int key_id(uint64_t k) { return static_cast<int>(~static_cast<uint32_t>(k)); }
+
+// Warp-wide sorted list in lanes 0..15 (descending).  Insert key k (uniform).
+__device__ __forceinline__ void insert(uint64_t &list, uint64_t k, int lane) {
+  const uint64_t up = __shfl_up_sync(0xffffffffu, list, 1);
+  if (lane < K) list = (list > k) ? list : ((lane == 0 || up > k) ? k : up);
+}
+
+// Offer one key per lane; inserts every key that beats the current 16th.
+__device__ __forceinline__ void offer(uint64_t &list, uint64_t &thr, uint64_t key, int lane) {
+  unsigned m = __ballot_sync(0xffffffffu, key > thr);
+  while (m) {
+    const int src = __ffs(m) - 1;
+    const uint64_t k = __shfl_sync(0xffffffffu, key, src);
+    insert(list, k, lane);
+    thr = __shfl_sync(0xffffffffu, list, K - 1);
+    m &= ~(1u << src);
+    m &= __ballot_sync(0xffffffffu, key > thr);
+  }
+}
+
+__global__ void __launch_bounds__(WARPS * 32) topk_kernel(const float *__restrict__ logits, int V, int chunk,
+                                                          int nchunks, int32_t *ids, float *vals,
+                                                          uint64_t *part, int *counters) {
+  grid_dep_wait();
+  __shared__ uint64_t sm[WARPS * K];
+  __shared__ int last;
+  const int row = blockIdx.y, c = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float *x = logits + static_cast<size_t>(row) * V;
+  const int lo = c * chunk, hi = min(V, lo + chunk);
+  uint64_t list = 0, thr = 0;
+  if ((V & 3) == 0) {
+    // lo is a multiple of 4 (chunk is), so float4 loads stay aligned
+    for (int wb = lo + warp * 128; wb < hi; wb += WARPS * 128) {   // warp-uniform trip count
+      const int base = wb + lane * 4;
+      float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      const bool in = base < hi;   // hi is a multiple of 4: the whole float4 is in range
+      if (in) v = __ldcs(reinterpret_cast<const float4 *>(x + base));
+      offer(list, thr, in ? make_key(v.x, base) : 0, lane);
+      offer(list, thr, in ? make_key(v.y, base + 1) : 0, lane);
+      offer(list, thr, in ? make_key(v.z, base + 2) : 0, lane);
+      offer(list, thr, in ? make_key(v.w, base + 3) : 0, lane);
+    }
+  } else {
+    for (int base = lo + warp * 32 + lane; base - lane < hi; base += WARPS * 32) {
+      const bool in = base < hi;
+      offer(list, thr, in ? make_key(__ldcs(x + base), base) : 0, lane);
+    }
+  }
+  if (lane < K) sm[warp * K + lane] = list;
+  __syncthreads();
+  if (warp == 0) {
+    uint64_t l2 = 0, t2 = 0;
+    for (int i = lane; i < WARPS * K; i += 32) offer(l2, t2, sm[i], lane);
+    if (nchunks == 1) {
+      if (lane < K) {
+        ids[row * K + lane] = key_id(l2);
+        vals[row * K + lane] = key_value(l2);
+      }
+    } else {
+      if (lane < K) __stcg(&part[(static_cast<size_t>(row) * nchunks + c) * K + lane], l2);
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) {
+        const int old = atomicAdd(&counters[row], 1);
+        last = (old == nchunks - 1);
+        if (last) counters[row] = 0;
+        __threadfence();
+      }
+      __syncwarp();
+      if (last) {
+        uint64_t l3 = 0, t3 = 0;
+        for (int i = lane; i < nchunks * K; i += 32) offer(l3, t3, __ldcg(&part[static_cast<size_t>(row) * nchunks * K + i]), lane);
+        if (lane < K) {
+          ids[row * K + lane] = key_id(l3);
+          vals[row * K + lane] = key_value(l3);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+int topk16(const Launch &lc, const float *logits, int rows, int V, int32_t *ids, float *vals, uint64_t *part_keys,
+           int *counters, int max_chunks) {
+  if (rows <= 0) return DFLASH_OK;
+  if (V < K) return set_error(DFLASH_ERR_SHAPE, "top-16 needs a vocabulary of at least 16");
+  // enough CTAs to cover the SMs twice, chunks of at least 4096 elements
+  int nch = (2 * lc.num_sms + rows - 1) / rows;
+  nch = nch > max_chunks ? max_chunks : nch;
+  const int maxc = (V + 4095) / 4096;
+  nch = nch > maxc ? maxc : nch;
+  nch = nch < 1 ? 1 : nch;
+  int chunk = (V + nch - 1) / nch;
+  chunk = (chunk + 127) & ~127;
+  nch = (V + chunk - 1) / chunk;
+  dim3 grid(nch, rows);
+  ProfScope ps(lc, "topk16", 4.0 * rows * V, 0.0);
+  topk_kernel<<<grid, WARPS * 32, 0, lc.stream>>>(logits, V, chunk, nch, ids, vals, part_keys, counters);
+  return cuda_check(cudaGetLastError(), "topk launch");
+}
+
+}  // namespace dflash

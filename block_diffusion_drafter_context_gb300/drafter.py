@@ -1,0 +1,199 @@
+"""Host-side convenience around the C ABI: weight upload/packing into the
+layouts include/dflash.h expects, the paged KV cache, the workspace, and a
+``Drafter`` object whose methods call the four entry points.
+
+Marshalling only: packing is concatenation / interleaving of weight rows; all
+drafting arithmetic happens in libdflash.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import binding as B
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def to_device(a, device="cuda"):
+    """numpy -> device tensor; uint16 arrays are bf16 bit patterns."""
+    torch = _torch()
+    if isinstance(a, torch.Tensor):
+        return a.to(device)
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    if a.dtype in (np.int32, np.int64):
+        return torch.from_numpy(a.astype(np.int32)).to(device)
+    return torch.from_numpy(a.astype(np.float32)).to(device)
+
+
+def make_config(cfg) -> B.dflash_config:
+    c = B.dflash_config()
+    c.dtype = B.DFLASH_F32 if cfg.dtype == "f32" else B.DFLASH_BF16
+    for k in ("hidden", "n_layers", "n_q_heads", "n_kv_heads", "head_dim", "ffn", "vocab",
+              "target_hidden", "n_target_layers", "sel_rank", "sel_dim", "page_size"):
+        setattr(c, k, int(getattr(cfg, k)))
+    c.block_size = int(cfg.block)
+    c.top_k = int(cfg.top_k)
+    c.use_conv = int(bool(cfg.use_conv))
+    c.use_selector = int(bool(cfg.use_selector))
+    c.qk_norm = int(bool(cfg.qk_norm))
+    c.fc_norm = int(bool(cfg.fc_norm))
+    c.mask_id = int(cfg.mask_id)
+    c.rope_base = float(cfg.rope_base)
+    c.eps = float(cfg.eps)
+    return c
+
+
+CONV_SITES = ("pre_attn", "post_attn", "pre_ffn", "post_ffn")
+
+
+def upload_weights(cfg, W: dict, device="cuda") -> dict:
+    """Upload a weight dict (layout of the synthetic generator) and pack it:
+    w_qkv = [w_q; w_k; w_v] rows; w_gu rows interleaved gate_i, up_i."""
+    torch = _torch()
+    d = lambda a: to_device(a, device)
+    out = {k: d(W[k]) for k in ("w_fc", "g_fc", "embed", "lm_head", "g_final")}
+    out["layers"] = []
+    for lw in W["layers"]:
+        gate, up = d(lw["w_gate"]), d(lw["w_up"])
+        L = {
+            "g_attn": d(lw["g_attn"]),
+            "w_qkv": torch.cat([d(lw["w_q"]), d(lw["w_k"]), d(lw["w_v"])], 0).contiguous(),
+            "g_q": d(lw["g_q"]), "g_k": d(lw["g_k"]), "w_o": d(lw["w_o"]), "g_ffn": d(lw["g_ffn"]),
+            "w_gu": torch.stack([gate, up], 1).reshape(2 * gate.shape[0], gate.shape[1]).contiguous(),
+            "w_down": d(lw["w_down"]),
+        }
+        del gate, up
+        if "conv" in lw:
+            L["w_conv"] = [d(lw["conv"][s][0]) for s in CONV_SITES]
+            L["b_conv"] = [d(lw["conv"][s][1]) for s in CONV_SITES]
+        out["layers"].append(L)
+    if "sel" in W:
+        s = W["sel"]
+        out["sel"] = {"e256": d(s["e256"]), "a": d(s["a"]), "b": d(s["b"]), "w_g": d(s["w_g"]),
+                      "b_g": float(s["b_g"])}
+    return out
+
+
+def make_weights_struct(dw: dict):
+    lay = (B.dflash_layer_weights * len(dw["layers"]))()
+    for i, L in enumerate(dw["layers"]):
+        s = lay[i]
+        for k in ("g_attn", "w_qkv", "g_q", "g_k", "w_o", "g_ffn", "w_gu", "w_down"):
+            setattr(s, k, L[k].data_ptr())
+        if "w_conv" in L:
+            for j in range(4):
+                s.w_conv[j] = L["w_conv"][j].data_ptr()
+                s.b_conv[j] = L["b_conv"][j].data_ptr()
+    w = B.dflash_weights()
+    for k in ("w_fc", "g_fc", "embed", "lm_head", "g_final"):
+        setattr(w, k, dw[k].data_ptr())
+    w.layers = lay
+    if "sel" in dw:
+        w.sel_e256 = dw["sel"]["e256"].data_ptr()
+        w.sel_a = dw["sel"]["a"].data_ptr()
+        w.sel_b = dw["sel"]["b"].data_ptr()
+        w.sel_w_g = dw["sel"]["w_g"].data_ptr()
+        w.sel_b_g = dw["sel"]["b_g"]
+    return w, lay
+
+
+class PagedKV:
+    """Device KV pools [L][num_pages][nkv][64][d] and the page table."""
+
+    def __init__(self, cfg, page_table: np.ndarray, num_pages: int, device="cuda", zero=True):
+        torch = _torch()
+        dt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+        shape = (cfg.n_layers, num_pages, cfg.n_kv_heads, cfg.page_size, cfg.head_dim)
+        alloc = torch.zeros if zero else torch.empty
+        self.k = alloc(shape, dtype=dt, device=device)
+        self.v = alloc(shape, dtype=dt, device=device)
+        self.page_table = to_device(np.ascontiguousarray(page_table, dtype=np.int32), device)
+        self.num_pages = int(num_pages)
+        self.max_pages = int(page_table.shape[1])
+        self.struct = B.dflash_kv(self.k.data_ptr(), self.v.data_ptr(), self.page_table.data_ptr(),
+                                  self.num_pages, self.max_pages)
+
+
+class Drafter:
+    """One drafter context: uploaded weights, a workspace, the C handle."""
+
+    def __init__(self, cfg, W: dict, max_batch: int, max_new_tokens: int, device="cuda", dev_weights=None):
+        torch = _torch()
+        self.cfg = cfg
+        self.dw = dev_weights if dev_weights is not None else upload_weights(cfg, W, device)
+        self.wstruct, self._lay = make_weights_struct(self.dw)
+        self.cstruct = make_config(cfg)
+        self.ctx = B.dflash_create(self.cstruct, self.wstruct)
+        self.ws_bytes = B.dflash_workspace_bytes(self.ctx, max_batch, max_new_tokens)
+        self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.max_batch, self.max_new_tokens = max_batch, max_new_tokens
+        self.device = device
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            B.dflash_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def act_dtype(self):
+        torch = _torch()
+        return torch.float32 if self.cfg.dtype == "f32" else torch.bfloat16
+
+    def status(self, stream=None) -> int:
+        return B.dflash_read_status(self.workspace, stream)
+
+    # ---- the four calls, allocating their outputs with torch
+    def inject_context(self, kv: PagedKV, target_hidden, cu_new, ctx_len_in, ctx_len_out=None, stream=None):
+        batch = int(cu_new.shape[0]) - 1
+        total = int(target_hidden.shape[0])
+        if ctx_len_out is None:
+            ctx_len_out = ctx_len_in
+        B.dflash_inject_context(self.ctx, kv.struct, target_hidden, cu_new, total, ctx_len_in, ctx_len_out,
+                                batch, self.workspace, self.ws_bytes, stream)
+        return ctx_len_out
+
+    def draft_block(self, kv: PagedKV, ctx_len, anchor_ids, want_logits=False, stream=None):
+        torch = _torch()
+        b = int(anchor_ids.shape[0])
+        dev = self.device
+        out = {
+            "topk_ids": torch.empty((b, 15, 16), dtype=torch.int32, device=dev),
+            "topk_logits": torch.empty((b, 15, 16), dtype=torch.float32, device=dev),
+            "final_hidden": torch.empty((b, 16, self.cfg.hidden), dtype=self.act_dtype, device=dev),
+            "logits": torch.empty((b, 15, self.cfg.vocab), dtype=torch.float32, device=dev) if want_logits else None,
+        }
+        B.dflash_draft_block(self.ctx, kv.struct, ctx_len, anchor_ids, b, out["topk_ids"], out["topk_logits"],
+                             out["final_hidden"], out["logits"], self.workspace, self.ws_bytes, stream)
+        return out
+
+    def select_path(self, anchor_ids, topk_ids, topk_logits, final_hidden, want_scores=True, stream=None):
+        torch = _torch()
+        b = int(topk_ids.shape[0])
+        draft = torch.empty((b, 15), dtype=torch.int32, device=self.device)
+        scores = (torch.empty((b, 15, 16, 16), dtype=torch.float32, device=self.device)
+                  if (want_scores and self.cfg.use_selector) else None)
+        B.dflash_select_path(self.ctx, anchor_ids, topk_ids, topk_logits, final_hidden, b, draft, scores,
+                             self.workspace, self.ws_bytes, stream)
+        return draft, scores
+
+    @staticmethod
+    def verify_greedy(draft_ids, target_ids, stream=None):
+        torch = _torch()
+        b = int(draft_ids.shape[0])
+        dev = draft_ids.device
+        acc = torch.empty(b, dtype=torch.int32, device=dev)
+        bonus = torch.empty(b, dtype=torch.int32, device=dev)
+        com = torch.empty((b, 16), dtype=torch.int32, device=dev)
+        B.dflash_verify_greedy(draft_ids, target_ids, b, acc, bonus, com, stream)
+        return acc, bonus, com

@@ -1,0 +1,254 @@
+/*
+ * dflash.h - C ABI of the GB300 (sm_103a) DFlash block-diffusion drafting
+ * library.  One call per step of the drafting hot path:
+ *
+ *   dflash_inject_context   target features -> every drafter layer's KV cache
+ *   dflash_draft_block      one parallel forward over a 16-token block
+ *   dflash_select_path      top-16 candidates -> one draft (DFlash-2 Path
+ *                           Selector, or top-1 per position)
+ *   dflash_verify_greedy    greedy prefix acceptance against target tokens
+ *
+ * Pages the operations are defined by (cited below by these tags):
+ *   [DF]  "DFlash - Difusion de Bloques para Decodificacion Especulativa en
+ *         Flash" (gist.science, paper 2602.06036)
+ *   [DF2] "DFlash 2: optimizacion de la decodificacion especulativa para
+ *         inferencia paralela de LLMs" (kerneldigest.dev)
+ *   [FD]  "FlexDraft" (gist.science, paper 2605.20022)
+ *   [BW]  "DFlash: Avance en la inferencia de LLM con decodificacion
+ *         especulativa en NVIDIA Blackwell" (emedoteme.es)
+ *
+ * General conventions
+ *   - Every pointer named "device" is CUDA device memory owned by the caller;
+ *     the library never allocates device memory and never frees caller memory.
+ *   - Every call is asynchronous on the given stream and never synchronises
+ *     (dflash_read_status and dflash_profile_end excepted).
+ *   - Return value: DFLASH_OK (0) or a negative DFLASH_ERR_* code; on error
+ *     nothing was launched and dflash_last_error() holds a message.
+ *   - Element type: dflash_config.dtype selects bf16 (DFLASH_BF16) or fp32
+ *     (DFLASH_F32) for every matrix, activation, KV cache and hidden state;
+ *     norm gains, biases and logits are always fp32; ids are int32.
+ *   - All matrices are row-major, W[out][in] (y = W x).  Every matrix base
+ *     pointer and every row stride must be 16-byte aligned.
+ *   - Workspace: one caller-owned device buffer of dflash_workspace_bytes()
+ *     bytes, zero-filled ONCE after allocation.  Calls sharing a workspace
+ *     must be ordered on one stream.  The first 256 bytes hold the device
+ *     status word (see dflash_read_status).
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DFLASH_API __attribute__((visibility("default")))
+#else
+#define DFLASH_API
+#endif
+
+typedef struct CUstream_st *dflash_stream_t;   /* == cudaStream_t */
+typedef struct dflash_ctx dflash_ctx;            /* opaque */
+
+enum {
+  DFLASH_OK = 0,
+  DFLASH_ERR_ARG = -1,          /* null pointer or out-of-range scalar       */
+  DFLASH_ERR_SHAPE = -2,        /* sizes inconsistent with the config        */
+  DFLASH_ERR_ALIGN = -3,        /* pointer / stride not 16-byte aligned      */
+  DFLASH_ERR_UNSUPPORTED = -4,  /* e.g. head_dim not 64/128, block != 16     */
+  DFLASH_ERR_CUDA = -5,         /* a CUDA runtime / driver call failed       */
+  DFLASH_ERR_TIMEOUT = -6,      /* a bounded device wait ran out             */
+  DFLASH_ERR_DEVICE = -7        /* a kernel reported bad data (page index)   */
+};
+
+enum { DFLASH_BF16 = 0, DFLASH_F32 = 1 };
+
+/* Drafter shape and flags.  block_size and top_k must be 16, page_size 64. */
+typedef struct dflash_config {
+  int dtype;             /* DFLASH_BF16 or DFLASH_F32                        */
+  int hidden;            /* H, multiple of 16                                */
+  int n_layers;          /* L                                                */
+  int n_q_heads;         /* nq                                               */
+  int n_kv_heads;        /* nkv, divides nq, nq/nkv <= 8                     */
+  int head_dim;          /* d: 128 (bf16) or 64/128 (fp32)                   */
+  int ffn;               /* F (SwiGLU width)                                 */
+  int vocab;             /* V                                                */
+  int target_hidden;     /* H_t                                              */
+  int n_target_layers;   /* n_sel; feature input width = n_sel * H_t         */
+  int block_size;        /* S = 16: anchor + 15 mask positions               */
+  int top_k;             /* 16                                               */
+  int use_conv;          /* DFlash-2 dynamic short convolution ([DF2] 2)     */
+  int use_selector;      /* DFlash-2 Path Selector ([DF2] 1)                 */
+  int qk_norm;           /* per-head RMSNorm of q and k                      */
+  int fc_norm;           /* RMSNorm after the context-feature projection     */
+  int sel_rank;          /* r of the bilinear form (<= 64)                   */
+  int sel_dim;           /* selector embedding width (256)                   */
+  int mask_id;           /* token id of the mask token                       */
+  int page_size;         /* KV page size in tokens: 64                       */
+  float rope_base;       /* RoPE base (1e6)                                  */
+  float eps;             /* RMSNorm epsilon (1e-6)                           */
+} dflash_config;
+
+/* Per-layer weights (device pointers, not owned). */
+typedef struct dflash_layer_weights {
+  const float *g_attn;   /* [H] pre-attention RMSNorm gain                   */
+  const void *w_qkv;     /* [(nq+2nkv)*d, H]: q heads, then k heads, then v  */
+  const float *g_q;      /* [d] per-head q RMSNorm gain                      */
+  const float *g_k;      /* [d] per-head k RMSNorm gain (also for injection) */
+  const void *w_o;       /* [H, nq*d]                                        */
+  const float *g_ffn;    /* [H] pre-FFN RMSNorm gain                         */
+  const void *w_gu;      /* [2F, H]: row 2i = gate_i, row 2i+1 = up_i        */
+  const void *w_down;    /* [H, F]                                           */
+  const void *w_conv[4]; /* [H/8, H] conv coefficient projections for the
+                            sites pre_attn, post_attn, pre_ffn, post_ffn;
+                            rows 0..H/16-1 = current tap, H/16.. = previous */
+  const float *b_conv[4];/* [H/8] their biases                               */
+} dflash_layer_weights;
+
+/* Model weights (device pointers, not owned; the layer array is host memory
+ * and is copied by dflash_create). */
+typedef struct dflash_weights {
+  const void *w_fc;      /* [H, n_sel*H_t] context-feature projection        */
+  const float *g_fc;     /* [H] its RMSNorm gain (fc_norm)                   */
+  const void *embed;     /* [V, H] token embedding shared with the target    */
+  const void *lm_head;   /* [V, H] LM head shared with the target            */
+  const float *g_final;  /* [H] final RMSNorm gain                           */
+  const dflash_layer_weights *layers;   /* host array [n_layers]            */
+  const void *sel_e256;  /* [V, sel_dim] selector token embeddings           */
+  const void *sel_a;     /* [r, sel_dim] projection of the previous token    */
+  const void *sel_b;     /* [r, sel_dim] projection of the current token     */
+  const float *sel_w_g;  /* [H] context-gate weights                         */
+  float sel_b_g;         /* context-gate bias                                */
+} dflash_weights;
+
+/* Paged drafter KV cache (device memory, not owned).
+ *   k_cache, v_cache: [L][num_pages][nkv][page_size][d] elements of dtype;
+ *   K is stored after the per-head k-norm and RoPE at its absolute position.
+ *   page_table: device int32 [batch][max_pages]; token position p of request
+ *   b lives in page page_table[b*max_pages + p/page_size], slot p%page_size.
+ *   Entries past a request's last used page are never read.  A page index
+ *   outside [0, num_pages) is skipped and reported as DFLASH_ERR_DEVICE. */
+typedef struct dflash_kv {
+  void *k_cache;
+  void *v_cache;
+  const int32_t *page_table;
+  int num_pages;
+  int max_pages;
+} dflash_kv;
+
+/* Per-kernel timing record returned by dflash_profile_end. */
+typedef struct dflash_kernel_stat {
+  char name[32];         /* kernel family                                    */
+  int launches;          /* launches recorded                                */
+  double ms;             /* summed CUDA-event durations                      */
+  double bytes;          /* summed algorithmic HBM bytes (compulsory traffic)*/
+  double flops;          /* summed algorithmic flops                         */
+} dflash_kernel_stat;
+
+/* Validate the config and weight pointers, record them (no copy of device
+ * data), query the device.  Host-only; allocates no device memory. */
+DFLASH_API int dflash_create(const dflash_config *cfg, const dflash_weights *w, dflash_ctx **out);
+DFLASH_API void dflash_destroy(dflash_ctx *ctx);
+
+/* Bytes of workspace needed for calls with at most max_batch requests and
+ * at most max_new_tokens tokens per dflash_inject_context call. */
+DFLASH_API size_t dflash_workspace_bytes(const dflash_ctx *ctx, int max_batch, int max_new_tokens);
+
+/* [DF] §2.2 (context-feature and KV-injection bullets; §3 item 2).
+ * The target's hidden states from a fixed set of layers, concatenated, are
+ * projected to the context feature f = RMSNorm(W_fc x); every drafter layer
+ * projects f with its own W_k, W_v; K gets the per-head k-norm and RoPE at
+ * its absolute position and both are written into that layer's pages.
+ *   target_hidden: device [total_new, n_sel*H_t] (dtype), rows grouped by
+ *                  request in order; concat order = ascending layer.
+ *   cu_new:        device int32 [batch+1] prefix sums of new tokens per
+ *                  request (cu_new[0] = 0, cu_new[batch] = total_new).
+ *   ctx_len_in:    device int32 [batch]: tokens already cached; request b's
+ *                  new tokens go to positions ctx_len_in[b] ...
+ *   ctx_len_out:   device int32 [batch]: receives ctx_len_in + new (may alias
+ *                  ctx_len_in).
+ *   The caller must have mapped pages for every written position. */
+DFLASH_API int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv,
+                          const void *target_hidden, const int32_t *cu_new, int total_new,
+                          const int32_t *ctx_len_in, int32_t *ctx_len_out, int batch,
+                          void *workspace, size_t workspace_bytes, dflash_stream_t stream);
+
+/* [DF] §2.2 (parallel block diffusion), §2.3 (anchor; shared embedding and
+ * LM head); mask semantics of [FD] Metodologia 1.  For each request b the
+ * block is [anchor_ids[b], mask x 15] at positions ctx_len[b] .. +15; one
+ * forward pass in which every block query attends to all ctx_len[b] cached
+ * tokens and to all 16 block tokens; the 15 mask positions' logits give the
+ * top-16 candidates (value desc, id asc).  The KV cache is only read.
+ *   ctx_len:      device int32 [batch], each <= max_pages*page_size.
+ *   anchor_ids:   device int32 [batch] in [0, V).
+ *   topk_ids:     device int32 [batch][15][16] out.
+ *   topk_logits:  device fp32 [batch][15][16] out (raw logits).
+ *   final_hidden: device [batch][16][H] (dtype) out, final-normed hidden
+ *                 (needed by dflash_select_path's gate); may be NULL.
+ *   logits:       device fp32 [batch][15][V] out; may be NULL (then kept in
+ *                 the workspace). */
+DFLASH_API int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv,
+                       const int32_t *ctx_len, const int32_t *anchor_ids, int batch,
+                       int32_t *topk_ids, float *topk_logits, void *final_hidden, float *logits,
+                       void *workspace, size_t workspace_bytes, dflash_stream_t stream);
+
+/* [DF2] Arquitectura 1 (Path Selector) with use_selector: pair scores
+ *   s[j][p][c] = z_j[c] + sigmoid(w_g.h_j + b_g) * (A e256[p]).(B e256[c])
+ * for j = 1..15, p over position j-1's candidates (the anchor for j = 1,
+ * repeated over the 16 rows), c over position j's; then the greedy path
+ * (ties to the lower token id).  Without use_selector: draft = top-1.
+ *   final_hidden: device [batch][16][H] from dflash_draft_block.
+ *   draft_ids:    device int32 [batch][15] out.
+ *   pair_scores:  device fp32 [batch][15][16][16] out, or NULL. */
+DFLASH_API int dflash_select_path(dflash_ctx *ctx, const int32_t *anchor_ids, const int32_t *topk_ids,
+                       const float *topk_logits, const void *final_hidden, int batch,
+                       int32_t *draft_ids, float *pair_scores,
+                       void *workspace, size_t workspace_bytes, dflash_stream_t stream);
+
+/* [DF2] Flujo de Inferencia 4-5, [BW] Contexto tecnico: k = length of the
+ * longest prefix with draft[i] == target[i] (0..15); bonus = target[k];
+ * committed = target[0..k] then -1.  Needs no context.
+ *   draft_ids: device int32 [batch][15]; target_ids: device int32 [batch][16]
+ *   accept_len, bonus: device int32 [batch]; committed: device int32 [batch][16]. */
+DFLASH_API int dflash_verify_greedy(const int32_t *draft_ids, const int32_t *target_ids, int batch,
+                         int32_t *accept_len, int32_t *bonus, int32_t *committed,
+                         dflash_stream_t stream);
+
+/* Synchronise `stream`, read the workspace's device status word into
+ * *device_status (0 = clean) and clear it.  Returns DFLASH_ERR_TIMEOUT or
+ * DFLASH_ERR_DEVICE when a kernel reported one, else DFLASH_OK. */
+DFLASH_API int dflash_read_status(const void *workspace, int *device_status, dflash_stream_t stream);
+
+/* Bound on every device-side wait, in nanoseconds (default 2e9). */
+DFLASH_API int dflash_set_wait_timeout(dflash_ctx *ctx, unsigned long long ns);
+
+/* Test hook: cap the CTA count of the persistent GEMM (0 = SM count). */
+DFLASH_API int dflash_set_gemm_ctas(dflash_ctx *ctx, int ctas);
+
+/* Test hook: force the split length of the block attention in tokens (a
+ * multiple of the page size; 0 = automatic). */
+DFLASH_API int dflash_set_attn_split(dflash_ctx *ctx, int tokens);
+
+/* Per-launch CUDA-event timing of every kernel the next calls launch (on
+ * their own streams), aggregated by kernel family.  profile_end
+ * synchronises the recorded events. */
+DFLASH_API int dflash_profile_begin(dflash_ctx *ctx);
+DFLASH_API int dflash_profile_end(dflash_ctx *ctx, dflash_kernel_stat *out, int max_out, int *n_out);
+
+/* Bounded-wait self test: one block spins on *flag (device int32) until it
+ * is non-zero or timeout_ns elapses; on timeout it writes
+ * DFLASH_ERR_TIMEOUT into the status word of `workspace`.  Used to check the
+ * timeout path without any fault. */
+DFLASH_API int dflash_debug_wait_flag(const int32_t *flag, unsigned long long timeout_ns,
+                           void *workspace, dflash_stream_t stream);
+
+/* Message for the last non-zero return on this thread. */
+DFLASH_API const char *dflash_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */
