@@ -1,0 +1,402 @@
+"""Benchmark of one DFlash drafting step on GB300.
+
+A step is the whole hot path for every request of the workload: inject the
+16 new tokens' target features into every drafter layer's paged KV cache,
+draft one 16-token block (one forward of the drafter), select the path, and
+verify greedily against synthetic target tokens.  Default workload: the
+Qwen3-8B-shaped drafter (5 layers, hidden 4096, vocab 151936), batch 1,
+2048 tokens of context (configs C2-C4 are parity cases, not bench lines).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle
+on the same workload instead (the deliberately slow reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synthetic import WORKLOADS, gen  # noqa: E402
+
+METRIC = "drafted blocks/sec (16-tok) at batch×ctx on 1 GB300; attention HBM GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def workload_desc(wl):
+    c = wl.cfg
+    return (f"{wl.name}: {c.name} drafter (L={c.n_layers}, H={c.hidden}, {c.n_q_heads}q/{c.n_kv_heads}kv x "
+            f"{c.head_dim}, F={c.ffn}, V={c.vocab}), batch {wl.batch}, context "
+            f"{wl.ctx_lo if wl.ctx_lo == wl.ctx_hi else f'U[{wl.ctx_lo},{wl.ctx_hi}]'}, "
+            f"{c.n_target_layers}x{c.target_hidden} target features, 16 new tokens injected per step")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling during the timed region (clocks + throttle reasons)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_setup(wl, W, ctx, X_prefill, cu):
+    import oracle as O
+    kvs = []
+    for b in range(wl.batch):
+        n = int(ctx[b])
+        kvs.append(O.inject_context(wl.cfg, W, X_prefill[cu[b]:cu[b + 1]], np.arange(n)))
+    return kvs
+
+
+def oracle_step(wl, W, kvs, ctx, Xn, anchor, target, requests):
+    import oracle as O
+    outs = []
+    for b in requests:
+        outs.append(O.drafting_step(wl.cfg, W, kvs[b], int(ctx[b]), Xn[16 * b:16 * (b + 1)], int(anchor[b]),
+                                    target[b]))
+    return outs
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- inputs
+def make_inputs(wl):
+    cfg = wl.cfg
+    W = gen.make_weights(cfg, wl.seed)
+    ctx = gen.context_lengths(wl)
+    B = len(ctx)
+    table, npages = gen.page_table(ctx + 16, cfg.page_size, wl.seed)
+    cu = np.concatenate([[0], np.cumsum(ctx)]).astype(np.int32)
+    Xp = gen.target_hidden(cfg, int(ctx.sum()), wl.seed, "prefill")
+    Xn = gen.target_hidden(cfg, 16 * B, wl.seed, "step")
+    anchor = gen.anchors(wl)
+    return W, ctx, table, npages, cu, Xp, Xn, anchor
+
+
+def run_reference(args, wl):
+    """The reference arm: the fp64 oracle on the host cores."""
+    W, ctx, table, npages, cu, Xp, Xn, anchor = make_inputs(wl)
+    t0 = time.time()
+    kvs = oracle_setup(wl, W, ctx, Xp, cu)
+    setup_s = time.time() - t0
+    import oracle as O
+    first = oracle_step(wl, W, kvs, ctx, Xn, anchor, np.zeros((wl.batch, 16), np.int32), range(wl.batch))
+    draft = np.stack([o["draft"] for o in first])
+    target = gen.target_ids(draft, wl.p_accept, wl.cfg.vocab, seed=wl.seed)
+    for _ in range(args.warmup):
+        oracle_step(wl, W, kvs, ctx, Xn, anchor, target, range(wl.batch))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(wl, W, kvs, ctx, Xn, anchor, target, range(wl.batch))
+    el = time.perf_counter() - t0
+    v = wl.batch * args.steps / el
+    cores = blas_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "blocks/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_desc(wl), "batch": wl.batch,
+                                            "ctx": int(ctx.max())},
+            "cpu_baseline": {"value": v, "unit": "blocks/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} full steps of all {wl.batch} request(s) after "
+                                       f"{args.warmup} warm-up; oracle KV prefill ({setup_s:.1f} s) untimed"},
+            "e2e": {"value": v, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+    from block_diffusion_drafter_context_gb300 import binding as Bd
+    from block_diffusion_drafter_context_gb300.build import build
+    from block_diffusion_drafter_context_gb300.drafter import Drafter, PagedKV, to_device
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        dist.barrier()
+    build()
+    cfg = wl.cfg
+    t_setup = time.time()
+    W, ctx, table, npages, cu, Xp, Xn, anchor = make_inputs(wl)
+    B = wl.batch
+    dr = Drafter(cfg, W, max_batch=B, max_new_tokens=max(16 * B, int(ctx.max())), device=dev)
+    kv = PagedKV(cfg, table, npages, device=dev)
+    stream = torch.cuda.current_stream()
+    # prefill: inject the whole context (chunked per request when large)
+    ctx0 = torch.zeros(B, dtype=torch.int32, device=dev)
+    ctx_n = torch.empty(B, dtype=torch.int32, device=dev)
+    for b in range(B):   # one request at a time through a view of its page-table row
+        one_cu = to_device(np.array([0, ctx[b]], np.int32), dev)
+        Bd.dflash_inject_context(dr.ctx, kv.row(b), to_device(Xp[cu[b]:cu[b + 1]], dev), one_cu,
+                                 int(ctx[b]), ctx0[:1], ctx_n[b:b + 1], 1, dr.workspace, dr.ws_bytes, stream)
+    torch.cuda.synchronize()
+    n_b = to_device(ctx.astype(np.int32), dev)
+    cu_new = to_device((16 * np.arange(B + 1)).astype(np.int32), dev)
+    Xn_d = to_device(Xn, dev)
+    anc_d = to_device(anchor, dev)
+    ctx_after = torch.empty(B, dtype=torch.int32, device=dev)
+    topk_ids = torch.empty((B, 15, 16), dtype=torch.int32, device=dev)
+    topk_logits = torch.empty((B, 15, 16), dtype=torch.float32, device=dev)
+    hfin = torch.empty((B, 16, cfg.hidden), dtype=dr.act_dtype, device=dev)
+    draft = torch.empty((B, 15), dtype=torch.int32, device=dev)
+    scores = torch.empty((B, 15, 16, 16), dtype=torch.float32, device=dev) if cfg.use_selector else None
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    bonus = torch.empty(B, dtype=torch.int32, device=dev)
+    com = torch.empty((B, 16), dtype=torch.int32, device=dev)
+    target_d = torch.zeros((B, 16), dtype=torch.int32, device=dev)
+
+    def step(x_in=Xn_d, a_in=anc_d, t_in=None):
+        t_in = target_d if t_in is None else t_in
+        Bd.dflash_inject_context(dr.ctx, kv.struct, x_in, cu_new, 16 * B, n_b, ctx_after, B, dr.workspace,
+                                 dr.ws_bytes, stream)
+        Bd.dflash_draft_block(dr.ctx, kv.struct, ctx_after, a_in, B, topk_ids, topk_logits, hfin, None,
+                              dr.workspace, dr.ws_bytes, stream)
+        Bd.dflash_select_path(dr.ctx, a_in, topk_ids, topk_logits, hfin, B, draft, scores, dr.workspace,
+                              dr.ws_bytes, stream)
+        Bd.dflash_verify_greedy(draft, t_in, B, acc, bonus, com, stream)
+
+    # synthetic target tokens from the step's own draft (identical every step)
+    step()
+    torch.cuda.synchronize()
+    tgt = gen.target_ids(draft.cpu().numpy(), wl.p_accept, cfg.vocab, seed=wl.seed)
+    target_d.copy_(torch.from_numpy(tgt))
+    setup_s = time.time() - t_setup
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert dr.status() == 0, "device status after warm-up"
+
+    def timed(fn, k):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+            dist.barrier()
+        return ms
+
+    with ClockSampler(local) as cs:
+        ms = timed(step, args.steps)
+    clocks = cs.summary()
+    assert dr.status() == 0, "device status after the timed region"
+
+    # ---- instrumented pass: per-launch CUDA events for the roofline
+    Bd.dflash_profile_begin(dr.ctx)
+    for _ in range(args.steps):
+        step()
+    stats = Bd.dflash_profile_end(dr.ctx)
+    launches = sum(s["launches"] for s in stats)
+
+    # ---- end to end through the public API with host buffers
+    pin_x = torch.from_numpy(Xn.view(np.int16) if Xn.dtype == np.uint16 else Xn).pin_memory()
+    pin_a = torch.from_numpy(anchor).pin_memory()
+    pin_t = torch.from_numpy(tgt).pin_memory()
+    out_acc = torch.empty(B, dtype=torch.int32).pin_memory()
+    out_bonus = torch.empty(B, dtype=torch.int32).pin_memory()
+    out_com = torch.empty((B, 16), dtype=torch.int32).pin_memory()
+    x_dev = torch.empty_like(Xn_d)
+    a_dev = torch.empty_like(anc_d)
+    t_dev = torch.empty_like(target_d)
+
+    def step_e2e():
+        x_dev.view(torch.int16 if Xn.dtype == np.uint16 else x_dev.dtype).copy_(pin_x, non_blocking=True)
+        a_dev.copy_(pin_a, non_blocking=True)
+        t_dev.copy_(pin_t, non_blocking=True)
+        step(x_dev, a_dev, t_dev)
+        out_acc.copy_(acc, non_blocking=True)
+        out_bonus.copy_(bonus, non_blocking=True)
+        out_com.copy_(com, non_blocking=True)
+        stream.synchronize()   # the host reads the step's result before the next step
+
+    for _ in range(2):
+        step_e2e()
+    ms_e2e = timed(step_e2e, args.steps)
+    h2d = pin_x.numel() * pin_x.element_size() + pin_a.numel() * 4 + pin_t.numel() * 4
+    d2h = (out_acc.numel() + out_bonus.numel() + out_com.numel()) * 4
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    pk, src = peaks()
+    hbm = float(pk["hbm_gbs"])
+    gemm = [s for s in stats if s["name"] in ("fc", "kv_inject", "qkv", "o_proj", "gate_up", "down", "lm_head",
+                                             "conv_coef")]
+    g_ms = sum(s["ms"] for s in gemm)
+    g_bytes = sum(s["bytes"] for s in gemm)
+    g_launch = sum(s["launches"] for s in gemm)
+    per_kernel = {s["name"]: {"launches": s["launches"], "ms_per_step": s["ms"] / args.steps,
+                              "gbs": (s["bytes"] / (s["ms"] * 1e-3) / 1e9) if s["bytes"] > 0 else None}
+                  for s in stats}
+    att = [s for s in stats if s["name"] == "attention"]
+    kv_bytes_step = float(sum(int(c) + 16 for c in ctx)) * cfg.n_layers * cfg.n_kv_heads * cfg.head_dim * 2 * 2
+    att_ms = sum(s["ms"] for s in att) / args.steps
+    att_gbs = kv_bytes_step / (att_ms * 1e-3) / 1e9 if att_ms > 0 else None
+    total_ms_inst = sum(s["ms"] for s in stats) / args.steps
+    step_ms = ms / args.steps
+    blocks = world * B * args.steps / (ms * 1e-3)
+    exp_k = 0.0
+    run_p = 1.0
+    for q in wl.p_accept:
+        run_p *= q
+        exp_k += run_p
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        try:
+            traffic = json.load(open(tfile)).get(wl.name, {}).get("gemm_bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only)
+    cpu = None
+    if world == 1 and not args.skip_cpu:
+        kvs = oracle_setup(wl, W, ctx, Xp, cu)
+        t0 = time.perf_counter()
+        oracle_step(wl, W, kvs, ctx, Xn, anchor, tgt, [0])
+        el = time.perf_counter() - t0
+        cpu = {"value": 1.0 / el, "unit": "blocks/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"one full drafting step (inject 16 tokens, forward, top-16, select, verify) of request "
+                         f"0 of {B}; {el:.1f} s of fp64 numpy on the host; oracle KV prefill untimed"}
+
+    line = {
+        "metric": METRIC, "value": blocks, "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(wl), "batch": B, "ctx": int(ctx.max()),
+                   "l2": "no flush: every step streams 3.4 GB of drafter weights, > 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "draft_tokens_per_s": 15 * blocks,
+        "expected_committed_tokens_per_s": (exp_k + 1) * blocks,
+        "roofline": {"kernel": "gemm_tc (all tcgen05 GEMM launches of a step)", "bound": "hbm",
+                     "achieved": g_bytes / (g_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                     "frac": g_bytes / (g_ms * 1e-3) / 1e9 / hbm, "peak_source": f"{src} hbm_gbs",
+                     "traffic": traffic, "algorithmic_bytes_per_launch": g_bytes / g_launch,
+                     "launches_per_step": g_launch / args.steps, "share_of_step": g_ms / (total_ms_inst * args.steps)},
+        "attention": {"kv_bytes_per_step": kv_bytes_step, "ms_per_step": att_ms, "gbs": att_gbs,
+                      "frac": (att_gbs / hbm) if att_gbs else None},
+        "per_kernel": per_kernel,
+        "instrumented_ms_per_step": total_ms_inst,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * B * args.steps / (ms_e2e * 1e-3), "unit": "blocks/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "setup_s": setup_s,
+    }
+    print(json.dumps(line), flush=True)
+    dr.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="C1")
+    ap.add_argument("--skip-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

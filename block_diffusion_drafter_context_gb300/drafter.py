@@ -118,6 +118,11 @@ class PagedKV:
         self.struct = B.dflash_kv(self.k.data_ptr(), self.v.data_ptr(), self.page_table.data_ptr(),
                                   self.num_pages, self.max_pages)
 
+    def row(self, b: int) -> B.dflash_kv:
+        """dflash_kv whose page table is request b's row alone (a batch of one)."""
+        r = self.page_table[b:b + 1]
+        return B.dflash_kv(self.k.data_ptr(), self.v.data_ptr(), r.data_ptr(), self.num_pages, self.max_pages)
+
 
 class Drafter:
     """One drafter context: uploaded weights, a workspace, the C handle."""

@@ -28,7 +28,7 @@ def to_np(t) -> np.ndarray:
 class Case:
     """A workload prefilled on the GPU through dflash_inject_context."""
 
-    def __init__(self, name: str, device: str = "cuda", gemm_ctas: int = 0):
+    def __init__(self, name: str, device: str = "cuda", gemm_ctas: int = 0, per_request: bool = False):
         import torch
         from block_diffusion_drafter_context_gb300 import binding as Bd
         from block_diffusion_drafter_context_gb300.drafter import Drafter, PagedKV, to_device
@@ -45,16 +45,26 @@ class Case:
         self.cu = np.concatenate([[0], np.cumsum(self.ctx)]).astype(np.int32)
         self.anchor = gen.anchors(wl)
         self.device = device
-        self.dr = Drafter(cfg, self.W, max_batch=self.B, max_new_tokens=max(16 * self.B, int(self.ctx.sum())),
+        self.per_request = per_request
+        self.dr = Drafter(cfg, self.W, max_batch=self.B,
+                          max_new_tokens=max(16 * self.B, int(self.ctx.max() if per_request else self.ctx.sum())),
                           device=device)
         if gemm_ctas:
             Bd.dflash_set_gemm_ctas(self.dr.ctx, gemm_ctas)
         self.kv = PagedKV(cfg, self.table, self.npages, device=device)
         self.ctx_d = torch.zeros(self.B, dtype=torch.int32, device=device)
-        if self.ctx.sum() > 0:
+        if per_request:
+            # one injection call per request, through a view of its page-table row
+            zero = torch.zeros(1, dtype=torch.int32, device=device)
+            for b in range(self.B):
+                if self.ctx[b] == 0:
+                    continue
+                cu1 = to_device(np.array([0, self.ctx[b]], np.int32), device)
+                Bd.dflash_inject_context(self.dr.ctx, self.kv.row(b), to_device(self.X[self.cu[b]:self.cu[b + 1]], device),
+                                         cu1, int(self.ctx[b]), zero, self.ctx_d[b:b + 1], 1, self.dr.workspace,
+                                         self.dr.ws_bytes, None)
+        elif self.ctx.sum() > 0:
             self.dr.inject_context(self.kv, to_device(self.X, device), to_device(self.cu, device), self.ctx_d)
-        else:
-            self.ctx_d.zero_()
         self.anchor_d = to_device(self.anchor, device)
         torch.cuda.synchronize()
 

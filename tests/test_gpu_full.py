@@ -1,0 +1,71 @@
+"""Parity at the full sizes of the Qwen3-8B-shaped workloads.
+
+C1 (batch 1, context 2048) is checked whole.  C2 (32 ragged requests,
+contexts 1k-8k) and C3 (DFlash-2, 8 requests x 4096) run whole on the GPU
+and are checked on sampled requests the oracle computes one by one (every
+request is independent of the others: the isolation invariant)."""
+import numpy as np
+import pytest
+
+import oracle as O
+from synthetic import gen
+from tests.gpu_case import TOL, Case, rel_err, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def check_requests(c, requests, kv_positions=64):
+    out = c.draft()
+    draft, scores = c.dr.select_path(c.anchor_d, out["topk_ids"], out["topk_logits"], out["final_hidden"])
+    assert c.dr.status() == 0
+    ids, vals = to_np(out["topk_ids"]), to_np(out["topk_logits"])
+    z, h, draft = to_np(out["logits"]), to_np(out["final_hidden"]), to_np(draft)
+    tol = TOL[c.cfg.dtype]
+    rng = np.random.default_rng(0)
+    for b in requests:
+        ref_kv = c.oracle_kv(b)
+        n = int(c.ctx[b])
+        pos = np.sort(rng.choice(n, size=min(kv_positions, n), replace=False))
+        for l in range(c.cfg.n_layers):
+            k, v = c.gpu_kv(b, l)
+            assert rel_err(k[pos], ref_kv[l][0][pos]) <= tol, (b, l)
+            assert rel_err(v[pos], ref_kv[l][1][pos]) <= tol, (b, l)
+        ref = c.oracle_draft(b)
+        assert rel_err(h[b], ref["h"]) <= tol, (b, "final hidden")
+        assert rel_err(z[b], ref["z"]) <= tol, (b, "logits")
+        oid, oval = O.top_k(z[b].astype(np.float64), 16)
+        assert (ids[b] == oid).all() and (vals[b] == oval).all(), b
+        if c.cfg.use_selector:
+            s_ref = O.pair_scores(c.cfg, c.W["sel"], int(c.anchor[b]), ids[b], vals[b], h[b])
+            assert rel_err(to_np(scores)[b], s_ref) <= 1e-4
+            path = O.greedy_path(s_ref, ids[b])
+            p = 0
+            for j in range(15):
+                row = np.sort(s_ref[j, p])[::-1]
+                if row[0] - row[1] < 1e-3:
+                    break
+                assert draft[b, j] == path[j], (b, j)
+                p = int(np.where(ids[b, j] == path[j])[0][0])
+        else:
+            assert (draft[b] == ids[b, :, 0]).all()
+    return out, draft
+
+
+def test_c1_full():
+    c = Case("C1")
+    check_requests(c, [0], kv_positions=2048)
+    c.dr.close()
+
+
+def test_c2_ragged_sampled():
+    c = Case("C2", per_request=True)
+    assert to_np(c.ctx_d).tolist() == c.ctx.tolist()
+    order = np.argsort(c.ctx)
+    check_requests(c, [int(order[0]), int(order[-1])])
+    c.dr.close()
+
+
+def test_c3_dflash2_sampled():
+    c = Case("C3", per_request=True)
+    check_requests(c, [0, c.B - 1])
+    c.dr.close()
