@@ -24,6 +24,7 @@ EXPORTS = (
     "dflash_draft_block", "dflash_select_path", "dflash_verify_greedy", "dflash_read_status",
     "dflash_set_wait_timeout", "dflash_set_gemm_ctas", "dflash_set_attn_split",
     "dflash_profile_begin", "dflash_profile_end", "dflash_debug_wait_flag", "dflash_last_error",
+    "dflash_topk16_noalloc",
 )
 
 
@@ -93,6 +94,7 @@ def load(path: str = LIB_PATH):
         "dflash_profile_end": (i, [vp, POINTER(dflash_kernel_stat), i, POINTER(c_int)]),
         "dflash_debug_wait_flag": (i, [vp, c_ulonglong, vp, vp]),
         "dflash_last_error": (ctypes.c_char_p, []),
+        "dflash_topk16_noalloc": (i, [vp, i, i, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -198,6 +200,12 @@ def dflash_profile_end(ctx) -> list:
 
 def dflash_debug_wait_flag(flag, timeout_ns: int, workspace, stream=None):
     return _check(load().dflash_debug_wait_flag(_p(flag), timeout_ns, _p(workspace), _stream(stream)))
+
+
+def dflash_topk16_noalloc(logits, rows, vocab, topk_ids, topk_logits, stream=None):
+    """Top-16 per row with the library's fixed scratch array (no device allocation)."""
+    return _check(load().dflash_topk16_noalloc(_p(logits), rows, vocab, _p(topk_ids), _p(topk_logits),
+                                               _stream(stream)))
 
 
 def dflash_last_error() -> str:

@@ -15,6 +15,8 @@
 #include "common.cuh"
 #include "internal.h"
 
+#include <mutex>
+
 namespace dflash {
 namespace {
 
@@ -135,4 +137,76 @@ int topk16(const Launch &lc, const float *logits, int rows, int V, int32_t *ids,
   return cuda_check(cudaGetLastError(), "topk launch");
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free top-16 (dflash_topk16_noalloc).
+//
+// Some callers cannot allocate device memory at all: inference-engine plugin
+// hooks that receive only their input and output buffers and run under a
+// device-memory budget the engine planned in advance, where a cudaMalloc
+// could fail or stall the device.  For them this entry point keeps the
+// selection's scratch (per-chunk partial top-16 keys and per-row completion
+// counters) in one fixed array inside the library instead of a caller
+// workspace.  Limits: at most NOALLOC_MAX_ROWS rows and NOALLOC_MAX_CHUNKS
+// chunks per row (4 MB + 4 KB held on every GPU that loads the library, until
+// the process exits).  All calls share the array: calls that overlap on the
+// GPU (different streams, no ordering between them) race on it.
+namespace {
+
+constexpr int NOALLOC_MAX_ROWS = 1024;
+constexpr int NOALLOC_MAX_CHUNKS = 32;
+constexpr size_t NOALLOC_CTR_BYTES = sizeof(int) * NOALLOC_MAX_ROWS;
+constexpr size_t NOALLOC_KEY_BYTES = sizeof(uint64_t) * NOALLOC_MAX_ROWS * NOALLOC_MAX_CHUNKS * 16;
+
+static __device__ __align__(256) unsigned char g_topk_scratch[NOALLOC_CTR_BYTES + NOALLOC_KEY_BYTES];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+void *g_scratch_addr[NOALLOC_MAX_DEVICES] = {};
+std::mutex g_scratch_mu;
+
+// Device address of the scratch array on the current device.  The array's
+// name is only a host-side stand-in; its device address is looked up once
+// per device, with that device current, and cached.
+int scratch_address(void **out) {
+  int dev = -1;
+  if (int e = cuda_check(cudaGetDevice(&dev), "noalloc top-16: cudaGetDevice")) return e;
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "noalloc top-16: device ordinal %d beyond %d", dev, NOALLOC_MAX_DEVICES);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void *p = nullptr;
+    if (int e = cuda_check(cudaGetSymbolAddress(&p, g_topk_scratch), "noalloc top-16: cudaGetSymbolAddress"))
+      return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return DFLASH_OK;
+}
+
+}  // namespace
 }  // namespace dflash
+
+extern "C" DFLASH_API int dflash_topk16_noalloc(const float *logits, int rows, int vocab, int32_t *topk_ids, float *topk_logits,
+                                     dflash_stream_t stream) {
+  using namespace dflash;
+  if (rows < 0 || vocab < 0) return set_error(DFLASH_ERR_ARG, "noalloc top-16: negative size");
+  if (rows == 0) return DFLASH_OK;
+  if (!logits || !topk_ids || !topk_logits) return set_error(DFLASH_ERR_ARG, "noalloc top-16: null pointer");
+  if (rows > NOALLOC_MAX_ROWS)
+    return set_error(DFLASH_ERR_SHAPE, "noalloc top-16: %d rows exceed the fixed scratch limit of %d rows", rows,
+                     NOALLOC_MAX_ROWS);
+  void *base = nullptr;
+  if (int e = scratch_address(&base)) return e;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the completion counters must start at zero; the array keeps whatever the
+  // previous call left, so clear them on the stream first
+  if (int e = cuda_check(cudaMemsetAsync(base, 0, sizeof(int) * rows, s), "noalloc top-16: clear counters"))
+    return e;
+  Launch lc;
+  lc.stream = s;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) lc.num_sms = sms;
+  return topk16(lc, logits, rows, vocab, topk_ids, topk_logits,
+                reinterpret_cast<uint64_t *>(static_cast<char *>(base) + NOALLOC_CTR_BYTES), static_cast<int *>(base),
+                NOALLOC_MAX_CHUNKS);
+}

@@ -245,6 +245,25 @@ DFLASH_API int dflash_profile_end(dflash_ctx *ctx, dflash_kernel_stat *out, int 
 DFLASH_API int dflash_debug_wait_flag(const int32_t *flag, unsigned long long timeout_ns,
                            void *workspace, dflash_stream_t stream);
 
+/* Allocation-free top-16, for callers that cannot allocate device memory:
+ * e.g. engine plugin hooks that are handed only their input and output
+ * buffers and must stay inside a device-memory budget planned in advance,
+ * where a cudaMalloc could fail or stall the device.  It computes what the
+ * top-16 stage of dflash_draft_block computes (per row of fp32 logits: the
+ * 16 largest values, ties to the lower id, sorted) but keeps its scratch in
+ * a fixed array inside the library (4 MB + 4 KB per GPU that loads it, held
+ * until the process exits) instead of a caller workspace.  No counterpart in
+ * the paper: it is an interface convenience, not part of the method.
+ *   logits:      device fp32 [rows][vocab];
+ *   topk_ids:    device int32 [rows][16] out; topk_logits: device fp32 [rows][16] out.
+ *   rows <= 1024, else DFLASH_ERR_SHAPE (nothing launched).
+ * Allocates nothing (no cudaMalloc / cudaFree).  The first call on each
+ * device looks up the array's device address; make that first call before
+ * any stream capture.  All calls share the array and clear its counters at
+ * the start of each call: calls that overlap on the GPU race. */
+DFLASH_API int dflash_topk16_noalloc(const float *logits, int rows, int vocab, int32_t *topk_ids,
+                                     float *topk_logits, dflash_stream_t stream);
+
 /* Message for the last non-zero return on this thread. */
 DFLASH_API const char *dflash_last_error(void);
 

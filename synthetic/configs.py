@@ -124,6 +124,8 @@ WORKLOADS = {
                      batch=2, ctx_lo=0, ctx_hi=0, explicit_ctx=(64, 37), seed=10),
     "T1": Workload("T1", SMALL_BF16, batch=3, ctx_lo=0, ctx_hi=0,
                    explicit_ctx=(0, 100, 777), p_accept=_decay(0.9, 0.5), seed=11),
+    "T1V": Workload("T1V", replace(SMALL_BF16, name="small-bf16-v40000", vocab=40000),
+                    batch=3, ctx_lo=0, ctx_hi=0, explicit_ctx=(7, 64, 129), seed=13),
     "T1D2": Workload("T1D2", replace(SMALL_BF16, name="small-bf16-dflash2",
                                      use_conv=True, use_selector=True),
                      batch=3, ctx_lo=0, ctx_hi=0, explicit_ctx=(5, 64, 300), seed=12),
