@@ -32,7 +32,7 @@ class dflash_config(ctypes.Structure):
     _fields_ = [(n, c_int) for n in (
         "dtype", "hidden", "n_layers", "n_q_heads", "n_kv_heads", "head_dim", "ffn", "vocab",
         "target_hidden", "n_target_layers", "block_size", "top_k", "use_conv", "use_selector",
-        "qk_norm", "fc_norm", "sel_rank", "sel_dim", "mask_id", "page_size")] + [
+        "qk_norm", "fc_norm", "split_act", "sel_rank", "sel_dim", "mask_id", "page_size")] + [
         ("rope_base", c_float), ("eps", c_float)]
 
 

@@ -121,7 +121,8 @@ constexpr int TOPK_MAX_CHUNKS = 64;
 struct Layout {
   size_t status, gemm_ctr, gemm_part, attn_ctr, attn_o, attn_ml, topk_ctr, topk_part;
   size_t x, u, u2, qkv, q, bk, bv, o, ysub, coef, hmid, hmask, hfinal, logits, scores;
-  size_t fc, f, kvproj, ctx_saved;
+  size_t u_lo, u2_lo, o_lo, ysub_lo, hmid_lo, hmask_lo, ysub32;
+  size_t fc, f, f_lo, kvproj, ctx_saved;
   size_t total;
   size_t gemm_part_floats;
 };
@@ -159,11 +160,21 @@ Layout layout(const dflash_ctx *c, int B, int Tn) {
   L.coef = take(4 * R * (H / 8));
   L.hmid = take(te * R * F);
   L.hmask = take(te * B * 15 * H);
+  // low halves of the GEMM activations (split activations, bf16 path)
+  const size_t tl = (g.dtype == DFLASH_F32 || !g.split_act) ? 0 : 2;
+  L.u_lo = take(tl * R * H);
+  L.u2_lo = take(tl * R * H);
+  L.o_lo = take(tl * R * nq * d);
+  L.ysub_lo = take(tl * R * H);
+  L.hmid_lo = take(tl * R * F);
+  L.hmask_lo = take(tl * B * 15 * H);
+  L.ysub32 = take(4 * R * H);
   L.hfinal = take(te * R * H);
   L.logits = take(4ull * B * 15 * V);
   L.scores = take(4ull * B * 15 * 256);
   L.fc = take(4ull * Tn * H);
   L.f = take(te * Tn * H);
+  L.f_lo = take(tl * Tn * H);
   L.kvproj = take(4ull * g.n_layers * Tn * 2 * nkv * d);
   L.ctx_saved = take(sizeof(int) * static_cast<size_t>(B));
   L.total = off;
@@ -190,17 +201,32 @@ Launch make_launch(dflash_ctx *c, void *ws, cudaStream_t s) {
 
 // One projection of the drafter on the path's GEMM (tcgen05 for bf16, CUDA
 // cores for fp32).
-int proj(dflash_ctx *c, const Launch &lc, void *ws, const Layout &L, const void *W, int ldw, const void *X, int ldx,
-         int M, int N, int K, int epi, void *out, int ldo, const float *bias, const char *name) {
-  if (c->cfg.dtype == DFLASH_F32)
-    return gemm_f32(lc, static_cast<const float *>(W), ldw, static_cast<const float *>(X), ldx, M, N, K,
-                    epi == EPI_STORE_T ? EPI_F32 : epi, out, ldo, bias, name);
+int proj(dflash_ctx *c, const Launch &lc, void *ws, const Layout &L, const GemmOp &op) {
+  if (c->cfg.dtype == DFLASH_F32) return gemm_f32(lc, op);
   GemmScratch sc;
   sc.partials = at<float>(ws, L.gemm_part);
   sc.partial_floats = L.gemm_part_floats;
   sc.counters = at<int>(ws, L.gemm_ctr);
   sc.n_counters = GEMM_COUNTERS;
-  return gemm_bf16(lc, W, ldw, X, ldx, M, N, K, epi, out, ldo, bias, sc, name);
+  return gemm_bf16(lc, op, sc);
+}
+
+GemmOp mk(const void *W, int ldw, const void *X, const void *X_lo, int ldx, int M, int N, int K, int epi, void *out,
+          int ldo, const char *name) {
+  GemmOp o;
+  o.W = W;
+  o.ldw = ldw;
+  o.X = X;
+  o.X_lo = X_lo;
+  o.ldx = ldx;
+  o.M = M;
+  o.N = N;
+  o.K = K;
+  o.epi = epi;
+  o.out = out;
+  o.ldo = ldo;
+  o.name = name;
+  return o;
 }
 
 int check_ws(const dflash_ctx *c, void *ws, size_t bytes, int B, int Tn) {
@@ -328,12 +354,15 @@ int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv, const void *targ
   Launch lc = make_launch(ctx, workspace, reinterpret_cast<cudaStream_t>(stream));
   const int H = g.hidden, d = g.head_dim, nq = g.n_q_heads, nkv = g.n_kv_heads, K = g.n_target_layers * g.target_hidden;
   const size_t te = f32 ? 4 : 2;
+  const bool split = !f32 && g.split_act;
+  void *f_lo = split ? at<void>(workspace, L.f_lo) : nullptr;
   // context feature: fc projection, then RMSNorm
-  if (int e = proj(ctx, lc, workspace, L, ctx->w.w_fc, K, target_hidden, K, total_new, H, K, EPI_F32,
-                   at<float>(workspace, L.fc), H, nullptr, "fc"))
+  if (int e = proj(ctx, lc, workspace, L,
+                   mk(ctx->w.w_fc, K, target_hidden, nullptr, K, total_new, H, K, EPI_F32, at<float>(workspace, L.fc),
+                      H, "fc")))
     return e;
   if (int e = feature_norm(lc, f32, at<float>(workspace, L.fc), total_new, H, ctx->w.g_fc, g.eps, g.fc_norm != 0,
-                           at<void>(workspace, L.f), ctx_len_in, at<int32_t>(workspace, L.ctx_saved), batch))
+                           at<void>(workspace, L.f), f_lo, ctx_len_in, at<int32_t>(workspace, L.ctx_saved), batch))
     return e;
   // every layer's own K/V projection of the feature (rows nq*d.. of w_qkv)
   std::vector<const float *> gk(g.n_layers);
@@ -341,8 +370,9 @@ int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv, const void *targ
     const dflash_layer_weights &lw = ctx->layers[l];
     const void *wkv = static_cast<const char *>(lw.w_qkv) + te * static_cast<size_t>(nq) * d * H;
     float *dst = at<float>(workspace, L.kvproj) + static_cast<size_t>(l) * total_new * 2 * nkv * d;
-    if (int e = proj(ctx, lc, workspace, L, wkv, H, at<void>(workspace, L.f), H, total_new, 2 * nkv * d, H, EPI_F32,
-                     dst, 2 * nkv * d, nullptr, "kv_inject"))
+    if (int e = proj(ctx, lc, workspace, L,
+                     mk(wkv, H, at<void>(workspace, L.f), f_lo, H, total_new, 2 * nkv * d, H, EPI_F32, dst, 2 * nkv * d,
+                        "kv_inject")))
       return e;
     gk[l] = lw.g_k;
   }
@@ -378,40 +408,65 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
   // split-KV plan: enough CTAs to cover the SMs twice, at most ATTN_SLOTS
   // partial slots, splits of at most 4096 tokens when that fits
   const int max_ctx = kv->max_pages * g.page_size;
-  int split = ctx->attn_split;
-  if (split <= 0) {
+  int split_tok = ctx->attn_split;
+  if (split_tok <= 0) {
     const int bh = B * nkv;
-    int want = (2 * ctx->num_sms + bh - 1) / bh;
-    split = (max_ctx + want - 1) / want;
-    split = split < 128 ? 128 : split;
-    split = split > 4096 ? 4096 : split;
-    split = (split + 63) / 64 * 64;
+    int want = (ctx->num_sms + bh - 1) / bh;
+    split_tok = (max_ctx + want - 1) / want;
+    split_tok = split_tok < 256 ? 256 : split_tok;
+    split_tok = split_tok > 4096 ? 4096 : split_tok;
+    split_tok = (split_tok + 63) / 64 * 64;
   }
-  int max_splits = (max_ctx + split - 1) / split;
+  int max_splits = (max_ctx + split_tok - 1) / split_tok;
   if (max_splits < 1) max_splits = 1;
   if (static_cast<long long>(max_splits) * B * nkv > ATTN_SLOTS) {
     max_splits = ATTN_SLOTS / (B * nkv);
     if (max_splits < 1) max_splits = 1;
-    split = ((max_ctx + max_splits - 1) / max_splits + 63) / 64 * 64;
-    max_splits = (max_ctx + split - 1) / split;
+    split_tok = ((max_ctx + max_splits - 1) / max_splits + 63) / 64 * 64;
+    max_splits = (max_ctx + split_tok - 1) / split_tok;
   }
 
-  if (int e = embed_rmsnorm(lc, f32, ctx->w.embed, anchor_ids, g.mask_id, V, ctx->layers[0].g_attn, g.eps, B, H, x, u))
+  const bool split = !f32 && g.split_act;
+  auto lo = [&](size_t off) -> void * { return split ? at<void>(ws, off) : nullptr; };
+  void *u_lo = lo(L.u_lo), *u2_lo = lo(L.u2_lo), *ysub_lo = lo(L.ysub_lo), *hmid_lo = lo(L.hmid_lo);
+  float *ysub32 = at<float>(ws, L.ysub32);
+
+  if (int e = embed_rmsnorm(lc, f32, ctx->w.embed, anchor_ids, g.mask_id, V, ctx->layers[0].g_attn, g.eps, B, H, x, u,
+                            u_lo))
     return e;
   const size_t lelems = layer_elems(ctx, kv);
   const size_t te = f32 ? 4 : 2;
+  // conv coefficients of one site: tanh(W_c y + b_c), fp32 [R][H/8]
+  auto coef_gemm = [&](int site, const dflash_layer_weights &lw, const void *y, const void *y_lo) {
+    GemmOp op = mk(lw.w_conv[site], H, y, y_lo, H, R, G8, H, EPI_TANH_BIAS, coef, G8, "conv_coef");
+    op.bias = lw.b_conv[site];
+    return proj(ctx, lc, ws, L, op);
+  };
+  // a sublayer's output projection: straight into the fp32 residual, or (conv)
+  // into fp32 + bf16 halves, then the post-site conv adds it to the residual
+  auto out_proj = [&](int site, const dflash_layer_weights &lw, const void *Wm, int K, const void *X, const void *X_lo,
+                      const char *name) -> int {
+    if (!g.use_conv) return proj(ctx, lc, ws, L, mk(Wm, K, X, X_lo, K, R, H, K, EPI_ADD_F32, x, H, name));
+    GemmOp op = mk(Wm, K, X, X_lo, K, R, H, K, f32 ? EPI_F32 : EPI_F32_SPLIT, ysub32, H, name);
+    op.out2 = ysub;
+    op.out2_lo = ysub_lo;
+    op.ldo2 = H;
+    if (int e = proj(ctx, lc, ws, L, op)) return e;
+    if (int e = coef_gemm(site, lw, f32 ? static_cast<const void *>(ysub32) : ysub, ysub_lo)) return e;
+    return conv_apply(lc, f32, nullptr, nullptr, ysub32, coef, B, H, nullptr, nullptr, x);
+  };
   for (int l = 0; l < g.n_layers; ++l) {
     const dflash_layer_weights &lw = ctx->layers[l];
-    const void *ua = u;
+    const void *ua = u, *ua_lo = u_lo;
     // ---- attention sublayer
     if (g.use_conv) {
-      if (int e = proj(ctx, lc, ws, L, lw.w_conv[0], H, u, H, R, G8, H, EPI_TANH_BIAS, coef, G8, lw.b_conv[0], "conv_coef"))
-        return e;
-      if (int e = conv_apply(lc, f32, u, coef, B, H, u2, nullptr)) return e;
+      if (int e = coef_gemm(0, lw, u, u_lo)) return e;
+      if (int e = conv_apply(lc, f32, u, u_lo, nullptr, coef, B, H, u2, u2_lo, nullptr)) return e;
       ua = u2;
+      ua_lo = u2_lo;
     }
-    if (int e = proj(ctx, lc, ws, L, lw.w_qkv, H, ua, H, R, nh * d, H, EPI_F32, at<float>(ws, L.qkv), nh * d, nullptr,
-                     "qkv"))
+    if (int e = proj(ctx, lc, ws, L, mk(lw.w_qkv, H, ua, ua_lo, H, R, nh * d, H, EPI_F32, at<float>(ws, L.qkv), nh * d,
+                                        "qkv")))
       return e;
     if (int e = qk_norm_rope(lc, f32, at<float>(ws, L.qkv), B, nq, nkv, d, lw.g_q, lw.g_k, g.qk_norm != 0, g.eps,
                              g.rope_base, ctx_len, at<void>(ws, L.q), at<void>(ws, L.bk), at<void>(ws, L.bv)))
@@ -428,6 +483,7 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     aa.page_size = g.page_size;
     aa.ctx_len = ctx_len;
     aa.out = at<void>(ws, L.o);
+    aa.out_lo = lo(L.o_lo);
     aa.part_o = at<float>(ws, L.attn_o);
     aa.part_ml = at<float>(ws, L.attn_ml);
     aa.counters = at<int>(ws, L.attn_ctr);
@@ -435,49 +491,35 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     aa.nq = nq;
     aa.nkv = nkv;
     aa.d = d;
-    aa.split_tokens = split;
+    aa.split_tokens = split_tok;
     aa.max_splits = max_splits;
     if (int e = f32 ? attention_f32(lc, aa) : attention_bf16(lc, aa)) return e;
-    if (g.use_conv) {
-      if (int e = proj(ctx, lc, ws, L, lw.w_o, nq * d, aa.out, nq * d, R, H, nq * d, EPI_STORE_T, ysub, H, nullptr, "o_proj"))
-        return e;
-      if (int e = proj(ctx, lc, ws, L, lw.w_conv[1], H, ysub, H, R, G8, H, EPI_TANH_BIAS, coef, G8, lw.b_conv[1], "conv_coef"))
-        return e;
-      if (int e = conv_apply(lc, f32, ysub, coef, B, H, nullptr, x)) return e;
-    } else {
-      if (int e = proj(ctx, lc, ws, L, lw.w_o, nq * d, aa.out, nq * d, R, H, nq * d, EPI_ADD_F32, x, H, nullptr, "o_proj"))
-        return e;
-    }
+    if (int e = out_proj(1, lw, lw.w_o, nq * d, aa.out, aa.out_lo, "o_proj")) return e;
     // ---- FFN sublayer
-    if (int e = rmsnorm_rows(lc, f32, x, R, H, lw.g_ffn, g.eps, u, nullptr)) return e;
+    if (int e = rmsnorm_rows(lc, f32, x, R, H, lw.g_ffn, g.eps, u, u_lo, nullptr, nullptr)) return e;
     ua = u;
+    ua_lo = u_lo;
     if (g.use_conv) {
-      if (int e = proj(ctx, lc, ws, L, lw.w_conv[2], H, u, H, R, G8, H, EPI_TANH_BIAS, coef, G8, lw.b_conv[2], "conv_coef"))
-        return e;
-      if (int e = conv_apply(lc, f32, u, coef, B, H, u2, nullptr)) return e;
+      if (int e = coef_gemm(2, lw, u, u_lo)) return e;
+      if (int e = conv_apply(lc, f32, u, u_lo, nullptr, coef, B, H, u2, u2_lo, nullptr)) return e;
       ua = u2;
+      ua_lo = u2_lo;
     }
-    if (int e = proj(ctx, lc, ws, L, lw.w_gu, H, ua, H, R, 2 * F, H, EPI_SWIGLU, at<void>(ws, L.hmid), F, nullptr,
-                     "gate_up"))
-      return e;
-    if (g.use_conv) {
-      if (int e = proj(ctx, lc, ws, L, lw.w_down, F, at<void>(ws, L.hmid), F, R, H, F, EPI_STORE_T, ysub, H, nullptr,
-                       "down"))
-        return e;
-      if (int e = proj(ctx, lc, ws, L, lw.w_conv[3], H, ysub, H, R, G8, H, EPI_TANH_BIAS, coef, G8, lw.b_conv[3], "conv_coef"))
-        return e;
-      if (int e = conv_apply(lc, f32, ysub, coef, B, H, nullptr, x)) return e;
-    } else {
-      if (int e = proj(ctx, lc, ws, L, lw.w_down, F, at<void>(ws, L.hmid), F, R, H, F, EPI_ADD_F32, x, H, nullptr,
-                       "down"))
-        return e;
+    {
+      GemmOp op = mk(lw.w_gu, H, ua, ua_lo, H, R, 2 * F, H, EPI_SWIGLU, at<void>(ws, L.hmid), F, "gate_up");
+      op.out_lo = hmid_lo;
+      if (int e = proj(ctx, lc, ws, L, op)) return e;
     }
+    if (int e = out_proj(3, lw, lw.w_down, F, at<void>(ws, L.hmid), hmid_lo, "down")) return e;
     if (l + 1 < g.n_layers)
-      if (int e = rmsnorm_rows(lc, f32, x, R, H, ctx->layers[l + 1].g_attn, g.eps, u, nullptr)) return e;
+      if (int e = rmsnorm_rows(lc, f32, x, R, H, ctx->layers[l + 1].g_attn, g.eps, u, u_lo, nullptr, nullptr)) return e;
   }
-  if (int e = rmsnorm_rows(lc, f32, x, R, H, ctx->w.g_final, g.eps, hfinal, at<void>(ws, L.hmask))) return e;
-  if (int e = proj(ctx, lc, ws, L, ctx->w.lm_head, H, at<void>(ws, L.hmask), H, B * 15, V, H, EPI_F32, lg, V, nullptr,
-                   "lm_head"))
+  if (int e = rmsnorm_rows(lc, f32, x, R, H, ctx->w.g_final, g.eps, hfinal, nullptr, at<void>(ws, L.hmask),
+                           lo(L.hmask_lo)))
+    return e;
+  if (int e = proj(ctx, lc, ws, L,
+                   mk(ctx->w.lm_head, H, at<void>(ws, L.hmask), lo(L.hmask_lo), H, B * 15, V, H, EPI_F32, lg, V,
+                      "lm_head")))
     return e;
   return topk16(lc, lg, B * 15, V, topk_ids, topk_logits, at<uint64_t>(ws, L.topk_part), at<int>(ws, L.topk_ctr),
                 TOPK_MAX_CHUNKS);

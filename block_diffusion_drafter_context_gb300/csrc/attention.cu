@@ -36,6 +36,7 @@ struct Params {
   const __nv_bfloat16 *q;
   int ldq;
   __nv_bfloat16 *out;
+  __nv_bfloat16 *out_lo;   // low halves (split activations) or null
   int ldo;
   const int32_t *page_table;
   int max_pages, num_pages;
@@ -50,6 +51,13 @@ struct Params {
 
 __device__ __forceinline__ uint32_t swz(uint32_t base, int tok, int dch) {
   return base + (dch >> 3) * HALF + tok * 128 + ((((dch & 7) ^ (tok & 7))) << 4);
+}
+
+// two consecutive bf16 outputs (high halves) and, if lo is given, their low halves
+__device__ __forceinline__ void store2_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t i, float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  *reinterpret_cast<__nv_bfloat162 *>(hi + i) = h;
+  if (lo) *reinterpret_cast<uint32_t *>(lo + i) = pack_bf16(a - __low2float(h), b - __high2float(h));
 }
 
 __device__ __forceinline__ uint32_t mask_pair(uint32_t v, int tok, int valid) {
@@ -283,13 +291,13 @@ __global__ void __launch_bounds__(32 * 9, 1)
   }
 
   if (nsplit == 1) {
-    __nv_bfloat16 *r0 = p.out + static_cast<size_t>(b * BLK + gr) * p.ldo + hq * HD;
-    __nv_bfloat16 *r1 = r0 + 8 * static_cast<size_t>(p.ldo);
+    const size_t o0 = static_cast<size_t>(b * BLK + gr) * p.ldo + hq * HD;
+    const size_t o1 = o0 + 8 * static_cast<size_t>(p.ldo);
     const float i0 = 1.f / l0, i1 = 1.f / l1;
 #pragma unroll
     for (int nd = 0; nd < 16; ++nd) {
-      *reinterpret_cast<uint32_t *>(r0 + nd * 8 + t2) = pack_bf16(o[nd][0] * i0, o[nd][1] * i0);
-      *reinterpret_cast<uint32_t *>(r1 + nd * 8 + t2) = pack_bf16(o[nd][2] * i1, o[nd][3] * i1);
+      store2_hl(p.out, p.out_lo, o0 + nd * 8 + t2, o[nd][0] * i0, o[nd][1] * i0);
+      store2_hl(p.out, p.out_lo, o1 + nd * 8 + t2, o[nd][2] * i1, o[nd][3] * i1);
     }
     return;
   }
@@ -323,29 +331,58 @@ __global__ void __launch_bounds__(32 * 9, 1)
   asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
   if (!*bcast) return;
 
-  // ---- merge the nsplit partials of this (request, kv head), split order
+  // ---- merge the nsplit partials of this (request, kv head); each warp
+  // merges its own 16 rows.  Lanes own splits for the (max, sum) pass
+  // (combined with warp shuffles), then own 4 of the 128 columns for the
+  // weighted sum of the partial outputs (16 independent loads per split).
+  const float *pml = p.part_ml + (slot0 * rows + w * BLK) * 2;
+  const float *pot = p.part_o + (slot0 * rows + w * BLK) * HD;
+  float M[BLK], L[BLK];
+#pragma unroll
   for (int j = 0; j < BLK; ++j) {
-    const size_t row = w * BLK + j;
-    float mx = -INFINITY;
-    for (int ss = 0; ss < nsplit; ++ss) mx = fmaxf(mx, __ldcg(p.part_ml + ((slot0 + ss) * rows + row) * 2));
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int ss = 0; ss < nsplit; ++ss) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + ((slot0 + ss) * rows + row) * 2));
-      const float wgt = fast_exp2(ml.x - mx);
-      L += wgt * ml.y;
-      const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + ((slot0 + ss) * rows + row) * HD) + lane);
-      acc.x += wgt * v.x;
-      acc.y += wgt * v.y;
-      acc.z += wgt * v.z;
-      acc.w += wgt * v.w;
+    M[j] = -INFINITY;
+    L[j] = 0.f;
+  }
+  for (int s0 = 0; s0 < nsplit; s0 += 32) {        // running max / sum over groups of 32 splits
+    const int ss = s0 + lane;
+    float2 ml[BLK];
+#pragma unroll
+    for (int j = 0; j < BLK; ++j)
+      ml[j] = ss < nsplit ? __ldcg(reinterpret_cast<const float2 *>(pml + (static_cast<size_t>(ss) * rows + j) * 2))
+                          : make_float2(-INFINITY, 0.f);
+#pragma unroll
+    for (int j = 0; j < BLK; ++j) {
+      const float gm = warp_max(ml[j].x);
+      const float mn = fmaxf(M[j], gm);
+      const float contrib = ss < nsplit ? fast_exp2(ml[j].x - mn) * ml[j].y : 0.f;
+      L[j] = L[j] * fast_exp2(M[j] - mn) + warp_sum(contrib);
+      M[j] = mn;
     }
-    const float inv = 1.f / L;
-    __nv_bfloat16 *dst = p.out + static_cast<size_t>(b * BLK + j) * p.ldo + hq * HD + lane * 4;
-    uint2 pk;
-    pk.x = pack_bf16(acc.x * inv, acc.y * inv);
-    pk.y = pack_bf16(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2 *>(dst) = pk;
+  }
+  float4 acc[BLK];
+#pragma unroll
+  for (int j = 0; j < BLK; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int ss = 0; ss < nsplit; ++ss) {
+    float4 v[BLK];
+#pragma unroll
+    for (int j = 0; j < BLK; ++j)
+      v[j] = __ldcg(reinterpret_cast<const float4 *>(pot + (static_cast<size_t>(ss) * rows + j) * HD) + lane);
+#pragma unroll
+    for (int j = 0; j < BLK; ++j) {
+      const float m = __ldcg(pml + (static_cast<size_t>(ss) * rows + j) * 2);   // L2 hit, uniform
+      const float wgt = fast_exp2(m - M[j]);
+      acc[j].x += wgt * v[j].x;
+      acc[j].y += wgt * v[j].y;
+      acc[j].z += wgt * v[j].z;
+      acc[j].w += wgt * v[j].w;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < BLK; ++j) {
+    const float inv = 1.f / L[j];
+    const size_t dst = static_cast<size_t>(b * BLK + j) * p.ldo + hq * HD + lane * 4;
+    store2_hl(p.out, p.out_lo, dst, acc[j].x * inv, acc[j].y * inv);
+    store2_hl(p.out, p.out_lo, dst + 2, acc[j].z * inv, acc[j].w * inv);
   }
 }
 
@@ -430,6 +467,7 @@ int attention_bf16(const Launch &lc, const AttnArgs &a) {
   p.q = static_cast<const __nv_bfloat16 *>(a.q);
   p.ldq = a.nq * HD;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
+  p.out_lo = static_cast<__nv_bfloat16 *>(a.out_lo);
   p.ldo = a.nq * HD;
   p.page_table = a.page_table;
   p.max_pages = a.max_pages;

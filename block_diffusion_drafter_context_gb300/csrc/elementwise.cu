@@ -4,9 +4,14 @@
 //
 // Readings used where the pages give no layer internals (Qwen3-shaped
 // drafter): RMSNorm y = g * x / sqrt(mean(x^2) + eps); RoPE pairs (i, i+d/2)
-// with theta_i = base^(-2i/d), rotation (x, y) -> (x cos - y sin, y cos + x sin);
-// the rotation angle is formed and range-reduced in fp64 so long positions
-// keep full fp32 accuracy.
+// with theta_i = base^(-2i/d), rotation (x, y) -> (x cos - y sin, y cos + x sin).
+//
+// GB300 notes: fp64 is a slow unit on this part, so theta_i is computed once
+// on the host and passed as an fp32 (hi, lo) pair; the device forms the angle
+// pos*theta with two fp64 multiply-adds, reduces it by 2*pi in fp64 and
+// evaluates sin/cos in fp32.  Row kernels issue all of a row's 128-bit loads
+// before the first use (no latency chain).  Outputs that feed a GEMM can be
+// written as bf16 high + low halves (split activations).
 #include "common.cuh"
 #include "internal.h"
 
@@ -15,12 +20,15 @@
 namespace dflash {
 namespace {
 
+constexpr int ROW_THREADS = 256;
+constexpr int MAXV = 8;            // float4 per thread: rows up to 256*4*8 = 8192
+
 template <typename T>
 __host__ __device__ inline T *tp(void *p) {
   return static_cast<T *>(p);
 }
 
-// Block-wide sum for blockDim.x a multiple of 32 (<= 1024).
+// Block-wide sum (blockDim.x a multiple of 32).
 __device__ __forceinline__ float block_sum(float v, float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   v = warp_sum(v);
@@ -32,21 +40,58 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
   return t;
 }
 
-// cos / sin of pos * base^(-2i/d)
-__device__ __forceinline__ void rope_cs(int pos, int i, int d, float rope_base, float &c, float &s) {
-  const double theta = exp2(-2.0 * i / d * log2(static_cast<double>(rope_base)));
-  double a = static_cast<double>(pos) * theta;
-  const double twopi = 6.283185307179586476925286766559;
-  a -= twopi * rint(a / twopi);
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16 *p) {
+  const uint2 u = *reinterpret_cast<const uint2 *>(p);
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+  return make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+}
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void st4(__nv_bfloat16 *p, float4 v) {
+  uint2 u;
+  u.x = pack_bf16(v.x, v.y);
+  u.y = pack_bf16(v.z, v.w);
+  *reinterpret_cast<uint2 *>(p) = u;
+}
+// bf16 high half to p, low half (v - high) to lo (if given)
+__device__ __forceinline__ void st4_hl(__nv_bfloat16 *p, __nv_bfloat16 *lo, float4 v) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t *>(&a);
+  u.y = *reinterpret_cast<const uint32_t *>(&b);
+  *reinterpret_cast<uint2 *>(p) = u;
+  if (lo) {
+    uint2 l;
+    l.x = pack_bf16(v.x - __low2float(a), v.y - __high2float(a));
+    l.y = pack_bf16(v.z - __low2float(b), v.w - __high2float(b));
+    *reinterpret_cast<uint2 *>(lo) = l;
+  }
+}
+__device__ __forceinline__ void st4_hl(float *p, float *, float4 v) { st4(p, v); }
+
+__device__ __forceinline__ float4 scale4(float4 a, float r, float4 g) {
+  return make_float4(a.x * r * g.x, a.y * r * g.y, a.z * r * g.z, a.w * r * g.w);
+}
+__device__ __forceinline__ float dot4(float4 a) { return a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w; }
+
+// cos / sin of pos * theta_i, theta_i = hi + lo (host-computed in fp64)
+__device__ __forceinline__ void rope_cs(int pos, float th_hi, float th_lo, float &c, float &s) {
+  const double p = static_cast<double>(pos);
+  double a = fma(p, static_cast<double>(th_lo), p * static_cast<double>(th_hi));
+  const double k = rint(a * 0.15915494309189533577);          // a / (2 pi)
+  a = fma(-k, 6.283185307179586232, a);                        // 2 pi, high part
+  a = fma(-k, 2.4492935982947064e-16, a);                      // 2 pi, low part
   sincosf(static_cast<float>(a), &s, &c);
 }
 
 // ------------------------------------------------------------------ embed
 // x[b*16+j] = E[id] (fp32 residual stream); u = RMSNorm(x) (activation dtype)
 template <typename T>
-__global__ void __launch_bounds__(256) embed_rmsnorm_kernel(const T *embed, const int32_t *anchor, int mask_id,
-                                                            int vocab, const float *gain, float eps, int H,
-                                                            float *x, T *u, int *status) {
+__global__ void __launch_bounds__(ROW_THREADS) embed_rmsnorm_kernel(const T *embed, const int32_t *anchor,
+                                                                    int mask_id, int vocab, const float *gain,
+                                                                    float eps, int H, float *x, T *u, T *u_lo,
+                                                                    int *status) {
   grid_dep_wait();
   __shared__ float red[32];
   const int row = blockIdx.x, b = row >> 4, j = row & 15;
@@ -56,37 +101,69 @@ __global__ void __launch_bounds__(256) embed_rmsnorm_kernel(const T *embed, cons
     id = 0;
   }
   const T *e = embed + static_cast<size_t>(id) * H;
+  const int nv = H >> 2;
+  float4 v[MAXV], g[MAXV];
   float ss = 0.f;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const float v = Elt<T>::ld(e + c);
-    x[static_cast<size_t>(row) * H + c] = v;
-    ss += v * v;
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k) {
+    const int i = threadIdx.x + k * ROW_THREADS;
+    if (i < nv) {
+      v[k] = ld4(e + 4 * i);
+      g[k] = ld4(gain + 4 * i);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k) {
+    const int i = threadIdx.x + k * ROW_THREADS;
+    if (i < nv) {
+      st4(x + static_cast<size_t>(row) * H + 4 * i, v[k]);
+      ss += dot4(v[k]);
+    }
   }
   const float r = rsqrtf(block_sum(ss, red) / H + eps);
-  for (int c = threadIdx.x; c < H; c += blockDim.x)
-    Elt<T>::st(u + static_cast<size_t>(row) * H + c, x[static_cast<size_t>(row) * H + c] * r * gain[c]);
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k) {
+    const int i = threadIdx.x + k * ROW_THREADS;
+    if (i < nv)
+      st4_hl(u + static_cast<size_t>(row) * H + 4 * i, u_lo ? u_lo + static_cast<size_t>(row) * H + 4 * i : nullptr,
+             scale4(v[k], r, g[k]));
+  }
 }
 
 // ------------------------------------------------------------------ rmsnorm
-// out[row] = RMSNorm(x[row]); if out_mask is given, rows with j >= 1 are also
+// out[row] = RMSNorm(x[row]) (+ low halves); rows with j >= 1 are also
 // written compactly to out_mask[b*15 + j-1] (LM-head input of the mask rows).
 template <typename T>
-__global__ void __launch_bounds__(256) rmsnorm_kernel(const float *x, int H, const float *gain, float eps, T *out,
-                                                      T *out_mask) {
+__global__ void __launch_bounds__(ROW_THREADS) rmsnorm_kernel(const float *x, int H, const float *gain, float eps,
+                                                              T *out, T *out_lo, T *out_mask, T *out_mask_lo) {
   grid_dep_wait();
   __shared__ float red[32];
   const int row = blockIdx.x;
   const float *xr = x + static_cast<size_t>(row) * H;
+  const int nv = H >> 2;
+  float4 v[MAXV], g[MAXV];
   float ss = 0.f;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) ss += xr[c] * xr[c];
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k) {
+    const int i = threadIdx.x + k * ROW_THREADS;
+    if (i < nv) {
+      v[k] = ld4(xr + 4 * i);
+      g[k] = ld4(gain + 4 * i);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k)
+    if (threadIdx.x + k * ROW_THREADS < nv) ss += dot4(v[k]);
   const float r = rsqrtf(block_sum(ss, red) / H + eps);
   const int b = row >> 4, j = row & 15;
-  T *o = out ? out + static_cast<size_t>(row) * H : nullptr;
-  T *om = (out_mask && j > 0) ? out_mask + static_cast<size_t>(b * 15 + j - 1) * H : nullptr;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const float v = xr[c] * r * gain[c];
-    if (o) Elt<T>::st(o + c, v);
-    if (om) Elt<T>::st(om + c, v);
+  const size_t mrow = static_cast<size_t>(b * 15 + j - 1) * H;
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k) {
+    const int i = threadIdx.x + k * ROW_THREADS;
+    if (i >= nv) continue;
+    const float4 y = scale4(v[k], r, g[k]);
+    if (out) st4_hl(out + static_cast<size_t>(row) * H + 4 * i, out_lo ? out_lo + static_cast<size_t>(row) * H + 4 * i : nullptr, y);
+    if (out_mask && j > 0) st4_hl(out_mask + mrow + 4 * i, out_mask_lo ? out_mask_lo + mrow + 4 * i : nullptr, y);
   }
 }
 
@@ -95,32 +172,48 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float *x, int H, con
 // incoming context lengths so the scatter can read them even when the caller
 // updates ctx_len in place.
 template <typename T>
-__global__ void __launch_bounds__(256) feature_norm_kernel(const float *in, int H, const float *gain, float eps,
-                                                           int apply, T *out, const int32_t *ctx_in,
-                                                           int32_t *ctx_saved, int B) {
+__global__ void __launch_bounds__(ROW_THREADS) feature_norm_kernel(const float *in, int H, const float *gain,
+                                                                   float eps, int apply, T *out, T *out_lo,
+                                                                   const int32_t *ctx_in, int32_t *ctx_saved, int B) {
   grid_dep_wait();
   __shared__ float red[32];
   const int row = blockIdx.x;
   if (row == 0)
     for (int b = threadIdx.x; b < B; b += blockDim.x) ctx_saved[b] = ctx_in[b];
   const float *xr = in + static_cast<size_t>(row) * H;
-  float r = 1.f;
-  if (apply) {
-    float ss = 0.f;
-    for (int c = threadIdx.x; c < H; c += blockDim.x) ss += xr[c] * xr[c];
-    r = rsqrtf(block_sum(ss, red) / H + eps);
+  const int nv = H >> 2;
+  float4 v[MAXV], g[MAXV];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k) {
+    const int i = threadIdx.x + k * ROW_THREADS;
+    if (i < nv) {
+      v[k] = ld4(xr + 4 * i);
+      g[k] = apply ? ld4(gain + 4 * i) : make_float4(1.f, 1.f, 1.f, 1.f);
+      ss += dot4(v[k]);
+    }
   }
-  for (int c = threadIdx.x; c < H; c += blockDim.x)
-    Elt<T>::st(out + static_cast<size_t>(row) * H + c, apply ? xr[c] * r * gain[c] : xr[c]);
+  const float r = apply ? rsqrtf(block_sum(ss, red) / H + eps) : 1.f;
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k) {
+    const int i = threadIdx.x + k * ROW_THREADS;
+    if (i < nv)
+      st4_hl(out + static_cast<size_t>(row) * H + 4 * i, out_lo ? out_lo + static_cast<size_t>(row) * H + 4 * i : nullptr,
+             scale4(v[k], r, g[k]));
+  }
 }
 
 // ------------------------------------------------------------------ q/k norm + rope
+struct RopeArgs {
+  float th_hi[64], th_lo[64];
+};
+
 // qkv: fp32 [B*16][(nq+2nkv)*d].  One warp per (token, head).  q heads ->
 // q_out [B*16][nq*d]; k heads -> bk [B][nkv][16][d] (normed, rotated);
 // v heads -> bv [B][nkv][16][d].
 template <typename T, int DPL>
 __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, int nkv, const float *g_q,
-                                                      const float *g_k, int qk_norm, float eps, float rope_base,
+                                                      const float *g_k, int qk_norm, float eps, const RopeArgs rp,
                                                       const int32_t *ctx_len, T *q_out, T *bk, T *bv) {
   grid_dep_wait();
   constexpr int D = DPL * 32;
@@ -139,6 +232,7 @@ __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, 
     return;
   }
   const bool is_q = head < nq;
+  const int pos = ctx_len[b] + j;
   if (qk_norm) {
     float ss = 0.f;
 #pragma unroll
@@ -148,12 +242,11 @@ __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, 
 #pragma unroll
     for (int i = 0; i < DPL; ++i) v[i] *= r * g[lane + 32 * i];
   }
-  const int pos = ctx_len[b] + j;
   float o[DPL];
 #pragma unroll
   for (int i = 0; i < DPL / 2; ++i) {   // pairs (lane + 32i, lane + 32i + D/2)
     float c, s;
-    rope_cs(pos, lane + 32 * i, D, rope_base, c, s);
+    rope_cs(pos, rp.th_hi[lane + 32 * i], rp.th_lo[lane + 32 * i], c, s);
     const float x1 = v[i], x2 = v[i + DPL / 2];
     o[i] = x1 * c - x2 * s;
     o[i + DPL / 2] = x2 * c + x1 * s;
@@ -173,7 +266,7 @@ struct ScatterArgs {
   int T, L, nkv;
   const float *g_k[16];
   int qk_norm;
-  float eps, rope_base;
+  float eps;
   const int32_t *cu_new;
   int B;
   const int32_t *ctx_saved;
@@ -186,7 +279,7 @@ struct ScatterArgs {
 };
 
 template <typename T, int DPL>
-__global__ void __launch_bounds__(256) inject_scatter_kernel(const ScatterArgs a) {
+__global__ void __launch_bounds__(256) inject_scatter_kernel(const ScatterArgs a, const RopeArgs rp) {
   grid_dep_wait();
   constexpr int D = DPL * 32;
   const int t = blockIdx.x;
@@ -231,7 +324,7 @@ __global__ void __launch_bounds__(256) inject_scatter_kernel(const ScatterArgs a
 #pragma unroll
     for (int i = 0; i < DPL / 2; ++i) {
       float c, s;
-      rope_cs(pos, lane + 32 * i, D, a.rope_base, c, s);
+      rope_cs(pos, rp.th_hi[lane + 32 * i], rp.th_lo[lane + 32 * i], c, s);
       o[i] = v[i] * c - v[i + DPL / 2] * s;
       o[i + DPL / 2] = v[i + DPL / 2] * c + v[i] * s;
     }
@@ -250,25 +343,34 @@ __global__ void __launch_bounds__(256) inject_scatter_kernel(const ScatterArgs a
 //   coef: fp32 [B*16][H/8] = tanh(W_c y + b_c): [0, H/16) current tap a,
 //         [H/16, H/8) previous tap b.
 //   out_j = y_j + a_j * y_j + b_j * y_{j-1}
-// pre sites: out_t = conv(y) (activation dtype); post sites: x_add += conv(y).
+// y is either an activation (hi [+ lo] halves) or fp32 (y32).  Pre sites
+// write out (+ low halves), post sites add into the residual x_add.
 template <typename T>
-__global__ void __launch_bounds__(256) conv_kernel(const T *y, const float *coef, int H, T *out_t, float *x_add) {
+__global__ void __launch_bounds__(256) conv_kernel(const T *y, const T *y_lo, const float *y32, const float *coef,
+                                                   int H, T *out_t, T *out_lo, float *x_add) {
   grid_dep_wait();
   const int b = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= H) return;
   const int G = H / 16, grp = c >> 4;
-  float prev = 0.f;
+  float yv[16], av[16], bv[16];
+#pragma unroll
   for (int j = 0; j < 16; ++j) {
     const size_t row = static_cast<size_t>(b) * 16 + j;
-    const float cur = Elt<T>::ld(y + row * H + c);
-    const float a = coef[row * (2 * G) + grp], bb = coef[row * (2 * G) + G + grp];
-    const float v = cur + a * cur + bb * prev;
-    if (out_t)
+    yv[j] = y32 ? y32[row * H + c] : Elt<T>::ld(y + row * H + c) + (y_lo ? Elt<T>::ld(y_lo + row * H + c) : 0.f);
+    av[j] = coef[row * (2 * G) + grp];
+    bv[j] = coef[row * (2 * G) + G + grp];
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const size_t row = static_cast<size_t>(b) * 16 + j;
+    const float v = yv[j] + av[j] * yv[j] + bv[j] * (j ? yv[j - 1] : 0.f);
+    if (out_t) {
       Elt<T>::st(out_t + row * H + c, v);
-    else
+      if (out_lo) Elt<T>::st(out_lo + row * H + c, v - Elt<T>::ld(out_t + row * H + c));
+    } else {
       x_add[row * H + c] += v;
-    prev = cur;
+    }
   }
 }
 
@@ -279,43 +381,64 @@ int run(const Launch &lc, const char *name, F f) {
   return cuda_check(cudaGetLastError(), name);
 }
 
+RopeArgs rope_table(int d, float base) {
+  RopeArgs r = {};
+  for (int i = 0; i < d / 2 && i < 64; ++i) {
+    const double th = pow(static_cast<double>(base), -2.0 * i / d);
+    r.th_hi[i] = static_cast<float>(th);
+    r.th_lo[i] = static_cast<float>(th - static_cast<double>(r.th_hi[i]));
+  }
+  return r;
+}
+
+int check_row(int H) {
+  if (H % 4 || H > ROW_THREADS * 4 * MAXV)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "row kernels need hidden %% 4 == 0 and hidden <= %d", ROW_THREADS * 4 * MAXV);
+  return DFLASH_OK;
+}
+
 }  // namespace
 
 int embed_rmsnorm(const Launch &lc, bool f32, const void *embed, const int32_t *anchor, int mask_id, int vocab,
-                  const float *gain, float eps, int B, int H, float *x, void *u) {
+                  const float *gain, float eps, int B, int H, float *x, void *u, void *u_lo) {
+  if (int e = check_row(H)) return e;
   return run(lc, "embed_norm", [&] {
     if (f32)
-      embed_rmsnorm_kernel<float><<<B * 16, 256, 0, lc.stream>>>(static_cast<const float *>(embed), anchor, mask_id,
-                                                                 vocab, gain, eps, H, x, tp<float>(u), lc.status);
+      embed_rmsnorm_kernel<float><<<B * 16, ROW_THREADS, 0, lc.stream>>>(
+          static_cast<const float *>(embed), anchor, mask_id, vocab, gain, eps, H, x, tp<float>(u), nullptr, lc.status);
     else
-      embed_rmsnorm_kernel<__nv_bfloat16><<<B * 16, 256, 0, lc.stream>>>(
-          static_cast<const __nv_bfloat16 *>(embed), anchor, mask_id, vocab, gain, eps, H, x,
-          tp<__nv_bfloat16>(u), lc.status);
+      embed_rmsnorm_kernel<__nv_bfloat16><<<B * 16, ROW_THREADS, 0, lc.stream>>>(
+          static_cast<const __nv_bfloat16 *>(embed), anchor, mask_id, vocab, gain, eps, H, x, tp<__nv_bfloat16>(u),
+          tp<__nv_bfloat16>(u_lo), lc.status);
   });
 }
 
 int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, const float *gain, float eps,
-                 void *out, void *out_mask_rows) {
+                 void *out, void *out_lo, void *out_mask_rows, void *out_mask_lo) {
+  if (int e = check_row(H)) return e;
   return run(lc, "rmsnorm", [&] {
     if (f32)
-      rmsnorm_kernel<float><<<rows, 256, 0, lc.stream>>>(x, H, gain, eps, tp<float>(out), tp<float>(out_mask_rows));
+      rmsnorm_kernel<float><<<rows, ROW_THREADS, 0, lc.stream>>>(x, H, gain, eps, tp<float>(out), nullptr,
+                                                                 tp<float>(out_mask_rows), nullptr);
     else
-      rmsnorm_kernel<__nv_bfloat16><<<rows, 256, 0, lc.stream>>>(x, H, gain, eps, tp<__nv_bfloat16>(out),
-                                                                 tp<__nv_bfloat16>(out_mask_rows));
+      rmsnorm_kernel<__nv_bfloat16><<<rows, ROW_THREADS, 0, lc.stream>>>(
+          x, H, gain, eps, tp<__nv_bfloat16>(out), tp<__nv_bfloat16>(out_lo), tp<__nv_bfloat16>(out_mask_rows),
+          tp<__nv_bfloat16>(out_mask_lo));
   });
 }
 
 int feature_norm(const Launch &lc, bool f32, const float *in, int rows, int H, const float *gain, float eps,
-                 bool apply_norm, void *out, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B) {
+                 bool apply_norm, void *out, void *out_lo, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B) {
   if (rows <= 0) return DFLASH_OK;
+  if (int e = check_row(H)) return e;
   return run(lc, "feature_norm", [&] {
     if (f32)
-      feature_norm_kernel<float><<<rows, 256, 0, lc.stream>>>(in, H, gain, eps, apply_norm, tp<float>(out),
-                                                              ctx_len_in, ctx_len_saved, B);
+      feature_norm_kernel<float><<<rows, ROW_THREADS, 0, lc.stream>>>(in, H, gain, eps, apply_norm, tp<float>(out),
+                                                                      nullptr, ctx_len_in, ctx_len_saved, B);
     else
-      feature_norm_kernel<__nv_bfloat16><<<rows, 256, 0, lc.stream>>>(in, H, gain, eps, apply_norm,
-                                                                      tp<__nv_bfloat16>(out), ctx_len_in,
-                                                                      ctx_len_saved, B);
+      feature_norm_kernel<__nv_bfloat16><<<rows, ROW_THREADS, 0, lc.stream>>>(
+          in, H, gain, eps, apply_norm, tp<__nv_bfloat16>(out), tp<__nv_bfloat16>(out_lo), ctx_len_in, ctx_len_saved,
+          B);
   });
 }
 
@@ -323,9 +446,10 @@ int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int nq, in
                  const float *g_k, bool qk_norm, float eps, float rope_base, const int32_t *ctx_len, void *q_out,
                  void *bk, void *bv) {
   dim3 grid(B * 16, (nq + 2 * nkv + 7) / 8);
+  const RopeArgs rp = rope_table(d, rope_base);
   return run(lc, "qk_norm_rope", [&] {
-#define QK(T, DPL)                                                                                              \
-  qk_rope_kernel<T, DPL><<<grid, 256, 0, lc.stream>>>(qkv, nq, nkv, g_q, g_k, qk_norm, eps, rope_base, ctx_len, \
+#define QK(T, DPL)                                                                                         \
+  qk_rope_kernel<T, DPL><<<grid, 256, 0, lc.stream>>>(qkv, nq, nkv, g_q, g_k, qk_norm, eps, rp, ctx_len, \
                                                       tp<T>(q_out), tp<T>(bk), tp<T>(bv))
     if (f32 && d == 64)
       QK(float, 2);
@@ -352,7 +476,6 @@ int inject_scatter(const Launch &lc, bool f32, const float *kvproj, int T, int L
   for (int l = 0; l < L; ++l) a.g_k[l] = g_k[l];
   a.qk_norm = qk_norm;
   a.eps = eps;
-  a.rope_base = rope_base;
   a.cu_new = cu_new;
   a.B = B;
   a.ctx_saved = ctx_len_saved;
@@ -365,28 +488,31 @@ int inject_scatter(const Launch &lc, bool f32, const float *kvproj, int T, int L
   a.page = 64;
   a.layer_elems = layer_elems;
   a.status = lc.status;
+  const RopeArgs rp = rope_table(d, rope_base);
   dim3 grid(T, (L * 2 * nkv + 7) / 8);
   return run(lc, "inject_scatter", [&] {
     if (f32 && d == 64)
-      inject_scatter_kernel<float, 2><<<grid, 256, 0, lc.stream>>>(a);
+      inject_scatter_kernel<float, 2><<<grid, 256, 0, lc.stream>>>(a, rp);
     else if (f32)
-      inject_scatter_kernel<float, 4><<<grid, 256, 0, lc.stream>>>(a);
+      inject_scatter_kernel<float, 4><<<grid, 256, 0, lc.stream>>>(a, rp);
     else if (d == 64)
-      inject_scatter_kernel<__nv_bfloat16, 2><<<grid, 256, 0, lc.stream>>>(a);
+      inject_scatter_kernel<__nv_bfloat16, 2><<<grid, 256, 0, lc.stream>>>(a, rp);
     else
-      inject_scatter_kernel<__nv_bfloat16, 4><<<grid, 256, 0, lc.stream>>>(a);
+      inject_scatter_kernel<__nv_bfloat16, 4><<<grid, 256, 0, lc.stream>>>(a, rp);
   });
 }
 
-int conv_apply(const Launch &lc, bool f32, const void *y, const float *coef, int B, int H, void *out_t,
-               float *x_add) {
+int conv_apply(const Launch &lc, bool f32, const void *y, const void *y_lo, const float *y32, const float *coef, int B,
+               int H, void *out_t, void *out_lo, float *x_add) {
   dim3 grid((H + 255) / 256, B);
   return run(lc, "short_conv", [&] {
     if (f32)
-      conv_kernel<float><<<grid, 256, 0, lc.stream>>>(static_cast<const float *>(y), coef, H, tp<float>(out_t), x_add);
+      conv_kernel<float><<<grid, 256, 0, lc.stream>>>(static_cast<const float *>(y), nullptr, y32, coef, H,
+                                                      tp<float>(out_t), nullptr, x_add);
     else
-      conv_kernel<__nv_bfloat16><<<grid, 256, 0, lc.stream>>>(static_cast<const __nv_bfloat16 *>(y), coef, H,
-                                                              tp<__nv_bfloat16>(out_t), x_add);
+      conv_kernel<__nv_bfloat16><<<grid, 256, 0, lc.stream>>>(
+          static_cast<const __nv_bfloat16 *>(y), static_cast<const __nv_bfloat16 *>(y_lo), y32, coef, H,
+          tp<__nv_bfloat16>(out_t), tp<__nv_bfloat16>(out_lo), x_add);
   });
 }
 

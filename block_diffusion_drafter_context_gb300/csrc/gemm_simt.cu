@@ -63,13 +63,17 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const float *__restrict__
 
 }  // namespace
 
-int gemm_f32(const Launch &lc, const float *W, int ldw, const float *X, int ldx, int M, int N, int K, int epi,
-             void *out, int ldo, const float *bias, const char *name) {
+int gemm_f32(const Launch &lc, const GemmOp &op) {
+  const int M = op.M, N = op.N, K = op.K;
   if (M <= 0 || N <= 0 || K <= 0) return DFLASH_OK;
-  if (epi == EPI_BF16) return set_error(DFLASH_ERR_UNSUPPORTED, "gemm %s: bf16 output on the fp32 path", name);
+  int epi = op.epi;
+  if (epi == EPI_STORE_T || epi == EPI_F32_SPLIT) epi = EPI_F32;
+  if (epi == EPI_BF16) return set_error(DFLASH_ERR_UNSUPPORTED, "gemm %s: bf16 output on the fp32 path", op.name);
   dim3 grid((N + TN - 1) / TN, (M + TM - 1) / TM), block(32, 8);
-  ProfScope ps(lc, name, 4.0 * N * K + 4.0 * M * K + 4.0 * M * N, 2.0 * M * N * K);
-  gemm_f32_kernel<<<grid, block, 0, lc.stream>>>(W, ldw, X, ldx, M, N, K, epi, out, ldo, bias);
+  ProfScope ps(lc, op.name, 4.0 * N * K + 4.0 * M * K + 4.0 * M * N, 2.0 * M * N * K);
+  gemm_f32_kernel<<<grid, block, 0, lc.stream>>>(static_cast<const float *>(op.W), op.ldw,
+                                                  static_cast<const float *>(op.X), op.ldx, M, N, K, epi, op.out,
+                                                  op.ldo, op.bias);
   return cuda_check(cudaGetLastError(), "gemm_f32 launch");
 }
 

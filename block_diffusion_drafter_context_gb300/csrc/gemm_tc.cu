@@ -16,7 +16,12 @@
 //     sums the fp32 partials in CTA order - deterministic, no spin-waits;
 //   * warp roles: warp 0 issues TMA loads into a STAGES-deep ring of
 //     128-byte-swizzled tiles, warp 1 owns TMEM and issues tcgen05.mma from
-//     one thread, warps 2-5 drain TMEM (double-buffered) into the epilogue.
+//     one thread, warps 2-5 drain TMEM (double-buffered) into the epilogue;
+//   * split activations (SPLIT): the activation operand arrives as two bf16
+//     tensors, high and low halves of the fp32 value; each k-step issues a
+//     second MMA on the same weight tile, so the product carries ~16 mantissa
+//     bits of the activation at no extra HBM traffic (the weight stream, not
+//     the tensor pipe, bounds these GEMMs).
 // Every mbarrier wait is bounded (status word + unwind on timeout).
 #include "common.cuh"
 #include "internal.h"
@@ -31,11 +36,11 @@ constexpr int BK = 64;    // bf16 elements per stage row = 128 bytes = one swizz
 constexpr int UK = 16;    // K per tcgen05.mma (kind::f16)
 constexpr int NTHREADS = 192;
 
-template <int BN>
+template <int BN, bool SPLIT>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES * (SPLIT ? 2 : 1);
   static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
@@ -50,6 +55,9 @@ struct Params {
   int epi;
   void *out;
   int ldo;
+  void *out_lo;        // low bf16 halves of a bf16 output, or null
+  void *out2, *out2_lo;
+  int ldo2;
   const float *bias;
   float *partials;     // [G][2][BM*BN]
   int *counters;       // [tiles]
@@ -69,15 +77,21 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: 
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
+__device__ __forceinline__ void store_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t i, float v) {
+  const __nv_bfloat16 h = f2bf(v);
+  hi[i] = h;
+  if (lo) lo[i] = f2bf(v - bf2f(h));
+}
+
 // Apply the epilogue to 16 consecutive token columns of weight row n.
 __device__ __forceinline__ void finalize(const Params &p, const float (&v)[16], int n, int tok0) {
   const bool nok = n < p.N;
   switch (p.epi) {
     case EPI_BF16: {
-      __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out);
+      __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out), *ol = static_cast<__nv_bfloat16 *>(p.out_lo);
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        if (nok && tok0 + i < p.M) o[static_cast<size_t>(tok0 + i) * p.ldo + n] = f2bf(v[i]);
+        if (nok && tok0 + i < p.M) store_hl(o, ol, static_cast<size_t>(tok0 + i) * p.ldo + n, v[i]);
     } break;
     case EPI_F32: {
       float *o = static_cast<float *>(p.out);
@@ -92,11 +106,12 @@ __device__ __forceinline__ void finalize(const Params &p, const float (&v)[16], 
         if (nok && tok0 + i < p.M) o[static_cast<size_t>(tok0 + i) * p.ldo + n] += v[i];
     } break;
     case EPI_SWIGLU: {
-      __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out);
+      __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out), *ol = static_cast<__nv_bfloat16 *>(p.out_lo);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float up = __shfl_xor_sync(0xffffffffu, v[i], 1);
-        if (nok && !(n & 1) && tok0 + i < p.M) o[static_cast<size_t>(tok0 + i) * p.ldo + (n >> 1)] = f2bf(silu(v[i]) * up);
+        if (nok && !(n & 1) && tok0 + i < p.M)
+          store_hl(o, ol, static_cast<size_t>(tok0 + i) * p.ldo + (n >> 1), silu(v[i]) * up);
       }
     } break;
     case EPI_TANH_BIAS: {
@@ -106,22 +121,33 @@ __device__ __forceinline__ void finalize(const Params &p, const float (&v)[16], 
       for (int i = 0; i < 16; ++i)
         if (nok && tok0 + i < p.M) o[static_cast<size_t>(tok0 + i) * p.ldo + n] = tanhf(v[i] + b);
     } break;
+    case EPI_F32_SPLIT: {
+      float *o = static_cast<float *>(p.out);
+      __nv_bfloat16 *o2 = static_cast<__nv_bfloat16 *>(p.out2), *o2l = static_cast<__nv_bfloat16 *>(p.out2_lo);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (nok && tok0 + i < p.M) {
+          o[static_cast<size_t>(tok0 + i) * p.ldo + n] = v[i];
+          store_hl(o2, o2l, static_cast<size_t>(tok0 + i) * p.ldo2 + n, v[i]);
+        }
+    } break;
     default:
       break;
   }
 }
 
-template <int BN>
+template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const Params p) {
-  using C = Cfg<BN>;
+                   const __grid_constant__ CUtensorMap tmXlo, const Params p) {
+  using C = Cfg<BN, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *base = smem_raw + pad;
   uint8_t *sA = base;
   uint8_t *sB = base + C::STAGES * C::A_BYTES;
-  uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::STAGES * C::B_BYTES);
+  uint8_t *sBl = sB + C::STAGES * C::B_BYTES;   // low halves (SPLIT only)
+  uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::STAGES * C::B_BYTES * (SPLIT ? 2 : 1));
   uint64_t *empty = full + C::STAGES;
   uint64_t *tfull = empty + C::STAGES;
   uint64_t *tempty = tfull + 2;
@@ -148,6 +174,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+    if (SPLIT) tma_prefetch_desc(&tmXlo);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -187,6 +214,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
           tma_load_2d_hint(sA + stage * C::A_BYTES, &tmW, &full[stage], kb * BK, row0, pol_w);
           tma_load_2d(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * BK, tok0);
+          if (SPLIT) tma_load_2d(sBl + stage * C::B_BYTES, &tmXlo, &full[stage], kb * BK, tok0);
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -232,10 +260,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
           const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+          const uint32_t bl = smem_u32(sBl + stage * C::B_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / UK; ++k)
-            umma_bf16(d, sdesc_k_sw128(a0 + k * UK * 2), sdesc_k_sw128(b0 + k * UK * 2), idesc,
-                      (kb > kb0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < BK / UK; ++k) {
+            const uint64_t ad = sdesc_k_sw128(a0 + k * UK * 2);
+            umma_bf16(d, ad, sdesc_k_sw128(b0 + k * UK * 2), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            if (SPLIT) umma_bf16(d, ad, sdesc_k_sw128(bl + k * UK * 2), idesc, 1u);
+          }
           umma_commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -334,12 +365,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int BN>
-int launch(const Launch &lc, const CUtensorMap &tW, const CUtensorMap &tX, const Params &p) {
+template <int BN, bool SPLIT>
+int launch(const Launch &lc, const CUtensorMap &tW, const CUtensorMap &tX, const CUtensorMap &tXl, const Params &p) {
   static bool attr_done = false;
   if (!attr_done) {
-    if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                Cfg<BN>::SMEM),
+    if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, SPLIT>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN, SPLIT>::SMEM),
                            "gemm smem attribute"))
       return e;
     attr_done = true;
@@ -347,26 +378,46 @@ int launch(const Launch &lc, const CUtensorMap &tW, const CUtensorMap &tX, const
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.G);
   cfg.blockDim = dim3(NTHREADS);
-  cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<BN, SPLIT>::SMEM;
   cfg.stream = lc.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tW, tX, p), "gemm launch");
+  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, SPLIT>, tW, tX, tXl, p), "gemm launch");
+}
+
+template <bool SPLIT>
+int launch_bn(int BN, const Launch &lc, const CUtensorMap &tW, const CUtensorMap &tX, const CUtensorMap &tXl,
+              const Params &p) {
+  switch (BN) {
+    case 16: return launch<16, SPLIT>(lc, tW, tX, tXl, p);
+    case 32: return launch<32, SPLIT>(lc, tW, tX, tXl, p);
+    case 64: return launch<64, SPLIT>(lc, tW, tX, tXl, p);
+    case 128: return launch<128, SPLIT>(lc, tW, tX, tXl, p);
+    default: return launch<256, SPLIT>(lc, tW, tX, tXl, p);
+  }
 }
 
 }  // namespace
 
-int gemm_bf16(const Launch &lc, const void *W, int ldw, const void *X, int ldx, int M, int N, int K, int epi,
-              void *out, int ldo, const float *bias, const GemmScratch &sc, const char *name) {
+int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
+  const int M = op.M, N = op.N, K = op.K;
+  const char *name = op.name;
   if (M <= 0 || N <= 0 || K <= 0) return DFLASH_OK;
-  if (!W || !X || !out) return set_error(DFLASH_ERR_ARG, "gemm %s: null operand", name);
-  if ((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(X)) & 15 || (ldw * 2) % 16 || (ldx * 2) % 16)
+  if (!op.W || !op.X || !op.out) return set_error(DFLASH_ERR_ARG, "gemm %s: null operand", name);
+  const uintptr_t al = reinterpret_cast<uintptr_t>(op.W) | reinterpret_cast<uintptr_t>(op.X) |
+                       reinterpret_cast<uintptr_t>(op.X_lo);
+  if ((al & 15) || (op.ldw * 2) % 16 || (op.ldx * 2) % 16)
     return set_error(DFLASH_ERR_ALIGN, "gemm %s: operands / row strides must be 16-byte aligned", name);
-  if (epi == EPI_STORE_T) epi = EPI_BF16;
-  const int BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  int epi = op.epi == EPI_STORE_T ? EPI_BF16 : op.epi;
+  if (epi == EPI_F32_SPLIT && !op.out2) return set_error(DFLASH_ERR_ARG, "gemm %s: split output missing", name);
+  const bool split = op.X_lo != nullptr;
+  // token tile: the smallest that covers M; with split activations at most
+  // 128 so that a stage (weights + two activation tiles) still leaves a
+  // 4-deep ring in shared memory
+  const int BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : (M <= 128 || split) ? 128 : 256;
   Params p = {};
   p.M = M;
   p.N = N;
@@ -379,32 +430,41 @@ int gemm_bf16(const Launch &lc, const void *W, int ldw, const void *X, int ldx, 
   const int cap = lc.gemm_ctas > 0 ? lc.gemm_ctas : lc.num_sms;
   p.G = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, (p.total + 3) / 4)));
   p.epi = epi;
-  p.out = out;
-  p.ldo = ldo;
-  p.bias = bias;
+  p.out = op.out;
+  p.ldo = op.ldo;
+  p.out_lo = op.out_lo;
+  p.out2 = op.out2;
+  p.out2_lo = op.out2_lo;
+  p.ldo2 = op.ldo2;
+  p.bias = op.bias;
   p.partials = sc.partials;
   p.counters = sc.counters;
   p.status = lc.status;
   p.timeout_ns = lc.timeout_ns;
   if (tiles > sc.n_counters || static_cast<size_t>(p.G) * 2 * BM * BN > sc.partial_floats)
     return set_error(DFLASH_ERR_SHAPE, "gemm %s: workspace too small for %lld tiles", name, tiles);
-  CUtensorMap tW, tX;
-  if (int e = make_tmap_2d(&tW, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, static_cast<uint64_t>(ldw) * 2, BK, BM))
+  CUtensorMap tW, tX, tXl;
+  if (int e = make_tmap_2d(&tW, op.W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, static_cast<uint64_t>(op.ldw) * 2,
+                           BK, BM))
     return e;
-  if (int e = make_tmap_2d(&tX, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M, static_cast<uint64_t>(ldx) * 2, BK, BN))
+  if (int e = make_tmap_2d(&tX, op.X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M, static_cast<uint64_t>(op.ldx) * 2,
+                           BK, BN))
     return e;
+  if (split) {
+    if (int e = make_tmap_2d(&tXl, op.X_lo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M,
+                             static_cast<uint64_t>(op.ldx) * 2, BK, BN))
+      return e;
+  } else {
+    tXl = tX;
+  }
+  const double xb = (split ? 4.0 : 2.0) * M * K;
   const double out_bytes = (epi == EPI_F32 || epi == EPI_TANH_BIAS) ? 4.0 * M * N
                            : epi == EPI_ADD_F32                      ? 8.0 * M * N
-                           : epi == EPI_SWIGLU                       ? 1.0 * M * N
-                                                                     : 2.0 * M * N;
-  ProfScope ps(lc, name, 2.0 * N * K + 2.0 * M * K + out_bytes, 2.0 * M * N * K);
-  switch (BN) {
-    case 16: return launch<16>(lc, tW, tX, p);
-    case 32: return launch<32>(lc, tW, tX, p);
-    case 64: return launch<64>(lc, tW, tX, p);
-    case 128: return launch<128>(lc, tW, tX, p);
-    default: return launch<256>(lc, tW, tX, p);
-  }
+                           : epi == EPI_F32_SPLIT                    ? 8.0 * M * N
+                           : epi == EPI_SWIGLU                       ? (op.out_lo ? 2.0 : 1.0) * M * N
+                                                                     : (op.out_lo ? 4.0 : 2.0) * M * N;
+  ProfScope ps(lc, name, 2.0 * N * K + xb + out_bytes, (split ? 4.0 : 2.0) * M * N * K);
+  return split ? launch_bn<true>(BN, lc, tW, tX, tXl, p) : launch_bn<false>(BN, lc, tW, tX, tXl, p);
 }
 
 }  // namespace dflash

@@ -14,12 +14,33 @@ namespace dflash {
 
 // GEMM epilogues: out[m][n] = epi(sum_k X[m][k] * W[n][k])
 enum Epi : int {
-  EPI_BF16 = 0,       // out (bf16)  = acc
+  EPI_BF16 = 0,       // out (bf16)  = acc      (+ out_lo = bf16(acc - out) when given)
   EPI_F32 = 1,        // out (fp32)  = acc
   EPI_ADD_F32 = 2,    // out (fp32) += acc          (residual stream)
-  EPI_SWIGLU = 3,     // rows 2i / 2i+1 = gate_i / up_i: out[m][i] = silu(gate) * up (out dtype)
+  EPI_SWIGLU = 3,     // rows 2i / 2i+1 = gate_i / up_i: out[m][i] = silu(gate) * up (+ out_lo)
   EPI_TANH_BIAS = 4,  // out (fp32)  = tanh(acc + bias[n])   (conv coefficients)
-  EPI_STORE_T = 5     // out (activation dtype) = acc  (bf16 or fp32 by the ctx dtype)
+  EPI_STORE_T = 5,    // out (activation dtype) = acc (+ out_lo on the bf16 path)
+  EPI_F32_SPLIT = 6   // out (fp32) = acc, out2 / out2_lo = bf16 hi / lo halves of acc
+};
+
+// One projection.  Activations may come as two bf16 tensors X (high half)
+// and X_lo (low half, X + X_lo ~ the fp32 value): the kernel then issues a
+// second MMA per k-step on the same weight tile.
+struct GemmOp {
+  const void *W = nullptr;
+  int ldw = 0;
+  const void *X = nullptr;
+  const void *X_lo = nullptr;
+  int ldx = 0;
+  int M = 0, N = 0, K = 0;
+  int epi = EPI_F32;
+  void *out = nullptr;
+  int ldo = 0;
+  void *out_lo = nullptr;
+  void *out2 = nullptr, *out2_lo = nullptr;
+  int ldo2 = 0;
+  const float *bias = nullptr;
+  const char *name = "gemm";
 };
 
 // Per-launch timing of kernel families (dflash_profile_begin / _end).
@@ -70,12 +91,10 @@ int cuda_check(cudaError_t e, const char *what);
 int make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elt_bytes, uint64_t cols,
                  uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows);
 
-// bf16 operands on tcgen05 tensor cores.  W: [N][ldw], X: [M][ldx].
-int gemm_bf16(const Launch &lc, const void *W, int ldw, const void *X, int ldx, int M, int N, int K, int epi,
-              void *out, int ldo, const float *bias, const GemmScratch &sc, const char *name);
+// bf16 operands on tcgen05 tensor cores.
+int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc);
 // fp32 operands on CUDA cores (tiny fp32 configurations).
-int gemm_f32(const Launch &lc, const float *W, int ldw, const float *X, int ldx, int M, int N, int K, int epi,
-             void *out, int ldo, const float *bias, const char *name);
+int gemm_f32(const Launch &lc, const GemmOp &op);
 
 // ---------------------------------------------------------------- attention
 struct AttnArgs {
@@ -87,6 +106,7 @@ struct AttnArgs {
   int max_pages, num_pages, page_size;
   const int32_t *ctx_len;   // [B]
   void *out;                // [B*16][nq*d] (dtype)
+  void *out_lo;             // low bf16 halves of out, or null
   float *part_o;            // split partials
   float *part_ml;
   int *counters;            // [B*nkv]
@@ -98,12 +118,14 @@ int attention_bf16(const Launch &lc, const AttnArgs &a);
 int attention_f32(const Launch &lc, const AttnArgs &a);
 
 // ---------------------------------------------------------------- elementwise
+// *_lo outputs: low bf16 halves (value - high half) for split activations;
+// null to skip (always null on the fp32 path).
 int embed_rmsnorm(const Launch &lc, bool f32, const void *embed, const int32_t *anchor, int mask_id, int vocab,
-                  const float *gain, float eps, int B, int H, float *x, void *u);
+                  const float *gain, float eps, int B, int H, float *x, void *u, void *u_lo);
 int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, const float *gain, float eps,
-                 void *out, void *out_mask_rows);
+                 void *out, void *out_lo, void *out_mask_rows, void *out_mask_lo);
 int feature_norm(const Launch &lc, bool f32, const float *in, int rows, int H, const float *gain, float eps,
-                 bool apply_norm, void *out, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B);
+                 bool apply_norm, void *out, void *out_lo, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B);
 int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int nq, int nkv, int d,
                  const float *g_q, const float *g_k, bool qk_norm, float eps, float rope_base,
                  const int32_t *ctx_len, void *q_out, void *bk, void *bv);
@@ -111,8 +133,10 @@ int inject_scatter(const Launch &lc, bool f32, const float *kvproj, int T, int L
                    const float *const *g_k, bool qk_norm, float eps, float rope_base, const int32_t *cu_new,
                    int B, const int32_t *ctx_len_saved, int32_t *ctx_len_out, const dflash_kv &kv,
                    size_t layer_elems);
-int conv_apply(const Launch &lc, bool f32, const void *y, const float *coef, int B, int H, void *out_t,
-               float *x_add);
+// y: activation (hi [+ y_lo]) or y32 (fp32); pre sites write out_t (+ out_lo),
+// post sites add into x_add.
+int conv_apply(const Launch &lc, bool f32, const void *y, const void *y_lo, const float *y32, const float *coef,
+               int B, int H, void *out_t, void *out_lo, float *x_add);
 
 // ---------------------------------------------------------------- top-k / select / verify
 int topk16(const Launch &lc, const float *logits, int rows, int V, int32_t *ids, float *vals,

@@ -42,6 +42,7 @@ def make_config(cfg) -> B.dflash_config:
     c.use_selector = int(bool(cfg.use_selector))
     c.qk_norm = int(bool(cfg.qk_norm))
     c.fc_norm = int(bool(cfg.fc_norm))
+    c.split_act = int(bool(getattr(cfg, "split_act", True)))
     c.mask_id = int(cfg.mask_id)
     c.rope_base = float(cfg.rope_base)
     c.eps = float(cfg.eps)

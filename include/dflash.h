@@ -84,6 +84,9 @@ typedef struct dflash_config {
   int use_selector;      /* DFlash-2 Path Selector ([DF2] 1)                 */
   int qk_norm;           /* per-head RMSNorm of q and k                      */
   int fc_norm;           /* RMSNorm after the context-feature projection     */
+  int split_act;         /* bf16 path: pass every GEMM activation as bf16
+                            high + low halves (two MMAs per k-step): fp32-grade
+                            activation precision; no extra weight traffic    */
   int sel_rank;          /* r of the bilinear form (<= 64)                   */
   int sel_dim;           /* selector embedding width (256)                   */
   int mask_id;           /* token id of the mask token                       */

@@ -46,6 +46,7 @@ class DrafterConfig:
     sel_dim: int = 256      # width of the selector token embeddings
     qk_norm: bool = True
     fc_norm: bool = True
+    split_act: bool = True  # GPU precision mode: GEMM activations as bf16 hi + lo
     rope_base: float = 1e6
     eps: float = 1e-6
     page_size: int = 64

@@ -51,7 +51,7 @@ def test_struct_layouts_match_the_header():
 #define O(T, f) printf(#T "." #f " %zu\n", offsetof(T, f));
 int main(void) {
   P(dflash_config) P(dflash_layer_weights) P(dflash_weights) P(dflash_kv) P(dflash_kernel_stat)
-  O(dflash_config, rope_base) O(dflash_config, eps) O(dflash_config, page_size)
+  O(dflash_config, rope_base) O(dflash_config, eps) O(dflash_config, page_size) O(dflash_config, split_act)
   O(dflash_layer_weights, w_conv) O(dflash_layer_weights, b_conv)
   O(dflash_weights, layers) O(dflash_weights, sel_b_g) O(dflash_kv, num_pages) O(dflash_kernel_stat, ms)
   return 0;
@@ -73,6 +73,7 @@ int main(void) {
         "dflash_config.rope_base": B.dflash_config.rope_base.offset,
         "dflash_config.eps": B.dflash_config.eps.offset,
         "dflash_config.page_size": B.dflash_config.page_size.offset,
+        "dflash_config.split_act": B.dflash_config.split_act.offset,
         "dflash_layer_weights.w_conv": B.dflash_layer_weights.w_conv.offset,
         "dflash_layer_weights.b_conv": B.dflash_layer_weights.b_conv.offset,
         "dflash_weights.layers": B.dflash_weights.layers.offset,
@@ -88,7 +89,7 @@ def _cfg(**kw):
     c = B.dflash_config()
     base = dict(dtype=0, hidden=256, n_layers=1, n_q_heads=4, n_kv_heads=2, head_dim=128, ffn=512, vocab=1024,
                 target_hidden=256, n_target_layers=3, block_size=16, top_k=16, use_conv=0, use_selector=0,
-                qk_norm=1, fc_norm=1, sel_rank=32, sel_dim=256, mask_id=1023, page_size=64, rope_base=1e6, eps=1e-6)
+                qk_norm=1, fc_norm=1, split_act=1, sel_rank=32, sel_dim=256, mask_id=1023, page_size=64, rope_base=1e6, eps=1e-6)
     base.update(kw)
     for k, v in base.items():
         setattr(c, k, v)
