@@ -94,6 +94,17 @@ Profiler::~Profiler() {
   for (auto e : pool) cudaEventDestroy(e);
 }
 
+// Inside a stream capture the records must be external event nodes, so that
+// replaying the graph stamps the events.
+static void record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
 ProfScope::ProfScope(const Launch &l, const char *name, double bytes, double flops) : lc(l) {
   if (!lc.prof || !lc.prof->on) return;
   Profiler::Rec r;
@@ -102,12 +113,12 @@ ProfScope::ProfScope(const Launch &l, const char *name, double bytes, double flo
   r.b = lc.prof->take();
   r.bytes = bytes;
   r.flops = flops;
-  cudaEventRecord(r.a, lc.stream);
+  record(r.a, lc.stream);
   lc.prof->recs.push_back(r);
   idx = static_cast<int>(lc.prof->recs.size()) - 1;
 }
 ProfScope::~ProfScope() {
-  if (idx >= 0) cudaEventRecord(lc.prof->recs[idx].b, lc.stream);
+  if (idx >= 0) record(lc.prof->recs[idx].b, lc.stream);
 }
 
 // ------------------------------------------------------------------ workspace layout
