@@ -375,17 +375,28 @@ int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv, const void *targ
   if (int e = feature_norm(lc, f32, at<float>(workspace, L.fc), total_new, H, ctx->w.g_fc, g.eps, g.fc_norm != 0,
                            at<void>(workspace, L.f), f_lo, ctx_len_in, at<int32_t>(workspace, L.ctx_saved), batch))
     return e;
-  // every layer's own K/V projection of the feature (rows nq*d.. of w_qkv)
+  // every layer's own K/V projection of the feature (rows nq*d.. of w_qkv);
+  // on tensor cores all layers share one grouped launch
   std::vector<const float *> gk(g.n_layers);
+  GemmOp kvop = mk(nullptr, H, at<void>(workspace, L.f), f_lo, H, total_new, 2 * nkv * d, H, EPI_F32,
+                   at<float>(workspace, L.kvproj), 2 * nkv * d, "kv_inject");
+  kvop.out_gstride = static_cast<size_t>(total_new) * 2 * nkv * d;
   for (int l = 0; l < g.n_layers; ++l) {
     const dflash_layer_weights &lw = ctx->layers[l];
-    const void *wkv = static_cast<const char *>(lw.w_qkv) + te * static_cast<size_t>(nq) * d * H;
-    float *dst = at<float>(workspace, L.kvproj) + static_cast<size_t>(l) * total_new * 2 * nkv * d;
-    if (int e = proj(ctx, lc, workspace, L,
-                     mk(wkv, H, at<void>(workspace, L.f), f_lo, H, total_new, 2 * nkv * d, H, EPI_F32, dst, 2 * nkv * d,
-                        "kv_inject")))
-      return e;
+    kvop.Wg[l] = static_cast<const char *>(lw.w_qkv) + te * static_cast<size_t>(nq) * d * H;
     gk[l] = lw.g_k;
+  }
+  if (!f32 && (2 * nkv * d) % 128 == 0) {
+    kvop.n_groups = g.n_layers;
+    if (int e = proj(ctx, lc, workspace, L, kvop)) return e;
+  } else {
+    for (int l = 0; l < g.n_layers; ++l) {
+      GemmOp one = kvop;
+      one.n_groups = 1;
+      one.W = kvop.Wg[l];
+      one.out = at<float>(workspace, L.kvproj) + l * kvop.out_gstride;
+      if (int e = proj(ctx, lc, workspace, L, one)) return e;
+    }
   }
   return inject_scatter(lc, f32, at<float>(workspace, L.kvproj), total_new, g.n_layers, nkv, d, gk.data(),
                         g.qk_norm != 0, g.eps, g.rope_base, cu_new, batch, at<int32_t>(workspace, L.ctx_saved),

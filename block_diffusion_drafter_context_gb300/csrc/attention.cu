@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = p.g;
 
-  grid_dep_wait();
+  pdl_start();
   int n_ctx = p.ctx_len[b];
   const int cap = p.max_pages * CH;
   if (n_ctx < 0 || n_ctx > cap) {
@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(512) attn_f32_kernel(const float *q, int ldq, 
                                                        const float *bk, const float *bv, const int32_t *pt,
                                                        int max_pages, int num_pages, int page, const int32_t *ctx_len,
                                                        float *out, int ldo, int nkv, int g, float scale, int *status) {
-  grid_dep_wait();
+  pdl_start();
   constexpr int D = DPL * 32;
   const int hq = blockIdx.x, b = blockIdx.y, j = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = hq / g;
@@ -509,9 +509,9 @@ int attention_f32(const Launch &lc, const AttnArgs &a) {
              static_cast<const float *>(a.bk), static_cast<const float *>(a.bv), a.page_table, a.max_pages, \
              a.num_pages, a.page_size, a.ctx_len, o, a.nq * a.d, a.nkv, g, scale, lc.status
   if (a.d == 64)
-    attn_f32_kernel<2><<<grid, block, 0, lc.stream>>>(ARGS);
+    launch_pdl(attn_f32_kernel<2>, grid, block, 0, lc.stream, ARGS);
   else if (a.d == 128)
-    attn_f32_kernel<4><<<grid, block, 0, lc.stream>>>(ARGS);
+    launch_pdl(attn_f32_kernel<4>, grid, block, 0, lc.stream, ARGS);
   else
     return set_error(DFLASH_ERR_UNSUPPORTED, "fp32 attention: head_dim must be 64 or 128");
 #undef ARGS

@@ -78,6 +78,32 @@ __device__ __forceinline__ void grid_dep_wait() {
 __device__ __forceinline__ void grid_dep_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Kernel entry under programmatic dependent launch: let the next kernel of
+// the stream be scheduled right away (it waits for this grid itself), then
+// wait until the previous grid has completed and its writes are visible.
+__device__ __forceinline__ void pdl_start() {
+  grid_dep_launch();
+  grid_dep_wait();
+}
+
+// Host: launch with programmatic stream serialisation (every kernel of this
+// library begins with pdl_start() or an equivalent wait before touching
+// memory another kernel of the stream produces or consumes).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
 
 // ---------------------------------------------------------------- smem
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

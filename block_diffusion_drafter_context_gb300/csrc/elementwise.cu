@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(ROW_THREADS) embed_rmsnorm_kernel(const T *emb
                                                                     int mask_id, int vocab, const float *gain,
                                                                     float eps, int H, float *x, T *u, T *u_lo,
                                                                     int *status) {
-  grid_dep_wait();
+  pdl_start();
   __shared__ float red[32];
   const int row = blockIdx.x, b = row >> 4, j = row & 15;
   int id = j == 0 ? anchor[b] : mask_id;
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(ROW_THREADS) embed_rmsnorm_kernel(const T *emb
 template <typename T>
 __global__ void __launch_bounds__(ROW_THREADS) rmsnorm_kernel(const float *x, int H, const float *gain, float eps,
                                                               T *out, T *out_lo, T *out_mask, T *out_mask_lo) {
-  grid_dep_wait();
+  pdl_start();
   __shared__ float red[32];
   const int row = blockIdx.x;
   const float *xr = x + static_cast<size_t>(row) * H;
@@ -175,7 +175,7 @@ template <typename T>
 __global__ void __launch_bounds__(ROW_THREADS) feature_norm_kernel(const float *in, int H, const float *gain,
                                                                    float eps, int apply, T *out, T *out_lo,
                                                                    const int32_t *ctx_in, int32_t *ctx_saved, int B) {
-  grid_dep_wait();
+  pdl_start();
   __shared__ float red[32];
   const int row = blockIdx.x;
   if (row == 0)
@@ -215,7 +215,7 @@ template <typename T, int DPL>
 __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, int nkv, const float *g_q,
                                                       const float *g_k, int qk_norm, float eps, const RopeArgs rp,
                                                       const int32_t *ctx_len, T *q_out, T *bk, T *bv) {
-  grid_dep_wait();
+  pdl_start();
   constexpr int D = DPL * 32;
   const int tok = blockIdx.x, b = tok >> 4, j = tok & 15;
   const int head = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -280,7 +280,7 @@ struct ScatterArgs {
 
 template <typename T, int DPL>
 __global__ void __launch_bounds__(256) inject_scatter_kernel(const ScatterArgs a, const RopeArgs rp) {
-  grid_dep_wait();
+  pdl_start();
   constexpr int D = DPL * 32;
   const int t = blockIdx.x;
   const int lane = threadIdx.x & 31;
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(256) inject_scatter_kernel(const ScatterArgs a
 template <typename T>
 __global__ void __launch_bounds__(256) conv_kernel(const T *y, const T *y_lo, const float *y32, const float *coef,
                                                    int H, T *out_t, T *out_lo, float *x_add) {
-  grid_dep_wait();
+  pdl_start();
   const int b = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= H) return;
@@ -404,10 +404,10 @@ int embed_rmsnorm(const Launch &lc, bool f32, const void *embed, const int32_t *
   if (int e = check_row(H)) return e;
   return run(lc, "embed_norm", [&] {
     if (f32)
-      embed_rmsnorm_kernel<float><<<B * 16, ROW_THREADS, 0, lc.stream>>>(
+      launch_pdl(embed_rmsnorm_kernel<float>, dim3(B * 16), dim3(ROW_THREADS), 0, lc.stream,
           static_cast<const float *>(embed), anchor, mask_id, vocab, gain, eps, H, x, tp<float>(u), nullptr, lc.status);
     else
-      embed_rmsnorm_kernel<__nv_bfloat16><<<B * 16, ROW_THREADS, 0, lc.stream>>>(
+      launch_pdl(embed_rmsnorm_kernel<__nv_bfloat16>, dim3(B * 16), dim3(ROW_THREADS), 0, lc.stream,
           static_cast<const __nv_bfloat16 *>(embed), anchor, mask_id, vocab, gain, eps, H, x, tp<__nv_bfloat16>(u),
           tp<__nv_bfloat16>(u_lo), lc.status);
   });
@@ -418,10 +418,10 @@ int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, co
   if (int e = check_row(H)) return e;
   return run(lc, "rmsnorm", [&] {
     if (f32)
-      rmsnorm_kernel<float><<<rows, ROW_THREADS, 0, lc.stream>>>(x, H, gain, eps, tp<float>(out), nullptr,
+      launch_pdl(rmsnorm_kernel<float>, dim3(rows), dim3(ROW_THREADS), 0, lc.stream, x, H, gain, eps, tp<float>(out), nullptr,
                                                                  tp<float>(out_mask_rows), nullptr);
     else
-      rmsnorm_kernel<__nv_bfloat16><<<rows, ROW_THREADS, 0, lc.stream>>>(
+      launch_pdl(rmsnorm_kernel<__nv_bfloat16>, dim3(rows), dim3(ROW_THREADS), 0, lc.stream,
           x, H, gain, eps, tp<__nv_bfloat16>(out), tp<__nv_bfloat16>(out_lo), tp<__nv_bfloat16>(out_mask_rows),
           tp<__nv_bfloat16>(out_mask_lo));
   });
@@ -433,10 +433,10 @@ int feature_norm(const Launch &lc, bool f32, const float *in, int rows, int H, c
   if (int e = check_row(H)) return e;
   return run(lc, "feature_norm", [&] {
     if (f32)
-      feature_norm_kernel<float><<<rows, ROW_THREADS, 0, lc.stream>>>(in, H, gain, eps, apply_norm, tp<float>(out),
+      launch_pdl(feature_norm_kernel<float>, dim3(rows), dim3(ROW_THREADS), 0, lc.stream, in, H, gain, eps, apply_norm, tp<float>(out),
                                                                       nullptr, ctx_len_in, ctx_len_saved, B);
     else
-      feature_norm_kernel<__nv_bfloat16><<<rows, ROW_THREADS, 0, lc.stream>>>(
+      launch_pdl(feature_norm_kernel<__nv_bfloat16>, dim3(rows), dim3(ROW_THREADS), 0, lc.stream,
           in, H, gain, eps, apply_norm, tp<__nv_bfloat16>(out), tp<__nv_bfloat16>(out_lo), ctx_len_in, ctx_len_saved,
           B);
   });
@@ -449,7 +449,7 @@ int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int nq, in
   const RopeArgs rp = rope_table(d, rope_base);
   return run(lc, "qk_norm_rope", [&] {
 #define QK(T, DPL)                                                                                         \
-  qk_rope_kernel<T, DPL><<<grid, 256, 0, lc.stream>>>(qkv, nq, nkv, g_q, g_k, qk_norm, eps, rp, ctx_len, \
+  launch_pdl(qk_rope_kernel<T, DPL>, dim3(grid), dim3(256), 0, lc.stream, qkv, nq, nkv, g_q, g_k, qk_norm, eps, rp, ctx_len, \
                                                       tp<T>(q_out), tp<T>(bk), tp<T>(bv))
     if (f32 && d == 64)
       QK(float, 2);
@@ -492,13 +492,13 @@ int inject_scatter(const Launch &lc, bool f32, const float *kvproj, int T, int L
   dim3 grid(T, (L * 2 * nkv + 7) / 8);
   return run(lc, "inject_scatter", [&] {
     if (f32 && d == 64)
-      inject_scatter_kernel<float, 2><<<grid, 256, 0, lc.stream>>>(a, rp);
+      launch_pdl(inject_scatter_kernel<float, 2>, dim3(grid), dim3(256), 0, lc.stream, a, rp);
     else if (f32)
-      inject_scatter_kernel<float, 4><<<grid, 256, 0, lc.stream>>>(a, rp);
+      launch_pdl(inject_scatter_kernel<float, 4>, dim3(grid), dim3(256), 0, lc.stream, a, rp);
     else if (d == 64)
-      inject_scatter_kernel<__nv_bfloat16, 2><<<grid, 256, 0, lc.stream>>>(a, rp);
+      launch_pdl(inject_scatter_kernel<__nv_bfloat16, 2>, dim3(grid), dim3(256), 0, lc.stream, a, rp);
     else
-      inject_scatter_kernel<__nv_bfloat16, 4><<<grid, 256, 0, lc.stream>>>(a, rp);
+      launch_pdl(inject_scatter_kernel<__nv_bfloat16, 4>, dim3(grid), dim3(256), 0, lc.stream, a, rp);
   });
 }
 
@@ -507,10 +507,10 @@ int conv_apply(const Launch &lc, bool f32, const void *y, const void *y_lo, cons
   dim3 grid((H + 255) / 256, B);
   return run(lc, "short_conv", [&] {
     if (f32)
-      conv_kernel<float><<<grid, 256, 0, lc.stream>>>(static_cast<const float *>(y), nullptr, y32, coef, H,
+      launch_pdl(conv_kernel<float>, dim3(grid), dim3(256), 0, lc.stream, static_cast<const float *>(y), nullptr, y32, coef, H,
                                                       tp<float>(out_t), nullptr, x_add);
     else
-      conv_kernel<__nv_bfloat16><<<grid, 256, 0, lc.stream>>>(
+      launch_pdl(conv_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, lc.stream,
           static_cast<const __nv_bfloat16 *>(y), static_cast<const __nv_bfloat16 *>(y_lo), y32, coef, H,
           tp<__nv_bfloat16>(out_t), tp<__nv_bfloat16>(out_lo), x_add);
   });

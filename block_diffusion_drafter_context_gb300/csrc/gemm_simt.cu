@@ -13,7 +13,7 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const float *__restrict__
                                                        const float *__restrict__ X, int ldx, int M, int N,
                                                        int K, int epi, void *out, int ldo,
                                                        const float *__restrict__ bias) {
-  grid_dep_wait();
+  pdl_start();
   __shared__ float Ws[TN][TK + 1];
   __shared__ float Xs[TM][TK + 1];
   const int tx = threadIdx.x;   // 0..31: n within tile (one warp row)
@@ -71,7 +71,7 @@ int gemm_f32(const Launch &lc, const GemmOp &op) {
   if (epi == EPI_BF16) return set_error(DFLASH_ERR_UNSUPPORTED, "gemm %s: bf16 output on the fp32 path", op.name);
   dim3 grid((N + TN - 1) / TN, (M + TM - 1) / TM), block(32, 8);
   ProfScope ps(lc, op.name, 4.0 * N * K + 4.0 * M * K + 4.0 * M * N, 2.0 * M * N * K);
-  gemm_f32_kernel<<<grid, block, 0, lc.stream>>>(static_cast<const float *>(op.W), op.ldw,
+  launch_pdl(gemm_f32_kernel, dim3(grid), dim3(block), 0, lc.stream, static_cast<const float *>(op.W), op.ldw,
                                                   static_cast<const float *>(op.X), op.ldx, M, N, K, epi, op.out,
                                                   op.ldo, op.bias);
   return cuda_check(cudaGetLastError(), "gemm_f32 launch");

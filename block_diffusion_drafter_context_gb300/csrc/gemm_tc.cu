@@ -35,6 +35,11 @@ constexpr int BM = 128;   // weight rows per tile (UMMA M)
 constexpr int BK = 64;    // bf16 elements per stage row = 128 bytes = one swizzle row
 constexpr int UK = 16;    // K per tcgen05.mma (kind::f16)
 constexpr int NTHREADS = 192;
+constexpr int MAX_GROUPS = 16;   // weight matrices sharing one launch (same shape, same activations)
+
+struct WMaps {
+  CUtensorMap m[MAX_GROUPS];
+};
 
 template <int BN, bool SPLIT>
 struct Cfg {
@@ -48,7 +53,9 @@ struct Cfg {
 };
 
 struct Params {
-  int M, N, K;
+  int M, N, K;          // N: output rows of one group
+  int n_groups, rtpg;   // groups, 128-row tiles per group
+  size_t out_gstride;   // output elements between groups
   int tok_tiles, kbpt;
   long long total;     // tiles * kbpt
   int G;               // CTAs
@@ -84,26 +91,26 @@ __device__ __forceinline__ void store_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, s
 }
 
 // Apply the epilogue to 16 consecutive token columns of weight row n.
-__device__ __forceinline__ void finalize(const Params &p, const float (&v)[16], int n, int tok0) {
+__device__ __forceinline__ void finalize(const Params &p, const float (&v)[16], int n, int tok0, size_t goff) {
   const bool nok = n < p.N;
   switch (p.epi) {
     case EPI_BF16: {
       __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out), *ol = static_cast<__nv_bfloat16 *>(p.out_lo);
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        if (nok && tok0 + i < p.M) store_hl(o, ol, static_cast<size_t>(tok0 + i) * p.ldo + n, v[i]);
+        if (nok && tok0 + i < p.M) store_hl(o, ol, goff + static_cast<size_t>(tok0 + i) * p.ldo + n, v[i]);
     } break;
     case EPI_F32: {
       float *o = static_cast<float *>(p.out);
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        if (nok && tok0 + i < p.M) o[static_cast<size_t>(tok0 + i) * p.ldo + n] = v[i];
+        if (nok && tok0 + i < p.M) o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] = v[i];
     } break;
     case EPI_ADD_F32: {
       float *o = static_cast<float *>(p.out);
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        if (nok && tok0 + i < p.M) o[static_cast<size_t>(tok0 + i) * p.ldo + n] += v[i];
+        if (nok && tok0 + i < p.M) o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] += v[i];
     } break;
     case EPI_SWIGLU: {
       __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out), *ol = static_cast<__nv_bfloat16 *>(p.out_lo);
@@ -111,7 +118,7 @@ __device__ __forceinline__ void finalize(const Params &p, const float (&v)[16], 
       for (int i = 0; i < 16; ++i) {
         const float up = __shfl_xor_sync(0xffffffffu, v[i], 1);
         if (nok && !(n & 1) && tok0 + i < p.M)
-          store_hl(o, ol, static_cast<size_t>(tok0 + i) * p.ldo + (n >> 1), silu(v[i]) * up);
+          store_hl(o, ol, goff + static_cast<size_t>(tok0 + i) * p.ldo + (n >> 1), silu(v[i]) * up);
       }
     } break;
     case EPI_TANH_BIAS: {
@@ -119,7 +126,7 @@ __device__ __forceinline__ void finalize(const Params &p, const float (&v)[16], 
       const float b = nok ? p.bias[n] : 0.f;
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        if (nok && tok0 + i < p.M) o[static_cast<size_t>(tok0 + i) * p.ldo + n] = tanhf(v[i] + b);
+        if (nok && tok0 + i < p.M) o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] = tanhf(v[i] + b);
     } break;
     case EPI_F32_SPLIT: {
       float *o = static_cast<float *>(p.out);
@@ -127,7 +134,7 @@ __device__ __forceinline__ void finalize(const Params &p, const float (&v)[16], 
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         if (nok && tok0 + i < p.M) {
-          o[static_cast<size_t>(tok0 + i) * p.ldo + n] = v[i];
+          o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] = v[i];
           store_hl(o2, o2l, static_cast<size_t>(tok0 + i) * p.ldo2 + n, v[i]);
         }
     } break;
@@ -138,7 +145,7 @@ __device__ __forceinline__ void finalize(const Params &p, const float (&v)[16], 
 
 template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+    gemm_tc_kernel(const __grid_constant__ WMaps wm, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmXlo, const Params p) {
   using C = Cfg<BN, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
@@ -172,10 +179,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmW);
+    for (int g = 0; g < p.n_groups; ++g) tma_prefetch_desc(&wm.m[g]);
     tma_prefetch_desc(&tmX);
     if (SPLIT) tma_prefetch_desc(&tmXlo);
   }
+  grid_dep_launch();   // the next kernel may be scheduled now; it waits for this grid itself
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
@@ -185,10 +193,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Operands and outputs may be produced / consumed by the neighbouring
-  // kernels of the step: wait for them here (no-op without PDL).
-  grid_dep_wait();
-
+  // The activations, outputs and stream-K scratch are produced / consumed by
+  // the neighbouring kernels of the step: only the weight stream may start
+  // before the previous grid has completed (programmatic dependent launch).
   const long long begin = range_begin(p.total, p.G, blockIdx.x);
   const long long end = range_begin(p.total, p.G, blockIdx.x + 1);
   const int first_tile = static_cast<int>(begin / p.kbpt);
@@ -197,33 +204,52 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
-      uint32_t stage = 0, phase = 0;
-      long long issued = 0;
-      bool ok = true;
-      for (long long it = begin; it < end && ok;) {
+      const long long n_my = end - begin;
+      auto coords = [&](long long i, int &g, int &row0, int &tok0, int &kb) {
+        const long long it = begin + i;
         const int tile = static_cast<int>(it / p.kbpt);
-        const int kb0 = static_cast<int>(it % p.kbpt);
-        const int kb1 = static_cast<int>((kb0 + (end - it) < p.kbpt ? kb0 + (end - it) : p.kbpt));
-        const int row0 = (tile / p.tok_tiles) * BM;
-        const int tok0 = (tile % p.tok_tiles) * BN;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d_hint(sA + stage * C::A_BYTES, &tmW, &full[stage], kb * BK, row0, pol_w);
-          tma_load_2d(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * BK, tok0);
-          if (SPLIT) tma_load_2d(sBl + stage * C::B_BYTES, &tmXlo, &full[stage], kb * BK, tok0);
-          ++issued;
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        it += kb1 - kb0;
+        kb = static_cast<int>(it % p.kbpt);
+        const int rt = tile / p.tok_tiles;
+        g = rt / p.rtpg;
+        row0 = (rt % p.rtpg) * BM;
+        tok0 = (tile % p.tok_tiles) * BN;
+      };
+      // weights of the first ring slots depend on nothing: stream them while
+      // the previous kernel finishes, then wait for it before the activations
+      const int n_pre = static_cast<int>(n_my < C::STAGES ? n_my : C::STAGES);
+      for (int i = 0; i < n_pre; ++i) {
+        int g, row0, tok0, kb;
+        coords(i, g, row0, tok0, kb);
+        mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+        tma_load_2d_hint(sA + i * C::A_BYTES, &wm.m[g], &full[i], kb * BK, row0, pol_w);
       }
-      grid_dep_launch();
+      grid_dep_wait();
+      for (int i = 0; i < n_pre; ++i) {
+        int g, row0, tok0, kb;
+        coords(i, g, row0, tok0, kb);
+        tma_load_2d(sB + i * C::B_BYTES, &tmX, &full[i], kb * BK, tok0);
+        if (SPLIT) tma_load_2d(sBl + i * C::B_BYTES, &tmXlo, &full[i], kb * BK, tok0);
+      }
+      uint32_t stage = n_pre % C::STAGES, phase = (n_pre == C::STAGES) ? 1u : 0u;
+      long long issued = n_pre;
+      bool ok = true;
+      for (long long i = n_pre; i < n_my; ++i) {
+        int g, row0, tok0, kb;
+        coords(i, g, row0, tok0, kb);
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+        tma_load_2d_hint(sA + stage * C::A_BYTES, &wm.m[g], &full[stage], kb * BK, row0, pol_w);
+        tma_load_2d(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * BK, tok0);
+        if (SPLIT) tma_load_2d(sBl + stage * C::B_BYTES, &tmXlo, &full[stage], kb * BK, tok0);
+        ++issued;
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
       if (!ok) {
         report(p.status, DFLASH_ERR_TIMEOUT);
         *abort_flag = 1;
@@ -289,6 +315,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int q = warp & 3;              // TMEM lane quarter of this warp
     const int r = q * 32 + lane;         // weight row within the tile
     const int et = threadIdx.x - 64;     // 0..127
+    grid_dep_wait();                     // outputs / scratch are shared with the previous kernel
     int seg = 0;
     for (long long it = begin; it < end; ++seg) {
       const int tile = static_cast<int>(it / p.kbpt);
@@ -303,14 +330,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         break;
       }
       tc_fence_after();
-      const int n = (tile / p.tok_tiles) * BM + r;
+      const int rt = tile / p.tok_tiles;
+      const int n = (rt % p.rtpg) * BM + r;                       // row within its group
+      const size_t goff = static_cast<size_t>(rt / p.rtpg) * p.out_gstride;
       const int tok0 = (tile % p.tok_tiles) * BN;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
       float v[16];
       if (kb0 == 0 && kb1 == p.kbpt) {
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
-          finalize(p, v, n, tok0 + c * 16);
+          finalize(p, v, n, tok0 + c * 16, goff);
         }
         tc_fence_before();
         __syncwarp();
@@ -350,7 +379,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[i] += __ldcg(&Q[(c * 16 + i) * BM + r]);
             }
-            finalize(p, v, n, tok0 + c * 16);
+            finalize(p, v, n, tok0 + c * 16, goff);
           }
         }
         epi_bar();
@@ -366,7 +395,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 template <int BN, bool SPLIT>
-int launch(const Launch &lc, const CUtensorMap &tW, const CUtensorMap &tX, const CUtensorMap &tXl, const Params &p) {
+int launch(const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const CUtensorMap &tXl, const Params &p) {
   static bool attr_done = false;
   if (!attr_done) {
     if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, SPLIT>,
@@ -389,7 +418,7 @@ int launch(const Launch &lc, const CUtensorMap &tW, const CUtensorMap &tX, const
 }
 
 template <bool SPLIT>
-int launch_bn(int BN, const Launch &lc, const CUtensorMap &tW, const CUtensorMap &tX, const CUtensorMap &tXl,
+int launch_bn(int BN, const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const CUtensorMap &tXl,
               const Params &p) {
   switch (BN) {
     case 16: return launch<16, SPLIT>(lc, tW, tX, tXl, p);
@@ -406,7 +435,7 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   const int M = op.M, N = op.N, K = op.K;
   const char *name = op.name;
   if (M <= 0 || N <= 0 || K <= 0) return DFLASH_OK;
-  if (!op.W || !op.X || !op.out) return set_error(DFLASH_ERR_ARG, "gemm %s: null operand", name);
+  if ((!op.W && op.n_groups <= 1) || !op.X || !op.out) return set_error(DFLASH_ERR_ARG, "gemm %s: null operand", name);
   const uintptr_t al = reinterpret_cast<uintptr_t>(op.W) | reinterpret_cast<uintptr_t>(op.X) |
                        reinterpret_cast<uintptr_t>(op.X_lo);
   if ((al & 15) || (op.ldw * 2) % 16 || (op.ldx * 2) % 16)
@@ -422,10 +451,14 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   p.M = M;
   p.N = N;
   p.K = K;
+  p.n_groups = op.n_groups > 1 ? op.n_groups : 1;
+  if (p.n_groups > MAX_GROUPS || (p.n_groups > 1 && N % BM))
+    return set_error(DFLASH_ERR_UNSUPPORTED, "gemm %s: at most %d groups of a multiple of %d rows", name, MAX_GROUPS, BM);
+  p.rtpg = (N + BM - 1) / BM;
+  p.out_gstride = op.out_gstride;
   p.tok_tiles = (M + BN - 1) / BN;
-  const int row_tiles = (N + BM - 1) / BM;
   p.kbpt = (K + BK - 1) / BK;
-  const long long tiles = static_cast<long long>(row_tiles) * p.tok_tiles;
+  const long long tiles = static_cast<long long>(p.rtpg) * p.n_groups * p.tok_tiles;
   p.total = tiles * p.kbpt;
   const int cap = lc.gemm_ctas > 0 ? lc.gemm_ctas : lc.num_sms;
   p.G = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, (p.total + 3) / 4)));
@@ -443,10 +476,15 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   p.timeout_ns = lc.timeout_ns;
   if (tiles > sc.n_counters || static_cast<size_t>(p.G) * 2 * BM * BN > sc.partial_floats)
     return set_error(DFLASH_ERR_SHAPE, "gemm %s: workspace too small for %lld tiles", name, tiles);
-  CUtensorMap tW, tX, tXl;
-  if (int e = make_tmap_2d(&tW, op.W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, static_cast<uint64_t>(op.ldw) * 2,
-                           BK, BM))
-    return e;
+  WMaps tW;
+  CUtensorMap tX, tXl;
+  for (int g = 0; g < p.n_groups; ++g) {
+    const void *Wg = p.n_groups > 1 ? op.Wg[g] : op.W;
+    if (!Wg) return set_error(DFLASH_ERR_ARG, "gemm %s: null weight group %d", name, g);
+    if (int e = make_tmap_2d(&tW.m[g], Wg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N,
+                             static_cast<uint64_t>(op.ldw) * 2, BK, BM))
+      return e;
+  }
   if (int e = make_tmap_2d(&tX, op.X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M, static_cast<uint64_t>(op.ldx) * 2,
                            BK, BN))
     return e;
@@ -463,7 +501,8 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
                            : epi == EPI_F32_SPLIT                    ? 8.0 * M * N
                            : epi == EPI_SWIGLU                       ? (op.out_lo ? 2.0 : 1.0) * M * N
                                                                      : (op.out_lo ? 4.0 : 2.0) * M * N;
-  ProfScope ps(lc, name, 2.0 * N * K + xb + out_bytes, (split ? 4.0 : 2.0) * M * N * K);
+  const double ng = p.n_groups;
+  ProfScope ps(lc, name, ng * (2.0 * N * K + out_bytes) + xb, ng * (split ? 4.0 : 2.0) * M * N * K);
   return split ? launch_bn<true>(BN, lc, tW, tX, tXl, p) : launch_bn<false>(BN, lc, tW, tX, tXl, p);
 }
 

@@ -41,6 +41,11 @@ struct GemmOp {
   int ldo2 = 0;
   const float *bias = nullptr;
   const char *name = "gemm";
+  // grouped launch: n_groups weight matrices Wg[g] of the same shape applied
+  // to the same activations, output g at out + g * out_gstride elements
+  int n_groups = 1;
+  const void *Wg[16] = {};
+  size_t out_gstride = 0;
 };
 
 // Per-launch timing of kernel families (dflash_profile_begin / _end).

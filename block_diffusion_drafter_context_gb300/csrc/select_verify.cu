@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(256) pair_scores_kernel(const int32_t *anchor,
                                                           const float *topk_logits, const T *hfinal, int H,
                                                           const T *e256, const T *A, const T *Bm, int r, int E,
                                                           const float *w_g, float b_g, float *scores) {
-  grid_dep_wait();
+  pdl_start();
   extern __shared__ float sh[];
   float *se = sh;                  // [32][E]: rows 0..15 previous, 16..31 current
   float *su = se + 32 * E;         // [16][r]
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(256) pair_scores_kernel(const int32_t *anchor,
 
 // one warp per request; lanes 0..15 are the candidates of the current position
 __global__ void greedy_kernel(const float *scores, const int32_t *topk_ids, int B, int use_scores, int32_t *draft) {
-  grid_dep_wait();
+  pdl_start();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (b >= B) return;
   int prev = 0;
@@ -108,7 +108,7 @@ __global__ void greedy_kernel(const float *scores, const int32_t *topk_ids, int 
 
 __global__ void verify_kernel(const int32_t *draft, const int32_t *target, int B, int32_t *accept, int32_t *bonus,
                               int32_t *committed) {
-  grid_dep_wait();
+  pdl_start();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   int k = 0;
@@ -144,14 +144,14 @@ int pair_scores(const Launch &lc, bool f32, const int32_t *anchor, const int32_t
   if (f32) {
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(pair_scores_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    pair_scores_kernel<float><<<grid, 256, smem, lc.stream>>>(
+    launch_pdl(pair_scores_kernel<float>, dim3(grid), dim3(256), smem, lc.stream,
         anchor, topk_ids, topk_logits, static_cast<const float *>(final_hidden), H, static_cast<const float *>(e256),
         static_cast<const float *>(sel_a), static_cast<const float *>(sel_b), r, E, w_g, b_g, scores);
   } else {
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(pair_scores_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
-    pair_scores_kernel<__nv_bfloat16><<<grid, 256, smem, lc.stream>>>(
+    launch_pdl(pair_scores_kernel<__nv_bfloat16>, dim3(grid), dim3(256), smem, lc.stream,
         anchor, topk_ids, topk_logits, static_cast<const __nv_bfloat16 *>(final_hidden), H,
         static_cast<const __nv_bfloat16 *>(e256), static_cast<const __nv_bfloat16 *>(sel_a),
         static_cast<const __nv_bfloat16 *>(sel_b), r, E, w_g, b_g, scores);
@@ -163,7 +163,7 @@ int greedy_path(const Launch &lc, const float *scores, const int32_t *topk_ids, 
                 int32_t *draft) {
   if (B <= 0) return DFLASH_OK;
   ProfScope ps(lc, "greedy_path", -1.0, -1.0);
-  greedy_kernel<<<(B + 3) / 4, 128, 0, lc.stream>>>(scores, topk_ids, B, use_scores ? 1 : 0, draft);
+  launch_pdl(greedy_kernel, dim3((B + 3) / 4), dim3(128), 0, lc.stream, scores, topk_ids, B, use_scores ? 1 : 0, draft);
   return cuda_check(cudaGetLastError(), "greedy launch");
 }
 
@@ -171,12 +171,12 @@ int verify(const Launch &lc, const int32_t *draft, const int32_t *target, int B,
            int32_t *committed) {
   if (B <= 0) return DFLASH_OK;
   ProfScope ps(lc, "verify", -1.0, -1.0);
-  verify_kernel<<<(B + 127) / 128, 128, 0, lc.stream>>>(draft, target, B, accept, bonus, committed);
+  launch_pdl(verify_kernel, dim3((B + 127) / 128), dim3(128), 0, lc.stream, draft, target, B, accept, bonus, committed);
   return cuda_check(cudaGetLastError(), "verify launch");
 }
 
 int wait_flag(const Launch &lc, const int32_t *flag) {
-  wait_flag_kernel<<<1, 1, 0, lc.stream>>>(flag, lc.status, lc.timeout_ns);
+  wait_flag_kernel<<<1, 1, 0, lc.stream>>>(flag, lc.status, lc.timeout_ns);   // ordinary launch: sees every earlier write
   return cuda_check(cudaGetLastError(), "wait_flag launch");
 }
 

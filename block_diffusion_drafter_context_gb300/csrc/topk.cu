@@ -57,7 +57,7 @@ __device__ __forceinline__ void offer(uint64_t &list, uint64_t &thr, uint64_t ke
 __global__ void __launch_bounds__(WARPS * 32) topk_kernel(const float *__restrict__ logits, int V, int chunk,
                                                           int nchunks, int32_t *ids, float *vals,
                                                           uint64_t *part, int *counters) {
-  grid_dep_wait();
+  pdl_start();
   __shared__ uint64_t sm[WARPS * K];
   __shared__ int last;
   const int row = blockIdx.y, c = blockIdx.x;
@@ -133,7 +133,7 @@ int topk16(const Launch &lc, const float *logits, int rows, int V, int32_t *ids,
   nch = (V + chunk - 1) / chunk;
   dim3 grid(nch, rows);
   ProfScope ps(lc, "topk16", 4.0 * rows * V, 0.0);
-  topk_kernel<<<grid, WARPS * 32, 0, lc.stream>>>(logits, V, chunk, nch, ids, vals, part_keys, counters);
+  launch_pdl(topk_kernel, dim3(grid), dim3(WARPS * 32), 0, lc.stream, logits, V, chunk, nch, ids, vals, part_keys, counters);
   return cuda_check(cudaGetLastError(), "topk launch");
 }
 
