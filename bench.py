@@ -98,6 +98,29 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
+# ---------------------------------------------------------------- multi-rank helpers
+def rank_requests(batch: int, world: int, rank: int) -> range:
+    """Contiguous shard of a batch of independent requests for one rank."""
+    lo = batch * rank // world
+    hi = batch * (rank + 1) // world
+    return range(lo, hi)
+
+
+def max_over_ranks(ms: float, dist=None, device=None) -> float:
+    """Slowest rank's time (the job's time): all-reduce MAX when distributed."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_blocks_per_s(world: int, batch_per_rank: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank's blocks over the slowest rank's time."""
+    return world * batch_per_rank * steps / (max_ms * 1e-3)
+
+
 # ---------------------------------------------------------------- CPU oracle
 def oracle_setup(wl, W, ctx, X_prefill, cu):
     import oracle as O
@@ -264,11 +287,8 @@ def run_ours(args, wl):
             fn()
         e1.record()
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
+        ms = max_over_ranks(e0.elapsed_time(e1), dist if world > 1 else None, dev)
         if world > 1:
-            t = torch.tensor([ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
             dist.barrier()
         return ms
 
@@ -344,7 +364,7 @@ def run_ours(args, wl):
     att_gbs = kv_bytes_step / (att_ms * 1e-3) / 1e9 if att_ms > 0 else None
     total_ms_inst = sum(s["ms"] for s in stats) / args.steps
     step_ms = ms / args.steps
-    blocks = world * B * args.steps / (ms * 1e-3)
+    blocks = aggregate_blocks_per_s(world, B, args.steps, ms)
     exp_k = 0.0
     run_p = 1.0
     for q in wl.p_accept:
@@ -389,7 +409,7 @@ def run_ours(args, wl):
         "instrumented_ms_per_step": total_ms_inst,
         "eager_ms_per_step": ms_eager / args.steps,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * B * args.steps / (ms_e2e * 1e-3), "unit": "blocks/s",
+        "e2e": {"value": aggregate_blocks_per_s(world, B, args.steps, ms_e2e), "unit": "blocks/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "launches_per_step": launches / args.steps,
