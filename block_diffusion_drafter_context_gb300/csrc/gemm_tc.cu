@@ -205,37 +205,62 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const long long n_my = end - begin;
-      auto coords = [&](long long i, int &g, int &row0, int &tok0, int &kb) {
-        const long long it = begin + i;
-        const int tile = static_cast<int>(it / p.kbpt);
-        kb = static_cast<int>(it % p.kbpt);
+      // iteration -> (group, weight row, token row, k-block), advanced
+      // incrementally: no integer division in the issue loop
+      struct Iter {
+        int kb, tok, rtin, g;
+      };
+      Iter it0;
+      {
+        const int tile = static_cast<int>(begin / p.kbpt);
+        it0.kb = static_cast<int>(begin - static_cast<long long>(tile) * p.kbpt);
         const int rt = tile / p.tok_tiles;
-        g = rt / p.rtpg;
-        row0 = (rt % p.rtpg) * BM;
-        tok0 = (tile % p.tok_tiles) * BN;
+        it0.tok = tile - rt * p.tok_tiles;
+        it0.g = rt / p.rtpg;
+        it0.rtin = rt - it0.g * p.rtpg;
+      }
+      auto advance = [&](Iter &q) {
+        if (++q.kb == p.kbpt) {
+          q.kb = 0;
+          if (++q.tok == p.tok_tiles) {
+            q.tok = 0;
+            if (++q.rtin == p.rtpg) {
+              q.rtin = 0;
+              ++q.g;
+            }
+          }
+        }
+      };
+      auto coords = [&](const Iter &q, int &g, int &row0, int &tok0, int &kb) {
+        g = q.g;
+        row0 = q.rtin * BM;
+        tok0 = q.tok * BN;
+        kb = q.kb;
       };
       // weights of the first ring slots depend on nothing: stream them while
       // the previous kernel finishes, then wait for it before the activations
       const int n_pre = static_cast<int>(n_my < C::STAGES ? n_my : C::STAGES);
-      for (int i = 0; i < n_pre; ++i) {
+      Iter q = it0;
+      for (int i = 0; i < n_pre; ++i, advance(q)) {
         int g, row0, tok0, kb;
-        coords(i, g, row0, tok0, kb);
+        coords(q, g, row0, tok0, kb);
         mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
         tma_load_2d_hint(sA + i * C::A_BYTES, &wm.m[g], &full[i], kb * BK, row0, pol_w);
       }
       grid_dep_wait();
-      for (int i = 0; i < n_pre; ++i) {
+      q = it0;
+      for (int i = 0; i < n_pre; ++i, advance(q)) {
         int g, row0, tok0, kb;
-        coords(i, g, row0, tok0, kb);
+        coords(q, g, row0, tok0, kb);
         tma_load_2d(sB + i * C::B_BYTES, &tmX, &full[i], kb * BK, tok0);
         if (SPLIT) tma_load_2d(sBl + i * C::B_BYTES, &tmXlo, &full[i], kb * BK, tok0);
       }
       uint32_t stage = n_pre % C::STAGES, phase = (n_pre == C::STAGES) ? 1u : 0u;
       long long issued = n_pre;
       bool ok = true;
-      for (long long i = n_pre; i < n_my; ++i) {
+      for (long long i = n_pre; i < n_my; ++i, advance(q)) {
         int g, row0, tok0, kb;
-        coords(i, g, row0, tok0, kb);
+        coords(q, g, row0, tok0, kb);
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
