@@ -28,7 +28,7 @@ constexpr int CH = 64;            // tokens per stage (= one KV page)
 constexpr int HD = 128;           // head dim of the bf16 path
 constexpr int HALF = CH * 64 * 2; // one 64-dim half of a 64-token tile, bytes
 constexpr int TILE = 2 * HALF;    // K or V tile of one stage
-constexpr int ST = 4;             // pipeline depth
+constexpr int ST = 3;             // pipeline depth (3 x 32 KB: fits beside a GEMM CTA on one SM)
 constexpr int BLK = 16;           // block tokens
 constexpr int SMEM = 1024 + ST * 2 * TILE + 128;
 

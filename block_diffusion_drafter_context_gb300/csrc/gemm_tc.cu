@@ -46,8 +46,14 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES * (SPLIT ? 2 : 1);
-  static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+  // Small token tiles (weight streaming): ~100 KB of ring, so two GEMM CTAs
+  // fit on one SM and, under programmatic dependent launch, the next GEMM's
+  // CTAs become resident and stream their weights while this one drains
+  // (152 x 5 stages in flight still exceed what HBM needs in flight).  Large
+  // token tiles (tensor-bound): one CTA per SM with a deeper ring.
+  static constexpr int BUDGET = (BN <= 32 ? 100 : 200) * 1024;
+  static constexpr int STAGES_RAW = BUDGET / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : (STAGES_RAW < 2 ? 2 : STAGES_RAW);
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
 };
@@ -107,10 +113,16 @@ __device__ __forceinline__ void finalize(const Params &p, const float (&v)[16], 
         if (nok && tok0 + i < p.M) o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] = v[i];
     } break;
     case EPI_ADD_F32: {
+      // all 16 residual loads first (independent), then the adds and stores:
+      // no chain of read-modify-write round trips
       float *o = static_cast<float *>(p.out);
+      float r[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        if (nok && tok0 + i < p.M) o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] += v[i];
+        r[i] = (nok && tok0 + i < p.M) ? __ldcg(o + goff + static_cast<size_t>(tok0 + i) * p.ldo + n) : 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (nok && tok0 + i < p.M) o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] = r[i] + v[i];
     } break;
     case EPI_SWIGLU: {
       __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out), *ol = static_cast<__nv_bfloat16 *>(p.out_lo);
