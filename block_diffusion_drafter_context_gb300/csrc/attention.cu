@@ -8,10 +8,13 @@
 // bf16 path - split-KV, decode style, HBM-bound:
 //   grid (split, kv head, request); one CTA handles the 16 queries x g query
 //   heads that share one KV head, over one contiguous range of the context.
-//   Warp 0 streams 64-token KV pages into a 4-deep shared-memory ring with TMA
-//   (128-byte swizzle, so ldmatrix reads are conflict-free); each of the g
-//   consumer warps owns one query head (16 rows) and runs QK^T and PV on
-//   mma.sync bf16 tensor cores with an online (exp2-domain) softmax.  The last
+//   Warp 0 streams 64-token KV pages into a 3-deep shared-memory ring with TMA
+//   (128-byte swizzle, so ldmatrix reads are conflict-free).  The consumers
+//   are NG groups of g warps; group i takes chunks i, i+NG, ...; inside a
+//   group each warp owns one query head (16 rows) and runs QK^T and PV on
+//   mma.sync bf16 tensor cores with an online (exp2-domain) softmax, so NG
+//   chunks are in flight per CTA; groups merge their softmax states in shared
+//   memory at the end.  The last
 //   split also covers the 16 block keys.  Splits write unnormalised partials
 //   plus (max, sum); the CTA that finishes a (request, head) last merges them
 //   in split order - deterministic, no spin-waits.
@@ -33,6 +36,7 @@ constexpr int BLK = 16;           // block tokens
 constexpr int SMEM = 1024 + ST * 2 * TILE + 128;
 
 struct Params {
+  int ng;                  // consumer groups
   const __nv_bfloat16 *q;
   int ldq;
   __nv_bfloat16 *out;
@@ -64,7 +68,7 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t v, int tok, int valid) {
   return (tok < valid ? (v & 0xFFFFu) : 0u) | (tok + 1 < valid ? (v & 0xFFFF0000u) : 0u);
 }
 
-__global__ void __launch_bounds__(32 * 9, 1)
+__global__ void __launch_bounds__(32 * 11, 1)
     attn_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmBK, const __grid_constant__ CUtensorMap tmBV,
                      const Params p) {
@@ -164,7 +168,9 @@ __global__ void __launch_bounds__(32 * 9, 1)
   }
 
   // -------------------------------------------------------------- consumers
-  const int w = warp - 1;                 // query head within the group
+  const int cw = warp - 1;                // consumer warp
+  const int grp = cw / g;                 // chunk group
+  const int w = cw % g;                   // query head within the group
   const int hq = h * g + w;
   const int gr = lane >> 2, t2 = (lane & 3) * 2;
   const int mi = lane >> 3, rr = lane & 7;
@@ -187,9 +193,10 @@ __global__ void __launch_bounds__(32 * 9, 1)
   for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   bool failed = false;
-  uint32_t stage = 0, phase = 0;
 
-  for (int ci = 0; ci < nchunks; ++ci) {
+  for (int ci = grp; ci < nchunks; ci += p.ng) {
+    const int stage = ci % ST;
+    const uint32_t phase = static_cast<uint32_t>((ci / ST) & 1);
     if (!mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns)) {
       failed = true;
       break;
@@ -273,10 +280,6 @@ __global__ void __launch_bounds__(32 * 9, 1)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
-    if (++stage == ST) {
-      stage = 0;
-      phase ^= 1u;
-    }
   }
 
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
@@ -284,11 +287,50 @@ __global__ void __launch_bounds__(32 * 9, 1)
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-  const int nthr = 32 * g;
-  if (bar_or(2, nthr, failed || *abort_flag)) {
+  // ---- merge the groups' softmax states (all chunks are consumed, so the
+  // stage buffers are free for the exchange)
+  if (bar_or(3, 32 * g * p.ng, failed || *abort_flag)) {
     if (threadIdx.x == 32) report(p.status, DFLASH_ERR_TIMEOUT);
     return;
   }
+  if (p.ng > 1) {
+    float *xs = reinterpret_cast<float *>(base);
+    if (grp > 0) {
+      float *dst = xs + (static_cast<size_t>((grp - 1) * g + w) * 32 + lane) * 68;
+#pragma unroll
+      for (int nd = 0; nd < 16; ++nd) {
+        dst[nd * 4 + 0] = o[nd][0];
+        dst[nd * 4 + 1] = o[nd][1];
+        dst[nd * 4 + 2] = o[nd][2];
+        dst[nd * 4 + 3] = o[nd][3];
+      }
+      dst[64] = m0;
+      dst[65] = m1;
+      dst[66] = l0;
+      dst[67] = l1;
+    }
+    asm volatile("bar.sync 3, %0;" ::"r"(32 * g * p.ng) : "memory");
+    if (grp > 0) return;
+    for (int og = 1; og < p.ng; ++og) {
+      const float *src = xs + (static_cast<size_t>((og - 1) * g + w) * 32 + lane) * 68;
+      const float mb0 = src[64], mb1 = src[65];
+      const float M0 = fmaxf(m0, mb0), M1 = fmaxf(m1, mb1);
+      const float a0 = fast_exp2(m0 - M0), b0 = fast_exp2(mb0 - M0);
+      const float a1 = fast_exp2(m1 - M1), b1 = fast_exp2(mb1 - M1);
+      l0 = l0 * a0 + src[66] * b0;
+      l1 = l1 * a1 + src[67] * b1;
+#pragma unroll
+      for (int nd = 0; nd < 16; ++nd) {
+        o[nd][0] = o[nd][0] * a0 + src[nd * 4 + 0] * b0;
+        o[nd][1] = o[nd][1] * a0 + src[nd * 4 + 1] * b0;
+        o[nd][2] = o[nd][2] * a1 + src[nd * 4 + 2] * b1;
+        o[nd][3] = o[nd][3] * a1 + src[nd * 4 + 3] * b1;
+      }
+      m0 = M0;
+      m1 = M1;
+    }
+  }
+  const int nthr = 32 * g;   // group 0 carries on
 
   if (nsplit == 1) {
     const size_t o0 = static_cast<size_t>(b * BLK + gr) * p.ldo + hq * HD;
@@ -464,6 +506,7 @@ int attention_bf16(const Launch &lc, const AttnArgs &a) {
   if (int e = make_tmap_2d(&tBK, a.bk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, HD, blk_rows, HD * 2, 64, BLK)) return e;
   if (int e = make_tmap_2d(&tBV, a.bv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, HD, blk_rows, HD * 2, 64, BLK)) return e;
   Params p = {};
+  p.ng = (1 + 2 * g) * 32 <= 352 ? 2 : 1;
   p.q = static_cast<const __nv_bfloat16 *>(a.q);
   p.ldq = a.nq * HD;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
@@ -485,7 +528,7 @@ int attention_bf16(const Launch &lc, const AttnArgs &a) {
   p.timeout_ns = lc.timeout_ns;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.max_splits, a.nkv, a.B);
-  cfg.blockDim = dim3(32 * (g + 1));
+  cfg.blockDim = dim3(32 * (1 + p.ng * g));
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = lc.stream;
   cudaLaunchAttribute attr[1];
