@@ -72,7 +72,7 @@ struct Params {
   void *out2, *out2_lo;
   int ldo2;
   const float *bias;
-  float *partials;     // [G][2][BM*BN]
+  float *partials;     // [G][2][BM][BN] row-major shares
   int *counters;       // [tiles]
   int *status;
   unsigned long long timeout_ns;
@@ -382,39 +382,70 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
       } else {
+        // partial tile: this CTA's fp32 share goes to its slot, row-major
+        // (each thread writes its row's BN columns as float4); the CTA that
+        // completes the tile's k-range sums all shares in CTA order
         const int slot = (tile == first_tile) ? 0 : 1;
-        float *P = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * (BM * BN);
+        float *P = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * (BM * BN) + static_cast<size_t>(r) * BN;
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
+          float4 *P4 = reinterpret_cast<float4 *>(P + c * 16);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) __stcg(&P[(c * 16 + i) * BM + r], v[i]);
+          for (int i = 0; i < 4; ++i) __stcg(P4 + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
-        __threadfence();
-        epi_bar();
+        epi_bar();   // every share of this CTA is written ...
         if (et == 0) {
+          __threadfence();   // ... and, through the barrier, visible before the count moves
           const int nk = kb1 - kb0;
           const int old = atomicAdd(&p.counters[tile], nk);
           const int last = (old + nk == p.kbpt) ? 1 : 0;
-          if (last) p.counters[tile] = 0;   // self-cleaning for the next launch
+          if (last) {
+            p.counters[tile] = 0;   // self-cleaning for the next launch
+            __threadfence();
+          }
           *bcast = last;
-          __threadfence();
         }
         epi_bar();
         if (*bcast) {
           const long long t_beg = static_cast<long long>(tile) * p.kbpt;
           const int c_lo = cta_of(t_beg, p.total, p.G);
           const int c_hi = cta_of(t_beg + p.kbpt - 1, p.total, p.G);
+          // only the first contributor can have started in an earlier tile
+          const int slot_lo = range_begin(p.total, p.G, c_lo) < t_beg ? 1 : 0;
           for (int c = 0; c < BN / 16; ++c) {
+            float4 acc[4];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0.f;
-            for (int cc = c_lo; cc <= c_hi; ++cc) {
-              const int ft = static_cast<int>(range_begin(p.total, p.G, cc) / p.kbpt);
-              const float *Q = p.partials + (static_cast<size_t>(cc) * 2 + (ft == tile ? 0 : 1)) * (BM * BN);
+            for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int cc0 = c_lo; cc0 <= c_hi; cc0 += 4) {
+              float4 t[4][4];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] += __ldcg(&Q[(c * 16 + i) * BM + r]);
+              for (int u = 0; u < 4; ++u) {   // up to 4 contributors' loads in flight
+                const int cc = cc0 + u;
+                const float4 *Q4 = reinterpret_cast<const float4 *>(
+                    p.partials + (static_cast<size_t>(cc) * 2 + (cc == c_lo ? slot_lo : 0)) * (BM * BN) +
+                    static_cast<size_t>(r) * BN + c * 16);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) t[u][i] = cc <= c_hi ? __ldcg(Q4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u)   // summed in contributor order: deterministic
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  acc[i].x += t[u][i].x;
+                  acc[i].y += t[u][i].y;
+                  acc[i].z += t[u][i].z;
+                  acc[i].w += t[u][i].w;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              v[4 * i] = acc[i].x;
+              v[4 * i + 1] = acc[i].y;
+              v[4 * i + 2] = acc[i].z;
+              v[4 * i + 3] = acc[i].w;
             }
             finalize(p, v, n, tok0 + c * 16, goff);
           }
