@@ -126,11 +126,10 @@ namespace {
 
 constexpr int GEMM_COUNTERS = 1 << 16;
 constexpr int GEMM_MAX_BN = 256;
-constexpr int ATTN_SLOTS = 4096;
 constexpr int TOPK_MAX_CHUNKS = 64;
 
 struct Layout {
-  size_t status, gemm_ctr, gemm_part, attn_ctr, attn_o, attn_ml, topk_ctr, topk_part;
+  size_t status, gemm_ctr, gemm_part, topk_ctr, topk_part;
   size_t x, u, u2, qkv, q, bk, bv, o, ysub, coef, hmid, hmask, hfinal, logits, scores;
   size_t u_lo, u2_lo, o_lo, ysub_lo, hmid_lo, hmask_lo, ysub32;
   size_t fc, f, f_lo, kvproj, ctx_saved;
@@ -142,7 +141,7 @@ Layout layout(const dflash_ctx *c, int B, int Tn) {
   const dflash_config &g = c->cfg;
   const size_t te = g.dtype == DFLASH_F32 ? 4 : 2;
   const size_t H = g.hidden, d = g.head_dim, nq = g.n_q_heads, nkv = g.n_kv_heads, F = g.ffn, V = g.vocab;
-  const size_t R = static_cast<size_t>(B) * 16, gq = nq / nkv;
+  const size_t R = static_cast<size_t>(B) * 16;
   Layout L = {};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -154,9 +153,6 @@ Layout layout(const dflash_ctx *c, int B, int Tn) {
   L.gemm_ctr = take(sizeof(int) * GEMM_COUNTERS);
   L.gemm_part_floats = static_cast<size_t>(c->num_sms) * 2 * 128 * GEMM_MAX_BN;
   L.gemm_part = take(4 * L.gemm_part_floats);
-  L.attn_ctr = take(sizeof(int) * static_cast<size_t>(B) * nkv);
-  L.attn_o = take(4ull * ATTN_SLOTS * 16 * gq * 128);
-  L.attn_ml = take(4ull * ATTN_SLOTS * 16 * gq * 2);
   L.topk_ctr = take(sizeof(int) * static_cast<size_t>(B) * 15);
   L.topk_part = take(8ull * B * 15 * TOPK_MAX_CHUNKS * 16);
   L.x = take(4 * R * H);
@@ -164,8 +160,8 @@ Layout layout(const dflash_ctx *c, int B, int Tn) {
   L.u2 = take(te * R * H);
   L.qkv = take(4 * R * (nq + 2 * nkv) * d);
   L.q = take(te * R * nq * d);
-  L.bk = take(te * R * nkv * d);
-  L.bv = take(te * R * nkv * d);
+  L.bk = take(te * B * nkv * 64 * d);   // block K [B][nkv][64][d], rows 16.. zero
+  L.bv = take(te * B * nkv * 64 * d);   // block V^T [B][nkv][d][64], cols 16.. zero
   L.o = take(te * R * nq * d);
   L.ysub = take(te * R * H);
   L.coef = take(4 * R * (H / 8));
@@ -427,26 +423,23 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
   void *hfinal = final_hidden ? final_hidden : at<void>(ws, L.hfinal);
   float *lg = logits ? logits : at<float>(ws, L.logits);
 
-  // split-KV plan: enough CTAs to cover the SMs twice, at most ATTN_SLOTS
-  // partial slots, splits of at most 4096 tokens when that fits
+  // split-KV plan: the S splits of one (request, kv head) form a thread-block
+  // cluster (S = 1, 2, 4 or 8) and merge on chip; S grows until the grid covers
+  // the SMs and no split holds more than 16 pages (load balance on ragged
+  // batches)
   const int max_ctx = kv->max_pages * g.page_size;
-  int split_tok = ctx->attn_split;
-  if (split_tok <= 0) {
-    const int bh = B * nkv;
-    int want = (ctx->num_sms + bh - 1) / bh;
-    split_tok = (max_ctx + want - 1) / want;
-    split_tok = split_tok < 256 ? 256 : split_tok;
-    split_tok = split_tok > 4096 ? 4096 : split_tok;
-    split_tok = (split_tok + 63) / 64 * 64;
+  const int max_chunks = (max_ctx + 63) / 64 + 1;
+  int max_splits = 1;
+  if (ctx->attn_split > 0) {
+    const int want = (max_ctx + ctx->attn_split - 1) / ctx->attn_split;
+    while (max_splits < 8 && max_splits < want) max_splits *= 2;
+  } else {
+    while (max_splits < 8 && (static_cast<long long>(B) * nkv * max_splits < ctx->num_sms ||
+                              max_chunks / max_splits > 16))
+      max_splits *= 2;
   }
-  int max_splits = (max_ctx + split_tok - 1) / split_tok;
-  if (max_splits < 1) max_splits = 1;
-  if (static_cast<long long>(max_splits) * B * nkv > ATTN_SLOTS) {
-    max_splits = ATTN_SLOTS / (B * nkv);
-    if (max_splits < 1) max_splits = 1;
-    split_tok = ((max_ctx + max_splits - 1) / max_splits + 63) / 64 * 64;
-    max_splits = (max_ctx + split_tok - 1) / split_tok;
-  }
+  int split_tok = ((max_ctx + max_splits - 1) / max_splits + 63) / 64 * 64;
+  if (split_tok < 64) split_tok = 64;
 
   const bool split = !f32 && g.split_act;
   auto lo = [&](size_t off) -> void * { return split ? at<void>(ws, off) : nullptr; };
@@ -506,9 +499,6 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     aa.ctx_len = ctx_len;
     aa.out = at<void>(ws, L.o);
     aa.out_lo = lo(L.o_lo);
-    aa.part_o = at<float>(ws, L.attn_o);
-    aa.part_ml = at<float>(ws, L.attn_ml);
-    aa.counters = at<int>(ws, L.attn_ctr);
     aa.B = B;
     aa.nq = nq;
     aa.nkv = nkv;

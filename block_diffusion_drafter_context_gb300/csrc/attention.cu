@@ -5,19 +5,25 @@
 // Metodologia 1: bidirectional in the block, all of the clean prefix, no
 // other block).
 //
-// bf16 path - split-KV, decode style, HBM-bound:
-//   grid (split, kv head, request); one CTA handles the 16 queries x g query
-//   heads that share one KV head, over one contiguous range of the context.
-//   Warp 0 streams 64-token KV pages into a 3-deep shared-memory ring with TMA
-//   (128-byte swizzle, so ldmatrix reads are conflict-free).  The consumers
-//   are NG groups of g warps; group i takes chunks i, i+NG, ...; inside a
-//   group each warp owns one query head (16 rows) and runs QK^T and PV on
-//   mma.sync bf16 tensor cores with an online (exp2-domain) softmax, so NG
-//   chunks are in flight per CTA; groups merge their softmax states in shared
-//   memory at the end.  The last
-//   split also covers the 16 block keys.  Splits write unnormalised partials
-//   plus (max, sum); the CTA that finishes a (request, head) last merges them
-//   in split order - deterministic, no spin-waits.
+// bf16 path - split-KV, decode style, HBM-bound, on the 5th-generation tensor
+// cores:
+//   grid (split, kv head, request); the S splits of one (request, kv head)
+//   form one thread-block cluster.  A CTA takes the 16 queries x g query
+//   heads sharing one KV head (16g rows, padded to the UMMA M of 128) over
+//   one contiguous range of the context, in 64-token chunks (one KV page):
+//     warp 0     TMA: Q once, then K and V^T pages into a 3-deep smem ring
+//                (128-byte swizzle; V pages are stored transposed so both
+//                products take K-major operands);
+//     warp 1     tcgen05.mma: S = Q K^T (M=128, N=64, K=128) into one of two
+//                TMEM buffers, then PV = P V (M=128, N=128, K=64) into TMEM;
+//     warps 2-5  one TMEM lane (= query row) per thread: online softmax in
+//                the exp2 domain on its 64 scores (no shuffles), P written
+//                back to smem in bf16 as the A operand of PV, O accumulated
+//                in registers.
+//   QK of chunk i+1 overlaps the softmax of chunk i.  The last split also
+//   covers the 16 block keys.  At the end the cluster's CTAs exchange
+//   (max, sum, O) through distributed shared memory and each finalises 16g/S
+//   rows: the split partials never leave the chip.
 // fp32 path - plain CUDA-core loop for the tiny fp32 configuration.
 #include "common.cuh"
 #include "internal.h"
@@ -27,35 +33,31 @@
 namespace dflash {
 namespace {
 
-constexpr int CH = 64;            // tokens per stage (= one KV page)
-constexpr int HD = 128;           // head dim of the bf16 path
-constexpr int HALF = CH * 64 * 2; // one 64-dim half of a 64-token tile, bytes
-constexpr int TILE = 2 * HALF;    // K or V tile of one stage
-constexpr int ST = 3;             // pipeline depth (3 x 32 KB: fits beside a GEMM CTA on one SM)
-constexpr int BLK = 16;           // block tokens
-constexpr int SMEM = 1024 + ST * 2 * TILE + 128;
+constexpr int CH = 64;                       // tokens per chunk (= one KV page)
+constexpr int HD = 128;                      // head dim of the bf16 path
+constexpr int ST = 3;                        // KV ring depth
+constexpr int BLK = 16;                      // block tokens
+constexpr int MROWS = 128;                   // UMMA M (query rows, padded)
+constexpr int Q_BYTES = MROWS * HD * 2;      // 32 KB: two 64-dim halves of [128][64]
+constexpr int K_BYTES = CH * HD * 2;         // 16 KB: two halves of [64 tok][64]
+constexpr int V_BYTES = HD * CH * 2;         // 16 KB: [128 d][64 tok]
+constexpr int P_BYTES = MROWS * CH * 2;      // 16 KB: [128 rows][64 tok]
+constexpr int SMEM = 1024 + Q_BYTES + ST * (K_BYTES + V_BYTES) + 2 * P_BYTES + 256;
+constexpr int NTHR = 192;
+constexpr int TMEM_COLS = 256;               // S x 2 (64 columns each) + PV (128 columns)
 
 struct Params {
-  int ng;                  // consumer groups
-  const __nv_bfloat16 *q;
-  int ldq;
   __nv_bfloat16 *out;
   __nv_bfloat16 *out_lo;   // low halves (split activations) or null
   int ldo;
   const int32_t *page_table;
   int max_pages, num_pages;
   const int32_t *ctx_len;
-  float *part_o, *part_ml;
-  int *counters;
-  int nkv, g, split, max_splits;
+  int nkv, g, split, S;
   float scale_log2;
   int *status;
   unsigned long long timeout_ns;
 };
-
-__device__ __forceinline__ uint32_t swz(uint32_t base, int tok, int dch) {
-  return base + (dch >> 3) * HALF + tok * 128 + ((((dch & 7) ^ (tok & 7))) << 4);
-}
 
 // two consecutive bf16 outputs (high halves) and, if lo is given, their low halves
 __device__ __forceinline__ void store2_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t i, float a, float b) {
@@ -64,27 +66,61 @@ __device__ __forceinline__ void store2_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, 
   if (lo) *reinterpret_cast<uint32_t *>(lo + i) = pack_bf16(a - __low2float(h), b - __high2float(h));
 }
 
-__device__ __forceinline__ uint32_t mask_pair(uint32_t v, int tok, int valid) {
-  return (tok < valid ? (v & 0xFFFFu) : 0u) | (tok + 1 < valid ? (v & 0xFFFF0000u) : 0u);
-}
-
-__global__ void __launch_bounds__(32 * 11, 1)
-    attn_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                     const __grid_constant__ CUtensorMap tmBK, const __grid_constant__ CUtensorMap tmBV,
-                     const Params p) {
+__global__ void __launch_bounds__(NTHR, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmBK,
+                   const __grid_constant__ CUtensorMap tmBV, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *base = smem_raw + pad;
-  uint8_t *sK = base;
-  uint8_t *sV = base + ST * TILE;
-  uint64_t *full = reinterpret_cast<uint64_t *>(base + 2 * ST * TILE);
-  uint64_t *empty = full + ST;
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + ST);
-  int *bcast = const_cast<int *>(abort_flag + 1);
+  uint8_t *sQ = base;
+  uint8_t *sK = sQ + Q_BYTES;
+  uint8_t *sV = sK + ST * K_BYTES;
+  uint8_t *sP = sV + ST * V_BYTES;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sP + 2 * P_BYTES);
+  uint64_t *qfull = bar, *full = bar + 1, *empty = full + ST, *sfull = empty + ST, *sempty = sfull + 2,
+           *pfull = sempty + 2, *ofull = pfull + 2, *oempty = ofull + 1, *drain = oempty + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = p.g;
+  const int g = p.g, R = BLK * g;
+
+  if (threadIdx.x == 0) {
+    mbar_init(qfull, 1);
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sempty[i], 4);
+      mbar_init(&pfull[i], 4);
+    }
+    mbar_init(ofull, 1);
+    mbar_init(oempty, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // query rows past 16g are padding: keep them zero so their scores stay finite
+  {
+    const int per_half = (MROWS - R) * 128 / 16;   // 16-byte chunks
+    for (int i = threadIdx.x; i < 2 * per_half; i += NTHR) {
+      const int half = i / per_half, k = i % per_half;
+      *reinterpret_cast<uint4 *>(sQ + half * (MROWS * 128) + R * 128 + k * 16) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  fence_proxy_async_smem();
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
   pdl_start();
   int n_ctx = p.ctx_len[b];
@@ -94,341 +130,277 @@ __global__ void __launch_bounds__(32 * 11, 1)
     n_ctx = n_ctx < 0 ? 0 : cap;
   }
   const int nsplit = n_ctx > 0 ? (n_ctx + p.split - 1) / p.split : 1;
-  if (s >= nsplit) return;   // uniform for the CTA
+  const bool active = s < nsplit;   // inactive CTAs still join the cluster merge
   const int t0 = s * p.split;
   const int t1 = min(n_ctx, t0 + p.split);
-  const int ctx_chunks = t1 > t0 ? (t1 - t0 + CH - 1) / CH : 0;
-  const bool has_block = (s == nsplit - 1);
+  const int ctx_chunks = (active && t1 > t0) ? (t1 - t0 + CH - 1) / CH : 0;
+  const bool has_block = active && (s == nsplit - 1);
   const int nchunks = ctx_chunks + (has_block ? 1 : 0);
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < ST; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], g);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
+  float O[HD];
+#pragma unroll
+  for (int i = 0; i < HD; ++i) O[i] = 0.f;
+  float m = -INFINITY, l = 0.f;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && nchunks > 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      uint32_t stage = 0, phase = 0;
+      mbar_arrive_expect_tx(qfull, g * 2 * BLK * 128);
+      for (int w = 0; w < g; ++w)
+        for (int half = 0; half < 2; ++half)
+          tma_load_2d(sQ + half * (MROWS * 128) + w * BLK * 128, &tmQ, qfull, (h * g + w) * HD + half * 64, b * BLK);
       int last_ci[ST];
       for (int i = 0; i < ST; ++i) last_ci[i] = -1;
       bool ok = true;
       for (int ci = 0; ci < nchunks; ++ci) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns)) {
+        const int st = ci % ST;
+        if (!mbar_wait(&empty[st], static_cast<uint32_t>(((ci / ST) & 1) ^ 1), abort_flag, p.timeout_ns)) {
           ok = false;
           break;
         }
-        uint8_t *dk = sK + stage * TILE, *dv = sV + stage * TILE;
+        uint8_t *dk = sK + st * K_BYTES, *dv = sV + st * V_BYTES;
+        const CUtensorMap *mk = &tmBK, *mv = &tmBV;
+        int rowk = (b * p.nkv + h) * CH, rowv = (b * p.nkv + h) * HD;
         if (ci < ctx_chunks) {
           const int tok = t0 + ci * CH;
           const int page = p.page_table[static_cast<size_t>(b) * p.max_pages + tok / CH];
           if (page < 0 || page >= p.num_pages) {
             report(p.status, DFLASH_ERR_DEVICE);
-            mbar_arrive(&full[stage]);   // completes the phase with no data
-          } else {
-            const int row = (page * p.nkv + h) * CH;
-            mbar_arrive_expect_tx(&full[stage], 2 * TILE);
-            tma_load_2d(dk, &tmK, &full[stage], 0, row);
-            tma_load_2d(dk + HALF, &tmK, &full[stage], 64, row);
-            tma_load_2d(dv, &tmV, &full[stage], 0, row);
-            tma_load_2d(dv + HALF, &tmV, &full[stage], 64, row);
-            last_ci[stage] = ci;
+            mbar_arrive(&full[st]);   // completes the phase with no data
+            continue;
           }
-        } else {
-          const int row = (b * p.nkv + h) * BLK;
-          mbar_arrive_expect_tx(&full[stage], 4 * BLK * 128);
-          tma_load_2d(dk, &tmBK, &full[stage], 0, row);
-          tma_load_2d(dk + HALF, &tmBK, &full[stage], 64, row);
-          tma_load_2d(dv, &tmBV, &full[stage], 0, row);
-          tma_load_2d(dv + HALF, &tmBV, &full[stage], 64, row);
-          last_ci[stage] = ci;
+          mk = &tmK;
+          mv = &tmV;
+          rowk = (page * p.nkv + h) * CH;
+          rowv = (page * p.nkv + h) * HD;
         }
-        if (++stage == ST) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        mbar_arrive_expect_tx(&full[st], K_BYTES + V_BYTES);
+        tma_load_2d(dk, mk, &full[st], 0, rowk);
+        tma_load_2d(dk + K_BYTES / 2, mk, &full[st], 64, rowk);
+        tma_load_2d(dv, mv, &full[st], 0, rowv);
+        last_ci[st] = ci;
       }
       if (!ok) {
         report(p.status, DFLASH_ERR_TIMEOUT);
         *abort_flag = 1;
-        // let every issued copy land before shared memory is released
-        for (int i = 0; i < ST; ++i)
-          if (last_ci[i] >= 0)
-            mbar_wait(&full[i], static_cast<uint32_t>((last_ci[i] / ST) & 1), nullptr, p.timeout_ns);
+        for (int i = 0; i < ST; ++i)   // let every issued copy land before smem goes away
+          if (last_ci[i] >= 0) mbar_wait(&full[i], static_cast<uint32_t>((last_ci[i] / ST) & 1), nullptr, p.timeout_ns);
+        mbar_wait(qfull, 0, nullptr, p.timeout_ns);
       }
     }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int cw = warp - 1;                // consumer warp
-  const int grp = cw / g;                 // chunk group
-  const int w = cw % g;                   // query head within the group
-  const int hq = h * g + w;
-  const int gr = lane >> 2, t2 = (lane & 3) * 2;
-  const int mi = lane >> 3, rr = lane & 7;
-
-  uint32_t qa[8][4];
-  {
-    const __nv_bfloat16 *q0 = p.q + static_cast<size_t>(b * BLK + gr) * p.ldq + hq * HD;
-    const __nv_bfloat16 *q1 = q0 + 8 * static_cast<size_t>(p.ldq);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nchunks > 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(MROWS, CH);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(MROWS, HD);
+      const uint32_t pv_tmem = tmem + 128;
+      bool ok = mbar_wait(qfull, 0, abort_flag, p.timeout_ns);
+      auto issue_qk = [&](int ci) -> bool {
+        const int st = ci % ST, sb = ci & 1;
+        if (!mbar_wait(&full[st], static_cast<uint32_t>((ci / ST) & 1), abort_flag, p.timeout_ns)) return false;
+        if (!mbar_wait(&sempty[sb], static_cast<uint32_t>(((ci >> 1) & 1) ^ 1), abort_flag, p.timeout_ns)) return false;
+        tc_fence_after();
+        const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + st * K_BYTES);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      qa[kk][0] = *reinterpret_cast<const uint32_t *>(q0 + kk * 16 + t2);
-      qa[kk][1] = *reinterpret_cast<const uint32_t *>(q1 + kk * 16 + t2);
-      qa[kk][2] = *reinterpret_cast<const uint32_t *>(q0 + kk * 16 + 8 + t2);
-      qa[kk][3] = *reinterpret_cast<const uint32_t *>(q1 + kk * 16 + 8 + t2);
-    }
-  }
-
-  float o[16][4];
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tmem + sb * CH, sdesc_k_sw128(q0 + (kk >> 2) * (MROWS * 128) + (kk & 3) * 32),
+                    sdesc_k_sw128(k0 + (kk >> 2) * (K_BYTES / 2) + (kk & 3) * 32), idesc_qk, kk > 0 ? 1u : 0u);
+        umma_commit(&sfull[sb]);
+        return true;
+      };
+      auto issue_pv = [&](int ci) -> bool {
+        const int st = ci % ST, pb = ci & 1;
+        if (!mbar_wait(&pfull[pb], static_cast<uint32_t>((ci >> 1) & 1), abort_flag, p.timeout_ns)) return false;
+        if (!mbar_wait(oempty, static_cast<uint32_t>((ci & 1) ^ 1), abort_flag, p.timeout_ns)) return false;
+        tc_fence_after();
+        const uint32_t p0 = smem_u32(sP + pb * P_BYTES), v0 = smem_u32(sV + st * V_BYTES);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  bool failed = false;
-
-  for (int ci = grp; ci < nchunks; ci += p.ng) {
-    const int stage = ci % ST;
-    const uint32_t phase = static_cast<uint32_t>((ci / ST) & 1);
-    if (!mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns)) {
-      failed = true;
-      break;
-    }
-    const int valid = ci < ctx_chunks ? min(CH, t1 - (t0 + ci * CH)) : BLK;
-    const uint32_t kb = smem_u32(sK + stage * TILE), vb = smem_u32(sV + stage * TILE);
-
-    float sc[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(swz(kb, np * 16 + (mi >> 1) * 8 + rr, kk * 2 + (mi & 1)), b0, b1, b2, b3);
-        mma_bf16_16816(sc[2 * np], qa[kk], b0, b1);
-        mma_bf16_16816(sc[2 * np + 1], qa[kk], b2, b3);
+        for (int kk = 0; kk < CH / 16; ++kk)
+          umma_bf16(pv_tmem, sdesc_k_sw128(p0 + kk * 32), sdesc_k_sw128(v0 + kk * 32), idesc_pv, kk > 0 ? 1u : 0u);
+        umma_commit(ofull);
+        umma_commit(&empty[st]);   // PV is the last reader of this KV stage
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      for (int ci = 0; ci < nchunks && ok; ++ci) {
+        if (ci + 1 < nchunks) ok = issue_qk(ci + 1);
+        if (ok) ok = issue_pv(ci);
       }
+      if (!ok) {
+        report(p.status, DFLASH_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      umma_commit(drain);   // every issued MMA retires before TMEM is released
+      mbar_wait(drain, 0, nullptr, p.timeout_ns);
     }
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+  } else {
+    // ------------------------------------------------------------ softmax / O
+    const int q = warp & 3;
+    const int r = q * 32 + lane;            // query row = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    float alpha_pending = 1.f;
+    bool failed = false;
+    for (int ci = 0; ci < nchunks; ++ci) {
+      const int sb = ci & 1, pb = ci & 1;
+      if (!mbar_wait(&sfull[sb], static_cast<uint32_t>((ci >> 1) & 1), abort_flag, p.timeout_ns)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      float sc[CH];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const int tok = nt * 8 + t2;
-      sc[nt][0] = tok < valid ? sc[nt][0] * p.scale_log2 : -INFINITY;
-      sc[nt][1] = tok + 1 < valid ? sc[nt][1] * p.scale_log2 : -INFINITY;
-      sc[nt][2] = tok < valid ? sc[nt][2] * p.scale_log2 : -INFINITY;
-      sc[nt][3] = tok + 1 < valid ? sc[nt][3] * p.scale_log2 : -INFINITY;
-      mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    float rs0 = 0.f, rs1 = 0.f;
+      for (int c = 0; c < CH / 16; ++c) {
+        float v[16];
+        tmem_ld16(lane_base + sb * CH + c * 16, v);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      sc[nt][0] = fast_exp2(sc[nt][0] - mn0);
-      sc[nt][1] = fast_exp2(sc[nt][1] - mn0);
-      sc[nt][2] = fast_exp2(sc[nt][2] - mn1);
-      sc[nt][3] = fast_exp2(sc[nt][3] - mn1);
-      rs0 += sc[nt][0] + sc[nt][1];
-      rs1 += sc[nt][2] + sc[nt][3];
-    }
-    l0 = l0 * a0 + rs0;
-    l1 = l1 * a1 + rs1;
+        for (int i = 0; i < 16; ++i) sc[c * 16 + i] = v[i];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sempty[sb]);
+      const int valid = ci < ctx_chunks ? min(CH, t1 - (t0 + ci * CH)) : BLK;
+      float mx = -INFINITY;
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-      o[nd][0] *= a0;
-      o[nd][1] *= a0;
-      o[nd][2] *= a1;
-      o[nd][3] *= a1;
-    }
-    const bool partial = valid < CH;
+      for (int c = 0; c < CH; ++c) {
+        sc[c] = c < valid ? sc[c] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, sc[c]);
+      }
+      const float mn = fmaxf(m, mx);
+      const float alpha = fast_exp2(m - mn);
+      float rs = 0.f;
 #pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2) {
-      uint32_t a[4];
-      a[0] = pack_bf16(sc[2 * k2][0], sc[2 * k2][1]);
-      a[1] = pack_bf16(sc[2 * k2][2], sc[2 * k2][3]);
-      a[2] = pack_bf16(sc[2 * k2 + 1][0], sc[2 * k2 + 1][1]);
-      a[3] = pack_bf16(sc[2 * k2 + 1][2], sc[2 * k2 + 1][3]);
-      const int tlo = k2 * 16 + t2, thi = tlo + 8;
+      for (int c = 0; c < CH; ++c) {
+        sc[c] = fast_exp2(sc[c] - mn);
+        rs += sc[c];
+      }
+      l = l * alpha + rs;
+      m = mn;
+      // P row -> smem (bf16, 128-byte swizzled K-major A operand of PV)
+      uint8_t *prow = sP + pb * P_BYTES + r * 128;
 #pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(swz(vb, k2 * 16 + (mi & 1) * 8 + rr, dp * 2 + (mi >> 1)), b0, b1, b2, b3);
-        if (partial) {   // rows past the valid tokens may hold stale data
-          b0 = mask_pair(b0, tlo, valid);
-          b1 = mask_pair(b1, thi, valid);
-          b2 = mask_pair(b2, tlo, valid);
-          b3 = mask_pair(b3, thi, valid);
+      for (int k = 0; k < 8; ++k) {
+        uint4 u;
+        u.x = pack_bf16(sc[8 * k + 0], sc[8 * k + 1]);
+        u.y = pack_bf16(sc[8 * k + 2], sc[8 * k + 3]);
+        u.z = pack_bf16(sc[8 * k + 4], sc[8 * k + 5]);
+        u.w = pack_bf16(sc[8 * k + 6], sc[8 * k + 7]);
+        *reinterpret_cast<uint4 *>(prow + ((k ^ (r & 7)) << 4)) = u;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pfull[pb]);
+      if (ci > 0) {   // fold in the previous chunk's PV (relative to that chunk's max)
+        if (!mbar_wait(ofull, static_cast<uint32_t>((ci - 1) & 1), abort_flag, p.timeout_ns)) {
+          failed = true;
+          break;
         }
-        mma_bf16_16816(o[2 * dp], a, b0, b1);
-        mma_bf16_16816(o[2 * dp + 1], a, b2, b3);
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < HD / 16; ++c) {
+          float v[16];
+          tmem_ld16(lane_base + 128 + c * 16, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) O[c * 16 + i] = O[c * 16 + i] * alpha_pending + v[i];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(oempty);
+      }
+      alpha_pending = alpha;
+    }
+    if (!failed && nchunks > 0) {
+      if (mbar_wait(ofull, static_cast<uint32_t>((nchunks - 1) & 1), abort_flag, p.timeout_ns)) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < HD / 16; ++c) {
+          float v[16];
+          tmem_ld16(lane_base + 128 + c * 16, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) O[c * 16 + i] = O[c * 16 + i] * alpha_pending + v[i];
+        }
+        tc_fence_before();
+      } else {
+        failed = true;
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);
-  }
-
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
-  // ---- merge the groups' softmax states (all chunks are consumed, so the
-  // stage buffers are free for the exchange)
-  if (bar_or(3, 32 * g * p.ng, failed || *abort_flag)) {
-    if (threadIdx.x == 32) report(p.status, DFLASH_ERR_TIMEOUT);
-    return;
-  }
-  if (p.ng > 1) {
-    float *xs = reinterpret_cast<float *>(base);
-    if (grp > 0) {
-      float *dst = xs + (static_cast<size_t>((grp - 1) * g + w) * 32 + lane) * 68;
-#pragma unroll
-      for (int nd = 0; nd < 16; ++nd) {
-        dst[nd * 4 + 0] = o[nd][0];
-        dst[nd * 4 + 1] = o[nd][1];
-        dst[nd * 4 + 2] = o[nd][2];
-        dst[nd * 4 + 3] = o[nd][3];
-      }
-      dst[64] = m0;
-      dst[65] = m1;
-      dst[66] = l0;
-      dst[67] = l1;
-    }
-    asm volatile("bar.sync 3, %0;" ::"r"(32 * g * p.ng) : "memory");
-    if (grp > 0) return;
-    for (int og = 1; og < p.ng; ++og) {
-      const float *src = xs + (static_cast<size_t>((og - 1) * g + w) * 32 + lane) * 68;
-      const float mb0 = src[64], mb1 = src[65];
-      const float M0 = fmaxf(m0, mb0), M1 = fmaxf(m1, mb1);
-      const float a0 = fast_exp2(m0 - M0), b0 = fast_exp2(mb0 - M0);
-      const float a1 = fast_exp2(m1 - M1), b1 = fast_exp2(mb1 - M1);
-      l0 = l0 * a0 + src[66] * b0;
-      l1 = l1 * a1 + src[67] * b1;
-#pragma unroll
-      for (int nd = 0; nd < 16; ++nd) {
-        o[nd][0] = o[nd][0] * a0 + src[nd * 4 + 0] * b0;
-        o[nd][1] = o[nd][1] * a0 + src[nd * 4 + 1] * b0;
-        o[nd][2] = o[nd][2] * a1 + src[nd * 4 + 2] * b1;
-        o[nd][3] = o[nd][3] * a1 + src[nd * 4 + 3] * b1;
-      }
-      m0 = M0;
-      m1 = M1;
+    if (failed) {
+      report(p.status, DFLASH_ERR_TIMEOUT);
+      *abort_flag = 1;
     }
   }
-  const int nthr = 32 * g;   // group 0 carries on
 
-  if (nsplit == 1) {
-    const size_t o0 = static_cast<size_t>(b * BLK + gr) * p.ldo + hq * HD;
-    const size_t o1 = o0 + 8 * static_cast<size_t>(p.ldo);
-    const float i0 = 1.f / l0, i1 = 1.f / l1;
+  // all roles done: TMEM and the KV ring are free
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+
+  const int qq = warp & 3;
+  const int rr = qq * 32 + lane;
+  const bool row_thread = warp >= 2 && rr < R;
+  if (p.S == 1) {
+    if (row_thread && nchunks > 0) {
+      const int hq = h * g + rr / BLK, j = rr % BLK;
+      const float inv = 1.f / l;
+      const size_t o0 = static_cast<size_t>(b * BLK + j) * p.ldo + hq * HD;
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-      store2_hl(p.out, p.out_lo, o0 + nd * 8 + t2, o[nd][0] * i0, o[nd][1] * i0);
-      store2_hl(p.out, p.out_lo, o1 + nd * 8 + t2, o[nd][2] * i1, o[nd][3] * i1);
+      for (int c = 0; c < HD; c += 2) store2_hl(p.out, p.out_lo, o0 + c, O[c] * inv, O[c + 1] * inv);
     }
     return;
   }
 
-  // ---- split partials: rows of this CTA are (w*16 + j), j = block position
-  const size_t rows = static_cast<size_t>(BLK) * g;
-  const size_t slot0 = (static_cast<size_t>(b) * p.nkv + h) * p.max_splits;
-  {
-    float *po = p.part_o + ((slot0 + s) * rows + w * BLK) * HD;
+  // ---- cluster merge: every CTA publishes (m, l, O) of its rows in its own
+  // smem; after a cluster barrier CTA k finalises rows [k*R/S, (k+1)*R/S)
+  // reading all S partials through distributed shared memory
+  float *xo = reinterpret_cast<float *>(sK);            // [128][HD] partial O
+  float *xml = xo + MROWS * HD;                           // [128][2] (max, sum)
+  if (row_thread) {
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-      __stcg(reinterpret_cast<float2 *>(po + gr * HD + nd * 8 + t2), make_float2(o[nd][0], o[nd][1]));
-      __stcg(reinterpret_cast<float2 *>(po + (gr + 8) * HD + nd * 8 + t2), make_float2(o[nd][2], o[nd][3]));
+    for (int c = 0; c < HD; c += 4)
+      *reinterpret_cast<float4 *>(xo + rr * HD + c) = make_float4(O[c], O[c + 1], O[c + 2], O[c + 3]);
+    xml[2 * rr] = m;
+    xml[2 * rr + 1] = l;
+  }
+  cluster_sync();
+  const int per = R / p.S;
+  const int rank = static_cast<int>(cluster_ctarank());
+  for (int it = threadIdx.x; it < per * (HD / 4); it += NTHR) {
+    const int row = rank * per + it / (HD / 4), c4 = it % (HD / 4);
+    float M = -INFINITY;
+    float2 ml[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      ml[k] = k < p.S ? ld_dsmem_f2(dsmem_addr(xml + 2 * row, k)) : make_float2(-INFINITY, 0.f);
+      M = fmaxf(M, ml[k].x);
     }
-    if ((lane & 3) == 0) {
-      float *pm = p.part_ml + ((slot0 + s) * rows + w * BLK) * 2;
-      __stcg(reinterpret_cast<float2 *>(pm + gr * 2), make_float2(m0, l0));
-      __stcg(reinterpret_cast<float2 *>(pm + (gr + 8) * 2), make_float2(m1, l1));
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k < p.S) {
+        const float w = ml[k].y > 0.f ? fast_exp2(ml[k].x - M) : 0.f;
+        L += w * ml[k].y;
+        const float4 v = ld_dsmem_f4(dsmem_addr(xo + row * HD + 4 * c4, k));
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+      }
     }
+    const float inv = 1.f / L;
+    const int hq = h * g + row / BLK, j = row % BLK;
+    const size_t dst = static_cast<size_t>(b * BLK + j) * p.ldo + hq * HD + 4 * c4;
+    store2_hl(p.out, p.out_lo, dst, acc.x * inv, acc.y * inv);
+    store2_hl(p.out, p.out_lo, dst + 2, acc.z * inv, acc.w * inv);
   }
-  __threadfence();
-  asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
-  if (threadIdx.x == 32) {
-    int *ctr = &p.counters[b * p.nkv + h];
-    const int old = atomicAdd(ctr, 1);
-    const int last = (old == nsplit - 1) ? 1 : 0;
-    if (last) *ctr = 0;
-    *bcast = last;
-    __threadfence();
-  }
-  asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
-  if (!*bcast) return;
-
-  // ---- merge the nsplit partials of this (request, kv head); each warp
-  // merges its own 16 rows.  Lanes own splits for the (max, sum) pass
-  // (combined with warp shuffles), then own 4 of the 128 columns for the
-  // weighted sum of the partial outputs (16 independent loads per split).
-  const float *pml = p.part_ml + (slot0 * rows + w * BLK) * 2;
-  const float *pot = p.part_o + (slot0 * rows + w * BLK) * HD;
-  float M[BLK], L[BLK];
-#pragma unroll
-  for (int j = 0; j < BLK; ++j) {
-    M[j] = -INFINITY;
-    L[j] = 0.f;
-  }
-  for (int s0 = 0; s0 < nsplit; s0 += 32) {        // running max / sum over groups of 32 splits
-    const int ss = s0 + lane;
-    float2 ml[BLK];
-#pragma unroll
-    for (int j = 0; j < BLK; ++j)
-      ml[j] = ss < nsplit ? __ldcg(reinterpret_cast<const float2 *>(pml + (static_cast<size_t>(ss) * rows + j) * 2))
-                          : make_float2(-INFINITY, 0.f);
-#pragma unroll
-    for (int j = 0; j < BLK; ++j) {
-      const float gm = warp_max(ml[j].x);
-      const float mn = fmaxf(M[j], gm);
-      const float contrib = ss < nsplit ? fast_exp2(ml[j].x - mn) * ml[j].y : 0.f;
-      L[j] = L[j] * fast_exp2(M[j] - mn) + warp_sum(contrib);
-      M[j] = mn;
-    }
-  }
-  float4 acc[BLK];
-#pragma unroll
-  for (int j = 0; j < BLK; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int ss = 0; ss < nsplit; ++ss) {
-    float4 v[BLK];
-#pragma unroll
-    for (int j = 0; j < BLK; ++j)
-      v[j] = __ldcg(reinterpret_cast<const float4 *>(pot + (static_cast<size_t>(ss) * rows + j) * HD) + lane);
-#pragma unroll
-    for (int j = 0; j < BLK; ++j) {
-      const float m = __ldcg(pml + (static_cast<size_t>(ss) * rows + j) * 2);   // L2 hit, uniform
-      const float wgt = fast_exp2(m - M[j]);
-      acc[j].x += wgt * v[j].x;
-      acc[j].y += wgt * v[j].y;
-      acc[j].z += wgt * v[j].z;
-      acc[j].w += wgt * v[j].w;
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < BLK; ++j) {
-    const float inv = 1.f / L[j];
-    const size_t dst = static_cast<size_t>(b * BLK + j) * p.ldo + hq * HD + lane * 4;
-    store2_hl(p.out, p.out_lo, dst, acc[j].x * inv, acc[j].y * inv);
-    store2_hl(p.out, p.out_lo, dst + 2, acc[j].z * inv, acc[j].w * inv);
-  }
+  cluster_sync();   // nobody leaves while others still read its smem
 }
 
 // ------------------------------------------------------------------ fp32
+// K pages [page][nkv][slot][d]; V pages transposed [page][nkv][d][slot];
+// block K [B][nkv][64][d], block V^T [B][nkv][d][64].
 template <int DPL>
 __global__ void __launch_bounds__(512) attn_f32_kernel(const float *q, int ldq, const float *kc, const float *vc,
                                                        const float *bk, const float *bv, const int32_t *pt,
@@ -453,19 +425,20 @@ __global__ void __launch_bounds__(512) attn_f32_kernel(const float *q, int ldq, 
   float m = -INFINITY, l = 0.f;
   for (int t = 0; t < n + BLK; ++t) {
     const float *kp, *vp;
+    int vstride;
     if (t < n) {
       const int pg = pt[static_cast<size_t>(b) * max_pages + t / page];
       if (pg < 0 || pg >= num_pages) {
         if (lane == 0) report(status, DFLASH_ERR_DEVICE);
         continue;
       }
-      const size_t off = ((static_cast<size_t>(pg) * nkv + h) * page + t % page) * D;
-      kp = kc + off;
-      vp = vc + off;
+      kp = kc + ((static_cast<size_t>(pg) * nkv + h) * page + t % page) * D;
+      vp = vc + (static_cast<size_t>(pg) * nkv + h) * D * page + t % page;
+      vstride = page;
     } else {
-      const size_t off = ((static_cast<size_t>(b) * nkv + h) * BLK + (t - n)) * D;
-      kp = bk + off;
-      vp = bv + off;
+      kp = bk + ((static_cast<size_t>(b) * nkv + h) * 64 + (t - n)) * D;
+      vp = bv + (static_cast<size_t>(b) * nkv + h) * D * 64 + (t - n);
+      vstride = 64;
     }
     float d = 0.f;
 #pragma unroll
@@ -475,7 +448,7 @@ __global__ void __launch_bounds__(512) attn_f32_kernel(const float *q, int ldq, 
     const float a = expf(m - mn), pw = expf(sc - mn);
     l = l * a + pw;
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) acc[i] = acc[i] * a + pw * vp[lane + 32 * i];
+    for (int i = 0; i < DPL; ++i) acc[i] = acc[i] * a + pw * vp[static_cast<size_t>(lane + 32 * i) * vstride];
     m = mn;
   }
   float *orow = out + static_cast<size_t>(b * BLK + j) * ldo + hq * D;
@@ -491,24 +464,28 @@ int attention_bf16(const Launch &lc, const AttnArgs &a) {
     return set_error(DFLASH_ERR_UNSUPPORTED, "bf16 attention needs head_dim 128 and 64-token pages");
   const int g = a.nq / a.nkv;
   if (g < 1 || g > 8) return set_error(DFLASH_ERR_UNSUPPORTED, "bf16 attention: q heads per kv head must be 1..8");
+  if (a.max_splits != 1 && a.max_splits != 2 && a.max_splits != 4 && a.max_splits != 8)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "bf16 attention: splits per request must be 1, 2, 4 or 8");
   static bool attr_done = false;
   if (!attr_done) {
-    if (int e = cuda_check(cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM),
+    if (int e = cuda_check(cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM),
                            "attention smem attribute"))
       return e;
     attr_done = true;
   }
-  CUtensorMap tK, tV, tBK, tBV;
-  const uint64_t kv_rows = static_cast<uint64_t>(a.num_pages) * a.nkv * CH;
-  const uint64_t blk_rows = static_cast<uint64_t>(a.B) * a.nkv * BLK;
-  if (int e = make_tmap_2d(&tK, a.k_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, HD, kv_rows, HD * 2, 64, CH)) return e;
-  if (int e = make_tmap_2d(&tV, a.v_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, HD, kv_rows, HD * 2, 64, CH)) return e;
-  if (int e = make_tmap_2d(&tBK, a.bk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, HD, blk_rows, HD * 2, 64, BLK)) return e;
-  if (int e = make_tmap_2d(&tBV, a.bv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, HD, blk_rows, HD * 2, 64, BLK)) return e;
+  CUtensorMap tQ, tK, tV, tBK, tBV;
+  const uint64_t kv_pages = static_cast<uint64_t>(a.num_pages) * a.nkv;
+  const uint64_t bkv = static_cast<uint64_t>(a.B) * a.nkv;
+  if (int e = make_tmap_2d(&tQ, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.nq) * HD,
+                           static_cast<uint64_t>(a.B) * BLK, static_cast<uint64_t>(a.nq) * HD * 2, 64, BLK))
+    return e;
+  if (int e = make_tmap_2d(&tK, a.k_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, HD, kv_pages * CH, HD * 2, 64, CH))
+    return e;
+  if (int e = make_tmap_2d(&tV, a.v_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CH, kv_pages * HD, CH * 2, 64, HD))
+    return e;
+  if (int e = make_tmap_2d(&tBK, a.bk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, HD, bkv * CH, HD * 2, 64, CH)) return e;
+  if (int e = make_tmap_2d(&tBV, a.bv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CH, bkv * HD, CH * 2, 64, HD)) return e;
   Params p = {};
-  p.ng = (1 + 2 * g) * 32 <= 352 ? 2 : 1;
-  p.q = static_cast<const __nv_bfloat16 *>(a.q);
-  p.ldq = a.nq * HD;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.out_lo = static_cast<__nv_bfloat16 *>(a.out_lo);
   p.ldo = a.nq * HD;
@@ -516,28 +493,29 @@ int attention_bf16(const Launch &lc, const AttnArgs &a) {
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
   p.ctx_len = a.ctx_len;
-  p.part_o = a.part_o;
-  p.part_ml = a.part_ml;
-  p.counters = a.counters;
   p.nkv = a.nkv;
   p.g = g;
   p.split = a.split_tokens;
-  p.max_splits = a.max_splits;
+  p.S = a.max_splits;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(HD)));
   p.status = lc.status;
   p.timeout_ns = lc.timeout_ns;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.max_splits, a.nkv, a.B);
-  cfg.blockDim = dim3(32 * (1 + p.ng * g));
+  cfg.blockDim = dim3(NTHR);
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = lc.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = a.max_splits;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   ProfScope ps(lc, "attention", -1.0, -1.0);
-  return cuda_check(cudaLaunchKernelEx(&cfg, attn_bf16_kernel, tK, tV, tBK, tBV, p), "attention launch");
+  return cuda_check(cudaLaunchKernelEx(&cfg, attn_tc_kernel, tQ, tK, tV, tBK, tBV, p), "attention launch");
 }
 
 int attention_f32(const Launch &lc, const AttnArgs &a) {

@@ -209,8 +209,9 @@ struct RopeArgs {
 };
 
 // qkv: fp32 [B*16][(nq+2nkv)*d].  One warp per (token, head).  q heads ->
-// q_out [B*16][nq*d]; k heads -> bk [B][nkv][16][d] (normed, rotated);
-// v heads -> bv [B][nkv][16][d].
+// q_out [B*16][nq*d]; k heads -> bk [B][nkv][64][d] (normed, rotated; rows
+// 16..63 stay zero); v heads -> bv [B][nkv][d][64], transposed like the V
+// pages (columns 16..63 stay zero).
 template <typename T, int DPL>
 __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, int nkv, const float *g_q,
                                                       const float *g_k, int qk_norm, float eps, const RopeArgs rp,
@@ -225,10 +226,10 @@ __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, 
   float v[DPL];
 #pragma unroll
   for (int i = 0; i < DPL; ++i) v[i] = src[lane + 32 * i];
-  if (head >= nq + nkv) {   // value head: copy
-    T *dst = bv + ((static_cast<size_t>(b) * nkv + (head - nq - nkv)) * 16 + j) * D;
+  if (head >= nq + nkv) {   // value head: copy, transposed
+    T *dst = bv + (static_cast<size_t>(b) * nkv + (head - nq - nkv)) * D * 64 + j;
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + lane + 32 * i, v[i]);
+    for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + static_cast<size_t>(lane + 32 * i) * 64, v[i]);
     return;
   }
   const bool is_q = head < nq;
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, 
     o[i + DPL / 2] = x2 * c + x1 * s;
   }
   T *dst = is_q ? q_out + static_cast<size_t>(tok) * nq * D + static_cast<size_t>(head) * D
-                : bk + ((static_cast<size_t>(b) * nkv + (head - nq)) * 16 + j) * D;
+                : bk + ((static_cast<size_t>(b) * nkv + (head - nq)) * 64 + j) * D;
 #pragma unroll
   for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + lane + 32 * i, o[i]);
 }
@@ -331,10 +332,17 @@ __global__ void __launch_bounds__(256) inject_scatter_kernel(const ScatterArgs a
 #pragma unroll
     for (int i = 0; i < DPL; ++i) v[i] = o[i];
   }
+  // K pages: [page][nkv][slot][d]; V pages transposed: [page][nkv][d][slot]
   T *cache = static_cast<T *>(kv == 0 ? a.k_cache : a.v_cache) + l * a.layer_elems;
-  T *dst = cache + ((static_cast<size_t>(pg) * a.nkv + h) * a.page + pos % a.page) * D;
+  if (kv == 0) {
+    T *dst = cache + ((static_cast<size_t>(pg) * a.nkv + h) * a.page + pos % a.page) * D;
 #pragma unroll
-  for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + lane + 32 * i, v[i]);
+    for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + lane + 32 * i, v[i]);
+  } else {
+    T *dst = cache + (static_cast<size_t>(pg) * a.nkv + h) * D * a.page + pos % a.page;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + static_cast<size_t>(lane + 32 * i) * a.page, v[i]);
+  }
 }
 
 // ------------------------------------------------------------------ short conv

@@ -106,18 +106,15 @@ struct AttnArgs {
   const void *q;            // [B*16][nq*d] (dtype)
   const void *k_cache;      // this layer: [num_pages][nkv][page][d]
   const void *v_cache;
-  const void *bk, *bv;      // block K/V [B][nkv][16][d]
+  const void *bk, *bv;      // block K [B][nkv][64][d], block V^T [B][nkv][d][64]
   const int32_t *page_table;
   int max_pages, num_pages, page_size;
   const int32_t *ctx_len;   // [B]
   void *out;                // [B*16][nq*d] (dtype)
   void *out_lo;             // low bf16 halves of out, or null
-  float *part_o;            // split partials
-  float *part_ml;
-  int *counters;            // [B*nkv]
   int B, nq, nkv, d;
   int split_tokens;         // multiple of page_size
-  int max_splits;
+  int max_splits;           // splits per (request, kv head) = cluster size: 1, 2, 4 or 8
 };
 int attention_bf16(const Launch &lc, const AttnArgs &a);
 int attention_f32(const Launch &lc, const AttnArgs &a);

@@ -104,15 +104,17 @@ def make_weights_struct(dw: dict):
 
 
 class PagedKV:
-    """Device KV pools [L][num_pages][nkv][64][d] and the page table."""
+    """Device KV pools (K [L][num_pages][nkv][64][d], V [L][num_pages][nkv][d][64])
+    and the page table; zero-filled (slots past a request's length stay finite)."""
 
     def __init__(self, cfg, page_table: np.ndarray, num_pages: int, device="cuda", zero=True):
         torch = _torch()
         dt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
         shape = (cfg.n_layers, num_pages, cfg.n_kv_heads, cfg.page_size, cfg.head_dim)
+        vshape = (cfg.n_layers, num_pages, cfg.n_kv_heads, cfg.head_dim, cfg.page_size)
         alloc = torch.zeros if zero else torch.empty
         self.k = alloc(shape, dtype=dt, device=device)
-        self.v = alloc(shape, dtype=dt, device=device)
+        self.v = alloc(vshape, dtype=dt, device=device)
         self.page_table = to_device(np.ascontiguousarray(page_table, dtype=np.int32), device)
         self.num_pages = int(num_pages)
         self.max_pages = int(page_table.shape[1])

@@ -127,9 +127,12 @@ typedef struct dflash_weights {
   float sel_b_g;         /* context-gate bias                                */
 } dflash_weights;
 
-/* Paged drafter KV cache (device memory, not owned).
- *   k_cache, v_cache: [L][num_pages][nkv][page_size][d] elements of dtype;
- *   K is stored after the per-head k-norm and RoPE at its absolute position.
+/* Paged drafter KV cache (device memory, not owned, zero-filled when
+ * allocated so that slots past a request's length hold finite values).
+ *   k_cache: [L][num_pages][nkv][page_size][d] elements of dtype, stored after
+ *            the per-head k-norm and RoPE at its absolute position;
+ *   v_cache: [L][num_pages][nkv][d][page_size] (each page slice transposed:
+ *            the PV product reads it as a K-major operand).
  *   page_table: device int32 [batch][max_pages]; token position p of request
  *   b lives in page page_table[b*max_pages + p/page_size], slot p%page_size.
  *   Entries past a request's last used page are never read.  A page index

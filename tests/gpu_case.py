@@ -87,7 +87,8 @@ class Case:
         npg = (n + 63) // 64
         pages = self.torch.as_tensor(self.table[b, :npg].astype(np.int64), device=self.device)
         k = self.kv.k[layer][pages].permute(0, 2, 1, 3).reshape(npg * 64, self.cfg.n_kv_heads, -1)[:n]
-        v = self.kv.v[layer][pages].permute(0, 2, 1, 3).reshape(npg * 64, self.cfg.n_kv_heads, -1)[:n]
+        # V pages are stored transposed: [page][nkv][d][slot]
+        v = self.kv.v[layer][pages].permute(0, 3, 1, 2).reshape(npg * 64, self.cfg.n_kv_heads, -1)[:n]
         return to_np(k), to_np(v)
 
     def draft(self, want_logits=True):
