@@ -160,8 +160,8 @@ Layout layout(const dflash_ctx *c, int B, int Tn) {
   L.u2 = take(te * R * H);
   L.qkv = take(4 * R * (nq + 2 * nkv) * d);
   L.q = take(te * R * nq * d);
-  L.bk = take(te * B * nkv * 64 * d);   // block K [B][nkv][64][d], rows 16.. zero
-  L.bv = take(te * B * nkv * 64 * d);   // block V^T [B][nkv][d][64], cols 16.. zero
+  L.bk = take(te * B * nkv * 64 * d);   // block K [B][nkv][64][d], rows 16.. unused
+  L.bv = take(te * B * nkv * 64 * d);   // block V^T [B][nkv][d][64], cols 16.. unused
   L.o = take(te * R * nq * d);
   L.ysub = take(te * R * H);
   L.coef = take(4 * R * (H / 8));

@@ -212,13 +212,19 @@ __global__ void __launch_bounds__(NTHR, 1)
       };
       auto issue_pv = [&](int ci) -> bool {
         const int st = ci % ST, pb = ci & 1;
+        // only the 16-token k-steps holding valid tokens: V columns past them
+        // (block slots 16..63, the unused tail of a last page) are never read,
+        // so whatever they hold cannot reach O through 0 * Inf
+        const int valid = ci < ctx_chunks ? min(CH, t1 - (t0 + ci * CH)) : BLK;
+        const int ksteps = (valid + 15) / 16;
         if (!mbar_wait(&pfull[pb], static_cast<uint32_t>((ci >> 1) & 1), abort_flag, p.timeout_ns)) return false;
         if (!mbar_wait(oempty, static_cast<uint32_t>((ci & 1) ^ 1), abort_flag, p.timeout_ns)) return false;
         tc_fence_after();
         const uint32_t p0 = smem_u32(sP + pb * P_BYTES), v0 = smem_u32(sV + st * V_BYTES);
 #pragma unroll
         for (int kk = 0; kk < CH / 16; ++kk)
-          umma_bf16(pv_tmem, sdesc_k_sw128(p0 + kk * 32), sdesc_k_sw128(v0 + kk * 32), idesc_pv, kk > 0 ? 1u : 0u);
+          if (kk < ksteps)
+            umma_bf16(pv_tmem, sdesc_k_sw128(p0 + kk * 32), sdesc_k_sw128(v0 + kk * 32), idesc_pv, kk > 0 ? 1u : 0u);
         umma_commit(ofull);
         umma_commit(&empty[st]);   // PV is the last reader of this KV stage
         return true;

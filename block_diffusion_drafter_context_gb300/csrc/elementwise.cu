@@ -209,9 +209,10 @@ struct RopeArgs {
 };
 
 // qkv: fp32 [B*16][(nq+2nkv)*d].  One warp per (token, head).  q heads ->
-// q_out [B*16][nq*d]; k heads -> bk [B][nkv][64][d] (normed, rotated; rows
-// 16..63 stay zero); v heads -> bv [B][nkv][d][64], transposed like the V
-// pages (columns 16..63 stay zero).
+// q_out [B*16][nq*d]; k heads -> bk [B][nkv][64][d] (normed, rotated); v
+// heads -> bv [B][nkv][d][64], transposed like the V pages.  Rows / columns
+// 16..63 are padding up to one 64-token page: never written, and attention
+// masks their scores and skips their V columns, so they may hold anything.
 template <typename T, int DPL>
 __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, int nkv, const float *g_q,
                                                       const float *g_k, int qk_norm, float eps, const RopeArgs rp,
