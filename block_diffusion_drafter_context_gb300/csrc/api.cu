@@ -128,8 +128,13 @@ constexpr int GEMM_COUNTERS = 1 << 16;
 constexpr int GEMM_MAX_BN = 256;
 constexpr int TOPK_MAX_CHUNKS = 64;
 
+// The header of the workspace (status word, self-resetting counters, split
+// scratch) sits at offsets that depend on neither the batch nor the token
+// count, so calls with different sizes on one workspace never read another
+// call's data as a counter.  Everything after it is rewritten before it is
+// read within each call.
 struct Layout {
-  size_t status, gemm_ctr, gemm_part, topk_ctr, topk_part;
+  size_t status, gemm_ctr, gemm_part, topk_ctr, attn_ctr, attn_part, attn_part_slots, topk_part;
   size_t x, u, u2, qkv, q, bk, bv, o, ysub, coef, hmid, hmask, hfinal, logits, scores;
   size_t u_lo, u2_lo, o_lo, ysub_lo, hmid_lo, hmask_lo, ysub32;
   size_t fc, f, f_lo, kvproj, ctx_saved;
@@ -153,7 +158,11 @@ Layout layout(const dflash_ctx *c, int B, int Tn) {
   L.gemm_ctr = take(sizeof(int) * GEMM_COUNTERS);
   L.gemm_part_floats = static_cast<size_t>(c->num_sms) * 2 * 128 * GEMM_MAX_BN;
   L.gemm_part = take(4 * L.gemm_part_floats);
-  L.topk_ctr = take(sizeof(int) * static_cast<size_t>(B) * 15);
+  L.topk_ctr = take(sizeof(int) * static_cast<size_t>(DFLASH_MAX_BATCH) * 15);
+  L.attn_ctr = take(sizeof(int) * static_cast<size_t>(DFLASH_MAX_BATCH) * nkv);
+  L.attn_part_slots = 2ull * c->num_sms;
+  L.attn_part = take(4ull * L.attn_part_slots * ATTN_PART_FLOATS);
+  (void)B;
   L.topk_part = take(8ull * B * 15 * TOPK_MAX_CHUNKS * 16);
   L.x = take(4 * R * H);
   L.u = take(te * R * H);
@@ -239,6 +248,7 @@ GemmOp mk(const void *W, int ldw, const void *X, const void *X_lo, int ldx, int 
 int check_ws(const dflash_ctx *c, void *ws, size_t bytes, int B, int Tn) {
   if (!ws) return set_error(DFLASH_ERR_ARG, "workspace is null");
   if (!aligned16(ws)) return set_error(DFLASH_ERR_ALIGN, "workspace must be 16-byte aligned");
+  if (B > DFLASH_MAX_BATCH) return set_error(DFLASH_ERR_ARG, "batch %d over DFLASH_MAX_BATCH", B);
   const size_t need = layout(c, B, Tn).total;
   if (bytes < need)
     return set_error(DFLASH_ERR_SHAPE, "workspace of %zu bytes is smaller than the %zu needed for batch %d", bytes, need,
@@ -423,24 +433,6 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
   void *hfinal = final_hidden ? final_hidden : at<void>(ws, L.hfinal);
   float *lg = logits ? logits : at<float>(ws, L.logits);
 
-  // split-KV plan: the S splits of one (request, kv head) form a thread-block
-  // cluster (S = 1, 2, 4 or 8) and merge on chip; S grows until the grid covers
-  // the SMs and no split holds more than 16 pages (load balance on ragged
-  // batches)
-  const int max_ctx = kv->max_pages * g.page_size;
-  const int max_chunks = (max_ctx + 63) / 64 + 1;
-  int max_splits = 1;
-  if (ctx->attn_split > 0) {
-    const int want = (max_ctx + ctx->attn_split - 1) / ctx->attn_split;
-    while (max_splits < 8 && max_splits < want) max_splits *= 2;
-  } else {
-    while (max_splits < 8 && (static_cast<long long>(B) * nkv * max_splits < ctx->num_sms ||
-                              max_chunks / max_splits > 16))
-      max_splits *= 2;
-  }
-  int split_tok = ((max_ctx + max_splits - 1) / max_splits + 63) / 64 * 64;
-  if (split_tok < 64) split_tok = 64;
-
   const bool split = !f32 && g.split_act;
   auto lo = [&](size_t off) -> void * { return split ? at<void>(ws, off) : nullptr; };
   void *u_lo = lo(L.u_lo), *u2_lo = lo(L.u2_lo), *ysub_lo = lo(L.ysub_lo), *hmid_lo = lo(L.hmid_lo);
@@ -503,8 +495,11 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     aa.nq = nq;
     aa.nkv = nkv;
     aa.d = d;
-    aa.split_tokens = split_tok;
-    aa.max_splits = max_splits;
+    aa.min_chunks = ctx->attn_split / 64;
+    aa.counters = at<int>(ws, L.attn_ctr);
+    aa.counter_cap = static_cast<size_t>(DFLASH_MAX_BATCH) * nkv;
+    aa.partials = at<float>(ws, L.attn_part);
+    aa.partial_slots = L.attn_part_slots;
     if (int e = f32 ? attention_f32(lc, aa) : attention_bf16(lc, aa)) return e;
     if (int e = out_proj(1, lw, lw.w_o, nq * d, aa.out, aa.out_lo, "o_proj")) return e;
     // ---- FFN sublayer

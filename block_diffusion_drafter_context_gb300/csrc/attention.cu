@@ -5,25 +5,27 @@
 // Metodologia 1: bidirectional in the block, all of the clean prefix, no
 // other block).
 //
-// bf16 path - split-KV, decode style, HBM-bound, on the 5th-generation tensor
-// cores:
-//   grid (split, kv head, request); the S splits of one (request, kv head)
-//   form one thread-block cluster.  A CTA takes the 16 queries x g query
-//   heads sharing one KV head (16g rows, padded to the UMMA M of 128) over
-//   one contiguous range of the context, in 64-token chunks (one KV page):
-//     warp 0     TMA: Q once, then K and V^T pages into a 3-deep smem ring
-//                (128-byte swizzle; V pages are stored transposed so both
-//                products take K-major operands);
-//     warp 1     tcgen05.mma: S = Q K^T (M=128, N=64, K=128) into one of two
-//                TMEM buffers, then PV = P V (M=128, N=128, K=64) into TMEM;
-//     warps 2-5  one TMEM lane (= query row) per thread: online softmax in
-//                the exp2 domain on its 64 scores (no shuffles), P written
-//                back to smem in bf16 as the A operand of PV, O accumulated
-//                in registers.
-//   QK of chunk i+1 overlaps the softmax of chunk i.  The last split also
-//   covers the 16 block keys.  At the end the cluster's CTAs exchange
-//   (max, sum, O) through distributed shared memory and each finalises 16g/S
-//   rows: the split partials never leave the chip.
+// bf16 path - persistent, balanced split-KV, HBM-bound, on the 5th-generation
+// tensor cores.  The work is the flat list of 64-token chunks (one KV page
+// each) over (request, kv head): ceil(n_b/64) context chunks plus one chunk of
+// the 16 block keys per (request, kv head).  One CTA per SM takes an equal
+// contiguous run of that list, so ragged batches stay balanced and a CTA's
+// pipeline never drains between requests.  Per CTA:
+//   warp 0     TMA: K and V^T pages into a 5-deep smem ring (128-byte swizzle;
+//              V pages are stored transposed so both products take K-major
+//              operands); the 16g query rows of each new (request, kv head);
+//   warp 1     tcgen05.mma: S = Q K^T (M=128, N=64, K=128) into one of two
+//              TMEM buffers; O += P V (M=128, N=128, K = the chunk's valid
+//              tokens rounded up to 16) into a TMEM accumulator;
+//   warps 2-5  one TMEM lane (= query row) per thread: online softmax in the
+//              exp2 domain on its 64 scores, P written back to smem in bf16
+//              as the A operand of PV.  O stays in TMEM; it is rescaled only
+//              when a row's running max grows by more than 2^8 (the exp2
+//              values stay below 256 in between, exact in fp32 sums).
+// A (request, kv head) whose chunks all fall in one CTA is normalised and
+// written directly.  One cut by a CTA boundary leaves (max, sum, O) partials
+// in a small L2-resident scratch, and the last contributing CTA to arrive (a
+// self-resetting per-(request, kv head) counter) merges them.
 // fp32 path - plain CUDA-core loop for the tiny fp32 configuration.
 #include "common.cuh"
 #include "internal.h"
@@ -35,16 +37,22 @@ namespace {
 
 constexpr int CH = 64;                       // tokens per chunk (= one KV page)
 constexpr int HD = 128;                      // head dim of the bf16 path
-constexpr int ST = 3;                        // KV ring depth
+constexpr int ST = 5;                        // KV ring depth
 constexpr int BLK = 16;                      // block tokens
 constexpr int MROWS = 128;                   // UMMA M (query rows, padded)
 constexpr int Q_BYTES = MROWS * HD * 2;      // 32 KB: two 64-dim halves of [128][64]
 constexpr int K_BYTES = CH * HD * 2;         // 16 KB: two halves of [64 tok][64]
 constexpr int V_BYTES = HD * CH * 2;         // 16 KB: [128 d][64 tok]
 constexpr int P_BYTES = MROWS * CH * 2;      // 16 KB: [128 rows][64 tok]
-constexpr int SMEM = 1024 + Q_BYTES + ST * (K_BYTES + V_BYTES) + 2 * P_BYTES + 256;
-constexpr int NTHR = 192;
-constexpr int TMEM_COLS = 256;               // S x 2 (64 columns each) + PV (128 columns)
+constexpr int CTRL_BYTES = 256;              // mbarriers, TMEM address, schedule
+constexpr int SMEM = 1024 + Q_BYTES + ST * (K_BYTES + V_BYTES) + 2 * P_BYTES + CTRL_BYTES;
+constexpr int NTHR = 224;                    // producer, QK issuer, 4 softmax warps, PV issuer
+constexpr int NSB = 3;                       // S buffers in TMEM: QK runs two chunks ahead
+constexpr int TMEM_COLS = 512;               // S x 3 (64 columns each), O (128 columns) at 256
+constexpr uint32_t O_COL = 256;
+constexpr float RESCALE_LOG2 = 8.f;
+constexpr int DEFAULT_MIN_CHUNKS = 4;        // fewer CTAs than SMs when the whole list is short
+static_assert(SMEM <= 232448, "attention smem over the per-block limit");
 
 struct Params {
   __nv_bfloat16 *out;
@@ -53,19 +61,151 @@ struct Params {
   const int32_t *page_table;
   int max_pages, num_pages;
   const int32_t *ctx_len;
-  int nkv, g, split, S;
+  int B, nkv, g;
+  int min_chunks;          // at least this many chunks per CTA
   float scale_log2;
+  int *counters;           // [B * nkv], zero between launches
+  float *partials;         // [gridDim.x * 2][ATTN_PART_FLOATS]
   int *status;
   unsigned long long timeout_ns;
 };
 
-// two consecutive bf16 outputs (high halves) and, if lo is given, their low halves
-__device__ __forceinline__ void store2_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t i, float a, float b) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  *reinterpret_cast<__nv_bfloat162 *>(hi + i) = h;
-  if (lo) *reinterpret_cast<uint32_t *>(lo + i) = pack_bf16(a - __low2float(h), b - __high2float(h));
+// This CTA's run of the chunk list (written by warp 0, read by every role).
+struct Sched {
+  int b, h, k;             // first chunk: request, kv head, index in that list
+  int n_mine;              // chunks in the run (0: idle CTA)
+  long long lo, total;     // global index of the first chunk; list length
+  int G;                   // CTAs that received a run
+  int merge_flag;
+};
+
+// control block: 26 mbarriers, TMEM address, abort flag, schedule
+static_assert(26 * 8 + 8 + sizeof(Sched) <= CTRL_BYTES, "attention control block overflows");
+
+__device__ __forceinline__ int ctx_of(const Params &p, int b) {
+  const int n = p.ctx_len[b], cap = p.max_pages * CH;
+  return n < 0 ? 0 : (n > cap ? cap : n);
+}
+__device__ __forceinline__ int chunks_of(int n) { return (n + CH - 1) / CH + 1; }
+__device__ __forceinline__ long long run_lo(int c, long long total, int G) {
+  return static_cast<long long>(c) * total / G;
+}
+// the CTA whose run holds global chunk x
+__device__ __forceinline__ int run_owner(long long x, long long total, int G) {
+  return static_cast<int>(((x + 1) * G + total - 1) / total) - 1;
 }
 
+// Cursor over the chunk list: (request, kv head, chunk) in list order.
+struct Walk {
+  int b, h, k, n, nch;
+  long long x;
+  __device__ void init(const Params &p, const Sched &s) {
+    b = s.b;
+    h = s.h;
+    k = s.k;
+    n = ctx_of(p, b);
+    nch = chunks_of(n);
+    x = s.lo;
+  }
+  __device__ void next(const Params &p) {
+    ++x;
+    if (++k < nch) return;
+    k = 0;
+    if (++h < p.nkv) return;
+    h = 0;
+    if (++b < p.B) {
+      n = ctx_of(p, b);
+      nch = chunks_of(n);
+    }
+  }
+  __device__ bool block_chunk() const { return k == nch - 1; }
+  __device__ int valid() const { return k < nch - 1 ? min(CH, n - k * CH) : BLK; }
+};
+
+// 16 consecutive outputs of one row: high bf16 halves and, if lo, low halves
+__device__ __forceinline__ void store16_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, const float (&v)[16], float s) {
+  uint32_t h[8], l[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float a = v[2 * i] * s, b = v[2 * i + 1] * s;
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(a, b);
+    h[i] = *reinterpret_cast<const uint32_t *>(&hb);
+    l[i] = pack_bf16(a - __low2float(hb), b - __high2float(hb));
+  }
+  uint4 *dh = reinterpret_cast<uint4 *>(hi);
+  dh[0] = make_uint4(h[0], h[1], h[2], h[3]);
+  dh[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  if (lo) {
+    uint4 *dl = reinterpret_cast<uint4 *>(lo);
+    dl[0] = make_uint4(l[0], l[1], l[2], l[3]);
+    dl[1] = make_uint4(l[4], l[5], l[6], l[7]);
+  }
+}
+
+// Partial slot of contributor CTA cc to the (request, kv head) whose list
+// starts at global chunk `start`: 0 when that list is cc's first segment.
+__device__ __forceinline__ const float *part_of(const Params &p, const Sched &sc, int cc, int cf, long long start) {
+  const int slot = (cc > cf || run_lo(cc, sc.total, sc.G) == start) ? 0 : 1;
+  return p.partials + (static_cast<size_t>(cc) * 2 + slot) * ATTN_PART_FLOATS;
+}
+
+// Last arriver of a (request, kv head): combine the (max, sum, O) partials of
+// contributors cf..cl for tile row `trow`, columns [c0, c0 + ncol); loads of
+// four contributors are in flight together.
+__device__ __noinline__ void merge_row(const Params &p, const Sched &sc, int cf, int cl, long long start, int trow,
+                                       int c0, int ncol, __nv_bfloat16 *out, __nv_bfloat16 *out_lo) {
+  float M = -INFINITY;
+  for (int cc0 = cf; cc0 <= cl; cc0 += 4) {
+    float mv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      mv[u] = cc0 + u <= cl ? __ldcg(part_of(p, sc, cc0 + u, cf, start) + HD * MROWS + trow) : -INFINITY;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) M = fmaxf(M, mv[u]);
+  }
+  float L = 0.f;
+  for (int cc0 = cf; cc0 <= cl; cc0 += 4) {
+    float mv[4], lv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool in = cc0 + u <= cl;
+      const float *pp = part_of(p, sc, in ? cc0 + u : cf, cf, start);
+      mv[u] = in ? __ldcg(pp + HD * MROWS + trow) : -INFINITY;
+      lv[u] = in ? __ldcg(pp + HD * MROWS + MROWS + trow) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) L += (lv[u] > 0.f ? fast_exp2(mv[u] - M) : 0.f) * lv[u];
+  }
+  const float inv = 1.f / L;
+  for (int c = c0; c < c0 + ncol; c += 16) {
+    float acc[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) acc[t] = 0.f;
+    for (int cc0 = cf; cc0 <= cl; cc0 += 4) {
+      float wv[4], vv[4][16];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const bool in = cc0 + u <= cl;
+        const float *pp = part_of(p, sc, in ? cc0 + u : cf, cf, start);
+        wv[u] = in ? fast_exp2(__ldcg(pp + HD * MROWS + trow) - M) : 0.f;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) vv[u][t] = in ? __ldcg(pp + (c + t) * MROWS + trow) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int t = 0; t < 16; ++t) acc[t] = fmaf(wv[u], vv[u][t], acc[t]);
+    }
+    store16_hl(out + c, out_lo ? out_lo + c : nullptr, acc, inv);
+  }
+}
+
+// DUP (g <= 4): head w of the group owns TMEM quadrant w, and its 16 query
+// rows are loaded twice (quadrant lanes 0-15 and 16-31), so S reaches both
+// halves of the warp and the two lanes of a row each take 32 of a chunk's 64
+// scores: every softmax warp works and each lane does half a row.
+// Otherwise (g = 5..8): row 16w + j per lane over all 64 scores.
+template <bool DUP>
 __global__ void __launch_bounds__(NTHR, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmBK,
@@ -78,39 +218,50 @@ __global__ void __launch_bounds__(NTHR, 1)
   uint8_t *sV = sK + ST * K_BYTES;
   uint8_t *sP = sV + ST * V_BYTES;
   uint64_t *bar = reinterpret_cast<uint64_t *>(sP + 2 * P_BYTES);
-  uint64_t *qfull = bar, *full = bar + 1, *empty = full + ST, *sfull = empty + ST, *sempty = sfull + 2,
-           *pfull = sempty + 2, *ofull = pfull + 2, *oempty = ofull + 1, *drain = oempty + 1;
+  uint64_t *qfull = bar, *qempty = bar + 1, *full = bar + 2, *empty = full + ST, *sfull = empty + ST,
+           *sempty = sfull + NSB, *pfull = sempty + NSB, *pdone = pfull + 2, *oempty = pdone + 2,
+           *mready = oempty + 1, *mdone = mready + 1, *drain = mdone + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  Sched *sch = reinterpret_cast<Sched *>(tmem_slot + 2);
 
-  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = p.g, R = BLK * g;
+  const int g = p.g;
+  const int R = DUP ? 32 * g : BLK * g;     // TMEM lanes (= A rows) that hold query rows
+  const int nact = (R + 31) / 32;           // softmax warps serving them
 
   if (threadIdx.x == 0) {
     mbar_init(qfull, 1);
+    mbar_init(qempty, 1);
     for (int i = 0; i < ST; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NSB; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&sempty[i], 4);
-      mbar_init(&pfull[i], 4);
+      mbar_init(&sempty[i], nact);
     }
-    mbar_init(ofull, 1);
-    mbar_init(oempty, 4);
-    mbar_init(drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&pfull[i], nact);
+      mbar_init(&pdone[i], 1);
+    }
+    mbar_init(oempty, nact);
+    mbar_init(mready, nact);
+    mbar_init(mdone, 1);
+    mbar_init(drain, 2);   // both MMA issuers
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // query rows past 16g are padding: keep them zero so their scores stay finite
+  // A rows past R (query padding) and the P rows no lane writes are never
+  // touched by TMA or the softmax: zero them once so everything stays finite
   {
     const int per_half = (MROWS - R) * 128 / 16;   // 16-byte chunks
     for (int i = threadIdx.x; i < 2 * per_half; i += NTHR) {
       const int half = i / per_half, k = i % per_half;
       *reinterpret_cast<uint4 *>(sQ + half * (MROWS * 128) + R * 128 + k * 16) = make_uint4(0, 0, 0, 0);
     }
+    for (int i = threadIdx.x; i < 2 * P_BYTES / 16; i += NTHR)
+      reinterpret_cast<uint4 *>(sP)[i] = make_uint4(0, 0, 0, 0);
   }
   fence_proxy_async_smem();
   if (warp == 1) {
@@ -123,84 +274,147 @@ __global__ void __launch_bounds__(NTHR, 1)
   const uint32_t tmem = *tmem_slot;
 
   pdl_start();
-  int n_ctx = p.ctx_len[b];
-  const int cap = p.max_pages * CH;
-  if (n_ctx < 0 || n_ctx > cap) {
-    if (threadIdx.x == 0 && s == 0) report(p.status, DFLASH_ERR_DEVICE);
-    n_ctx = n_ctx < 0 ? 0 : cap;
-  }
-  const int nsplit = n_ctx > 0 ? (n_ctx + p.split - 1) / p.split : 1;
-  const bool active = s < nsplit;   // inactive CTAs still join the cluster merge
-  const int t0 = s * p.split;
-  const int t1 = min(n_ctx, t0 + p.split);
-  const int ctx_chunks = (active && t1 > t0) ? (t1 - t0 + CH - 1) / CH : 0;
-  const bool has_block = active && (s == nsplit - 1);
-  const int nchunks = ctx_chunks + (has_block ? 1 : 0);
-
-  float O[HD];
+  // ---------------------------------------------------------------- schedule
+  // Lane i sums the chunk counts of a contiguous slice of the requests; a
+  // warp scan gives the list length and the slice holding this CTA's start.
+  if (warp == 0) {
+    const int per = (p.B + 31) / 32;
+    const int b0 = min(p.B, lane * per), b1 = min(p.B, b0 + per);
+    const int cap = p.max_pages * CH;
+    long long sum = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int raw = p.ctx_len[b];
+      if (blockIdx.x == 0 && (raw < 0 || raw > cap)) report(p.status, DFLASH_ERR_DEVICE);
+      sum += chunks_of(raw < 0 ? 0 : (raw > cap ? cap : raw));
+    }
+    long long inc = sum;
 #pragma unroll
-  for (int i = 0; i < HD; ++i) O[i] = 0.f;
-  float m = -INFINITY, l = 0.f;
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    const long long total = __shfl_sync(0xffffffffu, inc, 31) * p.nkv;
+    const long long want = (total + p.min_chunks - 1) / p.min_chunks;
+    const int G = static_cast<int>(want < static_cast<long long>(gridDim.x) ? (want < 1 ? 1 : want) : gridDim.x);
+    const int c = blockIdx.x;
+    const long long lo = c < G ? run_lo(c, total, G) : 0, hi = c < G ? run_lo(c + 1, total, G) : 0;
+    const long long ex = (inc - sum) * p.nkv, in = inc * p.nkv;
+    if (lane == 0) {
+      sch->n_mine = static_cast<int>(hi - lo);
+      sch->lo = lo;
+      sch->total = total;
+      sch->G = G;
+      sch->merge_flag = 0;
+    }
+    if (c < G && lo >= ex && lo < in) {   // exactly one lane: the slices partition the list
+      long long pre = ex;
+      for (int b = b0; b < b1; ++b) {
+        const int nch = chunks_of(ctx_of(p, b));
+        const long long span = static_cast<long long>(nch) * p.nkv;
+        if (lo < pre + span) {
+          const long long off = lo - pre;
+          sch->b = b;
+          sch->h = static_cast<int>(off / nch);
+          sch->k = static_cast<int>(off % nch);
+          break;
+        }
+        pre += span;
+      }
+    }
+  }
+  __syncthreads();
+  const Sched sc = *sch;
+  const int n = sc.n_mine;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && nchunks > 0) {
+    if (lane == 0 && n > 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(qfull, g * 2 * BLK * 128);
-      for (int w = 0; w < g; ++w)
-        for (int half = 0; half < 2; ++half)
-          tma_load_2d(sQ + half * (MROWS * 128) + w * BLK * 128, &tmQ, qfull, (h * g + w) * HD + half * 64, b * BLK);
+      Walk w;
+      w.init(p, sc);
       int last_ci[ST];
       for (int i = 0; i < ST; ++i) last_ci[i] = -1;
+      int seg = -1, q_issued = -1;
       bool ok = true;
-      for (int ci = 0; ci < nchunks; ++ci) {
-        const int st = ci % ST;
-        if (!mbar_wait(&empty[st], static_cast<uint32_t>(((ci / ST) & 1) ^ 1), abort_flag, p.timeout_ns)) {
+      for (int i = 0; i < n; ++i) {
+        const int st = i % ST;
+        const bool first = i == 0 || w.k == 0;
+        if (first) ++seg;
+        if (!mbar_wait(&empty[st], static_cast<uint32_t>(((i / ST) & 1) ^ 1), abort_flag, p.timeout_ns)) {
           ok = false;
           break;
         }
-        uint8_t *dk = sK + st * K_BYTES, *dv = sV + st * V_BYTES;
+        // the KV page first: it streams while the previous (request, head) drains
         const CUtensorMap *mk = &tmBK, *mv = &tmBV;
-        int rowk = (b * p.nkv + h) * CH, rowv = (b * p.nkv + h) * HD;
-        if (ci < ctx_chunks) {
-          const int tok = t0 + ci * CH;
-          const int page = p.page_table[static_cast<size_t>(b) * p.max_pages + tok / CH];
+        int rowk = (w.b * p.nkv + w.h) * CH, rowv = (w.b * p.nkv + w.h) * HD;
+        bool load = true;
+        if (!w.block_chunk()) {
+          const int page = p.page_table[static_cast<size_t>(w.b) * p.max_pages + w.k];
           if (page < 0 || page >= p.num_pages) {
             report(p.status, DFLASH_ERR_DEVICE);
             mbar_arrive(&full[st]);   // completes the phase with no data
-            continue;
+            load = false;
+          } else {
+            mk = &tmK;
+            mv = &tmV;
+            rowk = (page * p.nkv + w.h) * CH;
+            rowv = (page * p.nkv + w.h) * HD;
           }
-          mk = &tmK;
-          mv = &tmV;
-          rowk = (page * p.nkv + h) * CH;
-          rowv = (page * p.nkv + h) * HD;
         }
-        mbar_arrive_expect_tx(&full[st], K_BYTES + V_BYTES);
-        tma_load_2d(dk, mk, &full[st], 0, rowk);
-        tma_load_2d(dk + K_BYTES / 2, mk, &full[st], 64, rowk);
-        tma_load_2d(dv, mv, &full[st], 0, rowv);
-        last_ci[st] = ci;
+        if (load) {
+          uint8_t *dk = sK + st * K_BYTES, *dv = sV + st * V_BYTES;
+          mbar_arrive_expect_tx(&full[st], K_BYTES + V_BYTES);
+          tma_load_2d(dk, mk, &full[st], 0, rowk);
+          tma_load_2d(dk + K_BYTES / 2, mk, &full[st], 64, rowk);
+          tma_load_2d(dv, mv, &full[st], 0, rowv);
+          last_ci[st] = i;
+        }
+        if (first) {   // the query rows of this (request, kv head), once its predecessor's QKs are done
+          if (seg > 0 && !mbar_wait(qempty, static_cast<uint32_t>((seg - 1) & 1), abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(qfull, (DUP ? 2 : 1) * g * 2 * BLK * 128);
+          for (int hw = 0; hw < g; ++hw)
+            for (int half = 0; half < 2; ++half) {
+              const int col = (w.h * g + hw) * HD + half * 64;
+              uint8_t *dst = sQ + half * (MROWS * 128) + (DUP ? 32 : BLK) * hw * 128;
+              tma_load_2d(dst, &tmQ, qfull, col, w.b * BLK);
+              if (DUP) tma_load_2d(dst + BLK * 128, &tmQ, qfull, col, w.b * BLK);
+            }
+          q_issued = seg;
+        }
+        w.next(p);
       }
       if (!ok) {
         report(p.status, DFLASH_ERR_TIMEOUT);
         *abort_flag = 1;
         for (int i = 0; i < ST; ++i)   // let every issued copy land before smem goes away
-          if (last_ci[i] >= 0) mbar_wait(&full[i], static_cast<uint32_t>((last_ci[i] / ST) & 1), nullptr, p.timeout_ns);
-        mbar_wait(qfull, 0, nullptr, p.timeout_ns);
+          if (last_ci[i] >= 0)
+            mbar_wait(&full[i], static_cast<uint32_t>((last_ci[i] / ST) & 1), nullptr, p.timeout_ns);
+        if (q_issued >= 0) mbar_wait(qfull, static_cast<uint32_t>(q_issued & 1), nullptr, p.timeout_ns);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nchunks > 0) {
+    // ------------------------------------------------------------ QK issuer
+    // (one thread issues a tcgen05.mma about every 100 cycles, so QK and PV
+    // have an issuing warp each and overlap on the tensor core)
+    if (lane == 0 && n > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(MROWS, CH);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(MROWS, HD);
-      const uint32_t pv_tmem = tmem + 128;
-      bool ok = mbar_wait(qfull, 0, abort_flag, p.timeout_ns);
-      auto issue_qk = [&](int ci) -> bool {
-        const int st = ci % ST, sb = ci & 1;
-        if (!mbar_wait(&full[st], static_cast<uint32_t>((ci / ST) & 1), abort_flag, p.timeout_ns)) return false;
-        if (!mbar_wait(&sempty[sb], static_cast<uint32_t>(((ci >> 1) & 1) ^ 1), abort_flag, p.timeout_ns)) return false;
+      Walk wq;
+      wq.init(p, sc);
+      int seg_q = -1;
+      bool ok = true;
+      for (int i = 0; i < n && ok; ++i) {
+        const int st = i % ST, sb = i % NSB;
+        const bool first = i == 0 || wq.k == 0;
+        const bool last = i == n - 1 || wq.k == wq.nch - 1;
+        if (first) ++seg_q;
+        ok = mbar_wait(&full[st], static_cast<uint32_t>((i / ST) & 1), abort_flag, p.timeout_ns) &&
+             (!first || mbar_wait(qfull, static_cast<uint32_t>(seg_q & 1), abort_flag, p.timeout_ns)) &&
+             mbar_wait(&sempty[sb], static_cast<uint32_t>(((i / NSB) & 1) ^ 1), abort_flag, p.timeout_ns);
+        if (!ok) break;
         tc_fence_after();
         const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + st * K_BYTES);
 #pragma unroll
@@ -208,31 +422,8 @@ __global__ void __launch_bounds__(NTHR, 1)
           umma_bf16(tmem + sb * CH, sdesc_k_sw128(q0 + (kk >> 2) * (MROWS * 128) + (kk & 3) * 32),
                     sdesc_k_sw128(k0 + (kk >> 2) * (K_BYTES / 2) + (kk & 3) * 32), idesc_qk, kk > 0 ? 1u : 0u);
         umma_commit(&sfull[sb]);
-        return true;
-      };
-      auto issue_pv = [&](int ci) -> bool {
-        const int st = ci % ST, pb = ci & 1;
-        // only the 16-token k-steps holding valid tokens: V columns past them
-        // (block slots 16..63, the unused tail of a last page) are never read,
-        // so whatever they hold cannot reach O through 0 * Inf
-        const int valid = ci < ctx_chunks ? min(CH, t1 - (t0 + ci * CH)) : BLK;
-        const int ksteps = (valid + 15) / 16;
-        if (!mbar_wait(&pfull[pb], static_cast<uint32_t>((ci >> 1) & 1), abort_flag, p.timeout_ns)) return false;
-        if (!mbar_wait(oempty, static_cast<uint32_t>((ci & 1) ^ 1), abort_flag, p.timeout_ns)) return false;
-        tc_fence_after();
-        const uint32_t p0 = smem_u32(sP + pb * P_BYTES), v0 = smem_u32(sV + st * V_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < CH / 16; ++kk)
-          if (kk < ksteps)
-            umma_bf16(pv_tmem, sdesc_k_sw128(p0 + kk * 32), sdesc_k_sw128(v0 + kk * 32), idesc_pv, kk > 0 ? 1u : 0u);
-        umma_commit(ofull);
-        umma_commit(&empty[st]);   // PV is the last reader of this KV stage
-        return true;
-      };
-      if (ok) ok = issue_qk(0);
-      for (int ci = 0; ci < nchunks && ok; ++ci) {
-        if (ci + 1 < nchunks) ok = issue_qk(ci + 1);
-        if (ok) ok = issue_pv(ci);
+        if (last) umma_commit(qempty);   // the Q buffer may take the next (request, head)
+        wq.next(p);
       }
       if (!ok) {
         report(p.status, DFLASH_ERR_TIMEOUT);
@@ -241,95 +432,264 @@ __global__ void __launch_bounds__(NTHR, 1)
       umma_commit(drain);   // every issued MMA retires before TMEM is released
       mbar_wait(drain, 0, nullptr, p.timeout_ns);
     }
-  } else {
-    // ------------------------------------------------------------ softmax / O
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(MROWS, HD);
+      Walk wp;
+      wp.init(p, sc);
+      int seg_p = -1;
+      bool ok = true;
+      for (int i = 0; i < n && ok; ++i) {
+        const int st = i % ST, pb = i & 1;
+        const bool first = i == 0 || wp.k == 0;
+        if (first) ++seg_p;
+        // only the 16-token k-steps holding valid tokens: V columns past them
+        // (block slots 16..63, the unused tail of a last page) are never read,
+        // so whatever they hold cannot reach O through 0 * Inf
+        const int ksteps = (wp.valid() + 15) / 16;
+        ok = mbar_wait(&pfull[pb], static_cast<uint32_t>((i >> 1) & 1), abort_flag, p.timeout_ns) &&
+             mbar_wait(&full[st], static_cast<uint32_t>((i / ST) & 1), abort_flag, p.timeout_ns) &&
+             (!first || seg_p == 0 ||
+              mbar_wait(oempty, static_cast<uint32_t>((seg_p - 1) & 1), abort_flag, p.timeout_ns));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t p0 = smem_u32(sP + pb * P_BYTES), v0 = smem_u32(sV + st * V_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < CH / 16; ++kk)
+          if (kk < ksteps)
+            umma_bf16(tmem + O_COL, sdesc_k_sw128(p0 + kk * 32), sdesc_k_sw128(v0 + kk * 32), idesc_pv,
+                      (kk > 0 || !first) ? 1u : 0u);
+        umma_commit(&pdone[pb]);
+        umma_commit(&empty[st]);   // PV is the last reader of this KV stage (its QK finished before P existed)
+        wp.next(p);
+      }
+      if (!ok) {
+        report(p.status, DFLASH_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      umma_commit(drain);
+      mbar_wait(drain, 0, nullptr, p.timeout_ns);
+    }
+  } else if ((warp & 3) * 32 < R && n > 0) {
+    // ------------------------------------------------------------ softmax
+    constexpr int NC = DUP ? CH / 2 : CH;           // scores per lane
     const int q = warp & 3;
-    const int r = q * 32 + lane;            // query row = TMEM lane
+    const int hi = DUP ? lane >> 4 : 0;             // DUP: second half of the chunk's columns
+    const int lrow = DUP ? q * 32 + (lane & 15) : q * 32 + lane;   // P / O row (TMEM lane) this lane serves
+    const int trow = DUP ? q * BLK + (lane & 15) : lrow;          // tile row 16 * head + position
+    const bool real = trow < BLK * g;
+    const bool olane = DUP ? lane < 16 : real;      // lanes whose own TMEM lane holds a real O row
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    float alpha_pending = 1.f;
-    bool failed = false;
-    for (int ci = 0; ci < nchunks; ++ci) {
-      const int sb = ci & 1, pb = ci & 1;
-      if (!mbar_wait(&sfull[sb], static_cast<uint32_t>((ci >> 1) & 1), abort_flag, p.timeout_ns)) {
+    Walk w;
+    w.init(p, sc);
+    int seg = -1, nparts = 0;
+    bool seg_whole = false, failed = false;
+    float m = -INFINITY, l = 0.f;   // running max (scaled, log2 domain) and sum of this lane's row
+    auto waitw = [&](uint64_t *b, uint32_t par) -> bool {   // warp-uniform bounded wait
+      const bool ok = mbar_wait(b, par, abort_flag, p.timeout_ns);
+      return !__any_sync(0xffffffffu, !ok);
+    };
+    for (int i = 0; i < n; ++i) {
+      const int sb = i % NSB;
+      const bool first = i == 0 || w.k == 0;
+      const bool last = i == n - 1 || w.k == w.nch - 1;
+      if (first) {
+        ++seg;
+        seg_whole = w.k == 0;
+      }
+      const int valid = w.valid();
+      if (!waitw(&sfull[sb], static_cast<uint32_t>((i / NSB) & 1))) {
         failed = true;
         break;
       }
       tc_fence_after();
-      float sc[CH];
+      float x[NC];
+      {
+        uint32_t r0[16], r1[16], r2[16], r3[16];   // the four loads in flight together
+        tmem_ld16_nw(lane_base + sb * CH, r0);
+        tmem_ld16_nw(lane_base + sb * CH + 16, r1);
+        tmem_ld16_nw(lane_base + sb * CH + 32, r2);
+        tmem_ld16_nw(lane_base + sb * CH + 48, r3);
+        tmem_wait_ld();
+        tmem_regs_ready(r0);
+        tmem_regs_ready(r1);
+        tmem_regs_ready(r2);
+        tmem_regs_ready(r3);
 #pragma unroll
-      for (int c = 0; c < CH / 16; ++c) {
-        float v[16];
-        tmem_ld16(lane_base + sb * CH + c * 16, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) sc[c * 16 + i] = v[i];
+        for (int c = 0; c < NC; ++c) {   // DUP: lanes 16-31 take columns 32..63 (a select, no indexing)
+          const uint32_t a = c < 16 ? r0[c & 15] : c < 32 ? r1[c & 15] : c < 48 ? r2[c & 15] : r3[c & 15];
+          const uint32_t b = c < 16 ? r2[c & 15] : r3[c & 15];
+          x[c] = __uint_as_float((DUP && hi) ? b : a);
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[sb]);
-      const int valid = ci < ctx_chunks ? min(CH, t1 - (t0 + ci * CH)) : BLK;
-      float mx = -INFINITY;
+      if (valid < CH) {   // last page or block keys: mask the columns past the valid tokens
+        const int c0 = hi * NC;
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        sc[c] = c < valid ? sc[c] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, sc[c]);
+        for (int c = 0; c < NC; ++c)
+          if (c0 + c >= valid) x[c] = -INFINITY;
       }
-      const float mn = fmaxf(m, mx);
-      const float alpha = fast_exp2(m - mn);
-      float rs = 0.f;
+      float mx;
+      {
+        float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        sc[c] = fast_exp2(sc[c] - mn);
-        rs += sc[c];
+        for (int c = 4; c < NC; c += 4) {
+          a0 = fmaxf(a0, x[c]);
+          a1 = fmaxf(a1, x[c + 1]);
+          a2 = fmaxf(a2, x[c + 2]);
+          a3 = fmaxf(a3, x[c + 3]);
+        }
+        mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+        if (DUP) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       }
-      l = l * alpha + rs;
-      m = mn;
-      // P row -> smem (bf16, 128-byte swizzled K-major A operand of PV)
-      uint8_t *prow = sP + pb * P_BYTES + r * 128;
+      const float mxs = mx * p.scale_log2;
+      if (first) {
+        m = mxs;
+        l = 0.f;
+      } else {
+        const bool need = mxs > m + RESCALE_LOG2;
+        if (__any_sync(0xffffffffu, need)) {   // O holds chunks up to i-1: wait for that PV, rescale in TMEM
+          if (!waitw(&pdone[(i - 1) & 1], static_cast<uint32_t>(((i - 1) >> 1) & 1))) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const float f = need ? fast_exp2(m - mxs) : 1.f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+          for (int c0 = 0; c0 < HD / 16; c0 += 4) {   // four loads in flight, then four stores
+            uint32_t ov[4][16];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) tmem_ld16_nw(lane_base + O_COL + (c0 + u) * 16, ov[u]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              tmem_regs_ready(ov[u]);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) ov[u][j] = __float_as_uint(__uint_as_float(ov[u][j]) * f);
+              tmem_st16_nw(lane_base + O_COL + (c0 + u) * 16, ov[u]);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          if (need) {
+            l *= f;
+            m = mxs;
+          }
+        }
+      }
+      const float nm = -m;
+      float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+#pragma unroll
+      for (int c = 0; c < NC; c += 4) {
+        x[c] = fast_exp2(fmaf(x[c], p.scale_log2, nm));
+        x[c + 1] = fast_exp2(fmaf(x[c + 1], p.scale_log2, nm));
+        x[c + 2] = fast_exp2(fmaf(x[c + 2], p.scale_log2, nm));
+        x[c + 3] = fast_exp2(fmaf(x[c + 3], p.scale_log2, nm));
+        r0 += x[c];
+        r1 += x[c + 1];
+        r2 += x[c + 2];
+        r3 += x[c + 3];
+      }
+      float rs = (r0 + r1) + (r2 + r3);
+      if (DUP) rs += __shfl_xor_sync(0xffffffffu, rs, 16);
+      l += rs;
+      // P buffer i&1 was last read by the PV of chunk i-2
+      if (i >= 2 && !waitw(&pdone[i & 1], static_cast<uint32_t>(((i - 2) >> 1) & 1))) {
+        failed = true;
+        break;
+      }
+      uint8_t *prow = sP + (i & 1) * P_BYTES + lrow * 128;   // 128-byte swizzled K-major rows
+#pragma unroll
+      for (int kk = 0; kk < NC / 8; ++kk) {
+        const int k = hi * (NC / 8) + kk;
         uint4 u;
-        u.x = pack_bf16(sc[8 * k + 0], sc[8 * k + 1]);
-        u.y = pack_bf16(sc[8 * k + 2], sc[8 * k + 3]);
-        u.z = pack_bf16(sc[8 * k + 4], sc[8 * k + 5]);
-        u.w = pack_bf16(sc[8 * k + 6], sc[8 * k + 7]);
-        *reinterpret_cast<uint4 *>(prow + ((k ^ (r & 7)) << 4)) = u;
+        u.x = pack_bf16(x[8 * kk + 0], x[8 * kk + 1]);
+        u.y = pack_bf16(x[8 * kk + 2], x[8 * kk + 3]);
+        u.z = pack_bf16(x[8 * kk + 4], x[8 * kk + 5]);
+        u.w = pack_bf16(x[8 * kk + 6], x[8 * kk + 7]);
+        *reinterpret_cast<uint4 *>(prow + ((k ^ (lrow & 7)) << 4)) = u;
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&pfull[pb]);
-      if (ci > 0) {   // fold in the previous chunk's PV (relative to that chunk's max)
-        if (!mbar_wait(ofull, static_cast<uint32_t>((ci - 1) & 1), abort_flag, p.timeout_ns)) {
+      if (lane == 0) mbar_arrive(&pfull[i & 1]);
+
+      if (last) {
+        // ---- end of this CTA's part of a (request, kv head)
+        if (!waitw(&pdone[i & 1], static_cast<uint32_t>((i >> 1) & 1))) {
           failed = true;
           break;
         }
         tc_fence_after();
+        const bool whole = seg_whole && w.k == w.nch - 1;
+        const int hq = w.h * g + trow / BLK, j = trow % BLK;
+        const size_t orow = static_cast<size_t>(w.b * BLK + j) * p.ldo + static_cast<size_t>(hq) * HD;
+        float *part = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + (seg == 0 ? 0 : 1)) * ATTN_PART_FLOATS;
+        const float inv = 1.f / l;
 #pragma unroll
-        for (int c = 0; c < HD / 16; ++c) {
-          float v[16];
-          tmem_ld16(lane_base + 128 + c * 16, v);
+        for (int c0 = 0; c0 < HD / 16; c0 += 4) {   // four loads in flight
+          uint32_t ov[4][16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) O[c * 16 + i] = O[c * 16 + i] * alpha_pending + v[i];
+          for (int u = 0; u < 4; ++u) tmem_ld16_nw(lane_base + O_COL + (c0 + u) * 16, ov[u]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            tmem_regs_ready(ov[u]);
+            const int c = c0 + u;
+            float v[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(ov[u][t]);
+            if (olane) {
+              if (whole) {
+                store16_hl(p.out + orow + c * 16, p.out_lo ? p.out_lo + orow + c * 16 : nullptr, v, inv);
+              } else {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) part[(c * 16 + t) * MROWS + trow] = v[t];   // O^T: coalesced over rows
+              }
+            }
+          }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(oempty);
-      }
-      alpha_pending = alpha;
-    }
-    if (!failed && nchunks > 0) {
-      if (mbar_wait(ofull, static_cast<uint32_t>((nchunks - 1) & 1), abort_flag, p.timeout_ns)) {
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < HD / 16; ++c) {
-          float v[16];
-          tmem_ld16(lane_base + 128 + c * 16, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) O[c * 16 + i] = O[c * 16 + i] * alpha_pending + v[i];
+        if (lane == 0) mbar_arrive(oempty);   // the next (request, head) may overwrite O
+        if (!whole) {
+          if (olane) {
+            part[HD * MROWS + trow] = m;
+            part[HD * MROWS + MROWS + trow] = l;
+          }
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(mready);
+          const long long start = w.x - w.k, end = start + w.nch;
+          const int cf = run_owner(start, sc.total, sc.G), cl = run_owner(end - 1, sc.total, sc.G);
+          if (q == 0 && lane == 0) {
+            int flag = 0;
+            if (mbar_wait(mready, static_cast<uint32_t>(nparts & 1), abort_flag, p.timeout_ns)) {
+              __threadfence();
+              int *ctr = p.counters + w.b * p.nkv + w.h;
+              const int old = atomicAdd(ctr, 1);
+              if (old == cl - cf) {   // every contributor's partial is in: merge here
+                atomicExch(ctr, 0);
+                __threadfence();
+                flag = 1;
+              }
+            }
+            sch->merge_flag = flag;
+            mbar_arrive(mdone);
+          }
+          if (!waitw(mdone, static_cast<uint32_t>(nparts & 1))) {
+            failed = true;
+            break;
+          }
+          ++nparts;
+          if (sch->merge_flag && real)   // DUP: the two lanes of a row take 64 columns each
+            merge_row(p, sc, cf, cl, start, trow, DUP ? hi * 64 : 0, DUP ? 64 : HD, p.out + orow,
+                      p.out_lo ? p.out_lo + orow : nullptr);
         }
-        tc_fence_before();
-      } else {
-        failed = true;
       }
+      w.next(p);
     }
     if (failed) {
       report(p.status, DFLASH_ERR_TIMEOUT);
@@ -342,66 +702,6 @@ __global__ void __launch_bounds__(NTHR, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
-
-  const int qq = warp & 3;
-  const int rr = qq * 32 + lane;
-  const bool row_thread = warp >= 2 && rr < R;
-  if (p.S == 1) {
-    if (row_thread && nchunks > 0) {
-      const int hq = h * g + rr / BLK, j = rr % BLK;
-      const float inv = 1.f / l;
-      const size_t o0 = static_cast<size_t>(b * BLK + j) * p.ldo + hq * HD;
-#pragma unroll
-      for (int c = 0; c < HD; c += 2) store2_hl(p.out, p.out_lo, o0 + c, O[c] * inv, O[c + 1] * inv);
-    }
-    return;
-  }
-
-  // ---- cluster merge: every CTA publishes (m, l, O) of its rows in its own
-  // smem; after a cluster barrier CTA k finalises rows [k*R/S, (k+1)*R/S)
-  // reading all S partials through distributed shared memory
-  float *xo = reinterpret_cast<float *>(sK);            // [128][HD] partial O
-  float *xml = xo + MROWS * HD;                           // [128][2] (max, sum)
-  if (row_thread) {
-#pragma unroll
-    for (int c = 0; c < HD; c += 4)
-      *reinterpret_cast<float4 *>(xo + rr * HD + c) = make_float4(O[c], O[c + 1], O[c + 2], O[c + 3]);
-    xml[2 * rr] = m;
-    xml[2 * rr + 1] = l;
-  }
-  cluster_sync();
-  const int per = R / p.S;
-  const int rank = static_cast<int>(cluster_ctarank());
-  for (int it = threadIdx.x; it < per * (HD / 4); it += NTHR) {
-    const int row = rank * per + it / (HD / 4), c4 = it % (HD / 4);
-    float M = -INFINITY;
-    float2 ml[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      ml[k] = k < p.S ? ld_dsmem_f2(dsmem_addr(xml + 2 * row, k)) : make_float2(-INFINITY, 0.f);
-      M = fmaxf(M, ml[k].x);
-    }
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (k < p.S) {
-        const float w = ml[k].y > 0.f ? fast_exp2(ml[k].x - M) : 0.f;
-        L += w * ml[k].y;
-        const float4 v = ld_dsmem_f4(dsmem_addr(xo + row * HD + 4 * c4, k));
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
-      }
-    }
-    const float inv = 1.f / L;
-    const int hq = h * g + row / BLK, j = row % BLK;
-    const size_t dst = static_cast<size_t>(b * BLK + j) * p.ldo + hq * HD + 4 * c4;
-    store2_hl(p.out, p.out_lo, dst, acc.x * inv, acc.y * inv);
-    store2_hl(p.out, p.out_lo, dst + 2, acc.z * inv, acc.w * inv);
-  }
-  cluster_sync();   // nobody leaves while others still read its smem
 }
 
 // ------------------------------------------------------------------ fp32
@@ -464,17 +764,27 @@ __global__ void __launch_bounds__(512) attn_f32_kernel(const float *q, int ldq, 
 
 }  // namespace
 
+
 int attention_bf16(const Launch &lc, const AttnArgs &a) {
   if (a.B <= 0) return DFLASH_OK;
   if (a.d != HD || a.page_size != CH)
     return set_error(DFLASH_ERR_UNSUPPORTED, "bf16 attention needs head_dim 128 and 64-token pages");
   const int g = a.nq / a.nkv;
-  if (g < 1 || g > 8) return set_error(DFLASH_ERR_UNSUPPORTED, "bf16 attention: q heads per kv head must be 1..8");
-  if (a.max_splits != 1 && a.max_splits != 2 && a.max_splits != 4 && a.max_splits != 8)
-    return set_error(DFLASH_ERR_UNSUPPORTED, "bf16 attention: splits per request must be 1, 2, 4 or 8");
+  if (g < 1 || g > 8 || g * a.nkv != a.nq)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "bf16 attention: q heads per kv head must be 1..8");
+  if (!a.counters || !a.partials) return set_error(DFLASH_ERR_ARG, "bf16 attention: scratch missing");
+  const int grid = lc.num_sms;
+  if (a.partial_slots < 2ull * grid) return set_error(DFLASH_ERR_SHAPE, "bf16 attention: partial scratch too small");
+  if (static_cast<size_t>(a.B) * a.nkv > a.counter_cap)
+    return set_error(DFLASH_ERR_SHAPE, "bf16 attention: batch x kv heads over the counter capacity");
   static bool attr_done = false;
   if (!attr_done) {
-    if (int e = cuda_check(cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM),
+    if (int e = cuda_check(cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                SMEM),
+                           "attention smem attribute"))
+      return e;
+    if (int e = cuda_check(cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                SMEM),
                            "attention smem attribute"))
       return e;
     attr_done = true;
@@ -499,29 +809,19 @@ int attention_bf16(const Launch &lc, const AttnArgs &a) {
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
   p.ctx_len = a.ctx_len;
+  p.B = a.B;
   p.nkv = a.nkv;
   p.g = g;
-  p.split = a.split_tokens;
-  p.S = a.max_splits;
+  p.min_chunks = a.min_chunks > 0 ? a.min_chunks : DEFAULT_MIN_CHUNKS;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(HD)));
+  p.counters = a.counters;
+  p.partials = a.partials;
   p.status = lc.status;
   p.timeout_ns = lc.timeout_ns;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.max_splits, a.nkv, a.B);
-  cfg.blockDim = dim3(NTHR);
-  cfg.dynamicSmemBytes = SMEM;
-  cfg.stream = lc.stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = a.max_splits;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
   ProfScope ps(lc, "attention", -1.0, -1.0);
-  return cuda_check(cudaLaunchKernelEx(&cfg, attn_tc_kernel, tQ, tK, tV, tBK, tBV, p), "attention launch");
+  return cuda_check(launch_pdl(g <= 4 ? attn_tc_kernel<true> : attn_tc_kernel<false>, dim3(grid), dim3(NTHR), SMEM,
+                               lc.stream, tQ, tK, tV, tBK, tBV, p),
+                    "attention launch");
 }
 
 int attention_f32(const Launch &lc, const AttnArgs &a) {

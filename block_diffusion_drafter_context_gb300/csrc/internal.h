@@ -113,9 +113,14 @@ struct AttnArgs {
   void *out;                // [B*16][nq*d] (dtype)
   void *out_lo;             // low bf16 halves of out, or null
   int B, nq, nkv, d;
-  int split_tokens;         // multiple of page_size
-  int max_splits;           // splits per (request, kv head) = cluster size: 1, 2, 4 or 8
+  int min_chunks;           // bf16: at least this many 64-token chunks per CTA (0 = default)
+  int *counters;            // bf16: [counter_cap] ints, zero between launches (self-resetting)
+  size_t counter_cap;       // >= B * nkv
+  float *partials;          // bf16: [partial_slots][ATTN_PART_FLOATS] merge scratch
+  size_t partial_slots;     // >= 2 * SM count
 };
+// one split partial of the bf16 attention: O^T [128 d][128 rows], max [128], sum [128]
+constexpr int ATTN_PART_FLOATS = 128 * 128 + 2 * 128;
 int attention_bf16(const Launch &lc, const AttnArgs &a);
 int attention_f32(const Launch &lc, const AttnArgs &a);
 

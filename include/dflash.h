@@ -66,6 +66,10 @@ enum {
 
 enum { DFLASH_BF16 = 0, DFLASH_F32 = 1 };
 
+/* Largest batch (requests per call) the workspace header is sized for; a
+ * larger batch returns DFLASH_ERR_ARG. */
+#define DFLASH_MAX_BATCH 4096
+
 /* Drafter shape and flags.  block_size and top_k must be 16, page_size 64. */
 typedef struct dflash_config {
   int dtype;             /* DFLASH_BF16 or DFLASH_F32                        */
@@ -234,8 +238,9 @@ DFLASH_API int dflash_set_wait_timeout(dflash_ctx *ctx, unsigned long long ns);
 /* Test hook: cap the CTA count of the persistent GEMM (0 = SM count). */
 DFLASH_API int dflash_set_gemm_ctas(dflash_ctx *ctx, int ctas);
 
-/* Test hook: force the split length of the block attention in tokens (a
- * multiple of the page size; 0 = automatic). */
+/* Test hook: the least number of context tokens (a multiple of the page
+ * size) the bf16 block attention gives each CTA of its balanced split; 64
+ * splits the chunk list as finely as the SM count allows, 0 = automatic. */
 DFLASH_API int dflash_set_attn_split(dflash_ctx *ctx, int tokens);
 
 /* Per-launch CUDA-event timing of every kernel the next calls launch (on
