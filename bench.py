@@ -122,12 +122,17 @@ def aggregate_blocks_per_s(world: int, batch_per_rank: int, steps: int, max_ms: 
 
 
 # ---------------------------------------------------------------- CPU oracle
-def oracle_setup(wl, W, ctx, X_prefill, cu):
+def oracle_setup(wl, W, ctx, X_prefill, cu, requests=None, templates=None, table=None):
+    """The oracle's context KV of each request (None for requests not listed)."""
     import oracle as O
-    kvs = []
-    for b in range(wl.batch):
+    kvs = [None] * wl.batch
+    for b in (range(wl.batch) if requests is None else requests):
         n = int(ctx[b])
-        kvs.append(O.inject_context(wl.cfg, W, X_prefill[cu[b]:cu[b + 1]], np.arange(n)))
+        if templates is not None:
+            tk, tv, pmap = templates
+            kvs[b] = [(O.f64(k), O.f64(v)) for k, v in gen.template_request_kv(wl.cfg, tk, tv, pmap, table[b], n)]
+        else:
+            kvs[b] = O.inject_context(wl.cfg, W, X_prefill[cu[b]:cu[b + 1]], np.arange(n))
     return kvs
 
 
@@ -159,17 +164,26 @@ def make_inputs(wl):
     B = len(ctx)
     table, npages = gen.page_table(ctx + 16, cfg.page_size, wl.seed)
     cu = np.concatenate([[0], np.cumsum(ctx)]).astype(np.int32)
-    Xp = gen.target_hidden(cfg, int(ctx.sum()), wl.seed, "prefill")
+    # drawn cache state (template pages) or a prefill through the injection
+    Xp = None if wl.kv_fill == "template" else gen.target_hidden(cfg, int(ctx.sum()), wl.seed, "prefill")
     Xn = gen.target_hidden(cfg, 16 * B, wl.seed, "step")
     anchor = gen.anchors(wl)
     return W, ctx, table, npages, cu, Xp, Xn, anchor
+
+
+def kv_templates(wl, npages):
+    """(K templates, V templates, page map) of a drawn cache state, else None."""
+    if wl.kv_fill != "template":
+        return None
+    tk, tv = gen.kv_templates(wl.cfg, wl.kv_templates, wl.seed)
+    return tk, tv, gen.kv_page_map(wl.cfg, npages, wl.kv_templates, wl.seed)
 
 
 def run_reference(args, wl):
     """The reference arm: the fp64 oracle on the host cores."""
     W, ctx, table, npages, cu, Xp, Xn, anchor = make_inputs(wl)
     t0 = time.time()
-    kvs = oracle_setup(wl, W, ctx, Xp, cu)
+    kvs = oracle_setup(wl, W, ctx, Xp, cu, templates=kv_templates(wl, npages), table=table)
     setup_s = time.time() - t0
     import oracle as O
     first = oracle_step(wl, W, kvs, ctx, Xn, anchor, np.zeros((wl.batch, 16), np.int32), range(wl.batch))
@@ -219,16 +233,23 @@ def run_ours(args, wl):
     t_setup = time.time()
     W, ctx, table, npages, cu, Xp, Xn, anchor = make_inputs(wl)
     B = wl.batch
-    dr = Drafter(cfg, W, max_batch=B, max_new_tokens=max(16 * B, int(ctx.max())), device=dev)
+    prefill = 0 if wl.kv_fill == "template" else int(ctx.max())
+    dr = Drafter(cfg, W, max_batch=B, max_new_tokens=max(16 * B, prefill), device=dev)
     kv = PagedKV(cfg, table, npages, device=dev)
     stream = torch.cuda.current_stream().cuda_stream
-    # prefill: inject the whole context (chunked per request when large)
-    ctx0 = torch.zeros(B, dtype=torch.int32, device=dev)
-    ctx_n = torch.empty(B, dtype=torch.int32, device=dev)
-    for b in range(B):   # one request at a time through a view of its page-table row
-        one_cu = to_device(np.array([0, ctx[b]], np.int32), dev)
-        Bd.dflash_inject_context(dr.ctx, kv.row(b), to_device(Xp[cu[b]:cu[b + 1]], dev), one_cu,
-                                 int(ctx[b]), ctx0[:1], ctx_n[b:b + 1], 1, dr.workspace, dr.ws_bytes, stream)
+    templates = kv_templates(wl, npages)
+    if templates is not None:
+        # drawn cache state: template pages mapped onto the pool
+        kv.fill_from_templates(*templates)
+    else:
+        # prefill: inject the whole context, one request at a time through a
+        # view of its page-table row
+        ctx0 = torch.zeros(B, dtype=torch.int32, device=dev)
+        ctx_n = torch.empty(B, dtype=torch.int32, device=dev)
+        for b in range(B):
+            one_cu = to_device(np.array([0, ctx[b]], np.int32), dev)
+            Bd.dflash_inject_context(dr.ctx, kv.row(b), to_device(Xp[cu[b]:cu[b + 1]], dev), one_cu,
+                                     int(ctx[b]), ctx0[:1], ctx_n[b:b + 1], 1, dr.workspace, dr.ws_bytes, stream)
     torch.cuda.synchronize()
     n_b = to_device(ctx.astype(np.int32), dev)
     cu_new = to_device((16 * np.arange(B + 1)).astype(np.int32), dev)
@@ -381,7 +402,7 @@ def run_ours(args, wl):
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only)
     cpu = None
     if world == 1 and not args.skip_cpu:
-        kvs = oracle_setup(wl, W, ctx, Xp, cu)
+        kvs = oracle_setup(wl, W, ctx, Xp, cu, requests=[0], templates=templates, table=table)
         t0 = time.perf_counter()
         oracle_step(wl, W, kvs, ctx, Xn, anchor, tgt, [0])
         el = time.perf_counter() - t0

@@ -528,8 +528,13 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   p.kbpt = (K + BK - 1) / BK;
   const long long tiles = static_cast<long long>(p.rtpg) * p.n_groups * p.tok_tiles;
   p.total = tiles * p.kbpt;
+  // CTAs: at most one per SM, at least 4 k-blocks each, and no tile cut into
+  // more pieces than keep its fixup (the last piece sums the others' fp32
+  // partials from L2) under 256 KB: 32 pieces at BN = 16, 4 at BN = 128
   const int cap = lc.gemm_ctas > 0 ? lc.gemm_ctas : lc.num_sms;
-  p.G = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, (p.total + 3) / 4)));
+  const int max_parts = std::max(2, (256 * 1024) / (BM * BN * 4));
+  const int min_kb = std::max(4, (p.kbpt + max_parts - 1) / max_parts);
+  p.G = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, (p.total + min_kb - 1) / min_kb)));
   p.epi = epi;
   p.out = op.out;
   p.ldo = op.ldo;

@@ -121,6 +121,20 @@ class PagedKV:
         self.struct = B.dflash_kv(self.k.data_ptr(), self.v.data_ptr(), self.page_table.data_ptr(),
                                   self.num_pages, self.max_pages)
 
+    def fill_from_templates(self, tk: np.ndarray, tv: np.ndarray, page_map: np.ndarray):
+        """Set a drawn cache state: pool page p of layer l takes template page
+        page_map[l, p] of tk / tv ([L][T][nkv][page][d]); V is stored
+        transposed like every V page.  Set-up only (device copies)."""
+        torch = _torch()
+        dev = self.k.device
+        for l in range(self.k.shape[0]):
+            idx = torch.from_numpy(page_map[l].astype(np.int64)).to(dev)
+            kt = to_device(tk[l], dev).to(self.k.dtype)
+            vt = to_device(tv[l], dev).to(self.v.dtype).transpose(2, 3).contiguous()
+            self.k[l].copy_(kt.index_select(0, idx))
+            self.v[l].copy_(vt.index_select(0, idx))
+            del kt, vt
+
     def row(self, b: int) -> B.dflash_kv:
         """dflash_kv whose page table is request b's row alone (a batch of one)."""
         r = self.page_table[b:b + 1]

@@ -176,6 +176,32 @@ def page_table(ctx_capacity: np.ndarray, page_size: int, seed: int):
     return tab, total
 
 
+def kv_templates(cfg, n_templates: int, seed: int):
+    """Template KV pages for a drawn cache state: (K, V), each
+    [L][n_templates][nkv][page][d], N(0,1) entries in cfg.dtype."""
+    shape = (cfg.n_layers, n_templates, cfg.n_kv_heads, cfg.page_size, cfg.head_dim)
+    return (normal(shape, 1.0, seed, "kv_tmpl.k", cfg.dtype), normal(shape, 1.0, seed, "kv_tmpl.v", cfg.dtype))
+
+
+def kv_page_map(cfg, num_pages: int, n_templates: int, seed: int) -> np.ndarray:
+    """[L][num_pages] int32: the template page each pool page of each layer holds."""
+    g = _gen(seed, "kv_page_map", 0)
+    return g.integers(0, n_templates, size=(cfg.n_layers, num_pages)).astype(np.int32)
+
+
+def template_request_kv(cfg, tk, tv, page_map, table_row, n: int):
+    """Stored (K, V) [n, nkv, d] per layer of a request whose context is a
+    drawn cache state: token t sits in slot t % page of pool page
+    table_row[t // page], which holds template page page_map[l, page]."""
+    t = np.arange(n)
+    page = np.asarray(table_row)[t // cfg.page_size]
+    out = []
+    for l in range(cfg.n_layers):
+        tm = page_map[l][page]
+        out.append((tk[l][tm, :, t % cfg.page_size, :], tv[l][tm, :, t % cfg.page_size, :]))
+    return out
+
+
 def target_ids(draft: np.ndarray, p_accept, vocab: int, seed: int, step: int = 0) -> np.ndarray:
     """Synthetic target tokens [B, 16] for greedy verification.
 

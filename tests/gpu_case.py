@@ -41,19 +41,25 @@ class Case:
         self.ctx = gen.context_lengths(wl)
         self.B = len(self.ctx)
         self.table, self.npages = gen.page_table(self.ctx + 16, cfg.page_size, wl.seed)
-        self.X = gen.target_hidden(cfg, int(self.ctx.sum()), wl.seed, "prefill")
+        self.template = wl.kv_fill == "template"
+        self.X = None if self.template else gen.target_hidden(cfg, int(self.ctx.sum()), wl.seed, "prefill")
         self.cu = np.concatenate([[0], np.cumsum(self.ctx)]).astype(np.int32)
         self.anchor = gen.anchors(wl)
         self.device = device
         self.per_request = per_request
-        self.dr = Drafter(cfg, self.W, max_batch=self.B,
-                          max_new_tokens=max(16 * self.B, int(self.ctx.max() if per_request else self.ctx.sum())),
-                          device=device)
+        prefill = 0 if self.template else int(self.ctx.max() if per_request else self.ctx.sum())
+        self.dr = Drafter(cfg, self.W, max_batch=self.B, max_new_tokens=max(16 * self.B, prefill), device=device)
         if gemm_ctas:
             Bd.dflash_set_gemm_ctas(self.dr.ctx, gemm_ctas)
         self.kv = PagedKV(cfg, self.table, self.npages, device=device)
         self.ctx_d = torch.zeros(self.B, dtype=torch.int32, device=device)
-        if per_request:
+        if self.template:
+            # drawn cache state: template pages mapped onto the pool
+            self.tk, self.tv = gen.kv_templates(cfg, wl.kv_templates, wl.seed)
+            self.pmap = gen.kv_page_map(cfg, self.npages, wl.kv_templates, wl.seed)
+            self.kv.fill_from_templates(self.tk, self.tv, self.pmap)
+            self.ctx_d.copy_(to_device(self.ctx, device))
+        elif per_request:
             # one injection call per request, through a view of its page-table row
             zero = torch.zeros(1, dtype=torch.int32, device=device)
             for b in range(self.B):
@@ -75,6 +81,9 @@ class Case:
         if n == 0:
             z = np.zeros((0, self.cfg.n_kv_heads, self.cfg.head_dim))
             return [(z, z) for _ in range(self.cfg.n_layers)]
+        if self.template:
+            return [(O.f64(k), O.f64(v)) for k, v in
+                    gen.template_request_kv(self.cfg, self.tk, self.tv, self.pmap, self.table[b], n)]
         return O.inject_context(self.cfg, self.W, self.X[self.cu[b]:self.cu[b + 1]], np.arange(n))
 
     @functools.lru_cache(maxsize=None)

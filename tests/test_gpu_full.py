@@ -1,9 +1,10 @@
-"""Parity at the full sizes of the Qwen3-8B-shaped workloads.
+"""Parity at the full sizes of the benchmark workloads.
 
 C1 (batch 1, context 2048) is checked whole.  C2 (32 ragged requests,
-contexts 1k-8k) and C3 (DFlash-2, 8 requests x 4096) run whole on the GPU
-and are checked on sampled requests the oracle computes one by one (every
-request is independent of the others: the isolation invariant)."""
+contexts 1k-8k), C3 (DFlash-2, 8 requests x 4096) and C4 (27B-class, 64
+requests x 16k-32k, ~32 GB of draft KV) run whole on the GPU and are checked
+on sampled requests the oracle computes one by one (every request is
+independent of the others: the isolation invariant)."""
 import numpy as np
 import pytest
 
@@ -68,4 +69,12 @@ def test_c2_ragged_sampled():
 def test_c3_dflash2_sampled():
     c = Case("C3", per_request=True)
     check_requests(c, [0, c.B - 1])
+    c.dr.close()
+
+
+def test_c4_27b_class_sampled():
+    c = Case("C4")
+    assert to_np(c.ctx_d).tolist() == c.ctx.tolist()
+    order = np.argsort(c.ctx)
+    check_requests(c, [int(order[0]), int(order[-1])])
     c.dr.close()
