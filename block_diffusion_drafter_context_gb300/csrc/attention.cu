@@ -63,6 +63,7 @@ struct Params {
   const int32_t *ctx_len;
   int B, nkv, g;
   int min_chunks;          // at least this many chunks per CTA
+  int cs;                  // >1: cluster mode, cs CTAs (one cluster) per (request, kv head)
   float scale_log2;
   int *counters;           // [B * nkv], zero between launches
   float *partials;         // [gridDim.x * 2][ATTN_PART_FLOATS]
@@ -142,61 +143,81 @@ __device__ __forceinline__ void store16_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo,
   }
 }
 
-// Partial slot of contributor CTA cc to the (request, kv head) whose list
-// starts at global chunk `start`: 0 when that list is cc's first segment.
-__device__ __forceinline__ const float *part_of(const Params &p, const Sched &sc, int cc, int cf, long long start) {
-  const int slot = (cc > cf || run_lo(cc, sc.total, sc.G) == start) ? 0 : 1;
-  return p.partials + (static_cast<size_t>(cc) * 2 + slot) * ATTN_PART_FLOATS;
-}
-
 // Last arriver of a (request, kv head): combine the (max, sum, O) partials of
-// contributors cf..cl for tile row `trow`, columns [c0, c0 + ncol); loads of
-// four contributors are in flight together.
-__device__ __noinline__ void merge_row(const Params &p, const Sched &sc, int cf, int cl, long long start, int trow,
-                                       int c0, int ncol, __nv_bfloat16 *out, __nv_bfloat16 *out_lo) {
+// contributor CTAs cf..cl for tile row `trow`, columns [c0, c0 + 64 * nq).
+// A partial is O rows [128][HD] (row-major, fp32), max [128], sum [128];
+// contributor cc's slot is 0 when this (request, head) is its first segment,
+// which holds for every contributor but possibly the first.  The (max, sum)
+// of up to 16 contributors load together; O of two contributors per round
+// trip, 16 float4 per row half.
+constexpr int MERGE_MAX = 16;
+__device__ __noinline__ void merge_row(const Params &p, int cf, int cl, bool first_slot0, int trow, int c0, int nq64,
+                                       __nv_bfloat16 *out, __nv_bfloat16 *out_lo) {
+  auto part = [&](int cc) -> const float * {
+    const int slot = (cc > cf || first_slot0) ? 0 : 1;
+    return p.partials + (static_cast<size_t>(cc) * 2 + slot) * ATTN_PART_FLOATS;
+  };
+  const int np = cl - cf + 1;
+  float mw[MERGE_MAX], lw[MERGE_MAX];
   float M = -INFINITY;
-  for (int cc0 = cf; cc0 <= cl; cc0 += 4) {
-    float mv[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      mv[u] = cc0 + u <= cl ? __ldcg(part_of(p, sc, cc0 + u, cf, start) + HD * MROWS + trow) : -INFINITY;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) M = fmaxf(M, mv[u]);
+  for (int u = 0; u < MERGE_MAX; ++u) {
+    mw[u] = u < np ? __ldcg(part(cf + u) + HD * MROWS + trow) : -INFINITY;
+    lw[u] = u < np ? __ldcg(part(cf + u) + HD * MROWS + MROWS + trow) : 0.f;
   }
+  for (int cc = cf + MERGE_MAX; cc <= cl; ++cc) M = fmaxf(M, __ldcg(part(cc) + HD * MROWS + trow));
+#pragma unroll
+  for (int u = 0; u < MERGE_MAX; ++u) M = fmaxf(M, mw[u]);
   float L = 0.f;
-  for (int cc0 = cf; cc0 <= cl; cc0 += 4) {
-    float mv[4], lv[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const bool in = cc0 + u <= cl;
-      const float *pp = part_of(p, sc, in ? cc0 + u : cf, cf, start);
-      mv[u] = in ? __ldcg(pp + HD * MROWS + trow) : -INFINITY;
-      lv[u] = in ? __ldcg(pp + HD * MROWS + MROWS + trow) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) L += (lv[u] > 0.f ? fast_exp2(mv[u] - M) : 0.f) * lv[u];
+  for (int u = 0; u < MERGE_MAX; ++u) {
+    mw[u] = u < np ? fast_exp2(mw[u] - M) : 0.f;   // now the contributor's weight
+    L += mw[u] * lw[u];
+  }
+  for (int cc = cf + MERGE_MAX; cc <= cl; ++cc) {
+    const float *pp = part(cc);
+    L += fast_exp2(__ldcg(pp + HD * MROWS + trow) - M) * __ldcg(pp + HD * MROWS + MROWS + trow);
   }
   const float inv = 1.f / L;
-  for (int c = c0; c < c0 + ncol; c += 16) {
-    float acc[16];
+  for (int h = 0; h < nq64; ++h) {          // 64-column halves of this lane's range
+    const int cb = c0 + 64 * h;
+    float acc[64];
 #pragma unroll
-    for (int t = 0; t < 16; ++t) acc[t] = 0.f;
-    for (int cc0 = cf; cc0 <= cl; cc0 += 4) {
-      float wv[4], vv[4][16];
+    for (int t = 0; t < 64; ++t) acc[t] = 0.f;
+    for (int cc = cf; cc <= cl; cc += 2) {
+      const bool two = cc + 1 <= cl;
+      const float4 *a = reinterpret_cast<const float4 *>(part(cc) + static_cast<size_t>(trow) * HD + cb);
+      const float4 *b = reinterpret_cast<const float4 *>(part(two ? cc + 1 : cc) + static_cast<size_t>(trow) * HD + cb);
+      float4 va[16], vb[16];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const bool in = cc0 + u <= cl;
-        const float *pp = part_of(p, sc, in ? cc0 + u : cf, cf, start);
-        wv[u] = in ? fast_exp2(__ldcg(pp + HD * MROWS + trow) - M) : 0.f;
-#pragma unroll
-        for (int t = 0; t < 16; ++t) vv[u][t] = in ? __ldcg(pp + (c + t) * MROWS + trow) : 0.f;
+      for (int t = 0; t < 16; ++t) {
+        va[t] = __ldcg(a + t);
+        vb[t] = two ? __ldcg(b + t) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      const int ua = cc - cf, ub = ua + 1;
+      float wa = 0.f, wb = 0.f;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < MERGE_MAX; ++u) {   // register-array lookup without indexing
+        wa = u == ua ? mw[u] : wa;
+        wb = u == ub ? mw[u] : wb;
+      }
+      if (ua >= MERGE_MAX) wa = fast_exp2(__ldcg(part(cc) + HD * MROWS + trow) - M);
+      if (two && ub >= MERGE_MAX) wb = fast_exp2(__ldcg(part(cc + 1) + HD * MROWS + trow) - M);
 #pragma unroll
-        for (int t = 0; t < 16; ++t) acc[t] = fmaf(wv[u], vv[u][t], acc[t]);
+      for (int t = 0; t < 16; ++t) {
+        acc[4 * t + 0] = fmaf(wb, vb[t].x, fmaf(wa, va[t].x, acc[4 * t + 0]));
+        acc[4 * t + 1] = fmaf(wb, vb[t].y, fmaf(wa, va[t].y, acc[4 * t + 1]));
+        acc[4 * t + 2] = fmaf(wb, vb[t].z, fmaf(wa, va[t].z, acc[4 * t + 2]));
+        acc[4 * t + 3] = fmaf(wb, vb[t].w, fmaf(wa, va[t].w, acc[4 * t + 3]));
+      }
     }
-    store16_hl(out + c, out_lo ? out_lo + c : nullptr, acc, inv);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      float v[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) v[t] = acc[16 * q4 + t];
+      store16_hl(out + cb + 16 * q4, out_lo ? out_lo + cb + 16 * q4 : nullptr, v, inv);
+    }
   }
 }
 
@@ -275,9 +296,28 @@ __global__ void __launch_bounds__(NTHR, 1)
 
   pdl_start();
   // ---------------------------------------------------------------- schedule
-  // Lane i sums the chunk counts of a contiguous slice of the requests; a
-  // warp scan gives the list length and the slice holding this CTA's start.
-  if (warp == 0) {
+  if (p.cs > 1) {
+    // cluster mode: cluster = one (request, kv head); its cs CTAs split the
+    // chunk list evenly and merge on chip at the end
+    if (threadIdx.x == 0) {
+      const int list = blockIdx.x / p.cs, r = blockIdx.x % p.cs;
+      const int b = list / p.nkv;
+      const int raw = p.ctx_len[b], cap = p.max_pages * CH;
+      if (r == 0 && (raw < 0 || raw > cap)) report(p.status, DFLASH_ERR_DEVICE);
+      const int nch = chunks_of(ctx_of(p, b));
+      const int k0 = r * nch / p.cs, k1 = (r + 1) * nch / p.cs;
+      sch->b = b;
+      sch->h = list % p.nkv;
+      sch->k = k0;
+      sch->n_mine = k1 - k0;
+      sch->lo = 0;
+      sch->total = 0;
+      sch->G = 0;
+      sch->merge_flag = 0;
+    }
+  } else if (warp == 0) {
+    // Lane i sums the chunk counts of a contiguous slice of the requests; a
+    // warp scan gives the list length and the slice holding this CTA's start.
     const int per = (p.B + 31) / 32;
     const int b0 = min(p.B, lane * per), b1 = min(p.B, b0 + per);
     const int cap = p.max_pages * CH;
@@ -623,7 +663,34 @@ __global__ void __launch_bounds__(NTHR, 1)
           break;
         }
         tc_fence_after();
-        const bool whole = seg_whole && w.k == w.nch - 1;
+        const bool whole = p.cs <= 1 && seg_whole && w.k == w.nch - 1;
+        if (p.cs > 1) {
+          // cluster mode: (max, sum, O) of this CTA's share into its own smem
+          // (the K ring is idle: every QK has completed) for the on-chip merge
+          float *xo = reinterpret_cast<float *>(sK);
+#pragma unroll
+          for (int c0 = 0; c0 < HD / 16; c0 += 4) {
+            uint32_t ov[4][16];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) tmem_ld16_nw(lane_base + O_COL + (c0 + u) * 16, ov[u]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              tmem_regs_ready(ov[u]);
+              if (olane) {
+                float4 *d4 = reinterpret_cast<float4 *>(xo + trow * HD + (c0 + u) * 16);
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                  d4[t] = make_float4(__uint_as_float(ov[u][4 * t]), __uint_as_float(ov[u][4 * t + 1]),
+                                      __uint_as_float(ov[u][4 * t + 2]), __uint_as_float(ov[u][4 * t + 3]));
+              }
+            }
+          }
+          if (olane) reinterpret_cast<float2 *>(xo + MROWS * HD)[trow] = make_float2(m, l);
+          tc_fence_before();
+          w.next(p);
+          continue;
+        }
         const int hq = w.h * g + trow / BLK, j = trow % BLK;
         const size_t orow = static_cast<size_t>(w.b * BLK + j) * p.ldo + static_cast<size_t>(hq) * HD;
         float *part = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + (seg == 0 ? 0 : 1)) * ATTN_PART_FLOATS;
@@ -645,8 +712,9 @@ __global__ void __launch_bounds__(NTHR, 1)
               if (whole) {
                 store16_hl(p.out + orow + c * 16, p.out_lo ? p.out_lo + orow + c * 16 : nullptr, v, inv);
               } else {
+                float4 *d4 = reinterpret_cast<float4 *>(part + static_cast<size_t>(trow) * HD + c * 16);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) part[(c * 16 + t) * MROWS + trow] = v[t];   // O^T: coalesced over rows
+                for (int t = 0; t < 4; ++t) d4[t] = make_float4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
               }
             }
           }
@@ -685,8 +753,8 @@ __global__ void __launch_bounds__(NTHR, 1)
           }
           ++nparts;
           if (sch->merge_flag && real)   // DUP: the two lanes of a row take 64 columns each
-            merge_row(p, sc, cf, cl, start, trow, DUP ? hi * 64 : 0, DUP ? 64 : HD, p.out + orow,
-                      p.out_lo ? p.out_lo + orow : nullptr);
+            merge_row(p, cf, cl, run_lo(cf, sc.total, sc.G) == start, trow, DUP ? hi * 64 : 0, DUP ? 1 : 2,
+                      p.out + orow, p.out_lo ? p.out_lo + orow : nullptr);
         }
       }
       w.next(p);
@@ -696,12 +764,63 @@ __global__ void __launch_bounds__(NTHR, 1)
       *abort_flag = 1;
     }
   }
+  if (p.cs > 1 && n == 0 && warp >= 2 && warp <= 5) {   // an empty share: weight 0 in the merge
+    const int t = threadIdx.x - 64;
+    if (t < MROWS) reinterpret_cast<float2 *>(reinterpret_cast<float *>(sK) + MROWS * HD)[t] = make_float2(-INFINITY, 0.f);
+  }
 
   // all roles done: TMEM and the KV ring are free
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+
+  if (p.cs > 1) {
+    // ---- cluster merge through distributed shared memory: CTA r finalises
+    // tile rows [r*R/cs, (r+1)*R/cs) from the cs shares (16g real rows)
+    cluster_sync();
+    const float *xo = reinterpret_cast<const float *>(sK);
+    const float2 *xml = reinterpret_cast<const float2 *>(xo + MROWS * HD);
+    const int rows = BLK * g, rank = static_cast<int>(cluster_ctarank());
+    const int r0 = rank * rows / p.cs, r1 = (rank + 1) * rows / p.cs;
+    const int b = sch->b, h = sch->h;
+    for (int it = threadIdx.x; it < (r1 - r0) * (HD / 4); it += NTHR) {
+      const int row = r0 + it / (HD / 4), c4 = it % (HD / 4);
+      float2 ml[8];
+      float M = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        ml[k] = k < p.cs ? ld_dsmem_f2(dsmem_addr(xml + row, k)) : make_float2(-INFINITY, 0.f);
+        M = fmaxf(M, ml[k].x);
+      }
+      float L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (k < p.cs && ml[k].y > 0.f) {
+          const float wk = fast_exp2(ml[k].x - M);
+          L += wk * ml[k].y;
+          const float4 v = ld_dsmem_f4(dsmem_addr(xo + row * HD + 4 * c4, k));
+          acc.x += wk * v.x;
+          acc.y += wk * v.y;
+          acc.z += wk * v.z;
+          acc.w += wk * v.w;
+        }
+      }
+      const float inv = 1.f / L;
+      const int hq = h * g + row / BLK, j = row % BLK;
+      const size_t dst = static_cast<size_t>(b * BLK + j) * p.ldo + static_cast<size_t>(hq) * HD + 4 * c4;
+      const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      const __nv_bfloat162 h1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2 *>(p.out + dst) =
+          make_uint2(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1));
+      if (p.out_lo)
+        *reinterpret_cast<uint2 *>(p.out_lo + dst) =
+            make_uint2(pack_bf16(acc.x * inv - __low2float(h0), acc.y * inv - __high2float(h0)),
+                       pack_bf16(acc.z * inv - __low2float(h1), acc.w * inv - __high2float(h1)));
+    }
+    cluster_sync();   // no CTA leaves while others still read its shares
+  }
 }
 
 // ------------------------------------------------------------------ fp32
@@ -813,14 +932,36 @@ int attention_bf16(const Launch &lc, const AttnArgs &a) {
   p.nkv = a.nkv;
   p.g = g;
   p.min_chunks = a.min_chunks > 0 ? a.min_chunks : DEFAULT_MIN_CHUNKS;
+  // few (request, kv head) lists: one cluster of cs CTAs per list, merged on
+  // chip (global round trips cost ~2 us here); otherwise the balanced
+  // persistent split.  A forced split length (test hook) means persistent.
+  const long long lists = static_cast<long long>(a.B) * a.nkv;
+  int cs = 1;
+  if (a.min_chunks <= 0)
+    while (cs < 8 && lists * cs * 2 <= grid) cs *= 2;
+  p.cs = cs;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(HD)));
   p.counters = a.counters;
   p.partials = a.partials;
   p.status = lc.status;
   p.timeout_ns = lc.timeout_ns;
   ProfScope ps(lc, "attention", -1.0, -1.0);
-  return cuda_check(launch_pdl(g <= 4 ? attn_tc_kernel<true> : attn_tc_kernel<false>, dim3(grid), dim3(NTHR), SMEM,
-                               lc.stream, tQ, tK, tV, tBK, tBV, p),
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs > 1 ? static_cast<unsigned>(lists * cs) : static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(NTHR);
+  cfg.dynamicSmemBytes = SMEM;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cuda_check(cudaLaunchKernelEx(&cfg, g <= 4 ? attn_tc_kernel<true> : attn_tc_kernel<false>, tQ, tK, tV, tBK,
+                                       tBV, p),
                     "attention launch");
 }
 

@@ -119,7 +119,7 @@ struct AttnArgs {
   float *partials;          // bf16: [partial_slots][ATTN_PART_FLOATS] merge scratch
   size_t partial_slots;     // >= 2 * SM count
 };
-// one split partial of the bf16 attention: O^T [128 d][128 rows], max [128], sum [128]
+// one split partial of the bf16 attention: O [128 rows][128 d] (row-major), max [128], sum [128]
 constexpr int ATTN_PART_FLOATS = 128 * 128 + 2 * 128;
 int attention_bf16(const Launch &lc, const AttnArgs &a);
 int attention_f32(const Launch &lc, const AttnArgs &a);
