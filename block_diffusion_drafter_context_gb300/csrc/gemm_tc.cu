@@ -56,6 +56,7 @@ struct Cfg {
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : (STAGES_RAW < 2 ? 2 : STAGES_RAW);
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+  static_assert(STAGES * STAGE_BYTES >= BM * BN * 4, "the ring must hold one fp32 tile (cluster split-K share)");
 };
 
 struct Params {
@@ -65,6 +66,7 @@ struct Params {
   int tok_tiles, kbpt;
   long long total;     // tiles * kbpt
   int G;               // CTAs
+  int csk;             // >1: cluster split-K, csk CTAs (one cluster) per tile
   int epi;
   void *out;
   int ldo;
@@ -208,8 +210,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // The activations, outputs and stream-K scratch are produced / consumed by
   // the neighbouring kernels of the step: only the weight stream may start
   // before the previous grid has completed (programmatic dependent launch).
-  const long long begin = range_begin(p.total, p.G, blockIdx.x);
-  const long long end = range_begin(p.total, p.G, blockIdx.x + 1);
+  // stream-K: one contiguous range of the (tile, k-block) space per CTA;
+  // cluster split-K: the csk CTAs of a cluster split one tile's k-blocks
+  long long begin, end;
+  if (p.csk > 1) {
+    const long long tile = blockIdx.x / p.csk, r = blockIdx.x % p.csk;
+    begin = tile * p.kbpt + r * p.kbpt / p.csk;
+    end = tile * p.kbpt + (r + 1) * p.kbpt / p.csk;
+  } else {
+    begin = range_begin(p.total, p.G, blockIdx.x);
+    end = range_begin(p.total, p.G, blockIdx.x + 1);
+  }
   const int first_tile = static_cast<int>(begin / p.kbpt);
 
   if (warp == 0) {
@@ -381,6 +392,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
+      } else if (p.csk > 1) {
+        // cluster split-K: this CTA's fp32 share into its own smem, row-major
+        // (the ring is idle: every stage has been consumed); the cluster
+        // reduces it on chip after the main loop
+        float *sp = reinterpret_cast<float *>(sA) + static_cast<size_t>(r) * BN;
+        for (int c = 0; c < BN / 16; ++c) {
+          tmem_ld16(taddr + c * 16, v);
+          float4 *s4 = reinterpret_cast<float4 *>(sp + c * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) s4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
       } else {
         // partial tile: this CTA's fp32 share goes to its slot, row-major
         // (each thread writes its row's BN columns as float4); the CTA that
@@ -460,6 +485,49 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+
+  if (p.csk > 1) {
+    // ---- cluster split-K reduction through distributed shared memory: CTA
+    // r finalises tile rows [r*BM/csk, (r+1)*BM/csk) summing the csk shares in
+    // rank order (deterministic); lanes hold consecutive rows (coalesced
+    // stores, SwiGLU row pairs in neighbouring lanes)
+    cluster_sync();
+    if (warp >= 2) {
+      const int et = threadIdx.x - 64;
+      const int rank = static_cast<int>(cluster_ctarank());
+      const int r0 = rank * BM / p.csk, rows = (rank + 1) * BM / p.csk - r0;
+      const int tasks = rows * (BN / 16);
+      const int tile = first_tile;
+      const int rt = tile / p.tok_tiles;
+      const size_t goff = static_cast<size_t>(rt / p.rtpg) * p.out_gstride;
+      const int tokt = (tile % p.tok_tiles) * BN;
+      const float *sp = reinterpret_cast<const float *>(sA);
+      for (int t0 = 0; t0 < tasks; t0 += 128) {   // every thread takes each round (shuffles in SwiGLU)
+        const int task = t0 + et;
+        const bool valid = task < tasks;
+        const int row = r0 + (valid ? task % rows : 0), grp = valid ? task / rows : 0;
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        if (valid) {
+          for (int k = 0; k < p.csk; ++k) {
+            const uint32_t a = dsmem_addr(sp + static_cast<size_t>(row) * BN + grp * 16, static_cast<uint32_t>(k));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float4 x = ld_dsmem_f4(a + 16 * i);
+              v[4 * i] += x.x;
+              v[4 * i + 1] += x.y;
+              v[4 * i + 2] += x.z;
+              v[4 * i + 3] += x.w;
+            }
+          }
+        }
+        const int n = valid ? (rt % p.rtpg) * BM + row : p.N;   // n >= N: nothing stored
+        finalize(p, v, n, tokt + grp * 16, goff);
+      }
+    }
+    cluster_sync();   // nobody leaves while others still read its share
+  }
 }
 
 template <int BN, bool SPLIT>
@@ -477,11 +545,15 @@ int launch(const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const CUten
   cfg.blockDim = dim3(NTHREADS);
   cfg.dynamicSmemBytes = Cfg<BN, SPLIT>::SMEM;
   cfg.stream = lc.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(p.csk > 1 ? p.csk : 1);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, SPLIT>, tW, tX, tXl, p), "gemm launch");
 }
 
@@ -535,6 +607,22 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   const int max_parts = std::max(2, (256 * 1024) / (BM * BN * 4));
   const int min_kb = std::max(4, (p.kbpt + max_parts - 1) / max_parts);
   p.G = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, (p.total + min_kb - 1) / min_kb)));
+  // Few tiles (at most half the SMs): cluster split-K instead, csk CTAs per
+  // tile reducing through distributed shared memory - no global round trips
+  // (fence, counter atomic, partial loads: ~2 us each here) on the GEMM's
+  // tail.  The test hook (gemm_ctas) keeps stream-K.
+  p.csk = 1;
+  if (lc.gemm_ctas == 0 && tiles * 2 <= cap) {
+    long long s = std::min<long long>(std::min<long long>(8, cap / tiles), p.kbpt);
+    // SwiGLU pairs rows 2i / 2i+1 in neighbouring lanes: row ranges must be
+    // even-aligned, so a power-of-two cluster there
+    if (epi == EPI_SWIGLU)
+      while (s & (s - 1)) --s;
+    if (s >= 2) {
+      p.csk = static_cast<int>(s);
+      p.G = static_cast<int>(tiles * s);
+    }
+  }
   p.epi = epi;
   p.out = op.out;
   p.ldo = op.ldo;

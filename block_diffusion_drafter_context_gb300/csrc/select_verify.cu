@@ -23,7 +23,12 @@ namespace {
 constexpr int K = 16;
 constexpr int J = 15;
 
-// grid (15 positions, B); 256 threads.  Dynamic smem: e[32][E] + u[16][r] + w[16][r] + red.
+// grid (15 positions, B); 256 threads.  The 32 tokens' embeddings and the
+// two rank-r projections are staged in chunks of ECH embedding columns
+// (A^T, B^T with a padded pitch: conflict-free), each warp owns 4 of the 32
+// rows and each lane one rank index, so u(p) = A e[p] and w(c) = B e[c] are
+// shared-memory dot products with no dependent global loads.
+constexpr int ECH = 128;
 template <typename T>
 __global__ void __launch_bounds__(256) pair_scores_kernel(const int32_t *anchor, const int32_t *topk_ids,
                                                           const float *topk_logits, const T *hfinal, int H,
@@ -31,10 +36,12 @@ __global__ void __launch_bounds__(256) pair_scores_kernel(const int32_t *anchor,
                                                           const float *w_g, float b_g, float *scores) {
   pdl_start();
   extern __shared__ float sh[];
-  float *se = sh;                  // [32][E]: rows 0..15 previous, 16..31 current
-  float *su = se + 32 * E;         // [16][r]
-  float *sw = su + 16 * r;         // [16][r]
-  float *red = sw + 16 * r;        // [8]
+  const int rp = r + 1;
+  float *se = sh;                     // [32][ECH]: rows 0..15 previous, 16..31 current
+  float *smt = se + 32 * ECH;         // [2][ECH][rp]: A^T, B^T chunk
+  float *su = smt + 2 * ECH * rp;     // [16][r]
+  float *sw = su + 16 * r;            // [16][r]
+  float *red = sw + 16 * r;           // [8]
   __shared__ int tok[32];
   const int j = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -56,16 +63,45 @@ __global__ void __launch_bounds__(256) pair_scores_kernel(const int32_t *anchor,
   float gsum = 0.f;
   for (int i = 0; i < 8; ++i) gsum += red[i];
   const float gate = 1.f / (1.f + expf(-(gsum + b_g)));
-  for (int i = tid; i < 32 * E; i += blockDim.x) se[i] = Elt<T>::ld(e256 + static_cast<size_t>(tok[i / E]) * E + i % E);
-  __syncthreads();
-  // u(p) = A e[p] for rows 0..15, w(c) = B e[c] for rows 16..31
-  for (int o = tid; o < 32 * r; o += blockDim.x) {
-    const int row = o / r, k = o % r;
-    const T *m = (row < 16 ? A : Bm) + static_cast<size_t>(k) * E;
-    const float *ev = se + row * E;
-    float acc = 0.f;
-    for (int i = 0; i < E; ++i) acc = fmaf(Elt<T>::ld(m + i), ev[i], acc);
-    (row < 16 ? su : sw)[(row & 15) * r + k] = acc;
+  float acc[4][2];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = 0.f;
+  for (int e0 = 0; e0 < E; e0 += ECH) {
+    const int ne = min(ECH, E - e0);
+    __syncthreads();   // the previous chunk is consumed
+    for (int i = tid; i < 32 * ne; i += blockDim.x) {
+      const int row = i / ne, c = i % ne;
+      se[row * ECH + c] = Elt<T>::ld(e256 + static_cast<size_t>(tok[row]) * E + e0 + c);
+    }
+    for (int i = tid; i < 2 * r * ne; i += blockDim.x) {
+      const int m = i / (r * ne), rem = i % (r * ne), k = rem / ne, c = rem % ne;
+      smt[(m * ECH + c) * rp + k] = Elt<T>::ld((m ? Bm : A) + static_cast<size_t>(k) * E + e0 + c);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {   // rows warp, warp+8, ...: A for the previous tokens, B for the current
+      const int row = warp + 8 * q;
+      const float *ev = se + row * ECH;
+      const float *mt = smt + (row < 16 ? 0 : ECH * rp);
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const int k = lane + 32 * kk;
+        if (k < r) {
+          float a = acc[q][kk];
+          for (int c = 0; c < ne; ++c) a = fmaf(mt[c * rp + k], ev[c], a);
+          acc[q][kk] = a;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int row = warp + 8 * q;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const int k = lane + 32 * kk;
+      if (k < r) (row < 16 ? su : sw)[(row & 15) * r + k] = acc[q][kk];
+    }
   }
   __syncthreads();
   {
@@ -138,7 +174,7 @@ int pair_scores(const Launch &lc, bool f32, const int32_t *anchor, const int32_t
   if (B <= 0) return DFLASH_OK;
   if (r < 1 || r > 64 || E < 1 || E > 1024)
     return set_error(DFLASH_ERR_UNSUPPORTED, "selector rank must be 1..64 and embedding width 1..1024");
-  const size_t smem = (32 * static_cast<size_t>(E) + 32 * r + 8) * sizeof(float);
+  const size_t smem = (32 * static_cast<size_t>(ECH) + 2 * static_cast<size_t>(ECH) * (r + 1) + 32 * r + 8) * sizeof(float);
   dim3 grid(J, B);
   ProfScope ps(lc, "pair_scores", -1.0, -1.0);
   if (f32) {
