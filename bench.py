@@ -380,7 +380,8 @@ def run_ours(args, wl):
                               "gbs": (s["bytes"] / (s["ms"] * 1e-3) / 1e9) if s["bytes"] > 0 else None}
                   for s in stats}
     att = [s for s in stats if s["name"] == "attention"]
-    kv_bytes_step = float(sum(int(c) + 16 for c in ctx)) * cfg.n_layers * cfg.n_kv_heads * cfg.head_dim * 2 * 2
+    # K and V read per step: each request's context plus the 16 tokens this step injected, plus the 16 block keys
+    kv_bytes_step = float(sum(int(c) + 32 for c in ctx)) * cfg.n_layers * cfg.n_kv_heads * cfg.head_dim * 2 * 2
     att_ms = sum(s["ms"] for s in att) / args.steps
     att_gbs = kv_bytes_step / (att_ms * 1e-3) / 1e9 if att_ms > 0 else None
     total_ms_inst = sum(s["ms"] for s in stats) / args.steps
