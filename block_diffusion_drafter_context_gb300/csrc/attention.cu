@@ -371,6 +371,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     if (lane == 0 && n > 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      const uint64_t pol_kv = policy_evict_first();
       Walk w;
       w.init(p, sc);
       int last_ci[ST];
@@ -402,12 +403,12 @@ __global__ void __launch_bounds__(NTHR, 1)
             rowv = (page * p.nkv + w.h) * HD;
           }
         }
-        if (load) {
+        if (load) {   // K/V pages are read once per step: evict first
           uint8_t *dk = sK + st * K_BYTES, *dv = sV + st * V_BYTES;
           mbar_arrive_expect_tx(&full[st], K_BYTES + V_BYTES);
-          tma_load_2d(dk, mk, &full[st], 0, rowk);
-          tma_load_2d(dk + K_BYTES / 2, mk, &full[st], 64, rowk);
-          tma_load_2d(dv, mv, &full[st], 0, rowv);
+          tma_load_2d_hint(dk, mk, &full[st], 0, rowk, pol_kv);
+          tma_load_2d_hint(dk + K_BYTES / 2, mk, &full[st], 64, rowk, pol_kv);
+          tma_load_2d_hint(dv, mv, &full[st], 0, rowv, pol_kv);
           last_ci[st] = i;
         }
         if (first) {   // the query rows of this (request, kv head), once its predecessor's QKs are done

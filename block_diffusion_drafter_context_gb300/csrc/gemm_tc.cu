@@ -55,7 +55,12 @@ struct Cfg {
   static constexpr int STAGES_RAW = BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : (STAGES_RAW < 2 ? 2 : STAGES_RAW);
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+  // cluster split-K with small token tiles pushes each row's fp32 share into
+  // the owning CTA: at most (csk - 1) * ceil(128 / csk) <= 120 rows arrive
+  static constexpr bool PUSH = BN <= 32;
+  static constexpr int PUSH_BYTES = PUSH ? 120 * BN * 4 : 0;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256 + PUSH_BYTES;
+  static_assert((2 * STAGES + 6) * 8 + 12 <= 256, "GEMM control block overflows");
   static_assert(STAGES * STAGE_BYTES >= BM * BN * 4, "the ring must hold one fp32 tile (cluster split-K share)");
 };
 
@@ -173,7 +178,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t *tfull = empty + C::STAGES;
   uint64_t *tempty = tfull + 2;
   uint64_t *drain = tempty + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *rbar = drain + 1;   // cluster split-K (push): shares of the other CTAs have arrived
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(rbar + 1);
+  float *spush = reinterpret_cast<float *>(base + C::STAGES * C::STAGE_BYTES + 256);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *bcast = reinterpret_cast<int *>(tmem_slot + 2);
 
@@ -189,6 +196,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&tempty[0], 4);
     mbar_init(&tempty[1], 4);
     mbar_init(drain, 1);
+    mbar_init(rbar, p.csk > 1 ? p.csk - 1 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -206,6 +214,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (C::PUSH && p.csk > 1) cluster_sync();   // every CTA's barriers exist before any remote arrive
 
   // The activations, outputs and stream-K scratch are produced / consumed by
   // the neighbouring kernels of the step: only the weight stream may start
@@ -392,6 +401,66 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
+      } else if (C::PUSH && p.csk > 1) {
+        // cluster split-K, small token tile: each row's fp32 share goes straight
+        // into the shared memory of the CTA that finalises that row (rows
+        // [k*BM/csk, (k+1)*BM/csk) belong to rank k); one release arrive per
+        // peer, then the owner sums the csk shares in rank order
+        const int S = p.csk, rank = static_cast<int>(cluster_ctarank());
+        const int o = ((r + 1) * S - 1) / BM;
+        const int o_r0 = o * BM / S, o_rows = (o + 1) * BM / S - o_r0;
+        float own[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 16; ++c) {
+          tmem_ld16(taddr + c * 16, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) own[c * 16 + i] = v[i];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+        if (o != rank) {
+          const int slot = rank < o ? rank : rank - 1;
+          const uint32_t a = dsmem_addr(spush + (static_cast<size_t>(slot) * o_rows + (r - o_r0)) * BN,
+                                        static_cast<uint32_t>(o));
+#pragma unroll
+          for (int j = 0; j < BN / 4; ++j)
+            st_dsmem_f4(a + 16 * j, make_float4(own[4 * j], own[4 * j + 1], own[4 * j + 2], own[4 * j + 3]));
+        }
+        fence_acq_rel_cluster();
+        epi_bar();   // every push of this CTA is issued and fenced
+        if (et < S && et != rank) mbar_arrive_remote(dsmem_addr(rbar, static_cast<uint32_t>(et)));
+        const bool got_all = mbar_wait_cluster(rbar, 0, abort_flag, p.timeout_ns);
+        if (!got_all) {
+          if (et == 0) report(p.status, DFLASH_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        const bool mine = o == rank;
+        const int my_rows = (rank + 1) * BM / S - rank * BM / S, my_r0 = rank * BM / S;
+#pragma unroll
+        for (int c = 0; c < BN / 16; ++c) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          for (int k = 0; k < S; ++k) {   // rank order: deterministic
+            if (k == rank) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] += own[c * 16 + i];
+            } else if (mine) {
+              const int slot = k < rank ? k : k - 1;
+              const float4 *src = reinterpret_cast<const float4 *>(
+                  spush + (static_cast<size_t>(slot) * my_rows + (r - my_r0)) * BN + c * 16);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float4 x = src[i];
+                v[4 * i] += x.x;
+                v[4 * i + 1] += x.y;
+                v[4 * i + 2] += x.z;
+                v[4 * i + 3] += x.w;
+              }
+            }
+          }
+          finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff);   // n >= N: not this CTA's row
+        }
       } else if (p.csk > 1) {
         // cluster split-K: this CTA's fp32 share into its own smem, row-major
         // (the ring is idle: every stage has been consumed); the cluster
@@ -486,7 +555,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 
-  if (p.csk > 1) {
+  if (!C::PUSH && p.csk > 1) {
     // ---- cluster split-K reduction through distributed shared memory: CTA
     // r finalises tile rows [r*BM/csk, (r+1)*BM/csk) summing the csk shares in
     // rank order (deterministic); lanes hold consecutive rows (coalesced

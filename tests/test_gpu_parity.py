@@ -173,6 +173,22 @@ def test_stateless_isolated_and_cache_untouched():
         assert torch.equal(p[key][1:], a[key][1:]), key
 
 
+def test_single_request_views_match_oracle():
+    """Each request drafted alone (batch 1 through a view of its page-table
+    row: 16-token GEMM tiles, cluster split-K with pushed shares, cluster-mode
+    attention) matches the oracle like the batched call does."""
+    import types
+    c = case("T1")
+    tol = TOL[c.cfg.dtype]
+    for b in range(c.B):
+        view = types.SimpleNamespace(struct=c.kv.row(b))
+        out = c.dr.draft_block(view, c.ctx_d[b:b + 1], c.anchor_d[b:b + 1], want_logits=True)
+        assert c.dr.status() == 0
+        ref = c.oracle_draft(b)
+        assert rel_err(to_np(out["final_hidden"])[0], ref["h"]) <= tol, b
+        assert rel_err(to_np(out["logits"])[0], ref["z"]) <= tol, b
+
+
 def test_split_kv_and_gemm_partition_do_not_change_results():
     import torch
     from block_diffusion_drafter_context_gb300 import binding as Bd
