@@ -331,6 +331,88 @@ def verify_greedy(draft, target):
 
 
 # --------------------------------------------------------------------------
+# [DF2] "Arquitectura del Sistema" item 1: the other selection and
+# verification modes - sampling over the precomputed pair scores, and
+# rejection sampling that restores the target's exact distribution
+# --------------------------------------------------------------------------
+def inverse_cdf(weights, u: float) -> int:
+    """Index of the first element whose running sum (in index order) exceeds
+    u * total; the last positive weight when rounding leaves none."""
+    w = np.asarray(weights, dtype=np.float64)
+    total = w.sum()
+    c = np.cumsum(w)
+    hit = np.nonzero(c > u * total)[0]
+    if hit.size:
+        return int(hit[0])
+    pos = np.nonzero(w > 0)[0]
+    return int(pos[-1]) if pos.size else len(w) - 1
+
+
+def sample_path(scores, cand_ids, temperature: float, uniforms):
+    """Sampling over precomputed pair scores: at position j the draft
+    distribution over the 16 candidates is q_j = softmax(s_j(c_{j-1}, .) / T)
+    (c_0 = the anchor row), and c_j is drawn from it by inverse CDF in
+    candidate order with the uniform u_j.  scores [15, 16, 16] (rows indexed
+    by the previous candidate) -> (draft ids [15], q [15, 16], index [15])."""
+    s = np.asarray(scores, dtype=np.float64)
+    cand_ids = np.asarray(cand_ids)
+    J, K, _ = s.shape
+    draft = np.empty(J, dtype=np.int32)
+    q = np.empty((J, K))
+    idx = np.empty(J, dtype=np.int32)
+    p = 0
+    for j in range(J):
+        row = s[j, p] / float(temperature)
+        e = np.exp(row - row.max())
+        q[j] = e / e.sum()
+        c = inverse_cdf(q[j], float(uniforms[j]))
+        draft[j], idx[j], p = cand_ids[j, c], c, c
+    return draft, q, idx
+
+
+def logit_scores(cand_logits) -> np.ndarray:
+    """DFlash-1 (no selector): every previous candidate sees the drafter's
+    own top-16 logits.  [15, 16] -> [15, 16, 16]."""
+    z = np.asarray(cand_logits, dtype=np.float64)
+    return np.repeat(z[:, None, :], z.shape[1], axis=1)
+
+
+def verify_rejection(draft, q, cand_ids, target_logits, u_accept, u_bonus: float):
+    """Rejection-sampling verification: draft token d_i (drawn from q_i) is
+    accepted while u_i * q_i(d_i) < p_i(d_i), p_i = softmax of the target's
+    logits at position i; at the first rejection the bonus is drawn from the
+    residual max(0, p_i - q_i) (q_i zero outside the candidates), and after
+    15 acceptances from p_15; both by inverse CDF in vocabulary order with
+    u_bonus.  The committed tokens then follow p exactly.
+    target_logits [16, V] -> (k, bonus, committed [16], -1 padded)."""
+    zt = np.asarray(target_logits, dtype=np.float64)
+    draft = np.asarray(draft)
+    cand_ids = np.asarray(cand_ids)
+    q = np.asarray(q, dtype=np.float64)
+    J = draft.shape[0]
+    pt = np.exp(zt - zt.max(axis=1, keepdims=True))
+    pt /= pt.sum(axis=1, keepdims=True)
+    k = 0
+    while k < J:
+        c = int(np.nonzero(cand_ids[k] == draft[k])[0][0])
+        if u_accept[k] * q[k, c] < pt[k, draft[k]]:
+            k += 1
+        else:
+            break
+    if k < J:
+        r = pt[k].copy()
+        r[cand_ids[k]] -= q[k]
+        r = np.maximum(r, 0.0)
+        bonus = inverse_cdf(r if r.sum() > 0 else pt[k], u_bonus)
+    else:
+        bonus = inverse_cdf(pt[J], u_bonus)
+    committed = np.full(J + 1, -1, dtype=np.int32)
+    committed[:k] = draft[:k]
+    committed[k] = bonus
+    return k, int(bonus), committed
+
+
+# --------------------------------------------------------------------------
 # one request end to end
 # --------------------------------------------------------------------------
 def draft_request(cfg, W, kv_ctx, n_ctx: int, anchor: int):

@@ -505,3 +505,112 @@ def test_brute_force_micro_drafter_single_layer():
     np.testing.assert_allclose(h, hb, rtol=1e-11, atol=1e-12)
     zb = [mat(W["lm_head"], hb[j]) for j in range(1, S)]
     np.testing.assert_allclose(z, zb, rtol=1e-10, atol=1e-11)
+
+
+# ------------------------------------------------------------------ sampling modes
+def test_inverse_cdf_hand_worked():
+    # running sums of [1, 2, 1] / 4 = 0.25, 0.75, 1.0: first one above u
+    w = [1.0, 2.0, 1.0]
+    assert O.inverse_cdf(w, 0.0) == 0
+    assert O.inverse_cdf(w, 0.2499) == 0
+    assert O.inverse_cdf(w, 0.25) == 1      # 0.25 is not above 0.25
+    assert O.inverse_cdf(w, 0.7499) == 1
+    assert O.inverse_cdf(w, 0.75) == 2
+    assert O.inverse_cdf(w, 0.9999) == 2
+    assert O.inverse_cdf([0.0, 3.0, 0.0], 0.5) == 1
+
+
+def test_sample_path_low_temperature_is_greedy():
+    rng = np.random.default_rng(21)
+    for _ in range(20):
+        s = rng.normal(size=(15, 16, 16))
+        ids = np.stack([rng.permutation(1000)[:16] for _ in range(15)])
+        d, q, idx = O.sample_path(s, ids, 1e-6, rng.random(15))
+        assert (d == O.greedy_path(s, ids)).all()
+        assert np.allclose(q.max(axis=1), 1.0)
+
+
+def test_sample_path_frequencies_are_the_softmax():
+    # one position: the share of a uniform grid that selects candidate c is q(c)
+    rng = np.random.default_rng(22)
+    s = rng.normal(size=(1, 16, 16)) * 2.0
+    ids = np.arange(16)[None, :]
+    T = 0.7
+    grid = (np.arange(4000) + 0.5) / 4000
+    counts = np.zeros(16)
+    for u in grid:
+        _, q, idx = O.sample_path(s, ids, T, [u])
+        counts[idx[0]] += 1
+    e = np.exp(s[0, 0] / T - (s[0, 0] / T).max())
+    assert np.abs(counts / len(grid) - e / e.sum()).max() < 1e-3
+    assert np.allclose(q[0], e / e.sum())
+
+
+def test_sample_path_follows_the_previous_choice():
+    # rows of the score table are indexed by the previous candidate
+    s = np.zeros((2, 16, 16))
+    s[0, 0, 5] = 50.0            # position 1 (from the anchor row) picks candidate 5
+    s[1, 5, 9] = 50.0            # position 2 then reads row 5
+    s[1, 0, 3] = 50.0            # a row it must not read
+    ids = np.tile(np.arange(100, 116), (2, 1))
+    d, _, idx = O.sample_path(s, ids, 1.0, [0.5, 0.5])
+    assert idx.tolist() == [5, 9] and d.tolist() == [105, 109]
+
+
+def test_rejection_sampling_is_lossless():
+    # one position, V = 40: draft token drawn from q over 16 candidates, then
+    # accept / residual.  Sweeping the accept uniform gives the acceptance
+    # probability of each candidate; sweeping the bonus uniform after a
+    # rejection gives the residual draw.  The first committed token must follow
+    # the target distribution p exactly (to the grid's resolution).
+    rng = np.random.default_rng(23)
+    V = 40
+    n = 2000
+    grid = (np.arange(n) + 0.5) / n
+    for trial in range(3):
+        zt = rng.normal(size=(2, V)) * 1.5
+        p = np.exp(zt[0] - zt[0].max())
+        p /= p.sum()
+        cand = rng.permutation(V)[:16]
+        qv = rng.random(16) ** 3
+        qv /= qv.sum()
+        dist = np.zeros(V)
+        for c in range(16):
+            acc = np.mean([O.verify_rejection([cand[c]], qv[None, :], cand[None, :], zt, [ua], 0.0)[0] == 1
+                           for ua in grid])
+            dist[cand[c]] += qv[c] * acc
+            if acc < 1.0:
+                bon = np.zeros(V)
+                for ub in grid:
+                    bon[O.verify_rejection([cand[c]], qv[None, :], cand[None, :], zt, [1.0 - 1e-12], ub)[1]] += 1.0 / n
+                dist += qv[c] * (1.0 - acc) * bon
+        assert np.abs(dist - p).max() < 2e-3, (trial, np.abs(dist - p).max())
+
+
+def test_rejection_special_cases():
+    V = 30
+    cand = np.arange(16)
+    # the target puts all mass on the candidates and equals q there: always accept
+    zt = np.full((16, V), -1e9)
+    q = np.full((15, 16), 1.0 / 16)
+    zt[:, :16] = 0.0
+    draft = np.full(15, 3)
+    for u in (0.0, 0.5, 0.999):
+        k, bonus, com = O.verify_rejection(draft, q, np.tile(cand, (15, 1)), zt, np.full(15, u), 0.25)
+        assert k == 15 and com[:15].tolist() == [3] * 15
+        assert bonus == O.inverse_cdf(np.r_[np.ones(16), np.zeros(V - 16)], 0.25) == 4
+    # the target gives the draft token no mass: reject at once, bonus from p minus q
+    zt2 = np.zeros((16, V))
+    zt2[0, 3] = -1e9
+    k, bonus, com = O.verify_rejection(draft, q, np.tile(cand, (15, 1)), zt2, np.zeros(15), 0.0)
+    assert k == 0 and bonus != 3 and com[1:].tolist() == [-1] * 15
+    # residual max(0, p - q): tokens outside the candidates keep their full mass
+    p0 = np.r_[np.zeros(1), np.ones(V - 1)] / (V - 1)
+    r = np.maximum(p0 - np.r_[q[0], np.zeros(V - 16)], 0)
+    assert bonus == O.inverse_cdf(r, 0.0) == 16
+
+
+def test_logit_scores_ignore_the_previous_choice():
+    z = np.random.default_rng(24).normal(size=(15, 16))
+    s = O.logit_scores(z)
+    assert s.shape == (15, 16, 16) and (s == z[:, None, :]).all()
