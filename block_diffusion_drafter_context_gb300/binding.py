@@ -24,7 +24,7 @@ EXPORTS = (
     "dflash_draft_block", "dflash_select_path", "dflash_verify_greedy", "dflash_read_status",
     "dflash_set_wait_timeout", "dflash_set_gemm_ctas", "dflash_set_attn_split",
     "dflash_profile_begin", "dflash_profile_end", "dflash_debug_wait_flag", "dflash_last_error",
-    "dflash_topk16_noalloc",
+    "dflash_topk16_noalloc", "dflash_sample_path", "dflash_verify_rejection",
 )
 
 
@@ -86,6 +86,8 @@ def load(path: str = LIB_PATH):
         "dflash_draft_block": (i, [vp, POINTER(dflash_kv), vp, vp, i, vp, vp, vp, vp, vp, c_size_t, vp]),
         "dflash_select_path": (i, [vp, vp, vp, vp, vp, i, vp, vp, vp, c_size_t, vp]),
         "dflash_verify_greedy": (i, [vp, vp, i, vp, vp, vp, vp]),
+        "dflash_sample_path": (i, [vp, vp, vp, vp, vp, i, c_float, vp, vp, vp, vp, vp, c_size_t, vp]),
+        "dflash_verify_rejection": (i, [vp, vp, vp, vp, vp, vp, vp, i, vp, vp, vp, vp, c_size_t, vp]),
         "dflash_read_status": (i, [vp, POINTER(c_int), vp]),
         "dflash_set_wait_timeout": (i, [vp, c_ulonglong]),
         "dflash_set_gemm_ctas": (i, [vp, i]),
@@ -165,6 +167,22 @@ def dflash_select_path(ctx, anchor_ids, topk_ids, topk_logits, final_hidden, bat
 def dflash_verify_greedy(draft_ids, target_ids, batch, accept_len, bonus, committed, stream=None):
     return _check(load().dflash_verify_greedy(_p(draft_ids), _p(target_ids), batch, _p(accept_len), _p(bonus),
                                               _p(committed), _stream(stream)))
+
+
+def dflash_sample_path(ctx, anchor_ids, topk_ids, topk_logits, final_hidden, batch, temperature, uniforms,
+                       draft_ids, draft_probs, pair_scores, workspace, workspace_bytes, stream=None):
+    return _check(load().dflash_sample_path(ctx, _p(anchor_ids), _p(topk_ids), _p(topk_logits), _p(final_hidden),
+                                            batch, float(temperature), _p(uniforms), _p(draft_ids),
+                                            _p(draft_probs), _p(pair_scores), _p(workspace), workspace_bytes,
+                                            _stream(stream)))
+
+
+def dflash_verify_rejection(ctx, target_logits, draft_ids, topk_ids, draft_probs, u_accept, u_bonus, batch,
+                            accept_len, bonus, committed, workspace, workspace_bytes, stream=None):
+    return _check(load().dflash_verify_rejection(ctx, _p(target_logits), _p(draft_ids), _p(topk_ids),
+                                                 _p(draft_probs), _p(u_accept), _p(u_bonus), batch,
+                                                 _p(accept_len), _p(bonus), _p(committed), _p(workspace),
+                                                 workspace_bytes, _stream(stream)))
 
 
 def dflash_read_status(workspace, stream=None) -> int:

@@ -135,7 +135,7 @@ constexpr int TOPK_MAX_CHUNKS = 64;
 // read within each call.
 struct Layout {
   size_t status, gemm_ctr, gemm_part, topk_ctr, attn_ctr, attn_part, attn_part_slots, topk_part;
-  size_t x, u, u2, qkv, q, bk, bv, o, ysub, coef, hmid, hmask, hfinal, logits, scores;
+  size_t x, u, u2, qkv, q, bk, bv, o, ysub, coef, hmid, hmask, hfinal, logits, scores, lse;
   size_t u_lo, u2_lo, o_lo, ysub_lo, hmid_lo, hmask_lo, ysub32;
   size_t fc, f, f_lo, kvproj, ctx_saved;
   size_t total;
@@ -188,6 +188,7 @@ Layout layout(const dflash_ctx *c, int B, int Tn) {
   L.hfinal = take(te * R * H);
   L.logits = take(4ull * B * 15 * V);
   L.scores = take(4ull * B * 15 * 256);
+  L.lse = take(4ull * B * 16);
   L.fc = take(4ull * Tn * H);
   L.f = take(te * Tn * H);
   L.f_lo = take(tl * Tn * H);
@@ -554,6 +555,52 @@ int dflash_select_path(dflash_ctx *ctx, const int32_t *anchor_ids, const int32_t
                           ctx->w.sel_b_g, sc))
     return e;
   return greedy_path(lc, sc, topk_ids, batch, true, draft_ids);
+}
+
+int dflash_sample_path(dflash_ctx *ctx, const int32_t *anchor_ids, const int32_t *topk_ids, const float *topk_logits,
+                       const void *final_hidden, int batch, float temperature, const float *uniforms,
+                       int32_t *draft_ids, float *draft_probs, float *pair_scores_out, void *workspace,
+                       size_t workspace_bytes, dflash_stream_t stream) {
+  if (!ctx) return set_error(DFLASH_ERR_ARG, "null context");
+  if (batch < 0) return set_error(DFLASH_ERR_ARG, "negative batch");
+  if (batch == 0) return DFLASH_OK;
+  if (!(temperature > 0.f)) return set_error(DFLASH_ERR_ARG, "temperature must be positive");
+  if (!topk_ids || !topk_logits || !uniforms || !draft_ids || !draft_probs)
+    return set_error(DFLASH_ERR_ARG, "dflash_sample_path: null argument");
+  const dflash_config &g = ctx->cfg;
+  Launch lc = make_launch(ctx, workspace, reinterpret_cast<cudaStream_t>(stream));
+  const float *sc = nullptr;
+  if (g.use_selector) {
+    if (!anchor_ids || !final_hidden)
+      return set_error(DFLASH_ERR_ARG, "dflash_sample_path: the selector needs anchors and final_hidden");
+    float *s = pair_scores_out;
+    if (!s) {
+      if (int e = check_ws(ctx, workspace, workspace_bytes, batch, 0)) return e;
+      s = at<float>(workspace, layout(ctx, batch, 0).scores);
+    }
+    if (int e = pair_scores(lc, g.dtype == DFLASH_F32, anchor_ids, topk_ids, topk_logits, final_hidden, batch,
+                            g.hidden, ctx->w.sel_e256, ctx->w.sel_a, ctx->w.sel_b, g.sel_rank, g.sel_dim,
+                            ctx->w.sel_w_g, ctx->w.sel_b_g, s))
+      return e;
+    sc = s;
+  }
+  return sample_path(lc, sc, topk_logits, topk_ids, batch, temperature, uniforms, draft_ids, draft_probs);
+}
+
+int dflash_verify_rejection(dflash_ctx *ctx, const float *target_logits, const int32_t *draft_ids,
+                            const int32_t *topk_ids, const float *draft_probs, const float *u_accept,
+                            const float *u_bonus, int batch, int32_t *accept_len, int32_t *bonus, int32_t *committed,
+                            void *workspace, size_t workspace_bytes, dflash_stream_t stream) {
+  if (!ctx) return set_error(DFLASH_ERR_ARG, "null context");
+  if (batch < 0) return set_error(DFLASH_ERR_ARG, "negative batch");
+  if (batch == 0) return DFLASH_OK;
+  if (!target_logits || !draft_ids || !topk_ids || !draft_probs || !u_accept || !u_bonus || !accept_len || !bonus ||
+      !committed)
+    return set_error(DFLASH_ERR_ARG, "dflash_verify_rejection: null argument");
+  if (int e = check_ws(ctx, workspace, workspace_bytes, batch, 0)) return e;
+  Launch lc = make_launch(ctx, workspace, reinterpret_cast<cudaStream_t>(stream));
+  return verify_rejection(lc, target_logits, ctx->cfg.vocab, at<float>(workspace, layout(ctx, batch, 0).lse),
+                          draft_ids, topk_ids, draft_probs, u_accept, u_bonus, batch, accept_len, bonus, committed);
 }
 
 int dflash_verify_greedy(const int32_t *draft_ids, const int32_t *target_ids, int batch, int32_t *accept_len,

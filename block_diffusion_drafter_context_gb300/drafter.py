@@ -209,6 +209,28 @@ class Drafter:
                              self.workspace, self.ws_bytes, stream)
         return draft, scores
 
+    def sample_path(self, anchor_ids, topk_ids, topk_logits, final_hidden, temperature, uniforms, stream=None):
+        """Draft drawn over the path scores at a temperature: (draft [b,15], q [b,15,16])."""
+        torch = _torch()
+        b = int(topk_ids.shape[0])
+        draft = torch.empty((b, 15), dtype=torch.int32, device=self.device)
+        probs = torch.empty((b, 15, 16), dtype=torch.float32, device=self.device)
+        B.dflash_sample_path(self.ctx, anchor_ids, topk_ids, topk_logits, final_hidden, b, temperature, uniforms,
+                             draft, probs, None, self.workspace, self.ws_bytes, stream)
+        return draft, probs
+
+    def verify_rejection(self, target_logits, draft_ids, topk_ids, draft_probs, u_accept, u_bonus, stream=None):
+        """Rejection-sampling verification: (accept_len, bonus, committed)."""
+        torch = _torch()
+        b = int(draft_ids.shape[0])
+        dev = draft_ids.device
+        acc = torch.empty(b, dtype=torch.int32, device=dev)
+        bonus = torch.empty(b, dtype=torch.int32, device=dev)
+        com = torch.empty((b, 16), dtype=torch.int32, device=dev)
+        B.dflash_verify_rejection(self.ctx, target_logits, draft_ids, topk_ids, draft_probs, u_accept, u_bonus, b,
+                                  acc, bonus, com, self.workspace, self.ws_bytes, stream)
+        return acc, bonus, com
+
     @staticmethod
     def verify_greedy(draft_ids, target_ids, stream=None):
         torch = _torch()

@@ -7,6 +7,9 @@
  *   dflash_select_path      top-16 candidates -> one draft (DFlash-2 Path
  *                           Selector, or top-1 per position)
  *   dflash_verify_greedy    greedy prefix acceptance against target tokens
+ * and the sampling modes of the same steps:
+ *   dflash_sample_path      a draft drawn over the path scores at a temperature
+ *   dflash_verify_rejection rejection sampling against target logits (lossless)
  *
  * Pages the operations are defined by (cited below by these tags):
  *   [DF]  "DFlash - Difusion de Bloques para Decodificacion Especulativa en
@@ -226,6 +229,40 @@ DFLASH_API int dflash_select_path(dflash_ctx *ctx, const int32_t *anchor_ids, co
 DFLASH_API int dflash_verify_greedy(const int32_t *draft_ids, const int32_t *target_ids, int batch,
                          int32_t *accept_len, int32_t *bonus, int32_t *committed,
                          dflash_stream_t stream);
+
+/* [DF2] Arquitectura del Sistema item 1 (selection "by sampling over these
+ * precomputed scores").  Same scores as dflash_select_path (pair scores with
+ * use_selector, else every row = the top-16 logits); at position j the draft
+ * distribution over the 16 candidates is q_j = softmax(s_j(c_{j-1}, .) / T),
+ * c_0 the anchor row, and c_j is the first candidate (in candidate order)
+ * whose running probability exceeds uniforms[j] * total.
+ *   temperature:  T > 0.
+ *   uniforms:     device fp32 [batch][15] in [0, 1) (the caller's random draws).
+ *   draft_ids:    device int32 [batch][15] out.
+ *   draft_probs:  device fp32 [batch][15][16] out: q_j over the candidates, as
+ *                 needed by dflash_verify_rejection.
+ *   pair_scores:  device fp32 [batch][15][16][16] out, or NULL. */
+DFLASH_API int dflash_sample_path(dflash_ctx *ctx, const int32_t *anchor_ids, const int32_t *topk_ids,
+                       const float *topk_logits, const void *final_hidden, int batch, float temperature,
+                       const float *uniforms, int32_t *draft_ids, float *draft_probs, float *pair_scores,
+                       void *workspace, size_t workspace_bytes, dflash_stream_t stream);
+
+/* [DF2] Arquitectura del Sistema item 1 ("rejection sampling to restore the
+ * exact distribution of the target model").  p_i = softmax(target_logits[i]),
+ * the target's distributions over the drafted block (one target pass);
+ * draft token d_i is accepted while u_accept[i] * q_i(d_i) < p_i(d_i); at the
+ * first rejection k the bonus is drawn from max(0, p_k - q_k) (q_k zero
+ * outside position k's candidates), after 15 acceptances from p_15, both by
+ * inverse CDF in vocabulary order with u_bonus; committed = d_0..d_{k-1},
+ * bonus, then -1.  The committed tokens follow the target's distribution.
+ *   target_logits: device fp32 [batch][16][V], V = the context's vocabulary.
+ *   draft_ids, topk_ids, draft_probs: from dflash_sample_path / draft_block.
+ *   u_accept: device fp32 [batch][15]; u_bonus: device fp32 [batch], in [0, 1).
+ *   accept_len, bonus: device int32 [batch]; committed: device int32 [batch][16]. */
+DFLASH_API int dflash_verify_rejection(dflash_ctx *ctx, const float *target_logits, const int32_t *draft_ids,
+                       const int32_t *topk_ids, const float *draft_probs, const float *u_accept,
+                       const float *u_bonus, int batch, int32_t *accept_len, int32_t *bonus,
+                       int32_t *committed, void *workspace, size_t workspace_bytes, dflash_stream_t stream);
 
 /* Synchronise `stream`, read the workspace's device status word into
  * *device_status (0 = clean) and clear it.  Returns DFLASH_ERR_TIMEOUT or
