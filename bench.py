@@ -265,6 +265,18 @@ def run_ours(args, wl):
     bonus = torch.empty(B, dtype=torch.int32, device=dev)
     com = torch.empty((B, 16), dtype=torch.int32, device=dev)
     target_d = torch.zeros((B, 16), dtype=torch.int32, device=dev)
+    sampling = args.mode == "sampling"
+    if sampling:
+        # sampling mode: draft drawn over the path scores (T = 1) and rejection
+        # verification against target logits resident in HBM (in serving they
+        # come from the target model on the same GPU); seeded uniforms
+        rng = np.random.default_rng(wl.seed)
+        uni = rng.random((B, 15)).astype(np.float32)
+        ua = rng.random((B, 15)).astype(np.float32)
+        ub = rng.random(B).astype(np.float32)
+        uni_d, ua_d, ub_d = (torch.from_numpy(a).to(dev) for a in (uni, ua, ub))
+        zt_d = torch.from_numpy(gen.normal((B, 16, cfg.vocab), 1.5, wl.seed, "target_logits")).to(dev)
+        probs = torch.empty((B, 15, 16), dtype=torch.float32, device=dev)
 
     def step(x_in=Xn_d, a_in=anc_d, t_in=None):
         st = torch.cuda.current_stream().cuda_stream
@@ -273,6 +285,12 @@ def run_ours(args, wl):
                                  dr.ws_bytes, st)
         Bd.dflash_draft_block(dr.ctx, kv.struct, ctx_after, a_in, B, topk_ids, topk_logits, hfin, None,
                               dr.workspace, dr.ws_bytes, st)
+        if sampling:
+            Bd.dflash_sample_path(dr.ctx, a_in, topk_ids, topk_logits, hfin, B, 1.0, uni_d, draft, probs, scores,
+                                  dr.workspace, dr.ws_bytes, st)
+            Bd.dflash_verify_rejection(dr.ctx, zt_d, draft, topk_ids, probs, ua_d, ub_d, B, acc, bonus, com,
+                                       dr.workspace, dr.ws_bytes, st)
+            return
         Bd.dflash_select_path(dr.ctx, a_in, topk_ids, topk_logits, hfin, B, draft, scores, dr.workspace,
                               dr.ws_bytes, st)
         Bd.dflash_verify_greedy(draft, t_in, B, acc, bonus, com, st)
@@ -339,7 +357,10 @@ def run_ours(args, wl):
     # ---- end to end through the public API with host buffers
     pin_x = torch.from_numpy(Xn.view(np.int16) if Xn.dtype == np.uint16 else Xn).pin_memory()
     pin_a = torch.from_numpy(anchor).pin_memory()
-    pin_t = torch.from_numpy(tgt).pin_memory()
+    # per-step host inputs: the target's tokens (greedy) or the step's uniforms (sampling)
+    pin_t = (torch.from_numpy(np.concatenate([uni.ravel(), ua.ravel(), ub])).pin_memory() if sampling
+             else torch.from_numpy(tgt).pin_memory())
+    uni_all = torch.cat([uni_d.view(-1), ua_d.view(-1), ub_d.view(-1)]) if sampling else None
     out_acc = torch.empty(B, dtype=torch.int32).pin_memory()
     out_bonus = torch.empty(B, dtype=torch.int32).pin_memory()
     out_com = torch.empty((B, 16), dtype=torch.int32).pin_memory()
@@ -349,7 +370,13 @@ def run_ours(args, wl):
     def step_e2e():
         x_dev.copy_(pin_x, non_blocking=True)
         anc_d.copy_(pin_a, non_blocking=True)
-        target_d.copy_(pin_t, non_blocking=True)
+        if sampling:
+            uni_all.copy_(pin_t, non_blocking=True)
+            uni_d.view(-1).copy_(uni_all[:B * 15], non_blocking=True)
+            ua_d.view(-1).copy_(uni_all[B * 15:B * 30], non_blocking=True)
+            ub_d.copy_(uni_all[B * 30:], non_blocking=True)
+        else:
+            target_d.copy_(pin_t, non_blocking=True)
         graph.replay()
         out_acc.copy_(acc, non_blocking=True)
         out_bonus.copy_(bonus, non_blocking=True)
@@ -413,6 +440,7 @@ def run_ours(args, wl):
 
     line = {
         "metric": METRIC, "value": blocks, "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
+        "mode": "sampling (T=1 path sampling, rejection verification)" if sampling else "greedy",
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": workload_desc(wl), "batch": B, "ctx": int(ctx.max()),
@@ -452,6 +480,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="C1")
     ap.add_argument("--skip-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--mode", default="greedy", choices=["greedy", "sampling"],
+                    help="path selection and verification: greedy (default) or sampling + rejection")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = WORKLOADS[args.workload]

@@ -188,7 +188,7 @@ Layout layout(const dflash_ctx *c, int B, int Tn) {
   L.hfinal = take(te * R * H);
   L.logits = take(4ull * B * 15 * V);
   L.scores = take(4ull * B * 15 * 256);
-  L.lse = take(4ull * B * 16);
+  L.lse = take(4ull * verify_rejection_scratch_floats(B));   // rejection verification scratch
   L.fc = take(4ull * Tn * H);
   L.f = take(te * Tn * H);
   L.f_lo = take(tl * Tn * H);

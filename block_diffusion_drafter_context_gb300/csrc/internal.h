@@ -148,7 +148,8 @@ int conv_apply(const Launch &lc, bool f32, const void *y, const void *y_lo, cons
 // ---------------------------------------------------------------- top-k / select / verify
 int sample_path(const Launch &lc, const float *scores, const float *topk_logits, const int32_t *topk_ids, int B,
                 float temperature, const float *uniforms, int32_t *draft, float *qprob);
-int verify_rejection(const Launch &lc, const float *target_logits, int V, float *lse, const int32_t *draft,
+int verify_rejection_scratch_floats(int B);
+int verify_rejection(const Launch &lc, const float *target_logits, int V, float *scratch, const int32_t *draft,
                      const int32_t *topk_ids, const float *qprob, const float *u_accept, const float *u_bonus, int B,
                      int32_t *accept, int32_t *bonus, int32_t *committed);
 int topk16(const Launch &lc, const float *logits, int rows, int V, int32_t *ids, float *vals,

@@ -194,152 +194,260 @@ __global__ void sample_kernel(const float *scores, const float *topk_logits, con
   }
 }
 
-// log-sum-exp of one row of target logits: grid (16 positions, B), 256 threads.
-__global__ void __launch_bounds__(256) row_lse_kernel(const float *logits, int V, float *lse) {
-  pdl_start();
-  const float *row = logits + (static_cast<size_t>(blockIdx.y) * 16 + blockIdx.x) * V;
-  float m = -INFINITY, s = 0.f;
-  auto add = [&](float x) {
-    if (x > m) {
-      s = s * expf(m - x) + 1.f;
-      m = x;
-    } else {
-      s += expf(x - m);
-    }
-  };
-  if ((V & 3) == 0) {
+// Target rows are cut into LSE_CH chunks for the log-sum-exp and RES_CH
+// chunks for the residual draw, so that a single request still spreads
+// over many CTAs.
+constexpr int LSE_CH = 8;
+constexpr int RES_CH = 32;
+constexpr float LOG2E = 1.4426950408889634f;
+
+// Chunk [x0, x1) of a row (x0 a multiple of 4 when the row is 16-byte
+// aligned): max, or sum of exp2(x * LOG2E + off), with 16-byte loads, four
+// in flight per thread.
+template <bool SUM>
+__device__ __forceinline__ float chunk_reduce(const float *row, int x0, int x1, bool vec, float off) {
+  float acc = SUM ? 0.f : -INFINITY;
+  auto f = [&](float x) { acc = SUM ? acc + exp2f(fmaf(x, LOG2E, off)) : fmaxf(acc, x); };
+  int x = x0;
+  if (vec) {
     const float4 *r4 = reinterpret_cast<const float4 *>(row);
-    for (int i = threadIdx.x; i < V / 4; i += blockDim.x) {
-      const float4 v = r4[i];
-      add(v.x);
-      add(v.y);
-      add(v.z);
-      add(v.w);
+    const int i0 = x0 >> 2, i1 = x1 >> 2;
+    int i = i0 + threadIdx.x;
+    for (; i + 3 * static_cast<int>(blockDim.x) < i1; i += 4 * blockDim.x) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = r4[i + u * blockDim.x];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        f(v[u].x);
+        f(v[u].y);
+        f(v[u].z);
+        f(v[u].w);
+      }
     }
-  } else {
-    for (int i = threadIdx.x; i < V; i += blockDim.x) add(row[i]);
+    for (; i < i1; i += blockDim.x) {
+      const float4 v = r4[i];
+      f(v.x);
+      f(v.y);
+      f(v.z);
+      f(v.w);
+    }
+    x = i1 << 2;
   }
+  for (int t = x + static_cast<int>(threadIdx.x); t < x1; t += blockDim.x) f(row[t]);
+  return acc;
+}
+
+__device__ __forceinline__ int chunk_len(int V, int nch, bool vec) {
+  int per = (V + nch - 1) / nch;
+  return vec ? (per + 3) & ~3 : per;
+}
+
+// (max, sum exp(x - max)) of one chunk of one target row: grid (LSE_CH,
+// 16 positions, B), 256 threads; a max pass, then a branch-free sum pass.
+__global__ void __launch_bounds__(256) row_lse_kernel(const float *logits, int V, float2 *part) {
+  pdl_start();
+  const float *row = logits + (static_cast<size_t>(blockIdx.z) * 16 + blockIdx.y) * V;
+  const bool vec = (V & 3) == 0;
+  const int per = chunk_len(V, LSE_CH, vec);
+  const int x0 = min(V, blockIdx.x * per), x1 = min(V, x0 + per);
+  float m = chunk_reduce<false>(row, x0, x1, vec, 0.f);
   __shared__ float sm[8], ss[8];
+  __shared__ float bm;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const float wm = warp_max(m);
-  s = warp_sum(m == -INFINITY ? 0.f : s * expf(m - wm));
-  if (lane == 0) {
-    sm[warp] = wm;
-    ss[warp] = s;
-  }
+  float wm = warp_max(m);
+  if (lane == 0) sm[warp] = wm;
   __syncthreads();
   if (threadIdx.x == 0) {
-    float M = -INFINITY, S = 0.f;
+    float M = -INFINITY;
     for (int w = 0; w < 8; ++w) M = fmaxf(M, sm[w]);
-    for (int w = 0; w < 8; ++w) S += ss[w] == 0.f ? 0.f : ss[w] * expf(sm[w] - M);
-    lse[blockIdx.y * 16 + blockIdx.x] = M + logf(S);
+    bm = M;
+  }
+  __syncthreads();
+  const float M = bm, off = -M * LOG2E;
+  float s = M == -INFINITY ? 0.f : chunk_reduce<true>(row, x0, x1, vec, off);
+  s = warp_sum(s);
+  __syncthreads();
+  if (lane == 0) ss[warp] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float S = 0.f;
+    for (int w = 0; w < 8; ++w) S += ss[w];
+    part[(static_cast<size_t>(blockIdx.z) * 16 + blockIdx.y) * LSE_CH + blockIdx.x] = make_float2(M, S);
   }
 }
 
-// Rejection-sampling verification, one CTA (256 threads) per request: accept
-// while u_i * q_i(d_i) < p_i(d_i); then the bonus by inverse CDF in
-// vocabulary order from max(0, p_k - q_k) (p_15 after 15 acceptances).  Each
-// thread owns a contiguous vocabulary range; a block scan of the range sums
-// finds the range holding u * Z, whose owner walks it.
-__global__ void __launch_bounds__(256) reject_kernel(const float *logits, int V, const float *lse,
-                                                     const int32_t *draft, const int32_t *topk_ids,
-                                                     const float *qprob, const float *u_accept,
-                                                     const float *u_bonus, int32_t *accept, int32_t *bonus,
-                                                     int32_t *committed) {
-  pdl_start();
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __shared__ int k_sh, pick_sh;
-  __shared__ int cid[K];
-  __shared__ float cq[K];
-  __shared__ float wsum[8];
-  if (warp == 0) {   // accept loop: lanes 0..14 test their position, the first failure wins
-    bool ok = true;
-    if (lane < J) {
-      const size_t row = static_cast<size_t>(b) * J + lane;
-      const int d = draft[row];
-      int c = 0;   // the draft token's place among the candidates
-      for (int i = 0; i < K; ++i)
-        if (topk_ids[row * K + i] == d) {
-          c = i;
-          break;
-        }
-      const float p = expf(logits[(static_cast<size_t>(b) * 16 + lane) * V + d] - lse[b * 16 + lane]);
-      ok = u_accept[row] * qprob[row * K + c] < p;
-    }
-    const unsigned fail = __ballot_sync(0xffffffffu, lane < J && !ok);
-    if (lane == 0) k_sh = fail ? __ffs(fail) - 1 : J;
+__device__ __forceinline__ float row_lse(const float2 *part, int b, int i) {
+  const float2 *p = part + (static_cast<size_t>(b) * 16 + i) * LSE_CH;
+  float M = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < LSE_CH; ++c) M = fmaxf(M, p[c].x);
+  float S = 0.f;
+#pragma unroll
+  for (int c = 0; c < LSE_CH; ++c) S += p[c].y == 0.f ? 0.f : p[c].y * exp2f((p[c].x - M) * LOG2E);
+  return M + logf(S);
+}
+
+// The accept decisions of request b (lanes 0..14 of one warp): k = first rejection.
+__device__ __forceinline__ int first_reject(const float *logits, int V, const float2 *part, const int32_t *draft,
+                                            const int32_t *topk_ids, const float *qprob, const float *u_accept,
+                                            int b, int lane) {
+  bool ok = true;
+  if (lane < J) {
+    const size_t row = static_cast<size_t>(b) * J + lane;
+    const int d = draft[row];
+    int c = 0;   // the draft token's place among the candidates
+    for (int i = 0; i < K; ++i)
+      if (topk_ids[row * K + i] == d) {
+        c = i;
+        break;
+      }
+    const float p = expf(logits[(static_cast<size_t>(b) * 16 + lane) * V + d] - row_lse(part, b, lane));
+    ok = u_accept[row] * qprob[row * K + c] < p;
   }
-  __syncthreads();
-  const int k = k_sh;
-  const bool resid = k < J;
-  if (tid < K) {
-    cid[tid] = resid ? topk_ids[(static_cast<size_t>(b) * J + k) * K + tid] : -1;
-    cq[tid] = resid ? qprob[(static_cast<size_t>(b) * J + k) * K + tid] : 0.f;
-  }
-  __syncthreads();
-  const float *zr = logits + (static_cast<size_t>(b) * 16 + k) * V;
-  const float l = lse[b * 16 + k];
-  const int per = (V + blockDim.x - 1) / blockDim.x;
-  const int x0 = min(V, tid * per), x1 = min(V, x0 + per);
-  auto weight = [&](int x, bool use_resid) -> float {   // r(x) = max(0, p(x) - q(x)), or p(x)
-    float w = expf(zr[x] - l);
-    if (use_resid)
+  const unsigned fail = __ballot_sync(0xffffffffu, lane < J && !ok);
+  return fail ? __ffs(fail) - 1 : J;
+}
+
+// r(x) of the decisive row: max(0, p(x) - q(x)) after a rejection, p(x) after 15 acceptances.
+struct Resid {
+  const float *z;
+  float lse;
+  bool resid;
+  int cid[K];
+  float cq[K];
+  __device__ float w(int x) const {
+    float v = expf(z[x] - lse);
+    if (resid)
 #pragma unroll
       for (int c = 0; c < K; ++c)
-        if (cid[c] == x) w = fmaxf(w - cq[c], 0.f);
-    return w;
-  };
-  // range sums: p over the range minus min(p, q) for candidates inside it
-  float mine = 0.f;
-  for (int x = x0; x < x1; ++x) mine += expf(zr[x] - l);
-  if (resid)
+        if (cid[c] == x) v = fmaxf(v - cq[c], 0.f);
+    return v;
+  }
+};
+
+__device__ __forceinline__ void make_resid(Resid &r, const float *logits, int V, const float2 *part,
+                                           const int32_t *topk_ids, const float *qprob, int b, int k) {
+  r.z = logits + (static_cast<size_t>(b) * 16 + k) * V;
+  r.lse = row_lse(part, b, k);
+  r.resid = k < J;
 #pragma unroll
+  for (int c = 0; c < K; ++c) {
+    r.cid[c] = r.resid ? topk_ids[(static_cast<size_t>(b) * J + k) * K + c] : -1;
+    r.cq[c] = r.resid ? qprob[(static_cast<size_t>(b) * J + k) * K + c] : 0.f;
+  }
+}
+
+// Sums of r over RES_CH chunks of the decisive row: grid (RES_CH, B), 256 threads.
+__global__ void __launch_bounds__(256) resid_sum_kernel(const float *logits, int V, const float2 *part,
+                                                        const int32_t *draft, const int32_t *topk_ids,
+                                                        const float *qprob, const float *u_accept, float *csum) {
+  pdl_start();
+  const int b = blockIdx.y;
+  __shared__ int k_sh;
+  if (threadIdx.x < 32) {
+    const int k = first_reject(logits, V, part, draft, topk_ids, qprob, u_accept, b, threadIdx.x);
+    if (threadIdx.x == 0) k_sh = k;
+  }
+  __syncthreads();
+  Resid r;
+  make_resid(r, logits, V, part, topk_ids, qprob, b, k_sh);
+  const bool vec = (V & 3) == 0;
+  const int per = chunk_len(V, RES_CH, vec);
+  const int x0 = min(V, blockIdx.x * per), x1 = min(V, x0 + per);
+  float s = chunk_reduce<true>(r.z, x0, x1, vec, -r.lse * LOG2E);
+  // candidates inside the chunk: r = p - min(p, q)
+  if (threadIdx.x == 0 && r.resid)
     for (int c = 0; c < K; ++c)
-      if (cid[c] >= x0 && cid[c] < x1) mine -= fminf(expf(zr[cid[c]] - l), cq[c]);
-  mine = fmaxf(mine, 0.f);
-  // block exclusive scan of the range sums (thread order = vocabulary order)
-  float inc = mine;
+      if (r.cid[c] >= x0 && r.cid[c] < x1) s -= fminf(expf(r.z[r.cid[c]] - r.lse), r.cq[c]);
+  s = warp_sum(s);
+  __shared__ float ws[8];
+  if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < 8; ++w) t += ws[w];
+    csum[b * RES_CH + blockIdx.x] = fmaxf(t, 0.f);
+  }
+}
+
+// One CTA (256 threads) per request: the accept decisions, the chunk holding
+// u * Z (chunk sums in vocabulary order), then that chunk's inverse CDF:
+// per-thread contiguous ranges, a block scan, the owner walks its range.
+__global__ void __launch_bounds__(256) reject_kernel(const float *logits, int V, const float2 *part,
+                                                     const float *csum, const int32_t *draft,
+                                                     const int32_t *topk_ids, const float *qprob,
+                                                     const float *u_accept, const float *u_bonus, int32_t *accept,
+                                                     int32_t *bonus, int32_t *committed) {
+  pdl_start();
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ int k_sh, chunk_sh, pick_sh;
+  __shared__ float base_sh, total_sh;
+  __shared__ float wsum[8];
+  if (warp == 0) {
+    const int k = first_reject(logits, V, part, draft, topk_ids, qprob, u_accept, b, lane);
+    // chunk sums: running total in chunk order (lanes = chunks)
+    const float c = lane < RES_CH ? csum[b * RES_CH + lane] : 0.f;
+    float inc = c;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float t = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += t;
-  }
-  if (lane == 31) wsum[warp] = inc;
-  __syncthreads();
-  float base = 0.f, Z = 0.f;
-  for (int w = 0; w < 8; ++w) {
-    if (w < warp) base += wsum[w];
-    Z += wsum[w];
-  }
-  const float ex = base + inc - mine;
-  // a residual that rounds to nothing (p = q on the candidates: no rejection
-  // in exact arithmetic) takes the fallback below
-  if (threadIdx.x == 0) pick_sh = -1;
-  __syncthreads();
-  if (!resid || Z > 0.f) {
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    const float Z = __shfl_sync(0xffffffffu, inc, 31);
     const float thr = u_bonus[b] * Z;
-    if (thr >= ex && thr < ex + mine) {   // this thread's range holds the draw
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < RES_CH && c > 0.f && thr < inc);
+    const unsigned pos = __ballot_sync(0xffffffffu, lane < RES_CH && c > 0.f);
+    const int ch = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+    if (lane == 0) {
+      k_sh = k;
+      chunk_sh = ch;
+      total_sh = Z;
+      pick_sh = -1;
+    }
+    if (ch >= 0 && lane == ch) base_sh = inc - c;
+  }
+  __syncthreads();
+  const int k = k_sh, ch = chunk_sh;
+  Resid r;
+  make_resid(r, logits, V, part, topk_ids, qprob, b, k);
+  if (ch >= 0) {
+    const int per_c = chunk_len(V, RES_CH, (V & 3) == 0);
+    const int c0 = min(V, ch * per_c), c1 = min(V, c0 + per_c);
+    const int per = (c1 - c0 + blockDim.x - 1) / blockDim.x;
+    const int x0 = min(c1, c0 + tid * per), x1 = min(c1, x0 + per);
+    float mine = 0.f;
+    for (int x = x0; x < x1; ++x) mine += r.w(x);
+    float inc = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    float ex = base_sh + inc - mine;
+    for (int w = 0; w < warp; ++w) ex += wsum[w];
+    const float thr = u_bonus[b] * total_sh;
+    if (mine > 0.f && thr >= ex && thr < ex + mine) {   // this thread's range holds the draw
       float c = ex;
-      int pick = -1;
+      int pick = x1 - 1;
       for (int x = x0; x < x1; ++x) {
-        const float w = weight(x, resid);
-        c += w;
+        c += r.w(x);
         if (c > thr) {
           pick = x;
           break;
         }
       }
-      if (pick < 0) pick = x1 - 1;
       atomicMax(&pick_sh, pick);
     }
   }
   __syncthreads();
-  if (pick_sh < 0 && tid == 0) {
-    // rounding left no range holding the draw (or the residual vanished):
-    // the last token of positive weight under p
+  if (tid == 0 && pick_sh < 0) {
+    // rounding put the draw past every range: the last token of positive weight
     int last = V - 1;
     for (int x = V - 1; x >= 0; --x)
-      if (expf(zr[x] - l) > 0.f) {
+      if (r.w(x) > 0.f) {
         last = x;
         break;
       }
@@ -408,20 +516,27 @@ int sample_path(const Launch &lc, const float *scores, const float *topk_logits,
   return cuda_check(cudaGetLastError(), "sample_path launch");
 }
 
-int verify_rejection(const Launch &lc, const float *target_logits, int V, float *lse, const int32_t *draft,
-                     const int32_t *topk_ids, const float *qprob, const float *u_accept,
-                     const float *u_bonus, int B, int32_t *accept, int32_t *bonus, int32_t *committed) {
+int verify_rejection(const Launch &lc, const float *target_logits, int V, float *scratch, const int32_t *draft,
+                     const int32_t *topk_ids, const float *qprob, const float *u_accept, const float *u_bonus, int B,
+                     int32_t *accept, int32_t *bonus, int32_t *committed) {
   if (B <= 0) return DFLASH_OK;
+  float2 *part = reinterpret_cast<float2 *>(scratch);                  // [B][16][LSE_CH]
+  float *csum = scratch + static_cast<size_t>(B) * 16 * LSE_CH * 2;    // [B][RES_CH]
   {
     ProfScope ps(lc, "target_lse", 4.0 * B * 16 * V, -1.0);
-    launch_pdl(row_lse_kernel, dim3(16, B), dim3(256), 0, lc.stream, target_logits, V, lse);
+    launch_pdl(row_lse_kernel, dim3(LSE_CH, 16, B), dim3(256), 0, lc.stream, target_logits, V, part);
     if (int e = cuda_check(cudaGetLastError(), "target lse launch")) return e;
   }
-  ProfScope ps(lc, "verify_rejection", -1.0, -1.0);
-  launch_pdl(reject_kernel, dim3(B), dim3(256), 0, lc.stream, target_logits, V, static_cast<const float *>(lse),
-             draft, topk_ids, qprob, u_accept, u_bonus, accept, bonus, committed);
+  ProfScope ps(lc, "verify_rejection", 4.0 * B * V, -1.0);
+  launch_pdl(resid_sum_kernel, dim3(RES_CH, B), dim3(256), 0, lc.stream, target_logits, V,
+             static_cast<const float2 *>(part), draft, topk_ids, qprob, u_accept, csum);
+  if (int e = cuda_check(cudaGetLastError(), "residual sums launch")) return e;
+  launch_pdl(reject_kernel, dim3(B), dim3(256), 0, lc.stream, target_logits, V, static_cast<const float2 *>(part),
+             static_cast<const float *>(csum), draft, topk_ids, qprob, u_accept, u_bonus, accept, bonus, committed);
   return cuda_check(cudaGetLastError(), "verify_rejection launch");
 }
+
+int verify_rejection_scratch_floats(int B) { return B * (16 * LSE_CH * 2 + RES_CH); }
 
 int greedy_path(const Launch &lc, const float *scores, const int32_t *topk_ids, int B, bool use_scores,
                 int32_t *draft) {
