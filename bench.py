@@ -1,13 +1,15 @@
 """Benchmark of one DFlash drafting step on GB300.
 
 A step is the whole hot path for every request of the workload: inject the
-16 new tokens' target features into every drafter layer's paged KV cache,
-draft one 16-token block (one forward of the drafter), select the path, and
-verify greedily against synthetic target tokens.  Default workload: the
-Qwen3-8B-shaped drafter (5 layers, hidden 4096, vocab 151936), batch 1,
-2048 tokens of context (configs C2-C4 are parity cases, not bench lines).
+S new tokens' target features into every drafter layer's paged KV cache,
+draft one S-token block (one forward of the drafter), select the path, and
+verify greedily against synthetic target tokens (S = 16 unless the workload
+sets a smaller runtime block size).  Default workload: the Qwen3-8B-shaped
+drafter (5 layers, hidden 4096, vocab 151936), batch 1, 2048 tokens of
+context (configs C2-C4 are parity cases, not bench lines).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload C1|C2|C3|C4|C1S5|C2S5] [--mode greedy|sampling]
 
 Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle
 on the same workload instead (the deliberately slow reference arm).
@@ -31,6 +33,10 @@ sys.path.insert(0, ROOT)
 from synthetic import WORKLOADS, gen  # noqa: E402
 
 METRIC = "drafted blocks/sec (16-tok) at batch×ctx on 1 GB300; attention HBM GB/s"
+
+
+def metric(cfg) -> str:
+    return METRIC if cfg.block == 16 else METRIC.replace("(16-tok)", f"({cfg.block}-tok)")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -47,7 +53,8 @@ def workload_desc(wl):
     return (f"{wl.name}: {c.name} drafter (L={c.n_layers}, H={c.hidden}, {c.n_q_heads}q/{c.n_kv_heads}kv x "
             f"{c.head_dim}, F={c.ffn}, V={c.vocab}), batch {wl.batch}, context "
             f"{wl.ctx_lo if wl.ctx_lo == wl.ctx_hi else f'U[{wl.ctx_lo},{wl.ctx_hi}]'}, "
-            f"{c.n_target_layers}x{c.target_hidden} target features, 16 new tokens injected per step")
+            f"{c.n_target_layers}x{c.target_hidden} target features, block size {c.block}, "
+            f"{c.block} new tokens injected per step")
 
 
 # ---------------------------------------------------------------- clocks
@@ -59,16 +66,20 @@ class ClockSampler:
 
     def __init__(self, index: int):
         self.index = index
-        self.rows = []
+        self.rows = []          # (host arrival time, fields)
         self.proc = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.perf_counter() + 3.0   # running before the timed region starts
+            while not self.rows and time.perf_counter() < deadline:
+                time.sleep(0.005)
         except Exception:
             self.proc = None
         return self
@@ -77,7 +88,17 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 9:
-                self.rows.append(parts)
+                self.rows.append((time.perf_counter(), parts))
+
+    def mark(self, start: bool):
+        """Host time of the timed region's start / end."""
+        if start:
+            self.t0 = time.perf_counter()
+        else:
+            self.t1 = time.perf_counter()
+            deadline = self.t1 + 0.2               # one sample after the region ends
+            while time.perf_counter() < deadline and not any(t > self.t1 for t, _ in self.rows):
+                time.sleep(0.005)
 
     def __exit__(self, *a):
         if self.proc:
@@ -88,14 +109,21 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        if not self.rows:
+        rows = self.rows
+        if self.t0 is not None and self.t1 is not None:
+            inside = [r for t, r in rows if self.t0 <= t <= self.t1]
+            after = [r for t, r in rows if t > self.t1][:1]
+            rows = inside + after
+        else:
+            rows = [r for _, r in rows]
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in self.rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.rows)}
+                "reasons": reasons, "samples": len(rows)}
 
 
 # ---------------------------------------------------------------- multi-rank helpers
@@ -139,8 +167,9 @@ def oracle_setup(wl, W, ctx, X_prefill, cu, requests=None, templates=None, table
 def oracle_step(wl, W, kvs, ctx, Xn, anchor, target, requests):
     import oracle as O
     outs = []
+    S = wl.cfg.block
     for b in requests:
-        outs.append(O.drafting_step(wl.cfg, W, kvs[b], int(ctx[b]), Xn[16 * b:16 * (b + 1)], int(anchor[b]),
+        outs.append(O.drafting_step(wl.cfg, W, kvs[b], int(ctx[b]), Xn[S * b:S * (b + 1)], int(anchor[b]),
                                     target[b]))
     return outs
 
@@ -162,11 +191,11 @@ def make_inputs(wl):
     W = gen.make_weights(cfg, wl.seed)
     ctx = gen.context_lengths(wl)
     B = len(ctx)
-    table, npages = gen.page_table(ctx + 16, cfg.page_size, wl.seed)
+    table, npages = gen.page_table(ctx + cfg.block, cfg.page_size, wl.seed)
     cu = np.concatenate([[0], np.cumsum(ctx)]).astype(np.int32)
     # drawn cache state (template pages) or a prefill through the injection
     Xp = None if wl.kv_fill == "template" else gen.target_hidden(cfg, int(ctx.sum()), wl.seed, "prefill")
-    Xn = gen.target_hidden(cfg, 16 * B, wl.seed, "step")
+    Xn = gen.target_hidden(cfg, cfg.block * B, wl.seed, "step")
     anchor = gen.anchors(wl)
     return W, ctx, table, npages, cu, Xp, Xn, anchor
 
@@ -186,7 +215,8 @@ def run_reference(args, wl):
     kvs = oracle_setup(wl, W, ctx, Xp, cu, templates=kv_templates(wl, npages), table=table)
     setup_s = time.time() - t0
     import oracle as O
-    first = oracle_step(wl, W, kvs, ctx, Xn, anchor, np.zeros((wl.batch, 16), np.int32), range(wl.batch))
+    first = oracle_step(wl, W, kvs, ctx, Xn, anchor, np.zeros((wl.batch, wl.cfg.block), np.int32),
+                        range(wl.batch))
     draft = np.stack([o["draft"] for o in first])
     target = gen.target_ids(draft, wl.p_accept, wl.cfg.vocab, seed=wl.seed)
     for _ in range(args.warmup):
@@ -197,7 +227,7 @@ def run_reference(args, wl):
     el = time.perf_counter() - t0
     v = wl.batch * args.steps / el
     cores = blas_threads()
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "blocks/s", "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric(wl.cfg), "value": v, "unit": "blocks/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": workload_desc(wl), "batch": wl.batch,
@@ -232,9 +262,9 @@ def run_ours(args, wl):
     cfg = wl.cfg
     t_setup = time.time()
     W, ctx, table, npages, cu, Xp, Xn, anchor = make_inputs(wl)
-    B = wl.batch
+    B, S, J = wl.batch, cfg.block, cfg.block - 1
     prefill = 0 if wl.kv_fill == "template" else int(ctx.max())
-    dr = Drafter(cfg, W, max_batch=B, max_new_tokens=max(16 * B, prefill), device=dev)
+    dr = Drafter(cfg, W, max_batch=B, max_new_tokens=max(S * B, prefill), device=dev)
     kv = PagedKV(cfg, table, npages, device=dev)
     stream = torch.cuda.current_stream().cuda_stream
     templates = kv_templates(wl, npages)
@@ -252,36 +282,36 @@ def run_ours(args, wl):
                                      int(ctx[b]), ctx0[:1], ctx_n[b:b + 1], 1, dr.workspace, dr.ws_bytes, stream)
     torch.cuda.synchronize()
     n_b = to_device(ctx.astype(np.int32), dev)
-    cu_new = to_device((16 * np.arange(B + 1)).astype(np.int32), dev)
+    cu_new = to_device((S * np.arange(B + 1)).astype(np.int32), dev)
     Xn_d = to_device(Xn, dev)
     anc_d = to_device(anchor, dev)
     ctx_after = torch.empty(B, dtype=torch.int32, device=dev)
-    topk_ids = torch.empty((B, 15, 16), dtype=torch.int32, device=dev)
-    topk_logits = torch.empty((B, 15, 16), dtype=torch.float32, device=dev)
-    hfin = torch.empty((B, 16, cfg.hidden), dtype=dr.act_dtype, device=dev)
-    draft = torch.empty((B, 15), dtype=torch.int32, device=dev)
-    scores = torch.empty((B, 15, 16, 16), dtype=torch.float32, device=dev) if cfg.use_selector else None
+    topk_ids = torch.empty((B, J, 16), dtype=torch.int32, device=dev)
+    topk_logits = torch.empty((B, J, 16), dtype=torch.float32, device=dev)
+    hfin = torch.empty((B, S, cfg.hidden), dtype=dr.act_dtype, device=dev)
+    draft = torch.empty((B, J), dtype=torch.int32, device=dev)
+    scores = torch.empty((B, J, 16, 16), dtype=torch.float32, device=dev) if cfg.use_selector else None
     acc = torch.empty(B, dtype=torch.int32, device=dev)
     bonus = torch.empty(B, dtype=torch.int32, device=dev)
-    com = torch.empty((B, 16), dtype=torch.int32, device=dev)
-    target_d = torch.zeros((B, 16), dtype=torch.int32, device=dev)
+    com = torch.empty((B, S), dtype=torch.int32, device=dev)
+    target_d = torch.zeros((B, S), dtype=torch.int32, device=dev)
     sampling = args.mode == "sampling"
     if sampling:
         # sampling mode: draft drawn over the path scores (T = 1) and rejection
         # verification against target logits resident in HBM (in serving they
         # come from the target model on the same GPU); seeded uniforms
         rng = np.random.default_rng(wl.seed)
-        uni = rng.random((B, 15)).astype(np.float32)
-        ua = rng.random((B, 15)).astype(np.float32)
+        uni = rng.random((B, J)).astype(np.float32)
+        ua = rng.random((B, J)).astype(np.float32)
         ub = rng.random(B).astype(np.float32)
         uni_d, ua_d, ub_d = (torch.from_numpy(a).to(dev) for a in (uni, ua, ub))
-        zt_d = torch.from_numpy(gen.normal((B, 16, cfg.vocab), 1.5, wl.seed, "target_logits")).to(dev)
-        probs = torch.empty((B, 15, 16), dtype=torch.float32, device=dev)
+        zt_d = torch.from_numpy(gen.normal((B, S, cfg.vocab), 1.5, wl.seed, "target_logits")).to(dev)
+        probs = torch.empty((B, J, 16), dtype=torch.float32, device=dev)
 
     def step(x_in=Xn_d, a_in=anc_d, t_in=None):
         st = torch.cuda.current_stream().cuda_stream
         t_in = target_d if t_in is None else t_in
-        Bd.dflash_inject_context(dr.ctx, kv.struct, x_in, cu_new, 16 * B, n_b, ctx_after, B, dr.workspace,
+        Bd.dflash_inject_context(dr.ctx, kv.struct, x_in, cu_new, S * B, n_b, ctx_after, B, dr.workspace,
                                  dr.ws_bytes, st)
         Bd.dflash_draft_block(dr.ctx, kv.struct, ctx_after, a_in, B, topk_ids, topk_logits, hfin, None,
                               dr.workspace, dr.ws_bytes, st)
@@ -293,7 +323,7 @@ def run_ours(args, wl):
             return
         Bd.dflash_select_path(dr.ctx, a_in, topk_ids, topk_logits, hfin, B, draft, scores, dr.workspace,
                               dr.ws_bytes, st)
-        Bd.dflash_verify_greedy(draft, t_in, B, acc, bonus, com, st)
+        Bd.dflash_verify_greedy(draft, t_in, B, S, acc, bonus, com, st)
 
     # synthetic target tokens from the step's own draft (identical every step)
     step()
@@ -332,7 +362,9 @@ def run_ours(args, wl):
         return ms
 
     with ClockSampler(local) as cs:
+        cs.mark(True)
         ms = timed(graph.replay, args.steps)
+        cs.mark(False)
     clocks = cs.summary()
     ms_eager = timed(step, args.steps)
     assert dr.status() == 0, "device status after the timed region"
@@ -363,7 +395,7 @@ def run_ours(args, wl):
     uni_all = torch.cat([uni_d.view(-1), ua_d.view(-1), ub_d.view(-1)]) if sampling else None
     out_acc = torch.empty(B, dtype=torch.int32).pin_memory()
     out_bonus = torch.empty(B, dtype=torch.int32).pin_memory()
-    out_com = torch.empty((B, 16), dtype=torch.int32).pin_memory()
+    out_com = torch.empty((B, S), dtype=torch.int32).pin_memory()
     x_dev = Xn_d.view(torch.int16) if Xn.dtype == np.uint16 else Xn_d
     stream = torch.cuda.current_stream()
 
@@ -372,9 +404,9 @@ def run_ours(args, wl):
         anc_d.copy_(pin_a, non_blocking=True)
         if sampling:
             uni_all.copy_(pin_t, non_blocking=True)
-            uni_d.view(-1).copy_(uni_all[:B * 15], non_blocking=True)
-            ua_d.view(-1).copy_(uni_all[B * 15:B * 30], non_blocking=True)
-            ub_d.copy_(uni_all[B * 30:], non_blocking=True)
+            uni_d.view(-1).copy_(uni_all[:B * J], non_blocking=True)
+            ua_d.view(-1).copy_(uni_all[B * J:B * 2 * J], non_blocking=True)
+            ub_d.copy_(uni_all[B * 2 * J:], non_blocking=True)
         else:
             target_d.copy_(pin_t, non_blocking=True)
         graph.replay()
@@ -407,8 +439,8 @@ def run_ours(args, wl):
                               "gbs": (s["bytes"] / (s["ms"] * 1e-3) / 1e9) if s["bytes"] > 0 else None}
                   for s in stats}
     att = [s for s in stats if s["name"] == "attention"]
-    # K and V read per step: each request's context plus the 16 tokens this step injected, plus the 16 block keys
-    kv_bytes_step = float(sum(int(c) + 32 for c in ctx)) * cfg.n_layers * cfg.n_kv_heads * cfg.head_dim * 2 * 2
+    # K and V read per step: each request's context plus the S tokens this step injected, plus the S block keys
+    kv_bytes_step = float(sum(int(c) + 2 * S for c in ctx)) * cfg.n_layers * cfg.n_kv_heads * cfg.head_dim * 2 * 2
     att_ms = sum(s["ms"] for s in att) / args.steps
     att_gbs = kv_bytes_step / (att_ms * 1e-3) / 1e9 if att_ms > 0 else None
     total_ms_inst = sum(s["ms"] for s in stats) / args.steps
@@ -416,7 +448,7 @@ def run_ours(args, wl):
     blocks = aggregate_blocks_per_s(world, B, args.steps, ms)
     exp_k = 0.0
     run_p = 1.0
-    for q in wl.p_accept:
+    for q in wl.p_accept[:J]:
         run_p *= q
         exp_k += run_p
     traffic = None
@@ -435,18 +467,18 @@ def run_ours(args, wl):
         oracle_step(wl, W, kvs, ctx, Xn, anchor, tgt, [0])
         el = time.perf_counter() - t0
         cpu = {"value": 1.0 / el, "unit": "blocks/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"one full drafting step (inject 16 tokens, forward, top-16, select, verify) of request "
+               "sample": f"one full drafting step (inject {S} tokens, forward, top-16, select, verify) of request "
                          f"0 of {B}; {el:.1f} s of fp64 numpy on the host; oracle KV prefill untimed"}
 
     line = {
-        "metric": METRIC, "value": blocks, "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
+        "metric": metric(cfg), "value": blocks, "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
         "mode": "sampling (T=1 path sampling, rejection verification)" if sampling else "greedy",
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": workload_desc(wl), "batch": B, "ctx": int(ctx.max()),
                    "l2": "no flush: every step streams 3.4 GB of drafter weights, > 129 MB L2",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "draft_tokens_per_s": 15 * blocks,
+        "draft_tokens_per_s": J * blocks,
         "expected_committed_tokens_per_s": (exp_k + 1) * blocks,
         "roofline": {"kernel": "gemm_tc (all tcgen05 GEMM launches of a step)", "bound": "hbm",
                      "achieved": g_bytes / (g_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",

@@ -24,7 +24,8 @@ EXPORTS = (
     "dflash_draft_block", "dflash_select_path", "dflash_verify_greedy", "dflash_read_status",
     "dflash_set_wait_timeout", "dflash_set_gemm_ctas", "dflash_set_attn_split",
     "dflash_profile_begin", "dflash_profile_end", "dflash_debug_wait_flag", "dflash_last_error",
-    "dflash_topk16_noalloc", "dflash_sample_path", "dflash_verify_rejection",
+    "dflash_topk16_noalloc", "dflash_sample_path", "dflash_verify_rejection", "dflash_set_block_size",
+    "dflash_get_block_size",
 )
 
 
@@ -85,13 +86,15 @@ def load(path: str = LIB_PATH):
         "dflash_inject_context": (i, [vp, POINTER(dflash_kv), vp, vp, i, vp, vp, i, vp, c_size_t, vp]),
         "dflash_draft_block": (i, [vp, POINTER(dflash_kv), vp, vp, i, vp, vp, vp, vp, vp, c_size_t, vp]),
         "dflash_select_path": (i, [vp, vp, vp, vp, vp, i, vp, vp, vp, c_size_t, vp]),
-        "dflash_verify_greedy": (i, [vp, vp, i, vp, vp, vp, vp]),
+        "dflash_verify_greedy": (i, [vp, vp, i, i, vp, vp, vp, vp]),
         "dflash_sample_path": (i, [vp, vp, vp, vp, vp, i, c_float, vp, vp, vp, vp, vp, c_size_t, vp]),
         "dflash_verify_rejection": (i, [vp, vp, vp, vp, vp, vp, vp, i, vp, vp, vp, vp, c_size_t, vp]),
         "dflash_read_status": (i, [vp, POINTER(c_int), vp]),
         "dflash_set_wait_timeout": (i, [vp, c_ulonglong]),
         "dflash_set_gemm_ctas": (i, [vp, i]),
         "dflash_set_attn_split": (i, [vp, i]),
+        "dflash_set_block_size": (i, [vp, i]),
+        "dflash_get_block_size": (i, [vp]),
         "dflash_profile_begin": (i, [vp]),
         "dflash_profile_end": (i, [vp, POINTER(dflash_kernel_stat), i, POINTER(c_int)]),
         "dflash_debug_wait_flag": (i, [vp, c_ulonglong, vp, vp]),
@@ -164,9 +167,9 @@ def dflash_select_path(ctx, anchor_ids, topk_ids, topk_logits, final_hidden, bat
                                             _p(workspace), workspace_bytes, _stream(stream)))
 
 
-def dflash_verify_greedy(draft_ids, target_ids, batch, accept_len, bonus, committed, stream=None):
-    return _check(load().dflash_verify_greedy(_p(draft_ids), _p(target_ids), batch, _p(accept_len), _p(bonus),
-                                              _p(committed), _stream(stream)))
+def dflash_verify_greedy(draft_ids, target_ids, batch, block_size, accept_len, bonus, committed, stream=None):
+    return _check(load().dflash_verify_greedy(_p(draft_ids), _p(target_ids), batch, block_size, _p(accept_len),
+                                              _p(bonus), _p(committed), _stream(stream)))
 
 
 def dflash_sample_path(ctx, anchor_ids, topk_ids, topk_logits, final_hidden, batch, temperature, uniforms,
@@ -202,6 +205,14 @@ def dflash_set_gemm_ctas(ctx, n: int):
 
 def dflash_set_attn_split(ctx, tokens: int):
     return _check(load().dflash_set_attn_split(ctx, tokens))
+
+
+def dflash_set_block_size(ctx, block_size: int):
+    return _check(load().dflash_set_block_size(ctx, block_size))
+
+
+def dflash_get_block_size(ctx) -> int:
+    return int(load().dflash_get_block_size(ctx))
 
 
 def dflash_profile_begin(ctx):

@@ -22,6 +22,7 @@ struct dflash_ctx {
   unsigned long long timeout_ns = 2000000000ull;
   int gemm_ctas = 0;
   int attn_split = 0;
+  int block = 16;   // runtime block size S (2..cfg.block_size)
   dflash::Profiler prof;
 };
 
@@ -142,11 +143,14 @@ struct Layout {
   size_t gemm_part_floats;
 };
 
-Layout layout(const dflash_ctx *c, int B, int Tn) {
+// Byte offsets of every workspace buffer for batch B, Tn injected tokens and
+// block size S (default: the context's runtime block size).
+Layout layout(const dflash_ctx *c, int B, int Tn, int S_ = 0) {
   const dflash_config &g = c->cfg;
   const size_t te = g.dtype == DFLASH_F32 ? 4 : 2;
   const size_t H = g.hidden, d = g.head_dim, nq = g.n_q_heads, nkv = g.n_kv_heads, F = g.ffn, V = g.vocab;
-  const size_t R = static_cast<size_t>(B) * 16;
+  const size_t S = S_ > 0 ? S_ : c->block, J = S - 1;   // positions per request, mask positions
+  const size_t R = static_cast<size_t>(B) * S;
   Layout L = {};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -163,19 +167,19 @@ Layout layout(const dflash_ctx *c, int B, int Tn) {
   L.attn_part_slots = 2ull * c->num_sms;
   L.attn_part = take(4ull * L.attn_part_slots * ATTN_PART_FLOATS);
   (void)B;
-  L.topk_part = take(8ull * B * 15 * TOPK_MAX_CHUNKS * 16);
+  L.topk_part = take(8ull * B * J * TOPK_MAX_CHUNKS * 16);
   L.x = take(4 * R * H);
   L.u = take(te * R * H);
   L.u2 = take(te * R * H);
   L.qkv = take(4 * R * (nq + 2 * nkv) * d);
   L.q = take(te * R * nq * d);
-  L.bk = take(te * B * nkv * 64 * d);   // block K [B][nkv][64][d], rows 16.. unused
-  L.bv = take(te * B * nkv * 64 * d);   // block V^T [B][nkv][d][64], cols 16.. unused
+  L.bk = take(te * B * nkv * 64 * d);   // block K [B][nkv][64][d], rows S.. unused
+  L.bv = take(te * B * nkv * 64 * d);   // block V^T [B][nkv][d][64], cols S.. unused
   L.o = take(te * R * nq * d);
   L.ysub = take(te * R * H);
   L.coef = take(4 * R * (H / 8));
   L.hmid = take(te * R * F);
-  L.hmask = take(te * B * 15 * H);
+  L.hmask = take(te * B * J * H);
   // low halves of the GEMM activations (split activations, bf16 path)
   const size_t tl = (g.dtype == DFLASH_F32 || !g.split_act) ? 0 : 2;
   L.u_lo = take(tl * R * H);
@@ -183,12 +187,12 @@ Layout layout(const dflash_ctx *c, int B, int Tn) {
   L.o_lo = take(tl * R * nq * d);
   L.ysub_lo = take(tl * R * H);
   L.hmid_lo = take(tl * R * F);
-  L.hmask_lo = take(tl * B * 15 * H);
+  L.hmask_lo = take(tl * B * J * H);
   L.ysub32 = take(4 * R * H);
   L.hfinal = take(te * R * H);
-  L.logits = take(4ull * B * 15 * V);
-  L.scores = take(4ull * B * 15 * 256);
-  L.lse = take(4ull * verify_rejection_scratch_floats(B));   // rejection verification scratch
+  L.logits = take(4ull * B * J * V);
+  L.scores = take(4ull * B * J * 256);
+  L.lse = take(4ull * verify_rejection_scratch_floats(B, static_cast<int>(S)));   // rejection verification scratch
   L.fc = take(4ull * Tn * H);
   L.f = take(te * Tn * H);
   L.f_lo = take(tl * Tn * H);
@@ -284,8 +288,8 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *w, dflash_ctx 
   *out = nullptr;
   const dflash_config &g = *cfg;
   if (g.dtype != DFLASH_BF16 && g.dtype != DFLASH_F32) return set_error(DFLASH_ERR_ARG, "dtype must be bf16 or fp32");
-  if (g.block_size != 16 || g.top_k != 16 || g.page_size != 64)
-    return set_error(DFLASH_ERR_UNSUPPORTED, "block_size and top_k must be 16, page_size 64");
+  if (g.block_size < 2 || g.block_size > 16 || g.top_k != 16 || g.page_size != 64)
+    return set_error(DFLASH_ERR_UNSUPPORTED, "block_size must be 2..16, top_k 16, page_size 64");
   if (g.hidden <= 0 || g.hidden % 16 || g.n_layers < 1 || g.n_layers > 16 || g.n_q_heads <= 0 || g.n_kv_heads <= 0 ||
       g.n_q_heads % g.n_kv_heads || g.ffn <= 0 || g.ffn % 8 || g.vocab < 16 || g.target_hidden <= 0 ||
       g.n_target_layers <= 0 || (g.n_target_layers * g.target_hidden) % 8)
@@ -318,6 +322,7 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *w, dflash_ctx 
     return set_error(DFLASH_ERR_ARG, "selector weights missing");
   dflash_ctx *c = new dflash_ctx();
   c->cfg = g;
+  c->block = g.block_size;
   c->w = *w;
   c->layers.assign(w->layers, w->layers + g.n_layers);
   c->w.layers = c->layers.data();
@@ -334,7 +339,8 @@ void dflash_destroy(dflash_ctx *ctx) { delete ctx; }
 
 size_t dflash_workspace_bytes(const dflash_ctx *ctx, int max_batch, int max_new_tokens) {
   if (!ctx || max_batch < 0 || max_new_tokens < 0) return 0;
-  return layout(ctx, max_batch < 1 ? 1 : max_batch, max_new_tokens).total;
+  // sized for the largest block the context can run, so that any runtime block size fits
+  return layout(ctx, max_batch < 1 ? 1 : max_batch, max_new_tokens, ctx->cfg.block_size).total;
 }
 
 int dflash_set_wait_timeout(dflash_ctx *ctx, unsigned long long ns) {
@@ -348,6 +354,16 @@ int dflash_set_gemm_ctas(dflash_ctx *ctx, int ctas) {
   ctx->gemm_ctas = ctas > ctx->num_sms ? ctx->num_sms : ctas;
   return DFLASH_OK;
 }
+
+int dflash_set_block_size(dflash_ctx *ctx, int block_size) {
+  if (!ctx) return set_error(DFLASH_ERR_ARG, "null context");
+  if (block_size < 2 || block_size > ctx->cfg.block_size)
+    return set_error(DFLASH_ERR_ARG, "runtime block size must be 2..%d", ctx->cfg.block_size);
+  ctx->block = block_size;
+  return DFLASH_OK;
+}
+
+int dflash_get_block_size(const dflash_ctx *ctx) { return ctx ? ctx->block : 0; }
 
 int dflash_set_attn_split(dflash_ctx *ctx, int tokens) {
   if (!ctx || tokens < 0 || tokens % 64) return set_error(DFLASH_ERR_ARG, "split must be a multiple of 64");
@@ -426,7 +442,8 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
   const Layout L = layout(ctx, batch, 0);
   Launch lc = make_launch(ctx, workspace, reinterpret_cast<cudaStream_t>(stream));
   void *ws = workspace;
-  const int B = batch, R = B * 16, H = g.hidden, d = g.head_dim, nq = g.n_q_heads, nkv = g.n_kv_heads;
+  const int S = ctx->block, J = S - 1;
+  const int B = batch, R = B * S, H = g.hidden, d = g.head_dim, nq = g.n_q_heads, nkv = g.n_kv_heads;
   const int F = g.ffn, V = g.vocab, nh = nq + 2 * nkv, G8 = H / 8;
   float *x = at<float>(ws, L.x);
   void *u = at<void>(ws, L.u), *u2 = at<void>(ws, L.u2), *ysub = at<void>(ws, L.ysub);
@@ -439,8 +456,8 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
   void *u_lo = lo(L.u_lo), *u2_lo = lo(L.u2_lo), *ysub_lo = lo(L.ysub_lo), *hmid_lo = lo(L.hmid_lo);
   float *ysub32 = at<float>(ws, L.ysub32);
 
-  if (int e = embed_rmsnorm(lc, f32, ctx->w.embed, anchor_ids, g.mask_id, V, ctx->layers[0].g_attn, g.eps, B, H, x, u,
-                            u_lo))
+  if (int e = embed_rmsnorm(lc, f32, ctx->w.embed, anchor_ids, g.mask_id, V, ctx->layers[0].g_attn, g.eps, B, S, H, x,
+                            u, u_lo))
     return e;
   const size_t lelems = layer_elems(ctx, kv);
   const size_t te = f32 ? 4 : 2;
@@ -461,7 +478,7 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     op.ldo2 = H;
     if (int e = proj(ctx, lc, ws, L, op)) return e;
     if (int e = coef_gemm(site, lw, f32 ? static_cast<const void *>(ysub32) : ysub, ysub_lo)) return e;
-    return conv_apply(lc, f32, nullptr, nullptr, ysub32, coef, B, H, nullptr, nullptr, x);
+    return conv_apply(lc, f32, nullptr, nullptr, ysub32, coef, B, S, H, nullptr, nullptr, x);
   };
   for (int l = 0; l < g.n_layers; ++l) {
     const dflash_layer_weights &lw = ctx->layers[l];
@@ -469,14 +486,14 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     // ---- attention sublayer
     if (g.use_conv) {
       if (int e = coef_gemm(0, lw, u, u_lo)) return e;
-      if (int e = conv_apply(lc, f32, u, u_lo, nullptr, coef, B, H, u2, u2_lo, nullptr)) return e;
+      if (int e = conv_apply(lc, f32, u, u_lo, nullptr, coef, B, S, H, u2, u2_lo, nullptr)) return e;
       ua = u2;
       ua_lo = u2_lo;
     }
     if (int e = proj(ctx, lc, ws, L, mk(lw.w_qkv, H, ua, ua_lo, H, R, nh * d, H, EPI_F32, at<float>(ws, L.qkv), nh * d,
                                         "qkv")))
       return e;
-    if (int e = qk_norm_rope(lc, f32, at<float>(ws, L.qkv), B, nq, nkv, d, lw.g_q, lw.g_k, g.qk_norm != 0, g.eps,
+    if (int e = qk_norm_rope(lc, f32, at<float>(ws, L.qkv), B, S, nq, nkv, d, lw.g_q, lw.g_k, g.qk_norm != 0, g.eps,
                              g.rope_base, ctx_len, at<void>(ws, L.q), at<void>(ws, L.bk), at<void>(ws, L.bv)))
       return e;
     AttnArgs aa = {};
@@ -493,6 +510,7 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     aa.out = at<void>(ws, L.o);
     aa.out_lo = lo(L.o_lo);
     aa.B = B;
+    aa.S = S;
     aa.nq = nq;
     aa.nkv = nkv;
     aa.d = d;
@@ -504,12 +522,12 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     if (int e = f32 ? attention_f32(lc, aa) : attention_bf16(lc, aa)) return e;
     if (int e = out_proj(1, lw, lw.w_o, nq * d, aa.out, aa.out_lo, "o_proj")) return e;
     // ---- FFN sublayer
-    if (int e = rmsnorm_rows(lc, f32, x, R, H, lw.g_ffn, g.eps, u, u_lo, nullptr, nullptr)) return e;
+    if (int e = rmsnorm_rows(lc, f32, x, R, H, S, lw.g_ffn, g.eps, u, u_lo, nullptr, nullptr)) return e;
     ua = u;
     ua_lo = u_lo;
     if (g.use_conv) {
       if (int e = coef_gemm(2, lw, u, u_lo)) return e;
-      if (int e = conv_apply(lc, f32, u, u_lo, nullptr, coef, B, H, u2, u2_lo, nullptr)) return e;
+      if (int e = conv_apply(lc, f32, u, u_lo, nullptr, coef, B, S, H, u2, u2_lo, nullptr)) return e;
       ua = u2;
       ua_lo = u2_lo;
     }
@@ -520,16 +538,17 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     }
     if (int e = out_proj(3, lw, lw.w_down, F, at<void>(ws, L.hmid), hmid_lo, "down")) return e;
     if (l + 1 < g.n_layers)
-      if (int e = rmsnorm_rows(lc, f32, x, R, H, ctx->layers[l + 1].g_attn, g.eps, u, u_lo, nullptr, nullptr)) return e;
+      if (int e = rmsnorm_rows(lc, f32, x, R, H, S, ctx->layers[l + 1].g_attn, g.eps, u, u_lo, nullptr, nullptr))
+        return e;
   }
-  if (int e = rmsnorm_rows(lc, f32, x, R, H, ctx->w.g_final, g.eps, hfinal, nullptr, at<void>(ws, L.hmask),
+  if (int e = rmsnorm_rows(lc, f32, x, R, H, S, ctx->w.g_final, g.eps, hfinal, nullptr, at<void>(ws, L.hmask),
                            lo(L.hmask_lo)))
     return e;
   if (int e = proj(ctx, lc, ws, L,
-                   mk(ctx->w.lm_head, H, at<void>(ws, L.hmask), lo(L.hmask_lo), H, B * 15, V, H, EPI_F32, lg, V,
+                   mk(ctx->w.lm_head, H, at<void>(ws, L.hmask), lo(L.hmask_lo), H, B * J, V, H, EPI_F32, lg, V,
                       "lm_head")))
     return e;
-  return topk16(lc, lg, B * 15, V, topk_ids, topk_logits, at<uint64_t>(ws, L.topk_part), at<int>(ws, L.topk_ctr),
+  return topk16(lc, lg, B * J, V, topk_ids, topk_logits, at<uint64_t>(ws, L.topk_part), at<int>(ws, L.topk_ctr),
                 TOPK_MAX_CHUNKS);
 }
 
@@ -542,7 +561,8 @@ int dflash_select_path(dflash_ctx *ctx, const int32_t *anchor_ids, const int32_t
   if (!topk_ids || !draft_ids) return set_error(DFLASH_ERR_ARG, "dflash_select_path: null argument");
   const dflash_config &g = ctx->cfg;
   Launch lc = make_launch(ctx, workspace, reinterpret_cast<cudaStream_t>(stream));
-  if (!g.use_selector) return greedy_path(lc, nullptr, topk_ids, batch, false, draft_ids);
+  const int J = ctx->block - 1;
+  if (!g.use_selector) return greedy_path(lc, nullptr, topk_ids, batch, J, false, draft_ids);
   if (!anchor_ids || !topk_logits || !final_hidden)
     return set_error(DFLASH_ERR_ARG, "dflash_select_path: the selector needs anchors, logits and final_hidden");
   float *sc = pair_scores_out;
@@ -550,11 +570,11 @@ int dflash_select_path(dflash_ctx *ctx, const int32_t *anchor_ids, const int32_t
     if (int e = check_ws(ctx, workspace, workspace_bytes, batch, 0)) return e;
     sc = at<float>(workspace, layout(ctx, batch, 0).scores);
   }
-  if (int e = pair_scores(lc, g.dtype == DFLASH_F32, anchor_ids, topk_ids, topk_logits, final_hidden, batch, g.hidden,
-                          ctx->w.sel_e256, ctx->w.sel_a, ctx->w.sel_b, g.sel_rank, g.sel_dim, ctx->w.sel_w_g,
+  if (int e = pair_scores(lc, g.dtype == DFLASH_F32, anchor_ids, topk_ids, topk_logits, final_hidden, batch, J,
+                          g.hidden, ctx->w.sel_e256, ctx->w.sel_a, ctx->w.sel_b, g.sel_rank, g.sel_dim, ctx->w.sel_w_g,
                           ctx->w.sel_b_g, sc))
     return e;
-  return greedy_path(lc, sc, topk_ids, batch, true, draft_ids);
+  return greedy_path(lc, sc, topk_ids, batch, J, true, draft_ids);
 }
 
 int dflash_sample_path(dflash_ctx *ctx, const int32_t *anchor_ids, const int32_t *topk_ids, const float *topk_logits,
@@ -579,12 +599,13 @@ int dflash_sample_path(dflash_ctx *ctx, const int32_t *anchor_ids, const int32_t
       s = at<float>(workspace, layout(ctx, batch, 0).scores);
     }
     if (int e = pair_scores(lc, g.dtype == DFLASH_F32, anchor_ids, topk_ids, topk_logits, final_hidden, batch,
-                            g.hidden, ctx->w.sel_e256, ctx->w.sel_a, ctx->w.sel_b, g.sel_rank, g.sel_dim,
+                            ctx->block - 1, g.hidden, ctx->w.sel_e256, ctx->w.sel_a, ctx->w.sel_b, g.sel_rank, g.sel_dim,
                             ctx->w.sel_w_g, ctx->w.sel_b_g, s))
       return e;
     sc = s;
   }
-  return sample_path(lc, sc, topk_logits, topk_ids, batch, temperature, uniforms, draft_ids, draft_probs);
+  return sample_path(lc, sc, topk_logits, topk_ids, batch, ctx->block - 1, temperature, uniforms, draft_ids,
+                     draft_probs);
 }
 
 int dflash_verify_rejection(dflash_ctx *ctx, const float *target_logits, const int32_t *draft_ids,
@@ -600,18 +621,20 @@ int dflash_verify_rejection(dflash_ctx *ctx, const float *target_logits, const i
   if (int e = check_ws(ctx, workspace, workspace_bytes, batch, 0)) return e;
   Launch lc = make_launch(ctx, workspace, reinterpret_cast<cudaStream_t>(stream));
   return verify_rejection(lc, target_logits, ctx->cfg.vocab, at<float>(workspace, layout(ctx, batch, 0).lse),
-                          draft_ids, topk_ids, draft_probs, u_accept, u_bonus, batch, accept_len, bonus, committed);
+                          draft_ids, topk_ids, draft_probs, u_accept, u_bonus, batch, ctx->block - 1, accept_len,
+                          bonus, committed);
 }
 
-int dflash_verify_greedy(const int32_t *draft_ids, const int32_t *target_ids, int batch, int32_t *accept_len,
-                         int32_t *bonus, int32_t *committed, dflash_stream_t stream) {
+int dflash_verify_greedy(const int32_t *draft_ids, const int32_t *target_ids, int batch, int block_size,
+                         int32_t *accept_len, int32_t *bonus, int32_t *committed, dflash_stream_t stream) {
   if (batch < 0) return set_error(DFLASH_ERR_ARG, "negative batch");
+  if (block_size < 2 || block_size > 16) return set_error(DFLASH_ERR_ARG, "block_size must be 2..16");
   if (batch == 0) return DFLASH_OK;
   if (!draft_ids || !target_ids || !accept_len || !bonus || !committed)
     return set_error(DFLASH_ERR_ARG, "dflash_verify_greedy: null argument");
   Launch lc;
   lc.stream = reinterpret_cast<cudaStream_t>(stream);
-  return verify(lc, draft_ids, target_ids, batch, accept_len, bonus, committed);
+  return verify(lc, draft_ids, target_ids, batch, block_size - 1, accept_len, bonus, committed);
 }
 
 int dflash_read_status(const void *workspace, int *device_status, dflash_stream_t stream) {

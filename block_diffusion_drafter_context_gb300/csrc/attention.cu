@@ -38,7 +38,7 @@ namespace {
 constexpr int CH = 64;                       // tokens per chunk (= one KV page)
 constexpr int HD = 128;                      // head dim of the bf16 path
 constexpr int ST = 5;                        // KV ring depth
-constexpr int BLK = 16;                      // block tokens
+constexpr int BLK = 16;                      // query rows per head in the tile (block size S <= 16 of them real)
 constexpr int MROWS = 128;                   // UMMA M (query rows, padded)
 constexpr int Q_BYTES = MROWS * HD * 2;      // 32 KB: two 64-dim halves of [128][64]
 constexpr int K_BYTES = CH * HD * 2;         // 16 KB: two halves of [64 tok][64]
@@ -62,6 +62,7 @@ struct Params {
   int max_pages, num_pages;
   const int32_t *ctx_len;
   int B, nkv, g;
+  int S;                   // block size: queries per request and block keys (2..16)
   int min_chunks;          // at least this many chunks per CTA
   int cs;                  // >1: cluster mode, cs CTAs (one cluster) per (request, kv head)
   float scale_log2;
@@ -120,7 +121,7 @@ struct Walk {
     }
   }
   __device__ bool block_chunk() const { return k == nch - 1; }
-  __device__ int valid() const { return k < nch - 1 ? min(CH, n - k * CH) : BLK; }
+  __device__ int valid(int S) const { return k < nch - 1 ? min(CH, n - k * CH) : S; }
 };
 
 // 16 consecutive outputs of one row: high bf16 halves and, if lo, low halves
@@ -421,8 +422,8 @@ __global__ void __launch_bounds__(NTHR, 1)
             for (int half = 0; half < 2; ++half) {
               const int col = (w.h * g + hw) * HD + half * 64;
               uint8_t *dst = sQ + half * (MROWS * 128) + (DUP ? 32 : BLK) * hw * 128;
-              tma_load_2d(dst, &tmQ, qfull, col, w.b * BLK);
-              if (DUP) tma_load_2d(dst + BLK * 128, &tmQ, qfull, col, w.b * BLK);
+              tma_load_2d(dst, &tmQ, qfull, col, w.b * p.S);   // rows past S: the next request's, unused
+              if (DUP) tma_load_2d(dst + BLK * 128, &tmQ, qfull, col, w.b * p.S);
             }
           q_issued = seg;
         }
@@ -488,7 +489,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         // only the 16-token k-steps holding valid tokens: V columns past them
         // (block slots 16..63, the unused tail of a last page) are never read,
         // so whatever they hold cannot reach O through 0 * Inf
-        const int ksteps = (wp.valid() + 15) / 16;
+        const int ksteps = (wp.valid(p.S) + 15) / 16;
         ok = mbar_wait(&pfull[pb], static_cast<uint32_t>((i >> 1) & 1), abort_flag, p.timeout_ns) &&
              mbar_wait(&full[st], static_cast<uint32_t>((i / ST) & 1), abort_flag, p.timeout_ns) &&
              (!first || seg_p == 0 ||
@@ -539,7 +540,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         ++seg;
         seg_whole = w.k == 0;
       }
-      const int valid = w.valid();
+      const int valid = w.valid(p.S);
       if (!waitw(&sfull[sb], static_cast<uint32_t>((i / NSB) & 1))) {
         failed = true;
         break;
@@ -693,7 +694,8 @@ __global__ void __launch_bounds__(NTHR, 1)
           continue;
         }
         const int hq = w.h * g + trow / BLK, j = trow % BLK;
-        const size_t orow = static_cast<size_t>(w.b * BLK + j) * p.ldo + static_cast<size_t>(hq) * HD;
+        const bool out_row = j < p.S;   // tile rows past the block size are not queries
+        const size_t orow = static_cast<size_t>(w.b * p.S + j) * p.ldo + static_cast<size_t>(hq) * HD;
         float *part = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + (seg == 0 ? 0 : 1)) * ATTN_PART_FLOATS;
         const float inv = 1.f / l;
 #pragma unroll
@@ -711,7 +713,7 @@ __global__ void __launch_bounds__(NTHR, 1)
             for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(ov[u][t]);
             if (olane) {
               if (whole) {
-                store16_hl(p.out + orow + c * 16, p.out_lo ? p.out_lo + orow + c * 16 : nullptr, v, inv);
+                if (out_row) store16_hl(p.out + orow + c * 16, p.out_lo ? p.out_lo + orow + c * 16 : nullptr, v, inv);
               } else {
                 float4 *d4 = reinterpret_cast<float4 *>(part + static_cast<size_t>(trow) * HD + c * 16);
 #pragma unroll
@@ -753,7 +755,7 @@ __global__ void __launch_bounds__(NTHR, 1)
             break;
           }
           ++nparts;
-          if (sch->merge_flag && real)   // DUP: the two lanes of a row take 64 columns each
+          if (sch->merge_flag && real && out_row)   // DUP: the two lanes of a row take 64 columns each
             merge_row(p, cf, cl, run_lo(cf, sc.total, sc.G) == start, trow, DUP ? hi * 64 : 0, DUP ? 1 : 2,
                       p.out + orow, p.out_lo ? p.out_lo + orow : nullptr);
         }
@@ -810,7 +812,8 @@ __global__ void __launch_bounds__(NTHR, 1)
       }
       const float inv = 1.f / L;
       const int hq = h * g + row / BLK, j = row % BLK;
-      const size_t dst = static_cast<size_t>(b * BLK + j) * p.ldo + static_cast<size_t>(hq) * HD + 4 * c4;
+      if (j >= p.S) continue;   // not a query of this block size
+      const size_t dst = static_cast<size_t>(b * p.S + j) * p.ldo + static_cast<size_t>(hq) * HD + 4 * c4;
       const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
       const __nv_bfloat162 h1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
       *reinterpret_cast<uint2 *>(p.out + dst) =
@@ -831,10 +834,12 @@ template <int DPL>
 __global__ void __launch_bounds__(512) attn_f32_kernel(const float *q, int ldq, const float *kc, const float *vc,
                                                        const float *bk, const float *bv, const int32_t *pt,
                                                        int max_pages, int num_pages, int page, const int32_t *ctx_len,
-                                                       float *out, int ldo, int nkv, int g, float scale, int *status) {
+                                                       float *out, int ldo, int nkv, int g, int S, float scale,
+                                                       int *status) {
   pdl_start();
   constexpr int D = DPL * 32;
   const int hq = blockIdx.x, b = blockIdx.y, j = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (j >= S) return;   // one warp per query of the block
   const int h = hq / g;
   int n = ctx_len[b];
   if (n < 0 || n > max_pages * page) {
@@ -842,14 +847,14 @@ __global__ void __launch_bounds__(512) attn_f32_kernel(const float *q, int ldq, 
     n = n < 0 ? 0 : max_pages * page;
   }
   float qv[DPL], acc[DPL];
-  const float *qr = q + static_cast<size_t>(b * BLK + j) * ldq + hq * D;
+  const float *qr = q + static_cast<size_t>(b * S + j) * ldq + hq * D;
 #pragma unroll
   for (int i = 0; i < DPL; ++i) {
     qv[i] = qr[lane + 32 * i];
     acc[i] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
-  for (int t = 0; t < n + BLK; ++t) {
+  for (int t = 0; t < n + S; ++t) {
     const float *kp, *vp;
     int vstride;
     if (t < n) {
@@ -877,7 +882,7 @@ __global__ void __launch_bounds__(512) attn_f32_kernel(const float *q, int ldq, 
     for (int i = 0; i < DPL; ++i) acc[i] = acc[i] * a + pw * vp[static_cast<size_t>(lane + 32 * i) * vstride];
     m = mn;
   }
-  float *orow = out + static_cast<size_t>(b * BLK + j) * ldo + hq * D;
+  float *orow = out + static_cast<size_t>(b * S + j) * ldo + hq * D;
 #pragma unroll
   for (int i = 0; i < DPL; ++i) orow[lane + 32 * i] = acc[i] / l;
 }
@@ -887,6 +892,7 @@ __global__ void __launch_bounds__(512) attn_f32_kernel(const float *q, int ldq, 
 
 int attention_bf16(const Launch &lc, const AttnArgs &a) {
   if (a.B <= 0) return DFLASH_OK;
+  if (a.S < 2 || a.S > BLK) return set_error(DFLASH_ERR_UNSUPPORTED, "attention: block size must be 2..16");
   if (a.d != HD || a.page_size != CH)
     return set_error(DFLASH_ERR_UNSUPPORTED, "bf16 attention needs head_dim 128 and 64-token pages");
   const int g = a.nq / a.nkv;
@@ -913,7 +919,7 @@ int attention_bf16(const Launch &lc, const AttnArgs &a) {
   const uint64_t kv_pages = static_cast<uint64_t>(a.num_pages) * a.nkv;
   const uint64_t bkv = static_cast<uint64_t>(a.B) * a.nkv;
   if (int e = make_tmap_2d(&tQ, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.nq) * HD,
-                           static_cast<uint64_t>(a.B) * BLK, static_cast<uint64_t>(a.nq) * HD * 2, 64, BLK))
+                           static_cast<uint64_t>(a.B) * a.S, static_cast<uint64_t>(a.nq) * HD * 2, 64, BLK))
     return e;
   if (int e = make_tmap_2d(&tK, a.k_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, HD, kv_pages * CH, HD * 2, 64, CH))
     return e;
@@ -932,6 +938,7 @@ int attention_bf16(const Launch &lc, const AttnArgs &a) {
   p.B = a.B;
   p.nkv = a.nkv;
   p.g = g;
+  p.S = a.S;
   p.min_chunks = a.min_chunks > 0 ? a.min_chunks : DEFAULT_MIN_CHUNKS;
   // few (request, kv head) lists: one cluster of cs CTAs per list, merged on
   // chip (global round trips cost ~2 us here); otherwise the balanced
@@ -968,6 +975,7 @@ int attention_bf16(const Launch &lc, const AttnArgs &a) {
 
 int attention_f32(const Launch &lc, const AttnArgs &a) {
   if (a.B <= 0) return DFLASH_OK;
+  if (a.S < 2 || a.S > BLK) return set_error(DFLASH_ERR_UNSUPPORTED, "attention: block size must be 2..16");
   const int g = a.nq / a.nkv;
   dim3 grid(a.nq, a.B), block(512);
   const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(a.d)));
@@ -976,7 +984,7 @@ int attention_f32(const Launch &lc, const AttnArgs &a) {
   float *o = static_cast<float *>(a.out);
 #define ARGS q, a.nq * a.d, static_cast<const float *>(a.k_cache), static_cast<const float *>(a.v_cache), \
              static_cast<const float *>(a.bk), static_cast<const float *>(a.bv), a.page_table, a.max_pages, \
-             a.num_pages, a.page_size, a.ctx_len, o, a.nq * a.d, a.nkv, g, scale, lc.status
+             a.num_pages, a.page_size, a.ctx_len, o, a.nq * a.d, a.nkv, g, a.S, scale, lc.status
   if (a.d == 64)
     launch_pdl(attn_f32_kernel<2>, grid, block, 0, lc.stream, ARGS);
   else if (a.d == 128)

@@ -86,15 +86,16 @@ __device__ __forceinline__ void rope_cs(int pos, float th_hi, float th_lo, float
 }
 
 // ------------------------------------------------------------------ embed
-// x[b*16+j] = E[id] (fp32 residual stream); u = RMSNorm(x) (activation dtype)
+// x[b*S+j] = E[id] (fp32 residual stream); u = RMSNorm(x) (activation dtype);
+// S = block size: the anchor at j = 0, the mask token at j = 1..S-1
 template <typename T>
 __global__ void __launch_bounds__(ROW_THREADS) embed_rmsnorm_kernel(const T *embed, const int32_t *anchor,
                                                                     int mask_id, int vocab, const float *gain,
-                                                                    float eps, int H, float *x, T *u, T *u_lo,
+                                                                    float eps, int H, int S, float *x, T *u, T *u_lo,
                                                                     int *status) {
   pdl_start();
   __shared__ float red[32];
-  const int row = blockIdx.x, b = row >> 4, j = row & 15;
+  const int row = blockIdx.x, b = row / S, j = row % S;
   int id = j == 0 ? anchor[b] : mask_id;
   if (id < 0 || id >= vocab) {
     if (threadIdx.x == 0) report(status, DFLASH_ERR_DEVICE);
@@ -131,11 +132,12 @@ __global__ void __launch_bounds__(ROW_THREADS) embed_rmsnorm_kernel(const T *emb
 }
 
 // ------------------------------------------------------------------ rmsnorm
-// out[row] = RMSNorm(x[row]) (+ low halves); rows with j >= 1 are also
-// written compactly to out_mask[b*15 + j-1] (LM-head input of the mask rows).
+// out[row] = RMSNorm(x[row]) (+ low halves); rows with j = row % S >= 1 are
+// also written compactly to out_mask[b*(S-1) + j-1] (LM-head input of the
+// mask rows).
 template <typename T>
 __global__ void __launch_bounds__(ROW_THREADS) rmsnorm_kernel(const float *x, int H, const float *gain, float eps,
-                                                              T *out, T *out_lo, T *out_mask, T *out_mask_lo) {
+                                                              int S, T *out, T *out_lo, T *out_mask, T *out_mask_lo) {
   pdl_start();
   __shared__ float red[32];
   const int row = blockIdx.x;
@@ -155,8 +157,8 @@ __global__ void __launch_bounds__(ROW_THREADS) rmsnorm_kernel(const float *x, in
   for (int k = 0; k < MAXV; ++k)
     if (threadIdx.x + k * ROW_THREADS < nv) ss += dot4(v[k]);
   const float r = rsqrtf(block_sum(ss, red) / H + eps);
-  const int b = row >> 4, j = row & 15;
-  const size_t mrow = static_cast<size_t>(b * 15 + j - 1) * H;
+  const int b = row / S, j = row % S;
+  const size_t mrow = static_cast<size_t>(b * (S - 1) + j - 1) * H;
 #pragma unroll
   for (int k = 0; k < MAXV; ++k) {
     const int i = threadIdx.x + k * ROW_THREADS;
@@ -208,18 +210,19 @@ struct RopeArgs {
   float th_hi[64], th_lo[64];
 };
 
-// qkv: fp32 [B*16][(nq+2nkv)*d].  One warp per (token, head).  q heads ->
-// q_out [B*16][nq*d]; k heads -> bk [B][nkv][64][d] (normed, rotated); v
-// heads -> bv [B][nkv][d][64], transposed like the V pages.  Rows / columns
-// 16..63 are padding up to one 64-token page: never written, and attention
-// masks their scores and skips their V columns, so they may hold anything.
+// qkv: fp32 [B*S][(nq+2nkv)*d] (S = block size).  One warp per (token,
+// head).  q heads -> q_out [B*S][nq*d]; k heads -> bk [B][nkv][64][d]
+// (normed, rotated); v heads -> bv [B][nkv][d][64], transposed like the V
+// pages.  Rows / columns S..63 are padding up to one 64-token page:
+// attention masks the scores of rows S.. and skips V columns 16..; V columns
+// S..15 share a k-step with the block tokens and are written as zeros.
 template <typename T, int DPL>
-__global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, int nkv, const float *g_q,
+__global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, int nkv, int S, const float *g_q,
                                                       const float *g_k, int qk_norm, float eps, const RopeArgs rp,
                                                       const int32_t *ctx_len, T *q_out, T *bk, T *bv) {
   pdl_start();
   constexpr int D = DPL * 32;
-  const int tok = blockIdx.x, b = tok >> 4, j = tok & 15;
+  const int tok = blockIdx.x, b = tok / S, j = tok % S;
   const int head = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int nh = nq + 2 * nkv;
   if (head >= nh) return;
@@ -231,6 +234,12 @@ __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, 
     T *dst = bv + (static_cast<size_t>(b) * nkv + (head - nq - nkv)) * D * 64 + j;
 #pragma unroll
     for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + static_cast<size_t>(lane + 32 * i) * 64, v[i]);
+    // the block's PV k-step reads columns 0..15: below a block of 16 the
+    // columns S..15 get zeros (a 0 probability times a stale NaN is NaN)
+    if (j == S - 1)
+      for (int c = S; c < 16; ++c)
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + (c - j) + static_cast<size_t>(lane + 32 * i) * 64, 0.f);
     return;
   }
   const bool is_q = head < nq;
@@ -349,14 +358,14 @@ __global__ void __launch_bounds__(256) inject_scatter_kernel(const ScatterArgs a
 // ------------------------------------------------------------------ short conv
 // DFlash-2 ("DFlash 2", Arquitectura del Sistema item 2): two taps along the
 // block, coefficients per 16-channel group, nothing before position 0.
-//   coef: fp32 [B*16][H/8] = tanh(W_c y + b_c): [0, H/16) current tap a,
-//         [H/16, H/8) previous tap b.
+//   coef: fp32 [B*S][H/8] = tanh(W_c y + b_c): [0, H/16) current tap a,
+//         [H/16, H/8) previous tap b (S = block size <= 16).
 //   out_j = y_j + a_j * y_j + b_j * y_{j-1}
 // y is either an activation (hi [+ lo] halves) or fp32 (y32).  Pre sites
 // write out (+ low halves), post sites add into the residual x_add.
 template <typename T>
 __global__ void __launch_bounds__(256) conv_kernel(const T *y, const T *y_lo, const float *y32, const float *coef,
-                                                   int H, T *out_t, T *out_lo, float *x_add) {
+                                                   int H, int S, T *out_t, T *out_lo, float *x_add) {
   pdl_start();
   const int b = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
@@ -365,14 +374,16 @@ __global__ void __launch_bounds__(256) conv_kernel(const T *y, const T *y_lo, co
   float yv[16], av[16], bv[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const size_t row = static_cast<size_t>(b) * 16 + j;
+    if (j >= S) break;
+    const size_t row = static_cast<size_t>(b) * S + j;
     yv[j] = y32 ? y32[row * H + c] : Elt<T>::ld(y + row * H + c) + (y_lo ? Elt<T>::ld(y_lo + row * H + c) : 0.f);
     av[j] = coef[row * (2 * G) + grp];
     bv[j] = coef[row * (2 * G) + G + grp];
   }
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const size_t row = static_cast<size_t>(b) * 16 + j;
+    if (j >= S) break;
+    const size_t row = static_cast<size_t>(b) * S + j;
     const float v = yv[j] + av[j] * yv[j] + bv[j] * (j ? yv[j - 1] : 0.f);
     if (out_t) {
       Elt<T>::st(out_t + row * H + c, v);
@@ -409,29 +420,30 @@ int check_row(int H) {
 }  // namespace
 
 int embed_rmsnorm(const Launch &lc, bool f32, const void *embed, const int32_t *anchor, int mask_id, int vocab,
-                  const float *gain, float eps, int B, int H, float *x, void *u, void *u_lo) {
+                  const float *gain, float eps, int B, int S, int H, float *x, void *u, void *u_lo) {
   if (int e = check_row(H)) return e;
   return run(lc, "embed_norm", [&] {
     if (f32)
-      launch_pdl(embed_rmsnorm_kernel<float>, dim3(B * 16), dim3(ROW_THREADS), 0, lc.stream,
-          static_cast<const float *>(embed), anchor, mask_id, vocab, gain, eps, H, x, tp<float>(u), nullptr, lc.status);
+      launch_pdl(embed_rmsnorm_kernel<float>, dim3(B * S), dim3(ROW_THREADS), 0, lc.stream,
+          static_cast<const float *>(embed), anchor, mask_id, vocab, gain, eps, H, S, x, tp<float>(u), nullptr,
+          lc.status);
     else
-      launch_pdl(embed_rmsnorm_kernel<__nv_bfloat16>, dim3(B * 16), dim3(ROW_THREADS), 0, lc.stream,
-          static_cast<const __nv_bfloat16 *>(embed), anchor, mask_id, vocab, gain, eps, H, x, tp<__nv_bfloat16>(u),
+      launch_pdl(embed_rmsnorm_kernel<__nv_bfloat16>, dim3(B * S), dim3(ROW_THREADS), 0, lc.stream,
+          static_cast<const __nv_bfloat16 *>(embed), anchor, mask_id, vocab, gain, eps, H, S, x, tp<__nv_bfloat16>(u),
           tp<__nv_bfloat16>(u_lo), lc.status);
   });
 }
 
-int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, const float *gain, float eps,
+int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, int S, const float *gain, float eps,
                  void *out, void *out_lo, void *out_mask_rows, void *out_mask_lo) {
   if (int e = check_row(H)) return e;
   return run(lc, "rmsnorm", [&] {
     if (f32)
-      launch_pdl(rmsnorm_kernel<float>, dim3(rows), dim3(ROW_THREADS), 0, lc.stream, x, H, gain, eps, tp<float>(out), nullptr,
-                                                                 tp<float>(out_mask_rows), nullptr);
+      launch_pdl(rmsnorm_kernel<float>, dim3(rows), dim3(ROW_THREADS), 0, lc.stream, x, H, gain, eps, S,
+                 tp<float>(out), nullptr, tp<float>(out_mask_rows), nullptr);
     else
       launch_pdl(rmsnorm_kernel<__nv_bfloat16>, dim3(rows), dim3(ROW_THREADS), 0, lc.stream,
-          x, H, gain, eps, tp<__nv_bfloat16>(out), tp<__nv_bfloat16>(out_lo), tp<__nv_bfloat16>(out_mask_rows),
+          x, H, gain, eps, S, tp<__nv_bfloat16>(out), tp<__nv_bfloat16>(out_lo), tp<__nv_bfloat16>(out_mask_rows),
           tp<__nv_bfloat16>(out_mask_lo));
   });
 }
@@ -451,14 +463,14 @@ int feature_norm(const Launch &lc, bool f32, const float *in, int rows, int H, c
   });
 }
 
-int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int nq, int nkv, int d, const float *g_q,
-                 const float *g_k, bool qk_norm, float eps, float rope_base, const int32_t *ctx_len, void *q_out,
-                 void *bk, void *bv) {
-  dim3 grid(B * 16, (nq + 2 * nkv + 7) / 8);
+int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int S, int nq, int nkv, int d,
+                 const float *g_q, const float *g_k, bool qk_norm, float eps, float rope_base, const int32_t *ctx_len,
+                 void *q_out, void *bk, void *bv) {
+  dim3 grid(B * S, (nq + 2 * nkv + 7) / 8);
   const RopeArgs rp = rope_table(d, rope_base);
   return run(lc, "qk_norm_rope", [&] {
 #define QK(T, DPL)                                                                                         \
-  launch_pdl(qk_rope_kernel<T, DPL>, dim3(grid), dim3(256), 0, lc.stream, qkv, nq, nkv, g_q, g_k, qk_norm, eps, rp, ctx_len, \
+  launch_pdl(qk_rope_kernel<T, DPL>, dim3(grid), dim3(256), 0, lc.stream, qkv, nq, nkv, S, g_q, g_k, qk_norm, eps, rp, ctx_len, \
                                                       tp<T>(q_out), tp<T>(bk), tp<T>(bv))
     if (f32 && d == 64)
       QK(float, 2);
@@ -512,15 +524,15 @@ int inject_scatter(const Launch &lc, bool f32, const float *kvproj, int T, int L
 }
 
 int conv_apply(const Launch &lc, bool f32, const void *y, const void *y_lo, const float *y32, const float *coef, int B,
-               int H, void *out_t, void *out_lo, float *x_add) {
+               int S, int H, void *out_t, void *out_lo, float *x_add) {
   dim3 grid((H + 255) / 256, B);
   return run(lc, "short_conv", [&] {
     if (f32)
       launch_pdl(conv_kernel<float>, dim3(grid), dim3(256), 0, lc.stream, static_cast<const float *>(y), nullptr, y32, coef, H,
-                                                      tp<float>(out_t), nullptr, x_add);
+                 S, tp<float>(out_t), nullptr, x_add);
     else
       launch_pdl(conv_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, lc.stream,
-          static_cast<const __nv_bfloat16 *>(y), static_cast<const __nv_bfloat16 *>(y_lo), y32, coef, H,
+          static_cast<const __nv_bfloat16 *>(y), static_cast<const __nv_bfloat16 *>(y_lo), y32, coef, H, S,
           tp<__nv_bfloat16>(out_t), tp<__nv_bfloat16>(out_lo), x_add);
   });
 }

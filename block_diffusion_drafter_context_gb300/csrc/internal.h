@@ -113,6 +113,7 @@ struct AttnArgs {
   void *out;                // [B*16][nq*d] (dtype)
   void *out_lo;             // low bf16 halves of out, or null
   int B, nq, nkv, d;
+  int S;                    // block size (queries per request, block keys), 2..16
   int min_chunks;           // bf16: at least this many 64-token chunks per CTA (0 = default)
   int *counters;            // bf16: [counter_cap] ints, zero between launches (self-resetting)
   size_t counter_cap;       // >= B * nkv
@@ -127,13 +128,14 @@ int attention_f32(const Launch &lc, const AttnArgs &a);
 // ---------------------------------------------------------------- elementwise
 // *_lo outputs: low bf16 halves (value - high half) for split activations;
 // null to skip (always null on the fp32 path).
+// S = block size (anchor + S-1 mask positions), 2..16
 int embed_rmsnorm(const Launch &lc, bool f32, const void *embed, const int32_t *anchor, int mask_id, int vocab,
-                  const float *gain, float eps, int B, int H, float *x, void *u, void *u_lo);
-int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, const float *gain, float eps,
+                  const float *gain, float eps, int B, int S, int H, float *x, void *u, void *u_lo);
+int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, int S, const float *gain, float eps,
                  void *out, void *out_lo, void *out_mask_rows, void *out_mask_lo);
 int feature_norm(const Launch &lc, bool f32, const float *in, int rows, int H, const float *gain, float eps,
                  bool apply_norm, void *out, void *out_lo, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B);
-int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int nq, int nkv, int d,
+int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int S, int nq, int nkv, int d,
                  const float *g_q, const float *g_k, bool qk_norm, float eps, float rope_base,
                  const int32_t *ctx_len, void *q_out, void *bk, void *bv);
 int inject_scatter(const Launch &lc, bool f32, const float *kvproj, int T, int L, int nkv, int d,
@@ -143,24 +145,25 @@ int inject_scatter(const Launch &lc, bool f32, const float *kvproj, int T, int L
 // y: activation (hi [+ y_lo]) or y32 (fp32); pre sites write out_t (+ out_lo),
 // post sites add into x_add.
 int conv_apply(const Launch &lc, bool f32, const void *y, const void *y_lo, const float *y32, const float *coef,
-               int B, int H, void *out_t, void *out_lo, float *x_add);
+               int B, int S, int H, void *out_t, void *out_lo, float *x_add);
 
 // ---------------------------------------------------------------- top-k / select / verify
+// J = block size - 1 mask positions per request; S = J + 1 target rows.
 int sample_path(const Launch &lc, const float *scores, const float *topk_logits, const int32_t *topk_ids, int B,
-                float temperature, const float *uniforms, int32_t *draft, float *qprob);
-int verify_rejection_scratch_floats(int B);
+                int J, float temperature, const float *uniforms, int32_t *draft, float *qprob);
+int verify_rejection_scratch_floats(int B, int S);
 int verify_rejection(const Launch &lc, const float *target_logits, int V, float *scratch, const int32_t *draft,
                      const int32_t *topk_ids, const float *qprob, const float *u_accept, const float *u_bonus, int B,
-                     int32_t *accept, int32_t *bonus, int32_t *committed);
+                     int J, int32_t *accept, int32_t *bonus, int32_t *committed);
 int topk16(const Launch &lc, const float *logits, int rows, int V, int32_t *ids, float *vals,
            uint64_t *part_keys, int *counters, int max_chunks);
 int pair_scores(const Launch &lc, bool f32, const int32_t *anchor, const int32_t *topk_ids,
-                const float *topk_logits, const void *final_hidden, int B, int H, const void *e256,
+                const float *topk_logits, const void *final_hidden, int B, int J, int H, const void *e256,
                 const void *sel_a, const void *sel_b, int r, int E, const float *w_g, float b_g, float *scores);
-int greedy_path(const Launch &lc, const float *scores, const int32_t *topk_ids, int B, bool use_scores,
+int greedy_path(const Launch &lc, const float *scores, const int32_t *topk_ids, int B, int J, bool use_scores,
                 int32_t *draft);
-int verify(const Launch &lc, const int32_t *draft, const int32_t *target, int B, int32_t *accept, int32_t *bonus,
-           int32_t *committed);
+int verify(const Launch &lc, const int32_t *draft, const int32_t *target, int B, int J, int32_t *accept,
+           int32_t *bonus, int32_t *committed);
 int wait_flag(const Launch &lc, const int32_t *flag);
 
 }  // namespace dflash

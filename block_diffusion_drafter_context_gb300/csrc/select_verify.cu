@@ -20,8 +20,8 @@
 namespace dflash {
 namespace {
 
-constexpr int K = 16;
-constexpr int J = 15;
+constexpr int K = 16;   // candidates per position
+// J = block size - 1 mask positions per request (1..15) is a runtime argument.
 
 // grid (15 positions, B); 256 threads.  The 32 tokens' embeddings and the
 // two rank-r projections are staged in chunks of ECH embedding columns
@@ -33,7 +33,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) pair_scores_kernel(const int32_t *anchor, const int32_t *topk_ids,
                                                           const float *topk_logits, const T *hfinal, int H,
                                                           const T *e256, const T *A, const T *Bm, int r, int E,
-                                                          const float *w_g, float b_g, float *scores) {
+                                                          const float *w_g, float b_g, int J, float *scores) {
   pdl_start();
   extern __shared__ float sh[];
   const int rp = r + 1;
@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(256) pair_scores_kernel(const int32_t *anchor,
     tok[tid] = t;
   }
   // context gate on the final-normed hidden state of mask position j+1
-  const T *h = hfinal + (static_cast<size_t>(b) * 16 + j + 1) * H;
+  const T *h = hfinal + (static_cast<size_t>(b) * (J + 1) + j + 1) * H;
   float dot = 0.f;
   for (int c = tid; c < H; c += blockDim.x) dot += Elt<T>::ld(h + c) * w_g[c];
   dot = warp_sum(dot);
@@ -113,7 +113,8 @@ __global__ void __launch_bounds__(256) pair_scores_kernel(const int32_t *anchor,
 }
 
 // one warp per request; lanes 0..15 are the candidates of the current position
-__global__ void greedy_kernel(const float *scores, const int32_t *topk_ids, int B, int use_scores, int32_t *draft) {
+__global__ void greedy_kernel(const float *scores, const int32_t *topk_ids, int B, int J, int use_scores,
+                              int32_t *draft) {
   pdl_start();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (b >= B) return;
@@ -142,16 +143,17 @@ __global__ void greedy_kernel(const float *scores, const int32_t *topk_ids, int 
   }
 }
 
-__global__ void verify_kernel(const int32_t *draft, const int32_t *target, int B, int32_t *accept, int32_t *bonus,
+__global__ void verify_kernel(const int32_t *draft, const int32_t *target, int B, int J, int32_t *accept, int32_t *bonus,
                               int32_t *committed) {
   pdl_start();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   int k = 0;
-  while (k < J && draft[b * J + k] == target[b * 16 + k]) ++k;
+  const int S = J + 1;
+  while (k < J && draft[b * J + k] == target[b * S + k]) ++k;
   accept[b] = k;
-  bonus[b] = target[b * 16 + k];
-  for (int i = 0; i < 16; ++i) committed[b * 16 + i] = i <= k ? target[b * 16 + i] : -1;
+  bonus[b] = target[b * S + k];
+  for (int i = 0; i < S; ++i) committed[b * S + i] = i <= k ? target[b * S + i] : -1;
 }
 
 // ---------------------------------------------------------------------------
@@ -163,7 +165,7 @@ __global__ void verify_kernel(const int32_t *draft, const int32_t *target, int B
 // Path sampling: one warp per request, lanes 0..15 the candidates; q_j =
 // softmax(s_j(prev, .) / T) and the first candidate (in candidate order)
 // whose running probability exceeds u_j * total.
-__global__ void sample_kernel(const float *scores, const float *topk_logits, const int32_t *topk_ids, int B,
+__global__ void sample_kernel(const float *scores, const float *topk_logits, const int32_t *topk_ids, int B, int J,
                               float inv_t, const float *uniforms, int32_t *draft, float *qprob) {
   pdl_start();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -244,10 +246,10 @@ __device__ __forceinline__ int chunk_len(int V, int nch, bool vec) {
 }
 
 // (max, sum exp(x - max)) of one chunk of one target row: grid (LSE_CH,
-// 16 positions, B), 256 threads; a max pass, then a branch-free sum pass.
+// S positions, B), 256 threads; a max pass, then a branch-free sum pass.
 __global__ void __launch_bounds__(256) row_lse_kernel(const float *logits, int V, float2 *part) {
   pdl_start();
-  const float *row = logits + (static_cast<size_t>(blockIdx.z) * 16 + blockIdx.y) * V;
+  const float *row = logits + (static_cast<size_t>(blockIdx.z) * gridDim.y + blockIdx.y) * V;
   const bool vec = (V & 3) == 0;
   const int per = chunk_len(V, LSE_CH, vec);
   const int x0 = min(V, blockIdx.x * per), x1 = min(V, x0 + per);
@@ -273,25 +275,25 @@ __global__ void __launch_bounds__(256) row_lse_kernel(const float *logits, int V
   if (threadIdx.x == 0) {
     float S = 0.f;
     for (int w = 0; w < 8; ++w) S += ss[w];
-    part[(static_cast<size_t>(blockIdx.z) * 16 + blockIdx.y) * LSE_CH + blockIdx.x] = make_float2(M, S);
+    part[(static_cast<size_t>(blockIdx.z) * gridDim.y + blockIdx.y) * LSE_CH + blockIdx.x] = make_float2(M, S);
   }
 }
 
-__device__ __forceinline__ float row_lse(const float2 *part, int b, int i) {
-  const float2 *p = part + (static_cast<size_t>(b) * 16 + i) * LSE_CH;
+__device__ __forceinline__ float row_lse(const float2 *part, int S, int b, int i) {
+  const float2 *p = part + (static_cast<size_t>(b) * S + i) * LSE_CH;
   float M = -INFINITY;
 #pragma unroll
   for (int c = 0; c < LSE_CH; ++c) M = fmaxf(M, p[c].x);
-  float S = 0.f;
+  float sum = 0.f;
 #pragma unroll
-  for (int c = 0; c < LSE_CH; ++c) S += p[c].y == 0.f ? 0.f : p[c].y * exp2f((p[c].x - M) * LOG2E);
-  return M + logf(S);
+  for (int c = 0; c < LSE_CH; ++c) sum += p[c].y == 0.f ? 0.f : p[c].y * exp2f((p[c].x - M) * LOG2E);
+  return M + logf(sum);
 }
 
 // The accept decisions of request b (lanes 0..14 of one warp): k = first rejection.
-__device__ __forceinline__ int first_reject(const float *logits, int V, const float2 *part, const int32_t *draft,
-                                            const int32_t *topk_ids, const float *qprob, const float *u_accept,
-                                            int b, int lane) {
+__device__ __forceinline__ int first_reject(const float *logits, int V, int J, const float2 *part,
+                                            const int32_t *draft, const int32_t *topk_ids, const float *qprob,
+                                            const float *u_accept, int b, int lane) {
   bool ok = true;
   if (lane < J) {
     const size_t row = static_cast<size_t>(b) * J + lane;
@@ -302,7 +304,7 @@ __device__ __forceinline__ int first_reject(const float *logits, int V, const fl
         c = i;
         break;
       }
-    const float p = expf(logits[(static_cast<size_t>(b) * 16 + lane) * V + d] - row_lse(part, b, lane));
+    const float p = expf(logits[(static_cast<size_t>(b) * (J + 1) + lane) * V + d] - row_lse(part, J + 1, b, lane));
     ok = u_accept[row] * qprob[row * K + c] < p;
   }
   const unsigned fail = __ballot_sync(0xffffffffu, lane < J && !ok);
@@ -326,10 +328,10 @@ struct Resid {
   }
 };
 
-__device__ __forceinline__ void make_resid(Resid &r, const float *logits, int V, const float2 *part,
+__device__ __forceinline__ void make_resid(Resid &r, const float *logits, int V, int J, const float2 *part,
                                            const int32_t *topk_ids, const float *qprob, int b, int k) {
-  r.z = logits + (static_cast<size_t>(b) * 16 + k) * V;
-  r.lse = row_lse(part, b, k);
+  r.z = logits + (static_cast<size_t>(b) * (J + 1) + k) * V;
+  r.lse = row_lse(part, J + 1, b, k);
   r.resid = k < J;
 #pragma unroll
   for (int c = 0; c < K; ++c) {
@@ -339,19 +341,19 @@ __device__ __forceinline__ void make_resid(Resid &r, const float *logits, int V,
 }
 
 // Sums of r over RES_CH chunks of the decisive row: grid (RES_CH, B), 256 threads.
-__global__ void __launch_bounds__(256) resid_sum_kernel(const float *logits, int V, const float2 *part,
+__global__ void __launch_bounds__(256) resid_sum_kernel(const float *logits, int V, int J, const float2 *part,
                                                         const int32_t *draft, const int32_t *topk_ids,
                                                         const float *qprob, const float *u_accept, float *csum) {
   pdl_start();
   const int b = blockIdx.y;
   __shared__ int k_sh;
   if (threadIdx.x < 32) {
-    const int k = first_reject(logits, V, part, draft, topk_ids, qprob, u_accept, b, threadIdx.x);
+    const int k = first_reject(logits, V, J, part, draft, topk_ids, qprob, u_accept, b, threadIdx.x);
     if (threadIdx.x == 0) k_sh = k;
   }
   __syncthreads();
   Resid r;
-  make_resid(r, logits, V, part, topk_ids, qprob, b, k_sh);
+  make_resid(r, logits, V, J, part, topk_ids, qprob, b, k_sh);
   const bool vec = (V & 3) == 0;
   const int per = chunk_len(V, RES_CH, vec);
   const int x0 = min(V, blockIdx.x * per), x1 = min(V, x0 + per);
@@ -374,7 +376,7 @@ __global__ void __launch_bounds__(256) resid_sum_kernel(const float *logits, int
 // One CTA (256 threads) per request: the accept decisions, the chunk holding
 // u * Z (chunk sums in vocabulary order), then that chunk's inverse CDF:
 // per-thread contiguous ranges, a block scan, the owner walks its range.
-__global__ void __launch_bounds__(256) reject_kernel(const float *logits, int V, const float2 *part,
+__global__ void __launch_bounds__(256) reject_kernel(const float *logits, int V, int J, const float2 *part,
                                                      const float *csum, const int32_t *draft,
                                                      const int32_t *topk_ids, const float *qprob,
                                                      const float *u_accept, const float *u_bonus, int32_t *accept,
@@ -385,7 +387,7 @@ __global__ void __launch_bounds__(256) reject_kernel(const float *logits, int V,
   __shared__ float base_sh, total_sh;
   __shared__ float wsum[8];
   if (warp == 0) {
-    const int k = first_reject(logits, V, part, draft, topk_ids, qprob, u_accept, b, lane);
+    const int k = first_reject(logits, V, J, part, draft, topk_ids, qprob, u_accept, b, lane);
     // chunk sums: running total in chunk order (lanes = chunks)
     const float c = lane < RES_CH ? csum[b * RES_CH + lane] : 0.f;
     float inc = c;
@@ -410,7 +412,7 @@ __global__ void __launch_bounds__(256) reject_kernel(const float *logits, int V,
   __syncthreads();
   const int k = k_sh, ch = chunk_sh;
   Resid r;
-  make_resid(r, logits, V, part, topk_ids, qprob, b, k);
+  make_resid(r, logits, V, J, part, topk_ids, qprob, b, k);
   if (ch >= 0) {
     const int per_c = chunk_len(V, RES_CH, (V & 3) == 0);
     const int c0 = min(V, ch * per_c), c1 = min(V, c0 + per_c);
@@ -458,11 +460,11 @@ __global__ void __launch_bounds__(256) reject_kernel(const float *logits, int V,
     accept[b] = k;
     bonus[b] = pick_sh;
   }
-  if (tid < 16) {
+  if (tid <= J) {
     int v = -1;
     if (tid < k) v = draft[static_cast<size_t>(b) * J + tid];
     else if (tid == k) v = pick_sh;
-    committed[b * 16 + tid] = v;
+    committed[b * (J + 1) + tid] = v;
   }
 }
 
@@ -481,8 +483,8 @@ __global__ void wait_flag_kernel(const int32_t *flag, int *status, unsigned long
 }  // namespace
 
 int pair_scores(const Launch &lc, bool f32, const int32_t *anchor, const int32_t *topk_ids, const float *topk_logits,
-                const void *final_hidden, int B, int H, const void *e256, const void *sel_a, const void *sel_b, int r,
-                int E, const float *w_g, float b_g, float *scores) {
+                const void *final_hidden, int B, int J, int H, const void *e256, const void *sel_a, const void *sel_b,
+                int r, int E, const float *w_g, float b_g, float *scores) {
   if (B <= 0) return DFLASH_OK;
   if (r < 1 || r > 64 || E < 1 || E > 1024)
     return set_error(DFLASH_ERR_UNSUPPORTED, "selector rank must be 1..64 and embedding width 1..1024");
@@ -494,7 +496,7 @@ int pair_scores(const Launch &lc, bool f32, const int32_t *anchor, const int32_t
       cudaFuncSetAttribute(pair_scores_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     launch_pdl(pair_scores_kernel<float>, dim3(grid), dim3(256), smem, lc.stream,
         anchor, topk_ids, topk_logits, static_cast<const float *>(final_hidden), H, static_cast<const float *>(e256),
-        static_cast<const float *>(sel_a), static_cast<const float *>(sel_b), r, E, w_g, b_g, scores);
+        static_cast<const float *>(sel_a), static_cast<const float *>(sel_b), r, E, w_g, b_g, J, scores);
   } else {
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(pair_scores_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -502,55 +504,58 @@ int pair_scores(const Launch &lc, bool f32, const int32_t *anchor, const int32_t
     launch_pdl(pair_scores_kernel<__nv_bfloat16>, dim3(grid), dim3(256), smem, lc.stream,
         anchor, topk_ids, topk_logits, static_cast<const __nv_bfloat16 *>(final_hidden), H,
         static_cast<const __nv_bfloat16 *>(e256), static_cast<const __nv_bfloat16 *>(sel_a),
-        static_cast<const __nv_bfloat16 *>(sel_b), r, E, w_g, b_g, scores);
+        static_cast<const __nv_bfloat16 *>(sel_b), r, E, w_g, b_g, J, scores);
   }
   return cuda_check(cudaGetLastError(), "pair_scores launch");
 }
 
 int sample_path(const Launch &lc, const float *scores, const float *topk_logits, const int32_t *topk_ids, int B,
-                float temperature, const float *uniforms, int32_t *draft, float *qprob) {
+                int J, float temperature, const float *uniforms, int32_t *draft, float *qprob) {
   if (B <= 0) return DFLASH_OK;
   ProfScope ps(lc, "sample_path", -1.0, -1.0);
   launch_pdl(sample_kernel, dim3((B + 3) / 4), dim3(128), 0, lc.stream, scores, topk_logits, topk_ids, B,
-             1.f / temperature, uniforms, draft, qprob);
+             J, 1.f / temperature, uniforms, draft, qprob);
   return cuda_check(cudaGetLastError(), "sample_path launch");
 }
 
 int verify_rejection(const Launch &lc, const float *target_logits, int V, float *scratch, const int32_t *draft,
                      const int32_t *topk_ids, const float *qprob, const float *u_accept, const float *u_bonus, int B,
-                     int32_t *accept, int32_t *bonus, int32_t *committed) {
+                     int J, int32_t *accept, int32_t *bonus, int32_t *committed) {
   if (B <= 0) return DFLASH_OK;
-  float2 *part = reinterpret_cast<float2 *>(scratch);                  // [B][16][LSE_CH]
-  float *csum = scratch + static_cast<size_t>(B) * 16 * LSE_CH * 2;    // [B][RES_CH]
+  const int S = J + 1;
+  float2 *part = reinterpret_cast<float2 *>(scratch);                  // [B][S][LSE_CH]
+  float *csum = scratch + static_cast<size_t>(B) * S * LSE_CH * 2;     // [B][RES_CH]
   {
-    ProfScope ps(lc, "target_lse", 4.0 * B * 16 * V, -1.0);
-    launch_pdl(row_lse_kernel, dim3(LSE_CH, 16, B), dim3(256), 0, lc.stream, target_logits, V, part);
+    ProfScope ps(lc, "target_lse", 4.0 * B * S * V, -1.0);
+    launch_pdl(row_lse_kernel, dim3(LSE_CH, S, B), dim3(256), 0, lc.stream, target_logits, V, part);
     if (int e = cuda_check(cudaGetLastError(), "target lse launch")) return e;
   }
   ProfScope ps(lc, "verify_rejection", 4.0 * B * V, -1.0);
-  launch_pdl(resid_sum_kernel, dim3(RES_CH, B), dim3(256), 0, lc.stream, target_logits, V,
+  launch_pdl(resid_sum_kernel, dim3(RES_CH, B), dim3(256), 0, lc.stream, target_logits, V, J,
              static_cast<const float2 *>(part), draft, topk_ids, qprob, u_accept, csum);
   if (int e = cuda_check(cudaGetLastError(), "residual sums launch")) return e;
-  launch_pdl(reject_kernel, dim3(B), dim3(256), 0, lc.stream, target_logits, V, static_cast<const float2 *>(part),
+  launch_pdl(reject_kernel, dim3(B), dim3(256), 0, lc.stream, target_logits, V, J, static_cast<const float2 *>(part),
              static_cast<const float *>(csum), draft, topk_ids, qprob, u_accept, u_bonus, accept, bonus, committed);
   return cuda_check(cudaGetLastError(), "verify_rejection launch");
 }
 
-int verify_rejection_scratch_floats(int B) { return B * (16 * LSE_CH * 2 + RES_CH); }
+int verify_rejection_scratch_floats(int B, int S) { return B * (S * LSE_CH * 2 + RES_CH); }
 
-int greedy_path(const Launch &lc, const float *scores, const int32_t *topk_ids, int B, bool use_scores,
+int greedy_path(const Launch &lc, const float *scores, const int32_t *topk_ids, int B, int J, bool use_scores,
                 int32_t *draft) {
   if (B <= 0) return DFLASH_OK;
   ProfScope ps(lc, "greedy_path", -1.0, -1.0);
-  launch_pdl(greedy_kernel, dim3((B + 3) / 4), dim3(128), 0, lc.stream, scores, topk_ids, B, use_scores ? 1 : 0, draft);
+  launch_pdl(greedy_kernel, dim3((B + 3) / 4), dim3(128), 0, lc.stream, scores, topk_ids, B, J, use_scores ? 1 : 0,
+             draft);
   return cuda_check(cudaGetLastError(), "greedy launch");
 }
 
-int verify(const Launch &lc, const int32_t *draft, const int32_t *target, int B, int32_t *accept, int32_t *bonus,
-           int32_t *committed) {
+int verify(const Launch &lc, const int32_t *draft, const int32_t *target, int B, int J, int32_t *accept,
+           int32_t *bonus, int32_t *committed) {
   if (B <= 0) return DFLASH_OK;
   ProfScope ps(lc, "verify", -1.0, -1.0);
-  launch_pdl(verify_kernel, dim3((B + 127) / 128), dim3(128), 0, lc.stream, draft, target, B, accept, bonus, committed);
+  launch_pdl(verify_kernel, dim3((B + 127) / 128), dim3(128), 0, lc.stream, draft, target, B, J, accept, bonus,
+             committed);
   return cuda_check(cudaGetLastError(), "verify launch");
 }
 

@@ -155,6 +155,12 @@ class Drafter:
         self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
         self.max_batch, self.max_new_tokens = max_batch, max_new_tokens
         self.device = device
+        self.block = int(cfg.block)     # runtime block size S
+
+    def set_block_size(self, block_size: int):
+        """Run the next steps at block size S (2..the configured block size)."""
+        B.dflash_set_block_size(self.ctx, int(block_size))
+        self.block = int(block_size)
 
     def close(self):
         if getattr(self, "ctx", None):
@@ -189,11 +195,12 @@ class Drafter:
         torch = _torch()
         b = int(anchor_ids.shape[0])
         dev = self.device
+        S = self.block
         out = {
-            "topk_ids": torch.empty((b, 15, 16), dtype=torch.int32, device=dev),
-            "topk_logits": torch.empty((b, 15, 16), dtype=torch.float32, device=dev),
-            "final_hidden": torch.empty((b, 16, self.cfg.hidden), dtype=self.act_dtype, device=dev),
-            "logits": torch.empty((b, 15, self.cfg.vocab), dtype=torch.float32, device=dev) if want_logits else None,
+            "topk_ids": torch.empty((b, S - 1, 16), dtype=torch.int32, device=dev),
+            "topk_logits": torch.empty((b, S - 1, 16), dtype=torch.float32, device=dev),
+            "final_hidden": torch.empty((b, S, self.cfg.hidden), dtype=self.act_dtype, device=dev),
+            "logits": torch.empty((b, S - 1, self.cfg.vocab), dtype=torch.float32, device=dev) if want_logits else None,
         }
         B.dflash_draft_block(self.ctx, kv.struct, ctx_len, anchor_ids, b, out["topk_ids"], out["topk_logits"],
                              out["final_hidden"], out["logits"], self.workspace, self.ws_bytes, stream)
@@ -202,19 +209,21 @@ class Drafter:
     def select_path(self, anchor_ids, topk_ids, topk_logits, final_hidden, want_scores=True, stream=None):
         torch = _torch()
         b = int(topk_ids.shape[0])
-        draft = torch.empty((b, 15), dtype=torch.int32, device=self.device)
-        scores = (torch.empty((b, 15, 16, 16), dtype=torch.float32, device=self.device)
+        J = self.block - 1
+        draft = torch.empty((b, J), dtype=torch.int32, device=self.device)
+        scores = (torch.empty((b, J, 16, 16), dtype=torch.float32, device=self.device)
                   if (want_scores and self.cfg.use_selector) else None)
         B.dflash_select_path(self.ctx, anchor_ids, topk_ids, topk_logits, final_hidden, b, draft, scores,
                              self.workspace, self.ws_bytes, stream)
         return draft, scores
 
     def sample_path(self, anchor_ids, topk_ids, topk_logits, final_hidden, temperature, uniforms, stream=None):
-        """Draft drawn over the path scores at a temperature: (draft [b,15], q [b,15,16])."""
+        """Draft drawn over the path scores at a temperature: (draft [b,J], q [b,J,16])."""
         torch = _torch()
         b = int(topk_ids.shape[0])
-        draft = torch.empty((b, 15), dtype=torch.int32, device=self.device)
-        probs = torch.empty((b, 15, 16), dtype=torch.float32, device=self.device)
+        J = self.block - 1
+        draft = torch.empty((b, J), dtype=torch.int32, device=self.device)
+        probs = torch.empty((b, J, 16), dtype=torch.float32, device=self.device)
         B.dflash_sample_path(self.ctx, anchor_ids, topk_ids, topk_logits, final_hidden, b, temperature, uniforms,
                              draft, probs, None, self.workspace, self.ws_bytes, stream)
         return draft, probs
@@ -226,18 +235,19 @@ class Drafter:
         dev = draft_ids.device
         acc = torch.empty(b, dtype=torch.int32, device=dev)
         bonus = torch.empty(b, dtype=torch.int32, device=dev)
-        com = torch.empty((b, 16), dtype=torch.int32, device=dev)
+        com = torch.empty((b, self.block), dtype=torch.int32, device=dev)
         B.dflash_verify_rejection(self.ctx, target_logits, draft_ids, topk_ids, draft_probs, u_accept, u_bonus, b,
                                   acc, bonus, com, self.workspace, self.ws_bytes, stream)
         return acc, bonus, com
 
     @staticmethod
     def verify_greedy(draft_ids, target_ids, stream=None):
+        """Greedy prefix acceptance; the block size is target_ids' second extent."""
         torch = _torch()
-        b = int(draft_ids.shape[0])
+        b, S = int(target_ids.shape[0]), int(target_ids.shape[1])
         dev = draft_ids.device
         acc = torch.empty(b, dtype=torch.int32, device=dev)
         bonus = torch.empty(b, dtype=torch.int32, device=dev)
-        com = torch.empty((b, 16), dtype=torch.int32, device=dev)
-        B.dflash_verify_greedy(draft_ids, target_ids, b, acc, bonus, com, stream)
+        com = torch.empty((b, S), dtype=torch.int32, device=dev)
+        B.dflash_verify_greedy(draft_ids, target_ids, b, S, acc, bonus, com, stream)
         return acc, bonus, com

@@ -3,7 +3,7 @@
  * library.  One call per step of the drafting hot path:
  *
  *   dflash_inject_context   target features -> every drafter layer's KV cache
- *   dflash_draft_block      one parallel forward over a 16-token block
+ *   dflash_draft_block      one parallel forward over an S-token block
  *   dflash_select_path      top-16 candidates -> one draft (DFlash-2 Path
  *                           Selector, or top-1 per position)
  *   dflash_verify_greedy    greedy prefix acceptance against target tokens
@@ -61,7 +61,7 @@ enum {
   DFLASH_ERR_ARG = -1,          /* null pointer or out-of-range scalar       */
   DFLASH_ERR_SHAPE = -2,        /* sizes inconsistent with the config        */
   DFLASH_ERR_ALIGN = -3,        /* pointer / stride not 16-byte aligned      */
-  DFLASH_ERR_UNSUPPORTED = -4,  /* e.g. head_dim not 64/128, block != 16     */
+  DFLASH_ERR_UNSUPPORTED = -4,  /* e.g. head_dim not 64/128, block > 16      */
   DFLASH_ERR_CUDA = -5,         /* a CUDA runtime / driver call failed       */
   DFLASH_ERR_TIMEOUT = -6,      /* a bounded device wait ran out             */
   DFLASH_ERR_DEVICE = -7        /* a kernel reported bad data (page index)   */
@@ -73,7 +73,9 @@ enum { DFLASH_BF16 = 0, DFLASH_F32 = 1 };
  * larger batch returns DFLASH_ERR_ARG. */
 #define DFLASH_MAX_BATCH 4096
 
-/* Drafter shape and flags.  block_size and top_k must be 16, page_size 64. */
+/* Drafter shape and flags.  block_size S in 2..16 (J = S - 1 mask positions
+ * per request; 16 is the pages' block), top_k 16, page_size 64.  Below, S and
+ * J in a shape stand for these two numbers. */
 typedef struct dflash_config {
   int dtype;             /* DFLASH_BF16 or DFLASH_F32                        */
   int hidden;            /* H, multiple of 16                                */
@@ -85,7 +87,7 @@ typedef struct dflash_config {
   int vocab;             /* V                                                */
   int target_hidden;     /* H_t                                              */
   int n_target_layers;   /* n_sel; feature input width = n_sel * H_t         */
-  int block_size;        /* S = 16: anchor + 15 mask positions               */
+  int block_size;        /* S in 2..16: anchor + J = S-1 mask positions     */
   int top_k;             /* 16                                               */
   int use_conv;          /* DFlash-2 dynamic short convolution ([DF2] 2)     */
   int use_selector;      /* DFlash-2 Path Selector ([DF2] 1)                 */
@@ -191,17 +193,17 @@ DFLASH_API int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv,
 
 /* [DF] §2.2 (parallel block diffusion), §2.3 (anchor; shared embedding and
  * LM head); mask semantics of [FD] Metodologia 1.  For each request b the
- * block is [anchor_ids[b], mask x 15] at positions ctx_len[b] .. +15; one
+ * block is [anchor_ids[b], mask x J] at positions ctx_len[b] .. +J; one
  * forward pass in which every block query attends to all ctx_len[b] cached
- * tokens and to all 16 block tokens; the 15 mask positions' logits give the
+ * tokens and to all S block tokens; the J mask positions' logits give the
  * top-16 candidates (value desc, id asc).  The KV cache is only read.
  *   ctx_len:      device int32 [batch], each <= max_pages*page_size.
  *   anchor_ids:   device int32 [batch] in [0, V).
- *   topk_ids:     device int32 [batch][15][16] out.
- *   topk_logits:  device fp32 [batch][15][16] out (raw logits).
- *   final_hidden: device [batch][16][H] (dtype) out, final-normed hidden
+ *   topk_ids:     device int32 [batch][J][16] out.
+ *   topk_logits:  device fp32 [batch][J][16] out (raw logits).
+ *   final_hidden: device [batch][S][H] (dtype) out, final-normed hidden
  *                 (needed by dflash_select_path's gate); may be NULL.
- *   logits:       device fp32 [batch][15][V] out; may be NULL (then kept in
+ *   logits:       device fp32 [batch][J][V] out; may be NULL (then kept in
  *                 the workspace). */
 DFLASH_API int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv,
                        const int32_t *ctx_len, const int32_t *anchor_ids, int batch,
@@ -210,24 +212,25 @@ DFLASH_API int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv,
 
 /* [DF2] Arquitectura 1 (Path Selector) with use_selector: pair scores
  *   s[j][p][c] = z_j[c] + sigmoid(w_g.h_j + b_g) * (A e256[p]).(B e256[c])
- * for j = 1..15, p over position j-1's candidates (the anchor for j = 1,
+ * for j = 1..J, p over position j-1's candidates (the anchor for j = 1,
  * repeated over the 16 rows), c over position j's; then the greedy path
  * (ties to the lower token id).  Without use_selector: draft = top-1.
- *   final_hidden: device [batch][16][H] from dflash_draft_block.
- *   draft_ids:    device int32 [batch][15] out.
- *   pair_scores:  device fp32 [batch][15][16][16] out, or NULL. */
+ *   final_hidden: device [batch][S][H] from dflash_draft_block.
+ *   draft_ids:    device int32 [batch][J] out.
+ *   pair_scores:  device fp32 [batch][J][16][16] out, or NULL. */
 DFLASH_API int dflash_select_path(dflash_ctx *ctx, const int32_t *anchor_ids, const int32_t *topk_ids,
                        const float *topk_logits, const void *final_hidden, int batch,
                        int32_t *draft_ids, float *pair_scores,
                        void *workspace, size_t workspace_bytes, dflash_stream_t stream);
 
 /* [DF2] Flujo de Inferencia 4-5, [BW] Contexto tecnico: k = length of the
- * longest prefix with draft[i] == target[i] (0..15); bonus = target[k];
- * committed = target[0..k] then -1.  Needs no context.
- *   draft_ids: device int32 [batch][15]; target_ids: device int32 [batch][16]
- *   accept_len, bonus: device int32 [batch]; committed: device int32 [batch][16]. */
+ * longest prefix with draft[i] == target[i] (0..J); bonus = target[k];
+ * committed = target[0..k] then -1.  Needs no context; block_size = S in
+ * 2..16 (else DFLASH_ERR_ARG).
+ *   draft_ids: device int32 [batch][J]; target_ids: device int32 [batch][S]
+ *   accept_len, bonus: device int32 [batch]; committed: device int32 [batch][S]. */
 DFLASH_API int dflash_verify_greedy(const int32_t *draft_ids, const int32_t *target_ids, int batch,
-                         int32_t *accept_len, int32_t *bonus, int32_t *committed,
+                         int block_size, int32_t *accept_len, int32_t *bonus, int32_t *committed,
                          dflash_stream_t stream);
 
 /* [DF2] Arquitectura del Sistema item 1 (selection "by sampling over these
@@ -237,11 +240,11 @@ DFLASH_API int dflash_verify_greedy(const int32_t *draft_ids, const int32_t *tar
  * c_0 the anchor row, and c_j is the first candidate (in candidate order)
  * whose running probability exceeds uniforms[j] * total.
  *   temperature:  T > 0.
- *   uniforms:     device fp32 [batch][15] in [0, 1) (the caller's random draws).
- *   draft_ids:    device int32 [batch][15] out.
- *   draft_probs:  device fp32 [batch][15][16] out: q_j over the candidates, as
+ *   uniforms:     device fp32 [batch][J] in [0, 1) (the caller's random draws).
+ *   draft_ids:    device int32 [batch][J] out.
+ *   draft_probs:  device fp32 [batch][J][16] out: q_j over the candidates, as
  *                 needed by dflash_verify_rejection.
- *   pair_scores:  device fp32 [batch][15][16][16] out, or NULL. */
+ *   pair_scores:  device fp32 [batch][J][16][16] out, or NULL. */
 DFLASH_API int dflash_sample_path(dflash_ctx *ctx, const int32_t *anchor_ids, const int32_t *topk_ids,
                        const float *topk_logits, const void *final_hidden, int batch, float temperature,
                        const float *uniforms, int32_t *draft_ids, float *draft_probs, float *pair_scores,
@@ -252,13 +255,13 @@ DFLASH_API int dflash_sample_path(dflash_ctx *ctx, const int32_t *anchor_ids, co
  * the target's distributions over the drafted block (one target pass);
  * draft token d_i is accepted while u_accept[i] * q_i(d_i) < p_i(d_i); at the
  * first rejection k the bonus is drawn from max(0, p_k - q_k) (q_k zero
- * outside position k's candidates), after 15 acceptances from p_15, both by
+ * outside position k's candidates), after J acceptances from p_J, both by
  * inverse CDF in vocabulary order with u_bonus; committed = d_0..d_{k-1},
  * bonus, then -1.  The committed tokens follow the target's distribution.
- *   target_logits: device fp32 [batch][16][V], V = the context's vocabulary.
+ *   target_logits: device fp32 [batch][S][V], V = the context's vocabulary.
  *   draft_ids, topk_ids, draft_probs: from dflash_sample_path / draft_block.
- *   u_accept: device fp32 [batch][15]; u_bonus: device fp32 [batch], in [0, 1).
- *   accept_len, bonus: device int32 [batch]; committed: device int32 [batch][16]. */
+ *   u_accept: device fp32 [batch][J]; u_bonus: device fp32 [batch], in [0, 1).
+ *   accept_len, bonus: device int32 [batch]; committed: device int32 [batch][S]. */
 DFLASH_API int dflash_verify_rejection(dflash_ctx *ctx, const float *target_logits, const int32_t *draft_ids,
                        const int32_t *topk_ids, const float *draft_probs, const float *u_accept,
                        const float *u_bonus, int batch, int32_t *accept_len, int32_t *bonus,
@@ -279,6 +282,18 @@ DFLASH_API int dflash_set_gemm_ctas(dflash_ctx *ctx, int ctas);
  * size) the bf16 block attention gives each CTA of its balanced split; 64
  * splits the chunk list as finely as the SM count allows, 0 = automatic. */
 DFLASH_API int dflash_set_attn_split(dflash_ctx *ctx, int tokens);
+
+/* Runtime block size ([DF2] table of inference engines: engine flag "runtime
+ * block size", example 5; [DF] §3 item 4 and §4 block size: a drafter trained
+ * on larger blocks generalises to smaller inference blocks, so the serving
+ * engine may pick the block size per step).  block_size in
+ * 2..dflash_config.block_size (else DFLASH_ERR_ARG); every later call on the
+ * context uses it (S and J = S - 1 in the shapes above).  The workspace from
+ * dflash_workspace_bytes fits every runtime block size.  Host-only; must not
+ * change while calls on the context are being enqueued from another thread. */
+DFLASH_API int dflash_set_block_size(dflash_ctx *ctx, int block_size);
+/* The context's current runtime block size (0 for a null context). */
+DFLASH_API int dflash_get_block_size(const dflash_ctx *ctx);
 
 /* Per-launch CUDA-event timing of every kernel the next calls launch (on
  * their own streams), aggregated by kernel family.  profile_end

@@ -15,6 +15,9 @@ C3  C1 shapes plus the DFlash-2 pieces (dynamic short conv, Path Selector),
 C4  27B-class drafter (hidden 5120, 40 q / 8 kv heads, FFN 17408), 64
     requests, ragged contexts uniform in [16384, 32768].  Its ~1.6 M context
     tokens start as a drawn cache state (template pages), not a prefill.
+C1S5, C2S5  C1 and C2 run at a runtime block size of 5 (anchor + 4 mask
+    positions), the engine-flag example of the DFlash-2 page; the drafter is
+    unchanged (trained at 16, run at a smaller block).
 
 Small test-only workloads (``T*``) use ragged sizes (hidden 320, vocab 1000,
 contexts that end mid-page, an empty context) so that every kernel sees
@@ -39,7 +42,7 @@ class DrafterConfig:
     target_hidden: int      # H_t
     n_target_layers: int    # n_sel sampled target layers
     target_depth: int       # total target layers the n_sel are sampled from
-    block: int = 16         # S: anchor + 15 mask positions
+    block: int = 16         # S (2..16): anchor + S-1 mask positions
     top_k: int = 16
     use_conv: bool = False  # DFlash-2 dynamic short convolution
     use_selector: bool = False  # DFlash-2 Path Selector
@@ -129,6 +132,11 @@ WORKLOADS = {
                                  use_conv=True, use_selector=True, split_act=True),
                    batch=8, ctx_lo=4096, ctx_hi=4096, seed=3),
     "C4": Workload("C4", CLASS_27B, batch=64, ctx_lo=16384, ctx_hi=32768, seed=4, kv_fill="template"),
+    # runtime block size 5
+    "C1S5": Workload("C1S5", replace(QWEN3_8B_SHAPED, name="qwen3-8b-shaped-block5", block=5),
+                     batch=1, ctx_lo=2048, ctx_hi=2048, seed=1),
+    "C2S5": Workload("C2S5", replace(QWEN3_8B_SHAPED, name="qwen3-8b-shaped-block5", block=5),
+                     batch=32, ctx_lo=1024, ctx_hi=8192, p_accept=_decay(0.9, 0.5), seed=2),
     # test-only workloads
     "T0D2": Workload("T0D2", replace(TINY_F32, name="tiny-f32-dflash2",
                                      use_conv=True, use_selector=True),
@@ -140,5 +148,14 @@ WORKLOADS = {
     "T1D2": Workload("T1D2", replace(SMALL_BF16, name="small-bf16-dflash2",
                                      use_conv=True, use_selector=True, split_act=True),
                      batch=3, ctx_lo=0, ctx_hi=0, explicit_ctx=(5, 64, 300), seed=12),
+    # runtime block sizes below 16: 5 (bf16), 7 (fp32 DFlash-2), 2 (one mask position, bf16 DFlash-2)
+    "T1S5": Workload("T1S5", replace(SMALL_BF16, name="small-bf16-block5", block=5),
+                     batch=3, ctx_lo=0, ctx_hi=0, explicit_ctx=(0, 63, 500), p_accept=_decay(0.9, 0.5), seed=14),
+    "T0D2S7": Workload("T0D2S7", replace(TINY_F32, name="tiny-f32-dflash2-block7", use_conv=True,
+                                         use_selector=True, block=7),
+                       batch=2, ctx_lo=0, ctx_hi=0, explicit_ctx=(31, 90), seed=15),
+    "T1D2S2": Workload("T1D2S2", replace(SMALL_BF16, name="small-bf16-dflash2-block2", use_conv=True,
+                                         use_selector=True, split_act=True, block=2),
+                       batch=3, ctx_lo=0, ctx_hi=0, explicit_ctx=(1, 64, 200), seed=16),
 }
 

@@ -40,7 +40,7 @@ class Case:
         self.W = gen.make_weights(cfg, wl.seed)
         self.ctx = gen.context_lengths(wl)
         self.B = len(self.ctx)
-        self.table, self.npages = gen.page_table(self.ctx + 16, cfg.page_size, wl.seed)
+        self.table, self.npages = gen.page_table(self.ctx + cfg.block, cfg.page_size, wl.seed)
         self.template = wl.kv_fill == "template"
         self.X = None if self.template else gen.target_hidden(cfg, int(self.ctx.sum()), wl.seed, "prefill")
         self.cu = np.concatenate([[0], np.cumsum(self.ctx)]).astype(np.int32)

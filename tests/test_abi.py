@@ -97,7 +97,8 @@ def _cfg(**kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(block_size=8), -4), (dict(top_k=8), -4), (dict(page_size=32), -4), (dict(hidden=250), -2),
+    (dict(block_size=17), -4), (dict(block_size=1), -4), (dict(block_size=8), -3),   # 2..16 pass to the weights
+    (dict(top_k=8), -4), (dict(page_size=32), -4), (dict(hidden=250), -2),
     (dict(n_kv_heads=3), -2), (dict(head_dim=96), -4), (dict(mask_id=5000), -1), (dict(dtype=7), -1),
     (dict(use_selector=1, sel_rank=100), -4),
 ])
@@ -120,7 +121,11 @@ def test_create_rejects_missing_or_misaligned_weights(lib):
 
 def test_null_and_empty_calls(lib):
     assert lib.dflash_workspace_bytes(None, 1, 1) == 0
-    assert lib.dflash_verify_greedy(None, None, 0, None, None, None, None) == 0     # empty batch: no-op
-    assert lib.dflash_verify_greedy(None, None, 3, None, None, None, None) == -1
+    assert lib.dflash_verify_greedy(None, None, 0, 16, None, None, None, None) == 0     # empty batch: no-op
+    assert lib.dflash_verify_greedy(None, None, 3, 16, None, None, None, None) == -1
+    assert lib.dflash_verify_greedy(None, None, 3, 17, None, None, None, None) == -1    # block size above 16
+    assert lib.dflash_verify_greedy(None, None, 3, 1, None, None, None, None) == -1     # no mask position
     assert lib.dflash_draft_block(None, None, None, None, 1, None, None, None, None, None, 0, None) == -1
     assert lib.dflash_set_attn_split(None, 64) == -1
+    assert lib.dflash_set_block_size(None, 5) == -1
+    assert lib.dflash_get_block_size(None) == 0

@@ -30,7 +30,7 @@ def case(name, **kw):
 
 
 # ----------------------------------------------------------------- injection
-@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2"])
+@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2", "T1S5"])
 def test_inject_matches_oracle(name):
     c = case(name)
     assert c.dr.status() == 0
@@ -54,7 +54,7 @@ def _gap_ok(vals_sorted, i, thr=1e-3):
     return min(lo, hi) >= thr
 
 
-@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2"])
+@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2", "T1S5", "T0D2S7", "T1D2S2"])
 def test_draft_matches_oracle(name):
     c = case(name)
     out = c.draft()
@@ -75,13 +75,13 @@ def test_draft_matches_oracle(name):
         # end to end: ids agree wherever the oracle's gap is decisive
         if c.cfg.dtype == "f32":
             full = -np.sort(-ref["z"], axis=1)
-            for j in range(15):
+            for j in range(c.cfg.block - 1):
                 for r in range(16):
                     if _gap_ok(full[j], r):
                         assert ids[b, j, r] == ref["cand_ids"][j, r], (b, j, r)
 
 
-@pytest.mark.parametrize("name", ["T0D2", "T1D2", "T1"])
+@pytest.mark.parametrize("name", ["T0D2", "T1D2", "T1", "T0D2S7", "T1D2S2"])
 def test_select_path_matches_oracle(name):
     c = case(name)
     out = c.draft(want_logits=False)
@@ -98,7 +98,7 @@ def test_select_path_matches_oracle(name):
         assert rel_err(s, s_ref) <= 1e-4, b
         path_ref = O.greedy_path(s_ref, ids[b])
         p = 0
-        for j in range(15):
+        for j in range(c.cfg.block - 1):
             row = np.sort(s_ref[j, p])[::-1]
             if row[0] - row[1] < 1e-3:
                 break          # the oracle's own decision is within the gap: stop comparing
@@ -120,11 +120,27 @@ def test_verify_golden_cases():
     assert to_np(com).tolist() == [c["committed"] for c in g]
 
 
-def test_verify_random_against_oracle():
+def test_verify_golden_cases_short_blocks():
+    import torch
+    g = json.load(open(os.path.join(GOLDEN, "verify_cases_short_block.json")))["cases"]
+    from block_diffusion_drafter_context_gb300.drafter import Drafter
+    for S in sorted({c["S"] for c in g}):
+        cs = [c for c in g if c["S"] == S]
+        d = torch.tensor([c["draft"] for c in cs], dtype=torch.int32, device="cuda")
+        t = torch.tensor([c["target"] for c in cs], dtype=torch.int32, device="cuda")
+        acc, bonus, com = Drafter.verify_greedy(d, t)
+        torch.cuda.synchronize()
+        assert to_np(acc).tolist() == [c["k"] for c in cs]
+        assert to_np(bonus).tolist() == [c["bonus"] for c in cs]
+        assert to_np(com).tolist() == [c["committed"] for c in cs]
+
+
+@pytest.mark.parametrize("S", [16, 5, 2])
+def test_verify_random_against_oracle(S):
     import torch
     from block_diffusion_drafter_context_gb300.drafter import Drafter
     rng = np.random.default_rng(5)
-    d = rng.integers(0, 50, size=(1000, 15)).astype(np.int32)
+    d = rng.integers(0, 50, size=(1000, S - 1)).astype(np.int32)
     t = gen.target_ids(d, [0.85] * 15, 50, seed=5)
     acc, bonus, com = Drafter.verify_greedy(torch.from_numpy(d).cuda(), torch.from_numpy(t).cuda())
     acc, bonus, com = to_np(acc), to_np(bonus), to_np(com)
@@ -135,7 +151,7 @@ def test_verify_random_against_oracle():
 
 
 # ----------------------------------------------------------------- the whole step
-@pytest.mark.parametrize("name", ["T1", "T1D2"])
+@pytest.mark.parametrize("name", ["T1", "T1D2", "T1S5", "T1D2S2"])
 def test_step_is_lossless_and_verify_matches_oracle(name):
     import torch
     c = case(name)
@@ -187,6 +203,36 @@ def test_single_request_views_match_oracle():
         ref = c.oracle_draft(b)
         assert rel_err(to_np(out["final_hidden"])[0], ref["h"]) <= tol, b
         assert rel_err(to_np(out["logits"])[0], ref["z"]) <= tol, b
+
+
+def test_runtime_block_size_switch_matches_oracle():
+    """One context (configured block 16) switched between runtime block sizes
+    from step to step: each step matches the oracle at that block size, and
+    returning to 16 gives back the first step's results bit for bit."""
+    from dataclasses import replace
+    import torch
+    c = case("T1")
+    tol = TOL[c.cfg.dtype]
+    first = c.draft()
+    torch.cuda.synchronize()
+    for S in (5, 2, 9):
+        c.dr.set_block_size(S)
+        out = c.draft()
+        assert c.dr.status() == 0
+        assert tuple(out["logits"].shape) == (c.B, S - 1, c.cfg.vocab)
+        cfg_s = replace(c.cfg, block=S)
+        for b in range(c.B):
+            ref = O.draft_request(cfg_s, c.W, c.oracle_kv(b), int(c.ctx[b]), int(c.anchor[b]))
+            assert rel_err(to_np(out["final_hidden"])[b], ref["h"]) <= tol, (S, b)
+            assert rel_err(to_np(out["logits"])[b], ref["z"]) <= tol, (S, b)
+    from block_diffusion_drafter_context_gb300.binding import DflashError
+    with pytest.raises(DflashError):
+        c.dr.set_block_size(17)
+    c.dr.set_block_size(16)
+    again = c.draft()
+    torch.cuda.synchronize()
+    for key in ("topk_ids", "topk_logits", "final_hidden", "logits"):
+        assert torch.equal(first[key], again[key]), key
 
 
 def test_split_kv_and_gemm_partition_do_not_change_results():

@@ -29,14 +29,15 @@ def cdf_margin(w, u):
     return float(np.min(np.abs(c - u)))
 
 
-@pytest.mark.parametrize("name", ["T1", "T1D2"])
+@pytest.mark.parametrize("name", ["T1", "T1D2", "T1S5", "T0D2S7"])
 @pytest.mark.parametrize("temperature", [0.6, 1.0, 1.7])
 def test_sample_path_matches_oracle(name, temperature):
     import torch
     c = case(name)
+    J = c.cfg.block - 1
     out = c.draft(want_logits=False)
     rng = np.random.default_rng(31)
-    u = rng.random((c.B, 15)).astype(np.float32)
+    u = rng.random((c.B, J)).astype(np.float32)
     draft, q = c.dr.sample_path(c.anchor_d, out["topk_ids"], out["topk_logits"], out["final_hidden"], temperature,
                                 torch.from_numpy(u).cuda())
     assert c.dr.status() == 0
@@ -47,7 +48,7 @@ def test_sample_path_matches_oracle(name, temperature):
              else O.logit_scores(vals[b]))
         d_ref, q_ref, idx_ref = O.sample_path(s, ids[b], temperature, u[b].astype(np.float64))
         prev = 0
-        for j in range(15):
+        for j in range(J):
             row = s[j, prev] / temperature
             e = np.exp(row - row.max())
             qj = e / e.sum()
@@ -59,30 +60,31 @@ def test_sample_path_matches_oracle(name, temperature):
 
 
 def _target_logits(c, draft, rng, boost):
-    """Synthetic target logits [B, 16, V]: N(0, 1.5^2), the drafted token of
+    """Synthetic target logits [B, S, V]: N(0, 1.5^2), the drafted token of
     each position raised by `boost` (so that acceptance varies)."""
-    V = c.cfg.vocab
-    z = rng.normal(size=(c.B, 16, V)) * 1.5
+    V, S = c.cfg.vocab, c.cfg.block
+    z = rng.normal(size=(c.B, S, V)) * 1.5
     for b in range(c.B):
-        for i in range(15):
+        for i in range(S - 1):
             z[b, i, draft[b, i]] += boost[i]
     return z.astype(np.float32)
 
 
-@pytest.mark.parametrize("name", ["T1", "T1D2"])
+@pytest.mark.parametrize("name", ["T1", "T1D2", "T1S5", "T1D2S2"])
 def test_verify_rejection_matches_oracle(name):
     import torch
     c = case(name)
+    J = c.cfg.block - 1
     out = c.draft(want_logits=False)
     rng = np.random.default_rng(32)
     checked = 0
     for trial in range(6):
-        u = rng.random((c.B, 15)).astype(np.float32)
+        u = rng.random((c.B, J)).astype(np.float32)
         draft, q = c.dr.sample_path(c.anchor_d, out["topk_ids"], out["topk_logits"], out["final_hidden"], 1.0,
                                     torch.from_numpy(u).cuda())
         d, qn, ids = to_np(draft), to_np(q), to_np(out["topk_ids"])
-        zt = _target_logits(c, d, rng, boost=np.linspace(6.0, 0.0, 15) + trial)
-        ua = rng.random((c.B, 15)).astype(np.float32)
+        zt = _target_logits(c, d, rng, boost=np.linspace(6.0, 0.0, J) + trial)
+        ua = rng.random((c.B, J)).astype(np.float32)
         ub = rng.random(c.B).astype(np.float32)
         acc, bonus, com = c.dr.verify_rejection(torch.from_numpy(zt).cuda(), draft, out["topk_ids"], q,
                                                 torch.from_numpy(ua).cuda(), torch.from_numpy(ub).cuda())
@@ -96,7 +98,7 @@ def test_verify_rejection_matches_oracle(name):
             k_ref, bonus_ref, com_ref = O.verify_rejection(d[b], qn[b].astype(np.float64), ids[b], z64,
                                                            ua[b].astype(np.float64), float(ub[b]))
             margins = []
-            for i in range(min(k_ref + 1, 15)):
+            for i in range(min(k_ref + 1, J)):
                 cidx = int(np.nonzero(ids[b, i] == d[b, i])[0][0])
                 margins.append(abs(float(ua[b, i]) * qn[b, i, cidx] - p[i, d[b, i]]))
             if min(margins) < 1e-5:
@@ -104,12 +106,12 @@ def test_verify_rejection_matches_oracle(name):
             assert acc[b] == k_ref, (trial, b)
             assert (com[b, :k_ref] == d[b, :k_ref]).all()
             # the bonus: a valid inverse-CDF draw, equal to the oracle's where decisive
-            if k_ref < 15:
+            if k_ref < J:
                 r = p[k_ref].copy()
                 r[ids[b, k_ref]] -= qn[b, k_ref]
                 w = np.maximum(r, 0.0)
             else:
-                w = p[15]
+                w = p[J]
             if cdf_margin(w, float(ub[b])) >= 1e-5:
                 assert bonus[b] == bonus_ref, (trial, b)
             assert w[bonus[b]] > 0

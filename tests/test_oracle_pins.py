@@ -346,6 +346,14 @@ def test_verify_golden_cases():
         assert (k, bonus, committed.tolist()) == (c["k"], c["bonus"], c["committed"]), c["name"]
 
 
+def test_verify_golden_cases_short_blocks():
+    g = json.load(open(os.path.join(GOLDEN, "verify_cases_short_block.json")))
+    for c in g["cases"]:
+        assert len(c["draft"]) == c["S"] - 1 and len(c["target"]) == c["S"]
+        k, bonus, committed = O.verify_greedy(c["draft"], c["target"])
+        assert (k, bonus, committed.tolist()) == (c["k"], c["bonus"], c["committed"]), c["name"]
+
+
 @pytest.mark.parametrize("wl", ["C1", "C2"])
 def test_acceptance_statistics_closed_form(wl):
     """E[k] = sum_i prod_{j<=i} p_j for the synthetic target tokens."""
@@ -365,15 +373,17 @@ def test_acceptance_statistics_closed_form(wl):
 # --------------------------------------------------------------------------
 # the whole drafter
 # --------------------------------------------------------------------------
-def test_drafter_zero_sublayers_reduce_to_embedding_head():
-    cfg = micro_cfg()
+@pytest.mark.parametrize("S", [16, 5, 2])
+def test_drafter_zero_sublayers_reduce_to_embedding_head(S):
+    cfg = micro_cfg(block=S)
     W = f32_weights(cfg, 15)
     for lw in W["layers"]:
         lw["w_o"] = np.zeros_like(lw["w_o"])
         lw["w_down"] = np.zeros_like(lw["w_down"])
     anchor = 3
     h, z = O.drafter_forward(cfg, W, rand_kv(cfg, 10, 15), 10, anchor)
-    e = O.f64(W["embed"])[[anchor] + [cfg.mask_id] * 15]
+    assert h.shape == (S, cfg.hidden) and z.shape == (S - 1, cfg.vocab)
+    e = O.f64(W["embed"])[[anchor] + [cfg.mask_id] * (S - 1)]
     hh = e / np.sqrt((e * e).mean(1, keepdims=True) + cfg.eps) * O.f64(W["g_final"])
     np.testing.assert_allclose(h, hh, rtol=1e-12)
     np.testing.assert_allclose(z, hh[1:] @ O.f64(W["lm_head"]).T, rtol=1e-12)
@@ -449,11 +459,13 @@ def test_drafting_step_is_lossless():
         assert step["bonus"] == t[k]
 
 
-def test_brute_force_micro_drafter_single_layer():
+@pytest.mark.parametrize("S", [16, 5, 2])
+def test_brute_force_micro_drafter_single_layer(S):
     """Scalar-loop transcription of one pre-norm layer + head on a micro
-    drafter (1 layer, 2 q / 1 kv heads, d = 4), written from the layer reading."""
+    drafter (1 layer, 2 q / 1 kv heads, d = 4), written from the layer
+    reading, at the trained block size and at smaller runtime block sizes."""
     cfg = micro_cfg(hidden=8, n_layers=1, n_q_heads=2, n_kv_heads=1, head_dim=4,
-                    ffn=6, vocab=12, rope_base=10000.0)
+                    ffn=6, vocab=12, rope_base=10000.0, block=S)
     W = f32_weights(cfg, 20)
     n = 3
     kv = rand_kv(cfg, n, 20)
@@ -461,7 +473,7 @@ def test_brute_force_micro_drafter_single_layer():
     h, z = O.drafter_forward(cfg, W, kv, n, anchor)
     F = lambda a: O.f64(a)
     lw = W["layers"][0]
-    H, d, S = 8, 4, 16
+    H, d = 8, 4
 
     def rms(v, g):
         ms = sum(t * t for t in v) / len(v)
