@@ -235,11 +235,11 @@ __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, 
 #pragma unroll
     for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + static_cast<size_t>(lane + 32 * i) * 64, v[i]);
     // the block's PV k-step reads columns 0..15: below a block of 16 the
-    // columns S..15 get zeros (a 0 probability times a stale NaN is NaN)
-    if (j == S - 1)
-      for (int c = S; c < 16; ++c)
+    // columns S..15 get zeros (a 0 probability times a stale NaN is NaN),
+    // spread over the block's tokens: token j clears j+S, j+2S, ...
+    for (int c = j + S; c < 16; c += S)
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + (c - j) + static_cast<size_t>(lane + 32 * i) * 64, 0.f);
+      for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + (c - j) + static_cast<size_t>(lane + 32 * i) * 64, 0.f);
     return;
   }
   const bool is_q = head < nq;

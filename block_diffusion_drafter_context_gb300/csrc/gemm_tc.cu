@@ -676,6 +676,11 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   const int max_parts = std::max(2, (256 * 1024) / (BM * BN * 4));
   const int min_kb = std::max(4, (p.kbpt + max_parts - 1) / max_parts);
   p.G = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, (p.total + min_kb - 1) / min_kb)));
+  // A few more tiles than SMs with small token tiles (two ~100 KB CTAs fit on
+  // one SM): one whole tile per CTA, some SMs running two.  Splitting them
+  // over one CTA per SM would cut nearly every tile in two and put a global
+  // fixup on the tail of a weight-streaming GEMM.
+  if (lc.gemm_ctas == 0 && BN <= 32 && tiles > cap && tiles <= 2LL * cap) p.G = static_cast<int>(tiles);
   // Few tiles (at most half the SMs): cluster split-K instead, csk CTAs per
   // tile reducing through distributed shared memory - no global round trips
   // (fence, counter atomic, partial loads: ~2 us each here) on the GEMM's
