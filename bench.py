@@ -48,13 +48,23 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+def weight_bytes(cfg) -> float:
+    """Bytes of GEMM weights one drafting step streams (every projection once)."""
+    H, d, F, V = cfg.hidden, cfg.head_dim, cfg.ffn, cfg.vocab
+    per_layer = (cfg.n_q_heads + 2 * cfg.n_kv_heads) * d * H + cfg.n_q_heads * d * H + 3 * F * H
+    if cfg.use_conv:
+        per_layer += 4 * (H // 8) * H
+    n = cfg.n_layers * per_layer + V * H + H * cfg.feat_in
+    return n * (1.0 if cfg.weight_fp8 else 2.0)
+
+
 def workload_desc(wl):
     c = wl.cfg
     return (f"{wl.name}: {c.name} drafter (L={c.n_layers}, H={c.hidden}, {c.n_q_heads}q/{c.n_kv_heads}kv x "
             f"{c.head_dim}, F={c.ffn}, V={c.vocab}), batch {wl.batch}, context "
             f"{wl.ctx_lo if wl.ctx_lo == wl.ctx_hi else f'U[{wl.ctx_lo},{wl.ctx_hi}]'}, "
             f"{c.n_target_layers}x{c.target_hidden} target features, block size {c.block}, "
-            f"{c.block} new tokens injected per step")
+            f"{c.block} new tokens injected per step" + (", FP8 E4M3 weights (per-row scales)" if c.weight_fp8 else ""))
 
 
 # ---------------------------------------------------------------- clocks
@@ -476,7 +486,9 @@ def run_ours(args, wl):
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": workload_desc(wl), "batch": B, "ctx": int(ctx.max()),
-                   "l2": "no flush: every step streams 3.4 GB of drafter weights, > 129 MB L2",
+                   "l2": f"no flush: every step streams {weight_bytes(cfg) / 1e9:.1f} GB of drafter weights, "
+                         f"> 129 MB L2",
+                   "weights": "fp8-e4m3 + fp32 row scales (activations bf16)" if cfg.weight_fp8 else cfg.dtype,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "draft_tokens_per_s": J * blocks,
         "expected_committed_tokens_per_s": (exp_k + 1) * blocks,

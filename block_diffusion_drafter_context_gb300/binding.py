@@ -25,7 +25,7 @@ EXPORTS = (
     "dflash_set_wait_timeout", "dflash_set_gemm_ctas", "dflash_set_attn_split",
     "dflash_profile_begin", "dflash_profile_end", "dflash_debug_wait_flag", "dflash_last_error",
     "dflash_topk16_noalloc", "dflash_sample_path", "dflash_verify_rejection", "dflash_set_block_size",
-    "dflash_get_block_size",
+    "dflash_get_block_size", "dflash_debug_e4m3_to_bf16",
 )
 
 
@@ -34,20 +34,22 @@ class dflash_config(ctypes.Structure):
         "dtype", "hidden", "n_layers", "n_q_heads", "n_kv_heads", "head_dim", "ffn", "vocab",
         "target_hidden", "n_target_layers", "block_size", "top_k", "use_conv", "use_selector",
         "qk_norm", "fc_norm", "split_act", "sel_rank", "sel_dim", "mask_id", "page_size")] + [
-        ("rope_base", c_float), ("eps", c_float)]
+        ("rope_base", c_float), ("eps", c_float), ("weight_fp8", c_int)]
 
 
 class dflash_layer_weights(ctypes.Structure):
     _fields_ = [("g_attn", c_void_p), ("w_qkv", c_void_p), ("g_q", c_void_p), ("g_k", c_void_p),
                 ("w_o", c_void_p), ("g_ffn", c_void_p), ("w_gu", c_void_p), ("w_down", c_void_p),
-                ("w_conv", c_void_p * 4), ("b_conv", c_void_p * 4)]
+                ("w_conv", c_void_p * 4), ("b_conv", c_void_p * 4),
+                ("s_qkv", c_void_p), ("s_o", c_void_p), ("s_gu", c_void_p), ("s_down", c_void_p),
+                ("s_conv", c_void_p * 4)]
 
 
 class dflash_weights(ctypes.Structure):
     _fields_ = [("w_fc", c_void_p), ("g_fc", c_void_p), ("embed", c_void_p), ("lm_head", c_void_p),
                 ("g_final", c_void_p), ("layers", POINTER(dflash_layer_weights)),
                 ("sel_e256", c_void_p), ("sel_a", c_void_p), ("sel_b", c_void_p),
-                ("sel_w_g", c_void_p), ("sel_b_g", c_float)]
+                ("sel_w_g", c_void_p), ("sel_b_g", c_float), ("s_fc", c_void_p), ("s_lm_head", c_void_p)]
 
 
 class dflash_kv(ctypes.Structure):
@@ -98,6 +100,7 @@ def load(path: str = LIB_PATH):
         "dflash_profile_begin": (i, [vp]),
         "dflash_profile_end": (i, [vp, POINTER(dflash_kernel_stat), i, POINTER(c_int)]),
         "dflash_debug_wait_flag": (i, [vp, c_ulonglong, vp, vp]),
+        "dflash_debug_e4m3_to_bf16": (i, [vp, i, vp, vp]),
         "dflash_last_error": (ctypes.c_char_p, []),
         "dflash_topk16_noalloc": (i, [vp, i, i, vp, vp, vp]),
     }
@@ -213,6 +216,10 @@ def dflash_set_block_size(ctx, block_size: int):
 
 def dflash_get_block_size(ctx) -> int:
     return int(load().dflash_get_block_size(ctx))
+
+
+def dflash_debug_e4m3_to_bf16(codes, n, out, stream=None):
+    return _check(load().dflash_debug_e4m3_to_bf16(_p(codes), n, _p(out), _stream(stream)))
 
 
 def dflash_profile_begin(ctx):

@@ -60,7 +60,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 int make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elt_bytes, uint64_t cols,
-                 uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows) {
+                 uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows,
+                 CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
   if (!fn) return set_error(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   if (reinterpret_cast<uintptr_t>(base) & 15 || row_stride_bytes % 16)
@@ -71,7 +72,7 @@ int make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int e
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return set_error(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %llux%llu tensor", static_cast<int>(r),
                      static_cast<unsigned long long>(rows), static_cast<unsigned long long>(cols));
@@ -250,6 +251,15 @@ GemmOp mk(const void *W, int ldw, const void *X, const void *X_lo, int ldx, int 
   return o;
 }
 
+// The weight of a GEMM: bf16 matrix, or (weight_fp8) E4M3 codes with their row scales.
+GemmOp wq(const dflash_ctx *c, GemmOp op, const float *scale) {
+  if (c->cfg.weight_fp8) {
+    op.w_fp8 = true;
+    op.wscale = scale;
+  }
+  return op;
+}
+
 int check_ws(const dflash_ctx *c, void *ws, size_t bytes, int B, int Tn) {
   if (!ws) return set_error(DFLASH_ERR_ARG, "workspace is null");
   if (!aligned16(ws)) return set_error(DFLASH_ERR_ALIGN, "workspace must be 16-byte aligned");
@@ -302,6 +312,14 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *w, dflash_ctx 
   if (g.use_selector && (g.sel_rank < 1 || g.sel_rank > 64 || g.sel_dim < 1 || g.sel_dim > 1024))
     return set_error(DFLASH_ERR_UNSUPPORTED, "selector rank must be 1..64 and width 1..1024");
   if (!(g.eps >= 0.f) || !(g.rope_base > 1.f)) return set_error(DFLASH_ERR_ARG, "eps / rope_base out of range");
+  const bool f8 = g.weight_fp8 != 0;
+  if (f8 && g.dtype != DFLASH_BF16) return set_error(DFLASH_ERR_UNSUPPORTED, "FP8 weights need the bf16 path");
+  // FP8 code rows are K bytes: every GEMM's K a multiple of 16
+  if (f8 && (g.ffn % 16 || (g.n_target_layers * g.target_hidden) % 16))
+    return set_error(DFLASH_ERR_SHAPE, "FP8 weights: ffn and n_sel * H_t must be multiples of 16");
+  auto scale_ok = [](const float *s) { return s && (reinterpret_cast<uintptr_t>(s) & 3) == 0; };
+  if (f8 && (!scale_ok(w->s_fc) || !scale_ok(w->s_lm_head)))
+    return set_error(DFLASH_ERR_ARG, "FP8 weights: s_fc / s_lm_head missing");
   const void *req[] = {w->w_fc, w->embed, w->lm_head, w->g_final};
   for (const void *p : req)
     if (!p || !aligned16(p)) return set_error(DFLASH_ERR_ALIGN, "model weight missing or not 16-byte aligned");
@@ -315,8 +333,10 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *w, dflash_ctx 
     if (g.qk_norm && (!lw.g_q || !lw.g_k)) return set_error(DFLASH_ERR_ARG, "layer %d: qk_norm needs g_q, g_k", l);
     if (g.use_conv)
       for (int s = 0; s < 4; ++s)
-        if (!lw.w_conv[s] || !lw.b_conv[s] || !aligned16(lw.w_conv[s]))
+        if (!lw.w_conv[s] || !lw.b_conv[s] || !aligned16(lw.w_conv[s]) || (f8 && !scale_ok(lw.s_conv[s])))
           return set_error(DFLASH_ERR_ARG, "layer %d: conv site %d weights missing", l, s);
+    if (f8 && (!scale_ok(lw.s_qkv) || !scale_ok(lw.s_o) || !scale_ok(lw.s_gu) || !scale_ok(lw.s_down)))
+      return set_error(DFLASH_ERR_ARG, "layer %d: FP8 row scales missing", l);
   }
   if (g.use_selector && (!w->sel_e256 || !w->sel_a || !w->sel_b || !w->sel_w_g))
     return set_error(DFLASH_ERR_ARG, "selector weights missing");
@@ -392,8 +412,9 @@ int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv, const void *targ
   void *f_lo = split ? at<void>(workspace, L.f_lo) : nullptr;
   // context feature: fc projection, then RMSNorm
   if (int e = proj(ctx, lc, workspace, L,
-                   mk(ctx->w.w_fc, K, target_hidden, nullptr, K, total_new, H, K, EPI_F32, at<float>(workspace, L.fc),
-                      H, "fc")))
+                   wq(ctx, mk(ctx->w.w_fc, K, target_hidden, nullptr, K, total_new, H, K, EPI_F32,
+                              at<float>(workspace, L.fc), H, "fc"),
+                      ctx->w.s_fc)))
     return e;
   if (int e = feature_norm(lc, f32, at<float>(workspace, L.fc), total_new, H, ctx->w.g_fc, g.eps, g.fc_norm != 0,
                            at<void>(workspace, L.f), f_lo, ctx_len_in, at<int32_t>(workspace, L.ctx_saved), batch))
@@ -404,9 +425,12 @@ int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv, const void *targ
   GemmOp kvop = mk(nullptr, H, at<void>(workspace, L.f), f_lo, H, total_new, 2 * nkv * d, H, EPI_F32,
                    at<float>(workspace, L.kvproj), 2 * nkv * d, "kv_inject");
   kvop.out_gstride = static_cast<size_t>(total_new) * 2 * nkv * d;
+  kvop.w_fp8 = g.weight_fp8 != 0;
+  const size_t tw = kvop.w_fp8 ? 1 : te;   // bytes per weight element
   for (int l = 0; l < g.n_layers; ++l) {
     const dflash_layer_weights &lw = ctx->layers[l];
-    kvop.Wg[l] = static_cast<const char *>(lw.w_qkv) + te * static_cast<size_t>(nq) * d * H;
+    kvop.Wg[l] = static_cast<const char *>(lw.w_qkv) + tw * static_cast<size_t>(nq) * d * H;
+    if (kvop.w_fp8) kvop.wscale_g[l] = lw.s_qkv + static_cast<size_t>(nq) * d;
     gk[l] = lw.g_k;
   }
   if (!f32 && (2 * nkv * d) % 128 == 0) {
@@ -417,6 +441,7 @@ int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv, const void *targ
       GemmOp one = kvop;
       one.n_groups = 1;
       one.W = kvop.Wg[l];
+      one.wscale = kvop.wscale_g[l];
       one.out = at<float>(workspace, L.kvproj) + l * kvop.out_gstride;
       if (int e = proj(ctx, lc, workspace, L, one)) return e;
     }
@@ -463,16 +488,17 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
   const size_t te = f32 ? 4 : 2;
   // conv coefficients of one site: tanh(W_c y + b_c), fp32 [R][H/8]
   auto coef_gemm = [&](int site, const dflash_layer_weights &lw, const void *y, const void *y_lo) {
-    GemmOp op = mk(lw.w_conv[site], H, y, y_lo, H, R, G8, H, EPI_TANH_BIAS, coef, G8, "conv_coef");
+    GemmOp op = wq(ctx, mk(lw.w_conv[site], H, y, y_lo, H, R, G8, H, EPI_TANH_BIAS, coef, G8, "conv_coef"),
+                   lw.s_conv[site]);
     op.bias = lw.b_conv[site];
     return proj(ctx, lc, ws, L, op);
   };
   // a sublayer's output projection: straight into the fp32 residual, or (conv)
   // into fp32 + bf16 halves, then the post-site conv adds it to the residual
-  auto out_proj = [&](int site, const dflash_layer_weights &lw, const void *Wm, int K, const void *X, const void *X_lo,
-                      const char *name) -> int {
-    if (!g.use_conv) return proj(ctx, lc, ws, L, mk(Wm, K, X, X_lo, K, R, H, K, EPI_ADD_F32, x, H, name));
-    GemmOp op = mk(Wm, K, X, X_lo, K, R, H, K, f32 ? EPI_F32 : EPI_F32_SPLIT, ysub32, H, name);
+  auto out_proj = [&](int site, const dflash_layer_weights &lw, const void *Wm, const float *Ws, int K, const void *X,
+                      const void *X_lo, const char *name) -> int {
+    if (!g.use_conv) return proj(ctx, lc, ws, L, wq(ctx, mk(Wm, K, X, X_lo, K, R, H, K, EPI_ADD_F32, x, H, name), Ws));
+    GemmOp op = wq(ctx, mk(Wm, K, X, X_lo, K, R, H, K, f32 ? EPI_F32 : EPI_F32_SPLIT, ysub32, H, name), Ws);
     op.out2 = ysub;
     op.out2_lo = ysub_lo;
     op.ldo2 = H;
@@ -490,8 +516,9 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
       ua = u2;
       ua_lo = u2_lo;
     }
-    if (int e = proj(ctx, lc, ws, L, mk(lw.w_qkv, H, ua, ua_lo, H, R, nh * d, H, EPI_F32, at<float>(ws, L.qkv), nh * d,
-                                        "qkv")))
+    if (int e = proj(ctx, lc, ws, L,
+                     wq(ctx, mk(lw.w_qkv, H, ua, ua_lo, H, R, nh * d, H, EPI_F32, at<float>(ws, L.qkv), nh * d, "qkv"),
+                        lw.s_qkv)))
       return e;
     if (int e = qk_norm_rope(lc, f32, at<float>(ws, L.qkv), B, S, nq, nkv, d, lw.g_q, lw.g_k, g.qk_norm != 0, g.eps,
                              g.rope_base, ctx_len, at<void>(ws, L.q), at<void>(ws, L.bk), at<void>(ws, L.bv)))
@@ -520,7 +547,7 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     aa.partials = at<float>(ws, L.attn_part);
     aa.partial_slots = L.attn_part_slots;
     if (int e = f32 ? attention_f32(lc, aa) : attention_bf16(lc, aa)) return e;
-    if (int e = out_proj(1, lw, lw.w_o, nq * d, aa.out, aa.out_lo, "o_proj")) return e;
+    if (int e = out_proj(1, lw, lw.w_o, lw.s_o, nq * d, aa.out, aa.out_lo, "o_proj")) return e;
     // ---- FFN sublayer
     if (int e = rmsnorm_rows(lc, f32, x, R, H, S, lw.g_ffn, g.eps, u, u_lo, nullptr, nullptr)) return e;
     ua = u;
@@ -532,11 +559,12 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
       ua_lo = u2_lo;
     }
     {
-      GemmOp op = mk(lw.w_gu, H, ua, ua_lo, H, R, 2 * F, H, EPI_SWIGLU, at<void>(ws, L.hmid), F, "gate_up");
+      GemmOp op = wq(ctx, mk(lw.w_gu, H, ua, ua_lo, H, R, 2 * F, H, EPI_SWIGLU, at<void>(ws, L.hmid), F, "gate_up"),
+                     lw.s_gu);
       op.out_lo = hmid_lo;
       if (int e = proj(ctx, lc, ws, L, op)) return e;
     }
-    if (int e = out_proj(3, lw, lw.w_down, F, at<void>(ws, L.hmid), hmid_lo, "down")) return e;
+    if (int e = out_proj(3, lw, lw.w_down, lw.s_down, F, at<void>(ws, L.hmid), hmid_lo, "down")) return e;
     if (l + 1 < g.n_layers)
       if (int e = rmsnorm_rows(lc, f32, x, R, H, S, ctx->layers[l + 1].g_attn, g.eps, u, u_lo, nullptr, nullptr))
         return e;
@@ -545,8 +573,9 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
                            lo(L.hmask_lo)))
     return e;
   if (int e = proj(ctx, lc, ws, L,
-                   mk(ctx->w.lm_head, H, at<void>(ws, L.hmask), lo(L.hmask_lo), H, B * J, V, H, EPI_F32, lg, V,
-                      "lm_head")))
+                   wq(ctx, mk(ctx->w.lm_head, H, at<void>(ws, L.hmask), lo(L.hmask_lo), H, B * J, V, H, EPI_F32, lg, V,
+                              "lm_head"),
+                      ctx->w.s_lm_head)))
     return e;
   return topk16(lc, lg, B * J, V, topk_ids, topk_logits, at<uint64_t>(ws, L.topk_part), at<int>(ws, L.topk_ctr),
                 TOPK_MAX_CHUNKS);
@@ -699,6 +728,12 @@ int dflash_debug_wait_flag(const int32_t *flag, unsigned long long timeout_ns, v
   lc.status = at<int>(workspace, 0);
   lc.timeout_ns = timeout_ns;
   return wait_flag(lc, flag);
+}
+
+int dflash_debug_e4m3_to_bf16(const void *codes, int n, void *out, dflash_stream_t stream) {
+  Launch lc;
+  lc.stream = reinterpret_cast<cudaStream_t>(stream);
+  return e4m3_to_bf16(lc, codes, n, out);
 }
 
 }  // extern "C"

@@ -21,7 +21,18 @@
 //     tensors, high and low halves of the fp32 value; each k-step issues a
 //     second MMA on the same weight tile, so the product carries ~16 mantissa
 //     bits of the activation at no extra HBM traffic (the weight stream, not
-//     the tensor pipe, bounds these GEMMs).
+//     the tensor pipe, bounds these GEMMs);
+//   * FP8 weights (F8): the weight stream is E4M3 codes with one fp32 scale
+//     per output row.  TMA lands a [128 rows][128 codes] tile (16 KB,
+//     128-byte swizzle); four converter warps, one TMEM lane quarter each,
+//     turn their rows into the exact bf16 values and store them into tensor
+//     memory (three tiles), from where the MMA reads its A operand.  Staging
+//     the bf16 tile in shared memory instead would move ~6.5 bytes of shared
+//     memory per HBM byte, past the SM's shared-memory bandwidth at full HBM
+//     rate; this way it is ~2.5, as for bf16 weights.  Activations stay bf16,
+//     so the precision is that of the bf16 path; the row scale is applied in
+//     the epilogue.  Half the HBM bytes per weight; up to two CTAs per SM so
+//     that two threads issue MMAs on each SM.
 // Every mbarrier wait is bounded (status word + unwind on timeout).
 #include "common.cuh"
 #include "internal.h"
@@ -34,34 +45,55 @@ namespace {
 constexpr int BM = 128;   // weight rows per tile (UMMA M)
 constexpr int BK = 64;    // bf16 elements per stage row = 128 bytes = one swizzle row
 constexpr int UK = 16;    // K per tcgen05.mma (kind::f16)
-constexpr int NTHREADS = 192;
 constexpr int MAX_GROUPS = 16;   // weight matrices sharing one launch (same shape, same activations)
+constexpr int SMEM_PER_SM = 228 * 1024;   // shared memory of one SM (1 KB of it reserved per resident CTA)
 
 struct WMaps {
   CUtensorMap m[MAX_GROUPS];
 };
 
-template <int BN, bool SPLIT>
+constexpr int pow2_at_least(int x) { return x <= 32 ? 32 : 2 * pow2_at_least((x + 1) / 2); }
+
+template <int BN, bool SPLIT, bool F8>
 struct Cfg {
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES * (SPLIT ? 2 : 1);
-  // Small token tiles (weight streaming): ~100 KB of ring, so two GEMM CTAs
-  // fit on one SM and, under programmatic dependent launch, the next GEMM's
-  // CTAs become resident and stream their weights while this one drains
-  // (152 x 5 stages in flight still exceed what HBM needs in flight).  Large
-  // token tiles (tensor-bound): one CTA per SM with a deeper ring.
-  static constexpr int BUDGET = (BN <= 32 ? 100 : 200) * 1024;
-  static constexpr int STAGES_RAW = BUDGET / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : (STAGES_RAW < 2 ? 2 : STAGES_RAW);
-  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  // warps: 0 TMA, 1 MMA, 2-5 epilogue, (F8) 6-9 weight converters
+  static constexpr int CONV_WARPS = F8 ? 4 : 0;
+  static constexpr int NT = 192 + 32 * CONV_WARPS;
+  static constexpr int BKI = F8 ? 2 * BK : BK;         // k per ring stage (one k-block)
+  static constexpr int BT = BKI / BK;                  // 64-k activation tiles per stage
+  static constexpr int A_BYTES = F8 ? 0 : BM * BK * 2; // bf16 weight tile in shared memory
+  static constexpr int RAW_BYTES = F8 ? BM * BKI : 0;  // E4M3 code tile, 128-byte rows
+  static constexpr int B_BYTES = BN * BK * 2;          // one 64-k activation tile
+  static constexpr int B_STAGE = B_BYTES * BT;
+  // one ring stage as TMA fills it: the weight tile (bf16, or codes) and the activation tiles
+  static constexpr int STAGE_BYTES = (F8 ? RAW_BYTES : A_BYTES) + B_STAGE * (SPLIT ? 2 : 1);
+  static constexpr int CSTAGES = F8 ? 3 : 0;           // bf16 weight tiles in tensor memory
+  static constexpr int A_TCOLS = BKI / 2;              // TMEM columns of one (two bf16 per column)
+  static constexpr int A_COL = 2 * BN < 32 ? 32 : 2 * BN;   // first of them, after the accumulators
   // cluster split-K with small token tiles pushes each row's fp32 share into
   // the owning CTA: at most (csk - 1) * ceil(128 / csk) <= 120 rows arrive
   static constexpr bool PUSH = BN <= 32;
   static constexpr int PUSH_BYTES = PUSH ? 120 * BN * 4 : 0;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256 + PUSH_BYTES;
-  static_assert((2 * STAGES + 6) * 8 + 12 <= 256, "GEMM control block overflows");
-  static_assert(STAGES * STAGE_BYTES >= BM * BN * 4, "the ring must hold one fp32 tile (cluster split-K share)");
+  static constexpr int CTRL = 512;                     // mbarriers and flags
+  // Small token tiles (weight streaming): ~100 KB of ring, so two GEMM CTAs
+  // fit on one SM and, under programmatic dependent launch, the next GEMM's
+  // CTAs become resident and stream their weights while this one drains
+  // (152 x 5 stages in flight still exceed what HBM needs in flight).  F8
+  // keeps the whole CTA within half an SM.  Large token tiles (tensor-bound):
+  // one CTA per SM with a deeper ring.
+  static constexpr int BUDGET = BN <= 32 ? (F8 ? (SMEM_PER_SM / 2 - 1024 - 1024 - CTRL - PUSH_BYTES) : 100 * 1024)
+                                         : 200 * 1024;
+  static constexpr int STAGES_RAW = BUDGET / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : (STAGES_RAW < 2 ? 2 : STAGES_RAW);
+  static constexpr int TMEM_COLS = F8 ? pow2_at_least(A_COL + CSTAGES * A_TCOLS) : (2 * BN < 32 ? 32 : 2 * BN);
+  static constexpr int RING = STAGES * STAGE_BYTES;
+  static constexpr int SMEM = 1024 + RING + CTRL + PUSH_BYTES;
+  static_assert((2 * STAGES + 2 * CSTAGES + 6) * 8 + 12 <= CTRL, "GEMM control block overflows");
+  static_assert(RING >= BM * BN * 4, "the ring must hold one fp32 tile (cluster split-K share)");
+  static_assert(!F8 || BN > 32 || 2 * (SMEM + 1024) <= SMEM_PER_SM, "two F8 CTAs must fit on one SM");
+  // (two CTAs per SM only for small token tiles: the others take over 113 KB of shared memory)
+  static_assert(TMEM_COLS <= 512 && (BN > 32 || 2 * TMEM_COLS <= 512), "tensor memory of the CTAs resident on one SM");
+  static_assert(BN <= 32 || SMEM > SMEM_PER_SM / 2, "a large-tile CTA must not share its SM");
 };
 
 struct Params {
@@ -79,6 +111,7 @@ struct Params {
   void *out2, *out2_lo;
   int ldo2;
   const float *bias;
+  const float *wscale[MAX_GROUPS];   // F8: per-row weight scales of each group
   float *partials;     // [G][2][BM][BN] row-major shares
   int *counters;       // [tiles]
   int *status;
@@ -103,9 +136,16 @@ __device__ __forceinline__ void store_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, s
   if (lo) lo[i] = f2bf(v - bf2f(h));
 }
 
-// Apply the epilogue to 16 consecutive token columns of weight row n.
-__device__ __forceinline__ void finalize(const Params &p, const float (&v)[16], int n, int tok0, size_t goff) {
+// Apply the epilogue to 16 consecutive token columns of weight row n (ws:
+// the group's FP8 row scales, or null).
+__device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n, int tok0, size_t goff,
+                                         const float *ws) {
   const bool nok = n < p.N;
+  if (ws) {
+    const float sc = nok ? ws[n] : 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] *= sc;
+  }
   switch (p.epi) {
     case EPI_BF16: {
       __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out), *ol = static_cast<__nv_bfloat16 *>(p.out_lo);
@@ -162,25 +202,55 @@ __device__ __forceinline__ void finalize(const Params &p, const float (&v)[16], 
   }
 }
 
-template <int BN, bool SPLIT>
-__global__ void __launch_bounds__(NTHREADS, 1)
+// Four E4M3 codes -> four bf16 values, exact.  The code's bits, moved into
+// bf16 fields (sign to bit 15, exponent and mantissa to bits 4..10), encode
+// code * 2^-120 for every code (normal, subnormal, zero: bf16's exponent
+// bias is 120 more than E4M3's and both fields line up); one bf16 multiply by
+// 2^120 (0x7B80) restores the value.  Each 16-bit half is built by one byte
+// permute - the code byte low, its sign replicated into the high byte
+// (selector bit 3) - one shift by 4 and one mask keeping bits 4..10 and 15.
+// NaN codes (S.1111.111) are not weights.  Returns the two bf16x2 words of
+// bytes (0,1) and (2,3).
+__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
+  uint32_t lo, hi;
+  asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(lo) : "r"(w));   // [sign(b1), b1, sign(b0), b0]
+  asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(hi) : "r"(w));   // [sign(b3), b3, sign(b2), b2]
+  lo = (lo << 4) & 0x87F087F0u;
+  hi = (hi << 4) & 0x87F087F0u;
+  uint2 r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r.x) : "r"(lo), "r"(0x7B807B80u));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r.y) : "r"(hi), "r"(0x7B807B80u));
+  return r;
+}
+
+__global__ void e4m3_to_bf16_kernel(const uint32_t *codes, int n4, uint2 *out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n4) out[i] = e4m3x4_to_bf16x4(codes[i]);
+}
+
+template <int BN, bool SPLIT, bool F8>
+__global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 : 1)
     gemm_tc_kernel(const __grid_constant__ WMaps wm, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmXlo, const Params p) {
-  using C = Cfg<BN, SPLIT>;
+  using C = Cfg<BN, SPLIT, F8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *base = smem_raw + pad;
+  // [bf16 weight tiles (not F8)] [activation tiles] [low halves (SPLIT)] [code tiles (F8)]
   uint8_t *sA = base;
   uint8_t *sB = base + C::STAGES * C::A_BYTES;
-  uint8_t *sBl = sB + C::STAGES * C::B_BYTES;   // low halves (SPLIT only)
-  uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::STAGES * C::B_BYTES * (SPLIT ? 2 : 1));
+  uint8_t *sBl = sB + C::STAGES * C::B_STAGE;   // low halves (SPLIT only)
+  uint8_t *sRaw = sBl + (SPLIT ? C::STAGES * C::B_STAGE : 0);
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + C::RING);
   uint64_t *empty = full + C::STAGES;
   uint64_t *tfull = empty + C::STAGES;
   uint64_t *tempty = tfull + 2;
   uint64_t *drain = tempty + 2;
   uint64_t *rbar = drain + 1;   // cluster split-K (push): shares of the other CTAs have arrived
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(rbar + 1);
-  float *spush = reinterpret_cast<float *>(base + C::STAGES * C::STAGE_BYTES + 256);
+  uint64_t *cfull = rbar + 1;   // F8: converted weight tile ready
+  uint64_t *cempty = cfull + C::CSTAGES;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cempty + C::CSTAGES);
+  float *spush = reinterpret_cast<float *>(base + C::RING + C::CTRL);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *bcast = reinterpret_cast<int *>(tmem_slot + 2);
 
@@ -190,6 +260,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < C::CSTAGES; ++s) {
+      mbar_init(&cfull[s], C::CONV_WARPS);   // every converter warp
+      mbar_init(&cempty[s], 1);
     }
     mbar_init(&tfull[0], 1);
     mbar_init(&tfull[1], 1);
@@ -277,15 +351,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         int g, row0, tok0, kb;
         coords(q, g, row0, tok0, kb);
         mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
-        tma_load_2d_hint(sA + i * C::A_BYTES, &wm.m[g], &full[i], kb * BK, row0, pol_w);
+        tma_load_2d_hint(F8 ? sRaw + i * C::RAW_BYTES : sA + i * C::A_BYTES, &wm.m[g], &full[i], kb * C::BKI, row0,
+                         pol_w);
       }
       grid_dep_wait();
       q = it0;
       for (int i = 0; i < n_pre; ++i, advance(q)) {
         int g, row0, tok0, kb;
         coords(q, g, row0, tok0, kb);
-        tma_load_2d(sB + i * C::B_BYTES, &tmX, &full[i], kb * BK, tok0);
-        if (SPLIT) tma_load_2d(sBl + i * C::B_BYTES, &tmXlo, &full[i], kb * BK, tok0);
+#pragma unroll
+        for (int t = 0; t < C::BT; ++t) {
+          tma_load_2d(sB + i * C::B_STAGE + t * C::B_BYTES, &tmX, &full[i], kb * C::BKI + t * BK, tok0);
+          if (SPLIT) tma_load_2d(sBl + i * C::B_STAGE + t * C::B_BYTES, &tmXlo, &full[i], kb * C::BKI + t * BK, tok0);
+        }
       }
       uint32_t stage = n_pre % C::STAGES, phase = (n_pre == C::STAGES) ? 1u : 0u;
       long long issued = n_pre;
@@ -298,9 +376,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           break;
         }
         mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-        tma_load_2d_hint(sA + stage * C::A_BYTES, &wm.m[g], &full[stage], kb * BK, row0, pol_w);
-        tma_load_2d(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * BK, tok0);
-        if (SPLIT) tma_load_2d(sBl + stage * C::B_BYTES, &tmXlo, &full[stage], kb * BK, tok0);
+        tma_load_2d_hint(F8 ? sRaw + stage * C::RAW_BYTES : sA + stage * C::A_BYTES, &wm.m[g], &full[stage],
+                         kb * C::BKI, row0, pol_w);
+#pragma unroll
+        for (int t = 0; t < C::BT; ++t) {
+          tma_load_2d(sB + stage * C::B_STAGE + t * C::B_BYTES, &tmX, &full[stage], kb * C::BKI + t * BK, tok0);
+          if (SPLIT)
+            tma_load_2d(sBl + stage * C::B_STAGE + t * C::B_BYTES, &tmXlo, &full[stage], kb * C::BKI + t * BK, tok0);
+        }
         ++issued;
         if (++stage == C::STAGES) {
           stage = 0;
@@ -323,6 +406,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
       uint32_t stage = 0, phase = 0;
+      uint32_t cst = 0, cph = 0;   // F8: converted-tile ring
       int seg = 0;
       bool ok = true;
       for (long long it = begin; it < end && ok; ++seg) {
@@ -336,24 +420,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns)) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns) ||
+              (F8 && !mbar_wait(&cfull[cst], cph, abort_flag, p.timeout_ns))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
-          const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
-          const uint32_t bl = smem_u32(sBl + stage * C::B_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * C::B_STAGE);
+          const uint32_t bl = smem_u32(sBl + stage * C::B_STAGE);
+          if (F8) {
+            // A: the converted tile in tensor memory, 8 columns per K = 16 step
+            const uint32_t at = tmem + static_cast<uint32_t>(C::A_COL + cst * C::A_TCOLS);
 #pragma unroll
-          for (int k = 0; k < BK / UK; ++k) {
-            const uint64_t ad = sdesc_k_sw128(a0 + k * UK * 2);
-            umma_bf16(d, ad, sdesc_k_sw128(b0 + k * UK * 2), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-            if (SPLIT) umma_bf16(d, ad, sdesc_k_sw128(bl + k * UK * 2), idesc, 1u);
+            for (int k = 0; k < C::BKI / UK; ++k) {
+              const uint32_t boff = (k / (BK / UK)) * C::B_BYTES + (k % (BK / UK)) * UK * 2;
+              umma_bf16_ts(d, at + k * (UK / 2), sdesc_k_sw128(b0 + boff), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+              if (SPLIT) umma_bf16_ts(d, at + k * (UK / 2), sdesc_k_sw128(bl + boff), idesc, 1u);
+            }
+          } else {
+            const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / UK; ++k) {
+              const uint64_t ad = sdesc_k_sw128(a0 + k * UK * 2);
+              umma_bf16(d, ad, sdesc_k_sw128(b0 + k * UK * 2), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+              if (SPLIT) umma_bf16(d, ad, sdesc_k_sw128(bl + k * UK * 2), idesc, 1u);
+            }
           }
           umma_commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
+          }
+          if (F8) {
+            umma_commit(&cempty[cst]);
+            if (++cst == C::CSTAGES) {
+              cst = 0;
+              cph ^= 1u;
+            }
           }
         }
         if (!ok) break;
@@ -366,6 +469,52 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         umma_commit(drain);   // all issued MMAs retire before TMEM is freed
         mbar_wait(drain, 0, nullptr, p.timeout_ns);
       }
+    }
+  } else if (F8 && warp >= 6) {
+    // ------------------------------------------------------------ FP8 weight converters
+    // Code tile: [128 rows][128 codes], 128-byte rows whose 16-byte chunk j
+    // sits at j ^ (row & 7) (TMA's 128-byte swizzle: eight consecutive rows
+    // read at one chunk column touch every bank once).  Warp w owns TMEM lane
+    // quarter w & 3: lane i converts row 32 (w & 3) + i and stores its 128
+    // bf16 values into 64 consecutive columns of its lane (lower k in the low
+    // half of each column), the A layout of the MMA.
+    const int qd = warp & 3, r = qd * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(qd * 32) << 16) + static_cast<uint32_t>(C::A_COL);
+    uint32_t stage = 0, phase = 0, cst = 0, cph = 0;
+    bool ok = true;
+    for (long long i = begin; i < end && ok; ++i) {
+      if (!mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns) ||
+          !mbar_wait(&cempty[cst], cph ^ 1u, abort_flag, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();   // the MMAs that read this TMEM tile have completed
+      const uint8_t *row = sRaw + stage * C::RAW_BYTES + r * 128;
+      const uint32_t tcol = lane_base + static_cast<uint32_t>(cst * C::A_TCOLS);
+#pragma unroll
+      for (int j = 0; j < C::BKI / 16; ++j) {
+        const uint4 c = *reinterpret_cast<const uint4 *>(row + ((j ^ (r & 7)) << 4));
+        const uint2 a = e4m3x4_to_bf16x4(c.x), b = e4m3x4_to_bf16x4(c.y), e = e4m3x4_to_bf16x4(c.z),
+                    f = e4m3x4_to_bf16x4(c.w);
+        const uint32_t o[8] = {a.x, a.y, b.x, b.y, e.x, e.y, f.x, f.y};
+        tmem_st8_nw(tcol + j * 8, o);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cfull[cst]);
+      if (++stage == C::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      if (++cst == C::CSTAGES) {
+        cst = 0;
+        cph ^= 1u;
+      }
+    }
+    if (!ok) {
+      if (lane == 0) report(p.status, DFLASH_ERR_TIMEOUT);
+      *abort_flag = 1;
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -390,13 +539,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int rt = tile / p.tok_tiles;
       const int n = (rt % p.rtpg) * BM + r;                       // row within its group
       const size_t goff = static_cast<size_t>(rt / p.rtpg) * p.out_gstride;
+      const float *wsg = F8 ? p.wscale[rt / p.rtpg] : nullptr;
       const int tok0 = (tile % p.tok_tiles) * BN;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
       float v[16];
       if (kb0 == 0 && kb1 == p.kbpt) {
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
-          finalize(p, v, n, tok0 + c * 16, goff);
+          finalize(p, v, n, tok0 + c * 16, goff, wsg);
         }
         tc_fence_before();
         __syncwarp();
@@ -459,7 +609,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               }
             }
           }
-          finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff);   // n >= N: not this CTA's row
+          finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsg);   // n >= N: not this CTA's row
         }
       } else if (p.csk > 1) {
         // cluster split-K: this CTA's fp32 share into its own smem, row-major
@@ -541,7 +691,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               v[4 * i + 2] = acc[i].z;
               v[4 * i + 3] = acc[i].w;
             }
-            finalize(p, v, n, tok0 + c * 16, goff);
+            finalize(p, v, n, tok0 + c * 16, goff, wsg);
           }
         }
         epi_bar();
@@ -561,7 +711,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // rank order (deterministic); lanes hold consecutive rows (coalesced
     // stores, SwiGLU row pairs in neighbouring lanes)
     cluster_sync();
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 6) {   // the epilogue warps
       const int et = threadIdx.x - 64;
       const int rank = static_cast<int>(cluster_ctarank());
       const int r0 = rank * BM / p.csk, rows = (rank + 1) * BM / p.csk - r0;
@@ -569,6 +719,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int tile = first_tile;
       const int rt = tile / p.tok_tiles;
       const size_t goff = static_cast<size_t>(rt / p.rtpg) * p.out_gstride;
+      const float *wsg = F8 ? p.wscale[rt / p.rtpg] : nullptr;
       const int tokt = (tile % p.tok_tiles) * BN;
       const float *sp = reinterpret_cast<const float *>(sA);
       for (int t0 = 0; t0 < tasks; t0 += 128) {   // every thread takes each round (shuffles in SwiGLU)
@@ -592,27 +743,59 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
         const int n = valid ? (rt % p.rtpg) * BM + row : p.N;   // n >= N: nothing stored
-        finalize(p, v, n, tokt + grp * 16, goff);
+        finalize(p, v, n, tokt + grp * 16, goff, wsg);
       }
     }
     cluster_sync();   // nobody leaves while others still read its share
   }
 }
 
-template <int BN, bool SPLIT>
-int launch(const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const CUtensorMap &tXl, const Params &p) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, SPLIT>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN, SPLIT>::SMEM),
+// Kernel attributes (dynamic shared memory, and the whole unified L1 /
+// shared array as shared memory so that two small-tile CTAs can be
+// resident per SM) set once; returns the CTAs of the variant resident per SM
+// by registers and shared memory, or a negative error code.
+template <int BN, bool SPLIT, bool F8>
+int setup() {
+  using C = Cfg<BN, SPLIT, F8>;
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, SPLIT, F8>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
                            "gemm smem attribute"))
       return e;
-    attr_done = true;
+    if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, SPLIT, F8>,
+                                                cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                cudaSharedmemCarveoutMaxShared),
+                           "gemm carveout attribute"))
+      return e;
+    // resident CTAs per SM from the kernel's registers and shared memory
+    cudaFuncAttributes fa = {};
+    int dev = 0, smem_sm = 0, resv = 0;
+    if (int e = cuda_check(cudaFuncGetAttributes(&fa, gemm_tc_kernel<BN, SPLIT, F8>), "gemm attributes")) return e;
+    if (int e = cuda_check(cudaGetDevice(&dev), "device")) return e;
+    if (int e = cuda_check(cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev),
+                           "shared memory per SM"))
+      return e;
+    if (int e = cuda_check(cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev),
+                           "reserved shared memory"))
+      return e;
+    const int warp_regs = ((fa.numRegs * 32 + 255) / 256) * 256;   // allocated per warp in 256-register units
+    const int by_regs = 65536 / (warp_regs * (C::NT / 32));
+    const int by_smem = smem_sm / (C::SMEM + resv);
+    const int n = std::min(std::min(by_regs, by_smem), 2048 / C::NT);
+    per_sm = n > 0 ? n : 1;
   }
+  return per_sm;
+}
+
+template <int BN, bool SPLIT, bool F8>
+int launch(const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const CUtensorMap &tXl, const Params &p) {
+  using C = Cfg<BN, SPLIT, F8>;
+  if (int e = setup<BN, SPLIT, F8>(); e < 0) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.G);
-  cfg.blockDim = dim3(NTHREADS);
-  cfg.dynamicSmemBytes = Cfg<BN, SPLIT>::SMEM;
+  cfg.blockDim = dim3(C::NT);
+  cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = lc.stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -623,22 +806,44 @@ int launch(const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const CUten
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, SPLIT>, tW, tX, tXl, p), "gemm launch");
+  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, SPLIT, F8>, tW, tX, tXl, p), "gemm launch");
 }
 
-template <bool SPLIT>
+template <bool SPLIT, bool F8>
 int launch_bn(int BN, const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const CUtensorMap &tXl,
               const Params &p) {
   switch (BN) {
-    case 16: return launch<16, SPLIT>(lc, tW, tX, tXl, p);
-    case 32: return launch<32, SPLIT>(lc, tW, tX, tXl, p);
-    case 64: return launch<64, SPLIT>(lc, tW, tX, tXl, p);
-    case 128: return launch<128, SPLIT>(lc, tW, tX, tXl, p);
-    default: return launch<256, SPLIT>(lc, tW, tX, tXl, p);
+    case 16: return launch<16, SPLIT, F8>(lc, tW, tX, tXl, p);
+    case 32: return launch<32, SPLIT, F8>(lc, tW, tX, tXl, p);
+    case 64: return launch<64, SPLIT, F8>(lc, tW, tX, tXl, p);
+    case 128: return launch<128, SPLIT, F8>(lc, tW, tX, tXl, p);
+    default: return launch<F8 ? 128 : 256, SPLIT, F8>(lc, tW, tX, tXl, p);   // FP8 tiles stop at 128
+  }
+}
+
+// CTAs of the variant resident per SM (for the decomposition), or < 0.
+template <bool SPLIT, bool F8>
+int per_sm_of(int BN) {
+  switch (BN) {
+    case 16: return setup<16, SPLIT, F8>();
+    case 32: return setup<32, SPLIT, F8>();
+    case 64: return setup<64, SPLIT, F8>();
+    case 128: return setup<128, SPLIT, F8>();
+    default: return setup<F8 ? 128 : 256, SPLIT, F8>();
   }
 }
 
 }  // namespace
+
+int e4m3_to_bf16(const Launch &lc, const void *codes, int n, void *out) {
+  if (n <= 0 || n % 4 || !codes || !out || (reinterpret_cast<uintptr_t>(codes) & 3) ||
+      (reinterpret_cast<uintptr_t>(out) & 7))
+    return set_error(DFLASH_ERR_ARG, "e4m3_to_bf16: n must be a positive multiple of 4, buffers aligned");
+  const int n4 = n / 4;
+  e4m3_to_bf16_kernel<<<(n4 + 255) / 256, 256, 0, lc.stream>>>(static_cast<const uint32_t *>(codes), n4,
+                                                               static_cast<uint2 *>(out));
+  return cuda_check(cudaGetLastError(), "e4m3_to_bf16 launch");
+}
 
 int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   const int M = op.M, N = op.N, K = op.K;
@@ -647,7 +852,9 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   if ((!op.W && op.n_groups <= 1) || !op.X || !op.out) return set_error(DFLASH_ERR_ARG, "gemm %s: null operand", name);
   const uintptr_t al = reinterpret_cast<uintptr_t>(op.W) | reinterpret_cast<uintptr_t>(op.X) |
                        reinterpret_cast<uintptr_t>(op.X_lo);
-  if ((al & 15) || (op.ldw * 2) % 16 || (op.ldx * 2) % 16)
+  const bool f8 = op.w_fp8;
+  const int wbytes = f8 ? 1 : 2;   // bytes per weight element
+  if ((al & 15) || (op.ldw * wbytes) % 16 || (op.ldx * 2) % 16)
     return set_error(DFLASH_ERR_ALIGN, "gemm %s: operands / row strides must be 16-byte aligned", name);
   int epi = op.epi == EPI_STORE_T ? EPI_BF16 : op.epi;
   if (epi == EPI_F32_SPLIT && !op.out2) return set_error(DFLASH_ERR_ARG, "gemm %s: split output missing", name);
@@ -655,7 +862,8 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   // token tile: the smallest that covers M; with split activations at most
   // 128 so that a stage (weights + two activation tiles) still leaves a
   // 4-deep ring in shared memory
-  const int BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : (M <= 128 || split) ? 128 : 256;
+  // (FP8 weights: at most 128, so that the bf16 weight tiles fit in tensor memory beside the accumulators)
+  const int BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : (M <= 128 || split || f8) ? 128 : 256;
   Params p = {};
   p.M = M;
   p.N = N;
@@ -666,28 +874,38 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   p.rtpg = (N + BM - 1) / BM;
   p.out_gstride = op.out_gstride;
   p.tok_tiles = (M + BN - 1) / BN;
-  p.kbpt = (K + BK - 1) / BK;
+  const int bki = f8 ? 2 * BK : BK;   // k per ring stage
+  p.kbpt = (K + bki - 1) / bki;
   const long long tiles = static_cast<long long>(p.rtpg) * p.n_groups * p.tok_tiles;
   p.total = tiles * p.kbpt;
-  // CTAs: at most one per SM, at least 4 k-blocks each, and no tile cut into
-  // more pieces than keep its fixup (the last piece sums the others' fp32
-  // partials from L2) under 256 KB: 32 pieces at BN = 16, 4 at BN = 128
-  const int cap = lc.gemm_ctas > 0 ? lc.gemm_ctas : lc.num_sms;
+  // Resident CTA slots (the variant's occupancy, at most two per SM).  CTAs:
+  // one per SM (FP8 weights: one per slot, so that two threads issue MMAs
+  // on each SM), at least 4 k-blocks each, and no tile cut into more pieces
+  // than keep its fixup (the last piece sums the others' fp32 partials from
+  // L2) under 256 KB: 32 pieces at BN = 16, 4 at BN = 128
+  const int per_sm = f8 ? (split ? per_sm_of<true, true>(BN) : per_sm_of<false, true>(BN))
+                        : (split ? per_sm_of<true, false>(BN) : per_sm_of<false, false>(BN));
+  if (per_sm < 0) return per_sm;
+  const int slots = std::min(per_sm, 2) * lc.num_sms;
+  const int cap = lc.gemm_ctas > 0 ? lc.gemm_ctas : (f8 ? slots : lc.num_sms);
   const int max_parts = std::max(2, (256 * 1024) / (BM * BN * 4));
   const int min_kb = std::max(4, (p.kbpt + max_parts - 1) / max_parts);
   p.G = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, (p.total + min_kb - 1) / min_kb)));
-  // A few more tiles than SMs with small token tiles (two ~100 KB CTAs fit on
-  // one SM): one whole tile per CTA, some SMs running two.  Splitting them
-  // over one CTA per SM would cut nearly every tile in two and put a global
-  // fixup on the tail of a weight-streaming GEMM.
-  if (lc.gemm_ctas == 0 && BN <= 32 && tiles > cap && tiles <= 2LL * cap) p.G = static_cast<int>(tiles);
+  // More tiles than SMs but no more than the resident slots: one whole tile
+  // per CTA, some SMs running two.  Cutting them over the CTAs would split
+  // nearly every tile and put a global fixup on the tail of a
+  // weight-streaming GEMM.
+  if (lc.gemm_ctas == 0 && tiles > lc.num_sms && tiles <= slots) p.G = static_cast<int>(tiles);
   // Few tiles (at most half the SMs): cluster split-K instead, csk CTAs per
   // tile reducing through distributed shared memory - no global round trips
   // (fence, counter atomic, partial loads: ~2 us each here) on the GEMM's
   // tail.  The test hook (gemm_ctas) keeps stream-K.
   p.csk = 1;
   if (lc.gemm_ctas == 0 && tiles * 2 <= cap) {
-    long long s = std::min<long long>(std::min<long long>(8, cap / tiles), p.kbpt);
+    // at most 8 CTAs, and about 8 k-blocks or more each (short ranges are
+    // all pipeline fill; at least 2-way where the k-range allows)
+    long long s = std::min<long long>(std::min<long long>(8, cap / tiles),
+                                      std::min<long long>(p.kbpt, std::max<long long>(2, p.kbpt / 8)));
     // SwiGLU pairs rows 2i / 2i+1 in neighbouring lanes: row ranges must be
     // even-aligned, so a power-of-two cluster there
     if (epi == EPI_SWIGLU)
@@ -705,6 +923,12 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   p.out2_lo = op.out2_lo;
   p.ldo2 = op.ldo2;
   p.bias = op.bias;
+  if (f8) {
+    for (int g = 0; g < p.n_groups; ++g) {
+      p.wscale[g] = p.n_groups > 1 ? op.wscale_g[g] : op.wscale;
+      if (!p.wscale[g]) return set_error(DFLASH_ERR_ARG, "gemm %s: FP8 weights without row scales", name);
+    }
+  }
   p.partials = sc.partials;
   p.counters = sc.counters;
   p.status = lc.status;
@@ -716,8 +940,11 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   for (int g = 0; g < p.n_groups; ++g) {
     const void *Wg = p.n_groups > 1 ? op.Wg[g] : op.W;
     if (!Wg) return set_error(DFLASH_ERR_ARG, "gemm %s: null weight group %d", name, g);
-    if (int e = make_tmap_2d(&tW.m[g], Wg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N,
-                             static_cast<uint64_t>(op.ldw) * 2, BK, BM))
+    // FP8 codes: [128 rows][128 codes] tiles, 128-byte swizzle
+    if (int e = f8 ? make_tmap_2d(&tW.m[g], Wg, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, N, static_cast<uint64_t>(op.ldw),
+                                  2 * BK, BM)
+                   : make_tmap_2d(&tW.m[g], Wg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N,
+                                  static_cast<uint64_t>(op.ldw) * 2, BK, BM))
       return e;
   }
   if (int e = make_tmap_2d(&tX, op.X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M, static_cast<uint64_t>(op.ldx) * 2,
@@ -737,8 +964,10 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
                            : epi == EPI_SWIGLU                       ? (op.out_lo ? 2.0 : 1.0) * M * N
                                                                      : (op.out_lo ? 4.0 : 2.0) * M * N;
   const double ng = p.n_groups;
-  ProfScope ps(lc, name, ng * (2.0 * N * K + out_bytes) + xb, ng * (split ? 4.0 : 2.0) * M * N * K);
-  return split ? launch_bn<true>(BN, lc, tW, tX, tXl, p) : launch_bn<false>(BN, lc, tW, tX, tXl, p);
+  ProfScope ps(lc, name, ng * (wbytes * static_cast<double>(N) * K + (f8 ? 4.0 * N : 0.0) + out_bytes) + xb,
+               ng * (split ? 4.0 : 2.0) * M * N * K);
+  if (f8) return split ? launch_bn<true, true>(BN, lc, tW, tX, tXl, p) : launch_bn<false, true>(BN, lc, tW, tX, tXl, p);
+  return split ? launch_bn<true, false>(BN, lc, tW, tX, tXl, p) : launch_bn<false, false>(BN, lc, tW, tX, tXl, p);
 }
 
 }  // namespace dflash

@@ -46,6 +46,11 @@ struct GemmOp {
   int n_groups = 1;
   const void *Wg[16] = {};
   size_t out_gstride = 0;
+  // FP8 weights: W / Wg hold E4M3 codes (ldw in bytes = elements); row n of
+  // the result is scaled by wscale[n] (grouped: wscale_g[g][n])
+  bool w_fp8 = false;
+  const float *wscale = nullptr;
+  const float *wscale_g[16] = {};
 };
 
 // Per-launch timing of kernel families (dflash_profile_begin / _end).
@@ -91,10 +96,14 @@ struct GemmScratch {
 int set_error(int code, const char *fmt, ...);
 int cuda_check(cudaError_t e, const char *what);
 
-// TMA descriptor of a row-major 2-D tensor [rows][cols] with 128-byte
-// swizzle; box = box_cols x box_rows.
+// The FP8 GEMM's E4M3 -> bf16 conversion over n codes (test hook).
+int e4m3_to_bf16(const Launch &lc, const void *codes, int n, void *out);
+
+// TMA descriptor of a row-major 2-D tensor [rows][cols] (128-byte swizzle
+// unless told otherwise); box = box_cols x box_rows.
 int make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elt_bytes, uint64_t cols,
-                 uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows);
+                 uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows,
+                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 // bf16 operands on tcgen05 tensor cores.
 int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc);

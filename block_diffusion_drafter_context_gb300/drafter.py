@@ -17,6 +17,10 @@ def _torch():
     return torch
 
 
+def _is_fp8(a) -> bool:
+    return hasattr(a, "codes") and hasattr(a, "scale")
+
+
 def to_device(a, device="cuda"):
     """numpy -> device tensor; uint16 arrays are bf16 bit patterns."""
     torch = _torch()
@@ -46,6 +50,7 @@ def make_config(cfg) -> B.dflash_config:
     c.mask_id = int(cfg.mask_id)
     c.rope_base = float(cfg.rope_base)
     c.eps = float(cfg.eps)
+    c.weight_fp8 = int(bool(getattr(cfg, "weight_fp8", False)))
     return c
 
 
@@ -54,24 +59,48 @@ CONV_SITES = ("pre_attn", "post_attn", "pre_ffn", "post_ffn")
 
 def upload_weights(cfg, W: dict, device="cuda") -> dict:
     """Upload a weight dict (layout of the synthetic generator) and pack it:
-    w_qkv = [w_q; w_k; w_v] rows; w_gu rows interleaved gate_i, up_i."""
+    w_qkv = [w_q; w_k; w_v] rows; w_gu rows interleaved gate_i, up_i.  FP8
+    weights upload their codes (uint8) and put the row scales under s_*."""
     torch = _torch()
-    d = lambda a: to_device(a, device)
+
+    def d(a):
+        if _is_fp8(a):
+            return torch.from_numpy(a.codes).to(device)
+        return to_device(a, device)
+
+    def sc(a):
+        return torch.from_numpy(a.scale).to(device) if _is_fp8(a) else None
+
+    def rows_cat(parts):
+        return torch.cat(parts, 0).contiguous()
+
+    def interleave(a, b):
+        return torch.stack([a, b], 1).reshape(2 * a.shape[0], *a.shape[1:]).contiguous()
+
     out = {k: d(W[k]) for k in ("w_fc", "g_fc", "embed", "lm_head", "g_final")}
+    fp8 = _is_fp8(W["lm_head"])
+    if fp8:
+        out["s_fc"], out["s_lm_head"] = sc(W["w_fc"]), sc(W["lm_head"])
     out["layers"] = []
     for lw in W["layers"]:
         gate, up = d(lw["w_gate"]), d(lw["w_up"])
         L = {
             "g_attn": d(lw["g_attn"]),
-            "w_qkv": torch.cat([d(lw["w_q"]), d(lw["w_k"]), d(lw["w_v"])], 0).contiguous(),
+            "w_qkv": rows_cat([d(lw["w_q"]), d(lw["w_k"]), d(lw["w_v"])]),
             "g_q": d(lw["g_q"]), "g_k": d(lw["g_k"]), "w_o": d(lw["w_o"]), "g_ffn": d(lw["g_ffn"]),
-            "w_gu": torch.stack([gate, up], 1).reshape(2 * gate.shape[0], gate.shape[1]).contiguous(),
+            "w_gu": interleave(gate, up),
             "w_down": d(lw["w_down"]),
         }
         del gate, up
+        if fp8:
+            L["s_qkv"] = rows_cat([sc(lw["w_q"]), sc(lw["w_k"]), sc(lw["w_v"])])
+            L["s_o"], L["s_down"] = sc(lw["w_o"]), sc(lw["w_down"])
+            L["s_gu"] = interleave(sc(lw["w_gate"]), sc(lw["w_up"]))
         if "conv" in lw:
             L["w_conv"] = [d(lw["conv"][s][0]) for s in CONV_SITES]
             L["b_conv"] = [d(lw["conv"][s][1]) for s in CONV_SITES]
+            if fp8:
+                L["s_conv"] = [sc(lw["conv"][s][0]) for s in CONV_SITES]
         out["layers"].append(L)
     if "sel" in W:
         s = W["sel"]
@@ -90,9 +119,17 @@ def make_weights_struct(dw: dict):
             for j in range(4):
                 s.w_conv[j] = L["w_conv"][j].data_ptr()
                 s.b_conv[j] = L["b_conv"][j].data_ptr()
+                if "s_conv" in L:
+                    s.s_conv[j] = L["s_conv"][j].data_ptr()
+        for k in ("s_qkv", "s_o", "s_gu", "s_down"):
+            if k in L:
+                setattr(s, k, L[k].data_ptr())
     w = B.dflash_weights()
     for k in ("w_fc", "g_fc", "embed", "lm_head", "g_final"):
         setattr(w, k, dw[k].data_ptr())
+    for k in ("s_fc", "s_lm_head"):
+        if k in dw:
+            setattr(w, k, dw[k].data_ptr())
     w.layers = lay
     if "sel" in dw:
         w.sel_e256 = dw["sel"]["e256"].data_ptr()

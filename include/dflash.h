@@ -102,6 +102,15 @@ typedef struct dflash_config {
   int page_size;         /* KV page size in tokens: 64                       */
   float rope_base;       /* RoPE base (1e6)                                  */
   float eps;             /* RMSNorm epsilon (1e-6)                           */
+  int weight_fp8;        /* [DF2] engine flag "Draft quantization: enabled":
+                            every GEMM weight (w_fc, w_qkv, w_o, w_gu, w_down,
+                            w_conv, lm_head) is E4M3 codes (OCP FP8, 1 byte,
+                            row stride = K bytes, a multiple of 16) with one
+                            fp32 scale per output row in the s_* pointers:
+                            W[n][k] = s[n] * e4m3(code[n][k]).  NaN codes
+                            are invalid.  Activations stay bf16 (bf16 dtype
+                            only); the embedding and selector tables stay
+                            in dtype.                                       */
 } dflash_config;
 
 /* Per-layer weights (device pointers, not owned). */
@@ -118,6 +127,12 @@ typedef struct dflash_layer_weights {
                             sites pre_attn, post_attn, pre_ffn, post_ffn;
                             rows 0..H/16-1 = current tap, H/16.. = previous */
   const float *b_conv[4];/* [H/8] their biases                               */
+  /* weight_fp8 only: fp32 per-output-row scales of the matrices above */
+  const float *s_qkv;    /* [(nq+2nkv)*d]                                     */
+  const float *s_o;      /* [H]                                               */
+  const float *s_gu;     /* [2F], interleaved like w_gu                       */
+  const float *s_down;   /* [H]                                               */
+  const float *s_conv[4];/* [H/8]                                             */
 } dflash_layer_weights;
 
 /* Model weights (device pointers, not owned; the layer array is host memory
@@ -134,6 +149,8 @@ typedef struct dflash_weights {
   const void *sel_b;     /* [r, sel_dim] projection of the current token     */
   const float *sel_w_g;  /* [H] context-gate weights                         */
   float sel_b_g;         /* context-gate bias                                */
+  const float *s_fc;     /* weight_fp8 only: [H] row scales of w_fc          */
+  const float *s_lm_head;/* weight_fp8 only: [V] row scales of lm_head       */
 } dflash_weights;
 
 /* Paged drafter KV cache (device memory, not owned, zero-filled when
@@ -307,6 +324,11 @@ DFLASH_API int dflash_profile_end(dflash_ctx *ctx, dflash_kernel_stat *out, int 
  * timeout path without any fault. */
 DFLASH_API int dflash_debug_wait_flag(const int32_t *flag, unsigned long long timeout_ns,
                            void *workspace, dflash_stream_t stream);
+
+/* Test hook: the FP8 GEMM's own E4M3 -> bf16 weight conversion (the device
+ * function its converter warps run) applied to n codes.
+ *   codes: device uint8 [n], n > 0 a multiple of 4; out: device bf16 [n]. */
+DFLASH_API int dflash_debug_e4m3_to_bf16(const void *codes, int n, void *out, dflash_stream_t stream);
 
 /* Allocation-free top-16, for callers that cannot allocate device memory:
  * e.g. engine plugin hooks that are handed only their input and output

@@ -50,8 +50,26 @@ import numpy as np
 # --------------------------------------------------------------------------
 # storage decode
 # --------------------------------------------------------------------------
+def e4m3_decode(codes) -> np.ndarray:
+    """OCP FP8 E4M3 codes -> float64, from the format's definition (OFP8
+    specification, E4M3: sign bit, 4 exponent bits with bias 7, 3 mantissa
+    bits, no infinities).  Normal (E >= 1): (-1)^S * 2^(E-7) * (1 + M/8);
+    subnormal (E = 0): (-1)^S * 2^-6 * M/8; S.1111.111 is NaN."""
+    c = np.asarray(codes).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((e == 15) & ((c & 7) == 7), np.nan, mag)
+    return sign * mag
+
+
 def f64(a) -> np.ndarray:
-    """Stored input -> float64.  uint16 arrays hold bf16 bit patterns."""
+    """Stored input -> float64.  uint16 arrays hold bf16 bit patterns; an FP8
+    weight (E4M3 codes with one scale per row, "draft quantization") is
+    scale[n] * e4m3(codes[n][k])."""
+    if hasattr(a, "codes") and hasattr(a, "scale"):
+        return e4m3_decode(a.codes) * np.asarray(a.scale, dtype=np.float64)[:, None]
     a = np.asarray(a)
     if a.dtype == np.uint16:
         return (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)

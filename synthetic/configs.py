@@ -18,6 +18,8 @@ C4  27B-class drafter (hidden 5120, 40 q / 8 kv heads, FFN 17408), 64
 C1S5, C2S5  C1 and C2 run at a runtime block size of 5 (anchor + 4 mask
     positions), the engine-flag example of the DFlash-2 page; the drafter is
     unchanged (trained at 16, run at a smaller block).
+C1F8, C2F8, C3F8  C1 / C2 / C3 with FP8 (E4M3, per-row scale) drafter
+    weights: the "draft quantization" engine flag of the same page.
 
 Small test-only workloads (``T*``) use ragged sizes (hidden 320, vocab 1000,
 contexts that end mid-page, an empty context) so that every kernel sees
@@ -54,6 +56,9 @@ class DrafterConfig:
     # Needed where the DFlash-2 conv coefficients amplify bf16 rounding of the
     # activations past the 2% bound; plain bf16 activations elsewhere.
     split_act: bool = False
+    # FP8 E4M3 GEMM weights with per-row fp32 scales (weight-only: the
+    # activations stay bf16); the engine flag "draft quantization"
+    weight_fp8: bool = False
     rope_base: float = 1e6
     eps: float = 1e-6
     page_size: int = 64
@@ -132,6 +137,14 @@ WORKLOADS = {
                                  use_conv=True, use_selector=True, split_act=True),
                    batch=8, ctx_lo=4096, ctx_hi=4096, seed=3),
     "C4": Workload("C4", CLASS_27B, batch=64, ctx_lo=16384, ctx_hi=32768, seed=4, kv_fill="template"),
+    # FP8 drafter weights
+    "C1F8": Workload("C1F8", replace(QWEN3_8B_SHAPED, name="qwen3-8b-shaped-fp8", weight_fp8=True),
+                     batch=1, ctx_lo=2048, ctx_hi=2048, seed=1),
+    "C2F8": Workload("C2F8", replace(QWEN3_8B_SHAPED, name="qwen3-8b-shaped-fp8", weight_fp8=True),
+                     batch=32, ctx_lo=1024, ctx_hi=8192, p_accept=_decay(0.9, 0.5), seed=2),
+    "C3F8": Workload("C3F8", replace(QWEN3_8B_SHAPED, name="qwen3-8b-shaped-dflash2-fp8", use_conv=True,
+                                     use_selector=True, split_act=True, weight_fp8=True),
+                     batch=8, ctx_lo=4096, ctx_hi=4096, seed=3),
     # runtime block size 5
     "C1S5": Workload("C1S5", replace(QWEN3_8B_SHAPED, name="qwen3-8b-shaped-block5", block=5),
                      batch=1, ctx_lo=2048, ctx_hi=2048, seed=1),
@@ -154,6 +167,13 @@ WORKLOADS = {
     "T0D2S7": Workload("T0D2S7", replace(TINY_F32, name="tiny-f32-dflash2-block7", use_conv=True,
                                          use_selector=True, block=7),
                        batch=2, ctx_lo=0, ctx_hi=0, explicit_ctx=(31, 90), seed=15),
+    # FP8 weights: bf16 (every code planted in layer-0 W_q row 0 and LM-head
+    # row 0) and DFlash-2 with split activations at block size 7
+    "T1F8": Workload("T1F8", replace(SMALL_BF16, name="small-bf16-fp8", weight_fp8=True),
+                     batch=3, ctx_lo=0, ctx_hi=0, explicit_ctx=(0, 100, 777), p_accept=_decay(0.9, 0.5), seed=17),
+    "T1D2F8": Workload("T1D2F8", replace(SMALL_BF16, name="small-bf16-dflash2-fp8", use_conv=True,
+                                         use_selector=True, split_act=True, weight_fp8=True, block=7),
+                       batch=3, ctx_lo=0, ctx_hi=0, explicit_ctx=(5, 64, 300), seed=18),
     "T1D2S2": Workload("T1D2S2", replace(SMALL_BF16, name="small-bf16-dflash2-block2", use_conv=True,
                                          use_selector=True, split_act=True, block=2),
                        batch=3, ctx_lo=0, ctx_hi=0, explicit_ctx=(1, 64, 200), seed=16),

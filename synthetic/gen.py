@@ -13,7 +13,9 @@ alone.
 
 Storage: bf16 matrices are returned as ``uint16`` arrays of bf16 bit
 patterns (round-to-nearest-even from the fp32 draw); fp32 configs return
-``float32`` arrays.  Norm gains and biases are always ``float32``.
+``float32`` arrays.  Norm gains and biases are always ``float32``.  With
+``weight_fp8`` the GEMM weight matrices are ``FP8Weight`` objects: OCP FP8
+E4M3 codes with one fp32 scale per row, quantised from the fp32 draw.
 """
 from __future__ import annotations
 
@@ -71,6 +73,71 @@ def normal(shape, std: float, seed: int, name: str, dtype: str = "f32") -> np.nd
         with ThreadPoolExecutor(_threads()) as ex:
             list(ex.map(work, range(nchunks)))
     return out.reshape(shape)
+
+
+class FP8Weight:
+    """A weight matrix W[n][k] = scale[n] * e4m3(codes[n][k]) (OCP FP8 E4M3
+    codes, one fp32 scale per row).  A container only: decoding belongs to
+    whoever consumes the weights."""
+
+    def __init__(self, codes: np.ndarray, scale: np.ndarray):
+        self.codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        self.scale = np.ascontiguousarray(scale, dtype=np.float32)
+        assert self.codes.ndim == 2 and self.scale.shape == (self.codes.shape[0],)
+
+    @property
+    def shape(self):
+        return self.codes.shape
+
+
+def _e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """Nearest E4M3 code (ties to even) of fp32 values with |x| <= 448.
+    Normal range (|x| >= 2^-6): round the fp32 mantissa to 3 bits and re-bias
+    the exponent (127 -> 7); below it, multiples of 2^-9 (subnormal codes)."""
+    x = np.asarray(x, dtype=np.float32)
+    u = x.view(np.uint32)
+    sign = ((u >> np.uint32(24)) & np.uint32(0x80)).astype(np.uint8)
+    mag = u & np.uint32(0x7FFFFFFF)
+    # normal: round to 3 mantissa bits, nearest even
+    r = mag + np.uint32(0x7FFFF) + ((mag >> np.uint32(20)) & np.uint32(1))
+    e = (r >> np.uint32(23)).astype(np.int32) - 127 + 7
+    m = ((r >> np.uint32(20)) & np.uint32(7)).astype(np.int32)
+    normal_code = np.minimum((e << 3) | m, 0x7E)
+    # subnormal: |x| / 2^-9 rounded to the nearest integer, ties to even (8 = 2^-6, the first normal code)
+    sub_code = np.rint(np.abs(x).astype(np.float64) * 512.0).astype(np.int32)
+    code = np.where(mag >= np.uint32(0x3C800000), normal_code, sub_code)   # 0x3C800000 = 2^-6
+    return (code.astype(np.uint8) | sign).astype(np.uint8)
+
+
+def quantize_fp8_rows(w: np.ndarray, plant_all_codes: bool = False) -> FP8Weight:
+    """Per-row E4M3 quantisation of a weight matrix (stored bf16 bits or fp32):
+    scale[n] = max_k |w[n][k]| / 448, codes = nearest E4M3 of w / scale.
+    plant_all_codes: row 0 starts with every finite code (0x00..0x7E,
+    0x80..0xFE), so that a kernel meets each one (needs K >= 254)."""
+    w = np.asarray(w)
+    wf = bf16_bits_to_f32(w) if w.dtype == np.uint16 else np.asarray(w, dtype=np.float32)
+    amax = np.abs(wf).max(axis=1)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    codes = np.empty(wf.shape, dtype=np.uint8)
+    step = max(1, (1 << 24) // max(1, wf.shape[1]))
+
+    def work(r0: int) -> None:
+        r1 = min(wf.shape[0], r0 + step)
+        x = np.clip(wf[r0:r1] / scale[r0:r1, None], -448.0, 448.0).astype(np.float32)
+        codes[r0:r1] = _e4m3_encode(x)
+
+    starts = list(range(0, wf.shape[0], step))
+    if len(starts) <= 1:
+        for r0 in starts:
+            work(r0)
+    else:
+        with ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(work, starts))
+    if plant_all_codes:
+        allc = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+        assert wf.shape[1] >= len(allc)
+        codes[0, :len(allc)] = allc
+    return FP8Weight(codes, scale)
 
 
 def gain(n: int, seed: int, name: str) -> np.ndarray:
@@ -136,6 +203,18 @@ def make_weights(cfg, seed: int) -> dict:
             "w_g": normal((H,), H ** -0.5, seed, "sel.w_g"),
             "b_g": np.float32(0.1),
         }
+    if getattr(cfg, "weight_fp8", False):
+        # every GEMM weight as E4M3 codes + row scales; the embedding and the
+        # selector tables stay in dtype.  Small shapes plant every code into
+        # row 0 of the first layer's W_q and of the LM head.
+        plant = cfg.hidden >= 254
+        W["w_fc"] = quantize_fp8_rows(W["w_fc"])
+        W["lm_head"] = quantize_fp8_rows(W["lm_head"], plant_all_codes=plant and cfg.vocab <= 4096)
+        for l, lw in enumerate(W["layers"]):
+            for k in ("w_q", "w_k", "w_v", "w_o", "w_gate", "w_up", "w_down"):
+                lw[k] = quantize_fp8_rows(lw[k], plant_all_codes=plant and l == 0 and k == "w_q")
+            if "conv" in lw:
+                lw["conv"] = {s: (quantize_fp8_rows(w), b) for s, (w, b) in lw["conv"].items()}
     return W
 
 

@@ -54,6 +54,8 @@ int main(void) {
   O(dflash_config, rope_base) O(dflash_config, eps) O(dflash_config, page_size) O(dflash_config, split_act)
   O(dflash_layer_weights, w_conv) O(dflash_layer_weights, b_conv)
   O(dflash_weights, layers) O(dflash_weights, sel_b_g) O(dflash_kv, num_pages) O(dflash_kernel_stat, ms)
+  O(dflash_config, weight_fp8) O(dflash_layer_weights, s_qkv) O(dflash_layer_weights, s_conv)
+  O(dflash_weights, s_fc) O(dflash_weights, s_lm_head)
   return 0;
 }
 """
@@ -80,6 +82,11 @@ int main(void) {
         "dflash_weights.sel_b_g": B.dflash_weights.sel_b_g.offset,
         "dflash_kv.num_pages": B.dflash_kv.num_pages.offset,
         "dflash_kernel_stat.ms": B.dflash_kernel_stat.ms.offset,
+        "dflash_config.weight_fp8": B.dflash_config.weight_fp8.offset,
+        "dflash_layer_weights.s_qkv": B.dflash_layer_weights.s_qkv.offset,
+        "dflash_layer_weights.s_conv": B.dflash_layer_weights.s_conv.offset,
+        "dflash_weights.s_fc": B.dflash_weights.s_fc.offset,
+        "dflash_weights.s_lm_head": B.dflash_weights.s_lm_head.offset,
     }
     for k, v in py.items():
         assert int(got[k]) == v, k
@@ -101,6 +108,8 @@ def _cfg(**kw):
     (dict(top_k=8), -4), (dict(page_size=32), -4), (dict(hidden=250), -2),
     (dict(n_kv_heads=3), -2), (dict(head_dim=96), -4), (dict(mask_id=5000), -1), (dict(dtype=7), -1),
     (dict(use_selector=1, sel_rank=100), -4),
+    (dict(weight_fp8=1, dtype=1), -4),                 # FP8 weights: bf16 path only
+    (dict(weight_fp8=1, ffn=520), -2),                 # FP8 code rows must be 16-byte multiples
 ])
 def test_create_rejects_bad_configs_without_touching_the_gpu(lib, kw, code):
     w = B.dflash_weights()

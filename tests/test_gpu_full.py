@@ -1,6 +1,7 @@
 """Parity at the full sizes of the benchmark workloads.
 
-C1 (batch 1, context 2048) is checked whole.  C2 (32 ragged requests,
+C1 (batch 1, context 2048) is checked whole, with bf16 and with FP8
+weights.  C2 (32 ragged requests,
 contexts 1k-8k), C3 (DFlash-2, 8 requests x 4096) and C4 (27B-class, 64
 requests x 16k-32k, ~32 GB of draft KV) run whole on the GPU and are checked
 on sampled requests the oracle computes one by one (every request is
@@ -41,7 +42,7 @@ def check_requests(c, requests, kv_positions=64):
             assert rel_err(to_np(scores)[b], s_ref) <= 1e-4
             path = O.greedy_path(s_ref, ids[b])
             p = 0
-            for j in range(15):
+            for j in range(c.cfg.block - 1):
                 row = np.sort(s_ref[j, p])[::-1]
                 if row[0] - row[1] < 1e-3:
                     break
@@ -55,6 +56,20 @@ def check_requests(c, requests, kv_positions=64):
 def test_c1_full():
     c = Case("C1")
     check_requests(c, [0], kv_positions=2048)
+    c.dr.close()
+
+
+def test_c1_fp8_weights_full():
+    """C1 with FP8 (E4M3, per-row scale) drafter weights: the oracle decodes
+    the same codes, so the bar is the bf16 one."""
+    c = Case("C1F8")
+    check_requests(c, [0], kv_positions=2048)
+    c.dr.close()
+
+
+def test_c3_fp8_dflash2_sampled():
+    c = Case("C3F8", per_request=True)
+    check_requests(c, [0, c.B - 1])
     c.dr.close()
 
 

@@ -30,7 +30,7 @@ def case(name, **kw):
 
 
 # ----------------------------------------------------------------- injection
-@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2", "T1S5"])
+@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2", "T1S5", "T1F8", "T1D2F8"])
 def test_inject_matches_oracle(name):
     c = case(name)
     assert c.dr.status() == 0
@@ -54,7 +54,7 @@ def _gap_ok(vals_sorted, i, thr=1e-3):
     return min(lo, hi) >= thr
 
 
-@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2", "T1S5", "T0D2S7", "T1D2S2"])
+@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2", "T1S5", "T0D2S7", "T1D2S2", "T1F8", "T1D2F8"])
 def test_draft_matches_oracle(name):
     c = case(name)
     out = c.draft()
@@ -81,7 +81,7 @@ def test_draft_matches_oracle(name):
                         assert ids[b, j, r] == ref["cand_ids"][j, r], (b, j, r)
 
 
-@pytest.mark.parametrize("name", ["T0D2", "T1D2", "T1", "T0D2S7", "T1D2S2"])
+@pytest.mark.parametrize("name", ["T0D2", "T1D2", "T1", "T0D2S7", "T1D2S2", "T1D2F8"])
 def test_select_path_matches_oracle(name):
     c = case(name)
     out = c.draft(want_logits=False)
@@ -151,7 +151,7 @@ def test_verify_random_against_oracle(S):
 
 
 # ----------------------------------------------------------------- the whole step
-@pytest.mark.parametrize("name", ["T1", "T1D2", "T1S5", "T1D2S2"])
+@pytest.mark.parametrize("name", ["T1", "T1D2", "T1S5", "T1D2S2", "T1F8"])
 def test_step_is_lossless_and_verify_matches_oracle(name):
     import torch
     c = case(name)
@@ -189,12 +189,13 @@ def test_stateless_isolated_and_cache_untouched():
         assert torch.equal(p[key][1:], a[key][1:]), key
 
 
-def test_single_request_views_match_oracle():
+@pytest.mark.parametrize("name", ["T1", "T1F8"])
+def test_single_request_views_match_oracle(name):
     """Each request drafted alone (batch 1 through a view of its page-table
     row: 16-token GEMM tiles, cluster split-K with pushed shares, cluster-mode
     attention) matches the oracle like the batched call does."""
     import types
-    c = case("T1")
+    c = case(name)
     tol = TOL[c.cfg.dtype]
     for b in range(c.B):
         view = types.SimpleNamespace(struct=c.kv.row(b))
@@ -235,10 +236,11 @@ def test_runtime_block_size_switch_matches_oracle():
         assert torch.equal(first[key], again[key]), key
 
 
-def test_split_kv_and_gemm_partition_do_not_change_results():
+@pytest.mark.parametrize("name", ["T1", "T1F8"])
+def test_split_kv_and_gemm_partition_do_not_change_results(name):
     import torch
     from block_diffusion_drafter_context_gb300 import binding as Bd
-    c = case("T1")
+    c = case(name)
     ref = c.draft()
     ref_l = to_np(ref["logits"])
     for split in (64, 128, 256):
@@ -266,3 +268,19 @@ def test_bounded_wait_reports_timeout_without_fault():
     Bd.dflash_debug_wait_flag(flag, 200_000_000, ws)
     assert Bd.dflash_read_status(ws) == 0
     torch.ones(1, device="cuda").sum().item()                 # context still usable
+
+
+def test_e4m3_conversion_matches_oracle_decode_for_every_code():
+    """The FP8 GEMM's code -> bf16 conversion over all 256 codes (the finite
+    ones exactly, including the subnormals and both zeros) against the
+    oracle's decode from the format definition."""
+    import torch
+    from block_diffusion_drafter_context_gb300 import binding as Bd
+    codes = torch.arange(256, dtype=torch.uint8, device="cuda")
+    out = torch.empty(256, dtype=torch.bfloat16, device="cuda")
+    Bd.dflash_debug_e4m3_to_bf16(codes, 256, out)
+    got = out.float().cpu().numpy().astype(np.float64)
+    ref = O.e4m3_decode(np.arange(256))
+    finite = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[finite], ref[finite])
+    assert (np.signbit(got[finite]) == np.signbit(ref[finite])).all()

@@ -626,3 +626,56 @@ def test_logit_scores_ignore_the_previous_choice():
     z = np.random.default_rng(24).normal(size=(15, 16))
     s = O.logit_scores(z)
     assert s.shape == (15, 16, 16) and (s == z[:, None, :]).all()
+
+
+# ------------------------------------------------------------------ FP8 drafter weights
+def test_e4m3_decode_golden_values():
+    g = json.load(open(os.path.join(GOLDEN, "e4m3_values.json")))
+    for c in g["cases"]:
+        got = float(O.e4m3_decode(np.array([int(c["code"], 16)]))[0])
+        if c["value"] == "nan":
+            assert math.isnan(got), c["code"]
+        else:
+            assert got == c["value"] and math.copysign(1.0, got) == math.copysign(1.0, c["value"]), c["code"]
+
+
+def test_e4m3_decode_structure():
+    pos = O.e4m3_decode(np.arange(0x7F))
+    assert (np.diff(pos) > 0).all()                       # codes 0x00..0x7E increase strictly
+    assert pos[0] == 0.0 and pos[1] == 2.0 ** -9 and pos[-1] == 448.0
+    # within one binade the step is the binade's 1/8; the subnormal step equals the first normal binade's
+    assert np.allclose(np.diff(pos[:17]), 2.0 ** -9)
+    neg = O.e4m3_decode(np.arange(0x80, 0xFF))
+    np.testing.assert_array_equal(neg, -pos)              # the sign bit only negates
+
+
+def test_fp8_quantizer_is_round_to_nearest_even():
+    """The generator's per-row quantiser against brute force over the oracle's
+    own decode table: every code is a nearest finite E4M3 value of w / scale,
+    ties to the even code."""
+    r = np.random.default_rng(40)
+    w = np.concatenate([r.standard_normal((6, 200)) * 10 ** r.uniform(-4, 0, (6, 1)),
+                        np.full((1, 200), 3.0)], 0).astype(np.float32)
+    w[0, :5] = [0.0, -0.0, 1e-9, -1e-9, 448.0]
+    q = gen.quantize_fp8_rows(w)
+    table = O.e4m3_decode(np.arange(256))
+    finite = np.array([c for c in range(256) if not np.isnan(table[c])])
+    for n in range(w.shape[0]):
+        assert q.scale[n] == np.float32(np.abs(w[n]).max() / np.float32(448.0))
+        x = w[n].astype(np.float64) / float(q.scale[n])
+        for k in range(w.shape[1]):
+            d = np.abs(table[finite] - x[k])
+            best = finite[d == d.min()]
+            c = int(q.codes[n, k])
+            assert c in best or (table[c] == 0.0 and (table[best] == 0.0).all()), (n, k, x[k], c)
+            if len(best) > 1 and not (table[best] == 0.0).all():
+                assert c % 2 == 0, (n, k)
+    # a row's largest magnitude maps to +-448 exactly
+    assert (np.abs(O.e4m3_decode(q.codes)).max(axis=1) == 448.0).all()
+
+
+def test_fp8_planted_row_holds_every_finite_code():
+    w = np.random.default_rng(41).standard_normal((3, 300)).astype(np.float32)
+    q = gen.quantize_fp8_rows(w, plant_all_codes=True)
+    codes = set(q.codes[0, :254].tolist())
+    assert codes == {c for c in range(256) if (c & 0x7F) != 0x7F}
