@@ -750,8 +750,8 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
   }
 }
 
-// Kernel attributes (dynamic shared memory, and the whole unified L1 /
-// shared array as shared memory so that two small-tile CTAs can be
+// Kernel attributes (dynamic shared memory; for small tiles the whole
+// unified L1 / shared array as shared memory so that two CTAs can be
 // resident per SM) set once; returns the CTAs of the variant resident per SM
 // by registers and shared memory, or a negative error code.
 template <int BN, bool SPLIT, bool F8>
@@ -763,11 +763,12 @@ int setup() {
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
                            "gemm smem attribute"))
       return e;
-    if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, SPLIT, F8>,
-                                                cudaFuncAttributePreferredSharedMemoryCarveout,
-                                                cudaSharedmemCarveoutMaxShared),
-                           "gemm carveout attribute"))
-      return e;
+    if (BN <= 32)   // small tiles: two CTAs per SM need the whole array as shared memory
+      if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, SPLIT, F8>,
+                                                  cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                  cudaSharedmemCarveoutMaxShared),
+                             "gemm carveout attribute"))
+        return e;
     // resident CTAs per SM from the kernel's registers and shared memory
     cudaFuncAttributes fa = {};
     int dev = 0, smem_sm = 0, resv = 0;

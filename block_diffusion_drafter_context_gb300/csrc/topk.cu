@@ -66,16 +66,28 @@ __global__ void __launch_bounds__(WARPS * 32) topk_kernel(const float *__restric
   const int lo = c * chunk, hi = min(V, lo + chunk);
   uint64_t list = 0, thr = 0;
   if ((V & 3) == 0) {
-    // lo is a multiple of 4 (chunk is), so float4 loads stay aligned
-    for (int wb = lo + warp * 128; wb < hi; wb += WARPS * 128) {   // warp-uniform trip count
-      const int base = wb + lane * 4;
-      float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      const bool in = base < hi;   // hi is a multiple of 4: the whole float4 is in range
-      if (in) v = __ldcs(reinterpret_cast<const float4 *>(x + base));
-      offer(list, thr, in ? make_key(v.x, base) : 0, lane);
-      offer(list, thr, in ? make_key(v.y, base + 1) : 0, lane);
-      offer(list, thr, in ? make_key(v.z, base + 2) : 0, lane);
-      offer(list, thr, in ? make_key(v.w, base + 3) : 0, lane);
+    // lo is a multiple of 4 (chunk is), so float4 loads stay aligned.  U
+    // loads per lane are issued before any is offered: one HBM latency per
+    // U x 512 bytes of a warp instead of one per 512 (the offers are cheap
+    // once the list has filled, so the scan is bound by bytes in flight).
+    constexpr int U = 8;
+    for (int wb = lo + warp * 128; wb < hi; wb += WARPS * 128 * U) {   // warp-uniform trip count
+      float4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int base = wb + u * WARPS * 128 + lane * 4;
+        v[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (base < hi) v[u] = __ldcs(reinterpret_cast<const float4 *>(x + base));   // hi: a multiple of 4
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int base = wb + u * WARPS * 128 + lane * 4;
+        const bool in = base < hi;
+        offer(list, thr, in ? make_key(v[u].x, base) : 0, lane);
+        offer(list, thr, in ? make_key(v[u].y, base + 1) : 0, lane);
+        offer(list, thr, in ? make_key(v[u].z, base + 2) : 0, lane);
+        offer(list, thr, in ? make_key(v[u].w, base + 3) : 0, lane);
+      }
     }
   } else {
     for (int base = lo + warp * 32 + lane; base - lane < hi; base += WARPS * 32) {
