@@ -75,14 +75,22 @@ __device__ __forceinline__ float4 scale4(float4 a, float r, float4 g) {
 }
 __device__ __forceinline__ float dot4(float4 a) { return a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w; }
 
-// cos / sin of pos * theta_i, theta_i = hi + lo (host-computed in fp64)
+// cos / sin of pos * theta_i, theta_i = hi + lo (host-computed in fp64), all
+// in fp32 (this GPU's fp64 rate is a small fraction of fp32's): the product
+// pos * hi is split exactly into prod + err by one FMA, whole turns are
+// removed from prod with 2 pi in three parts (Cody-Waite: 6.28125 has few
+// significant bits; the rest in two fp32 terms), and the small terms are
+// added back.  Angle error below 4e-7 rad for positions up to 2^17.
 __device__ __forceinline__ void rope_cs(int pos, float th_hi, float th_lo, float &c, float &s) {
-  const double p = static_cast<double>(pos);
-  double a = fma(p, static_cast<double>(th_lo), p * static_cast<double>(th_hi));
-  const double k = rint(a * 0.15915494309189533577);          // a / (2 pi)
-  a = fma(-k, 6.283185307179586232, a);                        // 2 pi, high part
-  a = fma(-k, 2.4492935982947064e-16, a);                      // 2 pi, low part
-  sincosf(static_cast<float>(a), &s, &c);
+  const float p = static_cast<float>(pos);        // exact below 2^24
+  const float prod = p * th_hi;
+  const float err = fmaf(p, th_hi, -prod);        // p * th_hi = prod + err exactly
+  const float tail = fmaf(p, th_lo, err);
+  const float k = rintf(prod * 0.15915494309189535f);   // whole turns
+  float r = fmaf(-k, 6.28125f, prod);
+  r = fmaf(-k, 1.9353072e-3f, r);
+  r = fmaf(-k, 1.0253132e-11f, r);
+  sincosf(r + tail, &s, &c);
 }
 
 // ------------------------------------------------------------------ embed
@@ -210,6 +218,27 @@ struct RopeArgs {
   float th_hi[64], th_lo[64];
 };
 
+// This lane's angles theta_{lane + 32 i}, i < N, from the parameter table.
+// Kernel parameters indexed by lane serialise the constant bank (one access
+// per distinct address, each a possible miss); uniform reads broadcast, so
+// the warp walks the table uniformly and each lane keeps its entries.
+template <int N>
+__device__ __forceinline__ void lane_thetas(const RopeArgs &rp, int lane, float (&hi)[N], float (&lo)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) hi[i] = lo[i] = 0.f;
+#pragma unroll 4
+  for (int k = 0; k < 32; ++k) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const float h = rp.th_hi[k + 32 * i], l = rp.th_lo[k + 32 * i];
+      if (lane == k) {
+        hi[i] = h;
+        lo[i] = l;
+      }
+    }
+  }
+}
+
 // qkv: fp32 [B*S][(nq+2nkv)*d] (S = block size).  One warp per (token,
 // head).  q heads -> q_out [B*S][nq*d]; k heads -> bk [B][nkv][64][d]
 // (normed, rotated); v heads -> bv [B][nkv][d][64], transposed like the V
@@ -253,11 +282,12 @@ __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, 
 #pragma unroll
     for (int i = 0; i < DPL; ++i) v[i] *= r * g[lane + 32 * i];
   }
-  float o[DPL];
+  float o[DPL], th_hi[DPL / 2], th_lo[DPL / 2];
+  lane_thetas(rp, lane, th_hi, th_lo);
 #pragma unroll
   for (int i = 0; i < DPL / 2; ++i) {   // pairs (lane + 32i, lane + 32i + D/2)
     float c, s;
-    rope_cs(pos, rp.th_hi[lane + 32 * i], rp.th_lo[lane + 32 * i], c, s);
+    rope_cs(pos, th_hi[i], th_lo[i], c, s);
     const float x1 = v[i], x2 = v[i + DPL / 2];
     o[i] = x1 * c - x2 * s;
     o[i + DPL / 2] = x2 * c + x1 * s;
@@ -331,11 +361,12 @@ __global__ void __launch_bounds__(256) inject_scatter_kernel(const ScatterArgs a
 #pragma unroll
       for (int i = 0; i < DPL; ++i) v[i] *= r * a.g_k[l][lane + 32 * i];
     }
-    float o[DPL];
+    float o[DPL], th_hi[DPL / 2], th_lo[DPL / 2];
+    lane_thetas(rp, lane, th_hi, th_lo);
 #pragma unroll
     for (int i = 0; i < DPL / 2; ++i) {
       float c, s;
-      rope_cs(pos, rp.th_hi[lane + 32 * i], rp.th_lo[lane + 32 * i], c, s);
+      rope_cs(pos, th_hi[i], th_lo[i], c, s);
       o[i] = v[i] * c - v[i + DPL / 2] * s;
       o[i + DPL / 2] = v[i + DPL / 2] * c + v[i] * s;
     }
