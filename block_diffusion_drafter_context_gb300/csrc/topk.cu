@@ -54,6 +54,21 @@ __device__ __forceinline__ void offer(uint64_t &list, uint64_t &thr, uint64_t ke
   }
 }
 
+// The 16th largest of the 32 lanes' values (a warp-wide descending bitonic
+// sort; every lane gets the result).
+__device__ __forceinline__ float warp_16th_largest(float v, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, v, j);
+      const bool up = ((lane & k) == 0) == ((lane & j) == 0);   // this lane keeps the larger
+      v = up ? fmaxf(v, o) : fminf(v, o);
+    }
+  }
+  return __shfl_sync(0xffffffffu, v, K - 1);
+}
+
 __global__ void __launch_bounds__(WARPS * 32) topk_kernel(const float *__restrict__ logits, int V, int chunk,
                                                           int nchunks, int32_t *ids, float *vals,
                                                           uint64_t *part, int *counters) {
@@ -79,14 +94,27 @@ __global__ void __launch_bounds__(WARPS * 32) topk_kernel(const float *__restric
         v[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         if (base < hi) v[u] = __ldcs(reinterpret_cast<const float4 *>(x + base));   // hi: a multiple of 4
       }
+      // Exact pre-filter while the list fills (thr = 0, warp-uniform): 16
+      // lanes hold a maximum >= tau, so the warp's 16 largest of these values
+      // are all >= tau and only those are offered (the one-at-a-time inserts
+      // are the expensive part of the scan).  Once the list is full its 16th
+      // key filters on its own.
+      float tau = -INFINITY;
+      if (thr == 0) {
+        float lmax = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          lmax = fmaxf(lmax, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));   // out of range: -inf
+        tau = warp_16th_largest(lmax, lane);
+      }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int base = wb + u * WARPS * 128 + lane * 4;
         const bool in = base < hi;
-        offer(list, thr, in ? make_key(v[u].x, base) : 0, lane);
-        offer(list, thr, in ? make_key(v[u].y, base + 1) : 0, lane);
-        offer(list, thr, in ? make_key(v[u].z, base + 2) : 0, lane);
-        offer(list, thr, in ? make_key(v[u].w, base + 3) : 0, lane);
+        offer(list, thr, in && v[u].x >= tau ? make_key(v[u].x, base) : 0, lane);
+        offer(list, thr, in && v[u].y >= tau ? make_key(v[u].y, base + 1) : 0, lane);
+        offer(list, thr, in && v[u].z >= tau ? make_key(v[u].z, base + 2) : 0, lane);
+        offer(list, thr, in && v[u].w >= tau ? make_key(v[u].w, base + 3) : 0, lane);
       }
     }
   } else {
@@ -98,8 +126,11 @@ __global__ void __launch_bounds__(WARPS * 32) topk_kernel(const float *__restric
   if (lane < K) sm[warp * K + lane] = list;
   __syncthreads();
   if (warp == 0) {
-    uint64_t l2 = 0, t2 = 0;
-    for (int i = lane; i < WARPS * K; i += 32) offer(l2, t2, sm[i], lane);
+    // every warp list alone has 16 keys >= its 16th: the merged 16th is at
+    // least the largest of those, and smaller keys need not be offered
+    uint64_t l2 = 0, t2 = 0, floor2 = 0;
+    for (int w = 0; w < WARPS; ++w) floor2 = sm[w * K + K - 1] > floor2 ? sm[w * K + K - 1] : floor2;
+    for (int i = lane; i < WARPS * K; i += 32) offer(l2, t2, sm[i] >= floor2 ? sm[i] : 0, lane);
     if (nchunks == 1) {
       if (lane < K) {
         ids[row * K + lane] = key_id(l2);
@@ -117,8 +148,21 @@ __global__ void __launch_bounds__(WARPS * 32) topk_kernel(const float *__restric
       }
       __syncwarp();
       if (last) {
-        uint64_t l3 = 0, t3 = 0;
-        for (int i = lane; i < nchunks * K; i += 32) offer(l3, t3, __ldcg(&part[static_cast<size_t>(row) * nchunks * K + i]), lane);
+        const uint64_t *pr = part + static_cast<size_t>(row) * nchunks * K;
+        uint64_t l3 = 0, t3 = 0, floor3 = 0;
+        for (int c2 = lane; c2 < nchunks; c2 += 32) {   // the largest 16th key of the chunk lists
+          const uint64_t k16 = __ldcg(&pr[c2 * K + K - 1]);
+          floor3 = k16 > floor3 ? k16 : floor3;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const uint64_t t = __shfl_xor_sync(0xffffffffu, floor3, o);
+          floor3 = t > floor3 ? t : floor3;
+        }
+        for (int i = lane; i < nchunks * K; i += 32) {
+          const uint64_t k = __ldcg(&pr[i]);
+          offer(l3, t3, k >= floor3 ? k : 0, lane);
+        }
         if (lane < K) {
           ids[row * K + lane] = key_id(l3);
           vals[row * K + lane] = key_value(l3);
