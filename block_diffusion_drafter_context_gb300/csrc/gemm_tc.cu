@@ -9,11 +9,15 @@
 //   * swap-AB: the weight tile is the 128-row UMMA "M" operand, the token
 //     tile (BN = 16..256 rows) the "N" operand; the accumulator sits in TMEM
 //     as [weight row = lane][token = column];
-//   * stream-K: the (tile, 64-wide k-block) iteration space is cut into one
-//     contiguous range per CTA, one persistent CTA per SM, so a GEMM with 32
-//     row tiles still keeps all SMs streaming.  A tile split across CTAs is
-//     finished by whichever CTA completes it last (per-tile counter), which
-//     sums the fp32 partials in CTA order - deterministic, no spin-waits;
+//   * decomposition, chosen per launch on the host: cluster split-K when the
+//     GEMM has at most half as many tiles as CTA slots (the CTAs of one
+//     thread-block cluster split a tile's k-range and reduce on chip through
+//     distributed shared memory); one whole tile per CTA when there are more
+//     tiles than SMs but no more than slots; otherwise stream-K: the (tile,
+//     k-block) iteration space is cut into one contiguous range per CTA, and
+//     a tile split across CTAs is finished by whichever CTA completes it last
+//     (per-tile counter), which sums the fp32 partials in CTA order -
+//     deterministic, no spin-waits;
 //   * warp roles: warp 0 issues TMA loads into a STAGES-deep ring of
 //     128-byte-swizzled tiles, warp 1 owns TMEM and issues tcgen05.mma from
 //     one thread, warps 2-5 drain TMEM (double-buffered) into the epilogue;
