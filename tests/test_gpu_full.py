@@ -73,6 +73,14 @@ def test_c3_fp8_dflash2_sampled():
     c.dr.close()
 
 
+def test_c2s5_runtime_block_size_sampled():
+    """C2 at the runtime block size 5: 32 ragged requests, shortest and longest checked."""
+    c = Case("C2S5", per_request=True)
+    order = np.argsort(c.ctx)
+    check_requests(c, [int(order[0]), int(order[-1])])
+    c.dr.close()
+
+
 def test_c2_ragged_sampled():
     c = Case("C2", per_request=True)
     assert to_np(c.ctx_d).tolist() == c.ctx.tolist()
