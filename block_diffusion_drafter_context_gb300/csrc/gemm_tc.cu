@@ -227,6 +227,18 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
   return r;
 }
 
+// EPI_ADD_F32 for 16 token columns whose residual values r were loaded
+// earlier (before the accumulator was ready): out = r + scale * v.
+__device__ __forceinline__ void finalize_add_pre(const Params &p, float (&v)[16], const float (&r)[16], int n,
+                                                 int tok0, size_t goff, const float *ws) {
+  const bool nok = n < p.N;
+  const float sc = ws && nok ? ws[n] : 1.f;
+  float *o = static_cast<float *>(p.out);
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if (nok && tok0 + i < p.M) o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] = r[i] + sc * v[i];
+}
+
 __global__ void e4m3_to_bf16_kernel(const uint32_t *codes, int n4, uint2 *out) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n4) out[i] = e4m3x4_to_bf16x4(codes[i]);
@@ -532,6 +544,26 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
       const int kb0 = static_cast<int>(it % p.kbpt);
       const int kb1 = static_cast<int>((kb0 + (end - it) < p.kbpt ? kb0 + (end - it) : p.kbpt));
       const int buf = seg & 1;
+      // One 16-token column group with a residual add: load the residual of
+      // the row this thread will finalise (whole tile, or its own rows of a
+      // cluster split-K tile) while the MMAs still run - one L2 round trip
+      // off the GEMM's tail.
+      float rpre[16];
+      bool have_pre = false;
+      if (BN == 16 && p.epi == EPI_ADD_F32) {
+        const bool whole_t = kb0 == 0 && kb1 == p.kbpt;
+        const bool owner = C::PUSH && p.csk > 1 && ((r + 1) * p.csk - 1) / BM == static_cast<int>(cluster_ctarank());
+        if (whole_t || owner) {
+          const int rt0 = tile / p.tok_tiles;
+          const int n0 = (rt0 % p.rtpg) * BM + r, t0 = (tile % p.tok_tiles) * BN;
+          const size_t g0 = static_cast<size_t>(rt0 / p.rtpg) * p.out_gstride;
+          const float *o = static_cast<const float *>(p.out);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            rpre[i] = (n0 < p.N && t0 + i < p.M) ? __ldcg(o + g0 + static_cast<size_t>(t0 + i) * p.ldo + n0) : 0.f;
+          have_pre = true;
+        }
+      }
       const bool got = mbar_wait(&tfull[buf], static_cast<uint32_t>((seg >> 1) & 1), abort_flag, p.timeout_ns);
       // one uniform decision for all 128 epilogue threads (they meet at named barriers below)
       if (bar_or(1, 128, !got || *abort_flag)) {
@@ -550,7 +582,10 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
       if (kb0 == 0 && kb1 == p.kbpt) {
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
-          finalize(p, v, n, tok0 + c * 16, goff, wsg);
+          if (have_pre)
+            finalize_add_pre(p, v, rpre, n, tok0 + c * 16, goff, wsg);
+          else
+            finalize(p, v, n, tok0 + c * 16, goff, wsg);
         }
         tc_fence_before();
         __syncwarp();
@@ -613,7 +648,10 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
               }
             }
           }
-          finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsg);   // n >= N: not this CTA's row
+          if (have_pre && mine)
+            finalize_add_pre(p, v, rpre, n, tok0 + c * 16, goff, wsg);
+          else
+            finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsg);   // n >= N: not this CTA's row
         }
       } else if (p.csk > 1) {
         // cluster split-K: this CTA's fp32 share into its own smem, row-major
