@@ -903,18 +903,11 @@ int attention_bf16(const Launch &lc, const AttnArgs &a) {
   if (a.partial_slots < 2ull * grid) return set_error(DFLASH_ERR_SHAPE, "bf16 attention: partial scratch too small");
   if (static_cast<size_t>(a.B) * a.nkv > a.counter_cap)
     return set_error(DFLASH_ERR_SHAPE, "bf16 attention: batch x kv heads over the counter capacity");
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (int e = cuda_check(cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                SMEM),
-                           "attention smem attribute"))
-      return e;
-    if (int e = cuda_check(cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                SMEM),
-                           "attention smem attribute"))
-      return e;
-    attr_done = true;
-  }
+  // set on every call: per device, idempotent, a host call (no stream work)
+  if (int e = cuda_check(cudaFuncSetAttribute(g <= 4 ? attn_tc_kernel<true> : attn_tc_kernel<false>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM),
+                         "attention smem attribute"))
+    return e;
   CUtensorMap tQ, tK, tV, tBK, tBV;
   const uint64_t kv_pages = static_cast<uint64_t>(a.num_pages) * a.nkv;
   const uint64_t bkv = static_cast<uint64_t>(a.B) * a.nkv;

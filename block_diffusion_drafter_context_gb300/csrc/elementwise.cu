@@ -249,11 +249,18 @@ template <typename T, int DPL>
 __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, int nkv, int S, const float *g_q,
                                                       const float *g_k, int qk_norm, float eps, const RopeArgs rp,
                                                       const int32_t *ctx_len, T *q_out, T *bk, T *bv) {
-  pdl_start();
   constexpr int D = DPL * 32;
   const int tok = blockIdx.x, b = tok / S, j = tok % S;
   const int head = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int nh = nq + 2 * nkv;
+  // the norm gain and this lane's angles are weights: read before the wait
+  // for the projections, off the dependent chain
+  const bool is_q = head < nq, normed = qk_norm && head < nq + nkv;
+  float gn[DPL], th_hi[DPL / 2], th_lo[DPL / 2];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) gn[i] = normed ? (is_q ? g_q : g_k)[lane + 32 * i] : 1.f;
+  lane_thetas(rp, lane, th_hi, th_lo);
+  pdl_start();
   if (head >= nh) return;
   const float *src = qkv + static_cast<size_t>(tok) * nh * D + static_cast<size_t>(head) * D;
   float v[DPL];
@@ -271,19 +278,16 @@ __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, 
       for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + (c - j) + static_cast<size_t>(lane + 32 * i) * 64, 0.f);
     return;
   }
-  const bool is_q = head < nq;
   const int pos = ctx_len[b] + j;
   if (qk_norm) {
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < DPL; ++i) ss += v[i] * v[i];
     const float r = rsqrtf(warp_sum(ss) / D + eps);
-    const float *g = is_q ? g_q : g_k;
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) v[i] *= r * g[lane + 32 * i];
+    for (int i = 0; i < DPL; ++i) v[i] *= r * gn[i];
   }
-  float o[DPL], th_hi[DPL / 2], th_lo[DPL / 2];
-  lane_thetas(rp, lane, th_hi, th_lo);
+  float o[DPL];
 #pragma unroll
   for (int i = 0; i < DPL / 2; ++i) {   // pairs (lane + 32i, lane + 32i + D/2)
     float c, s;

@@ -42,6 +42,7 @@
 #include "internal.h"
 
 #include <algorithm>
+#include <atomic>
 
 namespace dflash {
 namespace {
@@ -797,38 +798,52 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
 // resident per SM) set once; returns the CTAs of the variant resident per SM
 // by registers and shared memory, or a negative error code.
 template <int BN, bool SPLIT, bool F8>
-int setup() {
+int setup_device(int dev) {
   using C = Cfg<BN, SPLIT, F8>;
-  static int per_sm = 0;
-  if (per_sm == 0) {
+  if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, SPLIT, F8>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
+                         "gemm smem attribute"))
+    return e;
+  if (BN <= 32)   // small tiles: two CTAs per SM need the whole array as shared memory
     if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, SPLIT, F8>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
-                           "gemm smem attribute"))
+                                                cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                cudaSharedmemCarveoutMaxShared),
+                           "gemm carveout attribute"))
       return e;
-    if (BN <= 32)   // small tiles: two CTAs per SM need the whole array as shared memory
-      if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, SPLIT, F8>,
-                                                  cudaFuncAttributePreferredSharedMemoryCarveout,
-                                                  cudaSharedmemCarveoutMaxShared),
-                             "gemm carveout attribute"))
-        return e;
-    // resident CTAs per SM from the kernel's registers and shared memory
-    cudaFuncAttributes fa = {};
-    int dev = 0, smem_sm = 0, resv = 0;
-    if (int e = cuda_check(cudaFuncGetAttributes(&fa, gemm_tc_kernel<BN, SPLIT, F8>), "gemm attributes")) return e;
-    if (int e = cuda_check(cudaGetDevice(&dev), "device")) return e;
-    if (int e = cuda_check(cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev),
-                           "shared memory per SM"))
-      return e;
-    if (int e = cuda_check(cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev),
-                           "reserved shared memory"))
-      return e;
-    const int warp_regs = ((fa.numRegs * 32 + 255) / 256) * 256;   // allocated per warp in 256-register units
-    const int by_regs = 65536 / (warp_regs * (C::NT / 32));
-    const int by_smem = smem_sm / (C::SMEM + resv);
-    const int n = std::min(std::min(by_regs, by_smem), 2048 / C::NT);
-    per_sm = n > 0 ? n : 1;
+  // resident CTAs per SM from the kernel's registers and shared memory
+  cudaFuncAttributes fa = {};
+  int smem_sm = 0, resv = 0;
+  if (int e = cuda_check(cudaFuncGetAttributes(&fa, gemm_tc_kernel<BN, SPLIT, F8>), "gemm attributes")) return e;
+  if (int e = cuda_check(cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev),
+                         "shared memory per SM"))
+    return e;
+  if (int e = cuda_check(cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev),
+                         "reserved shared memory"))
+    return e;
+  const int warp_regs = ((fa.numRegs * 32 + 255) / 256) * 256;   // allocated per warp in 256-register units
+  const int by_regs = 65536 / (warp_regs * (C::NT / 32));
+  const int by_smem = smem_sm / (C::SMEM + resv);
+  const int n = std::min(std::min(by_regs, by_smem), 2048 / C::NT);
+  return n > 0 ? n : 1;
+}
+
+// Per device, once (attributes are per device; concurrent first calls only
+// repeat the same idempotent setup): CTAs of the variant resident per SM, or
+// a negative error code.
+template <int BN, bool SPLIT, bool F8>
+int setup() {
+  constexpr int MAX_DEV = 64;
+  static std::atomic<int> per_dev[MAX_DEV];
+  int dev = 0;
+  if (int e = cuda_check(cudaGetDevice(&dev), "device")) return e;
+  if (dev < 0 || dev >= MAX_DEV) return set_error(DFLASH_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, MAX_DEV);
+  int v = per_dev[dev].load(std::memory_order_acquire);
+  if (v == 0) {
+    v = setup_device<BN, SPLIT, F8>(dev);
+    if (v < 0) return v;
+    per_dev[dev].store(v, std::memory_order_release);
   }
-  return per_sm;
+  return v;
 }
 
 template <int BN, bool SPLIT, bool F8>
