@@ -101,14 +101,14 @@ __global__ void __launch_bounds__(ROW_THREADS) embed_rmsnorm_kernel(const T *emb
                                                                     int mask_id, int vocab, const float *gain,
                                                                     float eps, int H, int S, float *x, T *u, T *u_lo,
                                                                     int *status) {
-  pdl_start();
+  // Every input is the caller's (anchor ids, complete before any kernel of
+  // this call starts) or a weight: all loads before the wait for the
+  // previous kernel; the stores (x, u) after it.
   __shared__ float red[32];
   const int row = blockIdx.x, b = row / S, j = row % S;
   int id = j == 0 ? anchor[b] : mask_id;
-  if (id < 0 || id >= vocab) {
-    if (threadIdx.x == 0) report(status, DFLASH_ERR_DEVICE);
-    id = 0;
-  }
+  const bool bad = id < 0 || id >= vocab;
+  if (bad) id = 0;
   const T *e = embed + static_cast<size_t>(id) * H;
   const int nv = H >> 2;
   float4 v[MAXV], g[MAXV];
@@ -121,6 +121,8 @@ __global__ void __launch_bounds__(ROW_THREADS) embed_rmsnorm_kernel(const T *emb
       g[k] = ld4(gain + 4 * i);
     }
   }
+  pdl_start();
+  if (bad && threadIdx.x == 0) report(status, DFLASH_ERR_DEVICE);
 #pragma unroll
   for (int k = 0; k < MAXV; ++k) {
     const int i = threadIdx.x + k * ROW_THREADS;
@@ -146,7 +148,6 @@ __global__ void __launch_bounds__(ROW_THREADS) embed_rmsnorm_kernel(const T *emb
 template <typename T>
 __global__ void __launch_bounds__(ROW_THREADS) rmsnorm_kernel(const float *x, int H, const float *gain, float eps,
                                                               int S, T *out, T *out_lo, T *out_mask, T *out_mask_lo) {
-  pdl_start();
   __shared__ float red[32];
   const int row = blockIdx.x;
   const float *xr = x + static_cast<size_t>(row) * H;
@@ -154,12 +155,13 @@ __global__ void __launch_bounds__(ROW_THREADS) rmsnorm_kernel(const float *x, in
   float4 v[MAXV], g[MAXV];
   float ss = 0.f;
 #pragma unroll
+  for (int k = 0; k < MAXV; ++k)   // the gain is a weight: read before the wait (it may come from HBM)
+    if (threadIdx.x + k * ROW_THREADS < nv) g[k] = ld4(gain + 4 * (threadIdx.x + k * ROW_THREADS));
+  pdl_start();
+#pragma unroll
   for (int k = 0; k < MAXV; ++k) {
     const int i = threadIdx.x + k * ROW_THREADS;
-    if (i < nv) {
-      v[k] = ld4(xr + 4 * i);
-      g[k] = ld4(gain + 4 * i);
-    }
+    if (i < nv) v[k] = ld4(xr + 4 * i);
   }
 #pragma unroll
   for (int k = 0; k < MAXV; ++k)
@@ -185,21 +187,24 @@ template <typename T>
 __global__ void __launch_bounds__(ROW_THREADS) feature_norm_kernel(const float *in, int H, const float *gain,
                                                                    float eps, int apply, T *out, T *out_lo,
                                                                    const int32_t *ctx_in, int32_t *ctx_saved, int B) {
-  pdl_start();
   __shared__ float red[32];
   const int row = blockIdx.x;
-  if (row == 0)
-    for (int b = threadIdx.x; b < B; b += blockDim.x) ctx_saved[b] = ctx_in[b];
-  const float *xr = in + static_cast<size_t>(row) * H;
   const int nv = H >> 2;
   float4 v[MAXV], g[MAXV];
   float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k)   // the gain is a weight: read before the wait
+    if (threadIdx.x + k * ROW_THREADS < nv)
+      g[k] = apply ? ld4(gain + 4 * (threadIdx.x + k * ROW_THREADS)) : make_float4(1.f, 1.f, 1.f, 1.f);
+  pdl_start();
+  if (row == 0)
+    for (int b = threadIdx.x; b < B; b += blockDim.x) ctx_saved[b] = ctx_in[b];
+  const float *xr = in + static_cast<size_t>(row) * H;
 #pragma unroll
   for (int k = 0; k < MAXV; ++k) {
     const int i = threadIdx.x + k * ROW_THREADS;
     if (i < nv) {
       v[k] = ld4(xr + 4 * i);
-      g[k] = apply ? ld4(gain + 4 * i) : make_float4(1.f, 1.f, 1.f, 1.f);
       ss += dot4(v[k]);
     }
   }
