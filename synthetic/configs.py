@@ -174,6 +174,9 @@ WORKLOADS = {
     "T1D2F8": Workload("T1D2F8", replace(SMALL_BF16, name="small-bf16-dflash2-fp8", use_conv=True,
                                          use_selector=True, split_act=True, weight_fp8=True, block=7),
                        batch=3, ctx_lo=0, ctx_hi=0, explicit_ctx=(5, 64, 300), seed=18),
+    # 8 query heads per KV head (the attention's plain row layout) at block size 5
+    "T1G8S5": Workload("T1G8S5", replace(SMALL_BF16, name="small-bf16-g8-block5", n_q_heads=8, n_kv_heads=1, block=5),
+                       batch=3, ctx_lo=0, ctx_hi=0, explicit_ctx=(10, 64, 450), seed=19),
     "T1D2S2": Workload("T1D2S2", replace(SMALL_BF16, name="small-bf16-dflash2-block2", use_conv=True,
                                          use_selector=True, split_act=True, block=2),
                        batch=3, ctx_lo=0, ctx_hi=0, explicit_ctx=(1, 64, 200), seed=16),

@@ -54,7 +54,7 @@ def _gap_ok(vals_sorted, i, thr=1e-3):
     return min(lo, hi) >= thr
 
 
-@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2", "T1S5", "T0D2S7", "T1D2S2", "T1F8", "T1D2F8"])
+@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2", "T1S5", "T0D2S7", "T1D2S2", "T1F8", "T1D2F8", "T1G8S5"])
 def test_draft_matches_oracle(name):
     c = case(name)
     out = c.draft()
