@@ -679,3 +679,78 @@ def test_fp8_planted_row_holds_every_finite_code():
     q = gen.quantize_fp8_rows(w, plant_all_codes=True)
     codes = set(q.codes[0, :254].tolist())
     assert codes == {c for c in range(256) if (c & 0x7F) != 0x7F}
+
+
+def test_brute_force_micro_dflash2_layer_with_short_convs():
+    """Scalar-loop transcription of one DFlash-2 layer (the two-tap dynamic
+    short convolution at its four sites: on the normed input and on the
+    output of each sublayer, before the residual add; coefficients from the
+    site's own input, one group per 16 channels, nothing before position 0),
+    written from that reading, against the oracle's drafter forward."""
+    S = 5
+    cfg = micro_cfg(hidden=32, n_layers=1, n_q_heads=2, n_kv_heads=1, head_dim=8,
+                    ffn=20, vocab=12, rope_base=10000.0, block=S, use_conv=True)
+    W = f32_weights(cfg, 21)
+    n = 4
+    kv = rand_kv(cfg, n, 21)
+    anchor = 2
+    h, z = O.drafter_forward(cfg, W, kv, n, anchor)
+    F = lambda a: O.f64(a)
+    lw = W["layers"][0]
+    H, d, G = cfg.hidden, cfg.head_dim, cfg.hidden // 16
+
+    def rms(v, g):
+        ms = sum(t * t for t in v) / len(v)
+        return [v[i] / math.sqrt(ms + cfg.eps) * float(g[i]) for i in range(len(v))]
+
+    def mat(Wm, v):
+        Wm = F(Wm)
+        return [sum(Wm[o, i] * v[i] for i in range(len(v))) for o in range(Wm.shape[0])]
+
+    def conv(site, rows):
+        wc, bc = lw["conv"][site]
+        out = []
+        for j in range(S):
+            c = [math.tanh(t + float(b)) for t, b in zip(mat(wc, rows[j]), F(bc))]
+            prev = rows[j - 1] if j > 0 else [0.0] * H
+            out.append([rows[j][ch] + c[ch // 16] * rows[j][ch] + c[G + ch // 16] * prev[ch] for ch in range(H)])
+        return out
+
+    def rot(v, p):
+        out = list(v)
+        for i in range(d // 2):
+            th = p * cfg.rope_base ** (-2.0 * i / d)
+            out[i] = v[i] * math.cos(th) - v[i + d // 2] * math.sin(th)
+            out[i + d // 2] = v[i + d // 2] * math.cos(th) + v[i] * math.sin(th)
+        return out
+
+    E = F(W["embed"])
+    x = [list(E[anchor if j == 0 else cfg.mask_id]) for j in range(S)]
+    u = conv("pre_attn", [rms(x[j], lw["g_attn"]) for j in range(S)])
+    q = [[rot(rms(mat(lw["w_q"], u[j])[hh * d:(hh + 1) * d], lw["g_q"]), n + j) for hh in range(2)] for j in range(S)]
+    k = [rot(rms(mat(lw["w_k"], u[j]), lw["g_k"]), n + j) for j in range(S)]
+    v = [mat(lw["w_v"], u[j]) for j in range(S)]
+    keys = [list(kv[0][0][t, 0]) for t in range(n)] + k
+    vals = [list(kv[0][1][t, 0]) for t in range(n)] + v
+    att = []
+    for j in range(S):
+        o = []
+        for hh in range(2):
+            sc = [sum(q[j][hh][i] * kk[i] for i in range(d)) / math.sqrt(d) for kk in keys]
+            m = max(sc)
+            w = [math.exp(s - m) for s in sc]
+            o += [sum(w[t] * vals[t][i] for t in range(len(w))) / sum(w) for i in range(d)]
+        att.append(mat(lw["w_o"], o))
+    att = conv("post_attn", att)
+    x = [[x[j][i] + att[j][i] for i in range(H)] for j in range(S)]
+    uf = conv("pre_ffn", [rms(x[j], lw["g_ffn"]) for j in range(S)])
+    mm = []
+    for j in range(S):
+        gt, up = mat(lw["w_gate"], uf[j]), mat(lw["w_up"], uf[j])
+        mm.append(mat(lw["w_down"], [gt[i] / (1 + math.exp(-gt[i])) * up[i] for i in range(cfg.ffn)]))
+    mm = conv("post_ffn", mm)
+    x = [[x[j][i] + mm[j][i] for i in range(H)] for j in range(S)]
+    hb = [rms(x[j], W["g_final"]) for j in range(S)]
+    np.testing.assert_allclose(h, hb, rtol=1e-10, atol=1e-12)
+    zb = [mat(W["lm_head"], hb[j]) for j in range(1, S)]
+    np.testing.assert_allclose(z, zb, rtol=1e-10, atol=1e-11)
