@@ -754,3 +754,29 @@ def test_brute_force_micro_dflash2_layer_with_short_convs():
     np.testing.assert_allclose(h, hb, rtol=1e-10, atol=1e-12)
     zb = [mat(W["lm_head"], hb[j]) for j in range(1, S)]
     np.testing.assert_allclose(z, zb, rtol=1e-10, atol=1e-11)
+
+
+@pytest.mark.parametrize("S", [16, 5])
+def test_incremental_injection_equals_one_shot(S):
+    """A token's injected K/V depend only on its own feature and absolute
+    position, so a steady-state step (inject T new tokens after n cached
+    ones, then draft at n + T) equals injecting all n + T tokens at once and
+    drafting after them.  Pins the positions the step uses."""
+    cfg = micro_cfg(block=S)
+    W = f32_weights(cfg, 22)
+    r = np.random.default_rng(22)
+    n, T = 9, S
+    X = r.standard_normal((n + T, cfg.feat_in))
+    kv_prefix = O.inject_context(cfg, W, X[:n], np.arange(n))
+    target = np.zeros(S, dtype=np.int32)
+    step = O.drafting_step(cfg, W, kv_prefix, n, X[n:], 3, target)
+    kv_all = O.inject_context(cfg, W, X, np.arange(n + T))
+    ref = O.draft_request(cfg, W, kv_all, n + T, 3)
+    np.testing.assert_allclose(step["h"], ref["h"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(step["z"], ref["z"], rtol=1e-11, atol=1e-12)
+    assert step["draft"].tolist() == ref["draft"].tolist()
+    # and the positions matter: injecting the new tokens from position 0 changes the draft's inputs
+    wrong = O.inject_context(cfg, W, X[n:], np.arange(T))
+    kv_wrong = [(np.concatenate([k0, k1]), np.concatenate([v0, v1])) for (k0, v0), (k1, v1) in zip(kv_prefix, wrong)]
+    bad = O.draft_request(cfg, W, kv_wrong, n + T, 3)
+    assert np.abs(bad["h"] - ref["h"]).max() > 1e-6
