@@ -204,11 +204,12 @@ def block_attention(cfg, q, k_ctx, v_ctx, k_blk, v_blk) -> np.ndarray:
 # shared embedding and LM head), §3 item 1 (few layers)
 # --------------------------------------------------------------------------
 def drafter_forward(cfg, W, kv_ctx, n_ctx: int, anchor: int):
-    """One forward pass of the drafter over a block of S = 16 positions.
+    """One forward pass of the drafter over a block of S = cfg.block positions
+    (16, or a smaller runtime block size).
 
     Position 0 holds the clean anchor token ([DF] §2.3, anchor sampling
-    mirrors inference), positions 1..15 the mask token; the block sits at
-    absolute positions n_ctx .. n_ctx+15 after the injected context.
+    mirrors inference), positions 1..S-1 the mask token; the block sits at
+    absolute positions n_ctx .. n_ctx+S-1 after the injected context.
     kv_ctx: list over layers of (K [n_ctx, nkv, d], V [n_ctx, nkv, d]).
 
     Returns (h [S, H] final-normed hidden, z [S-1, V] logits of the mask
@@ -276,13 +277,13 @@ def context_gate(cfg, sel, h) -> np.ndarray:
 
 
 def pair_scores(cfg, sel, anchor: int, cand_ids, cand_logits, h) -> np.ndarray:
-    """Adjacent-pair scores s[j, p, c] for mask positions j = 1..15.
+    """Adjacent-pair scores s[j, p, c] for mask positions j = 1..J (J = S-1).
 
     score = drafter logit of candidate c + gate_j * (A e256[p]) . (B e256[c]),
     a low-rank bilinear compatibility on 256-d token embeddings under a
     context gate; p runs over the previous position's candidates (the anchor
     for the first mask position, repeated over the 16 rows).
-    cand_ids, cand_logits: [15, 16] -> s: [15, 16, 16] indexed [j-1, p, c]."""
+    cand_ids, cand_logits: [J, 16] -> s: [J, 16, 16] indexed [j-1, p, c]."""
     cand_ids = np.asarray(cand_ids, dtype=np.int64)
     zc = np.asarray(cand_logits, dtype=np.float64)
     e = sel["e256"]
@@ -290,8 +291,8 @@ def pair_scores(cfg, sel, anchor: int, cand_ids, cand_logits, h) -> np.ndarray:
     Bm = f64(sel["b"])
     gate = context_gate(cfg, sel, h)
     prev = np.vstack([np.full((1, cand_ids.shape[1]), int(anchor)), cand_ids[:-1]])
-    up = f64(np.asarray(e)[prev]) @ A.T          # [15, 16, r]
-    wc = f64(np.asarray(e)[cand_ids]) @ Bm.T     # [15, 16, r]
+    up = f64(np.asarray(e)[prev]) @ A.T          # [J, 16, r]
+    wc = f64(np.asarray(e)[cand_ids]) @ Bm.T     # [J, 16, r]
     bil = np.einsum("jpr,jcr->jpc", up, wc)
     return zc[:, None, :] + gate[:, None, None] * bil
 
@@ -299,7 +300,7 @@ def pair_scores(cfg, sel, anchor: int, cand_ids, cand_logits, h) -> np.ndarray:
 def greedy_path(scores, cand_ids) -> np.ndarray:
     """Greedy traversal over precomputed pair scores: at each position take
     the best continuation of the previously chosen candidate (ties to the
-    lower token id).  Returns draft ids [15]."""
+    lower token id).  Returns draft ids [J]."""
     s = np.asarray(scores, dtype=np.float64)
     cand_ids = np.asarray(cand_ids)
     J, K, _ = s.shape
@@ -318,7 +319,7 @@ def greedy_path(scores, cand_ids) -> np.ndarray:
 
 def select_path(cfg, W, anchor, cand_ids, cand_logits, h):
     """DFlash-2 mode: pair scores + greedy path.  Otherwise (DFlash-1): the
-    top-1 candidate per position.  Returns (draft [15], scores or None)."""
+    top-1 candidate per position.  Returns (draft [J], scores or None)."""
     cand_ids = np.asarray(cand_ids)
     if not cfg.use_selector:
         return cand_ids[:, 0].astype(np.int32), None
@@ -335,7 +336,7 @@ def verify_greedy(draft, target):
     tokens, then take the target's token at the first mismatch (the bonus);
     the rest is discarded.
 
-    draft: [15]; target: [16] -> (k accepted drafts, bonus, committed [16]
+    draft: [J]; target: [J+1] -> (k accepted drafts, bonus, committed [J+1]
     = target[0..k] followed by -1)."""
     draft = np.asarray(draft)
     target = np.asarray(target)
@@ -370,8 +371,8 @@ def sample_path(scores, cand_ids, temperature: float, uniforms):
     """Sampling over precomputed pair scores: at position j the draft
     distribution over the 16 candidates is q_j = softmax(s_j(c_{j-1}, .) / T)
     (c_0 = the anchor row), and c_j is drawn from it by inverse CDF in
-    candidate order with the uniform u_j.  scores [15, 16, 16] (rows indexed
-    by the previous candidate) -> (draft ids [15], q [15, 16], index [15])."""
+    candidate order with the uniform u_j.  scores [J, 16, 16] (rows indexed
+    by the previous candidate) -> (draft ids [J], q [J, 16], index [J])."""
     s = np.asarray(scores, dtype=np.float64)
     cand_ids = np.asarray(cand_ids)
     J, K, _ = s.shape
@@ -390,7 +391,7 @@ def sample_path(scores, cand_ids, temperature: float, uniforms):
 
 def logit_scores(cand_logits) -> np.ndarray:
     """DFlash-1 (no selector): every previous candidate sees the drafter's
-    own top-16 logits.  [15, 16] -> [15, 16, 16]."""
+    own top-16 logits.  [J, 16] -> [J, 16, 16]."""
     z = np.asarray(cand_logits, dtype=np.float64)
     return np.repeat(z[:, None, :], z.shape[1], axis=1)
 
@@ -400,9 +401,9 @@ def verify_rejection(draft, q, cand_ids, target_logits, u_accept, u_bonus: float
     accepted while u_i * q_i(d_i) < p_i(d_i), p_i = softmax of the target's
     logits at position i; at the first rejection the bonus is drawn from the
     residual max(0, p_i - q_i) (q_i zero outside the candidates), and after
-    15 acceptances from p_15; both by inverse CDF in vocabulary order with
+    J acceptances from p_J; both by inverse CDF in vocabulary order with
     u_bonus.  The committed tokens then follow p exactly.
-    target_logits [16, V] -> (k, bonus, committed [16], -1 padded)."""
+    target_logits [J+1, V] -> (k, bonus, committed [J+1], -1 padded)."""
     zt = np.asarray(target_logits, dtype=np.float64)
     draft = np.asarray(draft)
     cand_ids = np.asarray(cand_ids)
