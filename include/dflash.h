@@ -10,6 +10,9 @@
  * and the sampling modes of the same steps:
  *   dflash_sample_path      a draft drawn over the path scores at a temperature
  *   dflash_verify_rejection rejection sampling against target logits (lossless)
+ * Engine options ([DF2] table of inference engines): the block size S may be
+ * changed between steps (dflash_set_block_size), and the drafter's weights
+ * may be FP8 (dflash_config.weight_fp8, "draft quantization").
  *
  * Pages the operations are defined by (cited below by these tags):
  *   [DF]  "DFlash - Difusion de Bloques para Decodificacion Especulativa en
