@@ -25,7 +25,7 @@ EXPORTS = (
     "dflash_set_wait_timeout", "dflash_set_gemm_ctas", "dflash_set_attn_split",
     "dflash_profile_begin", "dflash_profile_end", "dflash_debug_wait_flag", "dflash_last_error",
     "dflash_topk16_noalloc", "dflash_sample_path", "dflash_verify_rejection", "dflash_set_block_size",
-    "dflash_get_block_size", "dflash_debug_e4m3_to_bf16",
+    "dflash_get_block_size", "dflash_debug_e4m3_to_bf16", "dflash_debug_gemm_scratch_bytes", "dflash_debug_gemm",
 )
 
 
@@ -101,6 +101,8 @@ def load(path: str = LIB_PATH):
         "dflash_profile_end": (i, [vp, POINTER(dflash_kernel_stat), i, POINTER(c_int)]),
         "dflash_debug_wait_flag": (i, [vp, c_ulonglong, vp, vp]),
         "dflash_debug_e4m3_to_bf16": (i, [vp, i, vp, vp]),
+        "dflash_debug_gemm_scratch_bytes": (c_size_t, []),
+        "dflash_debug_gemm": (i, [vp, vp, i, vp, i, i, i, vp, vp, c_size_t, i, vp]),
         "dflash_last_error": (ctypes.c_char_p, []),
         "dflash_topk16_noalloc": (i, [vp, i, i, vp, vp, vp]),
     }
@@ -216,6 +218,15 @@ def dflash_set_block_size(ctx, block_size: int):
 
 def dflash_get_block_size(ctx) -> int:
     return int(load().dflash_get_block_size(ctx))
+
+
+def dflash_debug_gemm_scratch_bytes() -> int:
+    return int(load().dflash_debug_gemm_scratch_bytes())
+
+
+def dflash_debug_gemm(W, w_scale, w_fp8, X, M, N, K, out, scratch, scratch_bytes, gemm_ctas=0, stream=None):
+    return _check(load().dflash_debug_gemm(_p(W), _p(w_scale), int(w_fp8), _p(X), M, N, K, _p(out), _p(scratch),
+                                           scratch_bytes, gemm_ctas, _stream(stream)))
 
 
 def dflash_debug_e4m3_to_bf16(codes, n, out, stream=None):

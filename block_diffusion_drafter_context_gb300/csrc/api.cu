@@ -730,6 +730,42 @@ int dflash_debug_wait_flag(const int32_t *flag, unsigned long long timeout_ns, v
   return wait_flag(lc, flag);
 }
 
+size_t dflash_debug_gemm_scratch_bytes(void) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return 256 + sizeof(int) * GEMM_COUNTERS + 4ull * sms * 2 * 128 * GEMM_MAX_BN;
+}
+
+int dflash_debug_gemm(const void *W, const float *w_scale, int w_fp8, const void *X, int M, int N, int K, float *out,
+                      void *scratch, size_t scratch_bytes, int gemm_ctas, dflash_stream_t stream) {
+  if (!W || !X || !out || !scratch || (w_fp8 && !w_scale) || M <= 0 || N <= 0 || K <= 0 || gemm_ctas < 0)
+    return set_error(DFLASH_ERR_ARG, "debug gemm: bad argument");
+  if (K % (w_fp8 ? 16 : 8)) return set_error(DFLASH_ERR_SHAPE, "debug gemm: K must be a multiple of %d", w_fp8 ? 16 : 8);
+  if (!aligned16(scratch) || !aligned16(out)) return set_error(DFLASH_ERR_ALIGN, "debug gemm: misaligned buffer");
+  const size_t need = dflash_debug_gemm_scratch_bytes();
+  if (need == 0 || scratch_bytes < need) return set_error(DFLASH_ERR_SHAPE, "debug gemm: scratch too small");
+  int dev = 0;
+  Launch lc;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&lc.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return set_error(DFLASH_ERR_CUDA, "no CUDA device");
+  lc.stream = reinterpret_cast<cudaStream_t>(stream);
+  lc.status = static_cast<int *>(scratch);
+  lc.gemm_ctas = gemm_ctas;
+  GemmOp op = mk(W, K, X, nullptr, K, M, N, K, EPI_F32, out, N, "debug_gemm");
+  if (w_fp8) {
+    op.w_fp8 = true;
+    op.wscale = w_scale;
+  }
+  GemmScratch sc;
+  sc.counters = reinterpret_cast<int *>(static_cast<char *>(scratch) + 256);
+  sc.n_counters = GEMM_COUNTERS;
+  sc.partials = reinterpret_cast<float *>(static_cast<char *>(scratch) + 256 + sizeof(int) * GEMM_COUNTERS);
+  sc.partial_floats = static_cast<size_t>(lc.num_sms) * 2 * 128 * GEMM_MAX_BN;
+  return gemm_bf16(lc, op, sc);
+}
+
 int dflash_debug_e4m3_to_bf16(const void *codes, int n, void *out, dflash_stream_t stream) {
   Launch lc;
   lc.stream = reinterpret_cast<cudaStream_t>(stream);

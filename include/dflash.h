@@ -328,6 +328,19 @@ DFLASH_API int dflash_profile_end(dflash_ctx *ctx, dflash_kernel_stat *out, int 
 DFLASH_API int dflash_debug_wait_flag(const int32_t *flag, unsigned long long timeout_ns,
                            void *workspace, dflash_stream_t stream);
 
+/* Test hook: the library's tcgen05 GEMM on caller buffers, fp32 result
+ *   out[m][n] = scale[n] * sum_k X[m][k] * W[n][k]
+ * (scale = 1 for bf16 weights), with the same decomposition the drafting
+ * calls use (gemm_ctas > 0 forces persistent stream-K over that many CTAs).
+ *   W: device bf16 [N][K], or with w_fp8 E4M3 codes [N][K] and w_scale fp32 [N];
+ *   X: device bf16 [M][K]; out: device fp32 [M][N]; K a multiple of 8 (16 with
+ *   w_fp8); every pointer 16-byte aligned.
+ *   scratch: device buffer of dflash_debug_gemm_scratch_bytes() bytes,
+ *   zero-filled once (its first 256 bytes are a status word).  0 if no device. */
+DFLASH_API size_t dflash_debug_gemm_scratch_bytes(void);
+DFLASH_API int dflash_debug_gemm(const void *W, const float *w_scale, int w_fp8, const void *X, int M, int N, int K,
+                      float *out, void *scratch, size_t scratch_bytes, int gemm_ctas, dflash_stream_t stream);
+
 /* Test hook: the FP8 GEMM's own E4M3 -> bf16 weight conversion (the device
  * function its converter warps run) applied to n codes.
  *   codes: device uint8 [n], n > 0 a multiple of 4; out: device bf16 [n]. */

@@ -137,4 +137,5 @@ def test_null_and_empty_calls(lib):
     assert lib.dflash_draft_block(None, None, None, None, 1, None, None, None, None, None, 0, None) == -1
     assert lib.dflash_set_attn_split(None, 64) == -1
     assert lib.dflash_set_block_size(None, 5) == -1
+    assert lib.dflash_debug_gemm(None, None, 0, None, 16, 128, 64, None, None, 0, 0, None) == -1
     assert lib.dflash_get_block_size(None) == 0

@@ -284,3 +284,42 @@ def test_e4m3_conversion_matches_oracle_decode_for_every_code():
     finite = ~np.isnan(ref)
     np.testing.assert_array_equal(got[finite], ref[finite])
     assert (np.signbit(got[finite]) == np.signbit(ref[finite])).all()
+
+
+# E4M3 codes of the integers 0..4 (1 = 0x38, 2 = 0x40, 3 = 0x44, 4 = 0x48); the sign bit negates
+_E4M3_INT = {0: 0x00, 1: 0x38, 2: 0x40, 3: 0x44, 4: 0x48}
+
+
+@pytest.mark.parametrize("M,N,K,ctas,fp8", [
+    (1, 448, 320, 0, False), (15, 4096, 1024, 0, False), (16, 1000, 4096, 0, False), (17, 448, 1024, 0, False),
+    (33, 640, 1024, 0, False), (100, 1000, 320, 0, False), (300, 768, 1024, 0, False),
+    (15, 4096, 1024, 5, False), (100, 1000, 1024, 7, False), (15, 24576, 512, 0, False),
+    (15, 4096, 1024, 0, True), (17, 448, 1024, 0, True), (100, 1000, 320, 0, True), (300, 768, 1024, 0, True),
+    (15, 4096, 1024, 5, True), (15, 24576, 512, 0, True),
+])
+def test_gemm_exact_on_small_integers(M, N, K, ctas, fp8):
+    """The production GEMM (every decomposition: cluster split-K, one tile per
+    CTA, stream-K with partial tiles; every token-tile width; bf16 and FP8
+    weights) on integer inputs in [-4, 4]: every product and every fp32 sum
+    is exact, so the result equals the integer matrix product bit for bit."""
+    import torch
+    from block_diffusion_drafter_context_gb300 import binding as Bd
+    rng = np.random.default_rng(M * 7919 + N * 31 + K + ctas)
+    Xi = rng.integers(-4, 5, size=(M, K))
+    Wi = rng.integers(-4, 5, size=(N, K))
+    X = torch.from_numpy(Xi.astype(np.float32)).to(torch.bfloat16).cuda()
+    if fp8:
+        codes = np.vectorize(lambda v: _E4M3_INT[abs(v)] | (0x80 if v < 0 else 0))(Wi).astype(np.uint8)
+        W = torch.from_numpy(codes).cuda()
+        sexp = rng.integers(-1, 2, size=N)                       # power-of-two row scales stay exact
+        scale = torch.from_numpy((2.0 ** sexp).astype(np.float32)).cuda()
+    else:
+        W = torch.from_numpy(Wi.astype(np.float32)).to(torch.bfloat16).cuda()
+        sexp, scale = np.zeros(N), None
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    nbytes = Bd.dflash_debug_gemm_scratch_bytes()
+    scratch = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    Bd.dflash_debug_gemm(W, scale, fp8, X, M, N, K, out, scratch, nbytes, ctas)
+    assert Bd.dflash_read_status(scratch) == 0
+    ref = (Xi @ Wi.T).astype(np.float64) * (2.0 ** sexp)[None, :]
+    assert np.array_equal(to_np(out), ref)
