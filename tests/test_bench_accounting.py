@@ -48,3 +48,34 @@ def test_workload_table_is_consistent():
             assert c.dtype == "bf16", name
         if c.weight_fp8:
             assert c.ffn % 16 == 0 and c.feat_in % 16 == 0, name   # one-byte code rows: 16-byte multiples
+
+
+def _run_bench(*args, env_extra=None):
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, **(env_extra or {}))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), *args], capture_output=True, text=True,
+                       timeout=300, env=env, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    return [json.loads(l) for l in lines]
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) on the tiny
+    workload: one JSON line with the contract's keys, no GPU needed."""
+    (line,) = _run_bench("--impl", "reference", "--workload", "C0", "--steps", "1", "--warmup", "1")
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["warmup"] >= 3 and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["value"] == line["value"]
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    assert _run_bench("--impl", "reference", "--workload", "C0", "--steps", "1", "--warmup", "1",
+                      env_extra={"RANK": "1"}) == []
