@@ -26,6 +26,7 @@ EXPORTS = (
     "dflash_profile_begin", "dflash_profile_end", "dflash_debug_wait_flag", "dflash_last_error",
     "dflash_topk16_noalloc", "dflash_sample_path", "dflash_verify_rejection", "dflash_set_block_size",
     "dflash_get_block_size", "dflash_debug_e4m3_to_bf16", "dflash_debug_gemm_scratch_bytes", "dflash_debug_gemm",
+    "dflash_debug_gemm_plan",
 )
 
 
@@ -103,6 +104,7 @@ def load(path: str = LIB_PATH):
         "dflash_debug_e4m3_to_bf16": (i, [vp, i, vp, vp]),
         "dflash_debug_gemm_scratch_bytes": (c_size_t, []),
         "dflash_debug_gemm": (i, [vp, vp, i, vp, i, i, i, vp, vp, c_size_t, i, vp]),
+        "dflash_debug_gemm_plan": (i, [i, i, i, i, i, i, i, i, i, i, vp]),
         "dflash_last_error": (ctypes.c_char_p, []),
         "dflash_topk16_noalloc": (i, [vp, i, i, vp, vp, vp]),
     }
@@ -227,6 +229,17 @@ def dflash_debug_gemm_scratch_bytes() -> int:
 def dflash_debug_gemm(W, w_scale, w_fp8, X, M, N, K, out, scratch, scratch_bytes, gemm_ctas=0, stream=None):
     return _check(load().dflash_debug_gemm(_p(W), _p(w_scale), int(w_fp8), _p(X), M, N, K, _p(out), _p(scratch),
                                            scratch_bytes, gemm_ctas, _stream(stream)))
+
+
+GEMM_PLAN_KEYS = ("BN", "rtpg", "tok_tiles", "kbpt", "G", "csk", "tiles", "total", "partial_floats", "counters")
+
+
+def dflash_debug_gemm_plan(M, N, K, n_groups=1, w_fp8=False, split_act=False, swiglu=False, per_sm=2, num_sms=152,
+                           gemm_ctas=0) -> dict:
+    out = (ctypes.c_longlong * len(GEMM_PLAN_KEYS))()
+    _check(load().dflash_debug_gemm_plan(M, N, K, n_groups, int(w_fp8), int(split_act), int(swiglu), per_sm, num_sms,
+                                         gemm_ctas, out))
+    return dict(zip(GEMM_PLAN_KEYS, (int(v) for v in out)))
 
 
 def dflash_debug_e4m3_to_bf16(codes, n, out, stream=None):

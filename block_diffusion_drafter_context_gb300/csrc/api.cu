@@ -766,6 +766,17 @@ int dflash_debug_gemm(const void *W, const float *w_scale, int w_fp8, const void
   return gemm_bf16(lc, op, sc);
 }
 
+int dflash_debug_gemm_plan(int M, int N, int K, int n_groups, int w_fp8, int split_act, int swiglu, int per_sm,
+                           int num_sms, int gemm_ctas, long long *plan) {
+  if (!plan || M <= 0 || N <= 0 || K <= 0 || n_groups < 1 || per_sm < 1 || num_sms < 1 || gemm_ctas < 0)
+    return set_error(DFLASH_ERR_ARG, "debug gemm plan: bad argument");
+  const GemmPlan pl = gemm_plan(M, N, K, n_groups, w_fp8 != 0, split_act != 0, swiglu != 0, per_sm, num_sms, gemm_ctas);
+  const long long v[10] = {pl.BN, pl.rtpg, pl.tok_tiles, pl.kbpt, pl.G, pl.csk, pl.tiles, pl.total,
+                           static_cast<long long>(num_sms) * 2 * 128 * GEMM_MAX_BN, GEMM_COUNTERS};
+  for (int i = 0; i < 10; ++i) plan[i] = v[i];
+  return DFLASH_OK;
+}
+
 int dflash_debug_e4m3_to_bf16(const void *codes, int n, void *out, dflash_stream_t stream) {
   Launch lc;
   lc.stream = reinterpret_cast<cudaStream_t>(stream);

@@ -903,6 +903,61 @@ int e4m3_to_bf16(const Launch &lc, const void *codes, int n, void *out) {
   return cuda_check(cudaGetLastError(), "e4m3_to_bf16 launch");
 }
 
+// Token tile: the smallest that covers M; with split activations at most 128
+// so that a stage (weights + two activation tiles) still leaves a 4-deep
+// ring in shared memory, and with FP8 weights at most 128 so that the bf16
+// weight tiles fit in tensor memory beside the accumulators.
+int gemm_token_tile(int M, bool split, bool f8) {
+  return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : (M <= 128 || split || f8) ? 128 : 256;
+}
+
+GemmPlan gemm_plan(int M, int N, int K, int n_groups, bool f8, bool split, bool swiglu, int per_sm, int num_sms,
+                   int gemm_ctas) {
+  GemmPlan pl = {};
+  pl.BN = gemm_token_tile(M, split, f8);
+  pl.rtpg = (N + BM - 1) / BM;
+  pl.tok_tiles = (M + pl.BN - 1) / pl.BN;
+  const int bki = f8 ? 2 * BK : BK;   // k per ring stage
+  pl.kbpt = (K + bki - 1) / bki;
+  pl.tiles = static_cast<long long>(pl.rtpg) * (n_groups > 1 ? n_groups : 1) * pl.tok_tiles;
+  pl.total = pl.tiles * pl.kbpt;
+  // Resident CTA slots (the variant's occupancy, at most two per SM).  CTAs:
+  // one per SM (FP8 weights: one per slot, so that two threads issue MMAs
+  // on each SM), at least 4 k-blocks each, and no tile cut into so many
+  // pieces that its fixup (the last piece sums the others' fp32 partials
+  // from L2) reads more than 256 KB: 32 partials at BN = 16, 4 at BN = 128
+  const int slots = std::min(per_sm, 2) * num_sms;
+  const int cap = gemm_ctas > 0 ? gemm_ctas : (f8 ? slots : num_sms);
+  const int max_parts = std::max(2, (256 * 1024) / (BM * pl.BN * 4));
+  const int min_kb = std::max(4, (pl.kbpt + max_parts - 1) / max_parts);
+  pl.G = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, (pl.total + min_kb - 1) / min_kb)));
+  // More tiles than SMs but no more than the resident slots: one whole tile
+  // per CTA, some SMs running two.  Cutting them over the CTAs would split
+  // nearly every tile and put a global fixup on the tail of a
+  // weight-streaming GEMM.
+  if (gemm_ctas == 0 && pl.tiles > num_sms && pl.tiles <= slots) pl.G = static_cast<int>(pl.tiles);
+  // Few tiles (at most half the SMs): cluster split-K instead, csk CTAs per
+  // tile reducing through distributed shared memory - no global round trips
+  // (fence, counter atomic, partial loads: ~2 us each here) on the GEMM's
+  // tail.  The test hook (gemm_ctas) keeps stream-K.
+  pl.csk = 1;
+  if (gemm_ctas == 0 && pl.tiles * 2 <= cap) {
+    // at most 8 CTAs, and about 8 k-blocks or more each (short ranges are
+    // all pipeline fill; at least 2-way where the k-range allows)
+    long long s = std::min<long long>(std::min<long long>(8, cap / pl.tiles),
+                                      std::min<long long>(pl.kbpt, std::max<long long>(2, pl.kbpt / 8)));
+    // SwiGLU pairs rows 2i / 2i+1 in neighbouring lanes: row ranges must be
+    // even-aligned, so a power-of-two cluster there
+    if (swiglu)
+      while (s & (s - 1)) --s;
+    if (s >= 2) {
+      pl.csk = static_cast<int>(s);
+      pl.G = static_cast<int>(pl.tiles * s);
+    }
+  }
+  return pl;
+}
+
 int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   const int M = op.M, N = op.N, K = op.K;
   const char *name = op.name;
@@ -917,62 +972,27 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   int epi = op.epi == EPI_STORE_T ? EPI_BF16 : op.epi;
   if (epi == EPI_F32_SPLIT && !op.out2) return set_error(DFLASH_ERR_ARG, "gemm %s: split output missing", name);
   const bool split = op.X_lo != nullptr;
-  // token tile: the smallest that covers M; with split activations at most
-  // 128 so that a stage (weights + two activation tiles) still leaves a
-  // 4-deep ring in shared memory
-  // (FP8 weights: at most 128, so that the bf16 weight tiles fit in tensor memory beside the accumulators)
-  const int BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : (M <= 128 || split || f8) ? 128 : 256;
+  const int n_groups = op.n_groups > 1 ? op.n_groups : 1;
+  const int BN = gemm_token_tile(M, split, f8);
+  if (n_groups > MAX_GROUPS || (n_groups > 1 && N % BM))
+    return set_error(DFLASH_ERR_UNSUPPORTED, "gemm %s: at most %d groups of a multiple of %d rows", name, MAX_GROUPS, BM);
+  const int per_sm = f8 ? (split ? per_sm_of<true, true>(BN) : per_sm_of<false, true>(BN))
+                        : (split ? per_sm_of<true, false>(BN) : per_sm_of<false, false>(BN));
+  if (per_sm < 0) return per_sm;
+  const GemmPlan pl = gemm_plan(M, N, K, n_groups, f8, split, epi == EPI_SWIGLU, per_sm, lc.num_sms, lc.gemm_ctas);
+  const long long tiles = pl.tiles;
   Params p = {};
   p.M = M;
   p.N = N;
   p.K = K;
-  p.n_groups = op.n_groups > 1 ? op.n_groups : 1;
-  if (p.n_groups > MAX_GROUPS || (p.n_groups > 1 && N % BM))
-    return set_error(DFLASH_ERR_UNSUPPORTED, "gemm %s: at most %d groups of a multiple of %d rows", name, MAX_GROUPS, BM);
-  p.rtpg = (N + BM - 1) / BM;
+  p.n_groups = n_groups;
+  p.rtpg = pl.rtpg;
   p.out_gstride = op.out_gstride;
-  p.tok_tiles = (M + BN - 1) / BN;
-  const int bki = f8 ? 2 * BK : BK;   // k per ring stage
-  p.kbpt = (K + bki - 1) / bki;
-  const long long tiles = static_cast<long long>(p.rtpg) * p.n_groups * p.tok_tiles;
-  p.total = tiles * p.kbpt;
-  // Resident CTA slots (the variant's occupancy, at most two per SM).  CTAs:
-  // one per SM (FP8 weights: one per slot, so that two threads issue MMAs
-  // on each SM), at least 4 k-blocks each, and no tile cut into more pieces
-  // than keep its fixup (the last piece sums the others' fp32 partials from
-  // L2) under 256 KB: 32 pieces at BN = 16, 4 at BN = 128
-  const int per_sm = f8 ? (split ? per_sm_of<true, true>(BN) : per_sm_of<false, true>(BN))
-                        : (split ? per_sm_of<true, false>(BN) : per_sm_of<false, false>(BN));
-  if (per_sm < 0) return per_sm;
-  const int slots = std::min(per_sm, 2) * lc.num_sms;
-  const int cap = lc.gemm_ctas > 0 ? lc.gemm_ctas : (f8 ? slots : lc.num_sms);
-  const int max_parts = std::max(2, (256 * 1024) / (BM * BN * 4));
-  const int min_kb = std::max(4, (p.kbpt + max_parts - 1) / max_parts);
-  p.G = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, (p.total + min_kb - 1) / min_kb)));
-  // More tiles than SMs but no more than the resident slots: one whole tile
-  // per CTA, some SMs running two.  Cutting them over the CTAs would split
-  // nearly every tile and put a global fixup on the tail of a
-  // weight-streaming GEMM.
-  if (lc.gemm_ctas == 0 && tiles > lc.num_sms && tiles <= slots) p.G = static_cast<int>(tiles);
-  // Few tiles (at most half the SMs): cluster split-K instead, csk CTAs per
-  // tile reducing through distributed shared memory - no global round trips
-  // (fence, counter atomic, partial loads: ~2 us each here) on the GEMM's
-  // tail.  The test hook (gemm_ctas) keeps stream-K.
-  p.csk = 1;
-  if (lc.gemm_ctas == 0 && tiles * 2 <= cap) {
-    // at most 8 CTAs, and about 8 k-blocks or more each (short ranges are
-    // all pipeline fill; at least 2-way where the k-range allows)
-    long long s = std::min<long long>(std::min<long long>(8, cap / tiles),
-                                      std::min<long long>(p.kbpt, std::max<long long>(2, p.kbpt / 8)));
-    // SwiGLU pairs rows 2i / 2i+1 in neighbouring lanes: row ranges must be
-    // even-aligned, so a power-of-two cluster there
-    if (epi == EPI_SWIGLU)
-      while (s & (s - 1)) --s;
-    if (s >= 2) {
-      p.csk = static_cast<int>(s);
-      p.G = static_cast<int>(tiles * s);
-    }
-  }
+  p.tok_tiles = pl.tok_tiles;
+  p.kbpt = pl.kbpt;
+  p.total = pl.total;
+  p.G = pl.G;
+  p.csk = pl.csk;
   p.epi = epi;
   p.out = op.out;
   p.ldo = op.ldo;

@@ -105,6 +105,23 @@ int make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int e
                  uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows,
                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
+// Decomposition of one tensor-core GEMM launch (host arithmetic only).
+struct GemmPlan {
+  int BN;              // token tile (UMMA N)
+  int rtpg;            // 128-row weight tiles per group
+  int tok_tiles;       // token tiles
+  int kbpt;            // k-blocks (ring stages) per tile
+  int G;               // CTAs launched
+  int csk;             // > 1: cluster split-K, csk CTAs per tile
+  long long tiles;     // output tiles over all groups
+  long long total;     // tiles * kbpt
+};
+int gemm_token_tile(int M, bool split, bool f8);
+// per_sm: CTAs of the chosen variant resident per SM; gemm_ctas > 0 forces
+// that many stream-K CTAs (test hook).
+GemmPlan gemm_plan(int M, int N, int K, int n_groups, bool f8, bool split, bool swiglu, int per_sm, int num_sms,
+                   int gemm_ctas);
+
 // bf16 operands on tcgen05 tensor cores.
 int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc);
 // fp32 operands on CUDA cores (tiny fp32 configurations).

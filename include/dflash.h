@@ -341,6 +341,20 @@ DFLASH_API size_t dflash_debug_gemm_scratch_bytes(void);
 DFLASH_API int dflash_debug_gemm(const void *W, const float *w_scale, int w_fp8, const void *X, int M, int N, int K,
                       float *out, void *scratch, size_t scratch_bytes, int gemm_ctas, dflash_stream_t stream);
 
+/* Test hook, host only: the decomposition the tensor-core GEMM chooses for
+ * one launch of out[M][N] (n_groups weight matrices of N rows sharing the
+ * activations X[M][K]; w_fp8: E4M3 weights; split_act: activations as bf16
+ * high + low halves; swiglu: the gate/up epilogue), given per_sm CTAs of the
+ * chosen variant resident per SM and num_sms SMs (gemm_ctas as for
+ * dflash_debug_gemm).  plan (10 values, out): token tile, 128-row weight
+ * tiles per group, token tiles, k-blocks per tile, CTAs, cluster split-K
+ * width (1 = none), output tiles, (tile, k-block) iterations, then the fp32
+ * partial-scratch floats and tile counters a workspace holds for num_sms
+ * SMs.  Launches nothing; DFLASH_ERR_ARG on a null plan or a non-positive
+ * size. */
+DFLASH_API int dflash_debug_gemm_plan(int M, int N, int K, int n_groups, int w_fp8, int split_act, int swiglu,
+                                      int per_sm, int num_sms, int gemm_ctas, long long *plan);
+
 /* Test hook: the FP8 GEMM's own E4M3 -> bf16 weight conversion (the device
  * function its converter warps run) applied to n codes.
  *   codes: device uint8 [n], n > 0 a multiple of 4; out: device bf16 [n]. */
