@@ -12,7 +12,10 @@ __all__ = ["binding", "drafter", "DflashError", "load"]
 
 
 def __getattr__(name):
+    # ``drafter`` on first use; importing it by its full name keeps
+    # ``from block_diffusion_drafter_context_gb300 import drafter`` from
+    # re-entering this hook
     if name == "drafter":
-        from . import drafter
-        return drafter
+        import importlib
+        return importlib.import_module(__name__ + ".drafter")
     raise AttributeError(name)

@@ -1,0 +1,99 @@
+"""Host-side weight packing on the CPU: the layouts include/dflash.h
+documents (w_qkv = q, k, v rows; w_gu rows interleaved gate_i, up_i; FP8 row
+scales packed exactly like their code rows) and the C structs that carry
+the pointers.  Marshalling only, so it runs with CPU tensors."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from block_diffusion_drafter_context_gb300 import binding as B
+from block_diffusion_drafter_context_gb300 import drafter as D
+from synthetic import WORKLOADS, gen
+
+
+def _np(t):
+    t = t.cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def _codes(a):
+    return a.codes if hasattr(a, "codes") else np.asarray(a)
+
+
+@pytest.mark.parametrize("name", ["T1", "T1F8", "T1D2F8"])
+def test_packed_rows_follow_the_header(name):
+    wl = WORKLOADS[name]
+    cfg = wl.cfg
+    W = gen.make_weights(cfg, wl.seed)
+    dw = D.upload_weights(cfg, W, device="cpu")
+    fp8 = cfg.weight_fp8
+    for lw, L in zip(W["layers"], dw["layers"]):
+        q, k, v = (_codes(lw[n]) for n in ("w_q", "w_k", "w_v"))
+        qkv = _np(L["w_qkv"])
+        assert qkv.shape == (q.shape[0] + k.shape[0] + v.shape[0], cfg.hidden)
+        assert np.array_equal(qkv, np.concatenate([q, k, v]))
+        gate, up = _codes(lw["w_gate"]), _codes(lw["w_up"])
+        gu = _np(L["w_gu"])
+        assert gu.shape == (2 * cfg.ffn, cfg.hidden)
+        assert np.array_equal(gu[0::2], gate) and np.array_equal(gu[1::2], up)
+        if fp8:
+            assert gu.dtype == np.uint8
+            s_qkv = _np(L["s_qkv"])
+            assert np.array_equal(s_qkv, np.concatenate([lw["w_q"].scale, lw["w_k"].scale, lw["w_v"].scale]))
+            s_gu = _np(L["s_gu"])
+            assert np.array_equal(s_gu[0::2], lw["w_gate"].scale) and np.array_equal(s_gu[1::2], lw["w_up"].scale)
+            assert np.array_equal(_np(L["s_o"]), lw["w_o"].scale)
+            assert np.array_equal(_np(L["s_down"]), lw["w_down"].scale)
+            # every code row keeps its own scale: row r of the packed matrix
+            # decodes to the source row it came from
+            for packed_row, src, s_src in ((2 * 3 + 1, lw["w_up"], 3), (q.shape[0] + 2, lw["w_k"], 2)):
+                codes = gu[packed_row] if src is lw["w_up"] else qkv[packed_row]
+                scale = s_gu[packed_row] if src is lw["w_up"] else s_qkv[packed_row]
+                assert np.array_equal(codes, src.codes[s_src]) and scale == src.scale[s_src]
+        else:
+            assert "s_qkv" not in L and gu.dtype == np.uint16
+        if cfg.use_conv:
+            assert len(L["w_conv"]) == 4 and len(L["b_conv"]) == 4
+            for j, site in enumerate(D.CONV_SITES):
+                assert np.array_equal(_np(L["w_conv"][j]), _codes(lw["conv"][site][0]))
+                if fp8:
+                    assert np.array_equal(_np(L["s_conv"][j]), lw["conv"][site][0].scale)
+    if fp8:
+        assert np.array_equal(_np(dw["s_lm_head"]), W["lm_head"].scale)
+        assert np.array_equal(_np(dw["lm_head"]), W["lm_head"].codes)
+
+
+@pytest.mark.parametrize("name", ["T1F8", "T1D2"])
+def test_weight_struct_points_at_the_packed_tensors(name):
+    wl = WORKLOADS[name]
+    cfg = wl.cfg
+    dw = D.upload_weights(cfg, gen.make_weights(cfg, wl.seed), device="cpu")
+    w, lay = D.make_weights_struct(dw)
+    for k in ("w_fc", "embed", "lm_head", "g_final"):
+        assert getattr(w, k) == dw[k].data_ptr(), k
+    assert bool(w.s_lm_head) == cfg.weight_fp8
+    for i, L in enumerate(dw["layers"]):
+        s = lay[i]
+        for k in ("w_qkv", "w_o", "w_gu", "w_down", "g_attn", "g_ffn"):
+            assert getattr(s, k) == L[k].data_ptr(), (i, k)
+        if cfg.weight_fp8:
+            assert s.s_gu == L["s_gu"].data_ptr() and s.s_qkv == L["s_qkv"].data_ptr()
+        if cfg.use_conv:
+            assert [s.w_conv[j] for j in range(4)] == [t.data_ptr() for t in L["w_conv"]]
+    if cfg.use_selector:
+        assert w.sel_e256 == dw["sel"]["e256"].data_ptr()
+        assert w.sel_b_g == pytest.approx(dw["sel"]["b_g"])
+
+
+def test_config_struct_carries_every_field():
+    cfg = WORKLOADS["C3F8"].cfg
+    c = D.make_config(cfg)
+    assert c.dtype == B.DFLASH_BF16 and c.weight_fp8 == 1 and c.use_conv == 1 and c.use_selector == 1
+    for k in ("hidden", "n_layers", "n_q_heads", "n_kv_heads", "head_dim", "ffn", "vocab", "target_hidden",
+              "n_target_layers", "sel_rank", "sel_dim", "page_size", "mask_id"):
+        assert getattr(c, k) == getattr(cfg, k), k
+    assert c.block_size == cfg.block and c.top_k == 16
+    assert c.rope_base == pytest.approx(cfg.rope_base) and c.eps == pytest.approx(cfg.eps)
