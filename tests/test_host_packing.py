@@ -97,3 +97,29 @@ def test_config_struct_carries_every_field():
         assert getattr(c, k) == getattr(cfg, k), k
     assert c.block_size == cfg.block and c.top_k == 16
     assert c.rope_base == pytest.approx(cfg.rope_base) and c.eps == pytest.approx(cfg.eps)
+
+
+def test_paged_kv_templates_and_transposed_v():
+    """A drawn cache state: pool page p of layer l holds template page
+    page_map[l, p]; V pages are stored transposed ([d][slot])."""
+    cfg = WORKLOADS["T1"].cfg
+    rng = np.random.default_rng(5)
+    L, T, nkv, P, d = cfg.n_layers, 3, cfg.n_kv_heads, cfg.page_size, cfg.head_dim
+    tk = rng.standard_normal((L, T, nkv, P, d)).astype(np.float32)
+    tv = rng.standard_normal((L, T, nkv, P, d)).astype(np.float32)
+    num_pages = 5
+    page_map = rng.integers(0, T, size=(L, num_pages))
+    table = np.array([[0, 2, -1], [4, 1, 3]], dtype=np.int32)
+    kv = D.PagedKV(cfg, table, num_pages, device="cpu")
+    kv.fill_from_templates(tk, tv, page_map)
+    k = kv.k.float().numpy()
+    v = kv.v.float().numpy()
+    bf = lambda a: torch.from_numpy(a).to(torch.bfloat16).float().numpy()   # noqa: E731
+    for l in range(L):
+        for p in range(num_pages):
+            assert np.array_equal(k[l, p], bf(tk[l, page_map[l, p]]))
+            assert np.array_equal(v[l, p], bf(tv[l, page_map[l, p]].transpose(0, 2, 1)))
+    assert kv.max_pages == 3 and kv.struct.num_pages == num_pages
+    assert kv.struct.k_cache == kv.k.data_ptr() and kv.struct.page_table == kv.page_table.data_ptr()
+    r = kv.row(1)
+    assert r.page_table == kv.page_table.data_ptr() + 3 * 4 and r.max_pages == 3
