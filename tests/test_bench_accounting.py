@@ -79,3 +79,24 @@ def test_reference_arm_prints_one_contract_line():
 def test_reference_arm_other_ranks_print_nothing():
     assert _run_bench("--impl", "reference", "--workload", "C0", "--steps", "1", "--warmup", "1",
                       env_extra={"RANK": "1"}) == []
+
+
+def test_clock_summary_reads_only_the_timed_region():
+    """The nvidia-smi rows inside [t0, t1] plus the first one after: median SM
+    clock, max clock, and every throttle reason seen active there."""
+    cs = bench.ClockSampler(0)
+    na, ac = "Not Active", "Active"
+
+    def row(sm, hw=na, thermal=na, sw_thermal=na, cap=na):
+        return ["0", str(sm), "2070", "900.5", "0x0", hw, thermal, sw_thermal, cap]
+
+    cs.rows = [(0.5, row(1000, hw=ac)),                     # before the region: ignored
+               (1.1, row(2070)), (1.2, row(1950, cap=ac)), (1.3, row(2070)),
+               (2.05, row(1800, sw_thermal=ac)),            # first sample after the end: kept
+               (2.5, row(900, thermal=ac))]                 # later: ignored
+    cs.t0, cs.t1 = 1.0, 2.0
+    s = cs.summary()
+    assert s["samples"] == 4
+    assert s["sm_mhz"] == 2010.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap", "sw_thermal_slowdown"]
+    assert bench.ClockSampler(0).summary()["reasons"] == ["unsampled"]
