@@ -58,6 +58,13 @@ def weight_bytes(cfg) -> float:
     return n * (1.0 if cfg.weight_fp8 else 2.0)
 
 
+def prefill_injection_flops(cfg, tokens: int) -> float:
+    """Dense flops of injecting `tokens` context tokens: the context-feature
+    projection [tokens, n_sel*H_t] x [n_sel*H_t, H] and every layer's K and V
+    projections [tokens, H] x [H, 2*nkv*d]."""
+    return 2.0 * tokens * cfg.hidden * (cfg.feat_in + cfg.n_layers * 2 * cfg.n_kv_heads * cfg.head_dim)
+
+
 def workload_desc(wl):
     c = wl.cfg
     return (f"{wl.name}: {c.name} drafter (L={c.n_layers}, H={c.hidden}, {c.n_q_heads}q/{c.n_kv_heads}kv x "
@@ -432,6 +439,42 @@ def run_ours(args, wl):
     d2h = (out_acc.numel() + out_bonus.numel() + out_com.numel()) * 4
     del graph
 
+    # ---- prefill injection: request 0's whole context injected again into
+    # its own slots (the same values): the large-M context-feature and K/V
+    # projection GEMMs, measured apart from the step
+    prefill_inj = None
+    if Xp is not None and world == 1:
+        try:
+            T0 = int(ctx[0])
+            x0 = to_device(Xp[cu[0]:cu[1]], dev)
+            cu0 = to_device(np.array([0, T0], np.int32), dev)
+            c_in = torch.zeros(1, dtype=torch.int32, device=dev)
+            c_out = torch.empty(1, dtype=torch.int32, device=dev)
+            row0 = kv.row(0)
+
+            def inject_all():
+                Bd.dflash_inject_context(dr.ctx, row0, x0, cu0, T0, c_in, c_out, 1, dr.workspace, dr.ws_bytes,
+                                         torch.cuda.current_stream().cuda_stream)
+
+            for _ in range(3):
+                inject_all()
+            reps = 5
+            ms_inj = timed(inject_all, reps) / reps
+            Bd.dflash_profile_begin(dr.ctx)
+            inject_all()
+            st_inj = Bd.dflash_profile_end(dr.ctx)
+            assert dr.status() == 0, "device status after the prefill injection"
+            g_inj = sum(s["ms"] for s in st_inj if s["name"] in ("fc", "kv_inject"))
+            fl = prefill_injection_flops(cfg, T0)
+            pk_i, src_i = peaks()
+            tf = fl / (g_inj * 1e-3) / 1e12 if g_inj > 0 else None
+            prefill_inj = {"tokens": T0, "ms": ms_inj, "gemm_ms": g_inj, "gemm_flops": fl, "gemm_tflops": tf,
+                       "peak_tflops": float(pk_i["bf16_tflops"]), "peak_source": f"{src_i} bf16_tflops (burst)",
+                       "frac": tf / float(pk_i["bf16_tflops"]) if tf else None,
+                       "launches": sum(s["launches"] for s in st_inj)}
+        except Exception as e:   # reported, never fatal to the step's line
+            prefill_inj = {"error": f"{type(e).__name__}: {e}"}
+
     if world > 1:
         dist.barrier()
     if rank != 0:
@@ -505,6 +548,7 @@ def run_ours(args, wl):
         "cpu_baseline": cpu,
         "e2e": {"value": aggregate_blocks_per_s(world, B, args.steps, ms_e2e), "unit": "blocks/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "prefill_injection": prefill_inj,
         "gpu_launches": launches,
         "launches_per_step": launches / args.steps,
         "clocks": clocks,

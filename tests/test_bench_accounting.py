@@ -100,3 +100,12 @@ def test_clock_summary_reads_only_the_timed_region():
     assert s["sm_mhz"] == 2010.0 and s["sm_max_mhz"] == 2070.0
     assert s["reasons"] == ["sw_power_cap", "sw_thermal_slowdown"]
     assert bench.ClockSampler(0).summary()["reasons"] == ["unsampled"]
+
+
+def test_prefill_injection_flops():
+    """C1's 2048-token prefill: feature projection 20 480 -> 4 096 plus five
+    layers of K and V (8 heads x 128 each) from 4 096: 2 * 2048 * 4096 *
+    (20 480 + 5 * 2 * 1024) = 515.4 GFLOP."""
+    c1 = WORKLOADS["C1"].cfg
+    assert bench.prefill_injection_flops(c1, 2048) == 2.0 * 2048 * 4096 * 30720
+    assert bench.prefill_injection_flops(c1, 0) == 0.0
