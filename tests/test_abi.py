@@ -139,3 +139,20 @@ def test_null_and_empty_calls(lib):
     assert lib.dflash_set_block_size(None, 5) == -1
     assert lib.dflash_debug_gemm(None, None, 0, None, 16, 128, 64, None, None, 0, 0, None) == -1
     assert lib.dflash_get_block_size(None) == 0
+
+
+def test_noalloc_top16_validates_before_touching_the_device(lib):
+    fake = 0x10000   # never dereferenced: every case below returns before any device work
+    assert lib.dflash_topk16_noalloc(None, 0, 1000, None, None, None) == 0          # empty: no-op
+    assert lib.dflash_topk16_noalloc(fake, -1, 1000, fake, fake, None) == -1
+    assert lib.dflash_topk16_noalloc(None, 4, 1000, fake, fake, None) == -1
+    assert lib.dflash_topk16_noalloc(fake, 1025, 1000, fake, fake, None) == -2      # over the fixed scratch
+    assert "1024" in lib.dflash_last_error().decode()
+
+
+def test_sampling_calls_reject_a_null_context(lib):
+    assert lib.dflash_sample_path(None, None, None, None, None, 1, 1.0, None, None, None, None, None, 0, None) == -1
+    assert lib.dflash_verify_rejection(None, None, None, None, None, None, None, 1, None, None, None, None, 0,
+                                       None) == -1
+    assert lib.dflash_select_path(None, None, None, None, None, 1, None, None, None, 0, None) == -1
+    assert lib.dflash_inject_context(None, None, None, None, 16, None, None, 1, None, 0, None) == -1
