@@ -1,0 +1,12 @@
+"""Shapes of the GEMM's bit-exact small-integer parity cases (M tokens, N
+weight rows, K, forced stream-K CTAs or 0, FP8 weights).  Shared by the GPU
+test that runs them and the CPU test that checks, through the launch plan,
+that they reach every decomposition and token tile."""
+
+GEMM_EXACT_CASES = [
+    (1, 448, 320, 0, False), (15, 4096, 1024, 0, False), (16, 1000, 4096, 0, False), (17, 448, 1024, 0, False),
+    (33, 640, 1024, 0, False), (100, 1000, 320, 0, False), (300, 768, 1024, 0, False),
+    (15, 4096, 1024, 5, False), (100, 1000, 1024, 7, False), (15, 24576, 512, 0, False),
+    (15, 4096, 1024, 0, True), (17, 448, 1024, 0, True), (100, 1000, 320, 0, True), (300, 768, 1024, 0, True),
+    (15, 4096, 1024, 5, True), (15, 24576, 512, 0, True),
+]

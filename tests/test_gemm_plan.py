@@ -176,3 +176,30 @@ def test_plan_properties_over_random_shapes():
             assert tiles <= p["counters"], what
         checked += 1
     assert checked == 3000
+
+
+def test_exact_parity_cases_reach_every_decomposition():
+    """The GPU's bit-exact GEMM cases, planned here as they are launched on
+    one GB300: together they take cluster split-K, one whole tile per CTA and
+    stream-K with tiles split across CTAs, with bf16 and with FP8 weights,
+    and every bf16 token tile from 16 to 256."""
+    from tests.gemm_cases import GEMM_EXACT_CASES
+    seen = set()
+    for M, N, K, ctas, f8 in GEMM_EXACT_CASES:
+        bn = B.dflash_debug_gemm_plan(M, N, K, 1, f8, False, False, 1, SMS, ctas)["BN"]
+        p = B.dflash_debug_gemm_plan(M, N, K, 1, f8, False, False, 2 if bn <= 32 else 1, SMS, ctas)
+        if p["csk"] > 1:
+            kind = "cluster"
+        elif p["G"] == p["tiles"] and p["tiles"] > SMS:
+            kind = "whole-tile"
+        else:
+            pieces = _pieces_per_tile(p)
+            kind = "stream-k split" if max(pieces.values()) > 1 else "stream-k"
+        seen.add((kind, f8))
+        if not f8:
+            seen.add(("BN", p["BN"]))
+    for f8 in (False, True):
+        for kind in ("cluster", "whole-tile", "stream-k split"):
+            assert (kind, f8) in seen, (kind, f8)
+    for bn in (16, 32, 64, 128, 256):
+        assert ("BN", bn) in seen, bn

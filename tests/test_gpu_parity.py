@@ -14,6 +14,7 @@ import pytest
 
 import oracle as O
 from synthetic import gen
+from tests.gemm_cases import GEMM_EXACT_CASES
 from tests.gpu_case import TOL, Case, rel_err, to_np
 
 pytestmark = pytest.mark.gpu
@@ -290,13 +291,7 @@ def test_e4m3_conversion_matches_oracle_decode_for_every_code():
 _E4M3_INT = {0: 0x00, 1: 0x38, 2: 0x40, 3: 0x44, 4: 0x48}
 
 
-@pytest.mark.parametrize("M,N,K,ctas,fp8", [
-    (1, 448, 320, 0, False), (15, 4096, 1024, 0, False), (16, 1000, 4096, 0, False), (17, 448, 1024, 0, False),
-    (33, 640, 1024, 0, False), (100, 1000, 320, 0, False), (300, 768, 1024, 0, False),
-    (15, 4096, 1024, 5, False), (100, 1000, 1024, 7, False), (15, 24576, 512, 0, False),
-    (15, 4096, 1024, 0, True), (17, 448, 1024, 0, True), (100, 1000, 320, 0, True), (300, 768, 1024, 0, True),
-    (15, 4096, 1024, 5, True), (15, 24576, 512, 0, True),
-])
+@pytest.mark.parametrize("M,N,K,ctas,fp8", GEMM_EXACT_CASES)
 def test_gemm_exact_on_small_integers(M, N, K, ctas, fp8):
     """The production GEMM (every decomposition: cluster split-K, one tile per
     CTA, stream-K with partial tiles; every token-tile width; bf16 and FP8
