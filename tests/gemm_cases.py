@@ -9,4 +9,6 @@ GEMM_EXACT_CASES = [
     (15, 4096, 1024, 5, False), (100, 1000, 1024, 7, False), (15, 24576, 512, 0, False),
     (15, 4096, 1024, 0, True), (17, 448, 1024, 0, True), (100, 1000, 320, 0, True), (300, 768, 1024, 0, True),
     (15, 4096, 1024, 5, True), (15, 24576, 512, 0, True),
+    # several token tiles under stream-K, tiles split across CTAs
+    (300, 768, 1024, 7, False), (300, 768, 1024, 7, True),
 ]
