@@ -289,6 +289,28 @@ def test_pair_scores_brute_force():
                 assert s[j, p, c] == pytest.approx(zc[j, c] + gate * bil, rel=1e-12, abs=1e-12)
 
 
+def test_pair_scores_hand_worked():
+    """Rank 1, 2-wide embeddings: A picks coordinate 0 of the PREVIOUS token,
+    B coordinate 1 of the CURRENT one, so u(p) . w(c) = e[p][0] * e[c][1].
+    e[0] = (1, 0), e[1] = (0, 1), e[2] = (2, 3); zero logits; gate
+    sigmoid(0) = 1/2 at position 1 and sigmoid(ln 3) = 3/4 at position 2.
+    Position 1 (previous = anchor 2): s(c) = 1/2 * 2 * e[c][1] -> c = 0: 0,
+    c = 1: 1, c = 2: 3.  Position 2, previous 2, current 1: 3/4 * 2 * 1 = 1.5;
+    previous 0, current 2: 3/4 * 1 * 3 = 2.25; previous 1: 0 (e[1][0] = 0).
+    Swapping A and B, or the gate's positions, changes these numbers."""
+    cfg = micro_cfg(hidden=2, vocab=3, sel_dim=2, sel_rank=1, use_selector=True)
+    sel = {"e256": np.array([[1.0, 0.0], [0.0, 1.0], [2.0, 3.0]]), "a": np.array([[1.0, 0.0]]),
+           "b": np.array([[0.0, 1.0]]), "w_g": np.array([1.0, 0.0]), "b_g": 0.0}
+    h = np.array([[9.0, 9.0], [0.0, 5.0], [math.log(3.0), -5.0]])   # row 0 (the anchor) has no gate
+    cand = np.array([[0, 1, 2], [0, 1, 2]])
+    s = O.pair_scores(cfg, sel, 2, cand, np.zeros((2, 3)), h)
+    assert s[0].tolist() == [[0.0, 1.0, 3.0]] * 3                   # every row: the anchor is the previous token
+    assert s[1, 2, 1] == pytest.approx(1.5, abs=1e-15)
+    assert s[1, 0, 2] == pytest.approx(2.25, abs=1e-15)
+    assert s[1, 1].tolist() == [0.0, 0.0, 0.0]
+    assert O.greedy_path(s, cand).tolist() == [2, 2]                # 3, then 3/4 * 2 * 3 = 4.5
+
+
 @pytest.mark.parametrize("J", [1, 2, 3])
 def test_greedy_path_against_exhaustive_enumeration(J):
     for seed in range(5):
