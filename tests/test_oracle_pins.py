@@ -104,6 +104,26 @@ def test_attention_zero_query_is_mean_of_all_values():
         np.testing.assert_allclose(out[:, h, :], np.broadcast_to(allv[:, h // 2].mean(0), (16, 8)), rtol=1e-13)
 
 
+def test_attention_hand_worked_scale_and_head_grouping():
+    """d = 8, scale 1/sqrt(8).  One context key k = e_0 on kv head 0 and
+    sixteen zero block keys; query q = sqrt(8) ln 3 e_0.  Scores: ln 3 for the
+    context key, 0 for the block keys -> weights 3/19 and 1/19 each.  With
+    v_ctx = 19 e_0 and zero block values the output is 3 e_0, on query heads 0
+    and 1 (both on kv head 0 with 2 query heads per kv head) and 0 on heads 2
+    and 3 (kv head 1 holds zero keys and values).  A 1/d scale, no scale, or
+    heads mapped h -> h mod nkv give other numbers."""
+    cfg = micro_cfg()                     # 4 q heads, 2 kv heads, d = 8
+    q = np.zeros((16, 4, 8))
+    q[:, :, 0] = math.sqrt(8.0) * math.log(3.0)
+    kc, vc = np.zeros((1, 2, 8)), np.zeros((1, 2, 8))
+    kc[0, 0, 0] = 1.0
+    vc[0, 0, 0] = 19.0
+    out = O.block_attention(cfg, q, kc, vc, np.zeros((16, 2, 8)), np.zeros((16, 2, 8)))
+    expect = np.zeros((16, 4, 8))
+    expect[:, 0, 0] = expect[:, 1, 0] = 3.0
+    np.testing.assert_allclose(out, expect, rtol=1e-13, atol=1e-13)
+
+
 def test_attention_brute_force_loops():
     """Scalar-loop softmax attention over context + block, GQA head h -> h // g."""
     cfg = micro_cfg()
@@ -409,6 +429,30 @@ def test_drafter_zero_sublayers_reduce_to_embedding_head(S):
     hh = e / np.sqrt((e * e).mean(1, keepdims=True) + cfg.eps) * O.f64(W["g_final"])
     np.testing.assert_allclose(h, hh, rtol=1e-12)
     np.testing.assert_allclose(z, hh[1:] @ O.f64(W["lm_head"]).T, rtol=1e-12)
+
+
+def test_drafter_hand_worked_swiglu_layer():
+    """H = 2, one layer whose attention output projection is zero, so the
+    anchor row is x = E[anchor] = (1, 1) plus the FFN.  Unit gains: the FFN
+    input is (1, 1) (RMS 1).  Gate row 0 reads channel 0, up row 0 reads
+    twice channel 1, down row 0 copies hidden unit 0:
+    ffn = (silu(1) * 2, 0) = (1.462117, 0), x = (2.462117, 1), and the final
+    RMSNorm gives h = x / sqrt((2.462117^2 + 1) / 2) = (1.310265, 0.532170).
+    Gate and up swapped would give silu(2) * 1 = 1.761594 and h0 = 1.329719."""
+    cfg = micro_cfg(hidden=2, n_layers=1, n_q_heads=1, n_kv_heads=1, ffn=2, vocab=5, target_hidden=2,
+                    n_target_layers=1, block=2)
+    W = f32_weights(cfg, 3)
+    W["embed"] = np.ones((5, 2), np.float32)
+    W["g_final"] = np.ones(2, np.float32)
+    lw = W["layers"][0]
+    lw["w_o"] = np.zeros_like(lw["w_o"])
+    lw["g_ffn"] = np.ones(2, np.float32)
+    lw["w_gate"] = np.array([[1, 0], [0, 0]], np.float32)
+    lw["w_up"] = np.array([[0, 2], [0, 0]], np.float32)
+    lw["w_down"] = np.array([[1, 0], [0, 0]], np.float32)
+    h, _ = O.drafter_forward(cfg, W, rand_kv(cfg, 3, 3), 3, 0)
+    np.testing.assert_allclose(h[0], [1.310265, 0.532170], atol=2e-6)
+    np.testing.assert_allclose(h[1], h[0], rtol=1e-15)     # the mask row has the same embedding
 
 
 def test_drafter_non_causal_all_context_and_stateless():
