@@ -140,6 +140,7 @@ struct Layout {
   size_t x, u, u2, qkv, q, bk, bv, o, ysub, coef, hmid, hmask, hfinal, logits, scores, lse;
   size_t u_lo, u2_lo, o_lo, ysub_lo, hmid_lo, hmask_lo, ysub32;
   size_t fc, f, f_lo, kvproj, ctx_saved;
+  size_t cs_blk, cs_inj, tok_page, tok_slot;
   size_t total;
   size_t gemm_part_floats;
 };
@@ -199,6 +200,13 @@ Layout layout(const dflash_ctx *c, int B, int Tn, int S_ = 0) {
   L.f_lo = take(tl * Tn * H);
   L.kvproj = take(4ull * g.n_layers * Tn * 2 * nkv * d);
   L.ctx_saved = take(sizeof(int) * static_cast<size_t>(B));
+  // RoPE (cos, sin) per row and rotation pair for the head epilogues of the
+  // QKV projection (block rows) and of the K/V injection (new tokens), and
+  // each injected token's pool page and slot
+  L.cs_blk = take(8 * R * (d / 2));
+  L.cs_inj = take(8ull * Tn * (d / 2));
+  L.tok_page = take(sizeof(int) * static_cast<size_t>(Tn));
+  L.tok_slot = take(sizeof(int) * static_cast<size_t>(Tn));
   L.total = off;
   return L;
 }
@@ -410,14 +418,28 @@ int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv, const void *targ
   const size_t te = f32 ? 4 : 2;
   const bool split = !f32 && g.split_act;
   void *f_lo = split ? at<void>(workspace, L.f_lo) : nullptr;
-  // context feature: fc projection, then RMSNorm
+  // context feature: fc projection, then RMSNorm (bf16: the same kernel
+  // places every new token - pool page, slot - and tabulates its rotation
+  // for the K head epilogue below)
   if (int e = proj(ctx, lc, workspace, L,
                    wq(ctx, mk(ctx->w.w_fc, K, target_hidden, nullptr, K, total_new, H, K, EPI_F32,
                               at<float>(workspace, L.fc), H, "fc"),
                       ctx->w.s_fc)))
     return e;
+  InjectSlots slots;
+  slots.cu_new = cu_new;
+  slots.page_table = kv->page_table;
+  slots.max_pages = kv->max_pages;
+  slots.num_pages = kv->num_pages;
+  slots.page = g.page_size;
+  slots.d = d;
+  slots.rope_base = g.rope_base;
+  slots.cs = at<float2>(workspace, L.cs_inj);
+  slots.tok_page = at<int32_t>(workspace, L.tok_page);
+  slots.tok_slot = at<int32_t>(workspace, L.tok_slot);
   if (int e = feature_norm(lc, f32, at<float>(workspace, L.fc), total_new, H, ctx->w.g_fc, g.eps, g.fc_norm != 0,
-                           at<void>(workspace, L.f), f_lo, ctx_len_in, at<int32_t>(workspace, L.ctx_saved), batch))
+                           at<void>(workspace, L.f), f_lo, ctx_len_in, at<int32_t>(workspace, L.ctx_saved), batch,
+                           f32 ? nullptr : &slots))
     return e;
   // every layer's own K/V projection of the feature (rows nq*d.. of w_qkv);
   // on tensor cores all layers share one grouped launch
@@ -433,9 +455,33 @@ int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv, const void *targ
     if (kvop.w_fp8) kvop.wscale_g[l] = lw.s_qkv + static_cast<size_t>(nq) * d;
     gk[l] = lw.g_k;
   }
-  if (!f32 && (2 * nkv * d) % 128 == 0) {
+  if (!f32) {
+    // bf16: every layer's K/V projection in one grouped launch (one group per
+    // layer) whose head epilogue k-norms and rotates the K heads and writes K
+    // and V^T straight into the paged cache, then sets ctx_len_out
+    HeadArgs &ha = kvop.head;
+    ha.mode = 2;
+    ha.nkv = nkv;
+    ha.norm = g.qk_norm != 0;
+    ha.eps = g.eps;
+    for (int l = 0; l < g.n_layers; ++l) ha.gk[l] = gk[l];
+    ha.cs = at<float2>(workspace, L.cs_inj);
+    ha.k_cache = kv->k_cache;
+    ha.v_cache = kv->v_cache;
+    ha.layer_elems = layer_elems(ctx, kv);
+    ha.tok_page = at<int32_t>(workspace, L.tok_page);
+    ha.tok_slot = at<int32_t>(workspace, L.tok_slot);
+    ha.cu_new = cu_new;
+    ha.ctx_saved = at<int32_t>(workspace, L.ctx_saved);
+    ha.ctx_out = ctx_len_out;
+    ha.B = batch;
+    kvop.epi = EPI_HEADS;
     kvop.n_groups = g.n_layers;
-    if (int e = proj(ctx, lc, workspace, L, kvop)) return e;
+    if (g.n_layers == 1) {
+      kvop.W = kvop.Wg[0];
+      kvop.wscale = kvop.wscale_g[0];
+    }
+    return proj(ctx, lc, workspace, L, kvop);
   } else {
     for (int l = 0; l < g.n_layers; ++l) {
       GemmOp one = kvop;
@@ -482,15 +528,36 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
   float *ysub32 = at<float>(ws, L.ysub32);
 
   if (int e = embed_rmsnorm(lc, f32, ctx->w.embed, anchor_ids, g.mask_id, V, ctx->layers[0].g_attn, g.eps, B, S, H, x,
-                            u, u_lo))
+                            u, u_lo, ctx_len, d, g.rope_base, f32 ? nullptr : at<float2>(ws, L.cs_blk)))
     return e;
   const size_t lelems = layer_elems(ctx, kv);
   const size_t te = f32 ? 4 : 2;
-  // conv coefficients of one site: tanh(W_c y + b_c), fp32 [R][H/8]
-  auto coef_gemm = [&](int site, const dflash_layer_weights &lw, const void *y, const void *y_lo) {
-    GemmOp op = wq(ctx, mk(lw.w_conv[site], H, y, y_lo, H, R, G8, H, EPI_TANH_BIAS, coef, G8, "conv_coef"),
+  // short conv at one site (weight rows interleaved per channel group: 2g =
+  // current tap, 2g+1 = previous tap).  bf16: one GEMM whose epilogue turns
+  // the coefficients tanh(W_c y + b_c) into the convolved rows; fp32: the
+  // coefficients [R][H/8], then the conv kernel.  Pre sites (y = u) write
+  // out (+ out_lo); post sites (y = ysub32, the sublayer output) add into x.
+  auto conv_site = [&](int site, const dflash_layer_weights &lw, const void *y, const void *y_lo, void *out_t,
+                       void *out_lo, float *x_add) -> int {
+    const void *X = x_add ? (f32 ? static_cast<const void *>(ysub32) : ysub) : y;
+    const void *X_lo = x_add ? ysub_lo : y_lo;
+    if (f32) {
+      GemmOp op = mk(lw.w_conv[site], H, X, nullptr, H, R, G8, H, EPI_TANH_BIAS, coef, G8, "conv_coef");
+      op.bias = lw.b_conv[site];
+      if (int e = proj(ctx, lc, ws, L, op)) return e;
+      return conv_apply(lc, f32, x_add ? nullptr : y, nullptr, x_add ? ysub32 : nullptr, coef, B, S, H, out_t,
+                        nullptr, x_add);
+    }
+    GemmOp op = wq(ctx, mk(lw.w_conv[site], H, X, X_lo, H, R, G8, H, x_add ? EPI_CONV_POST : EPI_CONV_PRE,
+                           x_add ? static_cast<void *>(x_add) : out_t, H, "conv"),
                    lw.s_conv[site]);
     op.bias = lw.b_conv[site];
+    op.out_lo = out_lo;
+    op.conv_y = y;
+    op.conv_y_lo = y_lo;
+    op.conv_y32 = x_add ? ysub32 : nullptr;
+    op.ldy = H;
+    op.conv_S = S;
     return proj(ctx, lc, ws, L, op);
   };
   // a sublayer's output projection: straight into the fp32 residual, or (conv)
@@ -503,26 +570,43 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     op.out2_lo = ysub_lo;
     op.ldo2 = H;
     if (int e = proj(ctx, lc, ws, L, op)) return e;
-    if (int e = coef_gemm(site, lw, f32 ? static_cast<const void *>(ysub32) : ysub, ysub_lo)) return e;
-    return conv_apply(lc, f32, nullptr, nullptr, ysub32, coef, B, S, H, nullptr, nullptr, x);
+    return conv_site(site, lw, nullptr, nullptr, nullptr, nullptr, x);
   };
   for (int l = 0; l < g.n_layers; ++l) {
     const dflash_layer_weights &lw = ctx->layers[l];
     const void *ua = u, *ua_lo = u_lo;
     // ---- attention sublayer
     if (g.use_conv) {
-      if (int e = coef_gemm(0, lw, u, u_lo)) return e;
-      if (int e = conv_apply(lc, f32, u, u_lo, nullptr, coef, B, S, H, u2, u2_lo, nullptr)) return e;
+      if (int e = conv_site(0, lw, u, u_lo, u2, u2_lo, nullptr)) return e;
       ua = u2;
       ua_lo = u2_lo;
     }
-    if (int e = proj(ctx, lc, ws, L,
-                     wq(ctx, mk(lw.w_qkv, H, ua, ua_lo, H, R, nh * d, H, EPI_F32, at<float>(ws, L.qkv), nh * d, "qkv"),
-                        lw.s_qkv)))
-      return e;
-    if (int e = qk_norm_rope(lc, f32, at<float>(ws, L.qkv), B, S, nq, nkv, d, lw.g_q, lw.g_k, g.qk_norm != 0, g.eps,
-                             g.rope_base, ctx_len, at<void>(ws, L.q), at<void>(ws, L.bk), at<void>(ws, L.bv)))
-      return e;
+    if (f32) {
+      if (int e = proj(ctx, lc, ws, L, mk(lw.w_qkv, H, ua, ua_lo, H, R, nh * d, H, EPI_F32, at<float>(ws, L.qkv),
+                                          nh * d, "qkv")))
+        return e;
+      if (int e = qk_norm_rope(lc, f32, at<float>(ws, L.qkv), B, S, nq, nkv, d, lw.g_q, lw.g_k, g.qk_norm != 0, g.eps,
+                               g.rope_base, ctx_len, at<void>(ws, L.q), at<void>(ws, L.bk), at<void>(ws, L.bv)))
+        return e;
+    } else {
+      // bf16: the head epilogue q/k-norms and rotates the heads and writes q,
+      // block K and block V^T in the attention's layouts
+      GemmOp op = wq(ctx, mk(lw.w_qkv, H, ua, ua_lo, H, R, nh * d, H, EPI_HEADS, nullptr, 0, "qkv"), lw.s_qkv);
+      HeadArgs &ha = op.head;
+      ha.mode = 1;
+      ha.nq = nq;
+      ha.nkv = nkv;
+      ha.S = S;
+      ha.norm = g.qk_norm != 0;
+      ha.eps = g.eps;
+      ha.gq = lw.g_q;
+      ha.gk[0] = lw.g_k;
+      ha.cs = at<float2>(ws, L.cs_blk);
+      ha.q = at<void>(ws, L.q);
+      ha.bk = at<void>(ws, L.bk);
+      ha.bv = at<void>(ws, L.bv);
+      if (int e = proj(ctx, lc, ws, L, op)) return e;
+    }
     AttnArgs aa = {};
     aa.q = at<void>(ws, L.q);
     aa.k_cache = static_cast<const char *>(kv->k_cache) + te * lelems * l;
@@ -553,8 +637,7 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     ua = u;
     ua_lo = u_lo;
     if (g.use_conv) {
-      if (int e = coef_gemm(2, lw, u, u_lo)) return e;
-      if (int e = conv_apply(lc, f32, u, u_lo, nullptr, coef, B, S, H, u2, u2_lo, nullptr)) return e;
+      if (int e = conv_site(2, lw, u, u_lo, u2, u2_lo, nullptr)) return e;
       ua = u2;
       ua_lo = u2_lo;
     }

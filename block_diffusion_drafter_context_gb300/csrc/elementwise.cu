@@ -93,6 +93,22 @@ __device__ __forceinline__ void rope_cs(int pos, float th_hi, float th_lo, float
   sincosf(r + tail, &s, &c);
 }
 
+// theta_i = base^(-2i/d) of the rotation pairs, as fp32 (hi, lo) from the host
+struct RopeArgs {
+  float th_hi[64], th_lo[64];
+};
+
+// (cos, sin) of the angles pos * theta_i of the d/2 rotation pairs of one
+// row: threads 0 .. d/2-1 take one pair each.
+__device__ __forceinline__ void rope_row_cs(const RopeArgs &rp, int half, int pos, float2 *cs) {
+  const int i = threadIdx.x;
+  if (i < half) {
+    float c, s;
+    rope_cs(pos, rp.th_hi[i], rp.th_lo[i], c, s);
+    cs[i] = make_float2(c, s);
+  }
+}
+
 // ------------------------------------------------------------------ embed
 // x[b*S+j] = E[id] (fp32 residual stream); u = RMSNorm(x) (activation dtype);
 // S = block size: the anchor at j = 0, the mask token at j = 1..S-1
@@ -100,7 +116,8 @@ template <typename T>
 __global__ void __launch_bounds__(ROW_THREADS) embed_rmsnorm_kernel(const T *embed, const int32_t *anchor,
                                                                     int mask_id, int vocab, const float *gain,
                                                                     float eps, int H, int S, float *x, T *u, T *u_lo,
-                                                                    int *status) {
+                                                                    int *status, const int32_t *ctx_len,
+                                                                    const RopeArgs rp, int half, float2 *cs) {
   // Every input is the caller's (anchor ids, complete before any kernel of
   // this call starts) or a weight: all loads before the wait for the
   // previous kernel; the stores (x, u) after it.
@@ -123,6 +140,9 @@ __global__ void __launch_bounds__(ROW_THREADS) embed_rmsnorm_kernel(const T *emb
   }
   pdl_start();
   if (bad && threadIdx.x == 0) report(status, DFLASH_ERR_DEVICE);
+  // the rotation of this row's q / k heads (position ctx_len[b] + j), used by
+  // the QKV projection's head epilogue; ctx_len comes from the previous call
+  if (cs) rope_row_cs(rp, half, ctx_len[b] + j, cs + static_cast<size_t>(row) * half);
 #pragma unroll
   for (int k = 0; k < MAXV; ++k) {
     const int i = threadIdx.x + k * ROW_THREADS;
@@ -183,11 +203,21 @@ __global__ void __launch_bounds__(ROW_THREADS) rmsnorm_kernel(const float *x, in
 // f = RMSNorm(fc output) (or the plain projection); block 0 also saves the
 // incoming context lengths so the scatter can read them even when the caller
 // updates ctx_len in place.
+struct SlotArgs {
+  const int32_t *cu_new, *page_table;
+  int max_pages, num_pages, page, half;
+  float2 *cs;
+  int32_t *tok_page, *tok_slot;
+  int *status;
+};
+
 template <typename T>
 __global__ void __launch_bounds__(ROW_THREADS) feature_norm_kernel(const float *in, int H, const float *gain,
                                                                    float eps, int apply, T *out, T *out_lo,
-                                                                   const int32_t *ctx_in, int32_t *ctx_saved, int B) {
+                                                                   const int32_t *ctx_in, int32_t *ctx_saved, int B,
+                                                                   const SlotArgs sa, const RopeArgs rp) {
   __shared__ float red[32];
+  __shared__ int spos;
   const int row = blockIdx.x;
   const int nv = H >> 2;
   float4 v[MAXV], g[MAXV];
@@ -199,6 +229,30 @@ __global__ void __launch_bounds__(ROW_THREADS) feature_norm_kernel(const float *
   pdl_start();
   if (row == 0)
     for (int b = threadIdx.x; b < B; b += blockDim.x) ctx_saved[b] = ctx_in[b];
+  if (sa.cs) {
+    // where token `row` goes: request b (last with cu_new[b] <= row), its
+    // position, pool page and slot, and its rotation for the K head epilogue
+    if (threadIdx.x == 0) {
+      int lo = 0, hi = B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sa.cu_new[mid] <= row)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      const int pos = ctx_in[lo] + row - sa.cu_new[lo];
+      const int pidx = pos / sa.page;
+      const int pg = (pos >= 0 && pidx < sa.max_pages) ? sa.page_table[static_cast<size_t>(lo) * sa.max_pages + pidx] : -1;
+      const bool ok = pg >= 0 && pg < sa.num_pages;
+      if (!ok) report(sa.status, DFLASH_ERR_DEVICE);
+      sa.tok_page[row] = ok ? pg : -1;
+      sa.tok_slot[row] = pos % sa.page;
+      spos = pos;
+    }
+    __syncthreads();
+    rope_row_cs(rp, sa.half, spos, sa.cs + static_cast<size_t>(row) * sa.half);
+  }
   const float *xr = in + static_cast<size_t>(row) * H;
 #pragma unroll
   for (int k = 0; k < MAXV; ++k) {
@@ -219,9 +273,6 @@ __global__ void __launch_bounds__(ROW_THREADS) feature_norm_kernel(const float *
 }
 
 // ------------------------------------------------------------------ q/k norm + rope
-struct RopeArgs {
-  float th_hi[64], th_lo[64];
-};
 
 // This lane's angles theta_{lane + 32 i}, i < N, from the parameter table.
 // Kernel parameters indexed by lane serialise the constant bank (one access
@@ -398,8 +449,8 @@ __global__ void __launch_bounds__(256) inject_scatter_kernel(const ScatterArgs a
 // ------------------------------------------------------------------ short conv
 // DFlash-2 ("DFlash 2", Arquitectura del Sistema item 2): two taps along the
 // block, coefficients per 16-channel group, nothing before position 0.
-//   coef: fp32 [B*S][H/8] = tanh(W_c y + b_c): [0, H/16) current tap a,
-//         [H/16, H/8) previous tap b (S = block size <= 16).
+//   coef: fp32 [B*S][H/8] = tanh(W_c y + b_c), interleaved per group g:
+//         column 2g current tap a, 2g+1 previous tap b (S = block size <= 16).
 //   out_j = y_j + a_j * y_j + b_j * y_{j-1}
 // y is either an activation (hi [+ lo] halves) or fp32 (y32).  Pre sites
 // write out (+ low halves), post sites add into the residual x_add.
@@ -417,8 +468,8 @@ __global__ void __launch_bounds__(256) conv_kernel(const T *y, const T *y_lo, co
     if (j >= S) break;
     const size_t row = static_cast<size_t>(b) * S + j;
     yv[j] = y32 ? y32[row * H + c] : Elt<T>::ld(y + row * H + c) + (y_lo ? Elt<T>::ld(y_lo + row * H + c) : 0.f);
-    av[j] = coef[row * (2 * G) + grp];
-    bv[j] = coef[row * (2 * G) + G + grp];
+    av[j] = coef[row * (2 * G) + 2 * grp];
+    bv[j] = coef[row * (2 * G) + 2 * grp + 1];
   }
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
@@ -460,17 +511,22 @@ int check_row(int H) {
 }  // namespace
 
 int embed_rmsnorm(const Launch &lc, bool f32, const void *embed, const int32_t *anchor, int mask_id, int vocab,
-                  const float *gain, float eps, int B, int S, int H, float *x, void *u, void *u_lo) {
+                  const float *gain, float eps, int B, int S, int H, float *x, void *u, void *u_lo,
+                  const int32_t *ctx_len, int d, float rope_base, float2 *cs) {
   if (int e = check_row(H)) return e;
+  if (cs && (!ctx_len || d < 2 || d > 128 || d % 2))
+    return set_error(DFLASH_ERR_ARG, "embed_norm: rotation table needs ctx_len and head_dim <= 128");
+  const RopeArgs rp = cs ? rope_table(d, rope_base) : RopeArgs{};
+  const int half = d / 2;
   return run(lc, "embed_norm", [&] {
     if (f32)
       launch_pdl(embed_rmsnorm_kernel<float>, dim3(B * S), dim3(ROW_THREADS), 0, lc.stream,
           static_cast<const float *>(embed), anchor, mask_id, vocab, gain, eps, H, S, x, tp<float>(u), nullptr,
-          lc.status);
+          lc.status, ctx_len, rp, half, cs);
     else
       launch_pdl(embed_rmsnorm_kernel<__nv_bfloat16>, dim3(B * S), dim3(ROW_THREADS), 0, lc.stream,
           static_cast<const __nv_bfloat16 *>(embed), anchor, mask_id, vocab, gain, eps, H, S, x, tp<__nv_bfloat16>(u),
-          tp<__nv_bfloat16>(u_lo), lc.status);
+          tp<__nv_bfloat16>(u_lo), lc.status, ctx_len, rp, half, cs);
   });
 }
 
@@ -489,17 +545,36 @@ int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, in
 }
 
 int feature_norm(const Launch &lc, bool f32, const float *in, int rows, int H, const float *gain, float eps,
-                 bool apply_norm, void *out, void *out_lo, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B) {
+                 bool apply_norm, void *out, void *out_lo, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B,
+                 const InjectSlots *slots) {
   if (rows <= 0) return DFLASH_OK;
   if (int e = check_row(H)) return e;
+  SlotArgs sa = {};
+  RopeArgs rp = {};
+  if (slots) {
+    if (!slots->cu_new || !slots->page_table || !slots->cs || !slots->tok_page || !slots->tok_slot ||
+        slots->d < 2 || slots->d > 128 || slots->d % 2 || slots->page <= 0)
+      return set_error(DFLASH_ERR_ARG, "feature_norm: injection slot arguments");
+    sa.cu_new = slots->cu_new;
+    sa.page_table = slots->page_table;
+    sa.max_pages = slots->max_pages;
+    sa.num_pages = slots->num_pages;
+    sa.page = slots->page;
+    sa.half = slots->d / 2;
+    sa.cs = slots->cs;
+    sa.tok_page = slots->tok_page;
+    sa.tok_slot = slots->tok_slot;
+    sa.status = lc.status;
+    rp = rope_table(slots->d, slots->rope_base);
+  }
   return run(lc, "feature_norm", [&] {
     if (f32)
       launch_pdl(feature_norm_kernel<float>, dim3(rows), dim3(ROW_THREADS), 0, lc.stream, in, H, gain, eps, apply_norm, tp<float>(out),
-                                                                      nullptr, ctx_len_in, ctx_len_saved, B);
+                                                                      nullptr, ctx_len_in, ctx_len_saved, B, sa, rp);
     else
       launch_pdl(feature_norm_kernel<__nv_bfloat16>, dim3(rows), dim3(ROW_THREADS), 0, lc.stream,
           in, H, gain, eps, apply_norm, tp<__nv_bfloat16>(out), tp<__nv_bfloat16>(out_lo), ctx_len_in, ctx_len_saved,
-          B);
+          B, sa, rp);
   });
 }
 

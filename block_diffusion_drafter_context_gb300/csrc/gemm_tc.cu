@@ -18,6 +18,11 @@
 //     a tile split across CTAs is finished by whichever CTA completes it last
 //     (per-tile counter), which sums the fp32 partials in CTA order -
 //     deterministic, no spin-waits;
+//   * tile order: token tile outer, weight row tile inner (tile = tok * RT +
+//     rt).  With several token tiles the CTAs that own the same weight rows
+//     for different token tiles sit G / tok_tiles apart and advance in step,
+//     so each weight tile leaves DRAM once and the other readers hit L2; the
+//     evict-first hint on the weight stream is used only with one token tile;
 //   * warp roles: warp 0 issues TMA loads into a STAGES-deep ring of
 //     128-byte-swizzled tiles, warp 1 owns TMEM and issues tcgen05.mma from
 //     one thread, warps 2-5 drain TMEM (double-buffered) into the epilogue;
@@ -79,6 +84,10 @@ struct Cfg {
   // the owning CTA: at most (csk - 1) * ceil(128 / csk) <= 120 rows arrive
   static constexpr bool PUSH = BN <= 32;
   static constexpr int PUSH_BYTES = PUSH ? 120 * BN * 4 : 0;
+  // the head epilogue's exchange (16 tokens x 128 features + per-warp sums);
+  // it never runs with the push path, so the two share one region
+  static constexpr int XCH_BYTES = 128 * 16 * 4 + 4 * 16 * 4;
+  static constexpr int XREG = PUSH_BYTES > XCH_BYTES ? PUSH_BYTES : XCH_BYTES;
   static constexpr int CTRL = 512;                     // mbarriers and flags
   // Small token tiles (weight streaming): ~100 KB of ring, so two GEMM CTAs
   // fit on one SM and, under programmatic dependent launch, the next GEMM's
@@ -86,13 +95,13 @@ struct Cfg {
   // (152 x 5 stages in flight still exceed what HBM needs in flight).  F8
   // keeps the whole CTA within half an SM.  Large token tiles (tensor-bound):
   // one CTA per SM with a deeper ring.
-  static constexpr int BUDGET = BN <= 32 ? (F8 ? (SMEM_PER_SM / 2 - 1024 - 1024 - CTRL - PUSH_BYTES) : 100 * 1024)
+  static constexpr int BUDGET = BN <= 32 ? (F8 ? (SMEM_PER_SM / 2 - 1024 - 1024 - CTRL - XREG) : 100 * 1024)
                                          : 200 * 1024;
   static constexpr int STAGES_RAW = BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : (STAGES_RAW < 2 ? 2 : STAGES_RAW);
   static constexpr int TMEM_COLS = F8 ? pow2_at_least(A_COL + CSTAGES * A_TCOLS) : (2 * BN < 32 ? 32 : 2 * BN);
   static constexpr int RING = STAGES * STAGE_BYTES;
-  static constexpr int SMEM = 1024 + RING + CTRL + PUSH_BYTES;
+  static constexpr int SMEM = 1024 + RING + CTRL + XREG;
   static_assert((2 * STAGES + 2 * CSTAGES + 6) * 8 + 12 <= CTRL, "GEMM control block overflows");
   static_assert(RING >= BM * BN * 4, "the ring must hold one fp32 tile (cluster split-K share)");
   static_assert(!F8 || BN > 32 || 2 * (SMEM + 1024) <= SMEM_PER_SM, "two F8 CTAs must fit on one SM");
@@ -106,6 +115,7 @@ struct Params {
   int n_groups, rtpg;   // groups, 128-row tiles per group
   size_t out_gstride;   // output elements between groups
   int tok_tiles, kbpt;
+  int rt_total;         // weight row tiles of all groups (n_groups * rtpg): tile = tok * rt_total + rt
   long long total;     // tiles * kbpt
   int G;               // CTAs
   int csk;             // >1: cluster split-K, csk CTAs (one cluster) per tile
@@ -116,6 +126,10 @@ struct Params {
   void *out2, *out2_lo;
   int ldo2;
   const float *bias;
+  const void *cy, *cy_lo;   // EPI_CONV_PRE: convolved activation (bf16 hi / lo), row stride ldy
+  const float *cy32;        // EPI_CONV_POST: convolved activation (fp32)
+  int ldy, cS;              // EPI_CONV_*: row stride of y, block size
+  HeadArgs head;            // EPI_HEADS
   const float *wscale[MAX_GROUPS];   // F8: per-row weight scales of each group
   float *partials;     // [G][2][BM][BN] row-major shares
   int *counters;       // [tiles]
@@ -141,10 +155,215 @@ __device__ __forceinline__ void store_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, s
   if (lo) lo[i] = f2bf(v - bf2f(h));
 }
 
+// 8 consecutive channels of row r of the convolved activation (fp32 value).
+__device__ __forceinline__ void conv_load8(const Params &p, bool post, int r, int c0, float (&y)[8]) {
+  const size_t o = static_cast<size_t>(r) * p.ldy + c0;
+  if (post) {
+    const float4 a = *reinterpret_cast<const float4 *>(p.cy32 + o), b = *reinterpret_cast<const float4 *>(p.cy32 + o + 4);
+    y[0] = a.x, y[1] = a.y, y[2] = a.z, y[3] = a.w, y[4] = b.x, y[5] = b.y, y[6] = b.z, y[7] = b.w;
+  } else {
+    const uint4 h = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.cy) + o);
+    const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+    uint32_t lw[4] = {0u, 0u, 0u, 0u};
+    if (p.cy_lo) {
+      const uint4 l = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.cy_lo) + o);
+      lw[0] = l.x, lw[1] = l.y, lw[2] = l.z, lw[3] = l.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      y[2 * i] = __uint_as_float(hw[i] << 16) + __uint_as_float(lw[i] << 16);
+      y[2 * i + 1] = __uint_as_float(hw[i] & 0xFFFF0000u) + __uint_as_float(lw[i] & 0xFFFF0000u);
+    }
+  }
+}
+
+// DFlash-2 short convolution ("DFlash 2", Arquitectura del Sistema item 2)
+// of 8 channels c0.. of one 16-channel group over the 16 token rows tok0..:
+// out_j = y_j + a_j * y_j + b_j * y_{j-1}, y_{-1} = 0 at every block's first
+// position (rows are consecutive positions of S-token blocks).  Pre sites
+// store the bf16 hi / lo halves, post sites add into the fp32 residual.
+// CB rows at a time: their loads (y, and the residual at post sites) are
+// all issued before the first store, so the stores, which the compiler must
+// assume may alias the loads, do not serialise them (CB = 1 in the variants
+// capped at 96 registers).
+template <int CB>
+__device__ __noinline__ void conv_rows(const Params &p, bool post, const float (&a)[16], const float (&b)[16],
+                                       int c0, int tok0) {
+  float prev[8];
+  if (tok0 < p.M && tok0 % p.cS != 0) {
+    conv_load8(p, post, tok0 - 1, c0, prev);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) prev[k] = 0.f;
+  }
+#pragma unroll
+  for (int i0 = 0; i0 < 16; i0 += CB) {
+    float y[CB][8];
+    float4 xr[CB][2];
+#pragma unroll
+    for (int u = 0; u < CB; ++u) {
+      const int r = tok0 + i0 + u;
+      if (r < p.M) {
+        conv_load8(p, post, r, c0, y[u]);
+        if (post) {
+          const float4 *x = reinterpret_cast<const float4 *>(static_cast<const float *>(p.out) +
+                                                             static_cast<size_t>(r) * p.ldo + c0);
+          xr[u][0] = __ldcg(x);
+          xr[u][1] = __ldcg(x + 1);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < CB; ++u) {
+      const int i = i0 + u, r = tok0 + i;
+      if (r >= p.M) break;
+      if (r % p.cS == 0) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) prev[k] = 0.f;
+      }
+      float o[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) o[k] = y[u][k] + a[i] * y[u][k] + b[i] * prev[k];
+      const size_t off = static_cast<size_t>(r) * p.ldo + c0;
+      if (post) {
+        float4 *x = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off);
+        x[0] = make_float4(xr[u][0].x + o[0], xr[u][0].y + o[1], xr[u][0].z + o[2], xr[u][0].w + o[3]);
+        x[1] = make_float4(xr[u][1].x + o[4], xr[u][1].y + o[5], xr[u][1].z + o[6], xr[u][1].w + o[7]);
+      } else {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const __nv_bfloat16 h0 = f2bf(o[2 * k]), h1 = f2bf(o[2 * k + 1]);
+          const __nv_bfloat16 l0 = f2bf(o[2 * k] - bf2f(h0)), l1 = f2bf(o[2 * k + 1] - bf2f(h1));
+          hw[k] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
+                  (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+          lw[k] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
+                  (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+        }
+        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if (p.out_lo)
+          *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out_lo) + off) =
+              make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) prev[k] = y[u][k];
+    }
+  }
+}
+
+// EPI_HEADS: the tile is one attention head, row n = feature i (0..127) of
+// head n / 128 of group g; v holds that feature for the 16 token rows tok0...
+// Called by all 128 epilogue threads together, each with a different i (they
+// meet at the epilogue's named barrier).  q / k heads: per-token RMSNorm over
+// the head's 128 features ("DFlash" layer internals: Qwen3-style q/k norm),
+// then RoPE on the pairs (i, i + 64) with the row's (cos, sin); the partner
+// feature comes through shared memory.  The head is stored where the block
+// attention reads it.  V^T destinations (columns = tokens) are written by
+// lanes that cover 16 consecutive tokens of two features per instruction, so
+// each warp store fills whole 32-byte sectors instead of 32 scattered bytes.
+__device__ __noinline__ void heads_epi(const Params &p, float (&v)[16], int n, int g, int tok0, float *xch) {
+  const HeadArgs &a = p.head;
+  const int i = n & 127, head = n >> 7, lane = i & 31, q4 = i >> 5;
+  const int kind = head < a.nq ? 0 : (head < a.nq + a.nkv ? 1 : 2);   // q, k, v
+  const int h = kind == 0 ? head : (kind == 1 ? head - a.nq : head - a.nq - a.nkv);
+  float *red = xch + 16 * 128;
+  if (kind < 2) {
+    if (a.norm) {
+      const float gn = (kind == 0 ? a.gq : a.gk[g])[i];
+      float ss[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) ss[t] = warp_sum(v[t] * v[t]);
+      if (lane == 0) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) red[q4 * 16 + t] = ss[t];
+      }
+      epi_bar();
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const float tot = red[t] + red[16 + t] + red[32 + t] + red[48 + t];
+        v[t] *= rsqrtf(tot * (1.f / 128.f) + a.eps) * gn;
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) xch[t * 128 + i] = v[t];
+    epi_bar();
+    const bool lo = i < 64;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      const int row = tok0 + t < p.M ? tok0 + t : p.M - 1;
+      const float2 cs = a.cs[static_cast<size_t>(row) * 64 + (i & 63)];
+      const float o = xch[t * 128 + (i ^ 64)];
+      v[t] = lo ? v[t] * cs.x - o * cs.y : v[t] * cs.x + o * cs.y;
+    }
+    epi_bar();   // the exchange is free again
+  }
+  __nv_bfloat16 *dst = nullptr;
+  if (kind == 2) {
+    // V^T: this warp's 32 features, 16 tokens, via shared memory; lane l
+    // takes feature 32*q4 + 2k + l/16 of token l%16 in step k
+#pragma unroll
+    for (int t = 0; t < 16; ++t) xch[t * 128 + i] = v[t];
+    __syncwarp();
+    const int t = lane & 15, row = tok0 + t;
+    if (row < p.M) {
+      if (a.mode == 1) {
+        const int b = row / a.S, j = row % a.S;
+        dst = static_cast<__nv_bfloat16 *>(a.bv) + (static_cast<size_t>(b) * a.nkv + h) * 128 * 64 + j;
+      } else {
+        const int pg = a.tok_page[row];
+        if (pg >= 0)
+          dst = static_cast<__nv_bfloat16 *>(a.v_cache) + static_cast<size_t>(g) * a.layer_elems +
+                (static_cast<size_t>(pg) * a.nkv + h) * 128 * 64 + a.tok_slot[row];
+      }
+    }
+#pragma unroll 4
+    for (int k = 0; k < 16; ++k) {
+      const int f = q4 * 32 + 2 * k + (lane >> 4);
+      const float x = xch[t * 128 + f];
+      if (dst) dst[static_cast<size_t>(f) * 64] = f2bf(x);
+    }
+    __syncwarp();
+    // block V^T below a block of 16: the PV k-step reads columns 0..15, so
+    // the columns S..15 of each request get zeros (written by its first row)
+    if (a.mode == 1 && a.S < 16) {
+#pragma unroll
+      for (int t2 = 0; t2 < 16; ++t2) {
+        const int r2 = tok0 + t2;
+        if (r2 < p.M && r2 % a.S == 0) {
+          __nv_bfloat16 *z = static_cast<__nv_bfloat16 *>(a.bv) +
+                             (static_cast<size_t>(r2 / a.S) * a.nkv + h) * 128 * 64 + static_cast<size_t>(i) * 64;
+          for (int c = a.S; c < 16; ++c) z[c] = f2bf(0.f);
+        }
+      }
+    }
+    return;
+  }
+  // q rows and K rows: lanes cover consecutive features of one token
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const int row = tok0 + t;
+    if (row >= p.M) break;
+    __nv_bfloat16 *o;
+    if (a.mode == 1) {
+      const int b = row / a.S, j = row % a.S;
+      o = kind == 0 ? static_cast<__nv_bfloat16 *>(a.q) + static_cast<size_t>(row) * a.nq * 128 + h * 128 + i
+                    : static_cast<__nv_bfloat16 *>(a.bk) + ((static_cast<size_t>(b) * a.nkv + h) * 64 + j) * 128 + i;
+    } else {
+      const int pg = a.tok_page[row];
+      if (pg < 0) continue;
+      o = static_cast<__nv_bfloat16 *>(a.k_cache) + static_cast<size_t>(g) * a.layer_elems +
+          ((static_cast<size_t>(pg) * a.nkv + h) * 64 + a.tok_slot[row]) * 128 + i;
+    }
+    *o = f2bf(v[t]);
+  }
+}
+
 // Apply the epilogue to 16 consecutive token columns of weight row n (ws:
-// the group's FP8 row scales, or null).
+// the group's FP8 row scales, or null).  CB: rows per load batch of the
+// short-conv epilogue.
+template <int CB>
 __device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n, int tok0, size_t goff,
-                                         const float *ws) {
+                                         const float *ws, int grp, float *xch) {
   const bool nok = n < p.N;
   if (ws) {
     const float sc = nok ? ws[n] : 0.f;
@@ -152,6 +371,9 @@ __device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n,
     for (int i = 0; i < 16; ++i) v[i] *= sc;
   }
   switch (p.epi) {
+    case EPI_HEADS:
+      heads_epi(p, v, n, grp, tok0, xch);
+      break;
     case EPI_BF16: {
       __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out), *ol = static_cast<__nv_bfloat16 *>(p.out_lo);
 #pragma unroll
@@ -191,6 +413,25 @@ __device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n,
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         if (nok && tok0 + i < p.M) o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] = tanhf(v[i] + b);
+    } break;
+    case EPI_CONV_PRE:
+    case EPI_CONV_POST: {
+      // rows 2g / 2g+1 = tap a / tap b of channel group g, in neighbouring
+      // lanes: exchange them, then each lane of the pair takes 8 of the
+      // group's 16 channels
+      const float bn = nok ? p.bias[n] : 0.f;
+      float c[16], o[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) c[i] = tanhf(v[i] + bn);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i] = __shfl_xor_sync(0xffffffffu, c[i], 1);
+      if (!nok) break;
+      const bool odd = n & 1;
+      const int c0 = (n >> 1) * 16 + (odd ? 8 : 0);
+      if (odd)
+        conv_rows<CB>(p, p.epi == EPI_CONV_POST, o, c, c0, tok0);
+      else
+        conv_rows<CB>(p, p.epi == EPI_CONV_POST, c, o, c0, tok0);
     } break;
     case EPI_F32_SPLIT: {
       float *o = static_cast<float *>(p.out);
@@ -246,10 +487,11 @@ __global__ void e4m3_to_bf16_kernel(const uint32_t *codes, int n4, uint2 *out) {
 }
 
 template <int BN, bool SPLIT, bool F8>
-__global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 : 1)
+__global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, BN <= 32 ? 2 : 1)   // small tiles: two CTAs per SM
     gemm_tc_kernel(const __grid_constant__ WMaps wm, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmXlo, const Params p) {
   using C = Cfg<BN, SPLIT, F8>;
+  constexpr int CB_ = (F8 && BN <= 32) ? 1 : 4;   // short-conv load batch (96-register variants: 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *base = smem_raw + pad;
@@ -267,7 +509,11 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
   uint64_t *cfull = rbar + 1;   // F8: converted weight tile ready
   uint64_t *cempty = cfull + C::CSTAGES;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cempty + C::CSTAGES);
-  float *spush = reinterpret_cast<float *>(base + C::RING + C::CTRL);
+  float *spush = reinterpret_cast<float *>(base + C::RING + C::CTRL);   // push shares, or ...
+  float *xch = spush;                                                      // ... the head epilogue's exchange
+  // the head epilogue needs a whole tile in one CTA: no pushing of rows to
+  // the other CTAs of a cluster (its shares are pulled by rank 0 instead)
+  const bool push = C::PUSH && p.epi != EPI_HEADS;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *bcast = reinterpret_cast<int *>(tmem_slot + 2);
 
@@ -305,7 +551,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (C::PUSH && p.csk > 1) cluster_sync();   // every CTA's barriers exist before any remote arrive
+  if (push && p.csk > 1) cluster_sync();   // every CTA's barriers exist before any remote arrive
 
   // The activations, outputs and stream-K scratch are produced / consumed by
   // the neighbouring kernels of the step: only the weight stream may start
@@ -326,7 +572,17 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // one token tile: every weight tile is read once, evict it first; with
+      // several, the readers of the other token tiles follow within the ring
+      // depth, so no hint
       const uint64_t pol_w = policy_evict_first();
+      const bool hint_w = p.tok_tiles == 1;
+      auto load_w = [&](void *dst, const CUtensorMap *m, uint64_t *bar, int x, int y) {
+        if (hint_w)
+          tma_load_2d_hint(dst, m, bar, x, y, pol_w);
+        else
+          tma_load_2d(dst, m, bar, x, y);
+      };
       const long long n_my = end - begin;
       // iteration -> (group, weight row, token row, k-block), advanced
       // incrementally: no integer division in the issue loop
@@ -337,19 +593,19 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
       {
         const int tile = static_cast<int>(begin / p.kbpt);
         it0.kb = static_cast<int>(begin - static_cast<long long>(tile) * p.kbpt);
-        const int rt = tile / p.tok_tiles;
-        it0.tok = tile - rt * p.tok_tiles;
+        it0.tok = tile / p.rt_total;
+        const int rt = tile - it0.tok * p.rt_total;
         it0.g = rt / p.rtpg;
         it0.rtin = rt - it0.g * p.rtpg;
       }
       auto advance = [&](Iter &q) {
         if (++q.kb == p.kbpt) {
           q.kb = 0;
-          if (++q.tok == p.tok_tiles) {
-            q.tok = 0;
-            if (++q.rtin == p.rtpg) {
-              q.rtin = 0;
-              ++q.g;
+          if (++q.rtin == p.rtpg) {
+            q.rtin = 0;
+            if (++q.g == p.n_groups) {
+              q.g = 0;
+              ++q.tok;
             }
           }
         }
@@ -368,8 +624,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
         int g, row0, tok0, kb;
         coords(q, g, row0, tok0, kb);
         mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
-        tma_load_2d_hint(F8 ? sRaw + i * C::RAW_BYTES : sA + i * C::A_BYTES, &wm.m[g], &full[i], kb * C::BKI, row0,
-                         pol_w);
+        load_w(F8 ? sRaw + i * C::RAW_BYTES : sA + i * C::A_BYTES, &wm.m[g], &full[i], kb * C::BKI, row0);
       }
       grid_dep_wait();
       q = it0;
@@ -393,8 +648,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
           break;
         }
         mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-        tma_load_2d_hint(F8 ? sRaw + stage * C::RAW_BYTES : sA + stage * C::A_BYTES, &wm.m[g], &full[stage],
-                         kb * C::BKI, row0, pol_w);
+        load_w(F8 ? sRaw + stage * C::RAW_BYTES : sA + stage * C::A_BYTES, &wm.m[g], &full[stage], kb * C::BKI, row0);
 #pragma unroll
         for (int t = 0; t < C::BT; ++t) {
           tma_load_2d(sB + stage * C::B_STAGE + t * C::B_BYTES, &tmX, &full[stage], kb * C::BKI + t * BK, tok0);
@@ -539,6 +793,11 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
     const int r = q * 32 + lane;         // weight row within the tile
     const int et = threadIdx.x - 64;     // 0..127
     grid_dep_wait();                     // outputs / scratch are shared with the previous kernel
+    if (p.epi == EPI_HEADS && p.head.mode == 2 && blockIdx.x == 0)
+      // context injection: the requests' new lengths (the feature kernel saved
+      // the old ones; nothing reads ctx_len_in after it)
+      for (int b = et; b < p.head.B; b += 128)
+        p.head.ctx_out[b] = p.head.ctx_saved[b] + (p.head.cu_new[b + 1] - p.head.cu_new[b]);
     int seg = 0;
     for (long long it = begin; it < end; ++seg) {
       const int tile = static_cast<int>(it / p.kbpt);
@@ -553,10 +812,10 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
       bool have_pre = false;
       if (BN == 16 && p.epi == EPI_ADD_F32) {
         const bool whole_t = kb0 == 0 && kb1 == p.kbpt;
-        const bool owner = C::PUSH && p.csk > 1 && ((r + 1) * p.csk - 1) / BM == static_cast<int>(cluster_ctarank());
+        const bool owner = push && p.csk > 1 && ((r + 1) * p.csk - 1) / BM == static_cast<int>(cluster_ctarank());
         if (whole_t || owner) {
-          const int rt0 = tile / p.tok_tiles;
-          const int n0 = (rt0 % p.rtpg) * BM + r, t0 = (tile % p.tok_tiles) * BN;
+          const int rt0 = tile % p.rt_total;
+          const int n0 = (rt0 % p.rtpg) * BM + r, t0 = (tile / p.rt_total) * BN;
           const size_t g0 = static_cast<size_t>(rt0 / p.rtpg) * p.out_gstride;
           const float *o = static_cast<const float *>(p.out);
 #pragma unroll
@@ -573,11 +832,11 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
         break;
       }
       tc_fence_after();
-      const int rt = tile / p.tok_tiles;
+      const int rt = tile % p.rt_total;
       const int n = (rt % p.rtpg) * BM + r;                       // row within its group
       const size_t goff = static_cast<size_t>(rt / p.rtpg) * p.out_gstride;
       const float *wsg = F8 ? p.wscale[rt / p.rtpg] : nullptr;
-      const int tok0 = (tile % p.tok_tiles) * BN;
+      const int tok0 = (tile / p.rt_total) * BN;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
       float v[16];
       if (kb0 == 0 && kb1 == p.kbpt) {
@@ -586,12 +845,12 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
           if (have_pre)
             finalize_add_pre(p, v, rpre, n, tok0 + c * 16, goff, wsg);
           else
-            finalize(p, v, n, tok0 + c * 16, goff, wsg);
+            finalize<CB_>(p, v, n, tok0 + c * 16, goff, wsg, rt / p.rtpg, xch);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
-      } else if (C::PUSH && p.csk > 1) {
+      } else if (push && p.csk > 1) {
         // cluster split-K, small token tile: each row's fp32 share goes straight
         // into the shared memory of the CTA that finalises that row (rows
         // [k*BM/csk, (k+1)*BM/csk) belong to rank k); one release arrive per
@@ -652,7 +911,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
           if (have_pre && mine)
             finalize_add_pre(p, v, rpre, n, tok0 + c * 16, goff, wsg);
           else
-            finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsg);   // n >= N: not this CTA's row
+            finalize<CB_>(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsg, rt / p.rtpg, xch);   // n >= N: not this CTA's row
         }
       } else if (p.csk > 1) {
         // cluster split-K: this CTA's fp32 share into its own smem, row-major
@@ -734,7 +993,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
               v[4 * i + 2] = acc[i].z;
               v[4 * i + 3] = acc[i].w;
             }
-            finalize(p, v, n, tok0 + c * 16, goff, wsg);
+            finalize<CB_>(p, v, n, tok0 + c * 16, goff, wsg, rt / p.rtpg, xch);
           }
         }
         epi_bar();
@@ -748,7 +1007,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 
-  if (!C::PUSH && p.csk > 1) {
+  if (!push && p.csk > 1) {
     // ---- cluster split-K reduction through distributed shared memory: CTA
     // r finalises tile rows [r*BM/csk, (r+1)*BM/csk) summing the csk shares in
     // rank order (deterministic); lanes hold consecutive rows (coalesced
@@ -757,13 +1016,16 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
     if (warp >= 2 && warp < 6) {   // the epilogue warps
       const int et = threadIdx.x - 64;
       const int rank = static_cast<int>(cluster_ctarank());
-      const int r0 = rank * BM / p.csk, rows = (rank + 1) * BM / p.csk - r0;
+      // head epilogue: rank 0 finalises the whole tile (one head)
+      const bool heads = p.epi == EPI_HEADS;
+      const int r0 = heads ? 0 : rank * BM / p.csk;
+      const int rows = heads ? (rank == 0 ? BM : 0) : (rank + 1) * BM / p.csk - r0;
       const int tasks = rows * (BN / 16);
       const int tile = first_tile;
-      const int rt = tile / p.tok_tiles;
+      const int rt = tile % p.rt_total;
       const size_t goff = static_cast<size_t>(rt / p.rtpg) * p.out_gstride;
       const float *wsg = F8 ? p.wscale[rt / p.rtpg] : nullptr;
-      const int tokt = (tile % p.tok_tiles) * BN;
+      const int tokt = (tile / p.rt_total) * BN;
       const float *sp = reinterpret_cast<const float *>(sA);
       for (int t0 = 0; t0 < tasks; t0 += 128) {   // every thread takes each round (shuffles in SwiGLU)
         const int task = t0 + et;
@@ -786,7 +1048,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
           }
         }
         const int n = valid ? (rt % p.rtpg) * BM + row : p.N;   // n >= N: nothing stored
-        finalize(p, v, n, tokt + grp * 16, goff, wsg);
+        finalize<CB_>(p, v, n, tokt + grp * 16, goff, wsg, rt / p.rtpg, xch);
       }
     }
     cluster_sync();   // nobody leaves while others still read its share
@@ -911,7 +1173,7 @@ int gemm_token_tile(int M, bool split, bool f8) {
   return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : (M <= 128 || split || f8) ? 128 : 256;
 }
 
-GemmPlan gemm_plan(int M, int N, int K, int n_groups, bool f8, bool split, bool swiglu, int per_sm, int num_sms,
+GemmPlan gemm_plan(int M, int N, int K, int n_groups, bool f8, bool split, bool paired, int per_sm, int num_sms,
                    int gemm_ctas) {
   GemmPlan pl = {};
   pl.BN = gemm_token_tile(M, split, f8);
@@ -946,9 +1208,9 @@ GemmPlan gemm_plan(int M, int N, int K, int n_groups, bool f8, bool split, bool 
     // all pipeline fill; at least 2-way where the k-range allows)
     long long s = std::min<long long>(std::min<long long>(8, cap / pl.tiles),
                                       std::min<long long>(pl.kbpt, std::max<long long>(2, pl.kbpt / 8)));
-    // SwiGLU pairs rows 2i / 2i+1 in neighbouring lanes: row ranges must be
-    // even-aligned, so a power-of-two cluster there
-    if (swiglu)
+    // SwiGLU and the short conv pair rows 2i / 2i+1 in neighbouring lanes:
+    // row ranges must be even-aligned, so a power-of-two cluster there
+    if (paired)
       while (s & (s - 1)) --s;
     if (s >= 2) {
       pl.csk = static_cast<int>(s);
@@ -962,7 +1224,8 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   const int M = op.M, N = op.N, K = op.K;
   const char *name = op.name;
   if (M <= 0 || N <= 0 || K <= 0) return DFLASH_OK;
-  if ((!op.W && op.n_groups <= 1) || !op.X || !op.out) return set_error(DFLASH_ERR_ARG, "gemm %s: null operand", name);
+  if ((!op.W && op.n_groups <= 1) || !op.X || (!op.out && op.epi != EPI_HEADS))
+    return set_error(DFLASH_ERR_ARG, "gemm %s: null operand", name);
   const uintptr_t al = reinterpret_cast<uintptr_t>(op.W) | reinterpret_cast<uintptr_t>(op.X) |
                        reinterpret_cast<uintptr_t>(op.X_lo);
   const bool f8 = op.w_fp8;
@@ -979,7 +1242,27 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   const int per_sm = f8 ? (split ? per_sm_of<true, true>(BN) : per_sm_of<false, true>(BN))
                         : (split ? per_sm_of<true, false>(BN) : per_sm_of<false, false>(BN));
   if (per_sm < 0) return per_sm;
-  const GemmPlan pl = gemm_plan(M, N, K, n_groups, f8, split, epi == EPI_SWIGLU, per_sm, lc.num_sms, lc.gemm_ctas);
+  const bool conv = epi == EPI_CONV_PRE || epi == EPI_CONV_POST;
+  if (conv) {
+    const uintptr_t ya = reinterpret_cast<uintptr_t>(op.conv_y) | reinterpret_cast<uintptr_t>(op.conv_y_lo) |
+                         reinterpret_cast<uintptr_t>(op.conv_y32) | reinterpret_cast<uintptr_t>(op.out) |
+                         reinterpret_cast<uintptr_t>(op.out_lo);
+    if (N % 2 || !op.bias || op.conv_S < 1 || op.ldy % 8 || op.ldo % 8 || (ya & 31) ||
+        (epi == EPI_CONV_PRE ? !op.conv_y : !op.conv_y32))
+      return set_error(DFLASH_ERR_ARG, "gemm %s: short-conv epilogue operands", name);
+  }
+  if (epi == EPI_HEADS) {
+    const HeadArgs &h = op.head;
+    const int heads = h.mode == 1 ? h.nq + 2 * h.nkv : 2 * h.nkv;
+    const bool ok = (h.mode == 1 || h.mode == 2) && h.nkv > 0 && N == heads * BM && h.cs &&
+                    (h.mode == 2 ? (h.k_cache && h.v_cache && h.tok_page && h.tok_slot && h.cu_new && h.ctx_saved &&
+                                    h.ctx_out && n_groups <= MAX_GROUPS)
+                                 : (h.q && h.bk && h.bv && h.S >= 1 && h.S <= 16 && n_groups == 1)) &&
+                    (!h.norm || (h.mode == 2 || h.gq) && h.gk[0]);
+    if (!ok) return set_error(DFLASH_ERR_ARG, "gemm %s: head epilogue operands", name);
+  }
+  const GemmPlan pl = gemm_plan(M, N, K, n_groups, f8, split, epi == EPI_SWIGLU || conv, per_sm, lc.num_sms,
+                                lc.gemm_ctas);
   const long long tiles = pl.tiles;
   Params p = {};
   p.M = M;
@@ -989,6 +1272,7 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   p.rtpg = pl.rtpg;
   p.out_gstride = op.out_gstride;
   p.tok_tiles = pl.tok_tiles;
+  p.rt_total = pl.rtpg * n_groups;
   p.kbpt = pl.kbpt;
   p.total = pl.total;
   p.G = pl.G;
@@ -1001,6 +1285,12 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   p.out2_lo = op.out2_lo;
   p.ldo2 = op.ldo2;
   p.bias = op.bias;
+  p.cy = op.conv_y;
+  p.cy_lo = op.conv_y_lo;
+  p.cy32 = op.conv_y32;
+  p.ldy = op.ldy;
+  p.cS = op.conv_S;
+  p.head = op.head;
   if (f8) {
     for (int g = 0; g < p.n_groups; ++g) {
       p.wscale[g] = p.n_groups > 1 ? op.wscale_g[g] : op.wscale;
@@ -1036,7 +1326,12 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
     tXl = tX;
   }
   const double xb = (split ? 4.0 : 2.0) * M * K;
-  const double out_bytes = (epi == EPI_F32 || epi == EPI_TANH_BIAS) ? 4.0 * M * N
+  // short conv: y read and the result written for 8N channels (pre: bf16 y
+  // hi / lo in, hi / lo out; post: fp32 y in, fp32 residual read and written)
+  const double out_bytes = epi == EPI_HEADS       ? 2.0 * M * N
+                           : epi == EPI_CONV_PRE  ? (split ? 64.0 : 32.0) * M * N
+                           : epi == EPI_CONV_POST ? 96.0 * M * N
+                           : (epi == EPI_F32 || epi == EPI_TANH_BIAS) ? 4.0 * M * N
                            : epi == EPI_ADD_F32                      ? 8.0 * M * N
                            : epi == EPI_F32_SPLIT                    ? 8.0 * M * N
                            : epi == EPI_SWIGLU                       ? (op.out_lo ? 2.0 : 1.0) * M * N

@@ -219,12 +219,14 @@ constexpr int NOALLOC_MAX_DEVICES = 64;
 void *g_scratch_addr[NOALLOC_MAX_DEVICES] = {};
 std::mutex g_scratch_mu;
 
-// Device address of the scratch array on the current device.  The array's
-// name is only a host-side stand-in; its device address is looked up once
-// per device, with that device current, and cached.
-int scratch_address(void **out) {
+// Device address of the scratch array on the current device (returned with
+// the device ordinal).  The array's name is only a host-side stand-in; its
+// device address is looked up once per device, with that device current, and
+// cached (valid for the device's context: a cudaDeviceReset makes it stale).
+int scratch_address(void **out, int *dev_out) {
   int dev = -1;
   if (int e = cuda_check(cudaGetDevice(&dev), "noalloc top-16: cudaGetDevice")) return e;
+  *dev_out = dev;
   if (dev < 0 || dev >= NOALLOC_MAX_DEVICES)
     return set_error(DFLASH_ERR_UNSUPPORTED, "noalloc top-16: device ordinal %d beyond %d", dev, NOALLOC_MAX_DEVICES);
   std::lock_guard<std::mutex> lock(g_scratch_mu);
@@ -251,7 +253,8 @@ extern "C" DFLASH_API int dflash_topk16_noalloc(const float *logits, int rows, i
     return set_error(DFLASH_ERR_SHAPE, "noalloc top-16: %d rows exceed the fixed scratch limit of %d rows", rows,
                      NOALLOC_MAX_ROWS);
   void *base = nullptr;
-  if (int e = scratch_address(&base)) return e;
+  int dev = 0;
+  if (int e = scratch_address(&base, &dev)) return e;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the completion counters must start at zero; the array keeps whatever the
   // previous call left, so clear them on the stream first
@@ -259,9 +262,11 @@ extern "C" DFLASH_API int dflash_topk16_noalloc(const float *logits, int rows, i
     return e;
   Launch lc;
   lc.stream = s;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) lc.num_sms = sms;
+  int sms = 0;
+  if (int e = cuda_check(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+                         "noalloc top-16: SM count"))
+    return e;
+  if (sms > 0) lc.num_sms = sms;
   return topk16(lc, logits, rows, vocab, topk_ids, topk_logits,
                 reinterpret_cast<uint64_t *>(static_cast<char *>(base) + NOALLOC_CTR_BYTES), static_cast<int *>(base),
                 NOALLOC_MAX_CHUNKS);

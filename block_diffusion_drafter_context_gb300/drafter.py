@@ -59,8 +59,10 @@ CONV_SITES = ("pre_attn", "post_attn", "pre_ffn", "post_ffn")
 
 def upload_weights(cfg, W: dict, device="cuda") -> dict:
     """Upload a weight dict (layout of the synthetic generator) and pack it:
-    w_qkv = [w_q; w_k; w_v] rows; w_gu rows interleaved gate_i, up_i.  FP8
-    weights upload their codes (uint8) and put the row scales under s_*."""
+    w_qkv = [w_q; w_k; w_v] rows; w_gu rows interleaved gate_i, up_i; each
+    short-conv site's [a; b] coefficient rows (and biases) interleaved per
+    channel group, a_g, b_g.  FP8 weights upload their codes (uint8) and put
+    the row scales under s_*."""
     torch = _torch()
 
     def d(a):
@@ -76,6 +78,11 @@ def upload_weights(cfg, W: dict, device="cuda") -> dict:
 
     def interleave(a, b):
         return torch.stack([a, b], 1).reshape(2 * a.shape[0], *a.shape[1:]).contiguous()
+
+    def interleave_halves(t):
+        """[a; b] rows (first half a, second half b) -> a_0, b_0, a_1, b_1, ..."""
+        h = t.shape[0] // 2
+        return interleave(t[:h], t[h:])
 
     out = {k: d(W[k]) for k in ("w_fc", "g_fc", "embed", "lm_head", "g_final")}
     fp8 = _is_fp8(W["lm_head"])
@@ -97,10 +104,10 @@ def upload_weights(cfg, W: dict, device="cuda") -> dict:
             L["s_o"], L["s_down"] = sc(lw["w_o"]), sc(lw["w_down"])
             L["s_gu"] = interleave(sc(lw["w_gate"]), sc(lw["w_up"]))
         if "conv" in lw:
-            L["w_conv"] = [d(lw["conv"][s][0]) for s in CONV_SITES]
-            L["b_conv"] = [d(lw["conv"][s][1]) for s in CONV_SITES]
+            L["w_conv"] = [interleave_halves(d(lw["conv"][s][0])) for s in CONV_SITES]
+            L["b_conv"] = [interleave_halves(d(lw["conv"][s][1])) for s in CONV_SITES]
             if fp8:
-                L["s_conv"] = [sc(lw["conv"][s][0]) for s in CONV_SITES]
+                L["s_conv"] = [interleave_halves(sc(lw["conv"][s][0])) for s in CONV_SITES]
         out["layers"].append(L)
     if "sel" in W:
         s = W["sel"]

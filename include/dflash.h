@@ -128,14 +128,16 @@ typedef struct dflash_layer_weights {
   const void *w_down;    /* [H, F]                                           */
   const void *w_conv[4]; /* [H/8, H] conv coefficient projections for the
                             sites pre_attn, post_attn, pre_ffn, post_ffn;
-                            rows 0..H/16-1 = current tap, H/16.. = previous */
-  const float *b_conv[4];/* [H/8] their biases                               */
+                            rows interleaved per 16-channel group g: row 2g
+                            = current-tap coefficient of g, row 2g+1 =
+                            previous-tap coefficient of g                    */
+  const float *b_conv[4];/* [H/8] their biases, interleaved like the rows    */
   /* weight_fp8 only: fp32 per-output-row scales of the matrices above */
   const float *s_qkv;    /* [(nq+2nkv)*d]                                     */
   const float *s_o;      /* [H]                                               */
   const float *s_gu;     /* [2F], interleaved like w_gu                       */
   const float *s_down;   /* [H]                                               */
-  const float *s_conv[4];/* [H/8]                                             */
+  const float *s_conv[4];/* [H/8], interleaved like w_conv                   */
 } dflash_layer_weights;
 
 /* Model weights (device pointers, not owned; the layer array is host memory
@@ -373,9 +375,12 @@ DFLASH_API int dflash_debug_e4m3_to_bf16(const void *codes, int n, void *out, df
  *   topk_ids:    device int32 [rows][16] out; topk_logits: device fp32 [rows][16] out.
  *   rows <= 1024, else DFLASH_ERR_SHAPE (nothing launched).
  * Allocates nothing (no cudaMalloc / cudaFree).  The first call on each
- * device looks up the array's device address; make that first call before
- * any stream capture.  All calls share the array and clear its counters at
- * the start of each call: calls that overlap on the GPU race. */
+ * device looks up the array's device address and keeps it; make that first
+ * call before any stream capture.  The kept address belongs to the device's
+ * current CUDA context: after cudaDeviceReset (a new context) it is stale,
+ * so a process that resets a device must not call this entry point on that
+ * device again.  All calls share the array and clear its counters at the
+ * start of each call: calls that overlap on the GPU race. */
 DFLASH_API int dflash_topk16_noalloc(const float *logits, int rows, int vocab, int32_t *topk_ids,
                                      float *topk_logits, dflash_stream_t stream);
 

@@ -177,6 +177,9 @@ WORKLOADS = {
     # 8 query heads per KV head (the attention's plain row layout) at block size 5
     "T1G8S5": Workload("T1G8S5", replace(SMALL_BF16, name="small-bf16-g8-block5", n_q_heads=8, n_kv_heads=1, block=5),
                        batch=3, ctx_lo=0, ctx_hi=0, explicit_ctx=(10, 64, 450), seed=19),
+    # one drafter layer (the context injection's single-group GEMM)
+    "T1L1": Workload("T1L1", replace(SMALL_BF16, name="small-bf16-1layer", n_layers=1),
+                     batch=2, ctx_lo=0, ctx_hi=0, explicit_ctx=(50, 130), seed=20),
     "T1D2S2": Workload("T1D2S2", replace(SMALL_BF16, name="small-bf16-dflash2-block2", use_conv=True,
                                          use_selector=True, split_act=True, block=2),
                        batch=3, ctx_lo=0, ctx_hi=0, explicit_ctx=(1, 64, 200), seed=16),

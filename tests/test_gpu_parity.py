@@ -31,7 +31,7 @@ def case(name, **kw):
 
 
 # ----------------------------------------------------------------- injection
-@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2", "T1S5", "T1F8", "T1D2F8"])
+@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2", "T1S5", "T1F8", "T1D2F8", "T1L1"])
 def test_inject_matches_oracle(name):
     c = case(name)
     assert c.dr.status() == 0
@@ -55,7 +55,30 @@ def _gap_ok(vals_sorted, i, thr=1e-3):
     return min(lo, hi) >= thr
 
 
-@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2", "T1S5", "T0D2S7", "T1D2S2", "T1F8", "T1D2F8", "T1G8S5"])
+def end_to_end_ids(ids, z_gpu, z_ref):
+    """Top-16 ids of one request against the oracle's own, end to end.
+
+    Returns (checked, agree_1e3, ranks_1e3): `checked` asserts bit-exact ids
+    at every rank whose oracle gap to both neighbours exceeds twice the
+    measured max |logit error| (no rounding within that error can reorder
+    them); the counts give the agreement rate under the 1e-3 gap rule."""
+    err = float(np.abs(np.asarray(z_gpu, np.float64) - z_ref).max())
+    oid = O.top_k(z_ref, 17)[0]
+    full = -np.sort(-z_ref, axis=1)
+    checked = agree = ranks = 0
+    for j in range(z_ref.shape[0]):
+        for r in range(16):
+            if _gap_ok(full[j], r, 2 * err):
+                assert ids[j, r] == oid[j, r], (j, r, err)
+                checked += 1
+            if _gap_ok(full[j], r):
+                ranks += 1
+                agree += int(ids[j, r] == oid[j, r])
+    return checked, agree, ranks
+
+
+@pytest.mark.parametrize("name", ["C0", "T0D2", "T1", "T1D2", "T1S5", "T0D2S7", "T1D2S2", "T1F8", "T1D2F8", "T1G8S5",
+                                  "T1L1"])
 def test_draft_matches_oracle(name):
     c = case(name)
     out = c.draft()
@@ -80,6 +103,10 @@ def test_draft_matches_oracle(name):
                 for r in range(16):
                     if _gap_ok(full[j], r):
                         assert ids[b, j, r] == ref["cand_ids"][j, r], (b, j, r)
+        else:
+            checked, agree, ranks = end_to_end_ids(ids[b], z[b], ref["z"])
+            print(f"{name} request {b}: end-to-end top-16 ids bit-exact at {checked} ranks beyond twice the logit "
+                  f"error; {agree}/{ranks} agree where the oracle's gap is >= 1e-3")
 
 
 @pytest.mark.parametrize("name", ["T0D2", "T1D2", "T1", "T0D2S7", "T1D2S2", "T1D2F8"])

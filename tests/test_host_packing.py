@@ -57,10 +57,18 @@ def test_packed_rows_follow_the_header(name):
             assert "s_qkv" not in L and gu.dtype == np.uint16
         if cfg.use_conv:
             assert len(L["w_conv"]) == 4 and len(L["b_conv"]) == 4
+            G = cfg.hidden // 16
             for j, site in enumerate(D.CONV_SITES):
-                assert np.array_equal(_np(L["w_conv"][j]), _codes(lw["conv"][site][0]))
+                # rows interleaved per channel group: 2g = current tap (row g
+                # of [a; b]), 2g+1 = previous tap (row G + g)
+                w_src, b_src = _codes(lw["conv"][site][0]), np.asarray(lw["conv"][site][1])
+                w_pk, b_pk = _np(L["w_conv"][j]), _np(L["b_conv"][j])
+                assert w_pk.shape == w_src.shape == (2 * G, cfg.hidden)
+                assert np.array_equal(w_pk[0::2], w_src[:G]) and np.array_equal(w_pk[1::2], w_src[G:])
+                assert np.array_equal(b_pk[0::2], b_src[:G]) and np.array_equal(b_pk[1::2], b_src[G:])
                 if fp8:
-                    assert np.array_equal(_np(L["s_conv"][j]), lw["conv"][site][0].scale)
+                    s_src, s_pk = lw["conv"][site][0].scale, _np(L["s_conv"][j])
+                    assert np.array_equal(s_pk[0::2], s_src[:G]) and np.array_equal(s_pk[1::2], s_src[G:])
     if fp8:
         assert np.array_equal(_np(dw["s_lm_head"]), W["lm_head"].scale)
         assert np.array_equal(_np(dw["lm_head"]), W["lm_head"].codes)

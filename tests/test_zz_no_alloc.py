@@ -10,6 +10,7 @@ second call finds the first call's leftovers in the shared array).
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.
 """
+import numpy as np
 import pytest
 
 pytestmark = pytest.mark.gpu
@@ -39,3 +40,28 @@ def test_noalloc_top16_matches_draft_block_twice():
     with pytest.raises(Bd.DflashError) as e:
         Bd.dflash_topk16_noalloc(logits, 1025, V, ids, vals)
     assert e.value.code == -2
+
+
+@pytest.mark.parametrize("rows,vocab", [(1024, 40001), (3, 151936)])
+def test_noalloc_top16_matches_oracle_at_the_scratch_limits(rows, vocab):
+    """Seeded N(0,1) fp32 logits against the oracle's top-16 (value
+    descending, ties to the lower id) of the same values.  1024 rows is the
+    row limit, and a vocabulary that is not a multiple of 4 takes the scalar
+    load path; 3 rows of 151 936 fill all 32 chunks of the fixed scratch."""
+    import torch
+
+    import oracle as O
+    from block_diffusion_drafter_context_gb300 import binding as Bd
+    from block_diffusion_drafter_context_gb300.build import build
+
+    build()
+    z = np.random.default_rng(rows + vocab).standard_normal((rows, vocab), dtype=np.float32)
+    ref_ids, ref_vals = O.top_k(z.astype(np.float64), 16)
+    logits = torch.from_numpy(z).cuda()
+    for _ in range(2):   # the second call finds the first call's leftovers in the shared array
+        ids = torch.full((rows, 16), -1, dtype=torch.int32, device="cuda")
+        vals = torch.full((rows, 16), float("nan"), dtype=torch.float32, device="cuda")
+        Bd.dflash_topk16_noalloc(logits, rows, vocab, ids, vals)
+        torch.cuda.synchronize()
+        assert (ids.cpu().numpy() == ref_ids).all()
+        assert (vals.cpu().numpy().astype(np.float64) == ref_vals).all()
