@@ -416,6 +416,7 @@ def run_workload(args, wl, steps, warmup, world, local, dev, headline):
     B, S, J = wl.batch, cfg.block, cfg.block - 1
     prefill = 0 if wl.kv_fill == "template" else int(ctx.max())
     dr = Drafter(cfg, W, max_batch=B, max_new_tokens=max(S * B, prefill), device=dev)
+    Bd.dflash_set_gemm_pairs(dr.ctx, bool(args.gemm_pairs))
     kv = PagedKV(cfg, table, npages, device=dev)
     stream = torch.cuda.current_stream().cuda_stream
     templates = kv_templates(wl, npages)
@@ -775,7 +776,7 @@ def run_ours(args):
         "cpu_baseline": res.get("cpu_baseline"),
         "e2e": res["e2e"], "e2e_graph": res["e2e_graph"],
         "gpu_launches": res["gpu_launches"], "launches_per_step": res["launches_per_step"],
-        "clocks": res["clocks"],
+        "clocks": res["clocks"], "gemm_pairs": bool(args.gemm_pairs),
     }
     for k in ("draft_tokens_per_s", "expected_committed_tokens_per_s", "mean_accept_len", "expected_accept_len",
               "per_kernel", "instrumented_ms_per_step", "eager_ms_per_step", "prefill_injection", "setup_s"):
@@ -809,6 +810,8 @@ def main():
     ap.add_argument("--mode", default="greedy", choices=["greedy", "sampling"],
                     help="path selection and verification: greedy (default) or sampling + rejection")
     ap.add_argument("--oracle-probe", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--gemm-pairs", type=int, default=0,
+                    help="256-token GEMM tiles on CTA pairs with the 2-SM MMA (1) or single CTAs (0, default)")
     # smaller variants of the headline workload for profiling captures
     ap.add_argument("--layers", type=int, default=None, help="drafter layers (profiling cases)")
     ap.add_argument("--batch", type=int, default=None, help="requests (profiling cases)")

@@ -26,7 +26,8 @@ EXPORTS = (
     "dflash_profile_begin", "dflash_profile_end", "dflash_debug_wait_flag", "dflash_last_error",
     "dflash_topk16_noalloc", "dflash_sample_path", "dflash_verify_rejection", "dflash_set_block_size",
     "dflash_get_block_size", "dflash_debug_e4m3_to_bf16", "dflash_debug_gemm_scratch_bytes", "dflash_debug_gemm",
-    "dflash_debug_gemm_plan",
+    "dflash_debug_gemm_plan", "dflash_set_gemm_pairs", "dflash_fp8_weights_to_bf16",
+    "dflash_debug_gemm_pair_clusters",
 )
 
 
@@ -43,14 +44,17 @@ class dflash_layer_weights(ctypes.Structure):
                 ("w_o", c_void_p), ("g_ffn", c_void_p), ("w_gu", c_void_p), ("w_down", c_void_p),
                 ("w_conv", c_void_p * 4), ("b_conv", c_void_p * 4),
                 ("s_qkv", c_void_p), ("s_o", c_void_p), ("s_gu", c_void_p), ("s_down", c_void_p),
-                ("s_conv", c_void_p * 4)]
+                ("s_conv", c_void_p * 4),
+                ("w_qkv_bf16", c_void_p), ("w_o_bf16", c_void_p), ("w_gu_bf16", c_void_p), ("w_down_bf16", c_void_p),
+                ("w_conv_bf16", c_void_p * 4)]
 
 
 class dflash_weights(ctypes.Structure):
     _fields_ = [("w_fc", c_void_p), ("g_fc", c_void_p), ("embed", c_void_p), ("lm_head", c_void_p),
                 ("g_final", c_void_p), ("layers", POINTER(dflash_layer_weights)),
                 ("sel_e256", c_void_p), ("sel_a", c_void_p), ("sel_b", c_void_p),
-                ("sel_w_g", c_void_p), ("sel_b_g", c_float), ("s_fc", c_void_p), ("s_lm_head", c_void_p)]
+                ("sel_w_g", c_void_p), ("sel_b_g", c_float), ("s_fc", c_void_p), ("s_lm_head", c_void_p),
+                ("w_fc_bf16", c_void_p), ("lm_head_bf16", c_void_p)]
 
 
 class dflash_kv(ctypes.Structure):
@@ -95,6 +99,7 @@ def load(path: str = LIB_PATH):
         "dflash_read_status": (i, [vp, POINTER(c_int), vp]),
         "dflash_set_wait_timeout": (i, [vp, c_ulonglong]),
         "dflash_set_gemm_ctas": (i, [vp, i]),
+        "dflash_set_gemm_pairs": (i, [vp, i]),
         "dflash_set_attn_split": (i, [vp, i]),
         "dflash_set_block_size": (i, [vp, i]),
         "dflash_get_block_size": (i, [vp]),
@@ -102,6 +107,8 @@ def load(path: str = LIB_PATH):
         "dflash_profile_end": (i, [vp, POINTER(dflash_kernel_stat), i, POINTER(c_int)]),
         "dflash_debug_wait_flag": (i, [vp, c_ulonglong, vp, vp]),
         "dflash_debug_e4m3_to_bf16": (i, [vp, i, vp, vp]),
+        "dflash_fp8_weights_to_bf16": (i, [vp, vp, i, i, vp, vp]),
+        "dflash_debug_gemm_pair_clusters": (i, []),
         "dflash_debug_gemm_scratch_bytes": (c_size_t, []),
         "dflash_debug_gemm": (i, [vp, vp, i, vp, i, i, i, vp, vp, c_size_t, i, vp]),
         "dflash_debug_gemm_plan": (i, [i, i, i, i, i, i, i, i, i, i, vp]),
@@ -210,6 +217,10 @@ def dflash_set_gemm_ctas(ctx, n: int):
     return _check(load().dflash_set_gemm_ctas(ctx, n))
 
 
+def dflash_set_gemm_pairs(ctx, on: bool):
+    return _check(load().dflash_set_gemm_pairs(ctx, int(bool(on))))
+
+
 def dflash_set_attn_split(ctx, tokens: int):
     return _check(load().dflash_set_attn_split(ctx, tokens))
 
@@ -240,6 +251,14 @@ def dflash_debug_gemm_plan(M, N, K, n_groups=1, w_fp8=False, split_act=False, sw
     _check(load().dflash_debug_gemm_plan(M, N, K, n_groups, int(w_fp8), int(split_act), int(swiglu), per_sm, num_sms,
                                          gemm_ctas, out))
     return dict(zip(GEMM_PLAN_KEYS, (int(v) for v in out)))
+
+
+def dflash_debug_gemm_pair_clusters() -> int:
+    return load().dflash_debug_gemm_pair_clusters()
+
+
+def dflash_fp8_weights_to_bf16(codes, scale, rows, cols, out, stream=None):
+    return _check(load().dflash_fp8_weights_to_bf16(_p(codes), _p(scale), rows, cols, _p(out), _stream(stream)))
 
 
 def dflash_debug_e4m3_to_bf16(codes, n, out, stream=None):

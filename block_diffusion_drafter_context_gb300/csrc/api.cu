@@ -21,6 +21,7 @@ struct dflash_ctx {
   int num_sms = 148;
   unsigned long long timeout_ns = 2000000000ull;
   int gemm_ctas = 0;
+  int gemm_pairs = 0;
   int attn_split = 0;
   int block = 16;   // runtime block size S (2..cfg.block_size)
   dflash::Profiler prof;
@@ -140,7 +141,6 @@ struct Layout {
   size_t x, u, u2, qkv, q, bk, bv, o, ysub, coef, hmid, hmask, hfinal, logits, scores, lse;
   size_t u_lo, u2_lo, o_lo, ysub_lo, hmid_lo, hmask_lo, ysub32;
   size_t fc, f, f_lo, kvproj, ctx_saved;
-  size_t cs_blk, cs_inj, tok_page, tok_slot;
   size_t total;
   size_t gemm_part_floats;
 };
@@ -200,13 +200,6 @@ Layout layout(const dflash_ctx *c, int B, int Tn, int S_ = 0) {
   L.f_lo = take(tl * Tn * H);
   L.kvproj = take(4ull * g.n_layers * Tn * 2 * nkv * d);
   L.ctx_saved = take(sizeof(int) * static_cast<size_t>(B));
-  // RoPE (cos, sin) per row and rotation pair for the head epilogues of the
-  // QKV projection (block rows) and of the K/V injection (new tokens), and
-  // each injected token's pool page and slot
-  L.cs_blk = take(8 * R * (d / 2));
-  L.cs_inj = take(8ull * Tn * (d / 2));
-  L.tok_page = take(sizeof(int) * static_cast<size_t>(Tn));
-  L.tok_slot = take(sizeof(int) * static_cast<size_t>(Tn));
   L.total = off;
   return L;
 }
@@ -225,6 +218,7 @@ Launch make_launch(dflash_ctx *c, void *ws, cudaStream_t s) {
   lc.status = ws ? at<int>(ws, 0) : nullptr;
   lc.timeout_ns = c->timeout_ns;
   lc.gemm_ctas = c->gemm_ctas;
+  lc.gemm_pairs = c->gemm_pairs;
   lc.prof = &c->prof;
   return lc;
 }
@@ -259,9 +253,18 @@ GemmOp mk(const void *W, int ldw, const void *X, const void *X_lo, int ldx, int 
   return o;
 }
 
-// The weight of a GEMM: bf16 matrix, or (weight_fp8) E4M3 codes with their row scales.
-GemmOp wq(const dflash_ctx *c, GemmOp op, const float *scale) {
+// The weight of a GEMM: bf16 matrix, or (weight_fp8) E4M3 codes with their
+// row scales - unless a bf16 copy of the matrix is given and the launch is
+// tensor-bound (token tile of 128 or more: the FP8 tiles stop at 128 tokens,
+// where the weight stream no longer bounds the launch and the conversion
+// only costs), which then takes the copy.
+GemmOp wq(const dflash_ctx *c, GemmOp op, const float *scale, const void *bf16_copy = nullptr) {
   if (c->cfg.weight_fp8) {
+    const bool split = op.X_lo != nullptr;
+    if (bf16_copy && gemm_token_tile(op.M, split, false) >= 128) {
+      op.W = bf16_copy;
+      return op;
+    }
     op.w_fp8 = true;
     op.wscale = scale;
   }
@@ -383,6 +386,12 @@ int dflash_set_gemm_ctas(dflash_ctx *ctx, int ctas) {
   return DFLASH_OK;
 }
 
+int dflash_set_gemm_pairs(dflash_ctx *ctx, int on) {
+  if (!ctx) return set_error(DFLASH_ERR_ARG, "null context");
+  ctx->gemm_pairs = on != 0;
+  return DFLASH_OK;
+}
+
 int dflash_set_block_size(dflash_ctx *ctx, int block_size) {
   if (!ctx) return set_error(DFLASH_ERR_ARG, "null context");
   if (block_size < 2 || block_size > ctx->cfg.block_size)
@@ -418,28 +427,14 @@ int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv, const void *targ
   const size_t te = f32 ? 4 : 2;
   const bool split = !f32 && g.split_act;
   void *f_lo = split ? at<void>(workspace, L.f_lo) : nullptr;
-  // context feature: fc projection, then RMSNorm (bf16: the same kernel
-  // places every new token - pool page, slot - and tabulates its rotation
-  // for the K head epilogue below)
+  // context feature: fc projection, then RMSNorm
   if (int e = proj(ctx, lc, workspace, L,
                    wq(ctx, mk(ctx->w.w_fc, K, target_hidden, nullptr, K, total_new, H, K, EPI_F32,
                               at<float>(workspace, L.fc), H, "fc"),
-                      ctx->w.s_fc)))
+                      ctx->w.s_fc, ctx->w.w_fc_bf16)))
     return e;
-  InjectSlots slots;
-  slots.cu_new = cu_new;
-  slots.page_table = kv->page_table;
-  slots.max_pages = kv->max_pages;
-  slots.num_pages = kv->num_pages;
-  slots.page = g.page_size;
-  slots.d = d;
-  slots.rope_base = g.rope_base;
-  slots.cs = at<float2>(workspace, L.cs_inj);
-  slots.tok_page = at<int32_t>(workspace, L.tok_page);
-  slots.tok_slot = at<int32_t>(workspace, L.tok_slot);
   if (int e = feature_norm(lc, f32, at<float>(workspace, L.fc), total_new, H, ctx->w.g_fc, g.eps, g.fc_norm != 0,
-                           at<void>(workspace, L.f), f_lo, ctx_len_in, at<int32_t>(workspace, L.ctx_saved), batch,
-                           f32 ? nullptr : &slots))
+                           at<void>(workspace, L.f), f_lo, ctx_len_in, at<int32_t>(workspace, L.ctx_saved), batch))
     return e;
   // every layer's own K/V projection of the feature (rows nq*d.. of w_qkv);
   // on tensor cores all layers share one grouped launch
@@ -447,41 +442,21 @@ int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv, const void *targ
   GemmOp kvop = mk(nullptr, H, at<void>(workspace, L.f), f_lo, H, total_new, 2 * nkv * d, H, EPI_F32,
                    at<float>(workspace, L.kvproj), 2 * nkv * d, "kv_inject");
   kvop.out_gstride = static_cast<size_t>(total_new) * 2 * nkv * d;
-  kvop.w_fp8 = g.weight_fp8 != 0;
-  const size_t tw = kvop.w_fp8 ? 1 : te;   // bytes per weight element
+  // FP8 codes, or the layers' bf16 copies for a tensor-bound launch (as wq)
+  bool copies = g.weight_fp8 != 0 && gemm_token_tile(total_new, split, false) >= 128;
+  for (int l = 0; l < g.n_layers; ++l) copies = copies && ctx->layers[l].w_qkv_bf16;
+  kvop.w_fp8 = g.weight_fp8 != 0 && !copies;
+  const size_t tw = kvop.w_fp8 ? 1 : 2;   // bytes per weight element (fp32 path: te)
   for (int l = 0; l < g.n_layers; ++l) {
     const dflash_layer_weights &lw = ctx->layers[l];
-    kvop.Wg[l] = static_cast<const char *>(lw.w_qkv) + tw * static_cast<size_t>(nq) * d * H;
+    const void *wl = copies ? lw.w_qkv_bf16 : lw.w_qkv;
+    kvop.Wg[l] = static_cast<const char *>(wl) + (f32 ? te : tw) * static_cast<size_t>(nq) * d * H;
     if (kvop.w_fp8) kvop.wscale_g[l] = lw.s_qkv + static_cast<size_t>(nq) * d;
     gk[l] = lw.g_k;
   }
-  if (!f32) {
-    // bf16: every layer's K/V projection in one grouped launch (one group per
-    // layer) whose head epilogue k-norms and rotates the K heads and writes K
-    // and V^T straight into the paged cache, then sets ctx_len_out
-    HeadArgs &ha = kvop.head;
-    ha.mode = 2;
-    ha.nkv = nkv;
-    ha.norm = g.qk_norm != 0;
-    ha.eps = g.eps;
-    for (int l = 0; l < g.n_layers; ++l) ha.gk[l] = gk[l];
-    ha.cs = at<float2>(workspace, L.cs_inj);
-    ha.k_cache = kv->k_cache;
-    ha.v_cache = kv->v_cache;
-    ha.layer_elems = layer_elems(ctx, kv);
-    ha.tok_page = at<int32_t>(workspace, L.tok_page);
-    ha.tok_slot = at<int32_t>(workspace, L.tok_slot);
-    ha.cu_new = cu_new;
-    ha.ctx_saved = at<int32_t>(workspace, L.ctx_saved);
-    ha.ctx_out = ctx_len_out;
-    ha.B = batch;
-    kvop.epi = EPI_HEADS;
+  if (!f32 && (2 * nkv * d) % 128 == 0 && g.n_layers > 1) {
     kvop.n_groups = g.n_layers;
-    if (g.n_layers == 1) {
-      kvop.W = kvop.Wg[0];
-      kvop.wscale = kvop.wscale_g[0];
-    }
-    return proj(ctx, lc, workspace, L, kvop);
+    if (int e = proj(ctx, lc, workspace, L, kvop)) return e;
   } else {
     for (int l = 0; l < g.n_layers; ++l) {
       GemmOp one = kvop;
@@ -528,85 +503,48 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
   float *ysub32 = at<float>(ws, L.ysub32);
 
   if (int e = embed_rmsnorm(lc, f32, ctx->w.embed, anchor_ids, g.mask_id, V, ctx->layers[0].g_attn, g.eps, B, S, H, x,
-                            u, u_lo, ctx_len, d, g.rope_base, f32 ? nullptr : at<float2>(ws, L.cs_blk)))
+                            u, u_lo))
     return e;
   const size_t lelems = layer_elems(ctx, kv);
   const size_t te = f32 ? 4 : 2;
-  // short conv at one site (weight rows interleaved per channel group: 2g =
-  // current tap, 2g+1 = previous tap).  bf16: one GEMM whose epilogue turns
-  // the coefficients tanh(W_c y + b_c) into the convolved rows; fp32: the
-  // coefficients [R][H/8], then the conv kernel.  Pre sites (y = u) write
-  // out (+ out_lo); post sites (y = ysub32, the sublayer output) add into x.
-  auto conv_site = [&](int site, const dflash_layer_weights &lw, const void *y, const void *y_lo, void *out_t,
-                       void *out_lo, float *x_add) -> int {
-    const void *X = x_add ? (f32 ? static_cast<const void *>(ysub32) : ysub) : y;
-    const void *X_lo = x_add ? ysub_lo : y_lo;
-    if (f32) {
-      GemmOp op = mk(lw.w_conv[site], H, X, nullptr, H, R, G8, H, EPI_TANH_BIAS, coef, G8, "conv_coef");
-      op.bias = lw.b_conv[site];
-      if (int e = proj(ctx, lc, ws, L, op)) return e;
-      return conv_apply(lc, f32, x_add ? nullptr : y, nullptr, x_add ? ysub32 : nullptr, coef, B, S, H, out_t,
-                        nullptr, x_add);
-    }
-    GemmOp op = wq(ctx, mk(lw.w_conv[site], H, X, X_lo, H, R, G8, H, x_add ? EPI_CONV_POST : EPI_CONV_PRE,
-                           x_add ? static_cast<void *>(x_add) : out_t, H, "conv"),
-                   lw.s_conv[site]);
+  // conv coefficients of one site: tanh(W_c y + b_c), fp32 [R][H/8]
+  auto coef_gemm = [&](int site, const dflash_layer_weights &lw, const void *y, const void *y_lo) {
+    GemmOp op = wq(ctx, mk(lw.w_conv[site], H, y, y_lo, H, R, G8, H, EPI_TANH_BIAS, coef, G8, "conv_coef"),
+                   lw.s_conv[site], lw.w_conv_bf16[site]);
     op.bias = lw.b_conv[site];
-    op.out_lo = out_lo;
-    op.conv_y = y;
-    op.conv_y_lo = y_lo;
-    op.conv_y32 = x_add ? ysub32 : nullptr;
-    op.ldy = H;
-    op.conv_S = S;
     return proj(ctx, lc, ws, L, op);
   };
   // a sublayer's output projection: straight into the fp32 residual, or (conv)
   // into fp32 + bf16 halves, then the post-site conv adds it to the residual
-  auto out_proj = [&](int site, const dflash_layer_weights &lw, const void *Wm, const float *Ws, int K, const void *X,
-                      const void *X_lo, const char *name) -> int {
-    if (!g.use_conv) return proj(ctx, lc, ws, L, wq(ctx, mk(Wm, K, X, X_lo, K, R, H, K, EPI_ADD_F32, x, H, name), Ws));
-    GemmOp op = wq(ctx, mk(Wm, K, X, X_lo, K, R, H, K, f32 ? EPI_F32 : EPI_F32_SPLIT, ysub32, H, name), Ws);
+  auto out_proj = [&](int site, const dflash_layer_weights &lw, const void *Wm, const float *Ws, const void *Wb,
+                      int K, const void *X, const void *X_lo, const char *name) -> int {
+    if (!g.use_conv)
+      return proj(ctx, lc, ws, L, wq(ctx, mk(Wm, K, X, X_lo, K, R, H, K, EPI_ADD_F32, x, H, name), Ws, Wb));
+    GemmOp op = wq(ctx, mk(Wm, K, X, X_lo, K, R, H, K, f32 ? EPI_F32 : EPI_F32_SPLIT, ysub32, H, name), Ws, Wb);
     op.out2 = ysub;
     op.out2_lo = ysub_lo;
     op.ldo2 = H;
     if (int e = proj(ctx, lc, ws, L, op)) return e;
-    return conv_site(site, lw, nullptr, nullptr, nullptr, nullptr, x);
+    if (int e = coef_gemm(site, lw, f32 ? static_cast<const void *>(ysub32) : ysub, ysub_lo)) return e;
+    return conv_apply(lc, f32, nullptr, nullptr, ysub32, coef, B, S, H, nullptr, nullptr, x);
   };
   for (int l = 0; l < g.n_layers; ++l) {
     const dflash_layer_weights &lw = ctx->layers[l];
     const void *ua = u, *ua_lo = u_lo;
     // ---- attention sublayer
     if (g.use_conv) {
-      if (int e = conv_site(0, lw, u, u_lo, u2, u2_lo, nullptr)) return e;
+      if (int e = coef_gemm(0, lw, u, u_lo)) return e;
+      if (int e = conv_apply(lc, f32, u, u_lo, nullptr, coef, B, S, H, u2, u2_lo, nullptr)) return e;
       ua = u2;
       ua_lo = u2_lo;
     }
-    if (f32) {
-      if (int e = proj(ctx, lc, ws, L, mk(lw.w_qkv, H, ua, ua_lo, H, R, nh * d, H, EPI_F32, at<float>(ws, L.qkv),
-                                          nh * d, "qkv")))
-        return e;
-      if (int e = qk_norm_rope(lc, f32, at<float>(ws, L.qkv), B, S, nq, nkv, d, lw.g_q, lw.g_k, g.qk_norm != 0, g.eps,
-                               g.rope_base, ctx_len, at<void>(ws, L.q), at<void>(ws, L.bk), at<void>(ws, L.bv)))
-        return e;
-    } else {
-      // bf16: the head epilogue q/k-norms and rotates the heads and writes q,
-      // block K and block V^T in the attention's layouts
-      GemmOp op = wq(ctx, mk(lw.w_qkv, H, ua, ua_lo, H, R, nh * d, H, EPI_HEADS, nullptr, 0, "qkv"), lw.s_qkv);
-      HeadArgs &ha = op.head;
-      ha.mode = 1;
-      ha.nq = nq;
-      ha.nkv = nkv;
-      ha.S = S;
-      ha.norm = g.qk_norm != 0;
-      ha.eps = g.eps;
-      ha.gq = lw.g_q;
-      ha.gk[0] = lw.g_k;
-      ha.cs = at<float2>(ws, L.cs_blk);
-      ha.q = at<void>(ws, L.q);
-      ha.bk = at<void>(ws, L.bk);
-      ha.bv = at<void>(ws, L.bv);
-      if (int e = proj(ctx, lc, ws, L, op)) return e;
-    }
+    if (int e = proj(ctx, lc, ws, L,
+                     wq(ctx, mk(lw.w_qkv, H, ua, ua_lo, H, R, nh * d, H, EPI_F32, at<float>(ws, L.qkv), nh * d, "qkv"),
+                        lw.s_qkv, lw.w_qkv_bf16)))
+      return e;
+    if (int e = qk_norm_rope(lc, f32, at<float>(ws, L.qkv), B, S, nq, nkv, d, lw.g_q, lw.g_k, g.qk_norm != 0, g.eps,
+                             g.rope_base, ctx_len, at<void>(ws, L.q), at<void>(ws, L.bk), at<void>(ws, L.bv)))
+      return e;
     AttnArgs aa = {};
     aa.q = at<void>(ws, L.q);
     aa.k_cache = static_cast<const char *>(kv->k_cache) + te * lelems * l;
@@ -631,23 +569,24 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     aa.partials = at<float>(ws, L.attn_part);
     aa.partial_slots = L.attn_part_slots;
     if (int e = f32 ? attention_f32(lc, aa) : attention_bf16(lc, aa)) return e;
-    if (int e = out_proj(1, lw, lw.w_o, lw.s_o, nq * d, aa.out, aa.out_lo, "o_proj")) return e;
+    if (int e = out_proj(1, lw, lw.w_o, lw.s_o, lw.w_o_bf16, nq * d, aa.out, aa.out_lo, "o_proj")) return e;
     // ---- FFN sublayer
     if (int e = rmsnorm_rows(lc, f32, x, R, H, S, lw.g_ffn, g.eps, u, u_lo, nullptr, nullptr)) return e;
     ua = u;
     ua_lo = u_lo;
     if (g.use_conv) {
-      if (int e = conv_site(2, lw, u, u_lo, u2, u2_lo, nullptr)) return e;
+      if (int e = coef_gemm(2, lw, u, u_lo)) return e;
+      if (int e = conv_apply(lc, f32, u, u_lo, nullptr, coef, B, S, H, u2, u2_lo, nullptr)) return e;
       ua = u2;
       ua_lo = u2_lo;
     }
     {
       GemmOp op = wq(ctx, mk(lw.w_gu, H, ua, ua_lo, H, R, 2 * F, H, EPI_SWIGLU, at<void>(ws, L.hmid), F, "gate_up"),
-                     lw.s_gu);
+                     lw.s_gu, lw.w_gu_bf16);
       op.out_lo = hmid_lo;
       if (int e = proj(ctx, lc, ws, L, op)) return e;
     }
-    if (int e = out_proj(3, lw, lw.w_down, lw.s_down, F, at<void>(ws, L.hmid), hmid_lo, "down")) return e;
+    if (int e = out_proj(3, lw, lw.w_down, lw.s_down, lw.w_down_bf16, F, at<void>(ws, L.hmid), hmid_lo, "down")) return e;
     if (l + 1 < g.n_layers)
       if (int e = rmsnorm_rows(lc, f32, x, R, H, S, ctx->layers[l + 1].g_attn, g.eps, u, u_lo, nullptr, nullptr))
         return e;
@@ -658,7 +597,7 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
   if (int e = proj(ctx, lc, ws, L,
                    wq(ctx, mk(ctx->w.lm_head, H, at<void>(ws, L.hmask), lo(L.hmask_lo), H, B * J, V, H, EPI_F32, lg, V,
                               "lm_head"),
-                      ctx->w.s_lm_head)))
+                      ctx->w.s_lm_head, ctx->w.lm_head_bf16)))
     return e;
   return topk16(lc, lg, B * J, V, topk_ids, topk_logits, at<uint64_t>(ws, L.topk_part), at<int>(ws, L.topk_ctr),
                 TOPK_MAX_CHUNKS);
@@ -822,7 +761,7 @@ size_t dflash_debug_gemm_scratch_bytes(void) {
 
 int dflash_debug_gemm(const void *W, const float *w_scale, int w_fp8, const void *X, int M, int N, int K, float *out,
                       void *scratch, size_t scratch_bytes, int gemm_ctas, dflash_stream_t stream) {
-  if (!W || !X || !out || !scratch || (w_fp8 && !w_scale) || M <= 0 || N <= 0 || K <= 0 || gemm_ctas < 0)
+  if (!W || !X || !out || !scratch || (w_fp8 && !w_scale) || M <= 0 || N <= 0 || K <= 0)
     return set_error(DFLASH_ERR_ARG, "debug gemm: bad argument");
   if (K % (w_fp8 ? 16 : 8)) return set_error(DFLASH_ERR_SHAPE, "debug gemm: K must be a multiple of %d", w_fp8 ? 16 : 8);
   if (!aligned16(scratch) || !aligned16(out)) return set_error(DFLASH_ERR_ALIGN, "debug gemm: misaligned buffer");
@@ -859,6 +798,15 @@ int dflash_debug_gemm_plan(int M, int N, int K, int n_groups, int w_fp8, int spl
   for (int i = 0; i < 10; ++i) plan[i] = v[i];
   return DFLASH_OK;
 }
+
+int dflash_fp8_weights_to_bf16(const void *codes, const float *scale, int rows, int cols, void *out,
+                               dflash_stream_t stream) {
+  Launch lc;
+  lc.stream = reinterpret_cast<cudaStream_t>(stream);
+  return fp8_rows_to_bf16(lc, codes, scale, rows, cols, out);
+}
+
+int dflash_debug_gemm_pair_clusters(void) { return gemm_pair_clusters(); }
 
 int dflash_debug_e4m3_to_bf16(const void *codes, int n, void *out, dflash_stream_t stream) {
   Launch lc;

@@ -93,22 +93,6 @@ __device__ __forceinline__ void rope_cs(int pos, float th_hi, float th_lo, float
   sincosf(r + tail, &s, &c);
 }
 
-// theta_i = base^(-2i/d) of the rotation pairs, as fp32 (hi, lo) from the host
-struct RopeArgs {
-  float th_hi[64], th_lo[64];
-};
-
-// (cos, sin) of the angles pos * theta_i of the d/2 rotation pairs of one
-// row: threads 0 .. d/2-1 take one pair each.
-__device__ __forceinline__ void rope_row_cs(const RopeArgs &rp, int half, int pos, float2 *cs) {
-  const int i = threadIdx.x;
-  if (i < half) {
-    float c, s;
-    rope_cs(pos, rp.th_hi[i], rp.th_lo[i], c, s);
-    cs[i] = make_float2(c, s);
-  }
-}
-
 // ------------------------------------------------------------------ embed
 // x[b*S+j] = E[id] (fp32 residual stream); u = RMSNorm(x) (activation dtype);
 // S = block size: the anchor at j = 0, the mask token at j = 1..S-1
@@ -116,8 +100,7 @@ template <typename T>
 __global__ void __launch_bounds__(ROW_THREADS) embed_rmsnorm_kernel(const T *embed, const int32_t *anchor,
                                                                     int mask_id, int vocab, const float *gain,
                                                                     float eps, int H, int S, float *x, T *u, T *u_lo,
-                                                                    int *status, const int32_t *ctx_len,
-                                                                    const RopeArgs rp, int half, float2 *cs) {
+                                                                    int *status) {
   // Every input is the caller's (anchor ids, complete before any kernel of
   // this call starts) or a weight: all loads before the wait for the
   // previous kernel; the stores (x, u) after it.
@@ -140,9 +123,6 @@ __global__ void __launch_bounds__(ROW_THREADS) embed_rmsnorm_kernel(const T *emb
   }
   pdl_start();
   if (bad && threadIdx.x == 0) report(status, DFLASH_ERR_DEVICE);
-  // the rotation of this row's q / k heads (position ctx_len[b] + j), used by
-  // the QKV projection's head epilogue; ctx_len comes from the previous call
-  if (cs) rope_row_cs(rp, half, ctx_len[b] + j, cs + static_cast<size_t>(row) * half);
 #pragma unroll
   for (int k = 0; k < MAXV; ++k) {
     const int i = threadIdx.x + k * ROW_THREADS;
@@ -203,21 +183,11 @@ __global__ void __launch_bounds__(ROW_THREADS) rmsnorm_kernel(const float *x, in
 // f = RMSNorm(fc output) (or the plain projection); block 0 also saves the
 // incoming context lengths so the scatter can read them even when the caller
 // updates ctx_len in place.
-struct SlotArgs {
-  const int32_t *cu_new, *page_table;
-  int max_pages, num_pages, page, half;
-  float2 *cs;
-  int32_t *tok_page, *tok_slot;
-  int *status;
-};
-
 template <typename T>
 __global__ void __launch_bounds__(ROW_THREADS) feature_norm_kernel(const float *in, int H, const float *gain,
                                                                    float eps, int apply, T *out, T *out_lo,
-                                                                   const int32_t *ctx_in, int32_t *ctx_saved, int B,
-                                                                   const SlotArgs sa, const RopeArgs rp) {
+                                                                   const int32_t *ctx_in, int32_t *ctx_saved, int B) {
   __shared__ float red[32];
-  __shared__ int spos;
   const int row = blockIdx.x;
   const int nv = H >> 2;
   float4 v[MAXV], g[MAXV];
@@ -229,30 +199,6 @@ __global__ void __launch_bounds__(ROW_THREADS) feature_norm_kernel(const float *
   pdl_start();
   if (row == 0)
     for (int b = threadIdx.x; b < B; b += blockDim.x) ctx_saved[b] = ctx_in[b];
-  if (sa.cs) {
-    // where token `row` goes: request b (last with cu_new[b] <= row), its
-    // position, pool page and slot, and its rotation for the K head epilogue
-    if (threadIdx.x == 0) {
-      int lo = 0, hi = B - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (sa.cu_new[mid] <= row)
-          lo = mid;
-        else
-          hi = mid - 1;
-      }
-      const int pos = ctx_in[lo] + row - sa.cu_new[lo];
-      const int pidx = pos / sa.page;
-      const int pg = (pos >= 0 && pidx < sa.max_pages) ? sa.page_table[static_cast<size_t>(lo) * sa.max_pages + pidx] : -1;
-      const bool ok = pg >= 0 && pg < sa.num_pages;
-      if (!ok) report(sa.status, DFLASH_ERR_DEVICE);
-      sa.tok_page[row] = ok ? pg : -1;
-      sa.tok_slot[row] = pos % sa.page;
-      spos = pos;
-    }
-    __syncthreads();
-    rope_row_cs(rp, sa.half, spos, sa.cs + static_cast<size_t>(row) * sa.half);
-  }
   const float *xr = in + static_cast<size_t>(row) * H;
 #pragma unroll
   for (int k = 0; k < MAXV; ++k) {
@@ -273,6 +219,9 @@ __global__ void __launch_bounds__(ROW_THREADS) feature_norm_kernel(const float *
 }
 
 // ------------------------------------------------------------------ q/k norm + rope
+struct RopeArgs {
+  float th_hi[64], th_lo[64];
+};
 
 // This lane's angles theta_{lane + 32 i}, i < N, from the parameter table.
 // Kernel parameters indexed by lane serialise the constant bank (one access
@@ -295,47 +244,27 @@ __device__ __forceinline__ void lane_thetas(const RopeArgs &rp, int lane, float 
   }
 }
 
-// qkv: fp32 [B*S][(nq+2nkv)*d] (S = block size).  One warp per (token,
-// head).  q heads -> q_out [B*S][nq*d]; k heads -> bk [B][nkv][64][d]
-// (normed, rotated); v heads -> bv [B][nkv][d][64], transposed like the V
-// pages.  Rows / columns S..63 are padding up to one 64-token page:
-// attention masks the scores of rows S.. and skips V columns 16..; V columns
-// S..15 share a k-step with the block tokens and are written as zeros.
-template <typename T, int DPL>
-__global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, int nkv, int S, const float *g_q,
-                                                      const float *g_k, int qk_norm, float eps, const RopeArgs rp,
-                                                      const int32_t *ctx_len, T *q_out, T *bk, T *bv) {
+// 16 consecutive values with vector stores (dst 16-byte aligned).
+__device__ __forceinline__ void store16(float *dst, const float (&x)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    reinterpret_cast<float4 *>(dst)[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+}
+__device__ __forceinline__ void store16(__nv_bfloat16 *dst, const float (&x)[16]) {
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = pack_bf16(x[2 * i], x[2 * i + 1]);
+  reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Per-head RMSNorm and RoPE of one head row held as lane + 32 i (i < DPL),
+// pairs (i, i + DPL/2); cs: the row's (cos, sin) per pair, in shared memory.
+template <int DPL>
+__device__ __forceinline__ void norm_rope_row(float (&v)[DPL], const float (&gn)[DPL], bool norm, float eps,
+                                              const float2 *cs, int lane) {
   constexpr int D = DPL * 32;
-  const int tok = blockIdx.x, b = tok / S, j = tok % S;
-  const int head = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  const int nh = nq + 2 * nkv;
-  // the norm gain and this lane's angles are weights: read before the wait
-  // for the projections, off the dependent chain
-  const bool is_q = head < nq, normed = qk_norm && head < nq + nkv;
-  float gn[DPL], th_hi[DPL / 2], th_lo[DPL / 2];
-#pragma unroll
-  for (int i = 0; i < DPL; ++i) gn[i] = normed ? (is_q ? g_q : g_k)[lane + 32 * i] : 1.f;
-  lane_thetas(rp, lane, th_hi, th_lo);
-  pdl_start();
-  if (head >= nh) return;
-  const float *src = qkv + static_cast<size_t>(tok) * nh * D + static_cast<size_t>(head) * D;
-  float v[DPL];
-#pragma unroll
-  for (int i = 0; i < DPL; ++i) v[i] = src[lane + 32 * i];
-  if (head >= nq + nkv) {   // value head: copy, transposed
-    T *dst = bv + (static_cast<size_t>(b) * nkv + (head - nq - nkv)) * D * 64 + j;
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + static_cast<size_t>(lane + 32 * i) * 64, v[i]);
-    // the block's PV k-step reads columns 0..15: below a block of 16 the
-    // columns S..15 get zeros (a 0 probability times a stale NaN is NaN),
-    // spread over the block's tokens: token j clears j+S, j+2S, ...
-    for (int c = j + S; c < 16; c += S)
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + (c - j) + static_cast<size_t>(lane + 32 * i) * 64, 0.f);
-    return;
-  }
-  const int pos = ctx_len[b] + j;
-  if (qk_norm) {
+  if (norm) {
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < DPL; ++i) ss += v[i] * v[i];
@@ -345,17 +274,99 @@ __global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, 
   }
   float o[DPL];
 #pragma unroll
-  for (int i = 0; i < DPL / 2; ++i) {   // pairs (lane + 32i, lane + 32i + D/2)
-    float c, s;
-    rope_cs(pos, th_hi[i], th_lo[i], c, s);
+  for (int i = 0; i < DPL / 2; ++i) {
+    const float2 c = cs[lane + 32 * i];
     const float x1 = v[i], x2 = v[i + DPL / 2];
-    o[i] = x1 * c - x2 * s;
-    o[i + DPL / 2] = x2 * c + x1 * s;
+    o[i] = x1 * c.x - x2 * c.y;
+    o[i + DPL / 2] = x2 * c.x + x1 * c.y;
   }
-  T *dst = is_q ? q_out + static_cast<size_t>(tok) * nq * D + static_cast<size_t>(head) * D
-                : bk + ((static_cast<size_t>(b) * nkv + (head - nq)) * 64 + j) * D;
 #pragma unroll
-  for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + lane + 32 * i, o[i]);
+  for (int i = 0; i < DPL; ++i) v[i] = o[i];
+}
+
+// Rows of the block's q / k / v projections, CTAs (request b, kv head h,
+// split z): the g = nq/nkv query heads of h, the k head h and the v head h
+// over the request's S rows (qkv: fp32 [B*S][(nq+2nkv)*d]); with few
+// requests the (head, row) items and the v head's d-rows are split over
+// gridDim.z CTAs so that the launch still covers the SMs.  The rotation of
+// each row (position ctx_len[b] + j) is tabulated once per CTA in shared
+// memory and shared by its heads.  q heads -> q_out [B*S][nq*d]; k head -> bk
+// [B][nkv][64][d] (normed, rotated); v head -> bv [B][nkv][d][64],
+// transposed like the V pages: the CTA stages the S rows in shared memory
+// and each thread writes one d-row's 16 columns (32 bytes, whole sectors).
+// Rows / columns S..63 are padding up to one 64-token page: attention masks
+// the scores of rows S.. and skips V columns 16..; V columns S..15 share a
+// k-step with the block tokens and are written as zeros.
+template <typename T, int DPL>
+__global__ void __launch_bounds__(256) qk_rope_kernel(const float *qkv, int nq, int nkv, int S, const float *g_q,
+                                                      const float *g_k, int qk_norm, float eps, const RopeArgs rp,
+                                                      const int32_t *ctx_len, T *q_out, T *bk, T *bv) {
+  constexpr int D = DPL * 32, HALF = D / 2, U = 4;
+  __shared__ float2 cs[16][HALF];
+  __shared__ float vt[16][D];
+  const int b = blockIdx.x, h = blockIdx.y, g = nq / nkv, nh = nq + 2 * nkv;
+  const int z = blockIdx.z, nz = gridDim.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the norm gains and this lane's angles are weights: read before the wait
+  float gq[DPL], gk[DPL], th_hi[DPL / 2], th_lo[DPL / 2];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) {
+    gq[i] = qk_norm ? g_q[lane + 32 * i] : 1.f;
+    gk[i] = qk_norm ? g_k[lane + 32 * i] : 1.f;
+  }
+  lane_thetas(rp, lane, th_hi, th_lo);
+  pdl_start();
+  const int n0 = ctx_len[b];
+  for (int j = warp; j < S; j += 8)
+#pragma unroll
+    for (int i = 0; i < DPL / 2; ++i) {
+      float c, sn;
+      rope_cs(n0 + j, th_hi[i], th_lo[i], c, sn);
+      cs[j][lane + 32 * i] = make_float2(c, sn);
+    }
+  // this CTA's d-rows of the v head: S rows into shared memory
+  const int d0 = z * D / nz, d1 = (z + 1) * D / nz, dn = d1 - d0;
+  const float *vsrc = qkv + static_cast<size_t>(b) * S * nh * D + static_cast<size_t>(nq + nkv + h) * D + d0;
+  for (int e = threadIdx.x; e < S * dn; e += 256) vt[e / dn][e % dn] = vsrc[static_cast<size_t>(e / dn) * nh * D + e % dn];
+  __syncthreads();
+  // q and k rows: (g + 1) heads x S rows, one warp per (head, row), U rows'
+  // loads in flight per warp; this CTA's share of them
+  const int items_all = (g + 1) * S;
+  const int i_lo = z * items_all / nz, items = (z + 1) * items_all / nz;
+  for (int it0 = i_lo + warp * U; it0 < items; it0 += 8 * U) {
+    float v[U][DPL];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int it = it0 + u;
+      if (it < items) {
+        const int hh = it / S, j = it % S, head = hh < g ? h * g + hh : nq + h;
+        const float *src = qkv + static_cast<size_t>(b * S + j) * nh * D + static_cast<size_t>(head) * D;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) v[u][i] = src[lane + 32 * i];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int it = it0 + u;
+      if (it >= items) break;
+      const int hh = it / S, j = it % S;
+      const bool isq = hh < g;
+      norm_rope_row<DPL>(v[u], isq ? gq : gk, qk_norm != 0, eps, cs[j], lane);
+      T *dst = isq ? q_out + static_cast<size_t>(b * S + j) * nq * D + static_cast<size_t>(h * g + hh) * D
+                   : bk + ((static_cast<size_t>(b) * nkv + h) * 64 + j) * D;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + lane + 32 * i, v[u][i]);
+    }
+  }
+  // V^T: one thread per d-row writes its columns 0..15 (zeros from S on) as
+  // one 32-byte sector (bf16; 64 bytes fp32)
+  if (threadIdx.x < dn) {
+    const int d = threadIdx.x;
+    float x[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = j < S ? vt[j][d] : 0.f;
+    store16(bv + ((static_cast<size_t>(b) * nkv + h) * D + d0 + d) * 64, x);
+  }
 }
 
 // ------------------------------------------------------------------ injection scatter
@@ -379,70 +390,98 @@ struct ScatterArgs {
   int *status;
 };
 
+// One CTA per (16 consecutive new tokens, layer, kv head).
+// Each token is placed once (request, position, pool page, slot) and its
+// rotation tabulated once in shared memory.  K heads: k-norm + RoPE, one
+// warp per (head, token), U tokens' loads in flight; written to the K pages
+// ([page][nkv][slot][d]).  V heads: the 16 x d tile is staged in shared
+// memory and written transposed into the V pages ([page][nkv][d][slot]) by
+// lanes that cover 16 consecutive tokens of two d-rows per store (the
+// tokens of a request occupy consecutive slots: whole or two sectors per
+// d-row instead of one 2-byte write each).
 template <typename T, int DPL>
 __global__ void __launch_bounds__(256) inject_scatter_kernel(const ScatterArgs a, const RopeArgs rp) {
+  constexpr int D = DPL * 32, HALF = D / 2, U = 4;
+  __shared__ float2 cs[16][HALF];
+  __shared__ float vt[16][D];
+  __shared__ int s_page[16], s_slot[16];
+  const int t0 = blockIdx.x * 16, l = blockIdx.y, h = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = min(16, a.T - t0);
+  float gk[DPL], th_hi[DPL / 2], th_lo[DPL / 2];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) gk[i] = a.qk_norm ? a.g_k[l][lane + 32 * i] : 1.f;
+  lane_thetas(rp, lane, th_hi, th_lo);
   pdl_start();
-  constexpr int D = DPL * 32;
-  const int t = blockIdx.x;
-  const int lane = threadIdx.x & 31;
-  const int unit = blockIdx.y * 8 + (threadIdx.x >> 5);   // (layer, k/v, head)
-  if (t == 0 && blockIdx.y == 0)
+  if (blockIdx.x == 0 && l == 0 && h == 0)
     for (int b = threadIdx.x; b < a.B; b += blockDim.x)
       a.ctx_out[b] = a.ctx_saved[b] + (a.cu_new[b + 1] - a.cu_new[b]);
-  if (unit >= a.L * 2 * a.nkv) return;
-  const int l = unit / (2 * a.nkv), kv = (unit / a.nkv) & 1, h = unit % a.nkv;
-  // request of token t: last b with cu_new[b] <= t
-  int lo = 0, hi = a.B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (a.cu_new[mid] <= t)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  const int b = lo;
-  const int pos = a.ctx_saved[b] + t - a.cu_new[b];
-  const int pidx = pos / a.page;
-  const int pg = (pos >= 0 && pidx < a.max_pages) ? a.page_table[static_cast<size_t>(b) * a.max_pages + pidx] : -1;
-  if (pg < 0 || pg >= a.num_pages) {
-    if (lane == 0) report(a.status, DFLASH_ERR_DEVICE);
-    return;
-  }
-  const float *src = a.kvproj + (static_cast<size_t>(l) * a.T + t) * (2 * a.nkv * D) + (kv * a.nkv + h) * D;
-  float v[DPL];
-#pragma unroll
-  for (int i = 0; i < DPL; ++i) v[i] = src[lane + 32 * i];
-  if (kv == 0) {
-    if (a.qk_norm) {
-      float ss = 0.f;
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) ss += v[i] * v[i];
-      const float r = rsqrtf(warp_sum(ss) / D + a.eps);
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) v[i] *= r * a.g_k[l][lane + 32 * i];
+  __shared__ int s_pos[16];
+  if (threadIdx.x < nt) {
+    const int t = t0 + threadIdx.x;
+    // request of token t: last b with cu_new[b] <= t
+    int lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.cu_new[mid] <= t)
+        lo = mid;
+      else
+        hi = mid - 1;
     }
-    float o[DPL], th_hi[DPL / 2], th_lo[DPL / 2];
-    lane_thetas(rp, lane, th_hi, th_lo);
+    const int pos = a.ctx_saved[lo] + t - a.cu_new[lo];
+    const int pidx = pos / a.page;
+    const int pg = (pos >= 0 && pidx < a.max_pages) ? a.page_table[static_cast<size_t>(lo) * a.max_pages + pidx] : -1;
+    const bool ok = pg >= 0 && pg < a.num_pages;
+    if (!ok) report(a.status, DFLASH_ERR_DEVICE);
+    s_page[threadIdx.x] = ok ? pg : -1;
+    s_slot[threadIdx.x] = pos % a.page;
+    s_pos[threadIdx.x] = pos;
+  }
+  __syncthreads();
+  for (int j = warp; j < nt; j += 8)
 #pragma unroll
     for (int i = 0; i < DPL / 2; ++i) {
-      float c, s;
-      rope_cs(pos, th_hi[i], th_lo[i], c, s);
-      o[i] = v[i] * c - v[i + DPL / 2] * s;
-      o[i + DPL / 2] = v[i + DPL / 2] * c + v[i] * s;
+      float c, sn;
+      rope_cs(s_pos[j], th_hi[i], th_lo[i], c, sn);
+      cs[j][lane + 32 * i] = make_float2(c, sn);
     }
+  __syncthreads();
+  const size_t row_stride = static_cast<size_t>(2 * a.nkv) * D;
+  const float *base = a.kvproj + (static_cast<size_t>(l) * a.T + t0) * row_stride;
+  T *kc = static_cast<T *>(a.k_cache) + l * a.layer_elems;
+  T *vc = static_cast<T *>(a.v_cache) + l * a.layer_elems;
+  // the V head's 16 x d tile into shared memory (its loads in flight with
+  // the K rows' below)
+  for (int e = threadIdx.x; e < nt * D; e += 256)
+    vt[e / D][e % D] = base[(e / D) * row_stride + static_cast<size_t>(a.nkv + h) * D + e % D];
+  // K head: one warp per token, two tokens per warp
+  for (int j0 = warp * 2; j0 < nt; j0 += 16) {
+    float v[2][DPL];
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) v[i] = o[i];
+    for (int u = 0; u < 2; ++u)
+      if (j0 + u < nt) {
+        const float *src = base + (j0 + u) * row_stride + static_cast<size_t>(h) * D;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) v[u][i] = src[lane + 32 * i];
+      }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int j = j0 + u;
+      if (j >= nt) break;
+      norm_rope_row<DPL>(v[u], gk, a.qk_norm != 0, a.eps, cs[j], lane);
+      const int pg = s_page[j];
+      if (pg < 0) continue;
+      T *dst = kc + ((static_cast<size_t>(pg) * a.nkv + h) * a.page + s_slot[j]) * D;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + lane + 32 * i, v[u][i]);
+    }
   }
-  // K pages: [page][nkv][slot][d]; V pages transposed: [page][nkv][d][slot]
-  T *cache = static_cast<T *>(kv == 0 ? a.k_cache : a.v_cache) + l * a.layer_elems;
-  if (kv == 0) {
-    T *dst = cache + ((static_cast<size_t>(pg) * a.nkv + h) * a.page + pos % a.page) * D;
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + lane + 32 * i, v[i]);
-  } else {
-    T *dst = cache + (static_cast<size_t>(pg) * a.nkv + h) * D * a.page + pos % a.page;
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + static_cast<size_t>(lane + 32 * i) * a.page, v[i]);
+  __syncthreads();
+  // V^T: 16 consecutive threads cover one d-row's 16 tokens (consecutive slots)
+  for (int e = threadIdx.x; e < 16 * D; e += 256) {
+    const int d = e >> 4, j = e & 15;
+    const int pg = j < nt ? s_page[j] : -1;
+    if (pg >= 0) Elt<T>::st(vc + ((static_cast<size_t>(pg) * a.nkv + h) * D + d) * a.page + s_slot[j], vt[j][d]);
   }
 }
 
@@ -511,22 +550,17 @@ int check_row(int H) {
 }  // namespace
 
 int embed_rmsnorm(const Launch &lc, bool f32, const void *embed, const int32_t *anchor, int mask_id, int vocab,
-                  const float *gain, float eps, int B, int S, int H, float *x, void *u, void *u_lo,
-                  const int32_t *ctx_len, int d, float rope_base, float2 *cs) {
+                  const float *gain, float eps, int B, int S, int H, float *x, void *u, void *u_lo) {
   if (int e = check_row(H)) return e;
-  if (cs && (!ctx_len || d < 2 || d > 128 || d % 2))
-    return set_error(DFLASH_ERR_ARG, "embed_norm: rotation table needs ctx_len and head_dim <= 128");
-  const RopeArgs rp = cs ? rope_table(d, rope_base) : RopeArgs{};
-  const int half = d / 2;
   return run(lc, "embed_norm", [&] {
     if (f32)
       launch_pdl(embed_rmsnorm_kernel<float>, dim3(B * S), dim3(ROW_THREADS), 0, lc.stream,
           static_cast<const float *>(embed), anchor, mask_id, vocab, gain, eps, H, S, x, tp<float>(u), nullptr,
-          lc.status, ctx_len, rp, half, cs);
+          lc.status);
     else
       launch_pdl(embed_rmsnorm_kernel<__nv_bfloat16>, dim3(B * S), dim3(ROW_THREADS), 0, lc.stream,
           static_cast<const __nv_bfloat16 *>(embed), anchor, mask_id, vocab, gain, eps, H, S, x, tp<__nv_bfloat16>(u),
-          tp<__nv_bfloat16>(u_lo), lc.status, ctx_len, rp, half, cs);
+          tp<__nv_bfloat16>(u_lo), lc.status);
   });
 }
 
@@ -545,43 +579,31 @@ int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, in
 }
 
 int feature_norm(const Launch &lc, bool f32, const float *in, int rows, int H, const float *gain, float eps,
-                 bool apply_norm, void *out, void *out_lo, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B,
-                 const InjectSlots *slots) {
+                 bool apply_norm, void *out, void *out_lo, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B) {
   if (rows <= 0) return DFLASH_OK;
   if (int e = check_row(H)) return e;
-  SlotArgs sa = {};
-  RopeArgs rp = {};
-  if (slots) {
-    if (!slots->cu_new || !slots->page_table || !slots->cs || !slots->tok_page || !slots->tok_slot ||
-        slots->d < 2 || slots->d > 128 || slots->d % 2 || slots->page <= 0)
-      return set_error(DFLASH_ERR_ARG, "feature_norm: injection slot arguments");
-    sa.cu_new = slots->cu_new;
-    sa.page_table = slots->page_table;
-    sa.max_pages = slots->max_pages;
-    sa.num_pages = slots->num_pages;
-    sa.page = slots->page;
-    sa.half = slots->d / 2;
-    sa.cs = slots->cs;
-    sa.tok_page = slots->tok_page;
-    sa.tok_slot = slots->tok_slot;
-    sa.status = lc.status;
-    rp = rope_table(slots->d, slots->rope_base);
-  }
   return run(lc, "feature_norm", [&] {
     if (f32)
       launch_pdl(feature_norm_kernel<float>, dim3(rows), dim3(ROW_THREADS), 0, lc.stream, in, H, gain, eps, apply_norm, tp<float>(out),
-                                                                      nullptr, ctx_len_in, ctx_len_saved, B, sa, rp);
+                                                                      nullptr, ctx_len_in, ctx_len_saved, B);
     else
       launch_pdl(feature_norm_kernel<__nv_bfloat16>, dim3(rows), dim3(ROW_THREADS), 0, lc.stream,
           in, H, gain, eps, apply_norm, tp<__nv_bfloat16>(out), tp<__nv_bfloat16>(out_lo), ctx_len_in, ctx_len_saved,
-          B, sa, rp);
+          B);
   });
 }
 
 int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int S, int nq, int nkv, int d,
                  const float *g_q, const float *g_k, bool qk_norm, float eps, float rope_base, const int32_t *ctx_len,
                  void *q_out, void *bk, void *bv) {
-  dim3 grid(B * S, (nq + 2 * nkv + 7) / 8);
+  if (S > 16) return set_error(DFLASH_ERR_UNSUPPORTED, "q/k norm + RoPE: block size above 16");
+  // split each (request, kv head) over nz CTAs until the launch covers the
+  // SMs, keeping at least 8 (head, row) items per CTA
+  const int items = (nq / nkv + 1) * S;
+  int nz = (lc.num_sms + B * nkv - 1) / (B * nkv);
+  nz = nz < 1 ? 1 : (nz > items / 8 ? (items / 8 > 0 ? items / 8 : 1) : nz);
+  nz = nz > d ? d : nz;
+  dim3 grid(B, nkv, nz);
   const RopeArgs rp = rope_table(d, rope_base);
   return run(lc, "qk_norm_rope", [&] {
 #define QK(T, DPL)                                                                                         \
@@ -625,7 +647,7 @@ int inject_scatter(const Launch &lc, bool f32, const float *kvproj, int T, int L
   a.layer_elems = layer_elems;
   a.status = lc.status;
   const RopeArgs rp = rope_table(d, rope_base);
-  dim3 grid(T, (L * 2 * nkv + 7) / 8);
+  dim3 grid((T + 15) / 16, L, nkv);
   return run(lc, "inject_scatter", [&] {
     if (f32 && d == 64)
       launch_pdl(inject_scatter_kernel<float, 2>, dim3(grid), dim3(256), 0, lc.stream, a, rp);

@@ -84,10 +84,6 @@ struct Cfg {
   // the owning CTA: at most (csk - 1) * ceil(128 / csk) <= 120 rows arrive
   static constexpr bool PUSH = BN <= 32;
   static constexpr int PUSH_BYTES = PUSH ? 120 * BN * 4 : 0;
-  // the head epilogue's exchange (16 tokens x 128 features + per-warp sums);
-  // it never runs with the push path, so the two share one region
-  static constexpr int XCH_BYTES = 128 * 16 * 4 + 4 * 16 * 4;
-  static constexpr int XREG = PUSH_BYTES > XCH_BYTES ? PUSH_BYTES : XCH_BYTES;
   static constexpr int CTRL = 512;                     // mbarriers and flags
   // Small token tiles (weight streaming): ~100 KB of ring, so two GEMM CTAs
   // fit on one SM and, under programmatic dependent launch, the next GEMM's
@@ -95,13 +91,13 @@ struct Cfg {
   // (152 x 5 stages in flight still exceed what HBM needs in flight).  F8
   // keeps the whole CTA within half an SM.  Large token tiles (tensor-bound):
   // one CTA per SM with a deeper ring.
-  static constexpr int BUDGET = BN <= 32 ? (F8 ? (SMEM_PER_SM / 2 - 1024 - 1024 - CTRL - XREG) : 100 * 1024)
+  static constexpr int BUDGET = BN <= 32 ? (F8 ? (SMEM_PER_SM / 2 - 1024 - 1024 - CTRL - PUSH_BYTES) : 100 * 1024)
                                          : 200 * 1024;
   static constexpr int STAGES_RAW = BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : (STAGES_RAW < 2 ? 2 : STAGES_RAW);
   static constexpr int TMEM_COLS = F8 ? pow2_at_least(A_COL + CSTAGES * A_TCOLS) : (2 * BN < 32 ? 32 : 2 * BN);
   static constexpr int RING = STAGES * STAGE_BYTES;
-  static constexpr int SMEM = 1024 + RING + CTRL + XREG;
+  static constexpr int SMEM = 1024 + RING + CTRL + PUSH_BYTES;
   static_assert((2 * STAGES + 2 * CSTAGES + 6) * 8 + 12 <= CTRL, "GEMM control block overflows");
   static_assert(RING >= BM * BN * 4, "the ring must hold one fp32 tile (cluster split-K share)");
   static_assert(!F8 || BN > 32 || 2 * (SMEM + 1024) <= SMEM_PER_SM, "two F8 CTAs must fit on one SM");
@@ -126,10 +122,6 @@ struct Params {
   void *out2, *out2_lo;
   int ldo2;
   const float *bias;
-  const void *cy, *cy_lo;   // EPI_CONV_PRE: convolved activation (bf16 hi / lo), row stride ldy
-  const float *cy32;        // EPI_CONV_POST: convolved activation (fp32)
-  int ldy, cS;              // EPI_CONV_*: row stride of y, block size
-  HeadArgs head;            // EPI_HEADS
   const float *wscale[MAX_GROUPS];   // F8: per-row weight scales of each group
   float *partials;     // [G][2][BM][BN] row-major shares
   int *counters;       // [tiles]
@@ -155,215 +147,10 @@ __device__ __forceinline__ void store_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, s
   if (lo) lo[i] = f2bf(v - bf2f(h));
 }
 
-// 8 consecutive channels of row r of the convolved activation (fp32 value).
-__device__ __forceinline__ void conv_load8(const Params &p, bool post, int r, int c0, float (&y)[8]) {
-  const size_t o = static_cast<size_t>(r) * p.ldy + c0;
-  if (post) {
-    const float4 a = *reinterpret_cast<const float4 *>(p.cy32 + o), b = *reinterpret_cast<const float4 *>(p.cy32 + o + 4);
-    y[0] = a.x, y[1] = a.y, y[2] = a.z, y[3] = a.w, y[4] = b.x, y[5] = b.y, y[6] = b.z, y[7] = b.w;
-  } else {
-    const uint4 h = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.cy) + o);
-    const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
-    uint32_t lw[4] = {0u, 0u, 0u, 0u};
-    if (p.cy_lo) {
-      const uint4 l = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.cy_lo) + o);
-      lw[0] = l.x, lw[1] = l.y, lw[2] = l.z, lw[3] = l.w;
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      y[2 * i] = __uint_as_float(hw[i] << 16) + __uint_as_float(lw[i] << 16);
-      y[2 * i + 1] = __uint_as_float(hw[i] & 0xFFFF0000u) + __uint_as_float(lw[i] & 0xFFFF0000u);
-    }
-  }
-}
-
-// DFlash-2 short convolution ("DFlash 2", Arquitectura del Sistema item 2)
-// of 8 channels c0.. of one 16-channel group over the 16 token rows tok0..:
-// out_j = y_j + a_j * y_j + b_j * y_{j-1}, y_{-1} = 0 at every block's first
-// position (rows are consecutive positions of S-token blocks).  Pre sites
-// store the bf16 hi / lo halves, post sites add into the fp32 residual.
-// CB rows at a time: their loads (y, and the residual at post sites) are
-// all issued before the first store, so the stores, which the compiler must
-// assume may alias the loads, do not serialise them (CB = 1 in the variants
-// capped at 96 registers).
-template <int CB>
-__device__ __noinline__ void conv_rows(const Params &p, bool post, const float (&a)[16], const float (&b)[16],
-                                       int c0, int tok0) {
-  float prev[8];
-  if (tok0 < p.M && tok0 % p.cS != 0) {
-    conv_load8(p, post, tok0 - 1, c0, prev);
-  } else {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) prev[k] = 0.f;
-  }
-#pragma unroll
-  for (int i0 = 0; i0 < 16; i0 += CB) {
-    float y[CB][8];
-    float4 xr[CB][2];
-#pragma unroll
-    for (int u = 0; u < CB; ++u) {
-      const int r = tok0 + i0 + u;
-      if (r < p.M) {
-        conv_load8(p, post, r, c0, y[u]);
-        if (post) {
-          const float4 *x = reinterpret_cast<const float4 *>(static_cast<const float *>(p.out) +
-                                                             static_cast<size_t>(r) * p.ldo + c0);
-          xr[u][0] = __ldcg(x);
-          xr[u][1] = __ldcg(x + 1);
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < CB; ++u) {
-      const int i = i0 + u, r = tok0 + i;
-      if (r >= p.M) break;
-      if (r % p.cS == 0) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) prev[k] = 0.f;
-      }
-      float o[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) o[k] = y[u][k] + a[i] * y[u][k] + b[i] * prev[k];
-      const size_t off = static_cast<size_t>(r) * p.ldo + c0;
-      if (post) {
-        float4 *x = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off);
-        x[0] = make_float4(xr[u][0].x + o[0], xr[u][0].y + o[1], xr[u][0].z + o[2], xr[u][0].w + o[3]);
-        x[1] = make_float4(xr[u][1].x + o[4], xr[u][1].y + o[5], xr[u][1].z + o[6], xr[u][1].w + o[7]);
-      } else {
-        uint32_t hw[4], lw[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const __nv_bfloat16 h0 = f2bf(o[2 * k]), h1 = f2bf(o[2 * k + 1]);
-          const __nv_bfloat16 l0 = f2bf(o[2 * k] - bf2f(h0)), l1 = f2bf(o[2 * k + 1] - bf2f(h1));
-          hw[k] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
-                  (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
-          lw[k] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
-                  (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
-        }
-        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        if (p.out_lo)
-          *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out_lo) + off) =
-              make_uint4(lw[0], lw[1], lw[2], lw[3]);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) prev[k] = y[u][k];
-    }
-  }
-}
-
-// EPI_HEADS: the tile is one attention head, row n = feature i (0..127) of
-// head n / 128 of group g; v holds that feature for the 16 token rows tok0...
-// Called by all 128 epilogue threads together, each with a different i (they
-// meet at the epilogue's named barrier).  q / k heads: per-token RMSNorm over
-// the head's 128 features ("DFlash" layer internals: Qwen3-style q/k norm),
-// then RoPE on the pairs (i, i + 64) with the row's (cos, sin); the partner
-// feature comes through shared memory.  The head is stored where the block
-// attention reads it.  V^T destinations (columns = tokens) are written by
-// lanes that cover 16 consecutive tokens of two features per instruction, so
-// each warp store fills whole 32-byte sectors instead of 32 scattered bytes.
-__device__ __noinline__ void heads_epi(const Params &p, float (&v)[16], int n, int g, int tok0, float *xch) {
-  const HeadArgs &a = p.head;
-  const int i = n & 127, head = n >> 7, lane = i & 31, q4 = i >> 5;
-  const int kind = head < a.nq ? 0 : (head < a.nq + a.nkv ? 1 : 2);   // q, k, v
-  const int h = kind == 0 ? head : (kind == 1 ? head - a.nq : head - a.nq - a.nkv);
-  float *red = xch + 16 * 128;
-  if (kind < 2) {
-    if (a.norm) {
-      const float gn = (kind == 0 ? a.gq : a.gk[g])[i];
-      float ss[16];
-#pragma unroll
-      for (int t = 0; t < 16; ++t) ss[t] = warp_sum(v[t] * v[t]);
-      if (lane == 0) {
-#pragma unroll
-        for (int t = 0; t < 16; ++t) red[q4 * 16 + t] = ss[t];
-      }
-      epi_bar();
-#pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const float tot = red[t] + red[16 + t] + red[32 + t] + red[48 + t];
-        v[t] *= rsqrtf(tot * (1.f / 128.f) + a.eps) * gn;
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < 16; ++t) xch[t * 128 + i] = v[t];
-    epi_bar();
-    const bool lo = i < 64;
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      const int row = tok0 + t < p.M ? tok0 + t : p.M - 1;
-      const float2 cs = a.cs[static_cast<size_t>(row) * 64 + (i & 63)];
-      const float o = xch[t * 128 + (i ^ 64)];
-      v[t] = lo ? v[t] * cs.x - o * cs.y : v[t] * cs.x + o * cs.y;
-    }
-    epi_bar();   // the exchange is free again
-  }
-  __nv_bfloat16 *dst = nullptr;
-  if (kind == 2) {
-    // V^T: this warp's 32 features, 16 tokens, via shared memory; lane l
-    // takes feature 32*q4 + 2k + l/16 of token l%16 in step k
-#pragma unroll
-    for (int t = 0; t < 16; ++t) xch[t * 128 + i] = v[t];
-    __syncwarp();
-    const int t = lane & 15, row = tok0 + t;
-    if (row < p.M) {
-      if (a.mode == 1) {
-        const int b = row / a.S, j = row % a.S;
-        dst = static_cast<__nv_bfloat16 *>(a.bv) + (static_cast<size_t>(b) * a.nkv + h) * 128 * 64 + j;
-      } else {
-        const int pg = a.tok_page[row];
-        if (pg >= 0)
-          dst = static_cast<__nv_bfloat16 *>(a.v_cache) + static_cast<size_t>(g) * a.layer_elems +
-                (static_cast<size_t>(pg) * a.nkv + h) * 128 * 64 + a.tok_slot[row];
-      }
-    }
-#pragma unroll 4
-    for (int k = 0; k < 16; ++k) {
-      const int f = q4 * 32 + 2 * k + (lane >> 4);
-      const float x = xch[t * 128 + f];
-      if (dst) dst[static_cast<size_t>(f) * 64] = f2bf(x);
-    }
-    __syncwarp();
-    // block V^T below a block of 16: the PV k-step reads columns 0..15, so
-    // the columns S..15 of each request get zeros (written by its first row)
-    if (a.mode == 1 && a.S < 16) {
-#pragma unroll
-      for (int t2 = 0; t2 < 16; ++t2) {
-        const int r2 = tok0 + t2;
-        if (r2 < p.M && r2 % a.S == 0) {
-          __nv_bfloat16 *z = static_cast<__nv_bfloat16 *>(a.bv) +
-                             (static_cast<size_t>(r2 / a.S) * a.nkv + h) * 128 * 64 + static_cast<size_t>(i) * 64;
-          for (int c = a.S; c < 16; ++c) z[c] = f2bf(0.f);
-        }
-      }
-    }
-    return;
-  }
-  // q rows and K rows: lanes cover consecutive features of one token
-#pragma unroll
-  for (int t = 0; t < 16; ++t) {
-    const int row = tok0 + t;
-    if (row >= p.M) break;
-    __nv_bfloat16 *o;
-    if (a.mode == 1) {
-      const int b = row / a.S, j = row % a.S;
-      o = kind == 0 ? static_cast<__nv_bfloat16 *>(a.q) + static_cast<size_t>(row) * a.nq * 128 + h * 128 + i
-                    : static_cast<__nv_bfloat16 *>(a.bk) + ((static_cast<size_t>(b) * a.nkv + h) * 64 + j) * 128 + i;
-    } else {
-      const int pg = a.tok_page[row];
-      if (pg < 0) continue;
-      o = static_cast<__nv_bfloat16 *>(a.k_cache) + static_cast<size_t>(g) * a.layer_elems +
-          ((static_cast<size_t>(pg) * a.nkv + h) * 64 + a.tok_slot[row]) * 128 + i;
-    }
-    *o = f2bf(v[t]);
-  }
-}
-
 // Apply the epilogue to 16 consecutive token columns of weight row n (ws:
-// the group's FP8 row scales, or null).  CB: rows per load batch of the
-// short-conv epilogue.
-template <int CB>
+// the group's FP8 row scales, or null).
 __device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n, int tok0, size_t goff,
-                                         const float *ws, int grp, float *xch) {
+                                         const float *ws) {
   const bool nok = n < p.N;
   if (ws) {
     const float sc = nok ? ws[n] : 0.f;
@@ -371,9 +158,6 @@ __device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n,
     for (int i = 0; i < 16; ++i) v[i] *= sc;
   }
   switch (p.epi) {
-    case EPI_HEADS:
-      heads_epi(p, v, n, grp, tok0, xch);
-      break;
     case EPI_BF16: {
       __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out), *ol = static_cast<__nv_bfloat16 *>(p.out_lo);
 #pragma unroll
@@ -413,25 +197,6 @@ __device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n,
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         if (nok && tok0 + i < p.M) o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] = tanhf(v[i] + b);
-    } break;
-    case EPI_CONV_PRE:
-    case EPI_CONV_POST: {
-      // rows 2g / 2g+1 = tap a / tap b of channel group g, in neighbouring
-      // lanes: exchange them, then each lane of the pair takes 8 of the
-      // group's 16 channels
-      const float bn = nok ? p.bias[n] : 0.f;
-      float c[16], o[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) c[i] = tanhf(v[i] + bn);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) o[i] = __shfl_xor_sync(0xffffffffu, c[i], 1);
-      if (!nok) break;
-      const bool odd = n & 1;
-      const int c0 = (n >> 1) * 16 + (odd ? 8 : 0);
-      if (odd)
-        conv_rows<CB>(p, p.epi == EPI_CONV_POST, o, c, c0, tok0);
-      else
-        conv_rows<CB>(p, p.epi == EPI_CONV_POST, c, o, c0, tok0);
     } break;
     case EPI_F32_SPLIT: {
       float *o = static_cast<float *>(p.out);
@@ -481,17 +246,31 @@ __device__ __forceinline__ void finalize_add_pre(const Params &p, float (&v)[16]
     if (nok && tok0 + i < p.M) o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] = r[i] + sc * v[i];
 }
 
+// bf16(scale[row] * code value) for 4 codes of one row (cols % 4 == 0)
+__global__ void fp8_rows_to_bf16_kernel(const uint32_t *codes, const float *scale, int cols4, long long n4,
+                                        uint2 *out) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float s = scale[i / cols4];
+  const uint2 v = e4m3x4_to_bf16x4(codes[i]);
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&v.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&v.y);
+  uint2 r;
+  r.x = pack_bf16(__low2float(a) * s, __high2float(a) * s);
+  r.y = pack_bf16(__low2float(b) * s, __high2float(b) * s);
+  out[i] = r;
+}
+
 __global__ void e4m3_to_bf16_kernel(const uint32_t *codes, int n4, uint2 *out) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n4) out[i] = e4m3x4_to_bf16x4(codes[i]);
 }
 
 template <int BN, bool SPLIT, bool F8>
-__global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, BN <= 32 ? 2 : 1)   // small tiles: two CTAs per SM
+__global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 : 1)
     gemm_tc_kernel(const __grid_constant__ WMaps wm, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmXlo, const Params p) {
   using C = Cfg<BN, SPLIT, F8>;
-  constexpr int CB_ = (F8 && BN <= 32) ? 1 : 4;   // short-conv load batch (96-register variants: 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *base = smem_raw + pad;
@@ -509,11 +288,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, BN <= 32 ? 2 : 1)   //
   uint64_t *cfull = rbar + 1;   // F8: converted weight tile ready
   uint64_t *cempty = cfull + C::CSTAGES;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cempty + C::CSTAGES);
-  float *spush = reinterpret_cast<float *>(base + C::RING + C::CTRL);   // push shares, or ...
-  float *xch = spush;                                                      // ... the head epilogue's exchange
-  // the head epilogue needs a whole tile in one CTA: no pushing of rows to
-  // the other CTAs of a cluster (its shares are pulled by rank 0 instead)
-  const bool push = C::PUSH && p.epi != EPI_HEADS;
+  float *spush = reinterpret_cast<float *>(base + C::RING + C::CTRL);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *bcast = reinterpret_cast<int *>(tmem_slot + 2);
 
@@ -551,7 +326,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, BN <= 32 ? 2 : 1)   //
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (push && p.csk > 1) cluster_sync();   // every CTA's barriers exist before any remote arrive
+  if (C::PUSH && p.csk > 1) cluster_sync();   // every CTA's barriers exist before any remote arrive
 
   // The activations, outputs and stream-K scratch are produced / consumed by
   // the neighbouring kernels of the step: only the weight stream may start
@@ -793,11 +568,6 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, BN <= 32 ? 2 : 1)   //
     const int r = q * 32 + lane;         // weight row within the tile
     const int et = threadIdx.x - 64;     // 0..127
     grid_dep_wait();                     // outputs / scratch are shared with the previous kernel
-    if (p.epi == EPI_HEADS && p.head.mode == 2 && blockIdx.x == 0)
-      // context injection: the requests' new lengths (the feature kernel saved
-      // the old ones; nothing reads ctx_len_in after it)
-      for (int b = et; b < p.head.B; b += 128)
-        p.head.ctx_out[b] = p.head.ctx_saved[b] + (p.head.cu_new[b + 1] - p.head.cu_new[b]);
     int seg = 0;
     for (long long it = begin; it < end; ++seg) {
       const int tile = static_cast<int>(it / p.kbpt);
@@ -812,7 +582,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, BN <= 32 ? 2 : 1)   //
       bool have_pre = false;
       if (BN == 16 && p.epi == EPI_ADD_F32) {
         const bool whole_t = kb0 == 0 && kb1 == p.kbpt;
-        const bool owner = push && p.csk > 1 && ((r + 1) * p.csk - 1) / BM == static_cast<int>(cluster_ctarank());
+        const bool owner = C::PUSH && p.csk > 1 && ((r + 1) * p.csk - 1) / BM == static_cast<int>(cluster_ctarank());
         if (whole_t || owner) {
           const int rt0 = tile % p.rt_total;
           const int n0 = (rt0 % p.rtpg) * BM + r, t0 = (tile / p.rt_total) * BN;
@@ -845,12 +615,12 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, BN <= 32 ? 2 : 1)   //
           if (have_pre)
             finalize_add_pre(p, v, rpre, n, tok0 + c * 16, goff, wsg);
           else
-            finalize<CB_>(p, v, n, tok0 + c * 16, goff, wsg, rt / p.rtpg, xch);
+            finalize(p, v, n, tok0 + c * 16, goff, wsg);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
-      } else if (push && p.csk > 1) {
+      } else if (C::PUSH && p.csk > 1) {
         // cluster split-K, small token tile: each row's fp32 share goes straight
         // into the shared memory of the CTA that finalises that row (rows
         // [k*BM/csk, (k+1)*BM/csk) belong to rank k); one release arrive per
@@ -911,7 +681,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, BN <= 32 ? 2 : 1)   //
           if (have_pre && mine)
             finalize_add_pre(p, v, rpre, n, tok0 + c * 16, goff, wsg);
           else
-            finalize<CB_>(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsg, rt / p.rtpg, xch);   // n >= N: not this CTA's row
+            finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsg);   // n >= N: not this CTA's row
         }
       } else if (p.csk > 1) {
         // cluster split-K: this CTA's fp32 share into its own smem, row-major
@@ -993,7 +763,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, BN <= 32 ? 2 : 1)   //
               v[4 * i + 2] = acc[i].z;
               v[4 * i + 3] = acc[i].w;
             }
-            finalize<CB_>(p, v, n, tok0 + c * 16, goff, wsg, rt / p.rtpg, xch);
+            finalize(p, v, n, tok0 + c * 16, goff, wsg);
           }
         }
         epi_bar();
@@ -1007,7 +777,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, BN <= 32 ? 2 : 1)   //
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 
-  if (!push && p.csk > 1) {
+  if (!C::PUSH && p.csk > 1) {
     // ---- cluster split-K reduction through distributed shared memory: CTA
     // r finalises tile rows [r*BM/csk, (r+1)*BM/csk) summing the csk shares in
     // rank order (deterministic); lanes hold consecutive rows (coalesced
@@ -1016,10 +786,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, BN <= 32 ? 2 : 1)   //
     if (warp >= 2 && warp < 6) {   // the epilogue warps
       const int et = threadIdx.x - 64;
       const int rank = static_cast<int>(cluster_ctarank());
-      // head epilogue: rank 0 finalises the whole tile (one head)
-      const bool heads = p.epi == EPI_HEADS;
-      const int r0 = heads ? 0 : rank * BM / p.csk;
-      const int rows = heads ? (rank == 0 ? BM : 0) : (rank + 1) * BM / p.csk - r0;
+      const int r0 = rank * BM / p.csk, rows = (rank + 1) * BM / p.csk - r0;
       const int tasks = rows * (BN / 16);
       const int tile = first_tile;
       const int rt = tile % p.rt_total;
@@ -1048,11 +815,353 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, BN <= 32 ? 2 : 1)   //
           }
         }
         const int n = valid ? (rt % p.rtpg) * BM + row : p.N;   // n >= N: nothing stored
-        finalize<CB_>(p, v, n, tokt + grp * 16, goff, wsg, rt / p.rtpg, xch);
+        finalize(p, v, n, tokt + grp * 16, goff, wsg);
       }
     }
     cluster_sync();   // nobody leaves while others still read its share
   }
+}
+
+// ------------------------------------------------------------------ CTA pairs
+// The tensor-bound projections (256-token tiles, bf16 weights and
+// activations) on CTA pairs with the 2-SM tcgen05.mma (cta_group::2,
+// M = 256 weight rows x N = BN tokens): each CTA of a 2-CTA cluster stages
+// its own 128 weight rows and its half of the token tile, so a 64-k stage is
+// 32 KB per SM instead of 48 KB for the same MMA work; the same shared
+// memory holds a six-deep ring instead of four, which is what the pipeline
+// needs to cover the L2 / DRAM latency at this operand rate.  Work: stream-K
+// over pair tiles (token tile, pair of weight row tiles), with the same
+// last-arriver fixup per CTA half as the single-CTA kernel; an odd last row
+// tile pairs with a phantom half whose weight rows TMA fills with zeros and
+// whose output nobody stores.
+//   even CTA (rank 0): warp 0 TMA, warp 1 MMA issue for the pair, warps 2-5
+//   epilogue of rows 0..127;  odd CTA: warp 0 TMA, warps 2-5 epilogue of its
+//   rows.  Full barriers live in the even CTA (both CTAs' TMA complete on
+//   them); the MMA completion arrives on both CTAs' empty / accumulator-full
+//   barriers (multicast commit); both CTAs' epilogues release an accumulator
+//   on the even CTA's barrier.
+template <int BN>
+struct PairCfg {
+  static constexpr int NT = 192;
+  static constexpr int BH = BN / 2;                    // this CTA's token rows
+  static constexpr int A_BYTES = BM * BK * 2;          // this CTA's 128 weight rows, one 64-k block
+  static constexpr int B_BYTES = BH * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+  static constexpr int RING = STAGES * STAGE_BYTES;
+  static constexpr int CTRL = 512;
+  static constexpr int TMEM_COLS = 2 * BN;             // two accumulators of BN columns
+  static constexpr int SMEM = 1024 + RING + CTRL;
+  static_assert((2 * STAGES + 5) * 8 + 12 <= CTRL, "pair GEMM control block overflows");
+  static_assert(SMEM <= 227 * 1024 && TMEM_COLS <= 512, "pair GEMM resources");
+};
+
+template <int BN>
+__global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
+    gemm_pair_kernel(const __grid_constant__ WMaps wm, const __grid_constant__ CUtensorMap tmX, const Params p) {
+  using C = PairCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t *base = smem_raw + pad;
+  uint8_t *sA = base;
+  uint8_t *sB = base + C::STAGES * C::A_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + C::RING);
+  uint64_t *empty = full + C::STAGES;
+  uint64_t *tfull = empty + C::STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *bcast = reinterpret_cast<int *>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());   // 0: the pair's MMA issuer
+  const int pair = blockIdx.x >> 1, Gp = p.G >> 1;
+  const int RTP = (p.rt_total + 1) >> 1;                  // row-tile pairs per token tile
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    mbar_init(&tempty[0], 8);   // four epilogue warps of each CTA
+    mbar_init(&tempty[1], 8);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int g = 0; g < p.n_groups; ++g) tma_prefetch_desc(&wm.m[g]);
+    tma_prefetch_desc(&tmX);
+  }
+  grid_dep_launch();
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();   // both CTAs' barriers and tensor memory exist
+  const uint32_t tmem = *tmem_slot;
+  const long long begin = range_begin(p.total, Gp, pair), end = range_begin(p.total, Gp, pair + 1);
+  const int first_pt = static_cast<int>(begin / p.kbpt);
+
+  // this CTA's weight rows of pair tile pt: (group, first row); phantom past the last row tile
+  auto rows_of = [&](int pt, int &g, int &row0, bool &phantom) {
+    const int rt = 2 * (pt % RTP) + rank;
+    phantom = rt >= p.rt_total;
+    const int rtc = phantom ? p.rt_total - 1 : rt;
+    g = rtc / p.rtpg;
+    row0 = (phantom ? p.rtpg : rtc % p.rtpg) * BM;   // phantom: past the group's rows (zero fill)
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const bool hint_w = p.tok_tiles == 1;
+      const long long n_my = end - begin;
+      auto full_addr = [&](int s) { return dsmem_addr(&full[s], 0u); };   // the even CTA's full barrier
+      auto load_w = [&](int s, int g, int row0, int kb) {
+        if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
+        (void)hint_w;
+        (void)pol_w;
+        tma_load_2d_pair(sA + s * C::A_BYTES, &wm.m[g], full_addr(s), kb * BK, row0);
+      };
+      auto load_x = [&](int s, int pt, int kb) {
+        const int tok = pt / RTP;
+        tma_load_2d_pair(sB + s * C::B_BYTES, &tmX, full_addr(s), kb * BK, tok * BN + rank * C::BH);
+      };
+      const int n_pre = static_cast<int>(n_my < C::STAGES ? n_my : C::STAGES);
+      // weights of the first ring slots depend on nothing: stream them while
+      // the previous kernel finishes, then wait for it before the activations
+      for (int i = 0; i < n_pre; ++i) {
+        const long long it = begin + i;
+        const int pt = static_cast<int>(it / p.kbpt), kb = static_cast<int>(it % p.kbpt);
+        int g, row0;
+        bool ph;
+        rows_of(pt, g, row0, ph);
+        load_w(i, g, row0, kb);
+      }
+      grid_dep_wait();
+      for (int i = 0; i < n_pre; ++i) {
+        const long long it = begin + i;
+        load_x(i, static_cast<int>(it / p.kbpt), static_cast<int>(it % p.kbpt));
+      }
+      uint32_t stage = n_pre % C::STAGES, phase = (n_pre == C::STAGES) ? 1u : 0u;
+      long long issued = n_pre;
+      bool ok = true;
+      for (long long it = begin + n_pre; it < end; ++it) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        const int pt = static_cast<int>(it / p.kbpt), kb = static_cast<int>(it % p.kbpt);
+        int g, row0;
+        bool ph;
+        rows_of(pt, g, row0, ph);
+        load_w(stage, g, row0, kb);
+        load_x(stage, pt, kb);
+        ++issued;
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        report(p.status, DFLASH_ERR_TIMEOUT);
+        *abort_flag = 1;
+        // let the copies in flight land before shared memory goes away: the
+        // even CTA waits for each issued phase of its full barriers (they
+        // count both CTAs' bytes); the odd CTA's copies complete there too,
+        // so it only holds on for a bounded moment
+        if (rank == 0) {
+          for (int s = 0; s < C::STAGES; ++s) {
+            if (issued <= s) break;
+            const long long last = s + C::STAGES * ((issued - 1 - s) / C::STAGES);
+            mbar_wait(&full[s], static_cast<uint32_t>((last / C::STAGES) & 1), nullptr, p.timeout_ns);
+          }
+        } else {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 50000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
+      uint32_t stage = 0, phase = 0;
+      int seg = 0;
+      bool ok = true;
+      for (long long it = begin; it < end && ok; ++seg) {
+        const int kb0 = static_cast<int>(it % p.kbpt);
+        const int kb1 = static_cast<int>((kb0 + (end - it) < p.kbpt ? kb0 + (end - it) : p.kbpt));
+        const int buf = seg & 1;
+        if (!mbar_wait(&tempty[buf], static_cast<uint32_t>(((seg >> 1) & 1) ^ 1), abort_flag, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / UK; ++k)
+            umma_bf16_pair(d, sdesc_k_sw128(a0 + k * UK * 2), sdesc_k_sw128(b0 + k * UK * 2), idesc,
+                           (kb > kb0 || k > 0) ? 1u : 0u);
+          umma_commit_pair(&empty[stage]);   // frees this stage in both CTAs
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(&tfull[buf]);       // accumulator ready in both CTAs
+        it += kb1 - kb0;
+      }
+      if (!ok) {
+        report(p.status, DFLASH_ERR_TIMEOUT);
+        *abort_flag = 1;
+        umma_commit_pair(drain);   // all issued MMAs retire before tensor memory is freed
+        mbar_wait(drain, 0, nullptr, p.timeout_ns);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const int et = threadIdx.x - 64;
+    const uint32_t tempty_leader0 = dsmem_addr(&tempty[0], 0u), tempty_leader1 = dsmem_addr(&tempty[1], 0u);
+    grid_dep_wait();
+    int seg = 0;
+    for (long long it = begin; it < end; ++seg) {
+      const int pt = static_cast<int>(it / p.kbpt);
+      const int kb0 = static_cast<int>(it % p.kbpt);
+      const int kb1 = static_cast<int>((kb0 + (end - it) < p.kbpt ? kb0 + (end - it) : p.kbpt));
+      const int buf = seg & 1;
+      const bool got = mbar_wait(&tfull[buf], static_cast<uint32_t>((seg >> 1) & 1), abort_flag, p.timeout_ns);
+      if (bar_or(1, 128, !got || *abort_flag)) {
+        if (et == 0) report(p.status, DFLASH_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      int g, row0;
+      bool phantom;
+      rows_of(pt, g, row0, phantom);
+      const int n = row0 + r;                                   // row within its group
+      const size_t goff = static_cast<size_t>(g) * p.out_gstride;
+      const int tok0 = (pt / RTP) * BN;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      float v[16];
+      auto release = [&]() {   // this warp's accumulator rows are read
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0)
+            mbar_arrive(&tempty[buf]);
+          else
+            mbar_arrive_remote(buf ? tempty_leader1 : tempty_leader0);
+        }
+      };
+      if (phantom) {
+        release();
+      } else if (kb0 == 0 && kb1 == p.kbpt) {
+        for (int c = 0; c < BN / 16; ++c) {
+          tmem_ld16(taddr + c * 16, v);
+          finalize(p, v, n, tok0 + c * 16, goff, nullptr);
+        }
+        release();
+      } else {
+        // partial tile: this CTA's fp32 share of its 128 rows to its slot;
+        // the CTA (of the same rank) completing the tile's k-range sums all
+        // shares in pair order
+        const int tile_h = pt * 2 + rank;
+        const int slot = (pt == first_pt) ? 0 : 1;
+        float *P = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * (BM * BN) + static_cast<size_t>(r) * BN;
+        for (int c = 0; c < BN / 16; ++c) {
+          tmem_ld16(taddr + c * 16, v);
+          float4 *P4 = reinterpret_cast<float4 *>(P + c * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) __stcg(P4 + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+        }
+        release();
+        epi_bar();
+        if (et == 0) {
+          __threadfence();
+          const int nk = kb1 - kb0;
+          const int old = atomicAdd(&p.counters[tile_h], nk);
+          const int last = (old + nk == p.kbpt) ? 1 : 0;
+          if (last) {
+            p.counters[tile_h] = 0;
+            __threadfence();
+          }
+          *bcast = last;
+        }
+        epi_bar();
+        if (*bcast) {
+          const long long t_beg = static_cast<long long>(pt) * p.kbpt;
+          const int c_lo = cta_of(t_beg, p.total, Gp);
+          const int c_hi = cta_of(t_beg + p.kbpt - 1, p.total, Gp);
+          const int slot_lo = range_begin(p.total, Gp, c_lo) < t_beg ? 1 : 0;
+          for (int c = 0; c < BN / 16; ++c) {
+            float4 acc[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int cc0 = c_lo; cc0 <= c_hi; cc0 += 4) {
+              float4 t[4][4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int cc = cc0 + u;
+                const float4 *Q4 = reinterpret_cast<const float4 *>(
+                    p.partials + (static_cast<size_t>(2 * cc + rank) * 2 + (cc == c_lo ? slot_lo : 0)) * (BM * BN) +
+                    static_cast<size_t>(r) * BN + c * 16);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) t[u][i] = cc <= c_hi ? __ldcg(Q4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  acc[i].x += t[u][i].x;
+                  acc[i].y += t[u][i].y;
+                  acc[i].z += t[u][i].z;
+                  acc[i].w += t[u][i].w;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              v[4 * i] = acc[i].x;
+              v[4 * i + 1] = acc[i].y;
+              v[4 * i + 2] = acc[i].z;
+              v[4 * i + 3] = acc[i].w;
+            }
+            finalize(p, v, n, tok0 + c * 16, goff, nullptr);
+          }
+        }
+        epi_bar();
+      }
+      it += kb1 - kb0;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // the pair's MMAs read both CTAs' shared memory: nobody leaves early
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, C::TMEM_COLS);
 }
 
 // Kernel attributes (dynamic shared memory; for small tiles the whole
@@ -1153,7 +1262,79 @@ int per_sm_of(int BN) {
   }
 }
 
+// The pair kernel: attributes once per device; returns how many 2-CTA
+// clusters can be resident at once (pairs need two SMs of one GPC), or < 0.
+template <int BN>
+int pair_setup() {
+  using C = PairCfg<BN>;
+  constexpr int MAX_DEV = 64;
+  static std::atomic<int> per_dev[MAX_DEV];
+  int dev = 0;
+  if (int e = cuda_check(cudaGetDevice(&dev), "device")) return e;
+  if (dev < 0 || dev >= MAX_DEV) return set_error(DFLASH_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, MAX_DEV);
+  int v = per_dev[dev].load(std::memory_order_acquire);
+  if (v == 0) {
+    if (int e = cuda_check(cudaFuncSetAttribute(gemm_pair_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                C::SMEM),
+                           "pair gemm smem attribute"))
+      return e;
+    cudaLaunchConfig_t cfg = {};
+    int sms = 0;
+    if (int e = cuda_check(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "SM count")) return e;
+    cfg.gridDim = dim3(2 * (sms / 2));
+    cfg.blockDim = dim3(C::NT);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (int e = cuda_check(cudaOccupancyMaxActiveClusters(&clusters, gemm_pair_kernel<BN>, &cfg),
+                           "pair gemm cluster occupancy"))
+      return e;
+    v = clusters > 0 ? clusters : 1;
+    per_dev[dev].store(v, std::memory_order_release);
+  }
+  return v;
+}
+
+template <int BN>
+int launch_pair(const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const Params &p) {
+  using C = PairCfg<BN>;
+  if (int e = pair_setup<BN>(); e < 0) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.G);
+  cfg.blockDim = dim3(C::NT);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN>, tW, tX, p), "pair gemm launch");
+}
+
 }  // namespace
+
+int fp8_rows_to_bf16(const Launch &lc, const void *codes, const float *scale, int rows, int cols, void *out) {
+  if (rows <= 0 || cols <= 0 || cols % 4 || !codes || !scale || !out || (reinterpret_cast<uintptr_t>(codes) & 3) ||
+      (reinterpret_cast<uintptr_t>(out) & 7))
+    return set_error(DFLASH_ERR_ARG, "fp8 weights to bf16: cols a positive multiple of 4, buffers aligned");
+  const long long n4 = static_cast<long long>(rows) * (cols / 4);
+  fp8_rows_to_bf16_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, lc.stream>>>(
+      static_cast<const uint32_t *>(codes), scale, cols / 4, n4, static_cast<uint2 *>(out));
+  return cuda_check(cudaGetLastError(), "fp8 weights to bf16 launch");
+}
+
+int gemm_pair_clusters() { return pair_setup<256>(); }
 
 int e4m3_to_bf16(const Launch &lc, const void *codes, int n, void *out) {
   if (n <= 0 || n % 4 || !codes || !out || (reinterpret_cast<uintptr_t>(codes) & 3) ||
@@ -1173,7 +1354,7 @@ int gemm_token_tile(int M, bool split, bool f8) {
   return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : (M <= 128 || split || f8) ? 128 : 256;
 }
 
-GemmPlan gemm_plan(int M, int N, int K, int n_groups, bool f8, bool split, bool paired, int per_sm, int num_sms,
+GemmPlan gemm_plan(int M, int N, int K, int n_groups, bool f8, bool split, bool swiglu, int per_sm, int num_sms,
                    int gemm_ctas) {
   GemmPlan pl = {};
   pl.BN = gemm_token_tile(M, split, f8);
@@ -1208,9 +1389,9 @@ GemmPlan gemm_plan(int M, int N, int K, int n_groups, bool f8, bool split, bool 
     // all pipeline fill; at least 2-way where the k-range allows)
     long long s = std::min<long long>(std::min<long long>(8, cap / pl.tiles),
                                       std::min<long long>(pl.kbpt, std::max<long long>(2, pl.kbpt / 8)));
-    // SwiGLU and the short conv pair rows 2i / 2i+1 in neighbouring lanes:
-    // row ranges must be even-aligned, so a power-of-two cluster there
-    if (paired)
+    // SwiGLU pairs rows 2i / 2i+1 in neighbouring lanes: row ranges must be
+    // even-aligned, so a power-of-two cluster there
+    if (swiglu)
       while (s & (s - 1)) --s;
     if (s >= 2) {
       pl.csk = static_cast<int>(s);
@@ -1224,8 +1405,7 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   const int M = op.M, N = op.N, K = op.K;
   const char *name = op.name;
   if (M <= 0 || N <= 0 || K <= 0) return DFLASH_OK;
-  if ((!op.W && op.n_groups <= 1) || !op.X || (!op.out && op.epi != EPI_HEADS))
-    return set_error(DFLASH_ERR_ARG, "gemm %s: null operand", name);
+  if ((!op.W && op.n_groups <= 1) || !op.X || !op.out) return set_error(DFLASH_ERR_ARG, "gemm %s: null operand", name);
   const uintptr_t al = reinterpret_cast<uintptr_t>(op.W) | reinterpret_cast<uintptr_t>(op.X) |
                        reinterpret_cast<uintptr_t>(op.X_lo);
   const bool f8 = op.w_fp8;
@@ -1242,27 +1422,7 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   const int per_sm = f8 ? (split ? per_sm_of<true, true>(BN) : per_sm_of<false, true>(BN))
                         : (split ? per_sm_of<true, false>(BN) : per_sm_of<false, false>(BN));
   if (per_sm < 0) return per_sm;
-  const bool conv = epi == EPI_CONV_PRE || epi == EPI_CONV_POST;
-  if (conv) {
-    const uintptr_t ya = reinterpret_cast<uintptr_t>(op.conv_y) | reinterpret_cast<uintptr_t>(op.conv_y_lo) |
-                         reinterpret_cast<uintptr_t>(op.conv_y32) | reinterpret_cast<uintptr_t>(op.out) |
-                         reinterpret_cast<uintptr_t>(op.out_lo);
-    if (N % 2 || !op.bias || op.conv_S < 1 || op.ldy % 8 || op.ldo % 8 || (ya & 31) ||
-        (epi == EPI_CONV_PRE ? !op.conv_y : !op.conv_y32))
-      return set_error(DFLASH_ERR_ARG, "gemm %s: short-conv epilogue operands", name);
-  }
-  if (epi == EPI_HEADS) {
-    const HeadArgs &h = op.head;
-    const int heads = h.mode == 1 ? h.nq + 2 * h.nkv : 2 * h.nkv;
-    const bool ok = (h.mode == 1 || h.mode == 2) && h.nkv > 0 && N == heads * BM && h.cs &&
-                    (h.mode == 2 ? (h.k_cache && h.v_cache && h.tok_page && h.tok_slot && h.cu_new && h.ctx_saved &&
-                                    h.ctx_out && n_groups <= MAX_GROUPS)
-                                 : (h.q && h.bk && h.bv && h.S >= 1 && h.S <= 16 && n_groups == 1)) &&
-                    (!h.norm || (h.mode == 2 || h.gq) && h.gk[0]);
-    if (!ok) return set_error(DFLASH_ERR_ARG, "gemm %s: head epilogue operands", name);
-  }
-  const GemmPlan pl = gemm_plan(M, N, K, n_groups, f8, split, epi == EPI_SWIGLU || conv, per_sm, lc.num_sms,
-                                lc.gemm_ctas);
+  const GemmPlan pl = gemm_plan(M, N, K, n_groups, f8, split, epi == EPI_SWIGLU, per_sm, lc.num_sms, lc.gemm_ctas);
   const long long tiles = pl.tiles;
   Params p = {};
   p.M = M;
@@ -1285,12 +1445,6 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   p.out2_lo = op.out2_lo;
   p.ldo2 = op.ldo2;
   p.bias = op.bias;
-  p.cy = op.conv_y;
-  p.cy_lo = op.conv_y_lo;
-  p.cy32 = op.conv_y32;
-  p.ldy = op.ldy;
-  p.cS = op.conv_S;
-  p.head = op.head;
   if (f8) {
     for (int g = 0; g < p.n_groups; ++g) {
       p.wscale[g] = p.n_groups > 1 ? op.wscale_g[g] : op.wscale;
@@ -1303,6 +1457,28 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   p.timeout_ns = lc.timeout_ns;
   if (tiles > sc.n_counters || static_cast<size_t>(p.G) * 2 * BM * BN > sc.partial_floats)
     return set_error(DFLASH_ERR_SHAPE, "gemm %s: workspace too small for %lld tiles", name, tiles);
+  // Tensor-bound 256-token tiles (bf16 weights and activations, no cluster
+  // split-K): CTA pairs with the 2-SM MMA.  gemm_ctas < 0 (test hook) forces
+  // -gemm_ctas pairs.
+  const bool pairs = !f8 && !split && BN == 256 && (lc.gemm_ctas < 0 || (lc.gemm_pairs && lc.gemm_ctas == 0)) &&
+                     (p.n_groups == 1 || p.rtpg % 2 == 0);
+  if (pairs) {
+    p.csk = 1;
+    const int max_pairs = pair_setup<256>();
+    if (max_pairs < 0) return max_pairs;
+    const long long rtp = (pl.rtpg * static_cast<long long>(p.n_groups) + 1) / 2;
+    const long long ptiles = rtp * pl.tok_tiles;
+    p.total = ptiles * pl.kbpt;
+    // as many pairs as fit at once, each at least 4 k-blocks and no pair
+    // tile cut into more than 2 pieces (a fixup reads at most 256 KB)
+    const long long min_kb = std::max<long long>(4, (pl.kbpt + 1) / 2);
+    long long gp = std::min<long long>(max_pairs, (p.total + min_kb - 1) / min_kb);
+    if (lc.gemm_ctas < 0) gp = -lc.gemm_ctas;
+    gp = std::max<long long>(1, std::min<long long>(gp, ptiles * pl.kbpt));
+    p.G = static_cast<int>(2 * gp);
+    if (2 * ptiles > sc.n_counters || static_cast<size_t>(p.G) * 2 * BM * BN > sc.partial_floats)
+      return set_error(DFLASH_ERR_SHAPE, "gemm %s: workspace too small for %lld pair tiles", name, ptiles);
+  }
   WMaps tW;
   CUtensorMap tX, tXl;
   for (int g = 0; g < p.n_groups; ++g) {
@@ -1316,7 +1492,7 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
       return e;
   }
   if (int e = make_tmap_2d(&tX, op.X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M, static_cast<uint64_t>(op.ldx) * 2,
-                           BK, BN))
+                           BK, pairs ? BN / 2 : BN))   // a pair's CTA stages half of the token tile
     return e;
   if (split) {
     if (int e = make_tmap_2d(&tXl, op.X_lo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M,
@@ -1326,12 +1502,7 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
     tXl = tX;
   }
   const double xb = (split ? 4.0 : 2.0) * M * K;
-  // short conv: y read and the result written for 8N channels (pre: bf16 y
-  // hi / lo in, hi / lo out; post: fp32 y in, fp32 residual read and written)
-  const double out_bytes = epi == EPI_HEADS       ? 2.0 * M * N
-                           : epi == EPI_CONV_PRE  ? (split ? 64.0 : 32.0) * M * N
-                           : epi == EPI_CONV_POST ? 96.0 * M * N
-                           : (epi == EPI_F32 || epi == EPI_TANH_BIAS) ? 4.0 * M * N
+  const double out_bytes = (epi == EPI_F32 || epi == EPI_TANH_BIAS) ? 4.0 * M * N
                            : epi == EPI_ADD_F32                      ? 8.0 * M * N
                            : epi == EPI_F32_SPLIT                    ? 8.0 * M * N
                            : epi == EPI_SWIGLU                       ? (op.out_lo ? 2.0 : 1.0) * M * N
@@ -1339,6 +1510,7 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   const double ng = p.n_groups;
   ProfScope ps(lc, name, ng * (wbytes * static_cast<double>(N) * K + (f8 ? 4.0 * N : 0.0) + out_bytes) + xb,
                ng * (split ? 4.0 : 2.0) * M * N * K);
+  if (pairs) return launch_pair<256>(lc, tW, tX, p);
   if (f8) return split ? launch_bn<true, true>(BN, lc, tW, tX, tXl, p) : launch_bn<false, true>(BN, lc, tW, tX, tXl, p);
   return split ? launch_bn<true, false>(BN, lc, tW, tX, tXl, p) : launch_bn<false, false>(BN, lc, tW, tX, tXl, p);
 }

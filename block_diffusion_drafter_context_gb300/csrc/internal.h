@@ -20,45 +20,7 @@ enum Epi : int {
   EPI_SWIGLU = 3,     // rows 2i / 2i+1 = gate_i / up_i: out[m][i] = silu(gate) * up (+ out_lo)
   EPI_TANH_BIAS = 4,  // out (fp32)  = tanh(acc + bias[n])   (conv coefficients)
   EPI_STORE_T = 5,    // out (activation dtype) = acc (+ out_lo on the bf16 path)
-  EPI_F32_SPLIT = 6,  // out (fp32) = acc, out2 / out2_lo = bf16 hi / lo halves of acc
-  // DFlash-2 short convolution fused into its coefficient GEMM.  Weight rows
-  // interleaved per 16-channel group g: row 2g = current-tap coefficient a_g,
-  // row 2g+1 = previous-tap coefficient b_g (N = H/8); [a; b] = tanh(acc +
-  // bias) is never stored: the epilogue applies y_j + a_j*y_j + b_j*y_{j-1}
-  // (y_{-1} = 0 at each block's first position) to the 16 channels of g.
-  EPI_CONV_PRE = 7,   // y = conv_y (+ conv_y_lo); out / out_lo = bf16 hi / lo halves of the result
-  EPI_CONV_POST = 8,  // y = conv_y32 (fp32); out (fp32 residual) += the result
-  // One 128-row weight tile = one attention head (head_dim 128): the head's
-  // q / k RMSNorm and RoPE, then the head written where attention reads it
-  // (draft: q rows, block K, block V^T; injection: the paged K / V^T cache).
-  // See HeadArgs.
-  EPI_HEADS = 9
-};
-
-// EPI_HEADS: what the heads of the launch are and where they go.  Heads are
-// the 128-row tiles of each group in order: mode 1 (draft q/k/v projection,
-// one group) nq q heads, nkv k heads, nkv v heads; mode 2 (context K/V
-// injection, one group per layer) nkv k heads, nkv v heads.  q and k heads
-// get the per-head RMSNorm (norm) and the rotation by cs.
-struct HeadArgs {
-  int mode = 0;
-  int nq = 0, nkv = 0;
-  int S = 16;                               // mode 1: block size (token row = b*S + j)
-  int norm = 0;
-  float eps = 0.f;
-  const float *gq = nullptr;                // q gain [128]
-  const float *gk[16] = {};                 // k gain [128] of each group (layer)
-  const float2 *cs = nullptr;               // [M][64] (cos, sin) of each token row's position, per pair (i, i+64)
-  void *q = nullptr;                        // mode 1: [M][nq*128] bf16
-  void *bk = nullptr, *bv = nullptr;        // mode 1: block K [B][nkv][64][128], block V^T [B][nkv][128][64] bf16
-  void *k_cache = nullptr, *v_cache = nullptr;   // mode 2: layer g at + g * layer_elems elements
-  size_t layer_elems = 0;
-  const int32_t *tok_page = nullptr;        // mode 2: pool page of each token row (< 0: not written)
-  const int32_t *tok_slot = nullptr;        // mode 2: slot in that page
-  const int32_t *cu_new = nullptr;          // mode 2: CTA 0 sets ctx_out[b] = ctx_saved[b] + new tokens of b
-  const int32_t *ctx_saved = nullptr;
-  int32_t *ctx_out = nullptr;
-  int B = 0;
+  EPI_F32_SPLIT = 6   // out (fp32) = acc, out2 / out2_lo = bf16 hi / lo halves of acc
 };
 
 // One projection.  Activations may come as two bf16 tensors X (high half)
@@ -78,13 +40,6 @@ struct GemmOp {
   void *out2 = nullptr, *out2_lo = nullptr;
   int ldo2 = 0;
   const float *bias = nullptr;
-  // EPI_CONV_*: the convolved activation [M][8N] (row stride ldy): bf16 hi /
-  // lo halves (pre sites) or fp32 (post sites); S = block size (positions
-  // per request, consecutive rows)
-  const void *conv_y = nullptr, *conv_y_lo = nullptr;
-  const float *conv_y32 = nullptr;
-  int ldy = 0, conv_S = 16;
-  HeadArgs head;                            // EPI_HEADS
   const char *name = "gemm";
   // grouped launch: n_groups weight matrices Wg[g] of the same shape applied
   // to the same activations, output g at out + g * out_gstride elements
@@ -119,7 +74,8 @@ struct Launch {
   int num_sms = 148;
   int *status = nullptr;                 // device status word
   unsigned long long timeout_ns = 2000000000ull;
-  int gemm_ctas = 0;                     // 0 = SM count
+  int gemm_ctas = 0;                     // 0 = SM count; < 0: that many CTA pairs (test hook)
+  int gemm_pairs = 0;                    // 256-token tiles on CTA pairs (2-SM MMA)
   Profiler *prof = nullptr;
 };
 
@@ -143,6 +99,10 @@ int cuda_check(cudaError_t e, const char *what);
 
 // The FP8 GEMM's E4M3 -> bf16 conversion over n codes (test hook).
 int e4m3_to_bf16(const Launch &lc, const void *codes, int n, void *out);
+// 2-CTA clusters of the pair GEMM resident at once on the current device (< 0: error).
+int gemm_pair_clusters();
+// bf16 copy of an E4M3 weight matrix with fp32 row scales.
+int fp8_rows_to_bf16(const Launch &lc, const void *codes, const float *scale, int rows, int cols, void *out);
 
 // TMA descriptor of a row-major 2-D tensor [rows][cols] (128-byte swizzle
 // unless told otherwise); box = box_cols x box_rows.
@@ -164,9 +124,7 @@ struct GemmPlan {
 int gemm_token_tile(int M, bool split, bool f8);
 // per_sm: CTAs of the chosen variant resident per SM; gemm_ctas > 0 forces
 // that many stream-K CTAs (test hook).
-// paired: the epilogue pairs weight rows 2i / 2i+1 (SwiGLU, short conv), so a
-// cluster's row ranges must be even-aligned.
-GemmPlan gemm_plan(int M, int N, int K, int n_groups, bool f8, bool split, bool paired, int per_sm, int num_sms,
+GemmPlan gemm_plan(int M, int N, int K, int n_groups, bool f8, bool split, bool swiglu, int per_sm, int num_sms,
                    int gemm_ctas);
 
 // bf16 operands on tcgen05 tensor cores.
@@ -202,28 +160,12 @@ int attention_f32(const Launch &lc, const AttnArgs &a);
 // *_lo outputs: low bf16 halves (value - high half) for split activations;
 // null to skip (always null on the fp32 path).
 // S = block size (anchor + S-1 mask positions), 2..16
-// cs (optional): [B*S][d/2] (cos, sin) of each row's RoPE angles at
-// position ctx_len[b] + j, for the q/k head epilogue of the QKV projection.
 int embed_rmsnorm(const Launch &lc, bool f32, const void *embed, const int32_t *anchor, int mask_id, int vocab,
-                  const float *gain, float eps, int B, int S, int H, float *x, void *u, void *u_lo,
-                  const int32_t *ctx_len = nullptr, int d = 0, float rope_base = 0.f, float2 *cs = nullptr);
+                  const float *gain, float eps, int B, int S, int H, float *x, void *u, void *u_lo);
 int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, int S, const float *gain, float eps,
                  void *out, void *out_lo, void *out_mask_rows, void *out_mask_lo);
-// Slots of the injected tokens (optional, with cs): token t of request b
-// (cu_new[b] <= t < cu_new[b+1]) goes to position ctx_len_in[b] + t -
-// cu_new[b]: its pool page (tok_page, -1 and DFLASH_ERR_DEVICE when the page
-// table has none), slot, and RoPE (cos, sin) [T][d/2].
-struct InjectSlots {
-  const int32_t *cu_new = nullptr;
-  const int32_t *page_table = nullptr;
-  int max_pages = 0, num_pages = 0, page = 64, d = 128;
-  float rope_base = 0.f;
-  float2 *cs = nullptr;
-  int32_t *tok_page = nullptr, *tok_slot = nullptr;
-};
 int feature_norm(const Launch &lc, bool f32, const float *in, int rows, int H, const float *gain, float eps,
-                 bool apply_norm, void *out, void *out_lo, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B,
-                 const InjectSlots *slots = nullptr);
+                 bool apply_norm, void *out, void *out_lo, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B);
 int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int S, int nq, int nkv, int d,
                  const float *g_q, const float *g_k, bool qk_norm, float eps, float rope_base,
                  const int32_t *ctx_len, void *q_out, void *bk, void *bv);

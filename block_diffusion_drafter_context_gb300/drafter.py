@@ -57,6 +57,27 @@ def make_config(cfg) -> B.dflash_config:
 CONV_SITES = ("pre_attn", "post_attn", "pre_ffn", "post_ffn")
 
 
+def fp8_bf16_copies(dw: dict) -> None:
+    """bf16 copies of every packed FP8 matrix (the library converts codes x
+    row scales on the device), stored beside them under *_bf16: the drafter
+    uses them for its tensor-bound launches (128+ tokens per launch)."""
+    torch = _torch()
+
+    def conv(codes, scale):
+        out = torch.empty(codes.shape, dtype=torch.bfloat16, device=codes.device)
+        B.dflash_fp8_weights_to_bf16(codes, scale, codes.shape[0], codes.shape[1], out)
+        return out
+
+    dw["w_fc_bf16"] = conv(dw["w_fc"], dw["s_fc"])
+    dw["lm_head_bf16"] = conv(dw["lm_head"], dw["s_lm_head"])
+    for L in dw["layers"]:
+        for k, sk in (("w_qkv", "s_qkv"), ("w_o", "s_o"), ("w_gu", "s_gu"), ("w_down", "s_down")):
+            L[k + "_bf16"] = conv(L[k], L[sk])
+        if "s_conv" in L:
+            L["w_conv_bf16"] = [conv(w, sc) for w, sc in zip(L["w_conv"], L["s_conv"])]
+    torch.cuda.synchronize()
+
+
 def upload_weights(cfg, W: dict, device="cuda") -> dict:
     """Upload a weight dict (layout of the synthetic generator) and pack it:
     w_qkv = [w_q; w_k; w_v] rows; w_gu rows interleaved gate_i, up_i; each
@@ -128,13 +149,16 @@ def make_weights_struct(dw: dict):
                 s.b_conv[j] = L["b_conv"][j].data_ptr()
                 if "s_conv" in L:
                     s.s_conv[j] = L["s_conv"][j].data_ptr()
-        for k in ("s_qkv", "s_o", "s_gu", "s_down"):
+        for k in ("s_qkv", "s_o", "s_gu", "s_down", "w_qkv_bf16", "w_o_bf16", "w_gu_bf16", "w_down_bf16"):
             if k in L:
                 setattr(s, k, L[k].data_ptr())
+        if "w_conv_bf16" in L:
+            for j in range(4):
+                s.w_conv_bf16[j] = L["w_conv_bf16"][j].data_ptr()
     w = B.dflash_weights()
     for k in ("w_fc", "g_fc", "embed", "lm_head", "g_final"):
         setattr(w, k, dw[k].data_ptr())
-    for k in ("s_fc", "s_lm_head"):
+    for k in ("s_fc", "s_lm_head", "w_fc_bf16", "lm_head_bf16"):
         if k in dw:
             setattr(w, k, dw[k].data_ptr())
     w.layers = lay
@@ -188,10 +212,15 @@ class PagedKV:
 class Drafter:
     """One drafter context: uploaded weights, a workspace, the C handle."""
 
-    def __init__(self, cfg, W: dict, max_batch: int, max_new_tokens: int, device="cuda", dev_weights=None):
+    def __init__(self, cfg, W: dict, max_batch: int, max_new_tokens: int, device="cuda", dev_weights=None,
+                 fp8_copies: bool = True):
+        """fp8_copies (FP8 weights only): also keep bf16 copies of the matrices
+        for the launches of 128+ tokens, where bf16 weights are faster."""
         torch = _torch()
         self.cfg = cfg
         self.dw = dev_weights if dev_weights is not None else upload_weights(cfg, W, device)
+        if getattr(cfg, "weight_fp8", False) and fp8_copies and "w_fc_bf16" not in self.dw:
+            fp8_bf16_copies(self.dw)
         self.wstruct, self._lay = make_weights_struct(self.dw)
         self.cstruct = make_config(cfg)
         self.ctx = B.dflash_create(self.cstruct, self.wstruct)

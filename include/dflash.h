@@ -138,6 +138,16 @@ typedef struct dflash_layer_weights {
   const float *s_gu;     /* [2F], interleaved like w_gu                       */
   const float *s_down;   /* [H]                                               */
   const float *s_conv[4];/* [H/8], interleaved like w_conv                   */
+  /* weight_fp8 only, optional: bf16 copies of the matrices above in the
+   * bf16 layout (e.g. from dflash_fp8_weights_to_bf16).  When given, a
+   * projection whose token tile is 128 tokens or more (tensor-bound: 128+
+   * tokens per launch) uses the copy; smaller launches, bound by the weight
+   * stream, use the E4M3 codes.  NULL: codes everywhere. */
+  const void *w_qkv_bf16;
+  const void *w_o_bf16;
+  const void *w_gu_bf16;
+  const void *w_down_bf16;
+  const void *w_conv_bf16[4];
 } dflash_layer_weights;
 
 /* Model weights (device pointers, not owned; the layer array is host memory
@@ -156,6 +166,8 @@ typedef struct dflash_weights {
   float sel_b_g;         /* context-gate bias                                */
   const float *s_fc;     /* weight_fp8 only: [H] row scales of w_fc          */
   const float *s_lm_head;/* weight_fp8 only: [V] row scales of lm_head       */
+  const void *w_fc_bf16;    /* weight_fp8 only, optional: bf16 copies (see  */
+  const void *lm_head_bf16; /* dflash_layer_weights)                         */
 } dflash_weights;
 
 /* Paged drafter KV cache (device memory, not owned, zero-filled when
@@ -300,6 +312,15 @@ DFLASH_API int dflash_set_wait_timeout(dflash_ctx *ctx, unsigned long long ns);
 /* Test hook: cap the CTA count of the persistent GEMM (0 = SM count). */
 DFLASH_API int dflash_set_gemm_ctas(dflash_ctx *ctx, int ctas);
 
+/* Projections with 256-token tiles (bf16 weights and activations) run on CTA
+ * pairs with the 2-SM tensor-core MMA (on = 1) or on single CTAs (on = 0,
+ * the default): a switch for comparing the two; results are identical up to
+ * fp32 summation order.  Host-only. */
+DFLASH_API int dflash_set_gemm_pairs(dflash_ctx *ctx, int on);
+/* Test hook: 2-CTA clusters of the pair GEMM that fit on the current device
+ * at once (from the occupancy calculator), or a negative error code. */
+DFLASH_API int dflash_debug_gemm_pair_clusters(void);
+
 /* Test hook: the least number of context tokens (a multiple of the page
  * size) the bf16 block attention gives each CTA of its balanced split; 64
  * splits the chunk list as finely as the SM count allows, 0 = automatic. */
@@ -333,7 +354,9 @@ DFLASH_API int dflash_debug_wait_flag(const int32_t *flag, unsigned long long ti
 /* Test hook: the library's tcgen05 GEMM on caller buffers, fp32 result
  *   out[m][n] = scale[n] * sum_k X[m][k] * W[n][k]
  * (scale = 1 for bf16 weights), with the same decomposition the drafting
- * calls use (gemm_ctas > 0 forces persistent stream-K over that many CTAs).
+ * calls use (gemm_ctas > 0 forces persistent stream-K over that many single
+ * CTAs; gemm_ctas < 0, where the tile is 256 tokens of bf16 weights, forces
+ * -gemm_ctas CTA pairs with the 2-SM MMA).
  *   W: device bf16 [N][K], or with w_fp8 E4M3 codes [N][K] and w_scale fp32 [N];
  *   X: device bf16 [M][K]; out: device fp32 [M][N]; K a multiple of 8 (16 with
  *   w_fp8); every pointer 16-byte aligned.
@@ -356,6 +379,16 @@ DFLASH_API int dflash_debug_gemm(const void *W, const float *w_scale, int w_fp8,
  * size. */
 DFLASH_API int dflash_debug_gemm_plan(int M, int N, int K, int n_groups, int w_fp8, int split_act, int swiglu,
                                       int per_sm, int num_sms, int gemm_ctas, long long *plan);
+
+/* bf16 copy of an FP8 weight matrix ("Draft quantization", [DF2] engine
+ * table): out[n][k] = bf16(scale[n] * e4m3(codes[n][k])), the E4M3 value
+ * decoded exactly and scaled in fp32, rounded once to bf16 (nearest even).
+ * For the optional *_bf16 fields of dflash_weights / dflash_layer_weights,
+ * made once at set-up.  codes: device uint8 [rows][cols], cols a multiple of
+ * 4; scale: device fp32 [rows]; out: device bf16 [rows][cols].  Asynchronous
+ * on `stream`. */
+DFLASH_API int dflash_fp8_weights_to_bf16(const void *codes, const float *scale, int rows, int cols, void *out,
+                                          dflash_stream_t stream);
 
 /* Test hook: the FP8 GEMM's own E4M3 -> bf16 weight conversion (the device
  * function its converter warps run) applied to n codes.

@@ -56,6 +56,7 @@ int main(void) {
   O(dflash_weights, layers) O(dflash_weights, sel_b_g) O(dflash_kv, num_pages) O(dflash_kernel_stat, ms)
   O(dflash_config, weight_fp8) O(dflash_layer_weights, s_qkv) O(dflash_layer_weights, s_conv)
   O(dflash_weights, s_fc) O(dflash_weights, s_lm_head)
+  O(dflash_layer_weights, w_qkv_bf16) O(dflash_layer_weights, w_conv_bf16) O(dflash_weights, lm_head_bf16)
   return 0;
 }
 """
@@ -87,6 +88,9 @@ int main(void) {
         "dflash_layer_weights.s_conv": B.dflash_layer_weights.s_conv.offset,
         "dflash_weights.s_fc": B.dflash_weights.s_fc.offset,
         "dflash_weights.s_lm_head": B.dflash_weights.s_lm_head.offset,
+        "dflash_layer_weights.w_qkv_bf16": B.dflash_layer_weights.w_qkv_bf16.offset,
+        "dflash_layer_weights.w_conv_bf16": B.dflash_layer_weights.w_conv_bf16.offset,
+        "dflash_weights.lm_head_bf16": B.dflash_weights.lm_head_bf16.offset,
     }
     for k, v in py.items():
         assert int(got[k]) == v, k

@@ -186,6 +186,8 @@ def test_exact_parity_cases_reach_every_decomposition():
     from tests.gemm_cases import GEMM_EXACT_CASES
     seen = set()
     for M, N, K, ctas, f8 in GEMM_EXACT_CASES:
+        if ctas < 0:   # forced CTA pairs: not a single-CTA plan
+            continue
         bn = B.dflash_debug_gemm_plan(M, N, K, 1, f8, False, False, 1, SMS, ctas)["BN"]
         p = B.dflash_debug_gemm_plan(M, N, K, 1, f8, False, False, 2 if bn <= 32 else 1, SMS, ctas)
         if p["csk"] > 1:

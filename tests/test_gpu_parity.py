@@ -314,6 +314,25 @@ def test_e4m3_conversion_matches_oracle_decode_for_every_code():
     assert (np.signbit(got[finite]) == np.signbit(ref[finite])).all()
 
 
+def test_fp8_weight_bf16_copy_is_the_scaled_decode():
+    """dflash_fp8_weights_to_bf16 (the bf16 copies FP8 drafters keep for their
+    tensor-bound launches): every finite code in every row, times that row's
+    fp32 scale in fp32, rounded once to bf16 - bit for bit."""
+    import torch
+    from block_diffusion_drafter_context_gb300 import binding as Bd
+    rng = np.random.default_rng(5)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    rows, cols = 37, 508
+    codes = rng.choice(finite, size=(rows, cols)).astype(np.uint8)
+    codes[0, :len(finite)] = finite
+    scale = (rng.random(rows) * 0.01 + 1e-4).astype(np.float32)
+    out = torch.empty((rows, cols), dtype=torch.bfloat16, device="cuda")
+    Bd.dflash_fp8_weights_to_bf16(torch.from_numpy(codes).cuda(), torch.from_numpy(scale).cuda(), rows, cols, out)
+    torch.cuda.synchronize()
+    ref = gen.f32_to_bf16_bits(scale[:, None] * O.e4m3_decode(codes).astype(np.float32))
+    assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+
+
 # E4M3 codes of the integers 0..4 (1 = 0x38, 2 = 0x40, 3 = 0x44, 4 = 0x48); the sign bit negates
 _E4M3_INT = {0: 0x00, 1: 0x38, 2: 0x40, 3: 0x44, 4: 0x48}
 
