@@ -47,7 +47,7 @@ DEFAULT_EXTRA = "C1,C2,C3"
 # GEMMs with at least this many token rows are judged against the tensor
 # peak (ridge point of the measured bf16 rate over the measured HBM rate)
 TENSOR_BOUND_TOKENS = 300
-GEMM_NAMES = ("fc", "kv_inject", "qkv", "o_proj", "gate_up", "down", "lm_head", "conv_coef", "conv")
+GEMM_NAMES = ("fc", "kv_inject", "qkv", "o_proj", "gate_up", "down", "lm_head", "lm_head_topk", "conv_coef")
 # kernel source files whose ncu DRAM counters in profiles/traffic.json stay
 # valid only while these files are unchanged
 KERNEL_SOURCES = {"attention": ("attention.cu", "common.cuh"), "gemm": ("gemm_tc.cu", "common.cuh"),
@@ -417,6 +417,7 @@ def run_workload(args, wl, steps, warmup, world, local, dev, headline):
     prefill = 0 if wl.kv_fill == "template" else int(ctx.max())
     dr = Drafter(cfg, W, max_batch=B, max_new_tokens=max(S * B, prefill), device=dev)
     Bd.dflash_set_gemm_pairs(dr.ctx, bool(args.gemm_pairs))
+    Bd.dflash_set_fused_topk(dr.ctx, bool(args.fused_topk))
     kv = PagedKV(cfg, table, npages, device=dev)
     stream = torch.cuda.current_stream().cuda_stream
     templates = kv_templates(wl, npages)
@@ -776,7 +777,7 @@ def run_ours(args):
         "cpu_baseline": res.get("cpu_baseline"),
         "e2e": res["e2e"], "e2e_graph": res["e2e_graph"],
         "gpu_launches": res["gpu_launches"], "launches_per_step": res["launches_per_step"],
-        "clocks": res["clocks"], "gemm_pairs": bool(args.gemm_pairs),
+        "clocks": res["clocks"], "gemm_pairs": bool(args.gemm_pairs), "fused_topk": bool(args.fused_topk),
     }
     for k in ("draft_tokens_per_s", "expected_committed_tokens_per_s", "mean_accept_len", "expected_accept_len",
               "per_kernel", "instrumented_ms_per_step", "eager_ms_per_step", "prefill_injection", "setup_s"):
@@ -810,6 +811,8 @@ def main():
     ap.add_argument("--mode", default="greedy", choices=["greedy", "sampling"],
                     help="path selection and verification: greedy (default) or sampling + rejection")
     ap.add_argument("--oracle-probe", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--fused-topk", type=int, default=0,
+                    help="LM head with its top-16 epilogue (1) or logits + standalone top-16 (0, default)")
     ap.add_argument("--gemm-pairs", type=int, default=0,
                     help="256-token GEMM tiles on CTA pairs with the 2-SM MMA (1) or single CTAs (0, default)")
     # smaller variants of the headline workload for profiling captures

@@ -27,7 +27,7 @@ EXPORTS = (
     "dflash_topk16_noalloc", "dflash_sample_path", "dflash_verify_rejection", "dflash_set_block_size",
     "dflash_get_block_size", "dflash_debug_e4m3_to_bf16", "dflash_debug_gemm_scratch_bytes", "dflash_debug_gemm",
     "dflash_debug_gemm_plan", "dflash_set_gemm_pairs", "dflash_fp8_weights_to_bf16",
-    "dflash_debug_gemm_pair_clusters",
+    "dflash_debug_gemm_pair_clusters", "dflash_set_fused_topk",
 )
 
 
@@ -100,6 +100,7 @@ def load(path: str = LIB_PATH):
         "dflash_set_wait_timeout": (i, [vp, c_ulonglong]),
         "dflash_set_gemm_ctas": (i, [vp, i]),
         "dflash_set_gemm_pairs": (i, [vp, i]),
+        "dflash_set_fused_topk": (i, [vp, i]),
         "dflash_set_attn_split": (i, [vp, i]),
         "dflash_set_block_size": (i, [vp, i]),
         "dflash_get_block_size": (i, [vp]),
@@ -107,7 +108,7 @@ def load(path: str = LIB_PATH):
         "dflash_profile_end": (i, [vp, POINTER(dflash_kernel_stat), i, POINTER(c_int)]),
         "dflash_debug_wait_flag": (i, [vp, c_ulonglong, vp, vp]),
         "dflash_debug_e4m3_to_bf16": (i, [vp, i, vp, vp]),
-        "dflash_fp8_weights_to_bf16": (i, [vp, vp, i, i, vp, vp]),
+        "dflash_fp8_weights_to_bf16": (i, [vp, i, i, vp, vp]),
         "dflash_debug_gemm_pair_clusters": (i, []),
         "dflash_debug_gemm_scratch_bytes": (c_size_t, []),
         "dflash_debug_gemm": (i, [vp, vp, i, vp, i, i, i, vp, vp, c_size_t, i, vp]),
@@ -217,6 +218,10 @@ def dflash_set_gemm_ctas(ctx, n: int):
     return _check(load().dflash_set_gemm_ctas(ctx, n))
 
 
+def dflash_set_fused_topk(ctx, on: bool):
+    return _check(load().dflash_set_fused_topk(ctx, int(bool(on))))
+
+
 def dflash_set_gemm_pairs(ctx, on: bool):
     return _check(load().dflash_set_gemm_pairs(ctx, int(bool(on))))
 
@@ -257,8 +262,8 @@ def dflash_debug_gemm_pair_clusters() -> int:
     return load().dflash_debug_gemm_pair_clusters()
 
 
-def dflash_fp8_weights_to_bf16(codes, scale, rows, cols, out, stream=None):
-    return _check(load().dflash_fp8_weights_to_bf16(_p(codes), _p(scale), rows, cols, _p(out), _stream(stream)))
+def dflash_fp8_weights_to_bf16(codes, rows, cols, out, stream=None):
+    return _check(load().dflash_fp8_weights_to_bf16(_p(codes), rows, cols, _p(out), _stream(stream)))
 
 
 def dflash_debug_e4m3_to_bf16(codes, n, out, stream=None):

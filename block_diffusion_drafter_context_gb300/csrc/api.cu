@@ -22,6 +22,7 @@ struct dflash_ctx {
   unsigned long long timeout_ns = 2000000000ull;
   int gemm_ctas = 0;
   int gemm_pairs = 0;
+  int fused_topk = 0;      // bf16: LM head with its top-16 epilogue (no logits round trip)
   int attn_split = 0;
   int block = 16;   // runtime block size S (2..cfg.block_size)
   dflash::Profiler prof;
@@ -140,7 +141,7 @@ struct Layout {
   size_t status, gemm_ctr, gemm_part, topk_ctr, attn_ctr, attn_part, attn_part_slots, topk_part;
   size_t x, u, u2, qkv, q, bk, bv, o, ysub, coef, hmid, hmask, hfinal, logits, scores, lse;
   size_t u_lo, u2_lo, o_lo, ysub_lo, hmid_lo, hmask_lo, ysub32;
-  size_t fc, f, f_lo, kvproj, ctx_saved;
+  size_t fc, f, f_lo, kvproj, ctx_saved, cand;
   size_t total;
   size_t gemm_part_floats;
 };
@@ -200,6 +201,8 @@ Layout layout(const dflash_ctx *c, int B, int Tn, int S_ = 0) {
   L.f_lo = take(tl * Tn * H);
   L.kvproj = take(4ull * g.n_layers * Tn * 2 * nkv * d);
   L.ctx_saved = take(sizeof(int) * static_cast<size_t>(B));
+  // the LM head's top-16 candidates: 16 keys per mask row per 128-row vocabulary tile
+  L.cand = take(8ull * B * J * ((V + 127) / 128) * 16);
   L.total = off;
   return L;
 }
@@ -262,7 +265,8 @@ GemmOp wq(const dflash_ctx *c, GemmOp op, const float *scale, const void *bf16_c
   if (c->cfg.weight_fp8) {
     const bool split = op.X_lo != nullptr;
     if (bf16_copy && gemm_token_tile(op.M, split, false) >= 128) {
-      op.W = bf16_copy;
+      op.W = bf16_copy;        // exact code values; the row scales apply in the epilogue
+      op.wscale = scale;
       return op;
     }
     op.w_fp8 = true;
@@ -386,6 +390,12 @@ int dflash_set_gemm_ctas(dflash_ctx *ctx, int ctas) {
   return DFLASH_OK;
 }
 
+int dflash_set_fused_topk(dflash_ctx *ctx, int on) {
+  if (!ctx) return set_error(DFLASH_ERR_ARG, "null context");
+  ctx->fused_topk = on != 0;
+  return DFLASH_OK;
+}
+
 int dflash_set_gemm_pairs(dflash_ctx *ctx, int on) {
   if (!ctx) return set_error(DFLASH_ERR_ARG, "null context");
   ctx->gemm_pairs = on != 0;
@@ -451,7 +461,7 @@ int dflash_inject_context(dflash_ctx *ctx, const dflash_kv *kv, const void *targ
     const dflash_layer_weights &lw = ctx->layers[l];
     const void *wl = copies ? lw.w_qkv_bf16 : lw.w_qkv;
     kvop.Wg[l] = static_cast<const char *>(wl) + (f32 ? te : tw) * static_cast<size_t>(nq) * d * H;
-    if (kvop.w_fp8) kvop.wscale_g[l] = lw.s_qkv + static_cast<size_t>(nq) * d;
+    if (g.weight_fp8) kvop.wscale_g[l] = lw.s_qkv + static_cast<size_t>(nq) * d;   // codes or their exact copies
     gk[l] = lw.g_k;
   }
   if (!f32 && (2 * nkv * d) % 128 == 0 && g.n_layers > 1) {
@@ -594,6 +604,22 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
   if (int e = rmsnorm_rows(lc, f32, x, R, H, S, ctx->w.g_final, g.eps, hfinal, nullptr, at<void>(ws, L.hmask),
                            lo(L.hmask_lo)))
     return e;
+  // the fused epilogue hides under the LM head's weight stream only with
+  // small token tiles (at most 32 mask rows per launch); larger launches are
+  // tensor-bound and its per-tile selection would lengthen them
+  if (!f32 && ctx->fused_topk && gemm_token_tile(B * J, split, g.weight_fp8 != 0) <= 32) {
+    // LM head with the top-16 selection in its epilogue: per 128-row
+    // vocabulary tile the 16 largest keys of each mask row (the fp32 logits
+    // are written only when the caller asks for them), then one merge
+    GemmOp op = wq(ctx, mk(ctx->w.lm_head, H, at<void>(ws, L.hmask), lo(L.hmask_lo), H, B * J, V, H, EPI_TOPK,
+                           logits, V, "lm_head_topk"),
+                   ctx->w.s_lm_head, ctx->w.lm_head_bf16);
+    op.cand = at<uint64_t>(ws, L.cand);
+    op.cand_ld = (V + 127) / 128;
+    if (int e = proj(ctx, lc, ws, L, op)) return e;
+    return topk16_merge(lc, op.cand, B * J, op.cand_ld, topk_ids, topk_logits, at<uint64_t>(ws, L.topk_part),
+                        at<int>(ws, L.topk_ctr), TOPK_MAX_CHUNKS);
+  }
   if (int e = proj(ctx, lc, ws, L,
                    wq(ctx, mk(ctx->w.lm_head, H, at<void>(ws, L.hmask), lo(L.hmask_lo), H, B * J, V, H, EPI_F32, lg, V,
                               "lm_head"),
@@ -799,11 +825,12 @@ int dflash_debug_gemm_plan(int M, int N, int K, int n_groups, int w_fp8, int spl
   return DFLASH_OK;
 }
 
-int dflash_fp8_weights_to_bf16(const void *codes, const float *scale, int rows, int cols, void *out,
-                               dflash_stream_t stream) {
+int dflash_fp8_weights_to_bf16(const void *codes, int rows, int cols, void *out, dflash_stream_t stream) {
+  if (rows <= 0 || cols <= 0 || cols % 4)
+    return set_error(DFLASH_ERR_ARG, "fp8 weights to bf16: positive rows, cols a multiple of 4");
   Launch lc;
   lc.stream = reinterpret_cast<cudaStream_t>(stream);
-  return fp8_rows_to_bf16(lc, codes, scale, rows, cols, out);
+  return fp8_rows_to_bf16(lc, codes, static_cast<long long>(rows) * cols, out);
 }
 
 int dflash_debug_gemm_pair_clusters(void) { return gemm_pair_clusters(); }

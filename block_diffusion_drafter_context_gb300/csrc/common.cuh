@@ -71,6 +71,22 @@ __device__ __forceinline__ bool bar_or(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
+// ---------------------------------------------------------------- top-k keys
+// (value, id) packed into one 64-bit key whose unsigned order is value
+// descending, id ascending on ties: every key is unique, selections are
+// deterministic.  Key 0 lies below every real key.
+__device__ __forceinline__ uint64_t make_key(float v, int id) {
+  uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);   // -0 and +0 compare equal
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(id));
+}
+__device__ __forceinline__ float key_value(uint64_t k) {
+  uint32_t u = static_cast<uint32_t>(k >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(u);
+}
+__device__ __forceinline__ int key_id(uint64_t k) { return static_cast<int>(~static_cast<uint32_t>(k)); }
+
 // ---------------------------------------------------------------- PDL
 __device__ __forceinline__ void grid_dep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -258,6 +258,73 @@ __device__ __forceinline__ void store16(__nv_bfloat16 *dst, const float (&x)[16]
   reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// Small batches: the same outputs with one warp per (block row, head) and
+// no shared memory, so that the block attention's CTAs (which take nearly
+// all of an SM's shared memory) can already become resident - and set up -
+// while this kernel runs under programmatic dependent launch.
+// qkv: fp32 [B*S][(nq+2nkv)*d] (S = block size).  One warp per (token,
+// head).  q heads -> q_out [B*S][nq*d]; k heads -> bk [B][nkv][64][d]
+// (normed, rotated); v heads -> bv [B][nkv][d][64], transposed like the V
+// pages.  Rows / columns S..63 are padding up to one 64-token page:
+// attention masks the scores of rows S.. and skips V columns 16..; V columns
+// S..15 share a k-step with the block tokens and are written as zeros.
+template <typename T, int DPL>
+__global__ void __launch_bounds__(256) qk_rope_rows_kernel(const float *qkv, int nq, int nkv, int S, const float *g_q,
+                                                      const float *g_k, int qk_norm, float eps, const RopeArgs rp,
+                                                      const int32_t *ctx_len, T *q_out, T *bk, T *bv) {
+  constexpr int D = DPL * 32;
+  const int tok = blockIdx.x, b = tok / S, j = tok % S;
+  const int head = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int nh = nq + 2 * nkv;
+  // the norm gain and this lane's angles are weights: read before the wait
+  // for the projections, off the dependent chain
+  const bool is_q = head < nq, normed = qk_norm && head < nq + nkv;
+  float gn[DPL], th_hi[DPL / 2], th_lo[DPL / 2];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) gn[i] = normed ? (is_q ? g_q : g_k)[lane + 32 * i] : 1.f;
+  lane_thetas(rp, lane, th_hi, th_lo);
+  pdl_start();
+  if (head >= nh) return;
+  const float *src = qkv + static_cast<size_t>(tok) * nh * D + static_cast<size_t>(head) * D;
+  float v[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) v[i] = src[lane + 32 * i];
+  if (head >= nq + nkv) {   // value head: copy, transposed
+    T *dst = bv + (static_cast<size_t>(b) * nkv + (head - nq - nkv)) * D * 64 + j;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + static_cast<size_t>(lane + 32 * i) * 64, v[i]);
+    // the block's PV k-step reads columns 0..15: below a block of 16 the
+    // columns S..15 get zeros (a 0 probability times a stale NaN is NaN),
+    // spread over the block's tokens: token j clears j+S, j+2S, ...
+    for (int c = j + S; c < 16; c += S)
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + (c - j) + static_cast<size_t>(lane + 32 * i) * 64, 0.f);
+    return;
+  }
+  const int pos = ctx_len[b] + j;
+  if (qk_norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) ss += v[i] * v[i];
+    const float r = rsqrtf(warp_sum(ss) / D + eps);
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) v[i] *= r * gn[i];
+  }
+  float o[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL / 2; ++i) {   // pairs (lane + 32i, lane + 32i + D/2)
+    float c, s;
+    rope_cs(pos, th_hi[i], th_lo[i], c, s);
+    const float x1 = v[i], x2 = v[i + DPL / 2];
+    o[i] = x1 * c - x2 * s;
+    o[i + DPL / 2] = x2 * c + x1 * s;
+  }
+  T *dst = is_q ? q_out + static_cast<size_t>(tok) * nq * D + static_cast<size_t>(head) * D
+                : bk + ((static_cast<size_t>(b) * nkv + (head - nq)) * 64 + j) * D;
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) Elt<T>::st(dst + lane + 32 * i, o[i]);
+}
+
 // Per-head RMSNorm and RoPE of one head row held as lane + 32 i (i < DPL),
 // pairs (i, i + DPL/2); cs: the row's (cos, sin) per pair, in shared memory.
 template <int DPL>
@@ -597,6 +664,25 @@ int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int S, int
                  const float *g_q, const float *g_k, bool qk_norm, float eps, float rope_base, const int32_t *ctx_len,
                  void *q_out, void *bk, void *bv) {
   if (S > 16) return set_error(DFLASH_ERR_UNSUPPORTED, "q/k norm + RoPE: block size above 16");
+  const RopeArgs rp = rope_table(d, rope_base);
+  if (2 * B * nkv < lc.num_sms) {
+    // few (request, kv head) lists: the shared-memory-free row kernel
+    dim3 grid_rows(B * S, (nq + 2 * nkv + 7) / 8);
+    return run(lc, "qk_norm_rope", [&] {
+#define QKR(T, DPL)                                                                                        \
+  launch_pdl(qk_rope_rows_kernel<T, DPL>, dim3(grid_rows), dim3(256), 0, lc.stream, qkv, nq, nkv, S, g_q, g_k, qk_norm, \
+             eps, rp, ctx_len, tp<T>(q_out), tp<T>(bk), tp<T>(bv))
+      if (f32 && d == 64)
+        QKR(float, 2);
+      else if (f32)
+        QKR(float, 4);
+      else if (d == 64)
+        QKR(__nv_bfloat16, 2);
+      else
+        QKR(__nv_bfloat16, 4);
+#undef QKR
+    });
+  }
   // split each (request, kv head) over nz CTAs until the launch covers the
   // SMs, keeping at least 8 (head, row) items per CTA
   const int items = (nq / nkv + 1) * S;
@@ -604,7 +690,6 @@ int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int S, int
   nz = nz < 1 ? 1 : (nz > items / 8 ? (items / 8 > 0 ? items / 8 : 1) : nz);
   nz = nz > d ? d : nz;
   dim3 grid(B, nkv, nz);
-  const RopeArgs rp = rope_table(d, rope_base);
   return run(lc, "qk_norm_rope", [&] {
 #define QK(T, DPL)                                                                                         \
   launch_pdl(qk_rope_kernel<T, DPL>, dim3(grid), dim3(256), 0, lc.stream, qkv, nq, nkv, S, g_q, g_k, qk_norm, eps, rp, ctx_len, \

@@ -84,6 +84,10 @@ struct Cfg {
   // the owning CTA: at most (csk - 1) * ceil(128 / csk) <= 120 rows arrive
   static constexpr bool PUSH = BN <= 32;
   static constexpr int PUSH_BYTES = PUSH ? 120 * BN * 4 : 0;
+  // the top-16 epilogue's exchange (4 warps x 16 tokens x 16 keys); it never
+  // runs with the push path, so the two share one region
+  static constexpr int XCH_BYTES = 4 * 16 * 16 * 8;
+  static constexpr int XREG = PUSH_BYTES > XCH_BYTES ? PUSH_BYTES : XCH_BYTES;
   static constexpr int CTRL = 512;                     // mbarriers and flags
   // Small token tiles (weight streaming): ~100 KB of ring, so two GEMM CTAs
   // fit on one SM and, under programmatic dependent launch, the next GEMM's
@@ -91,13 +95,13 @@ struct Cfg {
   // (152 x 5 stages in flight still exceed what HBM needs in flight).  F8
   // keeps the whole CTA within half an SM.  Large token tiles (tensor-bound):
   // one CTA per SM with a deeper ring.
-  static constexpr int BUDGET = BN <= 32 ? (F8 ? (SMEM_PER_SM / 2 - 1024 - 1024 - CTRL - PUSH_BYTES) : 100 * 1024)
+  static constexpr int BUDGET = BN <= 32 ? (F8 ? (SMEM_PER_SM / 2 - 1024 - 1024 - CTRL - XREG) : 100 * 1024)
                                          : 200 * 1024;
   static constexpr int STAGES_RAW = BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : (STAGES_RAW < 2 ? 2 : STAGES_RAW);
   static constexpr int TMEM_COLS = F8 ? pow2_at_least(A_COL + CSTAGES * A_TCOLS) : (2 * BN < 32 ? 32 : 2 * BN);
   static constexpr int RING = STAGES * STAGE_BYTES;
-  static constexpr int SMEM = 1024 + RING + CTRL + PUSH_BYTES;
+  static constexpr int SMEM = 1024 + RING + CTRL + XREG;
   static_assert((2 * STAGES + 2 * CSTAGES + 6) * 8 + 12 <= CTRL, "GEMM control block overflows");
   static_assert(RING >= BM * BN * 4, "the ring must hold one fp32 tile (cluster split-K share)");
   static_assert(!F8 || BN > 32 || 2 * (SMEM + 1024) <= SMEM_PER_SM, "two F8 CTAs must fit on one SM");
@@ -122,6 +126,8 @@ struct Params {
   void *out2, *out2_lo;
   int ldo2;
   const float *bias;
+  uint64_t *cand;           // EPI_TOPK: [M][cand_ld][16]
+  int cand_ld;
   const float *wscale[MAX_GROUPS];   // F8: per-row weight scales of each group
   float *partials;     // [G][2][BM][BN] row-major shares
   int *counters;       // [tiles]
@@ -147,10 +153,68 @@ __device__ __forceinline__ void store_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, s
   if (lo) lo[i] = f2bf(v - bf2f(h));
 }
 
+// Lanes 0..15 sorted descending, lanes 16..31 ascending (a bitonic
+// sequence) -> all 32 sorted descending.
+__device__ __forceinline__ uint64_t warp_merge_desc(uint64_t key, int lane) {
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const uint64_t o = __shfl_xor_sync(0xffffffffu, key, j);
+    key = (lane & j) == 0 ? (key > o ? key : o) : (key < o ? key : o);
+  }
+  return key;
+}
+
+// EPI_TOPK ("DFlash 2", Arquitectura del Sistema item 1: 16 candidates per
+// position from the shared LM head): the 16 largest (logit, vocabulary id)
+// keys of each of the 16 token columns over this 128-row vocabulary tile,
+// without the logits leaving the chip.  Row n = vocabulary id (the LM head
+// is one group; n / 128 is the tile).  All 128 epilogue threads call it
+// together: every warp sorts its 32 rows per token (bitonic; the keys of the
+// 32 lanes end descending, lane 0 largest; four tokens at a time), the four warp
+// lists of each token meet in shared memory, and one warp per four tokens
+// merges them (two bitonic merges of 16 + 16, then one more).
+__device__ __noinline__ void topk_tile(const Params &p, const float (&v)[16], int n, int tok0, uint64_t *xch) {
+  const int r = n & 127, lane = r & 31, q4 = r >> 5, rt = n >> 7;
+  const bool nok = n < p.N;
+  for (int t0 = 0; t0 < 16; t0 += 4) {   // four independent sorting networks in flight
+    uint64_t key[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) key[u] = nok ? make_key(v[t0 + u], n) : 0ull;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const bool keep_max = ((lane & k) == 0) == ((lane & j) == 0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint64_t o = __shfl_xor_sync(0xffffffffu, key[u], j);
+          key[u] = keep_max ? (key[u] > o ? key[u] : o) : (key[u] < o ? key[u] : o);
+        }
+      }
+    if (lane < 16) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) xch[(q4 * 16 + t0 + u) * 16 + lane] = key[u];
+    }
+  }
+  epi_bar();
+  for (int tt = 0; tt < 4; ++tt) {
+    const int t = q4 * 4 + tt;
+    const uint64_t *l0 = xch + (0 * 16 + t) * 16, *l1 = xch + (1 * 16 + t) * 16;
+    const uint64_t *l2 = xch + (2 * 16 + t) * 16, *l3 = xch + (3 * 16 + t) * 16;
+    uint64_t a = warp_merge_desc(lane < 16 ? l0[lane] : l1[31 - lane], lane);
+    uint64_t b = warp_merge_desc(lane < 16 ? l2[lane] : l3[31 - lane], lane);
+    const uint64_t b_rev = __shfl_sync(0xffffffffu, b, 31 - lane);
+    const uint64_t c = warp_merge_desc(lane < 16 ? a : b_rev, lane);
+    const int row = tok0 + t;
+    if (row < p.M && lane < 16) p.cand[(static_cast<size_t>(row) * p.cand_ld + rt) * 16 + lane] = c;
+  }
+  epi_bar();   // the exchange is free again
+}
+
 // Apply the epilogue to 16 consecutive token columns of weight row n (ws:
 // the group's FP8 row scales, or null).
 __device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n, int tok0, size_t goff,
-                                         const float *ws) {
+                                         const float *ws, uint64_t *xch) {
   const bool nok = n < p.N;
   if (ws) {
     const float sc = nok ? ws[n] : 0.f;
@@ -158,6 +222,15 @@ __device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n,
     for (int i = 0; i < 16; ++i) v[i] *= sc;
   }
   switch (p.epi) {
+    case EPI_TOPK: {
+      if (p.out) {   // the logits too, when asked for
+        float *o = static_cast<float *>(p.out);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (nok && tok0 + i < p.M) o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] = v[i];
+      }
+      topk_tile(p, v, n, tok0, xch);
+    } break;
     case EPI_BF16: {
       __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out), *ol = static_cast<__nv_bfloat16 *>(p.out_lo);
 #pragma unroll
@@ -246,21 +319,6 @@ __device__ __forceinline__ void finalize_add_pre(const Params &p, float (&v)[16]
     if (nok && tok0 + i < p.M) o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] = r[i] + sc * v[i];
 }
 
-// bf16(scale[row] * code value) for 4 codes of one row (cols % 4 == 0)
-__global__ void fp8_rows_to_bf16_kernel(const uint32_t *codes, const float *scale, int cols4, long long n4,
-                                        uint2 *out) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n4) return;
-  const float s = scale[i / cols4];
-  const uint2 v = e4m3x4_to_bf16x4(codes[i]);
-  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&v.x);
-  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&v.y);
-  uint2 r;
-  r.x = pack_bf16(__low2float(a) * s, __high2float(a) * s);
-  r.y = pack_bf16(__low2float(b) * s, __high2float(b) * s);
-  out[i] = r;
-}
-
 __global__ void e4m3_to_bf16_kernel(const uint32_t *codes, int n4, uint2 *out) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n4) out[i] = e4m3x4_to_bf16x4(codes[i]);
@@ -288,7 +346,11 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
   uint64_t *cfull = rbar + 1;   // F8: converted weight tile ready
   uint64_t *cempty = cfull + C::CSTAGES;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cempty + C::CSTAGES);
-  float *spush = reinterpret_cast<float *>(base + C::RING + C::CTRL);
+  float *spush = reinterpret_cast<float *>(base + C::RING + C::CTRL);   // push shares, or ...
+  uint64_t *xch = reinterpret_cast<uint64_t *>(spush);                     // ... the top-16 exchange
+  // the top-16 epilogue needs a whole tile in one CTA: no pushing of rows to
+  // the other CTAs of a cluster (rank 0 pulls every share instead)
+  const bool push = C::PUSH && p.epi != EPI_TOPK;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *bcast = reinterpret_cast<int *>(tmem_slot + 2);
 
@@ -326,7 +388,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (C::PUSH && p.csk > 1) cluster_sync();   // every CTA's barriers exist before any remote arrive
+  if (push && p.csk > 1) cluster_sync();   // every CTA's barriers exist before any remote arrive
 
   // The activations, outputs and stream-K scratch are produced / consumed by
   // the neighbouring kernels of the step: only the weight stream may start
@@ -582,7 +644,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
       bool have_pre = false;
       if (BN == 16 && p.epi == EPI_ADD_F32) {
         const bool whole_t = kb0 == 0 && kb1 == p.kbpt;
-        const bool owner = C::PUSH && p.csk > 1 && ((r + 1) * p.csk - 1) / BM == static_cast<int>(cluster_ctarank());
+        const bool owner = push && p.csk > 1 && ((r + 1) * p.csk - 1) / BM == static_cast<int>(cluster_ctarank());
         if (whole_t || owner) {
           const int rt0 = tile % p.rt_total;
           const int n0 = (rt0 % p.rtpg) * BM + r, t0 = (tile / p.rt_total) * BN;
@@ -605,7 +667,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
       const int rt = tile % p.rt_total;
       const int n = (rt % p.rtpg) * BM + r;                       // row within its group
       const size_t goff = static_cast<size_t>(rt / p.rtpg) * p.out_gstride;
-      const float *wsg = F8 ? p.wscale[rt / p.rtpg] : nullptr;
+      const float *wsg = p.wscale[rt / p.rtpg];   // FP8 codes, or bf16 copies of them
       const int tok0 = (tile / p.rt_total) * BN;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
       float v[16];
@@ -615,12 +677,12 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
           if (have_pre)
             finalize_add_pre(p, v, rpre, n, tok0 + c * 16, goff, wsg);
           else
-            finalize(p, v, n, tok0 + c * 16, goff, wsg);
+            finalize(p, v, n, tok0 + c * 16, goff, wsg, xch);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
-      } else if (C::PUSH && p.csk > 1) {
+      } else if (push && p.csk > 1) {
         // cluster split-K, small token tile: each row's fp32 share goes straight
         // into the shared memory of the CTA that finalises that row (rows
         // [k*BM/csk, (k+1)*BM/csk) belong to rank k); one release arrive per
@@ -681,7 +743,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
           if (have_pre && mine)
             finalize_add_pre(p, v, rpre, n, tok0 + c * 16, goff, wsg);
           else
-            finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsg);   // n >= N: not this CTA's row
+            finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsg, xch);   // n >= N: not this CTA's row
         }
       } else if (p.csk > 1) {
         // cluster split-K: this CTA's fp32 share into its own smem, row-major
@@ -763,7 +825,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
               v[4 * i + 2] = acc[i].z;
               v[4 * i + 3] = acc[i].w;
             }
-            finalize(p, v, n, tok0 + c * 16, goff, wsg);
+            finalize(p, v, n, tok0 + c * 16, goff, wsg, xch);
           }
         }
         epi_bar();
@@ -777,7 +839,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 
-  if (!C::PUSH && p.csk > 1) {
+  if (!push && p.csk > 1) {
     // ---- cluster split-K reduction through distributed shared memory: CTA
     // r finalises tile rows [r*BM/csk, (r+1)*BM/csk) summing the csk shares in
     // rank order (deterministic); lanes hold consecutive rows (coalesced
@@ -786,12 +848,15 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
     if (warp >= 2 && warp < 6) {   // the epilogue warps
       const int et = threadIdx.x - 64;
       const int rank = static_cast<int>(cluster_ctarank());
-      const int r0 = rank * BM / p.csk, rows = (rank + 1) * BM / p.csk - r0;
+      // the top-16 epilogue: rank 0 finalises the whole tile
+      const bool whole = p.epi == EPI_TOPK;
+      const int r0 = whole ? 0 : rank * BM / p.csk;
+      const int rows = whole ? (rank == 0 ? BM : 0) : (rank + 1) * BM / p.csk - r0;
       const int tasks = rows * (BN / 16);
       const int tile = first_tile;
       const int rt = tile % p.rt_total;
       const size_t goff = static_cast<size_t>(rt / p.rtpg) * p.out_gstride;
-      const float *wsg = F8 ? p.wscale[rt / p.rtpg] : nullptr;
+      const float *wsg = p.wscale[rt / p.rtpg];   // FP8 codes, or bf16 copies of them
       const int tokt = (tile / p.rt_total) * BN;
       const float *sp = reinterpret_cast<const float *>(sA);
       for (int t0 = 0; t0 < tasks; t0 += 128) {   // every thread takes each round (shuffles in SwiGLU)
@@ -815,7 +880,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
           }
         }
         const int n = valid ? (rt % p.rtpg) * BM + row : p.N;   // n >= N: nothing stored
-        finalize(p, v, n, tokt + grp * 16, goff, wsg);
+        finalize(p, v, n, tokt + grp * 16, goff, wsg, xch);
       }
     }
     cluster_sync();   // nobody leaves while others still read its share
@@ -1081,7 +1146,7 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
       } else if (kb0 == 0 && kb1 == p.kbpt) {
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
-          finalize(p, v, n, tok0 + c * 16, goff, nullptr);
+          finalize(p, v, n, tok0 + c * 16, goff, p.wscale[g], nullptr);
         }
         release();
       } else {
@@ -1148,7 +1213,7 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
               v[4 * i + 2] = acc[i].z;
               v[4 * i + 3] = acc[i].w;
             }
-            finalize(p, v, n, tok0 + c * 16, goff, nullptr);
+            finalize(p, v, n, tok0 + c * 16, goff, p.wscale[g], nullptr);
           }
         }
         epi_bar();
@@ -1324,13 +1389,16 @@ int launch_pair(const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const 
 
 }  // namespace
 
-int fp8_rows_to_bf16(const Launch &lc, const void *codes, const float *scale, int rows, int cols, void *out) {
-  if (rows <= 0 || cols <= 0 || cols % 4 || !codes || !scale || !out || (reinterpret_cast<uintptr_t>(codes) & 3) ||
+int fp8_rows_to_bf16(const Launch &lc, const void *codes, long long n, void *out) {
+  if (n <= 0 || n % 4 || !codes || !out || (reinterpret_cast<uintptr_t>(codes) & 3) ||
       (reinterpret_cast<uintptr_t>(out) & 7))
-    return set_error(DFLASH_ERR_ARG, "fp8 weights to bf16: cols a positive multiple of 4, buffers aligned");
-  const long long n4 = static_cast<long long>(rows) * (cols / 4);
-  fp8_rows_to_bf16_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, lc.stream>>>(
-      static_cast<const uint32_t *>(codes), scale, cols / 4, n4, static_cast<uint2 *>(out));
+    return set_error(DFLASH_ERR_ARG, "fp8 weights to bf16: a positive multiple of 4 codes, buffers aligned");
+  const long long n4 = n / 4;
+  for (long long o = 0; o < n4; o += (1ll << 30)) {   // grid x stays within range
+    const int cnt = static_cast<int>(n4 - o < (1ll << 30) ? n4 - o : (1ll << 30));
+    e4m3_to_bf16_kernel<<<(cnt + 255) / 256, 256, 0, lc.stream>>>(static_cast<const uint32_t *>(codes) + o, cnt,
+                                                                  static_cast<uint2 *>(out) + o);
+  }
   return cuda_check(cudaGetLastError(), "fp8 weights to bf16 launch");
 }
 
@@ -1405,7 +1473,8 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   const int M = op.M, N = op.N, K = op.K;
   const char *name = op.name;
   if (M <= 0 || N <= 0 || K <= 0) return DFLASH_OK;
-  if ((!op.W && op.n_groups <= 1) || !op.X || !op.out) return set_error(DFLASH_ERR_ARG, "gemm %s: null operand", name);
+  if ((!op.W && op.n_groups <= 1) || !op.X || (!op.out && op.epi != EPI_TOPK))
+    return set_error(DFLASH_ERR_ARG, "gemm %s: null operand", name);
   const uintptr_t al = reinterpret_cast<uintptr_t>(op.W) | reinterpret_cast<uintptr_t>(op.X) |
                        reinterpret_cast<uintptr_t>(op.X_lo);
   const bool f8 = op.w_fp8;
@@ -1445,11 +1514,15 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   p.out2_lo = op.out2_lo;
   p.ldo2 = op.ldo2;
   p.bias = op.bias;
-  if (f8) {
-    for (int g = 0; g < p.n_groups; ++g) {
-      p.wscale[g] = p.n_groups > 1 ? op.wscale_g[g] : op.wscale;
-      if (!p.wscale[g]) return set_error(DFLASH_ERR_ARG, "gemm %s: FP8 weights without row scales", name);
-    }
+  p.cand = op.cand;
+  p.cand_ld = op.cand_ld;
+  if (epi == EPI_TOPK && (!op.cand || op.cand_ld < (N + BM - 1) / BM || n_groups != 1))
+    return set_error(DFLASH_ERR_ARG, "gemm %s: top-16 epilogue needs candidates for every tile", name);
+  // row scales: always with FP8 codes; with bf16 weights when given (the
+  // exact bf16 copies of FP8 codes keep their scales)
+  for (int g = 0; g < p.n_groups; ++g) {
+    p.wscale[g] = p.n_groups > 1 ? op.wscale_g[g] : op.wscale;
+    if (f8 && !p.wscale[g]) return set_error(DFLASH_ERR_ARG, "gemm %s: FP8 weights without row scales", name);
   }
   p.partials = sc.partials;
   p.counters = sc.counters;
@@ -1460,7 +1533,8 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   // Tensor-bound 256-token tiles (bf16 weights and activations, no cluster
   // split-K): CTA pairs with the 2-SM MMA.  gemm_ctas < 0 (test hook) forces
   // -gemm_ctas pairs.
-  const bool pairs = !f8 && !split && BN == 256 && (lc.gemm_ctas < 0 || (lc.gemm_pairs && lc.gemm_ctas == 0)) &&
+  const bool pairs = !f8 && !split && BN == 256 && epi != EPI_TOPK &&
+                     (lc.gemm_ctas < 0 || (lc.gemm_pairs && lc.gemm_ctas == 0)) &&
                      (p.n_groups == 1 || p.rtpg % 2 == 0);
   if (pairs) {
     p.csk = 1;
@@ -1502,7 +1576,9 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
     tXl = tX;
   }
   const double xb = (split ? 4.0 : 2.0) * M * K;
-  const double out_bytes = (epi == EPI_F32 || epi == EPI_TANH_BIAS) ? 4.0 * M * N
+  // top-16 epilogue: 16 keys per token per 128-row tile (+ logits if asked)
+  const double out_bytes = epi == EPI_TOPK ? 128.0 * M * ((N + BM - 1) / BM) + (op.out ? 4.0 * M * N : 0.0)
+                           : (epi == EPI_F32 || epi == EPI_TANH_BIAS) ? 4.0 * M * N
                            : epi == EPI_ADD_F32                      ? 8.0 * M * N
                            : epi == EPI_F32_SPLIT                    ? 8.0 * M * N
                            : epi == EPI_SWIGLU                       ? (op.out_lo ? 2.0 : 1.0) * M * N

@@ -20,7 +20,12 @@ enum Epi : int {
   EPI_SWIGLU = 3,     // rows 2i / 2i+1 = gate_i / up_i: out[m][i] = silu(gate) * up (+ out_lo)
   EPI_TANH_BIAS = 4,  // out (fp32)  = tanh(acc + bias[n])   (conv coefficients)
   EPI_STORE_T = 5,    // out (activation dtype) = acc (+ out_lo on the bf16 path)
-  EPI_F32_SPLIT = 6   // out (fp32) = acc, out2 / out2_lo = bf16 hi / lo halves of acc
+  EPI_F32_SPLIT = 6,  // out (fp32) = acc, out2 / out2_lo = bf16 hi / lo halves of acc
+  // LM head with its top-16 selection: the 16 largest (value, id) keys of
+  // each token over each 128-row vocabulary tile -> cand[token][tile][16]
+  // (64-bit keys, value descending, id ascending); out (fp32 logits) too
+  // when given
+  EPI_TOPK = 7
 };
 
 // One projection.  Activations may come as two bf16 tensors X (high half)
@@ -40,6 +45,8 @@ struct GemmOp {
   void *out2 = nullptr, *out2_lo = nullptr;
   int ldo2 = 0;
   const float *bias = nullptr;
+  uint64_t *cand = nullptr;   // EPI_TOPK: [M][cand_ld][16] keys
+  int cand_ld = 0;            // EPI_TOPK: vocabulary tiles per token row
   const char *name = "gemm";
   // grouped launch: n_groups weight matrices Wg[g] of the same shape applied
   // to the same activations, output g at out + g * out_gstride elements
@@ -101,8 +108,8 @@ int cuda_check(cudaError_t e, const char *what);
 int e4m3_to_bf16(const Launch &lc, const void *codes, int n, void *out);
 // 2-CTA clusters of the pair GEMM resident at once on the current device (< 0: error).
 int gemm_pair_clusters();
-// bf16 copy of an E4M3 weight matrix with fp32 row scales.
-int fp8_rows_to_bf16(const Launch &lc, const void *codes, const float *scale, int rows, int cols, void *out);
+// Exact bf16 values of n E4M3 weight codes (the row scales stay apart).
+int fp8_rows_to_bf16(const Launch &lc, const void *codes, long long n, void *out);
 
 // TMA descriptor of a row-major 2-D tensor [rows][cols] (128-byte swizzle
 // unless told otherwise); box = box_cols x box_rows.
@@ -188,6 +195,10 @@ int verify_rejection(const Launch &lc, const float *target_logits, int V, float 
                      int J, int32_t *accept, int32_t *bonus, int32_t *committed);
 int topk16(const Launch &lc, const float *logits, int rows, int V, int32_t *ids, float *vals,
            uint64_t *part_keys, int *counters, int max_chunks);
+// The top-16 of each row from the LM head's per-tile candidates (EPI_TOPK):
+// cand [rows][tiles][16] keys -> ids / vals [rows][16].
+int topk16_merge(const Launch &lc, const uint64_t *cand, int rows, int tiles, int32_t *ids, float *vals,
+                 uint64_t *part_keys, int *counters, int max_chunks);
 int pair_scores(const Launch &lc, bool f32, const int32_t *anchor, const int32_t *topk_ids,
                 const float *topk_logits, const void *final_hidden, int B, int J, int H, const void *e256,
                 const void *sel_a, const void *sel_b, int r, int E, const float *w_g, float b_g, float *scores);

@@ -23,17 +23,6 @@ namespace {
 constexpr int K = 16;
 constexpr int WARPS = 8;
 
-__device__ __forceinline__ uint64_t make_key(float v, int id) {
-  uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);   // -0 and +0 compare equal
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(id));
-}
-__device__ __forceinline__ float key_value(uint64_t k) {
-  uint32_t u = static_cast<uint32_t>(k >> 32);
-  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
-  return __uint_as_float(u);
-}
-__device__ __forceinline__ int key_id(uint64_t k) { return static_cast<int>(~static_cast<uint32_t>(k)); }
 
 // Warp-wide sorted list in lanes 0..15 (descending).  Insert key k (uniform).
 __device__ __forceinline__ void insert(uint64_t &list, uint64_t k, int lane) {
@@ -67,6 +56,62 @@ __device__ __forceinline__ float warp_16th_largest(float v, int lane) {
     }
   }
   return __shfl_sync(0xffffffffu, v, K - 1);
+}
+
+// The end of a row's selection: this CTA's warp lists merged in shared
+// memory; a row cut into chunks leaves its chunk's 16 keys in `part` and the
+// CTA that completes the row last (per-row counter, self-resetting) merges
+// the chunk lists.  Every warp list alone has 16 keys >= its 16th, so the
+// merged 16th is at least the largest of those and smaller keys are never
+// offered (the same floor between chunks).
+__device__ __forceinline__ void finish_row(uint64_t list, uint64_t *sm, int &last, int row, int c, int nchunks,
+                                           int32_t *ids, float *vals, uint64_t *part, int *counters) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane < K) sm[warp * K + lane] = list;
+  __syncthreads();
+  if (warp == 0) {
+    uint64_t l2 = 0, t2 = 0, floor2 = 0;
+    for (int w = 0; w < WARPS; ++w) floor2 = sm[w * K + K - 1] > floor2 ? sm[w * K + K - 1] : floor2;
+    for (int i = lane; i < WARPS * K; i += 32) offer(l2, t2, sm[i] >= floor2 ? sm[i] : 0, lane);
+    if (nchunks == 1) {
+      if (lane < K) {
+        ids[row * K + lane] = key_id(l2);
+        vals[row * K + lane] = key_value(l2);
+      }
+    } else {
+      if (lane < K) __stcg(&part[(static_cast<size_t>(row) * nchunks + c) * K + lane], l2);
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) {
+        const int old = atomicAdd(&counters[row], 1);
+        last = (old == nchunks - 1);
+        if (last) counters[row] = 0;
+        __threadfence();
+      }
+      __syncwarp();
+      if (last) {
+        const uint64_t *pr = part + static_cast<size_t>(row) * nchunks * K;
+        uint64_t l3 = 0, t3 = 0, floor3 = 0;
+        for (int c2 = lane; c2 < nchunks; c2 += 32) {   // the largest 16th key of the chunk lists
+          const uint64_t k16 = __ldcg(&pr[c2 * K + K - 1]);
+          floor3 = k16 > floor3 ? k16 : floor3;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const uint64_t t = __shfl_xor_sync(0xffffffffu, floor3, o);
+          floor3 = t > floor3 ? t : floor3;
+        }
+        for (int i = lane; i < nchunks * K; i += 32) {
+          const uint64_t k = __ldcg(&pr[i]);
+          offer(l3, t3, k >= floor3 ? k : 0, lane);
+        }
+        if (lane < K) {
+          ids[row * K + lane] = key_id(l3);
+          vals[row * K + lane] = key_value(l3);
+        }
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(WARPS * 32) topk_kernel(const float *__restrict__ logits, int V, int chunk,
@@ -123,53 +168,40 @@ __global__ void __launch_bounds__(WARPS * 32) topk_kernel(const float *__restric
       offer(list, thr, in ? make_key(__ldcs(x + base), base) : 0, lane);
     }
   }
-  if (lane < K) sm[warp * K + lane] = list;
-  __syncthreads();
-  if (warp == 0) {
-    // every warp list alone has 16 keys >= its 16th: the merged 16th is at
-    // least the largest of those, and smaller keys need not be offered
-    uint64_t l2 = 0, t2 = 0, floor2 = 0;
-    for (int w = 0; w < WARPS; ++w) floor2 = sm[w * K + K - 1] > floor2 ? sm[w * K + K - 1] : floor2;
-    for (int i = lane; i < WARPS * K; i += 32) offer(l2, t2, sm[i] >= floor2 ? sm[i] : 0, lane);
-    if (nchunks == 1) {
-      if (lane < K) {
-        ids[row * K + lane] = key_id(l2);
-        vals[row * K + lane] = key_value(l2);
-      }
-    } else {
-      if (lane < K) __stcg(&part[(static_cast<size_t>(row) * nchunks + c) * K + lane], l2);
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) {
-        const int old = atomicAdd(&counters[row], 1);
-        last = (old == nchunks - 1);
-        if (last) counters[row] = 0;
-        __threadfence();
-      }
-      __syncwarp();
-      if (last) {
-        const uint64_t *pr = part + static_cast<size_t>(row) * nchunks * K;
-        uint64_t l3 = 0, t3 = 0, floor3 = 0;
-        for (int c2 = lane; c2 < nchunks; c2 += 32) {   // the largest 16th key of the chunk lists
-          const uint64_t k16 = __ldcg(&pr[c2 * K + K - 1]);
-          floor3 = k16 > floor3 ? k16 : floor3;
-        }
+  finish_row(list, sm, last, row, c, nchunks, ids, vals, part, counters);
+}
+
+// The LM head's top-16 epilogue leaves, per row, 16 sorted keys of every
+// 128-row vocabulary tile; the row's top-16 is the top-16 of those keys
+// (every key of the row's true top-16 is among its tile's 16 largest).
+// Same chunking and merge as topk_kernel, over keys instead of logits, read
+// as 16-byte pairs with U loads per lane in flight.
+__global__ void __launch_bounds__(WARPS * 32) topk_merge_kernel(const uint64_t *__restrict__ cand, int n_keys,
+                                                                int chunk, int nchunks, int32_t *ids, float *vals,
+                                                                uint64_t *part, int *counters) {
+  pdl_start();
+  __shared__ uint64_t sm[WARPS * K];
+  __shared__ int last;
+  const int row = blockIdx.y, c = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t *x = cand + static_cast<size_t>(row) * n_keys;
+  const int lo = c * chunk, hi = min(n_keys, lo + chunk);   // chunk and n_keys are even
+  uint64_t list = 0, thr = 0;
+  constexpr int U = 4;
+  for (int wb = lo + warp * 64; wb < hi; wb += WARPS * 64 * U) {   // warp-uniform trip count
+    ulonglong2 v[U];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const uint64_t t = __shfl_xor_sync(0xffffffffu, floor3, o);
-          floor3 = t > floor3 ? t : floor3;
-        }
-        for (int i = lane; i < nchunks * K; i += 32) {
-          const uint64_t k = __ldcg(&pr[i]);
-          offer(l3, t3, k >= floor3 ? k : 0, lane);
-        }
-        if (lane < K) {
-          ids[row * K + lane] = key_id(l3);
-          vals[row * K + lane] = key_value(l3);
-        }
-      }
+    for (int u = 0; u < U; ++u) {
+      const int base = wb + u * WARPS * 64 + lane * 2;
+      v[u] = base < hi ? __ldcs(reinterpret_cast<const ulonglong2 *>(x + base)) : make_ulonglong2(0ull, 0ull);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      offer(list, thr, v[u].x, lane);
+      offer(list, thr, v[u].y, lane);
     }
   }
+  finish_row(list, sm, last, row, c, nchunks, ids, vals, part, counters);
 }
 
 }  // namespace
@@ -191,6 +223,28 @@ int topk16(const Launch &lc, const float *logits, int rows, int V, int32_t *ids,
   ProfScope ps(lc, "topk16", 4.0 * rows * V, 0.0);
   launch_pdl(topk_kernel, dim3(grid), dim3(WARPS * 32), 0, lc.stream, logits, V, chunk, nch, ids, vals, part_keys, counters);
   return cuda_check(cudaGetLastError(), "topk launch");
+}
+
+int topk16_merge(const Launch &lc, const uint64_t *cand, int rows, int tiles, int32_t *ids, float *vals,
+                 uint64_t *part_keys, int *counters, int max_chunks) {
+  if (rows <= 0) return DFLASH_OK;
+  if (tiles <= 0 || (reinterpret_cast<uintptr_t>(cand) & 15))
+    return set_error(DFLASH_ERR_ARG, "top-16 merge: candidates missing or misaligned");
+  const int n_keys = tiles * K;
+  // enough CTAs to cover the SMs twice, chunks of at least 2048 keys
+  int nch = (2 * lc.num_sms + rows - 1) / rows;
+  nch = nch > max_chunks ? max_chunks : nch;
+  const int maxc = (n_keys + 2047) / 2048;
+  nch = nch > maxc ? maxc : nch;
+  nch = nch < 1 ? 1 : nch;
+  int chunk = (n_keys + nch - 1) / nch;
+  chunk = (chunk + 63) & ~63;
+  nch = (n_keys + chunk - 1) / chunk;
+  dim3 grid(nch, rows);
+  ProfScope ps(lc, "topk16_merge", 8.0 * rows * n_keys, 0.0);
+  launch_pdl(topk_merge_kernel, dim3(grid), dim3(WARPS * 32), 0, lc.stream, cand, n_keys, chunk, nch, ids, vals,
+             part_keys, counters);
+  return cuda_check(cudaGetLastError(), "top-16 merge launch");
 }
 
 // ---------------------------------------------------------------------------

@@ -58,14 +58,15 @@ CONV_SITES = ("pre_attn", "post_attn", "pre_ffn", "post_ffn")
 
 
 def fp8_bf16_copies(dw: dict) -> None:
-    """bf16 copies of every packed FP8 matrix (the library converts codes x
-    row scales on the device), stored beside them under *_bf16: the drafter
-    uses them for its tensor-bound launches (128+ tokens per launch)."""
+    """bf16 copies of every packed FP8 matrix (the codes' exact values, made by
+    the library on the device; the row scales stay in s_*), stored beside them
+    under *_bf16: the drafter uses them for its tensor-bound launches (128+
+    tokens per launch)."""
     torch = _torch()
 
     def conv(codes, scale):
         out = torch.empty(codes.shape, dtype=torch.bfloat16, device=codes.device)
-        B.dflash_fp8_weights_to_bf16(codes, scale, codes.shape[0], codes.shape[1], out)
+        B.dflash_fp8_weights_to_bf16(codes, codes.shape[0], codes.shape[1], out)
         return out
 
     dw["w_fc_bf16"] = conv(dw["w_fc"], dw["s_fc"])

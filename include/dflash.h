@@ -138,11 +138,12 @@ typedef struct dflash_layer_weights {
   const float *s_gu;     /* [2F], interleaved like w_gu                       */
   const float *s_down;   /* [H]                                               */
   const float *s_conv[4];/* [H/8], interleaved like w_conv                   */
-  /* weight_fp8 only, optional: bf16 copies of the matrices above in the
-   * bf16 layout (e.g. from dflash_fp8_weights_to_bf16).  When given, a
-   * projection whose token tile is 128 tokens or more (tensor-bound: 128+
-   * tokens per launch) uses the copy; smaller launches, bound by the weight
-   * stream, use the E4M3 codes.  NULL: codes everywhere. */
+  /* weight_fp8 only, optional: the codes' exact bf16 values
+   * (dflash_fp8_weights_to_bf16), same layout, scaled by the same s_* rows.
+   * When given, a projection whose token tile is 128 tokens or more
+   * (tensor-bound: 128+ tokens per launch) uses the copy; smaller launches,
+   * bound by the weight stream, use the E4M3 codes.  NULL: codes everywhere.
+   * The results are the same either way up to fp32 summation order. */
   const void *w_qkv_bf16;
   const void *w_o_bf16;
   const void *w_gu_bf16;
@@ -317,6 +318,17 @@ DFLASH_API int dflash_set_gemm_ctas(dflash_ctx *ctx, int ctas);
  * the default): a switch for comparing the two; results are identical up to
  * fp32 summation order.  Host-only. */
 DFLASH_API int dflash_set_gemm_pairs(dflash_ctx *ctx, int on);
+/* bf16 drafters: the LM head selects the top-16 inside its GEMM epilogue
+ * (on = 1: per 128-row vocabulary tile the 16 largest keys of each mask row,
+ * then one merge; the fp32 logits are written only when dflash_draft_block
+ * is given a logits buffer) or writes the fp32 logits and runs the
+ * standalone top-16 over them (on = 0, the default: measured faster on
+ * GB300 at every batch size this library was benchmarked on).  On applies
+ * only where the LM head is bound by its weight stream (at most 32 mask rows
+ * per call); larger calls always take the logits path.  The same top-16
+ * either way.  Host-only. */
+DFLASH_API int dflash_set_fused_topk(dflash_ctx *ctx, int on);
+
 /* Test hook: 2-CTA clusters of the pair GEMM that fit on the current device
  * at once (from the occupancy calculator), or a negative error code. */
 DFLASH_API int dflash_debug_gemm_pair_clusters(void);
@@ -381,14 +393,13 @@ DFLASH_API int dflash_debug_gemm_plan(int M, int N, int K, int n_groups, int w_f
                                       int per_sm, int num_sms, int gemm_ctas, long long *plan);
 
 /* bf16 copy of an FP8 weight matrix ("Draft quantization", [DF2] engine
- * table): out[n][k] = bf16(scale[n] * e4m3(codes[n][k])), the E4M3 value
- * decoded exactly and scaled in fp32, rounded once to bf16 (nearest even).
- * For the optional *_bf16 fields of dflash_weights / dflash_layer_weights,
- * made once at set-up.  codes: device uint8 [rows][cols], cols a multiple of
- * 4; scale: device fp32 [rows]; out: device bf16 [rows][cols].  Asynchronous
- * on `stream`. */
-DFLASH_API int dflash_fp8_weights_to_bf16(const void *codes, const float *scale, int rows, int cols, void *out,
-                                          dflash_stream_t stream);
+ * table): out[n][k] = e4m3(codes[n][k]), every code's value exactly (bf16
+ * holds all of them); the row scales stay in the s_* pointers, which the
+ * projections apply to the copies as to the codes.  For the optional *_bf16
+ * fields of dflash_weights / dflash_layer_weights, made once at set-up.
+ * codes: device uint8 [rows][cols], cols a multiple of 4; out: device bf16
+ * [rows][cols].  Asynchronous on `stream`. */
+DFLASH_API int dflash_fp8_weights_to_bf16(const void *codes, int rows, int cols, void *out, dflash_stream_t stream);
 
 /* Test hook: the FP8 GEMM's own E4M3 -> bf16 weight conversion (the device
  * function its converter warps run) applied to n codes.
