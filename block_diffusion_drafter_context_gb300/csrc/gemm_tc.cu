@@ -17,7 +17,10 @@
 //     k-block) iteration space is cut into one contiguous range per CTA, and
 //     a tile split across CTAs is finished by whichever CTA completes it last
 //     (per-tile counter), which sums the fp32 partials in CTA order -
-//     deterministic, no spin-waits;
+//     deterministic, no spin-waits.  Its own share it takes from TMEM, the
+//     others (on its last segment, when the ring is idle) by bulk copy into
+//     the ring; shares are stored transposed (share_f4) so that every warp
+//     access is 512 contiguous bytes;
 //   * tile order: token tile outer, weight row tile inner (tile = tok * RT +
 //     rt).  With several token tiles the CTAs that own the same weight rows
 //     for different token tiles sit G / tok_tiles apart and advance in step,
@@ -64,6 +67,15 @@ struct WMaps {
 
 constexpr int pow2_at_least(int x) { return x <= 32 ? 32 : 2 * pow2_at_least((x + 1) / 2); }
 
+// The most fp32 share rows one CTA of a push-mode split-K cluster receives:
+// max over widths s = 2..16 of (s - 1) * ceil(128 / s).
+constexpr int max_push_rows(int s = 2) {
+  return s > 16 ? 0
+                : ((s - 1) * ((128 + s - 1) / s) > max_push_rows(s + 1) ? (s - 1) * ((128 + s - 1) / s)
+                                                                        : max_push_rows(s + 1));
+}
+static_assert(max_push_rows() == 130, "push-mode share rows");
+
 template <int BN, bool SPLIT, bool F8>
 struct Cfg {
   // warps: 0 TMA, 1 MMA, 2-5 epilogue, (F8) 6-9 weight converters
@@ -81,9 +93,10 @@ struct Cfg {
   static constexpr int A_TCOLS = BKI / 2;              // TMEM columns of one (two bf16 per column)
   static constexpr int A_COL = 2 * BN < 32 ? 32 : 2 * BN;   // first of them, after the accumulators
   // cluster split-K with small token tiles pushes each row's fp32 share into
-  // the owning CTA: at most (csk - 1) * ceil(128 / csk) <= 120 rows arrive
+  // the owning CTA: at most (csk - 1) * ceil(128 / csk) rows arrive, 130 for
+  // some cluster width up to 16 (14 CTAs)
   static constexpr bool PUSH = BN <= 32;
-  static constexpr int PUSH_BYTES = PUSH ? 120 * BN * 4 : 0;
+  static constexpr int PUSH_BYTES = PUSH ? max_push_rows() * BN * 4 : 0;
   // the top-16 epilogue's exchange (4 warps x 16 tokens x 16 keys); it never
   // runs with the push path, so the two share one region
   static constexpr int XCH_BYTES = 4 * 16 * 16 * 8;
@@ -102,7 +115,7 @@ struct Cfg {
   static constexpr int TMEM_COLS = F8 ? pow2_at_least(A_COL + CSTAGES * A_TCOLS) : (2 * BN < 32 ? 32 : 2 * BN);
   static constexpr int RING = STAGES * STAGE_BYTES;
   static constexpr int SMEM = 1024 + RING + CTRL + XREG;
-  static_assert((2 * STAGES + 2 * CSTAGES + 6) * 8 + 12 <= CTRL, "GEMM control block overflows");
+  static_assert((2 * STAGES + 2 * CSTAGES + 7) * 8 + 12 <= CTRL, "GEMM control block overflows");
   static_assert(RING >= BM * BN * 4, "the ring must hold one fp32 tile (cluster split-K share)");
   static_assert(!F8 || BN > 32 || 2 * (SMEM + 1024) <= SMEM_PER_SM, "two F8 CTAs must fit on one SM");
   // (two CTAs per SM only for small token tiles: the others take over 113 KB of shared memory)
@@ -129,7 +142,9 @@ struct Params {
   uint64_t *cand;           // EPI_TOPK: [M][cand_ld][16]
   int cand_ld;
   const float *wscale[MAX_GROUPS];   // F8: per-row weight scales of each group
-  float *partials;     // [G][2][BM][BN] row-major shares
+  // [G][2] fp32 shares of BM x BN tiles, each in the transposed layout of
+  // share_f4() (16-byte aligned: the fixup bulk-copies whole shares)
+  float *partials;
   int *counters;       // [tiles]
   int *status;
   unsigned long long timeout_ns;
@@ -142,6 +157,14 @@ __device__ __forceinline__ long long range_begin(long long total, int G, int c) 
 __device__ __forceinline__ int cta_of(long long i, long long total, int G) {
   return static_cast<int>(((i + 1) * G + total - 1) / total) - 1;
 }
+
+// One fp32 share of a BM x BN tile (stream-K partial, cluster split-K stage)
+// as float4 units [c][i][r]: row r's columns 16c + 4i .. 16c + 4i + 3 sit at
+// float4 index (4c + i) * rows + r.  Lanes hold consecutive rows, so every
+// warp access moves 512 contiguous bytes: coalesced in global memory, free of
+// bank conflicts in shared memory (row-major rows of 1 KB put all 32 lanes of
+// an access on the same banks).
+__device__ __forceinline__ int share_f4(int c, int i, int r, int rows) { return (4 * c + i) * rows + r; }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -345,7 +368,8 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
   uint64_t *rbar = drain + 1;   // cluster split-K (push): shares of the other CTAs have arrived
   uint64_t *cfull = rbar + 1;   // F8: converted weight tile ready
   uint64_t *cempty = cfull + C::CSTAGES;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cempty + C::CSTAGES);
+  uint64_t *fbar = cempty + C::CSTAGES;   // stream-K fixup: other CTAs' shares staged in the ring
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fbar + 1);
   float *spush = reinterpret_cast<float *>(base + C::RING + C::CTRL);   // push shares, or ...
   uint64_t *xch = reinterpret_cast<uint64_t *>(spush);                     // ... the top-16 exchange
   // the top-16 epilogue needs a whole tile in one CTA: no pushing of rows to
@@ -371,6 +395,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
     mbar_init(&tempty[1], 4);
     mbar_init(drain, 1);
     mbar_init(rbar, p.csk > 1 ? p.csk - 1 : 1);
+    mbar_init(fbar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -701,12 +726,16 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
         if (o != rank) {
+          // slot of this CTA in the owner's push area: one share of o_rows
+          // rows in the share_f4 layout (lanes on consecutive rows)
           const int slot = rank < o ? rank : rank - 1;
-          const uint32_t a = dsmem_addr(spush + (static_cast<size_t>(slot) * o_rows + (r - o_r0)) * BN,
+          const uint32_t a = dsmem_addr(reinterpret_cast<float4 *>(spush) + static_cast<size_t>(slot) * (BN / 4) * o_rows +
+                                            (r - o_r0),
                                         static_cast<uint32_t>(o));
 #pragma unroll
           for (int j = 0; j < BN / 4; ++j)
-            st_dsmem_f4(a + 16 * j, make_float4(own[4 * j], own[4 * j + 1], own[4 * j + 2], own[4 * j + 3]));
+            st_dsmem_f4(a + 16u * static_cast<uint32_t>(j * o_rows),
+                        make_float4(own[4 * j], own[4 * j + 1], own[4 * j + 2], own[4 * j + 3]));
         }
         fence_acq_rel_cluster();
         epi_bar();   // every push of this CTA is issued and fenced
@@ -728,11 +757,10 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
               for (int i = 0; i < 16; ++i) v[i] += own[c * 16 + i];
             } else if (mine) {
               const int slot = k < rank ? k : k - 1;
-              const float4 *src = reinterpret_cast<const float4 *>(
-                  spush + (static_cast<size_t>(slot) * my_rows + (r - my_r0)) * BN + c * 16);
+              const float4 *src = reinterpret_cast<const float4 *>(spush) + static_cast<size_t>(slot) * (BN / 4) * my_rows;
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const float4 x = src[i];
+                const float4 x = src[share_f4(c, i, r - my_r0, my_rows)];
                 v[4 * i] += x.x;
                 v[4 * i + 1] += x.y;
                 v[4 * i + 2] += x.z;
@@ -746,34 +774,34 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
             finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsg, xch);   // n >= N: not this CTA's row
         }
       } else if (p.csk > 1) {
-        // cluster split-K: this CTA's fp32 share into its own smem, row-major
-        // (the ring is idle: every stage has been consumed); the cluster
-        // reduces it on chip after the main loop
-        float *sp = reinterpret_cast<float *>(sA) + static_cast<size_t>(r) * BN;
+        // cluster split-K: this CTA's fp32 share into its own smem in the
+        // share_f4 layout (the ring is idle: every stage has been consumed);
+        // the cluster reduces it on chip after the main loop
+        float4 *s4 = reinterpret_cast<float4 *>(base);
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
-          float4 *s4 = reinterpret_cast<float4 *>(sp + c * 16);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) s4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          for (int i = 0; i < 4; ++i)
+            s4[share_f4(c, i, r, BM)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
       } else {
-        // partial tile: this CTA's fp32 share goes to its slot, row-major
-        // (each thread writes its row's BN columns as float4); the CTA that
-        // completes the tile's k-range sums all shares in CTA order
+        // partial tile: this CTA's fp32 share goes to its slot in the
+        // share_f4 layout; the CTA that completes the tile's k-range sums all
+        // shares in CTA order (deterministic), its own straight from tensor
+        // memory (the accumulator is released only after the fixup)
+        constexpr int SHARE = BM * BN;   // floats
         const int slot = (tile == first_tile) ? 0 : 1;
-        float *P = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * (BM * BN) + static_cast<size_t>(r) * BN;
+        float4 *P4 = reinterpret_cast<float4 *>(p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * SHARE);
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
-          float4 *P4 = reinterpret_cast<float4 *>(P + c * 16);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) __stcg(P4 + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+          for (int i = 0; i < 4; ++i)
+            __stcg(P4 + share_f4(c, i, r, BM), make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
+        fence_proxy_async_global();   // the completing CTA may bulk-copy these shares
         epi_bar();   // every share of this CTA is written ...
         if (et == 0) {
           __threadfence();   // ... and, through the barrier, visible before the count moves
@@ -793,30 +821,64 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
           const int c_hi = cta_of(t_beg + p.kbpt - 1, p.total, p.G);
           // only the first contributor can have started in an earlier tile
           const int slot_lo = range_begin(p.total, p.G, c_lo) < t_beg ? 1 : 0;
+          auto share_of = [&](int cc) -> const float4 * {
+            return reinterpret_cast<const float4 *>(p.partials +
+                                                    (static_cast<size_t>(cc) * 2 + (cc == c_lo ? slot_lo : 0)) * SHARE);
+          };
+          // On this CTA's last segment no copy is in flight and every ring
+          // stage has been consumed: the other contributors' shares (as many
+          // as the ring holds, in CTA order) arrive there by bulk copy, one
+          // L2 round trip for all of them; the rest are read from L2 directly.
+          const int others = c_hi - c_lo;
+          const int staged = (it + (kb1 - kb0) == end) ? (others < C::RING / (SHARE * 4) ? others : C::RING / (SHARE * 4))
+                                                       : 0;
+          if (staged > 0) {
+            if (et == 0) {
+              fence_proxy_async_global();   // after the acquiring atomic: the copies read the published shares
+              mbar_arrive_expect_tx(fbar, static_cast<uint32_t>(staged) * SHARE * 4);
+              for (int cc = c_lo, k = 0; k < staged; ++cc) {
+                if (cc == static_cast<int>(blockIdx.x)) continue;
+                bulk_load(base + static_cast<size_t>(k) * SHARE * 4, share_of(cc), SHARE * 4, fbar);
+                ++k;
+              }
+            }
+            const bool got_sh = mbar_wait(fbar, 0, abort_flag, p.timeout_ns);
+            if (bar_or(1, 128, !got_sh || *abort_flag)) {
+              if (et == 0) report(p.status, DFLASH_ERR_TIMEOUT);
+              *abort_flag = 1;
+              // the copies still land in the ring: wait for them (bounded) before the CTA exits
+              if (et == 0) mbar_wait(fbar, 0, nullptr, p.timeout_ns);
+              break;
+            }
+          }
+          const float4 *ring4 = reinterpret_cast<const float4 *>(base);
           for (int c = 0; c < BN / 16; ++c) {
             float4 acc[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int cc0 = c_lo; cc0 <= c_hi; cc0 += 4) {
-              float4 t[4][4];
+            int k = 0;   // staged shares met so far
+            for (int cc = c_lo; cc <= c_hi; ++cc) {   // summed in contributor order: deterministic
+              float4 t[4];
+              if (cc == static_cast<int>(blockIdx.x)) {
+                tmem_ld16(taddr + c * 16, v);
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {   // up to 4 contributors' loads in flight
-                const int cc = cc0 + u;
-                const float4 *Q4 = reinterpret_cast<const float4 *>(
-                    p.partials + (static_cast<size_t>(cc) * 2 + (cc == c_lo ? slot_lo : 0)) * (BM * BN) +
-                    static_cast<size_t>(r) * BN + c * 16);
+                for (int i = 0; i < 4; ++i) t[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+              } else if (k < staged) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) t[u][i] = cc <= c_hi ? __ldcg(Q4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int i = 0; i < 4; ++i) t[i] = ring4[static_cast<size_t>(k) * (SHARE / 4) + share_f4(c, i, r, BM)];
+                ++k;
+              } else {
+                const float4 *Q4 = share_of(cc);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) t[i] = __ldcg(Q4 + share_f4(c, i, r, BM));
               }
 #pragma unroll
-              for (int u = 0; u < 4; ++u)   // summed in contributor order: deterministic
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  acc[i].x += t[u][i].x;
-                  acc[i].y += t[u][i].y;
-                  acc[i].z += t[u][i].z;
-                  acc[i].w += t[u][i].w;
-                }
+              for (int i = 0; i < 4; ++i) {
+                acc[i].x += t[i].x;
+                acc[i].y += t[i].y;
+                acc[i].z += t[i].z;
+                acc[i].w += t[i].w;
+              }
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -828,6 +890,9 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
             finalize(p, v, n, tok0 + c * 16, goff, wsg, xch);
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
         epi_bar();
       }
       it += kb1 - kb0;
@@ -858,7 +923,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
       const size_t goff = static_cast<size_t>(rt / p.rtpg) * p.out_gstride;
       const float *wsg = p.wscale[rt / p.rtpg];   // FP8 codes, or bf16 copies of them
       const int tokt = (tile / p.rt_total) * BN;
-      const float *sp = reinterpret_cast<const float *>(sA);
+      const float4 *s4 = reinterpret_cast<const float4 *>(base);   // every CTA's share, share_f4 layout
       for (int t0 = 0; t0 < tasks; t0 += 128) {   // every thread takes each round (shuffles in SwiGLU)
         const int task = t0 + et;
         const bool valid = task < tasks;
@@ -868,10 +933,10 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
         for (int i = 0; i < 16; ++i) v[i] = 0.f;
         if (valid) {
           for (int k = 0; k < p.csk; ++k) {
-            const uint32_t a = dsmem_addr(sp + static_cast<size_t>(row) * BN + grp * 16, static_cast<uint32_t>(k));
+            const uint32_t a = dsmem_addr(s4 + share_f4(grp, 0, row, BM), static_cast<uint32_t>(k));
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float4 x = ld_dsmem_f4(a + 16 * i);
+              const float4 x = ld_dsmem_f4(a + 16u * static_cast<uint32_t>(i * BM));
               v[4 * i] += x.x;
               v[4 * i + 1] += x.y;
               v[4 * i + 2] += x.z;
@@ -1155,12 +1220,12 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
         // shares in pair order
         const int tile_h = pt * 2 + rank;
         const int slot = (pt == first_pt) ? 0 : 1;
-        float *P = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * (BM * BN) + static_cast<size_t>(r) * BN;
+        float4 *P4 = reinterpret_cast<float4 *>(p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * (BM * BN));
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
-          float4 *P4 = reinterpret_cast<float4 *>(P + c * 16);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) __stcg(P4 + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+          for (int i = 0; i < 4; ++i)
+            __stcg(P4 + share_f4(c, i, r, BM), make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
         }
         release();
         epi_bar();
@@ -1191,10 +1256,10 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
               for (int u = 0; u < 4; ++u) {
                 const int cc = cc0 + u;
                 const float4 *Q4 = reinterpret_cast<const float4 *>(
-                    p.partials + (static_cast<size_t>(2 * cc + rank) * 2 + (cc == c_lo ? slot_lo : 0)) * (BM * BN) +
-                    static_cast<size_t>(r) * BN + c * 16);
+                    p.partials + (static_cast<size_t>(2 * cc + rank) * 2 + (cc == c_lo ? slot_lo : 0)) * (BM * BN));
 #pragma unroll
-                for (int i = 0; i < 4; ++i) t[u][i] = cc <= c_hi ? __ldcg(Q4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int i = 0; i < 4; ++i)
+                  t[u][i] = cc <= c_hi ? __ldcg(Q4 + share_f4(c, i, r, BM)) : make_float4(0.f, 0.f, 0.f, 0.f);
               }
 #pragma unroll
               for (int u = 0; u < 4; ++u)
@@ -1239,6 +1304,10 @@ int setup_device(int dev) {
   if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, SPLIT, F8>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
                          "gemm smem attribute"))
+    return e;
+  if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, SPLIT, F8>,
+                                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+                         "gemm cluster-size attribute"))   // cluster split-K up to 16 CTAs
     return e;
   if (BN <= 32)   // small tiles: two CTAs per SM need the whole array as shared memory
     if (int e = cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, SPLIT, F8>,
@@ -1454,9 +1523,14 @@ GemmPlan gemm_plan(int M, int N, int K, int n_groups, bool f8, bool split, bool 
   pl.csk = 1;
   if (gemm_ctas == 0 && pl.tiles * 2 <= cap) {
     // at most 8 CTAs, and about 8 k-blocks or more each (short ranges are
-    // all pipeline fill; at least 2-way where the k-range allows)
-    long long s = std::min<long long>(std::min<long long>(8, cap / pl.tiles),
-                                      std::min<long long>(pl.kbpt, std::max<long long>(2, pl.kbpt / 8)));
+    // all pipeline fill; at least 2-way where the k-range allows); a GEMM of
+    // a handful of tiles (at most a sixteenth of the slots: the DFlash-2
+    // conv coefficients, 4 tiles) takes clusters of up to 16 CTAs (the
+    // non-portable size) at 4 or more k-blocks each, so that it still spreads
+    // over some 64 SMs
+    const bool wide = pl.tiles * 16 <= cap;
+    long long s = std::min<long long>(std::min<long long>(wide ? 16 : 8, cap / pl.tiles),
+                                      std::min<long long>(pl.kbpt, std::max<long long>(2, pl.kbpt / (wide ? 4 : 8))));
     // SwiGLU pairs rows 2i / 2i+1 in neighbouring lanes: row ranges must be
     // even-aligned, so a power-of-two cluster there
     if (swiglu)
@@ -1530,6 +1604,8 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   p.timeout_ns = lc.timeout_ns;
   if (tiles > sc.n_counters || static_cast<size_t>(p.G) * 2 * BM * BN > sc.partial_floats)
     return set_error(DFLASH_ERR_SHAPE, "gemm %s: workspace too small for %lld tiles", name, tiles);
+  if (reinterpret_cast<uintptr_t>(sc.partials) & 15)
+    return set_error(DFLASH_ERR_ALIGN, "gemm %s: partial scratch must be 16-byte aligned", name);
   // Tensor-bound 256-token tiles (bf16 weights and activations, no cluster
   // split-K): CTA pairs with the 2-SM MMA.  gemm_ctas < 0 (test hook) forces
   // -gemm_ctas pairs.
