@@ -19,7 +19,7 @@
 //     (per-tile counter), which sums the fp32 partials in CTA order -
 //     deterministic, no spin-waits.  Its own share it takes from TMEM, the
 //     others (on its last segment, when the ring is idle) by bulk copy into
-//     the ring; shares are stored transposed (share_f4) so that every warp
+//     the ring; shares are stored transposed (tile_f4) so that every warp
 //     access is 512 contiguous bytes;
 //   * tile order: token tile outer, weight row tile inner (tile = tok * RT +
 //     rt).  With several token tiles the CTAs that own the same weight rows
@@ -51,6 +51,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstring>
 
 namespace dflash {
 namespace {
@@ -63,6 +64,11 @@ constexpr int SMEM_PER_SM = 228 * 1024;   // shared memory of one SM (1 KB of it
 
 struct WMaps {
   CUtensorMap m[MAX_GROUPS];
+};
+// Output tensors for the bulk-store epilogue (Params::tma_out): the output
+// and, for bf16 outputs split into high and low halves, the low halves.
+struct OMaps {
+  CUtensorMap o, olo;
 };
 
 constexpr int pow2_at_least(int x) { return x <= 32 ? 32 : 2 * pow2_at_least((x + 1) / 2); }
@@ -100,7 +106,12 @@ struct Cfg {
   // the top-16 epilogue's exchange (4 warps x 16 tokens x 16 keys); it never
   // runs with the push path, so the two share one region
   static constexpr int XCH_BYTES = 4 * 16 * 16 * 8;
-  static constexpr int XREG = PUSH_BYTES > XCH_BYTES ? PUSH_BYTES : XCH_BYTES;
+  // the bulk-store epilogue (token tiles of 64+): per epilogue warp two 2 KB
+  // buffers of 16 tokens x 32 rows (fp32, or bf16 high + low halves)
+  static constexpr int OSTG_WARP = 4096;
+  static constexpr int OSTG_BYTES = BN >= 64 ? 4 * OSTG_WARP : 0;
+  static constexpr int XREG0 = PUSH_BYTES > XCH_BYTES ? PUSH_BYTES : XCH_BYTES;
+  static constexpr int XREG = XREG0 > OSTG_BYTES ? XREG0 : OSTG_BYTES;
   static constexpr int CTRL = 512;                     // mbarriers and flags
   // Small token tiles (weight streaming): ~100 KB of ring, so two GEMM CTAs
   // fit on one SM and, under programmatic dependent launch, the next GEMM's
@@ -133,6 +144,10 @@ struct Params {
   int G;               // CTAs
   int csk;             // >1: cluster split-K, csk CTAs (one cluster) per tile
   int epi;
+  // 1: outputs leave through bulk tensor stores (reduce-add for EPI_ADD_F32)
+  // staged per epilogue warp; token tiles of 64+, one group, the plain
+  // epilogues (F32, ADD_F32, TANH_BIAS, BF16, SWIGLU)
+  int tma_out;
   void *out;
   int ldo;
   void *out_lo;        // low bf16 halves of a bf16 output, or null
@@ -143,7 +158,7 @@ struct Params {
   int cand_ld;
   const float *wscale[MAX_GROUPS];   // F8: per-row weight scales of each group
   // [G][2] fp32 shares of BM x BN tiles, each in the transposed layout of
-  // share_f4() (16-byte aligned: the fixup bulk-copies whole shares)
+  // tile_f4() (16-byte aligned: the fixup bulk-copies whole shares)
   float *partials;
   int *counters;       // [tiles]
   int *status;
@@ -158,13 +173,18 @@ __device__ __forceinline__ int cta_of(long long i, long long total, int G) {
   return static_cast<int>(((i + 1) * G + total - 1) / total) - 1;
 }
 
-// One fp32 share of a BM x BN tile (stream-K partial, cluster split-K stage)
-// as float4 units [c][i][r]: row r's columns 16c + 4i .. 16c + 4i + 3 sit at
-// float4 index (4c + i) * rows + r.  Lanes hold consecutive rows, so every
-// warp access moves 512 contiguous bytes: coalesced in global memory, free of
-// bank conflicts in shared memory (row-major rows of 1 KB put all 32 lanes of
-// an access on the same banks).
+// One fp32 share of `rows` rows x BN columns (the rows a CTA of a cluster
+// split-K pushes to another) as float4 units [c][i][r]: row r's columns
+// 16c + 4i .. 16c + 4i + 3 sit at float4 index (4c + i) * rows + r.  Lanes
+// hold consecutive rows, so every warp access moves 512 contiguous bytes:
+// coalesced in global memory, free of bank conflicts in shared memory
+// (row-major rows of 1 KB put all 32 lanes of an access on the same banks).
 __device__ __forceinline__ int share_f4(int c, int i, int r, int rows) { return (4 * c + i) * rows + r; }
+// A whole BM-row share (stream-K partial, cluster split-K stage) orders the
+// same units [c][warp][i][lane]: each epilogue warp's part of a 16-column
+// group (rows 32w .. 32w + 31) is one contiguous 2 KB run, which the
+// bulk-store epilogue reuses as that warp's staging buffer once read.
+__device__ __forceinline__ int tile_f4(int c, int i, int r) { return ((c * 4 + (r >> 5)) * 4 + i) * 32 + (r & 31); }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -309,6 +329,84 @@ __device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n,
   }
 }
 
+// finalize() through the bulk-store epilogue: the 16 token columns of this
+// warp's 32 weight rows (row n = first row + lane) go to the warp's staging
+// slice as [token][row] (conflict-free: lanes write consecutive words), and
+// lane 0 writes them with one tiled bulk store, or reduce-add for the
+// residual epilogue (out += v, rounded as the plain path's r + v; every
+// output element has one finishing CTA).  b: the warp's 2 KB staging buffer
+// for this chunk, free to overwrite (the caller has waited for any earlier
+// store from it and for the warp's reads of it); lane 0 commits one bulk
+// group per chunk.  The same arithmetic as finalize(): identical results.
+__device__ __forceinline__ void finalize_tma(const Params &p, const OMaps &om, float (&v)[16], int n, int tok0,
+                                             const float *ws, uint8_t *b, int lane) {
+  const bool nok = n < p.N;
+  if (ws) {
+    const float sc = nok ? ws[n] : 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] *= sc;
+  }
+  const int row0 = n - lane;                      // the warp's first weight row
+  const bool live = row0 < p.N && tok0 < p.M;     // anything of the box inside the output
+  switch (p.epi) {
+    case EPI_BF16: {
+      __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(b), *l = h + 16 * 32;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const __nv_bfloat16 hv = f2bf(v[i]);
+        h[i * 32 + lane] = hv;
+        l[i * 32 + lane] = f2bf(v[i] - bf2f(hv));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && live) {
+        tma_store_2d(&om.o, h, row0, tok0);
+        if (p.out_lo) tma_store_2d(&om.olo, l, row0, tok0);
+      }
+    } break;
+    case EPI_SWIGLU: {
+      // rows 2j / 2j + 1 (neighbouring lanes) give output column j
+      __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(b), *l = h + 16 * 16;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float up = __shfl_xor_sync(0xffffffffu, v[i], 1);
+        if (!(lane & 1)) {
+          const float o = silu(v[i]) * up;
+          const __nv_bfloat16 hv = f2bf(o);
+          h[i * 16 + (lane >> 1)] = hv;
+          l[i * 16 + (lane >> 1)] = f2bf(o - bf2f(hv));
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && live) {
+        tma_store_2d(&om.o, h, row0 >> 1, tok0);
+        if (p.out_lo) tma_store_2d(&om.olo, l, row0 >> 1, tok0);
+      }
+    } break;
+    default: {   // EPI_F32, EPI_ADD_F32, EPI_TANH_BIAS
+      float *f = reinterpret_cast<float *>(b);
+      if (p.epi == EPI_TANH_BIAS) {
+        const float bb = nok ? p.bias[n] : 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i * 32 + lane] = tanhf(v[i] + bb);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i * 32 + lane] = v[i];
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && live) {
+        if (p.epi == EPI_ADD_F32)
+          tma_reduce_add_2d(&om.o, f, row0, tok0);
+        else
+          tma_store_2d(&om.o, f, row0, tok0);
+      }
+    } break;
+  }
+  if (lane == 0) bulk_commit();
+}
+
 // Four E4M3 codes -> four bf16 values, exact.  The code's bits, moved into
 // bf16 fields (sign to bit 15, exponent and mantissa to bits 4..10), encode
 // code * 2^-120 for every code (normal, subnormal, zero: bf16's exponent
@@ -350,7 +448,7 @@ __global__ void e4m3_to_bf16_kernel(const uint32_t *codes, int n4, uint2 *out) {
 template <int BN, bool SPLIT, bool F8>
 __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 : 1)
     gemm_tc_kernel(const __grid_constant__ WMaps wm, const __grid_constant__ CUtensorMap tmX,
-                   const __grid_constant__ CUtensorMap tmXlo, const Params p) {
+                   const __grid_constant__ CUtensorMap tmXlo, const __grid_constant__ OMaps om, const Params p) {
   using C = Cfg<BN, SPLIT, F8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -403,6 +501,10 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
     for (int g = 0; g < p.n_groups; ++g) tma_prefetch_desc(&wm.m[g]);
     tma_prefetch_desc(&tmX);
     if (SPLIT) tma_prefetch_desc(&tmXlo);
+    if (BN >= 64 && p.tma_out) {
+      tma_prefetch_desc(&om.o);
+      tma_prefetch_desc(&om.olo);
+    }
   }
   grid_dep_launch();   // the next kernel may be scheduled now; it waits for this grid itself
   if (warp == 1) {
@@ -654,6 +756,22 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
     const int q = warp & 3;              // TMEM lane quarter of this warp
     const int r = q * 32 + lane;         // weight row within the tile
     const int et = threadIdx.x - 64;     // 0..127
+    // bulk-store epilogue: this warp's staging slice and chunk count
+    uint8_t *ostg = base + C::RING + C::CTRL + (BN >= 64 ? q * C::OSTG_WARP : 0);
+    uint32_t ocnt = 0;
+    // a chunk's staging buffer from the warp's two alternating ones (after
+    // the store issued from it two chunks earlier has read it); on the CTA's
+    // last segment the idle ring serves instead, one 2 KB run per warp and
+    // chunk, with no waits
+    auto xbuf = [&]() -> uint8_t * {
+      uint8_t *b = ostg + (ocnt & 1u) * 2048;
+      if (ocnt >= 2) {
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+      }
+      ++ocnt;
+      return b;
+    };
     grid_dep_wait();                     // outputs / scratch are shared with the previous kernel
     int seg = 0;
     for (long long it = begin; it < end; ++seg) {
@@ -697,10 +815,13 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
       float v[16];
       if (kb0 == 0 && kb1 == p.kbpt) {
+        const bool ring_out = it + (kb1 - kb0) == end;   // last segment: the ring is idle
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
           if (have_pre)
             finalize_add_pre(p, v, rpre, n, tok0 + c * 16, goff, wsg);
+          else if (BN >= 64 && p.tma_out)
+            finalize_tma(p, om, v, n, tok0 + c * 16, wsg, ring_out ? base + (c * 4 + q) * 2048 : xbuf(), lane);
           else
             finalize(p, v, n, tok0 + c * 16, goff, wsg, xch);
         }
@@ -775,21 +896,21 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
         }
       } else if (p.csk > 1) {
         // cluster split-K: this CTA's fp32 share into its own smem in the
-        // share_f4 layout (the ring is idle: every stage has been consumed);
+        // tile_f4 layout (the ring is idle: every stage has been consumed);
         // the cluster reduces it on chip after the main loop
         float4 *s4 = reinterpret_cast<float4 *>(base);
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            s4[share_f4(c, i, r, BM)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            s4[tile_f4(c, i, r)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
       } else {
         // partial tile: this CTA's fp32 share goes to its slot in the
-        // share_f4 layout; the CTA that completes the tile's k-range sums all
+        // tile_f4 layout; the CTA that completes the tile's k-range sums all
         // shares in CTA order (deterministic), its own straight from tensor
         // memory (the accumulator is released only after the fixup)
         constexpr int SHARE = BM * BN;   // floats
@@ -799,7 +920,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
           tmem_ld16(taddr + c * 16, v);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            __stcg(P4 + share_f4(c, i, r, BM), make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+            __stcg(P4 + tile_f4(c, i, r), make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
         }
         fence_proxy_async_global();   // the completing CTA may bulk-copy these shares
         epi_bar();   // every share of this CTA is written ...
@@ -865,12 +986,12 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
                 for (int i = 0; i < 4; ++i) t[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
               } else if (k < staged) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) t[i] = ring4[static_cast<size_t>(k) * (SHARE / 4) + share_f4(c, i, r, BM)];
+                for (int i = 0; i < 4; ++i) t[i] = ring4[static_cast<size_t>(k) * (SHARE / 4) + tile_f4(c, i, r)];
                 ++k;
               } else {
                 const float4 *Q4 = share_of(cc);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) t[i] = __ldcg(Q4 + share_f4(c, i, r, BM));
+                for (int i = 0; i < 4; ++i) t[i] = __ldcg(Q4 + tile_f4(c, i, r));
               }
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
@@ -887,7 +1008,19 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
               v[4 * i + 2] = acc[i].z;
               v[4 * i + 3] = acc[i].w;
             }
-            finalize(p, v, n, tok0 + c * 16, goff, wsg, xch);
+            if (BN >= 64 && p.tma_out) {
+              // with staged shares the output of this group goes where the
+              // first staged share's run for it lay (read by this warp)
+              uint8_t *b;
+              if (staged > 0) {
+                __syncwarp();
+                b = base + (c * 4 + q) * 2048;
+              } else {
+                b = xbuf();
+              }
+              finalize_tma(p, om, v, n, tok0 + c * 16, wsg, b, lane);
+            } else
+              finalize(p, v, n, tok0 + c * 16, goff, wsg, xch);
           }
         }
         tc_fence_before();
@@ -897,6 +1030,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
       }
       it += kb1 - kb0;
     }
+    if (BN >= 64 && p.tma_out && lane == 0) bulk_wait_read<0>();   // staging read before the CTA may exit
   }
 
   tc_fence_before();
@@ -923,7 +1057,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
       const size_t goff = static_cast<size_t>(rt / p.rtpg) * p.out_gstride;
       const float *wsg = p.wscale[rt / p.rtpg];   // FP8 codes, or bf16 copies of them
       const int tokt = (tile / p.rt_total) * BN;
-      const float4 *s4 = reinterpret_cast<const float4 *>(base);   // every CTA's share, share_f4 layout
+      const float4 *s4 = reinterpret_cast<const float4 *>(base);   // every CTA's share, tile_f4 layout
       for (int t0 = 0; t0 < tasks; t0 += 128) {   // every thread takes each round (shuffles in SwiGLU)
         const int task = t0 + et;
         const bool valid = task < tasks;
@@ -933,10 +1067,10 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
         for (int i = 0; i < 16; ++i) v[i] = 0.f;
         if (valid) {
           for (int k = 0; k < p.csk; ++k) {
-            const uint32_t a = dsmem_addr(s4 + share_f4(grp, 0, row, BM), static_cast<uint32_t>(k));
+            const uint32_t a = dsmem_addr(s4 + tile_f4(grp, 0, row), static_cast<uint32_t>(k));
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float4 x = ld_dsmem_f4(a + 16u * static_cast<uint32_t>(i * BM));
+              const float4 x = ld_dsmem_f4(a + 512u * static_cast<uint32_t>(i));
               v[4 * i] += x.x;
               v[4 * i + 1] += x.y;
               v[4 * i + 2] += x.z;
@@ -1225,7 +1359,7 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
           tmem_ld16(taddr + c * 16, v);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            __stcg(P4 + share_f4(c, i, r, BM), make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+            __stcg(P4 + tile_f4(c, i, r), make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
         }
         release();
         epi_bar();
@@ -1259,7 +1393,7 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
                     p.partials + (static_cast<size_t>(2 * cc + rank) * 2 + (cc == c_lo ? slot_lo : 0)) * (BM * BN));
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                  t[u][i] = cc <= c_hi ? __ldcg(Q4 + share_f4(c, i, r, BM)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  t[u][i] = cc <= c_hi ? __ldcg(Q4 + tile_f4(c, i, r)) : make_float4(0.f, 0.f, 0.f, 0.f);
               }
 #pragma unroll
               for (int u = 0; u < 4; ++u)
@@ -1352,7 +1486,8 @@ int setup() {
 }
 
 template <int BN, bool SPLIT, bool F8>
-int launch(const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const CUtensorMap &tXl, const Params &p) {
+int launch(const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const CUtensorMap &tXl, const OMaps &tO,
+           const Params &p) {
   using C = Cfg<BN, SPLIT, F8>;
   if (int e = setup<BN, SPLIT, F8>(); e < 0) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1369,18 +1504,18 @@ int launch(const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const CUten
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, SPLIT, F8>, tW, tX, tXl, p), "gemm launch");
+  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, SPLIT, F8>, tW, tX, tXl, tO, p), "gemm launch");
 }
 
 template <bool SPLIT, bool F8>
 int launch_bn(int BN, const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const CUtensorMap &tXl,
-              const Params &p) {
+              const OMaps &tO, const Params &p) {
   switch (BN) {
-    case 16: return launch<16, SPLIT, F8>(lc, tW, tX, tXl, p);
-    case 32: return launch<32, SPLIT, F8>(lc, tW, tX, tXl, p);
-    case 64: return launch<64, SPLIT, F8>(lc, tW, tX, tXl, p);
-    case 128: return launch<128, SPLIT, F8>(lc, tW, tX, tXl, p);
-    default: return launch<F8 ? 128 : 256, SPLIT, F8>(lc, tW, tX, tXl, p);   // FP8 tiles stop at 128
+    case 16: return launch<16, SPLIT, F8>(lc, tW, tX, tXl, tO, p);
+    case 32: return launch<32, SPLIT, F8>(lc, tW, tX, tXl, tO, p);
+    case 64: return launch<64, SPLIT, F8>(lc, tW, tX, tXl, tO, p);
+    case 128: return launch<128, SPLIT, F8>(lc, tW, tX, tXl, tO, p);
+    default: return launch<F8 ? 128 : 256, SPLIT, F8>(lc, tW, tX, tXl, tO, p);   // FP8 tiles stop at 128
   }
 }
 
@@ -1651,6 +1786,32 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   } else {
     tXl = tX;
   }
+  // bulk-store epilogue: 256 / 128 / 64-token tiles of one group with a plain
+  // epilogue, outputs (and low halves) 16-byte aligned with 16-byte rows;
+  // box = 16 tokens x one warp's 32 rows (16 output columns for SwiGLU)
+  OMaps tO;
+  std::memset(&tO, 0, sizeof(tO));
+  p.tma_out = 0;
+  if (!pairs && BN >= 64 && p.n_groups == 1 &&
+      (epi == EPI_F32 || epi == EPI_ADD_F32 || epi == EPI_TANH_BIAS || epi == EPI_BF16 || epi == EPI_SWIGLU)) {
+    const bool f32o = epi == EPI_F32 || epi == EPI_ADD_F32 || epi == EPI_TANH_BIAS;
+    const int esz = f32o ? 4 : 2;
+    const uint64_t cols = epi == EPI_SWIGLU ? static_cast<uint64_t>(N / 2) : static_cast<uint64_t>(N);
+    const uintptr_t oal = reinterpret_cast<uintptr_t>(op.out) | reinterpret_cast<uintptr_t>(op.out_lo);
+    if (!(oal & 15) && (static_cast<long long>(op.ldo) * esz) % 16 == 0 && (epi != EPI_SWIGLU || N % 2 == 0)) {
+      const CUtensorMapDataType dt = f32o ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      const uint32_t bx = epi == EPI_SWIGLU ? 16 : 32;
+      const uint64_t stride = static_cast<uint64_t>(op.ldo) * esz;
+      if (int e = make_tmap_2d(&tO.o, op.out, dt, esz, cols, M, stride, bx, 16, CU_TENSOR_MAP_SWIZZLE_NONE)) return e;
+      if (op.out_lo) {
+        if (int e = make_tmap_2d(&tO.olo, op.out_lo, dt, esz, cols, M, stride, bx, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+          return e;
+      } else {
+        tO.olo = tO.o;
+      }
+      p.tma_out = 1;
+    }
+  }
   const double xb = (split ? 4.0 : 2.0) * M * K;
   // top-16 epilogue: 16 keys per token per 128-row tile (+ logits if asked)
   const double out_bytes = epi == EPI_TOPK ? 128.0 * M * ((N + BM - 1) / BM) + (op.out ? 4.0 * M * N : 0.0)
@@ -1663,8 +1824,9 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   ProfScope ps(lc, name, ng * (wbytes * static_cast<double>(N) * K + (f8 ? 4.0 * N : 0.0) + out_bytes) + xb,
                ng * (split ? 4.0 : 2.0) * M * N * K);
   if (pairs) return launch_pair<256>(lc, tW, tX, p);
-  if (f8) return split ? launch_bn<true, true>(BN, lc, tW, tX, tXl, p) : launch_bn<false, true>(BN, lc, tW, tX, tXl, p);
-  return split ? launch_bn<true, false>(BN, lc, tW, tX, tXl, p) : launch_bn<false, false>(BN, lc, tW, tX, tXl, p);
+  if (f8)
+    return split ? launch_bn<true, true>(BN, lc, tW, tX, tXl, tO, p) : launch_bn<false, true>(BN, lc, tW, tX, tXl, tO, p);
+  return split ? launch_bn<true, false>(BN, lc, tW, tX, tXl, tO, p) : launch_bn<false, false>(BN, lc, tW, tX, tXl, tO, p);
 }
 
 }  // namespace dflash
