@@ -11,15 +11,18 @@
 // the 16 block keys per (request, kv head).  One CTA per SM takes an equal
 // contiguous run of that list, so ragged batches stay balanced and a CTA's
 // pipeline never drains between requests.  Per CTA:
-//   warp 0     TMA: K and V^T pages into a 5-deep smem ring (128-byte swizzle;
+//   warp 0     TMA: K and V^T pages into a 6-deep smem ring (128-byte swizzle;
 //              V pages are stored transposed so both products take K-major
 //              operands); the 16g query rows of each new (request, kv head);
 //   warp 1     tcgen05.mma: S = Q K^T (M=128, N=64, K=128) into one of two
 //              TMEM buffers; O += P V (M=128, N=128, K = the chunk's valid
-//              tokens rounded up to 16) into a TMEM accumulator;
+//              tokens rounded up to 16) into a TMEM accumulator, with P, the
+//              A operand, read from TMEM;
 //   warps 2-5  one TMEM lane (= query row) per thread: online softmax in the
-//              exp2 domain on its 64 scores, P written back to smem in bf16
-//              as the A operand of PV.  O stays in TMEM; it is rescaled only
+//              exp2 domain on its 64 scores, P written back to TMEM in bf16
+//              (no shared memory: that room holds a sixth ring stage, which
+//              the chunk's load-to-PV lifetime of ~7 500 cycles needs to keep
+//              HBM busy).  O stays in TMEM; it is rescaled only
 //              when a row's running max grows by more than 2^8 (the exp2
 //              values stay below 256 in between, exact in fp32 sums).
 // A (request, kv head) whose chunks all fall in one CTA is normalised and
@@ -37,19 +40,19 @@ namespace {
 
 constexpr int CH = 64;                       // tokens per chunk (= one KV page)
 constexpr int HD = 128;                      // head dim of the bf16 path
-constexpr int ST = 5;                        // KV ring depth
+constexpr int ST = 6;                        // KV ring depth
 constexpr int BLK = 16;                      // query rows per head in the tile (block size S <= 16 of them real)
 constexpr int MROWS = 128;                   // UMMA M (query rows, padded)
 constexpr int Q_BYTES = MROWS * HD * 2;      // 32 KB: two 64-dim halves of [128][64]
 constexpr int K_BYTES = CH * HD * 2;         // 16 KB: two halves of [64 tok][64]
 constexpr int V_BYTES = HD * CH * 2;         // 16 KB: [128 d][64 tok]
-constexpr int P_BYTES = MROWS * CH * 2;      // 16 KB: [128 rows][64 tok]
 constexpr int CTRL_BYTES = 256;              // mbarriers, TMEM address, schedule
-constexpr int SMEM = 1024 + Q_BYTES + ST * (K_BYTES + V_BYTES) + 2 * P_BYTES + CTRL_BYTES;
+constexpr int SMEM = 1024 + Q_BYTES + ST * (K_BYTES + V_BYTES) + CTRL_BYTES;
 constexpr int NTHR = 224;                    // producer, QK issuer, 4 softmax warps, PV issuer
 constexpr int NSB = 3;                       // S buffers in TMEM: QK runs two chunks ahead
-constexpr int TMEM_COLS = 512;               // S x 3 (64 columns each), O (128 columns) at 256
+constexpr int TMEM_COLS = 512;               // S x 3 (64 columns each), O (128 columns) at 256, P x 2 at 384
 constexpr uint32_t O_COL = 256;
+constexpr uint32_t P_COL = 384;              // P buffers: 32 columns each (64 bf16 tokens per row)
 constexpr float RESCALE_LOG2 = 8.f;
 constexpr int DEFAULT_MIN_CHUNKS = 4;        // fewer CTAs than SMs when the whole list is short
 static_assert(SMEM <= 232448, "attention smem over the per-block limit");
@@ -238,8 +241,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   uint8_t *sQ = base;
   uint8_t *sK = sQ + Q_BYTES;
   uint8_t *sV = sK + ST * K_BYTES;
-  uint8_t *sP = sV + ST * V_BYTES;
-  uint64_t *bar = reinterpret_cast<uint64_t *>(sP + 2 * P_BYTES);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sV + ST * V_BYTES);
   uint64_t *qfull = bar, *qempty = bar + 1, *full = bar + 2, *empty = full + ST, *sfull = empty + ST,
            *sempty = sfull + NSB, *pfull = sempty + NSB, *pdone = pfull + 2, *oempty = pdone + 2,
            *mready = oempty + 1, *mdone = mready + 1, *drain = mdone + 1;
@@ -274,16 +276,14 @@ __global__ void __launch_bounds__(NTHR, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // A rows past R (query padding) and the P rows no lane writes are never
-  // touched by TMA or the softmax: zero them once so everything stays finite
+  // A rows past R (query padding) are never touched by TMA: zero them once
+  // so everything stays finite
   {
     const int per_half = (MROWS - R) * 128 / 16;   // 16-byte chunks
     for (int i = threadIdx.x; i < 2 * per_half; i += NTHR) {
       const int half = i / per_half, k = i % per_half;
       *reinterpret_cast<uint4 *>(sQ + half * (MROWS * 128) + R * 128 + k * 16) = make_uint4(0, 0, 0, 0);
     }
-    for (int i = threadIdx.x; i < 2 * P_BYTES / 16; i += NTHR)
-      reinterpret_cast<uint4 *>(sP)[i] = make_uint4(0, 0, 0, 0);
   }
   fence_proxy_async_smem();
   if (warp == 1) {
@@ -294,6 +294,16 @@ __global__ void __launch_bounds__(NTHR, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (warp >= 2 && warp <= 5) {
+    // P rows no softmax lane writes (quadrants without query rows) enter the
+    // PV products too: zero both P buffers of this warp's quadrant once
+    const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    const uint32_t pz = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + P_COL;
+#pragma unroll
+    for (int c = 0; c < 64; c += 16) tmem_st16_nw(pz + c, z);
+    tmem_wait_st();
+    tc_fence_before();
+  }
 
   pdl_start();
   // ---------------------------------------------------------------- schedule
@@ -496,12 +506,12 @@ __global__ void __launch_bounds__(NTHR, 1)
               mbar_wait(oempty, static_cast<uint32_t>((seg_p - 1) & 1), abort_flag, p.timeout_ns));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t p0 = smem_u32(sP + pb * P_BYTES), v0 = smem_u32(sV + st * V_BYTES);
+        const uint32_t pt = tmem + P_COL + static_cast<uint32_t>(pb * 32), v0 = smem_u32(sV + st * V_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < CH / 16; ++kk)
+        for (int kk = 0; kk < CH / 16; ++kk)   // A = P from TMEM: 16 tokens = 8 columns per k-step
           if (kk < ksteps)
-            umma_bf16(tmem + O_COL, sdesc_k_sw128(p0 + kk * 32), sdesc_k_sw128(v0 + kk * 32), idesc_pv,
-                      (kk > 0 || !first) ? 1u : 0u);
+            umma_bf16_ts(tmem + O_COL, pt + static_cast<uint32_t>(kk * 8), sdesc_k_sw128(v0 + kk * 32), idesc_pv,
+                         (kk > 0 || !first) ? 1u : 0u);
         umma_commit(&pdone[pb]);
         umma_commit(&empty[st]);   // PV is the last reader of this KV stage (its QK finished before P existed)
         wp.next(p);
@@ -643,18 +653,38 @@ __global__ void __launch_bounds__(NTHR, 1)
         failed = true;
         break;
       }
-      uint8_t *prow = sP + (i & 1) * P_BYTES + lrow * 128;   // 128-byte swizzled K-major rows
+      tc_fence_after();
+      // P in bf16 into this lane's row of P buffer i & 1: column j holds
+      // tokens 2j (low half) and 2j + 1, the A layout of the PV product
+      {
+        uint32_t pw[32];
+        if constexpr (DUP) {
+          // each lane of a pair holds half the row: trade halves with the
+          // partner (lane ^ 16) so both write the whole row (lanes 16-31
+          // into the duplicate rows, whose O nobody reads)
 #pragma unroll
-      for (int kk = 0; kk < NC / 8; ++kk) {
-        const int k = hi * (NC / 8) + kk;
-        uint4 u;
-        u.x = pack_bf16(x[8 * kk + 0], x[8 * kk + 1]);
-        u.y = pack_bf16(x[8 * kk + 2], x[8 * kk + 3]);
-        u.z = pack_bf16(x[8 * kk + 4], x[8 * kk + 5]);
-        u.w = pack_bf16(x[8 * kk + 6], x[8 * kk + 7]);
-        *reinterpret_cast<uint4 *>(prow + ((k ^ (lrow & 7)) << 4)) = u;
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t mine = pack_bf16(x[2 * j], x[2 * j + 1]);
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 16);
+            pw[j] = hi ? other : mine;
+            pw[16 + j] = hi ? mine : other;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pw[j] = pack_bf16(x[2 * j], x[2 * j + 1]);
+        }
+        const uint32_t pcol = lane_base + P_COL + static_cast<uint32_t>((i & 1) * 32);
+        uint32_t w0[16], w1[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          w0[j] = pw[j];
+          w1[j] = pw[16 + j];
+        }
+        tmem_st16_nw(pcol, w0);
+        tmem_st16_nw(pcol + 16, w1);
+        tmem_wait_st();
       }
-      fence_proxy_async_smem();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&pfull[i & 1]);
 
