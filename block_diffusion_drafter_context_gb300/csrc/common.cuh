@@ -152,6 +152,16 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *src, uint3
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// Bulk copy of bytes (a multiple of 16, 16-byte aligned) from this CTA's
+// shared memory into another CTA's of the cluster (dst and its mbarrier as
+// shared::cluster addresses), completing there as transaction bytes.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void *src, uint32_t bytes,
+                                                  uint32_t mbar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(smem_u32(src)), "r"(bytes), "r"(mbar_cluster)
+               : "memory");
+}
 // Tiled bulk store of a 2-D box from this CTA's shared memory to the tensor
 // (x, the innermost coordinate, times the element size a multiple of 16
 // bytes; x, y >= 0; parts of the box past the tensor's extent are not

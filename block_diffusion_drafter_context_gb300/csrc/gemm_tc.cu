@@ -126,7 +126,7 @@ struct Cfg {
   static constexpr int TMEM_COLS = F8 ? pow2_at_least(A_COL + CSTAGES * A_TCOLS) : (2 * BN < 32 ? 32 : 2 * BN);
   static constexpr int RING = STAGES * STAGE_BYTES;
   static constexpr int SMEM = 1024 + RING + CTRL + XREG;
-  static_assert((2 * STAGES + 2 * CSTAGES + 7) * 8 + 12 <= CTRL, "GEMM control block overflows");
+  static_assert((2 * STAGES + 2 * CSTAGES + 8) * 8 + 12 <= CTRL, "GEMM control block overflows");
   static_assert(RING >= BM * BN * 4, "the ring must hold one fp32 tile (cluster split-K share)");
   static_assert(!F8 || BN > 32 || 2 * (SMEM + 1024) <= SMEM_PER_SM, "two F8 CTAs must fit on one SM");
   // (two CTAs per SM only for small token tiles: the others take over 113 KB of shared memory)
@@ -467,12 +467,26 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
   uint64_t *cfull = rbar + 1;   // F8: converted weight tile ready
   uint64_t *cempty = cfull + C::CSTAGES;
   uint64_t *fbar = cempty + C::CSTAGES;   // stream-K fixup: other CTAs' shares staged in the ring
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fbar + 1);
+  uint64_t *xbar = fbar + 1;              // cluster split-K exchange: the other ranks' rows have arrived
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xbar + 1);
   float *spush = reinterpret_cast<float *>(base + C::RING + C::CTRL);   // push shares, or ...
   uint64_t *xch = reinterpret_cast<uint64_t *>(spush);                     // ... the top-16 exchange
   // the top-16 epilogue needs a whole tile in one CTA: no pushing of rows to
   // the other CTAs of a cluster (rank 0 pulls every share instead)
   const bool push = C::PUSH && p.epi != EPI_TOPK;
+  // Cluster split-K over two CTAs with 64+-token tiles: exchange by bulk
+  // copies.  Each CTA stages the rows the other finalises (share_f4 layout
+  // per owner block) and one thread sends the block with one cp.async.bulk;
+  // the owner sums in rank order, its own rows straight from TMEM, and
+  // writes them with the bulk-store epilogue.  Wider clusters pull every
+  // share through distributed shared memory instead: there the finalising
+  // rows of a rank (42 or fewer) would leave most epilogue lanes idle, which
+  // measured slower than the pull's spread over all four warps (so does the
+  // top-16 epilogue, whose rank 0 takes the whole tile).  The staging plus
+  // the receive slot must fit the idle ring.
+  const int x_rows = (BM + p.csk - 1) / p.csk;   // most rows any rank owns
+  const bool xchg = !C::PUSH && p.csk == 2 && p.epi != EPI_TOPK &&
+                    static_cast<long long>(BM + (p.csk - 1) * x_rows) * BN * 4 <= C::RING;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *bcast = reinterpret_cast<int *>(tmem_slot + 2);
 
@@ -494,6 +508,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
     mbar_init(drain, 1);
     mbar_init(rbar, p.csk > 1 ? p.csk - 1 : 1);
     mbar_init(fbar, 1);
+    mbar_init(xbar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -894,6 +909,25 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
           else
             finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsg, xch);   // n >= N: not this CTA's row
         }
+      } else if (xchg) {
+        // cluster split-K, exchange: the rows of other owners go to the
+        // staging blocks in the idle ring (owner o's block at row o_r0, its
+        // rows in the share_f4 layout); this CTA's own rows stay in TMEM
+        const int S = p.csk, rank = static_cast<int>(cluster_ctarank());
+        const int o = ((r + 1) * S - 1) / BM;   // the rank that owns row r
+        const bool send = o != rank;
+        const int o_r0 = o * BM / S, o_rows = (o + 1) * BM / S - o_r0;
+        float4 *blk = reinterpret_cast<float4 *>(base) + static_cast<size_t>(o_r0) * (BN / 4);
+        for (int c = 0; c < BN / 16; ++c) {
+          tmem_ld16(taddr + c * 16, v);   // warp-collective: every lane loads
+          if (send)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              blk[share_f4(c, i, r - o_r0, o_rows)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+        fence_proxy_async_smem();   // the bulk copies read the staging through the async proxy
+        tc_fence_before();
+        __syncwarp();
       } else if (p.csk > 1) {
         // cluster split-K: this CTA's fp32 share into its own smem in the
         // tile_f4 layout (the ring is idle: every stage has been consumed);
@@ -1033,12 +1067,90 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
     if (BN >= 64 && p.tma_out && lane == 0) bulk_wait_read<0>();   // staging read before the CTA may exit
   }
 
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (xchg) {
+    // ---- cluster split-K exchange (see xchg above): receive slots armed,
+    // every CTA's staging written and its ring idle, then one thread sends
+    // each owner its block; owners sum in rank order
+    const int S = p.csk, rank = static_cast<int>(cluster_ctarank());
+    const int my_r0 = rank * BM / S, my_rows = (rank + 1) * BM / S - my_r0;
+    const uint32_t recv = static_cast<uint32_t>(BM * BN * 4);   // receive slots after the staging
+    if (threadIdx.x == 64) mbar_arrive_expect_tx(xbar, static_cast<uint32_t>((S - 1) * my_rows * BN * 4));
+    cluster_sync();
+    if (threadIdx.x == 64) {
+      for (int o = 0; o < S; ++o) {
+        if (o == rank) continue;
+        const int o_r0 = o * BM / S, o_rows = (o + 1) * BM / S - o_r0;
+        const int slot = rank < o ? rank : rank - 1;   // this sender's slot at the owner
+        const uint32_t bytes = static_cast<uint32_t>(o_rows * BN * 4);
+        bulk_copy_to_peer(dsmem_addr(base + recv + static_cast<uint32_t>(slot) * bytes, static_cast<uint32_t>(o)),
+                          base + static_cast<size_t>(o_r0) * BN * 4, bytes, dsmem_addr(xbar, static_cast<uint32_t>(o)));
+      }
+    }
+    const int q = warp & 3;
+    // the epilogue warps whose TMEM lanes hold this CTA's rows finalise them
+    if (warp >= 2 && warp < 6 && q * 32 < my_r0 + my_rows && q * 32 + 32 > my_r0) {
+      const int r = q * 32 + lane;
+      const bool mine = r >= my_r0 && r < my_r0 + my_rows;
+      const bool got = mbar_wait(xbar, 0, abort_flag, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) report(p.status, DFLASH_ERR_TIMEOUT);
+        *abort_flag = 1;
+      } else {
+        tc_fence_after();
+        const int tile = first_tile;
+        const int rt = tile % p.rt_total;
+        const size_t goff = static_cast<size_t>(rt / p.rtpg) * p.out_gstride;
+        const float *wsg = p.wscale[rt / p.rtpg];   // FP8 codes, or bf16 copies of them
+        const int tokt = (tile / p.rt_total) * BN;
+        const int n = mine ? (rt % p.rtpg) * BM + r : p.N;   // n >= N: nothing stored
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);   // the one segment: buffer 0
+        const float4 *rv = reinterpret_cast<const float4 *>(base + recv);
+        const int rr = mine ? r - my_r0 : 0;
+        // whole warps of rows: the bulk-store epilogue (two buffers per warp)
+        const bool tma_w = BN >= 64 && p.tma_out && my_rows % 32 == 0 && my_r0 % 32 == 0;
+        uint8_t *ostg = base + C::RING + C::CTRL + (BN >= 64 ? q * C::OSTG_WARP : 0);
+        uint32_t ocnt = 0;
+        for (int c = 0; c < BN / 16; ++c) {
+          float v[16], w[16];
+          tmem_ld16(taddr + c * 16, w);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          for (int k = 0; k < S; ++k) {   // rank order: deterministic
+            if (k == rank) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] += w[i];
+            } else {
+              const int slot = k < rank ? k : k - 1;
+              const float4 *src = rv + static_cast<size_t>(slot) * my_rows * (BN / 4);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float4 x = src[share_f4(c, i, rr, my_rows)];
+                v[4 * i] += x.x;
+                v[4 * i + 1] += x.y;
+                v[4 * i + 2] += x.z;
+                v[4 * i + 3] += x.w;
+              }
+            }
+          }
+          if (tma_w) {
+            uint8_t *b = ostg + (ocnt & 1u) * 2048;
+            if (ocnt >= 2) {
+              if (lane == 0) bulk_wait_read<1>();
+              __syncwarp();
+            }
+            ++ocnt;
+            finalize_tma(p, om, v, n, tokt + c * 16, wsg, b, lane);
+          } else {
+            finalize(p, v, n, tokt + c * 16, goff, wsg, xch);
+          }
+        }
+        if (tma_w && lane == 0) bulk_wait_read<0>();
+      }
+    }
+    cluster_sync();   // every copy has landed (its owner waited) before a sender's smem goes away
+  }
 
-  if (!push && p.csk > 1) {
+  if (!xchg && !push && p.csk > 1) {
     // ---- cluster split-K reduction through distributed shared memory: CTA
     // r finalises tile rows [r*BM/csk, (r+1)*BM/csk) summing the csk shares in
     // rank order (deterministic); lanes hold consecutive rows (coalesced
@@ -1066,16 +1178,28 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = 0.f;
         if (valid) {
-          for (int k = 0; k < p.csk; ++k) {
-            const uint32_t a = dsmem_addr(s4 + tile_f4(grp, 0, row), static_cast<uint32_t>(k));
+          // KB ranks' loads in flight at once (one where registers are
+          // scarce: the small-tile variants), then summed in rank order
+          constexpr int KB = C::PUSH ? 1 : 4;
+          for (int k0 = 0; k0 < p.csk; k0 += KB) {
+            float4 xs[KB][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float4 x = ld_dsmem_f4(a + 512u * static_cast<uint32_t>(i));
-              v[4 * i] += x.x;
-              v[4 * i + 1] += x.y;
-              v[4 * i + 2] += x.z;
-              v[4 * i + 3] += x.w;
-            }
+            for (int u = 0; u < KB; ++u)
+              if (k0 + u < p.csk) {
+                const uint32_t a = dsmem_addr(s4 + tile_f4(grp, 0, row), static_cast<uint32_t>(k0 + u));
+#pragma unroll
+                for (int i = 0; i < 4; ++i) xs[u][i] = ld_dsmem_f4(a + 512u * static_cast<uint32_t>(i));
+              }
+#pragma unroll
+            for (int u = 0; u < KB; ++u)
+              if (k0 + u < p.csk)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  v[4 * i] += xs[u][i].x;
+                  v[4 * i + 1] += xs[u][i].y;
+                  v[4 * i + 2] += xs[u][i].z;
+                  v[4 * i + 3] += xs[u][i].w;
+                }
           }
         }
         const int n = valid ? (rt % p.rtpg) * BM + row : p.N;   // n >= N: nothing stored
@@ -1084,6 +1208,11 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
     }
     cluster_sync();   // nobody leaves while others still read its share
   }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 // ------------------------------------------------------------------ CTA pairs

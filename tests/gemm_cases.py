@@ -17,4 +17,7 @@ GEMM_EXACT_CASES = [
     # pair's phantom half), four token tiles, a 512-token projection
     (300, 768, 1024, -1, False), (300, 768, 1024, -5, False), (257, 896, 512, -3, False),
     (1024, 1152, 640, 0, False), (512, 4096, 4096, 0, False),
+    # cluster split-K exchange with uneven row ranges (3 CTAs: 42 / 43 / 43
+    # rows) and with 16 CTAs of 8 rows (a four-tile GEMM)
+    (128, 6144, 4096, 0, False), (128, 512, 4096, 0, False),
 ]
