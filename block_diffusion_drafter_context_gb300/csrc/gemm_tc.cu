@@ -188,7 +188,22 @@ __device__ __forceinline__ int tile_f4(int c, int i, int r) { return ((c * 4 + (
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+// silu with the fast exponential and division (relative error ~1e-7,
+// far below the bf16 rounding of the output)
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// SwiGLU of one lane pair's 16 token columns (rows 2j = gate and 2j + 1 = up
+// sit in neighbouring lanes): one shuffle per output, the transcendental
+// work split evenly - the even lane returns tokens 0..7, the odd lane tokens
+// 8..15 (o[j] is token j + 8 * odd).  Every lane of the warp calls it.
+__device__ __forceinline__ void swiglu_pair(const float (&v)[16], bool odd, float (&o)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float p = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[8 + j], 1);
+    const float g = odd ? p : v[j], u = odd ? v[8 + j] : p;
+    o[j] = silu(g) * u;
+  }
+}
 
 __device__ __forceinline__ void store_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t i, float v) {
   const __nv_bfloat16 h = f2bf(v);
@@ -299,12 +314,15 @@ __device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n,
         if (nok && tok0 + i < p.M) o[goff + static_cast<size_t>(tok0 + i) * p.ldo + n] = r[i] + v[i];
     } break;
     case EPI_SWIGLU: {
+      // lane parity = row parity in every caller (pairs share an owner)
       __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out), *ol = static_cast<__nv_bfloat16 *>(p.out_lo);
+      const bool odd = threadIdx.x & 1;
+      float sw[8];
+      swiglu_pair(v, odd, sw);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float up = __shfl_xor_sync(0xffffffffu, v[i], 1);
-        if (nok && !(n & 1) && tok0 + i < p.M)
-          store_hl(o, ol, goff + static_cast<size_t>(tok0 + i) * p.ldo + (n >> 1), silu(v[i]) * up);
+      for (int j = 0; j < 8; ++j) {
+        const int i = j + (odd ? 8 : 0);
+        if (nok && tok0 + i < p.M) store_hl(o, ol, goff + static_cast<size_t>(tok0 + i) * p.ldo + (n >> 1), sw[j]);
       }
     } break;
     case EPI_TANH_BIAS: {
@@ -367,15 +385,15 @@ __device__ __forceinline__ void finalize_tma(const Params &p, const OMaps &om, f
     case EPI_SWIGLU: {
       // rows 2j / 2j + 1 (neighbouring lanes) give output column j
       __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(b), *l = h + 16 * 16;
+      const bool odd = lane & 1;
+      float sw[8];
+      swiglu_pair(v, odd, sw);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float up = __shfl_xor_sync(0xffffffffu, v[i], 1);
-        if (!(lane & 1)) {
-          const float o = silu(v[i]) * up;
-          const __nv_bfloat16 hv = f2bf(o);
-          h[i * 16 + (lane >> 1)] = hv;
-          l[i * 16 + (lane >> 1)] = f2bf(o - bf2f(hv));
-        }
+      for (int j = 0; j < 8; ++j) {
+        const int i = j + (odd ? 8 : 0);
+        const __nv_bfloat16 hv = f2bf(sw[j]);
+        h[i * 16 + (lane >> 1)] = hv;
+        l[i * 16 + (lane >> 1)] = f2bf(sw[j] - bf2f(hv));
       }
       fence_proxy_async_smem();
       __syncwarp();
