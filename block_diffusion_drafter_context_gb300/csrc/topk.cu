@@ -152,14 +152,23 @@ __global__ void __launch_bounds__(WARPS * 32) topk_kernel(const float *__restric
           lmax = fmaxf(lmax, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));   // out of range: -inf
         tau = warp_16th_largest(lmax, lane);
       }
+      // Once the list is full, a value below its 16th key's value cannot
+      // enter (keys order by value first): one float compare per element and
+      // one vote per four decide whether any lane builds keys at all.
+      float floor_v = thr == 0 ? -INFINITY : key_value(thr);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int base = wb + u * WARPS * 128 + lane * 4;
         const bool in = base < hi;
-        offer(list, thr, in && v[u].x >= tau ? make_key(v[u].x, base) : 0, lane);
-        offer(list, thr, in && v[u].y >= tau ? make_key(v[u].y, base + 1) : 0, lane);
-        offer(list, thr, in && v[u].z >= tau ? make_key(v[u].z, base + 2) : 0, lane);
-        offer(list, thr, in && v[u].w >= tau ? make_key(v[u].w, base + 3) : 0, lane);
+        const float lo_v = fmaxf(tau, floor_v);
+        const bool cand = in && (v[u].x >= lo_v || v[u].y >= lo_v || v[u].z >= lo_v || v[u].w >= lo_v);
+        if (__any_sync(0xffffffffu, cand)) {
+          offer(list, thr, in && v[u].x >= tau ? make_key(v[u].x, base) : 0, lane);
+          offer(list, thr, in && v[u].y >= tau ? make_key(v[u].y, base + 1) : 0, lane);
+          offer(list, thr, in && v[u].z >= tau ? make_key(v[u].z, base + 2) : 0, lane);
+          offer(list, thr, in && v[u].w >= tau ? make_key(v[u].w, base + 3) : 0, lane);
+          floor_v = thr == 0 ? -INFINITY : key_value(thr);
+        }
       }
     }
   } else {
