@@ -492,18 +492,16 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
   // the top-16 epilogue needs a whole tile in one CTA: no pushing of rows to
   // the other CTAs of a cluster (rank 0 pulls every share instead)
   const bool push = C::PUSH && p.epi != EPI_TOPK;
-  // Cluster split-K over two CTAs with 64+-token tiles: exchange by bulk
-  // copies.  Each CTA stages the rows the other finalises (share_f4 layout
-  // per owner block) and one thread sends the block with one cp.async.bulk;
-  // the owner sums in rank order, its own rows straight from TMEM, and
-  // writes them with the bulk-store epilogue.  Wider clusters pull every
-  // share through distributed shared memory instead: there the finalising
-  // rows of a rank (42 or fewer) would leave most epilogue lanes idle, which
-  // measured slower than the pull's spread over all four warps (so does the
-  // top-16 epilogue, whose rank 0 takes the whole tile).  The staging plus
-  // the receive slot must fit the idle ring.
+  // Cluster split-K with 64+-token tiles: exchange by bulk copies.  Each CTA
+  // stages its whole share grouped by owner (share_f4 layout per owner
+  // block) and one thread sends every other owner its block with one
+  // cp.async.bulk; each owner's four epilogue warps sum its rows in rank
+  // order from local shared memory and finalise them.  The staging plus the
+  // csk - 1 receive slots must fit the idle ring (else, and for the top-16
+  // epilogue, whose rank 0 takes the whole tile, the owners pull every
+  // share through distributed shared memory).
   const int x_rows = (BM + p.csk - 1) / p.csk;   // most rows any rank owns
-  const bool xchg = !C::PUSH && p.csk == 2 && p.epi != EPI_TOPK &&
+  const bool xchg = !C::PUSH && p.csk > 1 && p.epi != EPI_TOPK &&
                     static_cast<long long>(BM + (p.csk - 1) * x_rows) * BN * 4 <= C::RING;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *bcast = reinterpret_cast<int *>(tmem_slot + 2);
@@ -928,20 +926,19 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
             finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsg, xch);   // n >= N: not this CTA's row
         }
       } else if (xchg) {
-        // cluster split-K, exchange: the rows of other owners go to the
-        // staging blocks in the idle ring (owner o's block at row o_r0, its
-        // rows in the share_f4 layout); this CTA's own rows stay in TMEM
-        const int S = p.csk, rank = static_cast<int>(cluster_ctarank());
+        // cluster split-K, exchange: every row goes to its owner's staging
+        // block in the idle ring (owner o's block at row o_r0, its rows in
+        // the share_f4 layout); the other owners' blocks are sent, this
+        // CTA's own stays for its sums
+        const int S = p.csk;
         const int o = ((r + 1) * S - 1) / BM;   // the rank that owns row r
-        const bool send = o != rank;
         const int o_r0 = o * BM / S, o_rows = (o + 1) * BM / S - o_r0;
         float4 *blk = reinterpret_cast<float4 *>(base) + static_cast<size_t>(o_r0) * (BN / 4);
         for (int c = 0; c < BN / 16; ++c) {
-          tmem_ld16(taddr + c * 16, v);   // warp-collective: every lane loads
-          if (send)
+          tmem_ld16(taddr + c * 16, v);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              blk[share_f4(c, i, r - o_r0, o_rows)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          for (int i = 0; i < 4; ++i)
+            blk[share_f4(c, i, r - o_r0, o_rows)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
         fence_proxy_async_smem();   // the bulk copies read the staging through the async proxy
         tc_fence_before();
@@ -1088,7 +1085,9 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
   if (xchg) {
     // ---- cluster split-K exchange (see xchg above): receive slots armed,
     // every CTA's staging written and its ring idle, then one thread sends
-    // each owner its block; owners sum in rank order
+    // each owner its block; the owner's four epilogue warps share its rows'
+    // sums (every share, its own staged block included, in local shared
+    // memory in the same layout), rank order per element
     const int S = p.csk, rank = static_cast<int>(cluster_ctarank());
     const int my_r0 = rank * BM / S, my_rows = (rank + 1) * BM / S - my_r0;
     const uint32_t recv = static_cast<uint32_t>(BM * BN * 4);   // receive slots after the staging
@@ -1104,52 +1103,46 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
                           base + static_cast<size_t>(o_r0) * BN * 4, bytes, dsmem_addr(xbar, static_cast<uint32_t>(o)));
       }
     }
-    const int q = warp & 3;
-    // the epilogue warps whose TMEM lanes hold this CTA's rows finalise them
-    if (warp >= 2 && warp < 6 && q * 32 < my_r0 + my_rows && q * 32 + 32 > my_r0) {
-      const int r = q * 32 + lane;
-      const bool mine = r >= my_r0 && r < my_r0 + my_rows;
+    if (warp >= 2 && warp < 6) {   // the epilogue warps
+      const int et = threadIdx.x - 64;
       const bool got = mbar_wait(xbar, 0, abort_flag, p.timeout_ns);
-      if (!__all_sync(0xffffffffu, got)) {
-        if (lane == 0) report(p.status, DFLASH_ERR_TIMEOUT);
+      if (bar_or(1, 128, !got)) {
+        if (et == 0) report(p.status, DFLASH_ERR_TIMEOUT);
         *abort_flag = 1;
       } else {
-        tc_fence_after();
         const int tile = first_tile;
         const int rt = tile % p.rt_total;
         const size_t goff = static_cast<size_t>(rt / p.rtpg) * p.out_gstride;
         const float *wsg = p.wscale[rt / p.rtpg];   // FP8 codes, or bf16 copies of them
         const int tokt = (tile / p.rt_total) * BN;
-        const int n = mine ? (rt % p.rtpg) * BM + r : p.N;   // n >= N: nothing stored
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);   // the one segment: buffer 0
+        const float4 *own = reinterpret_cast<const float4 *>(base) + static_cast<size_t>(my_r0) * (BN / 4);
         const float4 *rv = reinterpret_cast<const float4 *>(base + recv);
-        const int rr = mine ? r - my_r0 : 0;
-        // whole warps of rows: the bulk-store epilogue (two buffers per warp)
-        const bool tma_w = BN >= 64 && p.tma_out && my_rows % 32 == 0 && my_r0 % 32 == 0;
-        uint8_t *ostg = base + C::RING + C::CTRL + (BN >= 64 ? q * C::OSTG_WARP : 0);
+        const int tasks = my_rows * (BN / 16);
+        // whole warps of consecutive rows: the bulk-store epilogue
+        const bool tma_w = BN >= 64 && p.tma_out && my_rows % 32 == 0;
+        uint8_t *ostg = base + C::RING + C::CTRL + (BN >= 64 ? (warp & 3) * C::OSTG_WARP : 0);
         uint32_t ocnt = 0;
-        for (int c = 0; c < BN / 16; ++c) {
-          float v[16], w[16];
-          tmem_ld16(taddr + c * 16, w);
+        for (int t0 = 0; t0 < tasks; t0 += 128) {   // every thread takes each round (shuffles in SwiGLU)
+          const int task = t0 + et;
+          const bool valid = task < tasks;
+          const int row = valid ? task % my_rows : 0, grp = valid ? task / my_rows : 0;
+          float v[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] = 0.f;
-          for (int k = 0; k < S; ++k) {   // rank order: deterministic
-            if (k == rank) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] += w[i];
-            } else {
-              const int slot = k < rank ? k : k - 1;
-              const float4 *src = rv + static_cast<size_t>(slot) * my_rows * (BN / 4);
+          if (valid)
+            for (int k = 0; k < S; ++k) {   // rank order: deterministic
+              const float4 *src =
+                  k == rank ? own : rv + static_cast<size_t>(k < rank ? k : k - 1) * my_rows * (BN / 4);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const float4 x = src[share_f4(c, i, rr, my_rows)];
+                const float4 x = src[share_f4(grp, i, row, my_rows)];
                 v[4 * i] += x.x;
                 v[4 * i + 1] += x.y;
                 v[4 * i + 2] += x.z;
                 v[4 * i + 3] += x.w;
               }
             }
-          }
+          const int n = valid ? (rt % p.rtpg) * BM + my_r0 + row : p.N;   // n >= N: nothing stored
           if (tma_w) {
             uint8_t *b = ostg + (ocnt & 1u) * 2048;
             if (ocnt >= 2) {
@@ -1157,9 +1150,9 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
               __syncwarp();
             }
             ++ocnt;
-            finalize_tma(p, om, v, n, tokt + c * 16, wsg, b, lane);
+            finalize_tma(p, om, v, n, tokt + grp * 16, wsg, b, lane);
           } else {
-            finalize(p, v, n, tokt + c * 16, goff, wsg, xch);
+            finalize(p, v, n, tokt + grp * 16, goff, wsg, xch);
           }
         }
         if (tma_w && lane == 0) bulk_wait_read<0>();
