@@ -699,7 +699,9 @@ def run_workload(args, wl, steps, warmup, world, local, dev, headline):
         "e2e": {"value": aggregate_blocks_per_s(world, B, steps, ms_e2e), "unit": "blocks/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "per step: H2D of the new tokens' features, anchors and target ids from pinned memory, "
-                       "the four C-ABI calls launched eagerly, D2H of accept/bonus/committed, synchronise"},
+                       "the four C-ABI calls launched eagerly, D2H of accept/bonus/committed, synchronise"
+                       + ("; sampling mode: the target logits and uniforms stay resident in HBM (not copied per "
+                          "step: in serving they come from the target model on the same GPU)" if sampling else "")},
         "e2e_graph": {"value": aggregate_blocks_per_s(world, B, steps, ms_e2e_graph), "unit": "blocks/s",
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                       "how": "the same copies around one replay of the captured step"},
