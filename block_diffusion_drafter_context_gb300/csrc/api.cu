@@ -526,6 +526,9 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
   };
   // a sublayer's output projection: straight into the fp32 residual, or (conv)
   // into fp32 + bf16 halves, then the post-site conv adds it to the residual
+  // a post-sublayer short conv waiting for the next RMSNorm, which applies
+  // it to the residual on the way (one launch fewer per site)
+  const float *conv_y = nullptr, *conv_c = nullptr;
   auto out_proj = [&](int site, const dflash_layer_weights &lw, const void *Wm, const float *Ws, const void *Wb,
                       int K, const void *X, const void *X_lo, const char *name) -> int {
     if (!g.use_conv)
@@ -536,7 +539,15 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     op.ldo2 = H;
     if (int e = proj(ctx, lc, ws, L, op)) return e;
     if (int e = coef_gemm(site, lw, f32 ? static_cast<const void *>(ysub32) : ysub, ysub_lo)) return e;
-    return conv_apply(lc, f32, nullptr, nullptr, ysub32, coef, B, S, H, nullptr, nullptr, x);
+    conv_y = ysub32;
+    conv_c = coef;
+    return DFLASH_OK;
+  };
+  // the next RMSNorm, taking the pending conv if there is one
+  auto norm = [&](const float *gain, void *out, void *out_lo, void *mrows, void *mrows_lo) -> int {
+    const float *cy = conv_y, *cc = conv_c;
+    conv_y = conv_c = nullptr;
+    return rmsnorm_rows(lc, f32, x, R, H, S, gain, g.eps, out, out_lo, mrows, mrows_lo, cy, cc);
   };
   for (int l = 0; l < g.n_layers; ++l) {
     const dflash_layer_weights &lw = ctx->layers[l];
@@ -581,7 +592,7 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     if (int e = f32 ? attention_f32(lc, aa) : attention_bf16(lc, aa)) return e;
     if (int e = out_proj(1, lw, lw.w_o, lw.s_o, lw.w_o_bf16, nq * d, aa.out, aa.out_lo, "o_proj")) return e;
     // ---- FFN sublayer
-    if (int e = rmsnorm_rows(lc, f32, x, R, H, S, lw.g_ffn, g.eps, u, u_lo, nullptr, nullptr)) return e;
+    if (int e = norm(lw.g_ffn, u, u_lo, nullptr, nullptr)) return e;
     ua = u;
     ua_lo = u_lo;
     if (g.use_conv) {
@@ -598,12 +609,9 @@ int dflash_draft_block(dflash_ctx *ctx, const dflash_kv *kv, const int32_t *ctx_
     }
     if (int e = out_proj(3, lw, lw.w_down, lw.s_down, lw.w_down_bf16, F, at<void>(ws, L.hmid), hmid_lo, "down")) return e;
     if (l + 1 < g.n_layers)
-      if (int e = rmsnorm_rows(lc, f32, x, R, H, S, ctx->layers[l + 1].g_attn, g.eps, u, u_lo, nullptr, nullptr))
-        return e;
+      if (int e = norm(ctx->layers[l + 1].g_attn, u, u_lo, nullptr, nullptr)) return e;
   }
-  if (int e = rmsnorm_rows(lc, f32, x, R, H, S, ctx->w.g_final, g.eps, hfinal, nullptr, at<void>(ws, L.hmask),
-                           lo(L.hmask_lo)))
-    return e;
+  if (int e = norm(ctx->w.g_final, hfinal, nullptr, at<void>(ws, L.hmask), lo(L.hmask_lo))) return e;
   // the fused epilogue hides under the LM head's weight stream only with
   // small token tiles (at most 32 mask rows per launch); larger launches are
   // tensor-bound and its per-tile selection would lengthen them

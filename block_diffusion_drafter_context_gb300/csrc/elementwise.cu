@@ -144,10 +144,16 @@ __global__ void __launch_bounds__(ROW_THREADS) embed_rmsnorm_kernel(const T *emb
 // ------------------------------------------------------------------ rmsnorm
 // out[row] = RMSNorm(x[row]) (+ low halves); rows with j = row % S >= 1 are
 // also written compactly to out_mask[b*(S-1) + j-1] (LM-head input of the
-// mask rows).
+// mask rows).  With conv_coef, the DFlash-2 short conv of a post-sublayer
+// site is applied first ("DFlash 2", Arquitectura del Sistema item 2):
+// x[row] += y + a*y + b*y_prev (y = conv_y32, fp32 [rows][H]; a, b the
+// row's two taps of each 16-channel group, interleaved in conv_coef
+// [rows][H/8]; nothing before block position 0) and x written back - the
+// same arithmetic as conv_kernel, one launch fewer.
 template <typename T>
-__global__ void __launch_bounds__(ROW_THREADS) rmsnorm_kernel(const float *x, int H, const float *gain, float eps,
-                                                              int S, T *out, T *out_lo, T *out_mask, T *out_mask_lo) {
+__global__ void __launch_bounds__(ROW_THREADS) rmsnorm_kernel(float *x, int H, const float *gain, float eps,
+                                                              int S, T *out, T *out_lo, T *out_mask, T *out_mask_lo,
+                                                              const float *conv_y32, const float *conv_coef) {
   __shared__ float red[32];
   const int row = blockIdx.x;
   const float *xr = x + static_cast<size_t>(row) * H;
@@ -163,11 +169,28 @@ __global__ void __launch_bounds__(ROW_THREADS) rmsnorm_kernel(const float *x, in
     const int i = threadIdx.x + k * ROW_THREADS;
     if (i < nv) v[k] = ld4(xr + 4 * i);
   }
+  const int b = row / S, j = row % S;
+  if (conv_coef) {
+    const float *yr = conv_y32 + static_cast<size_t>(row) * H;
+    const float *cr = conv_coef + static_cast<size_t>(row) * (H / 8);
+    float *xw = x + static_cast<size_t>(row) * H;
+#pragma unroll
+    for (int k = 0; k < MAXV; ++k) {
+      const int i = threadIdx.x + k * ROW_THREADS;
+      if (i >= nv) continue;
+      const float4 yv = ld4(yr + 4 * i);
+      const float4 yp = j ? ld4(yr - H + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float ca = cr[2 * (i >> 2)], cb = cr[2 * (i >> 2) + 1];   // group (4i) / 16
+      const float cx = yv.x + ca * yv.x + cb * yp.x, cy = yv.y + ca * yv.y + cb * yp.y;
+      const float cz = yv.z + ca * yv.z + cb * yp.z, cw = yv.w + ca * yv.w + cb * yp.w;
+      v[k] = make_float4(v[k].x + cx, v[k].y + cy, v[k].z + cz, v[k].w + cw);
+      *reinterpret_cast<float4 *>(xw + 4 * i) = v[k];
+    }
+  }
 #pragma unroll
   for (int k = 0; k < MAXV; ++k)
     if (threadIdx.x + k * ROW_THREADS < nv) ss += dot4(v[k]);
   const float r = rsqrtf(block_sum(ss, red) / H + eps);
-  const int b = row / S, j = row % S;
   const size_t mrow = static_cast<size_t>(b * (S - 1) + j - 1) * H;
 #pragma unroll
   for (int k = 0; k < MAXV; ++k) {
@@ -631,17 +654,19 @@ int embed_rmsnorm(const Launch &lc, bool f32, const void *embed, const int32_t *
   });
 }
 
-int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, int S, const float *gain, float eps,
-                 void *out, void *out_lo, void *out_mask_rows, void *out_mask_lo) {
+int rmsnorm_rows(const Launch &lc, bool f32, float *x, int rows, int H, int S, const float *gain, float eps,
+                 void *out, void *out_lo, void *out_mask_rows, void *out_mask_lo, const float *conv_y32,
+                 const float *conv_coef) {
   if (int e = check_row(H)) return e;
+  if (conv_coef && (!conv_y32 || H % 16)) return set_error(DFLASH_ERR_ARG, "rmsnorm: conv needs y and 16-channel groups");
   return run(lc, "rmsnorm", [&] {
     if (f32)
       launch_pdl(rmsnorm_kernel<float>, dim3(rows), dim3(ROW_THREADS), 0, lc.stream, x, H, gain, eps, S,
-                 tp<float>(out), nullptr, tp<float>(out_mask_rows), nullptr);
+                 tp<float>(out), nullptr, tp<float>(out_mask_rows), nullptr, conv_y32, conv_coef);
     else
       launch_pdl(rmsnorm_kernel<__nv_bfloat16>, dim3(rows), dim3(ROW_THREADS), 0, lc.stream,
           x, H, gain, eps, S, tp<__nv_bfloat16>(out), tp<__nv_bfloat16>(out_lo), tp<__nv_bfloat16>(out_mask_rows),
-          tp<__nv_bfloat16>(out_mask_lo));
+          tp<__nv_bfloat16>(out_mask_lo), conv_y32, conv_coef);
   });
 }
 

@@ -169,8 +169,11 @@ int attention_f32(const Launch &lc, const AttnArgs &a);
 // S = block size (anchor + S-1 mask positions), 2..16
 int embed_rmsnorm(const Launch &lc, bool f32, const void *embed, const int32_t *anchor, int mask_id, int vocab,
                   const float *gain, float eps, int B, int S, int H, float *x, void *u, void *u_lo);
-int rmsnorm_rows(const Launch &lc, bool f32, const float *x, int rows, int H, int S, const float *gain, float eps,
-                 void *out, void *out_lo, void *out_mask_rows, void *out_mask_lo);
+// conv_y32 / conv_coef (both or neither): a post-sublayer DFlash-2 short conv
+// added into x first (x written back), see rmsnorm_kernel
+int rmsnorm_rows(const Launch &lc, bool f32, float *x, int rows, int H, int S, const float *gain, float eps,
+                 void *out, void *out_lo, void *out_mask_rows, void *out_mask_lo, const float *conv_y32 = nullptr,
+                 const float *conv_coef = nullptr);
 int feature_norm(const Launch &lc, bool f32, const float *in, int rows, int H, const float *gain, float eps,
                  bool apply_norm, void *out, void *out_lo, const int32_t *ctx_len_in, int32_t *ctx_len_saved, int B);
 int qk_norm_rope(const Launch &lc, bool f32, const float *qkv, int B, int S, int nq, int nkv, int d,
