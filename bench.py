@@ -815,8 +815,9 @@ def main():
     ap.add_argument("--oracle-probe", default=None, help=argparse.SUPPRESS)
     ap.add_argument("--fused-topk", type=int, default=0,
                     help="LM head with its top-16 epilogue (1) or logits + standalone top-16 (0, default)")
-    ap.add_argument("--gemm-pairs", type=int, default=0,
-                    help="256-token GEMM tiles on CTA pairs with the 2-SM MMA (1) or single CTAs (0, default)")
+    ap.add_argument("--gemm-pairs", type=int, default=1,
+                    help="256-token GEMM tiles on CTA pairs with the 2-SM MMA where the plan favours it "
+                         "(1, default) or always on single CTAs (0)")
     # smaller variants of the headline workload for profiling captures
     ap.add_argument("--layers", type=int, default=None, help="drafter layers (profiling cases)")
     ap.add_argument("--batch", type=int, default=None, help="requests (profiling cases)")

@@ -21,7 +21,7 @@ struct dflash_ctx {
   int num_sms = 148;
   unsigned long long timeout_ns = 2000000000ull;
   int gemm_ctas = 0;
-  int gemm_pairs = 0;
+  int gemm_pairs = 1;
   int fused_topk = 0;      // bf16: LM head with its top-16 epilogue (no logits round trip)
   int attn_split = 0;
   int block = 16;   // runtime block size S (2..cfg.block_size)

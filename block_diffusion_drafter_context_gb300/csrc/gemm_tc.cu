@@ -1255,15 +1255,17 @@ struct PairCfg {
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
   static constexpr int RING = STAGES * STAGE_BYTES;
   static constexpr int CTRL = 512;
+  static constexpr int OSTG_WARP = 4096;               // bulk-store staging per epilogue warp
   static constexpr int TMEM_COLS = 2 * BN;             // two accumulators of BN columns
-  static constexpr int SMEM = 1024 + RING + CTRL;
+  static constexpr int SMEM = 1024 + RING + CTRL + 4 * OSTG_WARP;
   static_assert((2 * STAGES + 5) * 8 + 12 <= CTRL, "pair GEMM control block overflows");
   static_assert(SMEM <= 227 * 1024 && TMEM_COLS <= 512, "pair GEMM resources");
 };
 
 template <int BN>
 __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
-    gemm_pair_kernel(const __grid_constant__ WMaps wm, const __grid_constant__ CUtensorMap tmX, const Params p) {
+    gemm_pair_kernel(const __grid_constant__ WMaps wm, const __grid_constant__ CUtensorMap tmX,
+                     const __grid_constant__ OMaps om, const Params p) {
   using C = PairCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -1336,40 +1338,51 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
         (void)pol_w;
         tma_load_2d_pair(sA + s * C::A_BYTES, &wm.m[g], full_addr(s), kb * BK, row0);
       };
-      auto load_x = [&](int s, int pt, int kb) {
-        const int tok = pt / RTP;
+      auto load_x = [&](int s, int tok, int kb) {
         tma_load_2d_pair(sB + s * C::B_BYTES, &tmX, full_addr(s), kb * BK, tok * BN + rank * C::BH);
       };
       const int n_pre = static_cast<int>(n_my < C::STAGES ? n_my : C::STAGES);
+      // iteration -> (pair tile, k-block) and the tile's weight rows, advanced
+      // incrementally: no 64-bit division in the issue loop (one thread
+      // issues both loads of every ~650-cycle k-block)
+      struct PIter {
+        int pt, kb, g, row0, tok;
+      };
+      auto start = [&](long long it) {
+        PIter q;
+        q.pt = static_cast<int>(it / p.kbpt);
+        q.kb = static_cast<int>(it - static_cast<long long>(q.pt) * p.kbpt);
+        bool ph;
+        rows_of(q.pt, q.g, q.row0, ph);
+        q.tok = q.pt / RTP;
+        return q;
+      };
+      auto advance = [&](PIter &q) {
+        if (++q.kb == p.kbpt) {
+          q.kb = 0;
+          ++q.pt;
+          bool ph;
+          rows_of(q.pt, q.g, q.row0, ph);
+          q.tok = q.pt / RTP;
+        }
+      };
       // weights of the first ring slots depend on nothing: stream them while
       // the previous kernel finishes, then wait for it before the activations
-      for (int i = 0; i < n_pre; ++i) {
-        const long long it = begin + i;
-        const int pt = static_cast<int>(it / p.kbpt), kb = static_cast<int>(it % p.kbpt);
-        int g, row0;
-        bool ph;
-        rows_of(pt, g, row0, ph);
-        load_w(i, g, row0, kb);
-      }
+      PIter q = start(begin);
+      for (int i = 0; i < n_pre; ++i, advance(q)) load_w(i, q.g, q.row0, q.kb);
       grid_dep_wait();
-      for (int i = 0; i < n_pre; ++i) {
-        const long long it = begin + i;
-        load_x(i, static_cast<int>(it / p.kbpt), static_cast<int>(it % p.kbpt));
-      }
+      q = start(begin);
+      for (int i = 0; i < n_pre; ++i, advance(q)) load_x(i, q.tok, q.kb);
       uint32_t stage = n_pre % C::STAGES, phase = (n_pre == C::STAGES) ? 1u : 0u;
       long long issued = n_pre;
       bool ok = true;
-      for (long long it = begin + n_pre; it < end; ++it) {
+      for (long long it = begin + n_pre; it < end; ++it, advance(q)) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
         }
-        const int pt = static_cast<int>(it / p.kbpt), kb = static_cast<int>(it % p.kbpt);
-        int g, row0;
-        bool ph;
-        rows_of(pt, g, row0, ph);
-        load_w(stage, g, row0, kb);
-        load_x(stage, pt, kb);
+        load_w(stage, q.g, q.row0, q.kb);
+        load_x(stage, q.tok, q.kb);
         ++issued;
         if (++stage == C::STAGES) {
           stage = 0;
@@ -1448,6 +1461,19 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
     const int r = q * 32 + lane;
     const int et = threadIdx.x - 64;
     const uint32_t tempty_leader0 = dsmem_addr(&tempty[0], 0u), tempty_leader1 = dsmem_addr(&tempty[1], 0u);
+    // bulk-store epilogue staging (see the single-CTA kernel): two buffers
+    // per warp, or the idle ring on the pair's last segment
+    uint8_t *ostg = base + C::RING + C::CTRL + q * C::OSTG_WARP;
+    uint32_t ocnt = 0;
+    auto xbuf = [&]() -> uint8_t * {
+      uint8_t *b = ostg + (ocnt & 1u) * 2048;
+      if (ocnt >= 2) {
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+      }
+      ++ocnt;
+      return b;
+    };
     grid_dep_wait();
     int seg = 0;
     for (long long it = begin; it < end; ++seg) {
@@ -1483,9 +1509,14 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
       if (phantom) {
         release();
       } else if (kb0 == 0 && kb1 == p.kbpt) {
+        // the pair's last segment: every MMA of both CTAs has completed, the rings are idle
+        const bool ring_out = it + (kb1 - kb0) == end;
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
-          finalize(p, v, n, tok0 + c * 16, goff, p.wscale[g], nullptr);
+          if (p.tma_out)
+            finalize_tma(p, om, v, n, tok0 + c * 16, p.wscale[g], ring_out ? base + (c * 4 + q) * 2048 : xbuf(), lane);
+          else
+            finalize(p, v, n, tok0 + c * 16, goff, p.wscale[g], nullptr);
         }
         release();
       } else {
@@ -1552,13 +1583,17 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
               v[4 * i + 2] = acc[i].z;
               v[4 * i + 3] = acc[i].w;
             }
-            finalize(p, v, n, tok0 + c * 16, goff, p.wscale[g], nullptr);
+            if (p.tma_out)
+              finalize_tma(p, om, v, n, tok0 + c * 16, p.wscale[g], xbuf(), lane);
+            else
+              finalize(p, v, n, tok0 + c * 16, goff, p.wscale[g], nullptr);
           }
         }
         epi_bar();
       }
       it += kb1 - kb0;
     }
+    if (p.tma_out && lane == 0) bulk_wait_read<0>();   // staging read before the CTA may exit
   }
 
   tc_fence_before();
@@ -1711,7 +1746,7 @@ int pair_setup() {
 }
 
 template <int BN>
-int launch_pair(const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const Params &p) {
+int launch_pair(const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const OMaps &tO, const Params &p) {
   using C = PairCfg<BN>;
   if (int e = pair_setup<BN>(); e < 0) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1728,7 +1763,7 @@ int launch_pair(const Launch &lc, const WMaps &tW, const CUtensorMap &tX, const 
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN>, tW, tX, p), "pair gemm launch");
+  return cuda_check(cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN>, tW, tX, tO, p), "pair gemm launch");
 }
 
 }  // namespace
@@ -1881,18 +1916,28 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
     return set_error(DFLASH_ERR_SHAPE, "gemm %s: workspace too small for %lld tiles", name, tiles);
   if (reinterpret_cast<uintptr_t>(sc.partials) & 15)
     return set_error(DFLASH_ERR_ALIGN, "gemm %s: partial scratch must be 16-byte aligned", name);
-  // Tensor-bound 256-token tiles (bf16 weights and activations, no cluster
-  // split-K): CTA pairs with the 2-SM MMA.  gemm_ctas < 0 (test hook) forces
+  // Tensor-bound 256-token tiles (bf16 weights and activations) whose
+  // single-CTA plan is stream-K or whole tiles: CTA pairs with the 2-SM MMA
+  // (a third less operand traffic per MMA), unless a residual-add launch
+  // gives each pair under 128 k-blocks - there its tail, whose split tiles
+  // the pair kernel reduces through L2, outweighs the gain (27B-class O
+  // projection: 307 us single, 319 us pairs per step).  Cluster split-K
+  // launches stay on single CTAs.  gemm_ctas < 0 (test hook) forces
   // -gemm_ctas pairs.
-  const bool pairs = !f8 && !split && BN == 256 && epi != EPI_TOPK &&
-                     (lc.gemm_ctas < 0 || (lc.gemm_pairs && lc.gemm_ctas == 0)) &&
-                     (p.n_groups == 1 || p.rtpg % 2 == 0);
+  bool pairs = !f8 && !split && BN == 256 && epi != EPI_TOPK &&
+               (lc.gemm_ctas < 0 || (lc.gemm_pairs && lc.gemm_ctas == 0 && pl.csk == 1)) &&
+               (p.n_groups == 1 || p.rtpg % 2 == 0);
+  int max_pairs = 0;
+  long long rtp = 0, ptiles = 0;
+  if (pairs) {
+    max_pairs = pair_setup<256>();
+    if (max_pairs < 0) return max_pairs;
+    rtp = (pl.rtpg * static_cast<long long>(p.n_groups) + 1) / 2;
+    ptiles = rtp * pl.tok_tiles;
+    if (lc.gemm_ctas == 0 && epi == EPI_ADD_F32 && ptiles * pl.kbpt < 128ll * max_pairs) pairs = false;
+  }
   if (pairs) {
     p.csk = 1;
-    const int max_pairs = pair_setup<256>();
-    if (max_pairs < 0) return max_pairs;
-    const long long rtp = (pl.rtpg * static_cast<long long>(p.n_groups) + 1) / 2;
-    const long long ptiles = rtp * pl.tok_tiles;
     p.total = ptiles * pl.kbpt;
     // as many pairs as fit at once, each at least 4 k-blocks and no pair
     // tile cut into more than 2 pieces (a fixup reads at most 256 KB)
@@ -1932,7 +1977,7 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   OMaps tO;
   std::memset(&tO, 0, sizeof(tO));
   p.tma_out = 0;
-  if (!pairs && BN >= 64 && p.n_groups == 1 &&
+  if (BN >= 64 && p.n_groups == 1 &&
       (epi == EPI_F32 || epi == EPI_ADD_F32 || epi == EPI_TANH_BIAS || epi == EPI_BF16 || epi == EPI_SWIGLU)) {
     const bool f32o = epi == EPI_F32 || epi == EPI_ADD_F32 || epi == EPI_TANH_BIAS;
     const int esz = f32o ? 4 : 2;
@@ -1963,7 +2008,7 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   const double ng = p.n_groups;
   ProfScope ps(lc, name, ng * (wbytes * static_cast<double>(N) * K + (f8 ? 4.0 * N : 0.0) + out_bytes) + xb,
                ng * (split ? 4.0 : 2.0) * M * N * K);
-  if (pairs) return launch_pair<256>(lc, tW, tX, p);
+  if (pairs) return launch_pair<256>(lc, tW, tX, tO, p);
   if (f8)
     return split ? launch_bn<true, true>(BN, lc, tW, tX, tXl, tO, p) : launch_bn<false, true>(BN, lc, tW, tX, tXl, tO, p);
   return split ? launch_bn<true, false>(BN, lc, tW, tX, tXl, tO, p) : launch_bn<false, false>(BN, lc, tW, tX, tXl, tO, p);

@@ -82,7 +82,7 @@ struct Launch {
   int *status = nullptr;                 // device status word
   unsigned long long timeout_ns = 2000000000ull;
   int gemm_ctas = 0;                     // 0 = SM count; < 0: that many CTA pairs (test hook)
-  int gemm_pairs = 0;                    // 256-token tiles on CTA pairs (2-SM MMA)
+  int gemm_pairs = 1;                    // 256-token tiles on CTA pairs (2-SM MMA) where that pays
   Profiler *prof = nullptr;
 };
 

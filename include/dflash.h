@@ -314,9 +314,10 @@ DFLASH_API int dflash_set_wait_timeout(dflash_ctx *ctx, unsigned long long ns);
 DFLASH_API int dflash_set_gemm_ctas(dflash_ctx *ctx, int ctas);
 
 /* Projections with 256-token tiles (bf16 weights and activations) run on CTA
- * pairs with the 2-SM tensor-core MMA (on = 1) or on single CTAs (on = 0,
- * the default): a switch for comparing the two; results are identical up to
- * fp32 summation order.  Host-only. */
+ * pairs with the 2-SM tensor-core MMA where the launch's plan favours it
+ * (on = 1, the default) or always on single CTAs (on = 0): a switch for
+ * comparing the two; results are identical up to fp32 summation order.
+ * Host-only. */
 DFLASH_API int dflash_set_gemm_pairs(dflash_ctx *ctx, int on);
 /* bf16 drafters: the LM head selects the top-16 inside its GEMM epilogue
  * (on = 1: per 128-row vocabulary tile the 16 largest keys of each mask row,
