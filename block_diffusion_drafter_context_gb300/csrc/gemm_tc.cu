@@ -1258,7 +1258,7 @@ struct PairCfg {
   static constexpr int OSTG_WARP = 4096;               // bulk-store staging per epilogue warp
   static constexpr int TMEM_COLS = 2 * BN;             // two accumulators of BN columns
   static constexpr int SMEM = 1024 + RING + CTRL + 4 * OSTG_WARP;
-  static_assert((2 * STAGES + 5) * 8 + 12 <= CTRL, "pair GEMM control block overflows");
+  static_assert((2 * STAGES + 6) * 8 + 12 <= CTRL, "pair GEMM control block overflows");
   static_assert(SMEM <= 227 * 1024 && TMEM_COLS <= 512, "pair GEMM resources");
 };
 
@@ -1277,7 +1277,8 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
   uint64_t *tfull = empty + C::STAGES;
   uint64_t *tempty = tfull + 2;
   uint64_t *drain = tempty + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *fbar = drain + 1;   // fixup: the other contributors' shares staged in the ring
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fbar + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *bcast = reinterpret_cast<int *>(tmem_slot + 2);
 
@@ -1296,6 +1297,7 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
     mbar_init(&tempty[0], 8);   // four epilogue warps of each CTA
     mbar_init(&tempty[1], 8);
     mbar_init(drain, 1);
+    mbar_init(fbar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1520,19 +1522,22 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
         }
         release();
       } else {
-        // partial tile: this CTA's fp32 share of its 128 rows to its slot;
-        // the CTA (of the same rank) completing the tile's k-range sums all
-        // shares in pair order
+        // partial tile: this CTA's fp32 share of its 128 rows to its slot
+        // (tile_f4 layout); the CTA (of the same rank) completing the tile's
+        // k-range sums all shares in pair order, its own straight from TMEM
+        // (the accumulator is released after the fixup) and, on its last
+        // segment, the others bulk-copied into its idle ring
+        constexpr int SHARE = BM * BN;   // floats
         const int tile_h = pt * 2 + rank;
         const int slot = (pt == first_pt) ? 0 : 1;
-        float4 *P4 = reinterpret_cast<float4 *>(p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * (BM * BN));
+        float4 *P4 = reinterpret_cast<float4 *>(p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * SHARE);
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             __stcg(P4 + tile_f4(c, i, r), make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
         }
-        release();
+        fence_proxy_async_global();   // the completing CTA may bulk-copy these shares
         epi_bar();
         if (et == 0) {
           __threadfence();
@@ -1551,30 +1556,59 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
           const int c_lo = cta_of(t_beg, p.total, Gp);
           const int c_hi = cta_of(t_beg + p.kbpt - 1, p.total, Gp);
           const int slot_lo = range_begin(p.total, Gp, c_lo) < t_beg ? 1 : 0;
+          auto share_of = [&](int cc) -> const float4 * {
+            return reinterpret_cast<const float4 *>(
+                p.partials + (static_cast<size_t>(2 * cc + rank) * 2 + (cc == c_lo ? slot_lo : 0)) * SHARE);
+          };
+          const int others = c_hi - c_lo;
+          const int staged = (it + (kb1 - kb0) == end) ? (others < C::RING / (SHARE * 4) ? others : C::RING / (SHARE * 4))
+                                                       : 0;
+          if (staged > 0) {
+            if (et == 0) {
+              fence_proxy_async_global();   // after the acquiring atomic: the copies read the published shares
+              mbar_arrive_expect_tx(fbar, static_cast<uint32_t>(staged) * SHARE * 4);
+              for (int cc = c_lo, k = 0; k < staged; ++cc) {
+                if (cc == pair) continue;
+                bulk_load(base + static_cast<size_t>(k) * SHARE * 4, share_of(cc), SHARE * 4, fbar);
+                ++k;
+              }
+            }
+            const bool got_sh = mbar_wait(fbar, 0, abort_flag, p.timeout_ns);
+            if (bar_or(1, 128, !got_sh || *abort_flag)) {
+              if (et == 0) report(p.status, DFLASH_ERR_TIMEOUT);
+              *abort_flag = 1;
+              if (et == 0) mbar_wait(fbar, 0, nullptr, p.timeout_ns);   // the copies land before the CTA exits
+              break;
+            }
+          }
+          const float4 *ring4 = reinterpret_cast<const float4 *>(base);
           for (int c = 0; c < BN / 16; ++c) {
             float4 acc[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int cc0 = c_lo; cc0 <= c_hi; cc0 += 4) {
-              float4 t[4][4];
+            int k = 0;   // staged shares met so far
+            for (int cc = c_lo; cc <= c_hi; ++cc) {   // summed in pair order: deterministic
+              float4 t[4];
+              if (cc == pair) {
+                tmem_ld16(taddr + c * 16, v);
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int cc = cc0 + u;
-                const float4 *Q4 = reinterpret_cast<const float4 *>(
-                    p.partials + (static_cast<size_t>(2 * cc + rank) * 2 + (cc == c_lo ? slot_lo : 0)) * (BM * BN));
+                for (int i = 0; i < 4; ++i) t[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+              } else if (k < staged) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  t[u][i] = cc <= c_hi ? __ldcg(Q4 + tile_f4(c, i, r)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int i = 0; i < 4; ++i) t[i] = ring4[static_cast<size_t>(k) * (SHARE / 4) + tile_f4(c, i, r)];
+                ++k;
+              } else {
+                const float4 *Q4 = share_of(cc);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) t[i] = __ldcg(Q4 + tile_f4(c, i, r));
               }
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  acc[i].x += t[u][i].x;
-                  acc[i].y += t[u][i].y;
-                  acc[i].z += t[u][i].z;
-                  acc[i].w += t[u][i].w;
-                }
+              for (int i = 0; i < 4; ++i) {
+                acc[i].x += t[i].x;
+                acc[i].y += t[i].y;
+                acc[i].z += t[i].z;
+                acc[i].w += t[i].w;
+              }
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -1583,12 +1617,21 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
               v[4 * i + 2] = acc[i].z;
               v[4 * i + 3] = acc[i].w;
             }
-            if (p.tma_out)
-              finalize_tma(p, om, v, n, tok0 + c * 16, p.wscale[g], xbuf(), lane);
-            else
+            if (p.tma_out) {
+              uint8_t *b;
+              if (staged > 0) {   // the first staged share's run for this group, read by this warp
+                __syncwarp();
+                b = base + (c * 4 + q) * 2048;
+              } else {
+                b = xbuf();
+              }
+              finalize_tma(p, om, v, n, tok0 + c * 16, p.wscale[g], b, lane);
+            } else {
               finalize(p, v, n, tok0 + c * 16, goff, p.wscale[g], nullptr);
+            }
           }
         }
+        release();
         epi_bar();
       }
       it += kb1 - kb0;
@@ -1918,25 +1961,16 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
     return set_error(DFLASH_ERR_ALIGN, "gemm %s: partial scratch must be 16-byte aligned", name);
   // Tensor-bound 256-token tiles (bf16 weights and activations) whose
   // single-CTA plan is stream-K or whole tiles: CTA pairs with the 2-SM MMA
-  // (a third less operand traffic per MMA), unless a residual-add launch
-  // gives each pair under 128 k-blocks - there its tail, whose split tiles
-  // the pair kernel reduces through L2, outweighs the gain (27B-class O
-  // projection: 307 us single, 319 us pairs per step).  Cluster split-K
-  // launches stay on single CTAs.  gemm_ctas < 0 (test hook) forces
-  // -gemm_ctas pairs.
-  bool pairs = !f8 && !split && BN == 256 && epi != EPI_TOPK &&
-               (lc.gemm_ctas < 0 || (lc.gemm_pairs && lc.gemm_ctas == 0 && pl.csk == 1)) &&
-               (p.n_groups == 1 || p.rtpg % 2 == 0);
-  int max_pairs = 0;
-  long long rtp = 0, ptiles = 0;
+  // (a third less operand traffic per MMA).  Cluster split-K launches stay
+  // on single CTAs.  gemm_ctas < 0 (test hook) forces -gemm_ctas pairs.
+  const bool pairs = !f8 && !split && BN == 256 && epi != EPI_TOPK &&
+                     (lc.gemm_ctas < 0 || (lc.gemm_pairs && lc.gemm_ctas == 0 && pl.csk == 1)) &&
+                     (p.n_groups == 1 || p.rtpg % 2 == 0);
   if (pairs) {
-    max_pairs = pair_setup<256>();
+    const int max_pairs = pair_setup<256>();
     if (max_pairs < 0) return max_pairs;
-    rtp = (pl.rtpg * static_cast<long long>(p.n_groups) + 1) / 2;
-    ptiles = rtp * pl.tok_tiles;
-    if (lc.gemm_ctas == 0 && epi == EPI_ADD_F32 && ptiles * pl.kbpt < 128ll * max_pairs) pairs = false;
-  }
-  if (pairs) {
+    const long long rtp = (pl.rtpg * static_cast<long long>(p.n_groups) + 1) / 2;
+    const long long ptiles = rtp * pl.tok_tiles;
     p.csk = 1;
     p.total = ptiles * pl.kbpt;
     // as many pairs as fit at once, each at least 4 k-blocks and no pair
