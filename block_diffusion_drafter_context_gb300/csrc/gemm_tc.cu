@@ -1959,12 +1959,16 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
     return set_error(DFLASH_ERR_SHAPE, "gemm %s: workspace too small for %lld tiles", name, tiles);
   if (reinterpret_cast<uintptr_t>(sc.partials) & 15)
     return set_error(DFLASH_ERR_ALIGN, "gemm %s: partial scratch must be 16-byte aligned", name);
-  // Tensor-bound 256-token tiles (bf16 weights and activations) whose
-  // single-CTA plan is stream-K or whole tiles: CTA pairs with the 2-SM MMA
-  // (a third less operand traffic per MMA).  Cluster split-K launches stay
-  // on single CTAs.  gemm_ctas < 0 (test hook) forces -gemm_ctas pairs.
+  // Tensor-bound 256-token tiles (bf16 weights and activations): CTA pairs
+  // with the 2-SM MMA (a third less operand traffic per MMA), except where
+  // the single-CTA plan is cluster split-K over a short k-range (under 128
+  // k-blocks per tile: the 512-token O projection, 190 us per step on
+  // two-CTA clusters against 202 on pairs; longer ones gain, the 512-token
+  // down projection 311 -> 275 us).  gemm_ctas < 0 (test hook) forces
+  // -gemm_ctas pairs.
   const bool pairs = !f8 && !split && BN == 256 && epi != EPI_TOPK &&
-                     (lc.gemm_ctas < 0 || (lc.gemm_pairs && lc.gemm_ctas == 0 && pl.csk == 1)) &&
+                     (lc.gemm_ctas < 0 ||
+                      (lc.gemm_pairs && lc.gemm_ctas == 0 && (pl.csk == 1 || pl.kbpt >= 128))) &&
                      (p.n_groups == 1 || p.rtpg % 2 == 0);
   if (pairs) {
     const int max_pairs = pair_setup<256>();
