@@ -1960,29 +1960,37 @@ int gemm_bf16(const Launch &lc, const GemmOp &op, const GemmScratch &sc) {
   if (reinterpret_cast<uintptr_t>(sc.partials) & 15)
     return set_error(DFLASH_ERR_ALIGN, "gemm %s: partial scratch must be 16-byte aligned", name);
   // Tensor-bound 256-token tiles (bf16 weights and activations): CTA pairs
-  // with the 2-SM MMA (a third less operand traffic per MMA), except where
-  // the single-CTA plan is cluster split-K over a short k-range (under 128
-  // k-blocks per tile: the 512-token O projection, 190 us per step on
-  // two-CTA clusters against 202 on pairs; longer ones gain, the 512-token
-  // down projection 311 -> 275 us).  gemm_ctas < 0 (test hook) forces
-  // -gemm_ctas pairs.
-  const bool pairs = !f8 && !split && BN == 256 && epi != EPI_TOPK &&
-                     (lc.gemm_ctas < 0 ||
-                      (lc.gemm_pairs && lc.gemm_ctas == 0 && (pl.csk == 1 || pl.kbpt >= 128))) &&
-                     (p.n_groups == 1 || p.rtpg % 2 == 0);
+  // with the 2-SM MMA (a third less operand traffic per MMA) where that
+  // pays, as measured:
+  //  * at least one full 256-token tile (at 160 tokens pairs were slower:
+  //    gate/up 344 -> 364 us per step);
+  //  * a single-CTA cluster split-K plan only over a long k-range (128+
+  //    k-blocks per tile: 512-token down 311 -> 275 us, while the O
+  //    projection's 64 stay on two-CTA clusters, 190 against 202 us) and
+  //    only if the pair plan keeps as many CTAs busy (its pair tiles are cut
+  //    at most in two: with few of them it would leave SMs idle).
+  // gemm_ctas < 0 (test hook) forces -gemm_ctas pairs.
+  bool pairs = !f8 && !split && BN == 256 && epi != EPI_TOPK &&
+               (lc.gemm_ctas < 0 || (lc.gemm_pairs && lc.gemm_ctas == 0 && M >= 256 &&
+                                     (pl.csk == 1 || pl.kbpt >= 128))) &&
+               (p.n_groups == 1 || p.rtpg % 2 == 0);
+  long long ptiles = 0, gp = 0;
   if (pairs) {
     const int max_pairs = pair_setup<256>();
     if (max_pairs < 0) return max_pairs;
     const long long rtp = (pl.rtpg * static_cast<long long>(p.n_groups) + 1) / 2;
-    const long long ptiles = rtp * pl.tok_tiles;
-    p.csk = 1;
-    p.total = ptiles * pl.kbpt;
+    ptiles = rtp * pl.tok_tiles;
     // as many pairs as fit at once, each at least 4 k-blocks and no pair
     // tile cut into more than 2 pieces (a fixup reads at most 256 KB)
     const long long min_kb = std::max<long long>(4, (pl.kbpt + 1) / 2);
-    long long gp = std::min<long long>(max_pairs, (p.total + min_kb - 1) / min_kb);
+    gp = std::min<long long>(max_pairs, (ptiles * pl.kbpt + min_kb - 1) / min_kb);
     if (lc.gemm_ctas < 0) gp = -lc.gemm_ctas;
     gp = std::max<long long>(1, std::min<long long>(gp, ptiles * pl.kbpt));
+    if (lc.gemm_ctas == 0 && pl.csk > 1 && 2 * gp < pl.G) pairs = false;
+  }
+  if (pairs) {
+    p.csk = 1;
+    p.total = ptiles * pl.kbpt;
     p.G = static_cast<int>(2 * gp);
     if (2 * ptiles > sc.n_counters || static_cast<size_t>(p.G) * 2 * BM * BN > sc.partial_floats)
       return set_error(DFLASH_ERR_SHAPE, "gemm %s: workspace too small for %lld pair tiles", name, ptiles);
