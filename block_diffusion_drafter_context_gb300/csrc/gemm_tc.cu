@@ -271,11 +271,17 @@ __device__ __noinline__ void topk_tile(const Params &p, const float (&v)[16], in
 
 // Apply the epilogue to 16 consecutive token columns of weight row n (ws:
 // the group's FP8 row scales, or null).
-__device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n, int tok0, size_t goff,
-                                         const float *ws, uint64_t *xch) {
+// The row scale of weight row n (FP8 codes or their bf16 copies): 1 without
+// scales, 0 past the rows.  Read once per tile by the callers, not per
+// 16-column group (its load latency would sit on every group's path).
+__device__ __forceinline__ float row_scale(const Params &p, const float *ws, int n) {
+  return ws ? (n < p.N ? ws[n] : 0.f) : 1.f;
+}
+
+__device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n, int tok0, size_t goff, float sc,
+                                         uint64_t *xch) {
   const bool nok = n < p.N;
-  if (ws) {
-    const float sc = nok ? ws[n] : 0.f;
+  if (sc != 1.f) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] *= sc;
   }
@@ -357,10 +363,9 @@ __device__ __forceinline__ void finalize(const Params &p, float (&v)[16], int n,
 // store from it and for the warp's reads of it); lane 0 commits one bulk
 // group per chunk.  The same arithmetic as finalize(): identical results.
 __device__ __forceinline__ void finalize_tma(const Params &p, const OMaps &om, float (&v)[16], int n, int tok0,
-                                             const float *ws, uint8_t *b, int lane) {
+                                             float sc, uint8_t *b, int lane) {
   const bool nok = n < p.N;
-  if (ws) {
-    const float sc = nok ? ws[n] : 0.f;
+  if (sc != 1.f) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] *= sc;
   }
@@ -449,9 +454,8 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
 // EPI_ADD_F32 for 16 token columns whose residual values r were loaded
 // earlier (before the accumulator was ready): out = r + scale * v.
 __device__ __forceinline__ void finalize_add_pre(const Params &p, float (&v)[16], const float (&r)[16], int n,
-                                                 int tok0, size_t goff, const float *ws) {
+                                                 int tok0, size_t goff, float sc) {
   const bool nok = n < p.N;
-  const float sc = ws && nok ? ws[n] : 1.f;
   float *o = static_cast<float *>(p.out);
 #pragma unroll
   for (int i = 0; i < 16; ++i)
@@ -847,14 +851,15 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
       float v[16];
       if (kb0 == 0 && kb1 == p.kbpt) {
         const bool ring_out = it + (kb1 - kb0) == end;   // last segment: the ring is idle
+        const float wsc = row_scale(p, wsg, n);
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
           if (have_pre)
-            finalize_add_pre(p, v, rpre, n, tok0 + c * 16, goff, wsg);
+            finalize_add_pre(p, v, rpre, n, tok0 + c * 16, goff, wsc);
           else if (BN >= 64 && p.tma_out)
-            finalize_tma(p, om, v, n, tok0 + c * 16, wsg, ring_out ? base + (c * 4 + q) * 2048 : xbuf(), lane);
+            finalize_tma(p, om, v, n, tok0 + c * 16, wsc, ring_out ? base + (c * 4 + q) * 2048 : xbuf(), lane);
           else
-            finalize(p, v, n, tok0 + c * 16, goff, wsg, xch);
+            finalize(p, v, n, tok0 + c * 16, goff, wsc, xch);
         }
         tc_fence_before();
         __syncwarp();
@@ -898,6 +903,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
           *abort_flag = 1;
         }
         const bool mine = o == rank;
+        const float wsc = row_scale(p, wsg, n);
         const int my_rows = (rank + 1) * BM / S - rank * BM / S, my_r0 = rank * BM / S;
 #pragma unroll
         for (int c = 0; c < BN / 16; ++c) {
@@ -921,9 +927,9 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
             }
           }
           if (have_pre && mine)
-            finalize_add_pre(p, v, rpre, n, tok0 + c * 16, goff, wsg);
+            finalize_add_pre(p, v, rpre, n, tok0 + c * 16, goff, wsc);
           else
-            finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsg, xch);   // n >= N: not this CTA's row
+            finalize(p, v, mine ? n : p.N, tok0 + c * 16, goff, wsc, xch);   // n >= N: not this CTA's row
         }
       } else if (xchg) {
         // cluster split-K, exchange: every row goes to its owner's staging
@@ -1022,6 +1028,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
             }
           }
           const float4 *ring4 = reinterpret_cast<const float4 *>(base);
+          const float wsc = row_scale(p, wsg, n);
           for (int c = 0; c < BN / 16; ++c) {
             float4 acc[4];
 #pragma unroll
@@ -1067,9 +1074,9 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
               } else {
                 b = xbuf();
               }
-              finalize_tma(p, om, v, n, tok0 + c * 16, wsg, b, lane);
+              finalize_tma(p, om, v, n, tok0 + c * 16, wsc, b, lane);
             } else
-              finalize(p, v, n, tok0 + c * 16, goff, wsg, xch);
+              finalize(p, v, n, tok0 + c * 16, goff, wsc, xch);
           }
         }
         tc_fence_before();
@@ -1150,9 +1157,9 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
               __syncwarp();
             }
             ++ocnt;
-            finalize_tma(p, om, v, n, tokt + grp * 16, wsg, b, lane);
+            finalize_tma(p, om, v, n, tokt + grp * 16, row_scale(p, wsg, n), b, lane);
           } else {
-            finalize(p, v, n, tokt + grp * 16, goff, wsg, xch);
+            finalize(p, v, n, tokt + grp * 16, goff, row_scale(p, wsg, n), xch);
           }
         }
         if (tma_w && lane == 0) bulk_wait_read<0>();
@@ -1214,7 +1221,7 @@ __global__ void __launch_bounds__(Cfg<BN, SPLIT, F8>::NT, (F8 && BN <= 32) ? 2 :
           }
         }
         const int n = valid ? (rt % p.rtpg) * BM + row : p.N;   // n >= N: nothing stored
-        finalize(p, v, n, tokt + grp * 16, goff, wsg, xch);
+        finalize(p, v, n, tokt + grp * 16, goff, row_scale(p, wsg, n), xch);
       }
     }
     cluster_sync();   // nobody leaves while others still read its share
@@ -1513,12 +1520,13 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
       } else if (kb0 == 0 && kb1 == p.kbpt) {
         // the pair's last segment: every MMA of both CTAs has completed, the rings are idle
         const bool ring_out = it + (kb1 - kb0) == end;
+        const float wsc = row_scale(p, p.wscale[g], n);
         for (int c = 0; c < BN / 16; ++c) {
           tmem_ld16(taddr + c * 16, v);
           if (p.tma_out)
-            finalize_tma(p, om, v, n, tok0 + c * 16, p.wscale[g], ring_out ? base + (c * 4 + q) * 2048 : xbuf(), lane);
+            finalize_tma(p, om, v, n, tok0 + c * 16, wsc, ring_out ? base + (c * 4 + q) * 2048 : xbuf(), lane);
           else
-            finalize(p, v, n, tok0 + c * 16, goff, p.wscale[g], nullptr);
+            finalize(p, v, n, tok0 + c * 16, goff, wsc, nullptr);
         }
         release();
       } else {
@@ -1582,6 +1590,7 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
             }
           }
           const float4 *ring4 = reinterpret_cast<const float4 *>(base);
+          const float wsc = row_scale(p, p.wscale[g], n);
           for (int c = 0; c < BN / 16; ++c) {
             float4 acc[4];
 #pragma unroll
@@ -1625,9 +1634,9 @@ __global__ void __launch_bounds__(PairCfg<BN>::NT, 1)
               } else {
                 b = xbuf();
               }
-              finalize_tma(p, om, v, n, tok0 + c * 16, p.wscale[g], b, lane);
+              finalize_tma(p, om, v, n, tok0 + c * 16, wsc, b, lane);
             } else {
-              finalize(p, v, n, tok0 + c * 16, goff, p.wscale[g], nullptr);
+              finalize(p, v, n, tok0 + c * 16, goff, wsc, nullptr);
             }
           }
         }
