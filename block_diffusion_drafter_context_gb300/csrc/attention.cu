@@ -43,21 +43,26 @@ constexpr int HD = 128;                      // head dim of the bf16 path
 constexpr int ST = 6;                        // KV ring depth
 constexpr int BLK = 16;                      // query rows per head in the tile (block size S <= 16 of them real)
 constexpr int MROWS = 128;                   // UMMA M (query rows, padded)
-constexpr int Q_BYTES = MROWS * HD * 2;      // 32 KB: two 64-dim halves of [128][64]
+constexpr int Q_BYTES = MROWS * HD * 2;      // 32 KB: shared-memory Q (g <= 4), two 64-dim halves of [128][64]
 constexpr int K_BYTES = CH * HD * 2;         // 16 KB: two halves of [64 tok][64]
 constexpr int V_BYTES = HD * CH * 2;         // 16 KB: [128 d][64 tok]
-constexpr int CTRL_BYTES = 256;              // mbarriers, TMEM address, schedule
+constexpr int CTRL_BYTES = 512;              // mbarriers, TMEM address, schedule
 constexpr int SMEM = 1024 + Q_BYTES + ST * (K_BYTES + V_BYTES) + CTRL_BYTES;
 constexpr int NTHR = 224;                    // producer, QK issuer, 4 softmax warps, PV issuer
 constexpr int NSB = 3;                       // S buffers in TMEM: QK runs two chunks ahead
-constexpr int TMEM_COLS = 512;               // S x 3 (64 columns each), O (128 columns) at 256, P x 2 at 384
+constexpr int TMEM_COLS = 512;   // S x 3 (64 columns each), Q at 192, O (128 columns) at 256, P x 2 at 384, Q at 448
 constexpr uint32_t O_COL = 256;
 constexpr uint32_t P_COL = 384;              // P buffers: 32 columns each (64 bf16 tokens per row)
+// Q buffers in TMEM (g = 5..8: the QK product's A operand, 128 dims = 64
+// columns per row), one per (request, kv head) in flight: the next one is
+// written while the current one is read
+__device__ __forceinline__ uint32_t q_col(int buf) { return buf ? 448u : 192u; }
 constexpr float RESCALE_LOG2 = 8.f;
 constexpr int DEFAULT_MIN_CHUNKS = 4;        // fewer CTAs than SMs when the whole list is short
 static_assert(SMEM <= 232448, "attention smem over the per-block limit");
 
 struct Params {
+  const __nv_bfloat16 *q;  // [B*S][nq*HD] block queries (normed, rotated)
   __nv_bfloat16 *out;
   __nv_bfloat16 *out_lo;   // low halves (split activations) or null
   int ldo;
@@ -84,8 +89,9 @@ struct Sched {
   int merge_flag;
 };
 
-// control block: 26 mbarriers, TMEM address, abort flag, schedule
-static_assert(26 * 8 + 8 + sizeof(Sched) <= CTRL_BYTES, "attention control block overflows");
+// control block: mbarriers, TMEM address, abort flag, schedule
+constexpr int N_MBAR = 3 + 2 * ST + 2 * NSB + 8;
+static_assert(N_MBAR * 8 + 8 + sizeof(Sched) <= CTRL_BYTES, "attention control block overflows");
 
 __device__ __forceinline__ int ctx_of(const Params &p, int b) {
   const int n = p.ctx_len[b], cap = p.max_pages * CH;
@@ -230,6 +236,13 @@ __device__ __noinline__ void merge_row(const Params &p, int cf, int cl, bool fir
 // halves of the warp and the two lanes of a row each take 32 of a chunk's 64
 // scores: every softmax warp works and each lane does half a row.
 // Otherwise (g = 5..8): row 16w + j per lane over all 64 scores.
+// Q: for g <= 4 the producer loads it into shared memory by TMA once the
+// previous (request, kv head)'s QKs are done; for g = 5..8 the softmax warps
+// write it into one of two TMEM buffers a segment ahead (the QK reads A from
+// TMEM), which hides that reload and halves the shared-memory reads of QK.
+// Measured per case: the TMEM form gained 5 % on 16k-32k contexts at g = 5
+// and lost 3 % at g = 4 with 1k-8k contexts, where (request, kv head)
+// switches are frequent.
 template <bool DUP>
 __global__ void __launch_bounds__(NTHR, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -238,11 +251,12 @@ __global__ void __launch_bounds__(NTHR, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *base = smem_raw + pad;
+  constexpr bool QT = !DUP;   // Q in TMEM
   uint8_t *sQ = base;
   uint8_t *sK = sQ + Q_BYTES;
   uint8_t *sV = sK + ST * K_BYTES;
   uint64_t *bar = reinterpret_cast<uint64_t *>(sV + ST * V_BYTES);
-  uint64_t *qfull = bar, *qempty = bar + 1, *full = bar + 2, *empty = full + ST, *sfull = empty + ST,
+  uint64_t *qfull = bar, *qempty = bar + 2, *full = bar + 3, *empty = full + ST, *sfull = empty + ST,
            *sempty = sfull + NSB, *pfull = sempty + NSB, *pdone = pfull + 2, *oempty = pdone + 2,
            *mready = oempty + 1, *mdone = mready + 1, *drain = mdone + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -255,7 +269,8 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int nact = (R + 31) / 32;           // softmax warps serving them
 
   if (threadIdx.x == 0) {
-    mbar_init(qfull, 1);
+    mbar_init(&qfull[0], QT ? nact : 1);   // TMEM: written by the softmax warps; smem: by TMA
+    mbar_init(&qfull[1], nact);
     mbar_init(qempty, 1);
     for (int i = 0; i < ST; ++i) {
       mbar_init(&full[i], 1);
@@ -276,16 +291,16 @@ __global__ void __launch_bounds__(NTHR, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // A rows past R (query padding) are never touched by TMA: zero them once
-  // so everything stays finite
-  {
+  if constexpr (!QT) {
+    // A rows past R (query padding) are never touched by TMA: zero them once
+    // so everything stays finite
     const int per_half = (MROWS - R) * 128 / 16;   // 16-byte chunks
     for (int i = threadIdx.x; i < 2 * per_half; i += NTHR) {
       const int half = i / per_half, k = i % per_half;
       *reinterpret_cast<uint4 *>(sQ + half * (MROWS * 128) + R * 128 + k * 16) = make_uint4(0, 0, 0, 0);
     }
+    fence_proxy_async_smem();
   }
-  fence_proxy_async_smem();
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
@@ -295,12 +310,19 @@ __global__ void __launch_bounds__(NTHR, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (warp >= 2 && warp <= 5) {
-    // P rows no softmax lane writes (quadrants without query rows) enter the
-    // PV products too: zero both P buffers of this warp's quadrant once
+    // P and Q rows no softmax lane writes (quadrants without query rows,
+    // query padding) enter the products too: zero both P and both Q buffers
+    // of this warp's quadrant once
     const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    const uint32_t pz = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + P_COL;
+    const uint32_t lz = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
 #pragma unroll
-    for (int c = 0; c < 64; c += 16) tmem_st16_nw(pz + c, z);
+    for (int c = 0; c < 64; c += 16) {
+      tmem_st16_nw(lz + P_COL + c, z);
+      if (QT) {
+        tmem_st16_nw(lz + q_col(0) + c, z);
+        tmem_st16_nw(lz + q_col(1) + c, z);
+      }
+    }
     tmem_wait_st();
     tc_fence_before();
   }
@@ -422,7 +444,7 @@ __global__ void __launch_bounds__(NTHR, 1)
           tma_load_2d_hint(dv, mv, &full[st], 0, rowv, pol_kv);
           last_ci[st] = i;
         }
-        if (first) {   // the query rows of this (request, kv head), once its predecessor's QKs are done
+        if (!QT && first) {   // the query rows of this (request, kv head), once its predecessor's QKs are done
           if (seg > 0 && !mbar_wait(qempty, static_cast<uint32_t>((seg - 1) & 1), abort_flag, p.timeout_ns)) {
             ok = false;
             break;
@@ -463,18 +485,32 @@ __global__ void __launch_bounds__(NTHR, 1)
         const bool first = i == 0 || wq.k == 0;
         const bool last = i == n - 1 || wq.k == wq.nch - 1;
         if (first) ++seg_q;
+        // this (request, kv head)'s query rows: TMEM Q buffer seg_q & 1,
+        // filled by the softmax warps for the (seg_q >> 1)-th time, or the
+        // shared-memory Q, filled by TMA for the seg_q-th time
+        const int qb = QT ? (seg_q & 1) : 0;
+        const uint32_t qpar = static_cast<uint32_t>((QT ? seg_q >> 1 : seg_q) & 1);
         ok = mbar_wait(&full[st], static_cast<uint32_t>((i / ST) & 1), abort_flag, p.timeout_ns) &&
-             (!first || mbar_wait(qfull, static_cast<uint32_t>(seg_q & 1), abort_flag, p.timeout_ns)) &&
+             (!first || mbar_wait(&qfull[qb], qpar, abort_flag, p.timeout_ns)) &&
              mbar_wait(&sempty[sb], static_cast<uint32_t>(((i / NSB) & 1) ^ 1), abort_flag, p.timeout_ns);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + st * K_BYTES);
+        const uint32_t k0 = smem_u32(sK + st * K_BYTES);
+        if constexpr (QT) {
+          const uint32_t qa = tmem + q_col(qb);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16(tmem + sb * CH, sdesc_k_sw128(q0 + (kk >> 2) * (MROWS * 128) + (kk & 3) * 32),
-                    sdesc_k_sw128(k0 + (kk >> 2) * (K_BYTES / 2) + (kk & 3) * 32), idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < HD / 16; ++kk)   // A = Q from TMEM: 16 dims = 8 columns per k-step
+            umma_bf16_ts(tmem + sb * CH, qa + static_cast<uint32_t>(kk * 8),
+                         sdesc_k_sw128(k0 + (kk >> 2) * (K_BYTES / 2) + (kk & 3) * 32), idesc_qk, kk > 0 ? 1u : 0u);
+        } else {
+          const uint32_t q0 = smem_u32(sQ);
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_bf16(tmem + sb * CH, sdesc_k_sw128(q0 + (kk >> 2) * (MROWS * 128) + (kk & 3) * 32),
+                      sdesc_k_sw128(k0 + (kk >> 2) * (K_BYTES / 2) + (kk & 3) * 32), idesc_qk, kk > 0 ? 1u : 0u);
+        }
         umma_commit(&sfull[sb]);
-        if (last) umma_commit(qempty);   // the Q buffer may take the next (request, head)
+        if (!QT && last) umma_commit(qempty);   // the shared-memory Q may take the next (request, head)
         wq.next(p);
       }
       if (!ok) {
@@ -542,6 +578,36 @@ __global__ void __launch_bounds__(NTHR, 1)
       const bool ok = mbar_wait(b, par, abort_flag, p.timeout_ns);
       return !__any_sync(0xffffffffu, !ok);
     };
+    // The query rows of (request bt, kv head ht) into Q buffer qb, this
+    // lane's TMEM lane holding row qj of the group's query head qhw (both
+    // lanes of a DUP pair hold it); rows past the block size stay zero.
+    // Column c holds dims 2c (low half) and 2c + 1: the A layout of QK.
+    const int qhw = DUP ? q : trow / BLK, qj = DUP ? (lane & 15) : trow % BLK;
+    auto write_q = [&](int bt, int ht, int qb) {
+      const bool live = qhw < g && qj < p.S;
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          p.q + (static_cast<size_t>(bt) * p.S + qj) * (static_cast<size_t>(p.nkv) * g * HD) +
+          static_cast<size_t>(ht * g + qhw) * HD);
+      uint4 u[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) u[t] = live ? __ldg(src + t) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {   // 16 columns per store
+        uint32_t wv[16];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          wv[4 * t] = u[4 * c4 + t].x;
+          wv[4 * t + 1] = u[4 * c4 + t].y;
+          wv[4 * t + 2] = u[4 * c4 + t].z;
+          wv[4 * t + 3] = u[4 * c4 + t].w;
+        }
+        tmem_st16_nw(lane_base + q_col(qb) + static_cast<uint32_t>(16 * c4), wv);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qfull[qb]);
+    };
     for (int i = 0; i < n; ++i) {
       const int sb = i % NSB;
       const bool first = i == 0 || w.k == 0;
@@ -549,6 +615,9 @@ __global__ void __launch_bounds__(NTHR, 1)
       if (first) {
         ++seg;
         seg_whole = w.k == 0;
+        // Q of this segment (the first one only: the others were written a
+        // segment ahead); the next one's follows this chunk's P
+        if (QT && i == 0) write_q(w.b, w.h, 0);
       }
       const int valid = w.valid(p.S);
       if (!waitw(&sfull[sb], static_cast<uint32_t>((i / NSB) & 1))) {
@@ -687,6 +756,14 @@ __global__ void __launch_bounds__(NTHR, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&pfull[i & 1]);
+      // the next (request, kv head)'s Q, if the run reaches it, into the
+      // other buffer: it held the previous segment's Q, whose QKs all
+      // completed before this warp consumed their scores.  Written after the
+      // P of this segment's first chunk, so the loads overlap its PV.
+      if (QT && first && (n - i) - (w.nch - w.k) > 0) {
+        const bool nb = w.h + 1 < p.nkv;
+        write_q(nb ? w.b : w.b + 1, nb ? w.h + 1 : 0, (seg + 1) & 1);
+      }
 
       if (last) {
         // ---- end of this CTA's part of a (request, kv head)
@@ -951,6 +1028,7 @@ int attention_bf16(const Launch &lc, const AttnArgs &a) {
   if (int e = make_tmap_2d(&tBK, a.bk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, HD, bkv * CH, HD * 2, 64, CH)) return e;
   if (int e = make_tmap_2d(&tBV, a.bv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CH, bkv * HD, CH * 2, 64, HD)) return e;
   Params p = {};
+  p.q = static_cast<const __nv_bfloat16 *>(a.q);
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.out_lo = static_cast<__nv_bfloat16 *>(a.out_lo);
   p.ldo = a.nq * HD;
