@@ -13,18 +13,21 @@
 // pipeline never drains between requests.  Per CTA:
 //   warp 0     TMA: K and V^T pages into a 6-deep smem ring (128-byte swizzle;
 //              V pages are stored transposed so both products take K-major
-//              operands); the 16g query rows of each new (request, kv head);
-//   warp 1     tcgen05.mma: S = Q K^T (M=128, N=64, K=128) into one of two
-//              TMEM buffers; O += P V (M=128, N=128, K = the chunk's valid
-//              tokens rounded up to 16) into a TMEM accumulator, with P, the
-//              A operand, read from TMEM;
+//              operands); for g <= 4 also the 16g query rows of each new
+//              (request, kv head), into shared memory;
+//   warp 1     tcgen05.mma S = Q K^T (M=128, N=64, K=128) into one of three
+//              TMEM score buffers; for g = 5..8 Q, the A operand, is read
+//              from one of two TMEM Q buffers that the softmax warps fill a
+//              (request, kv head) ahead;
 //   warps 2-5  one TMEM lane (= query row) per thread: online softmax in the
-//              exp2 domain on its 64 scores, P written back to TMEM in bf16
-//              (no shared memory: that room holds a sixth ring stage, which
-//              the chunk's load-to-PV lifetime of ~7 500 cycles needs to keep
-//              HBM busy).  O stays in TMEM; it is rescaled only
-//              when a row's running max grows by more than 2^8 (the exp2
-//              values stay below 256 in between, exact in fp32 sums).
+//              exp2 domain, P written back to TMEM in bf16 (no shared memory:
+//              that room holds the ring's depth, which the chunk's
+//              load-to-PV lifetime needs to keep HBM busy).  O stays in TMEM;
+//              it is rescaled only when a row's running max grows by more
+//              than 2^8 (the exp2 values stay below 256 in between, exact in
+//              fp32 sums);
+//   warp 6     tcgen05.mma O += P V (M=128, N=128, K = the chunk's valid
+//              tokens rounded up to 16), P, the A operand, read from TMEM.
 // A (request, kv head) whose chunks all fall in one CTA is normalised and
 // written directly.  One cut by a CTA boundary leaves (max, sum, O) partials
 // in a small L2-resident scratch, and the last contributing CTA to arrive (a
