@@ -44,7 +44,7 @@ from synthetic import WORKLOADS, gen  # noqa: E402
 METRIC = "drafted blocks/sec (16-tok) at batch×ctx on 1 GB300; attention HBM GB/s"
 DEFAULT_WORKLOAD = "C4"
 DEFAULT_EXTRA = "C1,C2,C3"
-# GEMMs with at least this many token rows are judged against the tensor
+# GEMMs with at least this many token rows are measured against the tensor
 # peak (ridge point of the measured bf16 rate over the measured HBM rate)
 TENSOR_BOUND_TOKENS = 300
 GEMM_NAMES = ("fc", "kv_inject", "qkv", "o_proj", "gate_up", "down", "lm_head", "lm_head_topk", "conv_coef")
