@@ -2,7 +2,7 @@
 the same seeded inputs.
 
 Floats: max |err| <= 2e-2 * max |ref| (bf16) or 1e-4 (fp32) per tensor.
-Integers: bit-exact, judged stage-isolated (the oracle's top-16 / path /
+Integers: bit-exact, compared stage-isolated (the oracle's top-16 / path /
 verify re-run on the GPU's own fp32 logits and hidden states), except where
 the oracle's deciding gap is below 1e-3.
 """
